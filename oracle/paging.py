@@ -1,0 +1,135 @@
+"""Reference model of the block table and its CPU-side allocator.
+
+Follows "Batching, Scheduling, and Paging" (datasystem.school, module 4):
+
+* section *PagedAttention*: each sequence's KV cache is split into fixed-size
+  blocks stored non-contiguously; a per-sequence block table maps logical
+  block ``j`` to a physical block; the CPU allocates a new block only when the
+  previous one fills and frees blocks when the request completes;
+* section *Block sharing*: parallel samples point at the same physical blocks;
+  the first divergent write triggers copy-on-write, and reference counts keep
+  a shared block alive until its last user finishes.
+
+Readings where the page is silent:
+
+* free blocks are handed out first-in first-out; the initial order is the
+  caller's permutation, and a block whose count drops to zero joins the tail;
+* copy-on-write applies only to a *partially filled* shared last block that
+  receives a new token: the writer gets a fresh block, a ``(src, dst)`` copy
+  pair is emitted and the source's count drops by one, so with four sharers
+  the first three writers copy and the fourth writes in place; full shared
+  blocks are never written and never copied;
+* a slot is ``physical_block * block_size + offset``;
+* an append that cannot get all the blocks it needs fails as a whole and
+  changes nothing.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+"""
+
+from __future__ import annotations
+
+from collections import deque
+
+
+class OutOfBlocks(Exception):
+    """No free block for an append; the allocator state is unchanged."""
+
+
+class BlockAllocator:
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        if free_order is None:
+            free_order = range(num_blocks)
+        order = [int(b) for b in free_order]
+        assert sorted(order) == list(range(num_blocks)), "free_order must be a permutation"
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+        self.free = deque(order)
+        self.refcount = [0] * num_blocks
+        self.seqs: dict[int, dict] = {}
+        self._next_id = 0
+
+    # -- sequences ---------------------------------------------------------
+    def create(self) -> int:
+        sid = self._next_id
+        self._next_id += 1
+        self.seqs[sid] = {"blocks": [], "len": 0}
+        return sid
+
+    def fork(self, parent: int) -> int:
+        """A new sequence that shares every block of ``parent`` (Block sharing)."""
+        src = self.seqs[parent]
+        sid = self._next_id
+        self._next_id += 1
+        self.seqs[sid] = {"blocks": list(src["blocks"]), "len": src["len"]}
+        for b in src["blocks"]:
+            self.refcount[b] += 1
+        return sid
+
+    def free_seq(self, sid: int) -> None:
+        """Drop the sequence; a block returns to the free list at count zero."""
+        seq = self.seqs.pop(sid)
+        for b in seq["blocks"]:
+            self.refcount[b] -= 1
+            if self.refcount[b] == 0:
+                self.free.append(b)
+
+    def _take(self) -> int:
+        b = self.free.popleft()
+        self.refcount[b] = 1
+        return b
+
+    def blocks_needed(self, sid: int, n: int) -> int:
+        seq = self.seqs[sid]
+        B = self.block_size
+        L = seq["len"]
+        need = -(-(L + n) // B) - len(seq["blocks"])
+        if n > 0 and L % B != 0 and self.refcount[seq["blocks"][-1]] > 1:
+            need += 1
+        return need
+
+    def append_slots(self, sid: int, n: int):
+        """Reserve slots for ``n`` new tokens; return ``(slots, cow_pairs)``."""
+        if self.blocks_needed(sid, n) > len(self.free):
+            raise OutOfBlocks(f"sequence {sid} needs {self.blocks_needed(sid, n)} blocks, "
+                              f"{len(self.free)} free")
+        seq = self.seqs[sid]
+        B = self.block_size
+        slots, pairs = [], []
+        for pos in range(seq["len"], seq["len"] + n):
+            j, off = divmod(pos, B)
+            if j == len(seq["blocks"]):
+                # previous block is full (or there is none): allocate on fill
+                seq["blocks"].append(self._take())
+            elif self.refcount[seq["blocks"][j]] > 1:
+                # first divergent write into a shared partial block
+                old = seq["blocks"][j]
+                new = self._take()
+                self.refcount[old] -= 1
+                seq["blocks"][j] = new
+                pairs.append((old, new))
+            slots.append(seq["blocks"][j] * B + off)
+        seq["len"] += n
+        return slots, pairs
+
+    # -- queries -----------------------------------------------------------
+    def block_table(self, sid: int) -> list[int]:
+        return list(self.seqs[sid]["blocks"])
+
+    def seq_len(self, sid: int) -> int:
+        return self.seqs[sid]["len"]
+
+    def num_free(self) -> int:
+        return len(self.free)
+
+    def check_invariants(self) -> None:
+        """Counts equal table references; free + referenced = all blocks."""
+        refs = [0] * self.num_blocks
+        for seq in self.seqs.values():
+            assert len(seq["blocks"]) == -(-seq["len"] // self.block_size)
+            for b in seq["blocks"]:
+                refs[b] += 1
+        assert refs == self.refcount
+        free = set(self.free)
+        assert len(free) == len(self.free)
+        for b in range(self.num_blocks):
+            assert (b in free) == (refs[b] == 0)

@@ -1,0 +1,111 @@
+"""Builds the oracle's view of a workload: its own allocator, pools and outputs.
+
+Test infrastructure: everything here runs the CPU oracle on the seeded
+workload inputs; nothing reads a value produced by the library.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+from oracle import attention, cache, paging
+from workloads import BF16_NAN
+
+
+@dataclass
+class OracleDecodeState:
+    alloc: paging.BlockAllocator
+    seq_ids: list
+    k_cache: np.ndarray
+    v_cache: np.ndarray
+    tables: list                  # list of per-sequence block lists
+    slots: list                   # per-sequence slot lists (all tokens)
+
+    def padded_tables(self, width: int | None = None) -> np.ndarray:
+        width = width or max(1, max(len(t) for t in self.tables))
+        out = np.zeros((len(self.tables), width), dtype=np.int32)
+        for s, t in enumerate(self.tables):
+            out[s, :len(t)] = t
+        return out
+
+
+def empty_pools(num_blocks, Hkv, B, D, poison=True):
+    fill = BF16_NAN if poison else np.uint16(0)
+    k = np.full((num_blocks, Hkv, B, D), fill, dtype=np.uint16)
+    v = np.full((num_blocks, Hkv, B, D), fill, dtype=np.uint16)
+    return k, v
+
+
+def build_decode_state(w, poison=True, include_last=True) -> OracleDecodeState:
+    """Allocate every sequence's blocks through the oracle allocator and write
+    its tokens (all of them, or all but the last when ``include_last`` is
+    False) into NaN-poisoned pools."""
+    alloc = paging.BlockAllocator(w.num_blocks, w.block_size, w.free_order)
+    k_cache, v_cache = empty_pools(w.num_blocks, w.Hkv, w.block_size, w.D, poison)
+    cu = w.cu_lens
+    seq_ids, tables, slots = [], [], []
+    for s in range(w.S):
+        sid = alloc.create()
+        sl, pairs = alloc.append_slots(sid, int(w.context_lens[s]))
+        assert not pairs
+        seq_ids.append(sid)
+        tables.append(alloc.block_table(sid))
+        slots.append(sl)
+        n = len(sl) if include_last else len(sl) - 1
+        cache.append(k_cache, v_cache, w.k[cu[s]:cu[s] + n], w.v[cu[s]:cu[s] + n],
+                     sl[:n], w.block_size)
+    return OracleDecodeState(alloc, seq_ids, k_cache, v_cache, tables, slots)
+
+
+def decode_reference(w, st: OracleDecodeState, seqs=None) -> np.ndarray:
+    return attention.decode(w.q, st.k_cache, st.v_cache, st.tables, w.context_lens,
+                            w.block_size, w.scale, seqs=seqs)
+
+
+@dataclass
+class OracleSharedPrefixState:
+    alloc: paging.BlockAllocator
+    sample_ids: list              # [n_prompts * n_samples] sequence ids
+    k_cache: np.ndarray
+    v_cache: np.ndarray
+    prefix_slots: list            # per prompt
+    tail_slots: list              # per sample
+    cow_pairs: list               # all (src, dst) pairs, in append order
+    tables: list
+
+
+def build_shared_prefix_state(w, poison=True) -> OracleSharedPrefixState:
+    """The build order of a shared-prefix workload, on the oracle side."""
+    alloc = paging.BlockAllocator(w.num_blocks, w.block_size, w.free_order)
+    k_cache, v_cache = empty_pools(w.num_blocks, w.Hkv, w.block_size, w.D, poison)
+    sample_ids, prefix_slots = [], []
+    for p in range(w.n_prompts):
+        sid = alloc.create()
+        sl, pairs = alloc.append_slots(sid, w.prefix_len)
+        assert not pairs
+        prefix_slots.append(sl)
+        cache.append(k_cache, v_cache, w.prefix_k[p], w.prefix_v[p], sl, w.block_size)
+        sample_ids.append(sid)
+        for _ in range(w.n_samples - 1):
+            sample_ids.append(alloc.fork(sid))
+    tail_slots, cow_pairs = [], []
+    for i, sid in enumerate(sample_ids):
+        sl, pairs = alloc.append_slots(sid, int(w.tails.reshape(-1)[i]))
+        tail_slots.append(sl)
+        cow_pairs.extend(pairs)
+    # copy-on-write copies run before any tail token is written
+    cache.block_copy(k_cache, v_cache, cow_pairs)
+    cu = w.cu_tails
+    for i in range(len(sample_ids)):
+        cache.append(k_cache, v_cache, w.tail_k[cu[i]:cu[i + 1]], w.tail_v[cu[i]:cu[i + 1]],
+                     tail_slots[i], w.block_size)
+    tables = [alloc.block_table(sid) for sid in sample_ids]
+    return OracleSharedPrefixState(alloc, sample_ids, k_cache, v_cache, prefix_slots,
+                                   tail_slots, cow_pairs, tables)
+
+
+def bf16_tolerance_ok(gpu: np.ndarray, ref: np.ndarray, atol=2e-3, rtol=1e-2) -> np.ndarray:
+    """Elementwise ``|gpu - ref| <= atol + rtol * |ref|``."""
+    return np.abs(gpu - ref) <= atol + rtol * np.abs(ref)
