@@ -1,0 +1,355 @@
+"""Benchmark: one paged decode step of a Llama-3-8B-shaped GQA layer.
+
+A step is the whole decode hot path over one batch: ``pkv_kv_append`` of each
+sequence's newest token into its slot, then ``pkv_paged_attention_decode``
+(work plan, split-K partitions, combine) over all 256 sequences. The workload
+is synthetic and seeded: 256 sequences, 32 query / 8 KV heads, head_dim 128,
+bf16, block size 16, context lengths log-normal (median 1024, sigma 0.8)
+clipped to [16, 8192], blocks placed by a seeded permutation of a pool with
+10% free blocks, Q/K/V ~ N(0, 1).
+
+``value`` is the KV bytes the decode must read per step (each sequence's keys
+and values once) divided by the device time of a step; the line also reports
+attention tokens/s per layer (decode queries per second), the decode call's
+share of the HBM roofline, an end-to-end figure through the C ABI with host
+buffers, and the fp64 CPU oracle's throughput on a bounded sample.
+
+``--impl reference`` times the CPU oracle instead (the only reference
+implementation this method has): each step is the oracle's decode over a
+bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn KV GB/s and % of HBM peak; attention tokens/s per layer"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+CPU_SAMPLE_SEQS = 48
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_for_rank(rank: int):
+    from workloads import config3, make_decode_workload, SEED_BASE
+    w = config3()
+    if rank == 0:
+        return w
+    # weak scaling: every rank decodes its own batch of the same shape
+    return make_decode_workload(w.name, w.context_lens, w.Hq, w.Hkv, w.D, w.block_size,
+                                seed=SEED_BASE + 3 + 1000 * rank)
+
+
+def workload_description(w, partition_size):
+    return {
+        "workload": "llama3_8b_gqa decode step (kv_append + paged decode attention)",
+        "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "block_size": w.block_size,
+        "num_blocks": w.num_blocks, "context_tokens": w.total_tokens,
+        "context_len": {"median": 1024, "sigma": 0.8, "clip": [16, 8192],
+                        "max": w.max_context_len},
+        "kv_bytes_per_step": w.kv_bytes(),
+        "partition_size": partition_size or 512,
+        "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB of L2"
+              % (w.kv_bytes() / 1e9),
+    }
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.device_index = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, seqs: int = CPU_SAMPLE_SEQS):
+    """Times the fp64 oracle's decode on a bounded sample of the workload, in a
+    single-threaded child process."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--_oracle-sample", str(seqs)]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": "failed: " + r.stderr.strip()[-200:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def oracle_sample_main(n_seqs: int):
+    """Child process: the oracle on ``n_seqs`` sequences drawn from the workload."""
+    from oracle import attention
+    from tests.oracle_side import build_decode_state
+    from workloads import config3_lengths, generator, make_decode_workload, SEED_BASE
+    lens = config3_lengths()
+    pick = np.sort(generator(SEED_BASE + 3, 9).choice(len(lens), n_seqs, replace=False))
+    w = make_decode_workload("llama3_8b_gqa_sample", lens[pick], Hq=32, Hkv=8, D=128,
+                             block_size=16, seed=SEED_BASE + 3)
+    st = build_decode_state(w)
+    t0 = time.perf_counter()
+    attention.decode(w.q, st.k_cache, st.v_cache, st.tables, w.context_lens, w.block_size,
+                     w.scale)
+    dt = time.perf_counter() - t0
+    print(json.dumps({"value": w.kv_bytes() / dt / 1e9, "unit": UNIT, "cores": 1,
+                      "kind": "oracle", "seconds": dt,
+                      "sample": f"{n_seqs} of 256 sequences ({w.total_tokens} context tokens, "
+                                f"seeded pick), fp64 gather + softmax attention, 1 thread"}))
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return 0
+    from oracle import attention
+    from tests.oracle_side import build_decode_state
+    from workloads import config3, config3_lengths, generator, make_decode_workload, SEED_BASE
+    full = config3()
+    lens = config3_lengths()
+    n = 8
+    times, bytes_ = [], []
+    for step in range(args.warmup + args.steps):
+        pick = np.sort(generator(SEED_BASE + 3, 10, step).choice(len(lens), n, replace=False))
+        w = make_decode_workload("llama3_8b_gqa_sample", lens[pick], Hq=32, Hkv=8, D=128,
+                                 block_size=16, seed=SEED_BASE + 3 + step)
+        st = build_decode_state(w)
+        t0 = time.perf_counter()
+        attention.decode(w.q, st.k_cache, st.v_cache, st.tables, w.context_lens, w.block_size,
+                         w.scale)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+            bytes_.append(w.kv_bytes())
+    value = sum(bytes_) / sum(times) / 1e9
+    ms = 1e3 * sum(times) / len(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_description(full, args.partition_size),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step: {n} of 256 sequences (seeded pick), fp64 oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    import paged_kv_cache_281_gb300 as pkv
+    from tests.gpu_harness import decode_step, setup_decode, to_dev_bf16
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w = workload_for_rank(rank)
+    d = setup_decode(w, partition_size=args.partition_size, append_last=False)
+    stream = torch.cuda.current_stream()
+    parts = pkv.pkv_decode_workspace_bytes(1, 1, w.D, w.max_context_len, args.partition_size)
+    del parts
+    P = args.partition_size or 512
+    launches_per_step = 1 + 2 + (1 if math.ceil(w.max_context_len / P) > 1 else 0)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        decode_step(w, d)
+    pkv.pkv_check_status(d.status)
+    barrier()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        barrier()
+        start.record(stream)
+        for i in range(args.steps):
+            pkv.pkv_kv_append(d.k_last, d.v_last, d.last_slot_mapping, d.k_cache, d.v_cache,
+                              status=d.status, stream=stream)
+            ev[i][0].record(stream)
+            pkv.pkv_paged_attention_decode(d.out, d.q, d.k_cache, d.v_cache, d.block_tables,
+                                           d.context_lens, d.max_context_len, w.scale,
+                                           d.workspace, partition_size=args.partition_size,
+                                           status=d.status, stream=stream)
+            ev[i][1].record(stream)
+        end.record(stream)
+        barrier()
+    pkv.pkv_check_status(d.status)
+    total_ms = start.elapsed_time(end)
+    decode_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    kv_bytes = w.kv_bytes()
+    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
+
+    e2e = None if args.no_e2e else e2e_measure(w, d, args, pkv, torch)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_description(w, args.partition_size),
+        "attention_tokens_per_s_per_layer": world * w.S / (ms_per_step * 1e-3),
+        "pct_hbm_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "hbm", "kernel": "pkv_paged_attention_decode (plan + split-K "
+                     "partitions + combine)", "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": kv_bytes,
+                     "avg_launch_ms": decode_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def e2e_measure(w, d, args, pkv, torch, steps=None):
+    """The same step through the C ABI from pinned host buffers: each step
+    copies its inputs host->device, appends, decodes, and reads the output back."""
+    steps = steps or max(20, min(args.steps, 200))
+    stream = torch.cuda.current_stream()
+    host = {
+        "q": d.q.cpu().pin_memory(), "k": d.k_last.cpu().pin_memory(),
+        "v": d.v_last.cpu().pin_memory(), "slots": d.last_slot_mapping.cpu().pin_memory(),
+        "bt": d.block_tables.cpu().pin_memory(), "lens": d.context_lens.cpu().pin_memory(),
+    }
+    out_h = torch.empty(d.out.shape, dtype=d.out.dtype).pin_memory()
+    dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def one():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        pkv.pkv_kv_append(dev["k"], dev["v"], dev["slots"], d.k_cache, d.v_cache,
+                          status=d.status, stream=stream)
+        pkv.pkv_paged_attention_decode(d.out, dev["q"], d.k_cache, d.v_cache, dev["bt"],
+                                       dev["lens"], d.max_context_len, w.scale, d.workspace,
+                                       partition_size=args.partition_size, status=d.status,
+                                       stream=stream)
+        out_h.copy_(d.out, non_blocking=True)
+
+    for _ in range(5):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": w.kv_bytes() / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
+            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "note": "KV pools stay resident (they are the cache); per-step inputs and the "
+                    "output cross PCIe/C2C from pinned host memory"}
+
+
+if __name__ == "__main__":
+    if len(sys.argv) >= 3 and sys.argv[1] == "--_oracle-sample":
+        oracle_sample_main(int(sys.argv[2]))
+        sys.exit(0)
+    sys.exit(main())

@@ -1,0 +1,216 @@
+/*
+ * pagedkv.h — C ABI of the paged-KV attention library for GB300 (sm_103a).
+ *
+ * What the library computes, and where the pages on continuous batching and
+ * PagedAttention say so:
+ *
+ *   "Batching, Scheduling, and Paging" (datasystem.school, module 4)
+ *     section PagedAttention: each sequence's KV cache is cut into fixed-size
+ *       blocks stored non-contiguously; a per-sequence block table maps logical
+ *       blocks to physical ones; the CPU allocates a block only when the
+ *       previous one fills and frees blocks when the request completes; the
+ *       attention kernels gather K and V through the block table.
+ *     section Block sharing: parallel samples point at the same physical blocks;
+ *       the first divergent write does copy-on-write; reference counts keep a
+ *       shared block alive until its last user finishes.
+ *   "Deep Dive: continuous batching" (worksonmygpu.com)
+ *     section Selective batching: attention, softmax(Q K^T / sqrt(d_k)) V, runs
+ *       per request over that request's own tokens only.
+ *     section The prefill/decode mix: a new request's prompt (prefill) and a
+ *       running request's single new token (decode) are different shapes of
+ *       work mixed in one iteration.
+ *
+ * Conventions
+ *   - Every call returns an int status: PKV_OK (0) or a negative PKV_E* code;
+ *     pkv_last_error() then describes the failure (thread-local string).
+ *   - Memory layout of the KV cache (the pages fix none): two separate pools,
+ *     keys and values, each bf16 [num_blocks][Hkv][block_size][D], row-major.
+ *     Token j of a sequence with block table bt lives in block bt[j / B] at
+ *     offset j % B. A slot is block * B + offset (int32); slot -1 means "skip".
+ *   - Query head h reads key/value head h / (Hq / Hkv) (grouped heads).
+ *   - bf16 pointers are passed as void*; they must be 16-byte aligned and the
+ *     arrays contiguous. int32 arrays are int32_t*.
+ *   - Ownership: the caller owns all device memory (the library allocates
+ *     none in these calls) and the allocator handle (create/destroy).
+ *   - GPU calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream). Pointers must stay valid until that work completes.
+ *   - Device-side faults are never raised on purpose: a table entry or slot out
+ *     of range, or a bounded wait that expires, skips the access and records a
+ *     code in the caller's status block (`dev_status`, 4 int32 on the device,
+ *     zeroed by pkv_status_reset); pkv_check_status() synchronises and reports.
+ *     `dev_status` may be NULL, in which case such events are dropped silently.
+ *   - Supported shapes: bf16 only; D in {64, 128}; block_size in {8, 16, 32};
+ *     Hq / Hkv in {1, 2, 4, 8}.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  PKV_OK = 0,
+  PKV_EINVAL = -1,   /* bad argument: null pointer, unsupported shape, size mismatch */
+  PKV_ENOMEM = -2,   /* allocator: not enough free blocks; state unchanged          */
+  PKV_ECUDA = -3,    /* a CUDA launch or API call failed                             */
+  PKV_ETIMEOUT = -4, /* a device wait exceeded its time limit (reported by status)  */
+  PKV_EDEVICE = -5   /* a device range check fired (reported by status)             */
+};
+
+/* Thread-local description of the last failing call on this thread. */
+const char* pkv_last_error(void);
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pkv_version(void);
+
+/* ------------------------------------------------------------------------
+ * Host block allocator ("Batching, Scheduling, and Paging", sections
+ * PagedAttention and Block sharing). CPU only, single-threaded, deterministic.
+ *   - Free blocks are handed out first-in first-out. The initial order is
+ *     `free_order` (a permutation of 0..num_blocks-1, e.g. a seeded shuffle) or
+ *     0,1,2,... when NULL; a block whose count drops to 0 joins the tail.
+ *   - A new block is taken only when a sequence's last block is full.
+ *   - fork shares every block of the parent and adds one reference to each.
+ *   - An append whose first new token lands in a partially filled block that
+ *     other sequences share copies it first (copy-on-write): a fresh block
+ *     replaces it in this sequence's table, one (src, dst) pair is reported and
+ *     the source loses one reference. Full shared blocks are never copied; the
+ *     last remaining user writes in place. At most one pair per append.
+ *   - An append that cannot get every block it needs returns PKV_ENOMEM and
+ *     changes nothing.
+ *   - Sequence ids are 0, 1, 2, ... in creation order; they are never reused.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_alloc pkv_alloc;
+
+int pkv_alloc_create(int32_t num_blocks, int32_t block_size, const int32_t* free_order,
+                     pkv_alloc** out);
+int pkv_alloc_destroy(pkv_alloc* a);
+int pkv_seq_create(pkv_alloc* a, int64_t* seq_id);
+int pkv_seq_fork(pkv_alloc* a, int64_t parent, int64_t* child);
+/* Reserve slots for n new tokens of `seq`. slots_out: n int32 (host).
+ * cow_pair_out: 2 int32 (host), receives (src, dst) when *n_cow == 1. */
+int pkv_seq_append_slots(pkv_alloc* a, int64_t seq, int32_t n, int32_t* slots_out,
+                         int32_t* cow_pair_out, int32_t* n_cow);
+/* The request completed: drop its references, freeing blocks that reach 0. */
+int pkv_seq_free(pkv_alloc* a, int64_t seq);
+int pkv_seq_len(pkv_alloc* a, int64_t seq, int32_t* len);
+/* Copies min(cap, table length) entries to out (host); *n = table length. */
+int pkv_seq_block_table(pkv_alloc* a, int64_t seq, int32_t* out, int32_t cap, int32_t* n);
+int pkv_block_refcount(pkv_alloc* a, int32_t block, int32_t* out);
+int pkv_num_free_blocks(pkv_alloc* a, int32_t* out);
+/* Per-iteration metadata for n sequences (host arrays): tables_out is
+ * [n][max_blocks_per_seq] int32, padded with 0; lens_out is [n] int32.
+ * PKV_EINVAL if a table is longer than max_blocks_per_seq. */
+int pkv_build_block_tables(pkv_alloc* a, const int64_t* seqs, int32_t n, int32_t* tables_out,
+                           int32_t max_blocks_per_seq, int32_t* lens_out);
+
+/* ------------------------------------------------------------------------
+ * Device status block (4 int32 in device memory, owned by the caller):
+ *   [0] first error code (0, PKV_ETIMEOUT or PKV_EDEVICE), [1] detail (the
+ *   offending index or wait site), [2] kernel id, [3] count of events.
+ * ---------------------------------------------------------------------- */
+int pkv_status_reset(int32_t* dev_status, void* stream);
+/* Synchronises `stream`, reads the block and returns PKV_OK, PKV_ETIMEOUT or
+ * PKV_EDEVICE (pkv_last_error() gives the detail). Does not clear it. */
+int pkv_check_status(const int32_t* dev_status, void* stream);
+/* Debug knob for tests: when nonzero, the next kernels treat their first
+ * pipeline wait as expired (they record PKV_ETIMEOUT, let their own copies in
+ * flight land, and return). Also sets the wait limit in nanoseconds when
+ * timeout_ns > 0 (default 2e9). */
+int pkv_debug_set_wait(int32_t force_timeout, uint64_t timeout_ns);
+
+/* ------------------------------------------------------------------------
+ * kv_append — "Batching, Scheduling, and Paging", section PagedAttention:
+ * each new token's key and value rows are written into the slot the block
+ * table assigned to it.
+ *   k_new, v_new : bf16 [T][Hkv][D] (device)
+ *   slot_mapping : int32 [T] (device); -1 skips the token; a slot outside
+ *                  [0, num_blocks * block_size) is skipped and recorded as
+ *                  PKV_EDEVICE in dev_status.
+ *   k_cache, v_cache : the pools (device), written in place.
+ * Bit-exact copy. Slots must be distinct (two tokens in one slot race).
+ * ---------------------------------------------------------------------- */
+int pkv_kv_append(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t T,
+                  void* k_cache, void* v_cache, int32_t num_blocks, int32_t Hkv, int32_t D,
+                  int32_t block_size, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * block_copy — "Batching, Scheduling, and Paging", section Block sharing:
+ * copy-on-write duplicates a whole physical block (keys and values).
+ *   pairs : int32 [n][2] (device), (src, dst) block ids. No dst may appear
+ *           twice or also be a src in the same call (they run in parallel).
+ *           An id outside [0, num_blocks) skips the pair (PKV_EDEVICE).
+ * Run it before the kv_append that writes into the copies, on one stream.
+ * ---------------------------------------------------------------------- */
+int pkv_block_copy(void* k_cache, void* v_cache, const int32_t* pairs, int32_t n,
+                   int32_t num_blocks, int32_t Hkv, int32_t D, int32_t block_size,
+                   int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * paged_attention_decode — one query token per sequence ("Deep Dive:
+ * continuous batching", section Selective batching; "Batching, Scheduling,
+ * and Paging", section PagedAttention):
+ *   out[s][h] = softmax_j(scale * q[s][h] . K_s[j]) V_s[j],  j = 0 .. L_s - 1
+ * where K_s[j] = k_cache[bt_s[j / B]][h / G][j % B] and L_s = context_lens[s]
+ * (the query's own token is already in the cache and is included).
+ *   out          : bf16 [S][Hq][D] (device, written)
+ *   q            : bf16 [S][Hq][D] (device)
+ *   block_tables : int32 [S][max_blocks_per_seq] (device); entries past
+ *                  ceil(L_s / B) are never read.
+ *   context_lens : int32 [S] (device), each in [1, max_context_len].
+ *   max_context_len : an upper bound of context_lens (host value); it sizes
+ *                  the split into partitions and the workspace.
+ *   partition_size : tokens per split-K partition (multiple of 16, >= 16), or
+ *                  0 for the library default (512). Long contexts are split
+ *                  into partitions whose partial softmax states are merged by
+ *                  a second kernel; the split depends only on positions, so
+ *                  results do not depend on physical placement.
+ *   workspace    : device scratch of pkv_decode_workspace_bytes() bytes.
+ * Arithmetic: bf16 inputs, fp32 scores and accumulation, probabilities
+ * rounded to bf16 for the P.V product, output rounded to bf16.
+ * ---------------------------------------------------------------------- */
+int pkv_decode_workspace_bytes(int32_t S, int32_t Hq, int32_t D, int32_t max_context_len,
+                               int32_t partition_size, size_t* out);
+int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                               int32_t max_context_len, int32_t S, int32_t Hq, int32_t Hkv,
+                               int32_t D, int32_t block_size, int32_t num_blocks, float scale,
+                               int32_t partition_size, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * paged_attention_prefill — a chunk of a prompt attending causally over its
+ * own cached blocks ("Deep Dive: continuous batching", section The
+ * prefill/decode mix; the chunk's keys and values are appended first).
+ * Sequence s owns query rows cu_q_lens[s] .. cu_q_lens[s+1]-1 (c_s rows);
+ * they are its last c_s tokens, so row i sits at position L_s - c_s + i and
+ *   out[row][h] = softmax_j(scale * q[row][h] . K_s[j]) V_s[j],
+ *                 j = 0 .. L_s - c_s + i.
+ *   out, q       : bf16 [total_q][Hq][D] (device)
+ *   cu_q_lens    : int32 [S + 1] (device), cu_q_lens[0] = 0, nondecreasing,
+ *                  cu_q_lens[S] = total_q, each c_s <= L_s and <= max_q_len.
+ *   context_lens : int32 [S] (device), after the chunk was appended.
+ *   workspace    : pkv_prefill_workspace_bytes() bytes of device scratch.
+ * QK^T and PV run on the tcgen05 tensor cores (bf16 operands, fp32
+ * accumulation in tensor memory); probabilities are rounded to bf16.
+ * ---------------------------------------------------------------------- */
+int pkv_prefill_workspace_bytes(int32_t S, int32_t total_q, int32_t Hq, int32_t D,
+                                size_t* out);
+int pkv_paged_attention_prefill(void* out, const void* q, const int32_t* cu_q_lens,
+                                const int32_t* context_lens, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables,
+                                int32_t max_blocks_per_seq, int32_t S, int32_t total_q,
+                                int32_t max_q_len, int32_t max_context_len, int32_t Hq,
+                                int32_t Hkv, int32_t D, int32_t block_size, int32_t num_blocks,
+                                float scale, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,260 @@
+"""Python binding of the C ABI: argument marshalling only.
+
+Each function carries the name of the C call it wraps and passes tensor data
+pointers, sizes and the current CUDA stream straight through; every step of
+the computation runs in the library's kernels. Shapes are read from the
+tensors:
+
+* ``k_cache``/``v_cache``: bf16 ``[num_blocks, Hkv, block_size, D]``
+* ``q``/``out`` (decode): bf16 ``[S, Hq, D]``; (prefill): ``[total_q, Hq, D]``
+* ``block_tables``: int32 ``[S, max_blocks_per_seq]``; ``context_lens``: int32 ``[S]``
+* ``slot_mapping``: int32 ``[T]``; ``pairs``: int32 ``[n, 2]``
+* ``status``: int32 ``[4]`` on the device (optional)
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from ._lib import PagedKVError, check, lib
+
+__all__ = [
+    "PagedKVError", "pkv_version", "pkv_last_error", "BlockAllocator",
+    "pkv_kv_append", "pkv_block_copy", "pkv_decode_workspace_bytes",
+    "pkv_paged_attention_decode", "pkv_prefill_workspace_bytes",
+    "pkv_paged_attention_prefill", "pkv_status_reset", "pkv_check_status",
+    "pkv_debug_set_wait", "new_status",
+]
+
+
+def pkv_version() -> int:
+    return lib().pkv_version()
+
+
+def pkv_last_error() -> str:
+    return lib().pkv_last_error().decode()
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int | None = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    return t
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed device status block (4 int32)."""
+    return torch.zeros(4, dtype=torch.int32, device=device or "cuda")
+
+
+# ---------------------------------------------------------------- allocator
+
+class BlockAllocator:
+    """The library's host block allocator (``pkv_alloc_*`` / ``pkv_seq_*``)."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        self._h = ctypes.c_void_p()
+        order = None
+        if free_order is not None:
+            self._order = np.ascontiguousarray(free_order, dtype=np.int32)
+            order = self._order.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        check(lib().pkv_alloc_create(int(num_blocks), int(block_size), order,
+                                     ctypes.byref(self._h)))
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def close(self) -> None:
+        if self._h:
+            lib().pkv_alloc_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def seq_create(self) -> int:
+        out = ctypes.c_int64()
+        check(lib().pkv_seq_create(self._h, ctypes.byref(out)))
+        return out.value
+
+    def seq_fork(self, parent: int) -> int:
+        out = ctypes.c_int64()
+        check(lib().pkv_seq_fork(self._h, int(parent), ctypes.byref(out)))
+        return out.value
+
+    def seq_append_slots(self, seq: int, n: int):
+        """Returns ``(slots int32[n], (src, dst) or None)``."""
+        slots = np.empty(max(int(n), 1), dtype=np.int32)
+        pair = np.zeros(2, dtype=np.int32)
+        ncow = ctypes.c_int32()
+        check(lib().pkv_seq_append_slots(
+            self._h, int(seq), int(n), slots.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            pair.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), ctypes.byref(ncow)))
+        return slots[:int(n)], ((int(pair[0]), int(pair[1])) if ncow.value else None)
+
+    def seq_free(self, seq: int) -> None:
+        check(lib().pkv_seq_free(self._h, int(seq)))
+
+    def seq_len(self, seq: int) -> int:
+        out = ctypes.c_int32()
+        check(lib().pkv_seq_len(self._h, int(seq), ctypes.byref(out)))
+        return out.value
+
+    def seq_block_table(self, seq: int) -> list[int]:
+        n = ctypes.c_int32()
+        check(lib().pkv_seq_block_table(self._h, int(seq), None, 0, ctypes.byref(n)))
+        buf = np.empty(max(n.value, 1), dtype=np.int32)
+        check(lib().pkv_seq_block_table(self._h, int(seq),
+                                        buf.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                        n.value, ctypes.byref(n)))
+        return buf[:n.value].tolist()
+
+    def block_refcount(self, block: int) -> int:
+        out = ctypes.c_int32()
+        check(lib().pkv_block_refcount(self._h, int(block), ctypes.byref(out)))
+        return out.value
+
+    def num_free_blocks(self) -> int:
+        out = ctypes.c_int32()
+        check(lib().pkv_num_free_blocks(self._h, ctypes.byref(out)))
+        return out.value
+
+    def build_block_tables(self, seqs, max_blocks_per_seq: int):
+        """Padded int32 ``[n, max_blocks_per_seq]`` tables and ``[n]`` lengths (host)."""
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        n = ids.shape[0]
+        tables = np.empty((max(n, 1), int(max_blocks_per_seq)), dtype=np.int32)
+        lens = np.empty(max(n, 1), dtype=np.int32)
+        check(lib().pkv_build_block_tables(
+            self._h, ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n,
+            tables.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(max_blocks_per_seq),
+            lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
+        return tables[:n], lens[:n]
+
+
+# ---------------------------------------------------------------- GPU calls
+
+def _pool_shape(k_cache: torch.Tensor, v_cache: torch.Tensor):
+    _dev(k_cache, "k_cache", torch.bfloat16, 4)
+    _dev(v_cache, "v_cache", torch.bfloat16, 4)
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must have the same shape")
+    return tuple(int(x) for x in k_cache.shape)  # N, Hkv, B, D
+
+
+def pkv_status_reset(status: torch.Tensor, stream=None) -> None:
+    _dev(status, "status", torch.int32, 1)
+    check(lib().pkv_status_reset(status.data_ptr(), _stream(stream)))
+
+
+def pkv_check_status(status: torch.Tensor, stream=None) -> None:
+    """Raises PagedKVError (PKV_ETIMEOUT / PKV_EDEVICE) if a kernel recorded one."""
+    _dev(status, "status", torch.int32, 1)
+    check(lib().pkv_check_status(status.data_ptr(), _stream(stream)))
+
+
+def pkv_debug_set_wait(force_timeout: bool, timeout_ns: int = 0) -> None:
+    check(lib().pkv_debug_set_wait(1 if force_timeout else 0, int(timeout_ns)))
+
+
+def pkv_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, status=None, stream=None) -> None:
+    N, Hkv, B, D = _pool_shape(k_cache, v_cache)
+    _dev(k_new, "k_new", torch.bfloat16, 3)
+    _dev(v_new, "v_new", torch.bfloat16, 3)
+    _dev(slot_mapping, "slot_mapping", torch.int32, 1)
+    T = int(slot_mapping.shape[0])
+    if k_new.shape != (T, Hkv, D) or v_new.shape != (T, Hkv, D):
+        raise ValueError(f"k_new/v_new must be [{T}, {Hkv}, {D}]")
+    check(lib().pkv_kv_append(k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), T,
+                              k_cache.data_ptr(), v_cache.data_ptr(), N, Hkv, D, B,
+                              _ptr(status), _stream(stream)))
+
+
+def pkv_block_copy(k_cache, v_cache, pairs, status=None, stream=None) -> None:
+    N, Hkv, B, D = _pool_shape(k_cache, v_cache)
+    _dev(pairs, "pairs", torch.int32, 2)
+    if pairs.shape[1] != 2:
+        raise ValueError("pairs must be [n, 2]")
+    check(lib().pkv_block_copy(k_cache.data_ptr(), v_cache.data_ptr(), pairs.data_ptr(),
+                               int(pairs.shape[0]), N, Hkv, D, B, _ptr(status), _stream(stream)))
+
+
+def pkv_decode_workspace_bytes(S: int, Hq: int, D: int, max_context_len: int,
+                               partition_size: int = 0) -> int:
+    out = ctypes.c_size_t()
+    check(lib().pkv_decode_workspace_bytes(int(S), int(Hq), int(D), int(max_context_len),
+                                           int(partition_size), ctypes.byref(out)))
+    return out.value
+
+
+def pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
+                               max_context_len: int, scale: float, workspace,
+                               partition_size: int = 0, status=None, stream=None) -> None:
+    N, Hkv, B, D = _pool_shape(k_cache, v_cache)
+    _dev(q, "q", torch.bfloat16, 3)
+    _dev(out, "out", torch.bfloat16, 3)
+    _dev(block_tables, "block_tables", torch.int32, 2)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    _dev(workspace, "workspace", torch.uint8, 1)
+    S, Hq = int(q.shape[0]), int(q.shape[1])
+    if q.shape[2] != D or out.shape != q.shape:
+        raise ValueError("q/out must be [S, Hq, D] with the pools' D")
+    if block_tables.shape[0] != S or context_lens.shape[0] != S:
+        raise ValueError("block_tables/context_lens must have S rows")
+    check(lib().pkv_paged_attention_decode(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_tables.data_ptr(), int(block_tables.shape[1]), context_lens.data_ptr(),
+        int(max_context_len), S, Hq, Hkv, D, B, N, float(scale), int(partition_size),
+        workspace.data_ptr(), int(workspace.numel()), _ptr(status), _stream(stream)))
+
+
+def pkv_prefill_workspace_bytes(S: int, total_q: int, Hq: int, D: int) -> int:
+    out = ctypes.c_size_t()
+    check(lib().pkv_prefill_workspace_bytes(int(S), int(total_q), int(Hq), int(D),
+                                            ctypes.byref(out)))
+    return out.value
+
+
+def pkv_paged_attention_prefill(out, q, cu_q_lens, context_lens, k_cache, v_cache, block_tables,
+                                max_q_len: int, max_context_len: int, scale: float, workspace,
+                                status=None, stream=None) -> None:
+    N, Hkv, B, D = _pool_shape(k_cache, v_cache)
+    _dev(q, "q", torch.bfloat16, 3)
+    _dev(out, "out", torch.bfloat16, 3)
+    _dev(cu_q_lens, "cu_q_lens", torch.int32, 1)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    _dev(block_tables, "block_tables", torch.int32, 2)
+    _dev(workspace, "workspace", torch.uint8, 1)
+    total_q, Hq = int(q.shape[0]), int(q.shape[1])
+    S = int(context_lens.shape[0])
+    if cu_q_lens.shape[0] != S + 1 or block_tables.shape[0] != S:
+        raise ValueError("cu_q_lens must be [S+1] and block_tables [S, *]")
+    if q.shape[2] != D or out.shape != q.shape:
+        raise ValueError("q/out must be [total_q, Hq, D] with the pools' D")
+    check(lib().pkv_paged_attention_prefill(
+        out.data_ptr(), q.data_ptr(), cu_q_lens.data_ptr(), context_lens.data_ptr(),
+        k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        int(block_tables.shape[1]), S, total_q, int(max_q_len), int(max_context_len), Hq, Hkv,
+        D, B, N, float(scale), workspace.data_ptr(), int(workspace.numel()), _ptr(status),
+        _stream(stream)))

@@ -1,0 +1,161 @@
+// kv_append and block_copy: the two bit-exact cache writers.
+//
+// kv_append ("Batching, Scheduling, and Paging", section PagedAttention): each
+// new token's key and value rows go to the slot its block table assigned.
+// block_copy (same page, section Block sharing): copy-on-write duplicates a
+// whole physical block before a divergent write lands in it.
+//
+// Both are pure data movement, bound by HBM bandwidth (or by launch latency
+// at decode sizes). Every thread moves 16-byte vectors; one (token, head) row
+// of D bf16 is D/8 consecutive vectors, so a warp touches whole 128-byte lines
+// on both the read and the write side.
+#include "device.cuh"
+#include "host_util.h"
+
+namespace pkv {
+
+namespace {
+
+struct AppendArgs {
+  const uint4* k_new;
+  const uint4* v_new;
+  const int32_t* slot_mapping;
+  uint4* k_cache;
+  uint4* v_cache;
+  int64_t num_slots;      // num_blocks * block_size
+  int32_t T;
+  int32_t Hkv;
+  int32_t vec_per_row;    // D / 8
+  int32_t block_size;
+  int32_t* status;
+};
+
+// One thread per 16-byte vector of the new rows; grid-stride over T*Hkv*D/8.
+__global__ void __launch_bounds__(256) kv_append_kernel(const AppendArgs a) {
+  const int64_t vec_per_tok = (int64_t)a.Hkv * a.vec_per_row;
+  const int64_t total = (int64_t)a.T * vec_per_tok;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t t = (int32_t)(i / vec_per_tok);
+    const int64_t rem = i - (int64_t)t * vec_per_tok;
+    const int32_t h = (int32_t)(rem / a.vec_per_row);
+    const int32_t c = (int32_t)(rem - (int64_t)h * a.vec_per_row);
+    const int32_t slot = __ldg(a.slot_mapping + t);
+    if (slot < 0) continue;
+    if (slot >= a.num_slots) {
+      if (h == 0 && c == 0) record_status(a.status, PKV_EDEVICE, slot, kKernelAppend);
+      continue;
+    }
+    const int32_t blk = slot / a.block_size;
+    const int32_t off = slot - blk * a.block_size;
+    const int64_t dst = (((int64_t)blk * a.Hkv + h) * a.block_size + off) * a.vec_per_row + c;
+    a.k_cache[dst] = __ldg(a.k_new + i);
+    a.v_cache[dst] = __ldg(a.v_new + i);
+  }
+}
+
+struct CopyArgs {
+  uint4* k_cache;
+  uint4* v_cache;
+  const int32_t* pairs;
+  int32_t n;
+  int32_t num_blocks;
+  int64_t vec_per_block;  // Hkv * B * D / 8
+  int32_t* status;
+};
+
+// blockIdx.y picks the pair, blockIdx.z the pool (0 keys, 1 values);
+// blockIdx.x strides over the block's vectors.
+__global__ void __launch_bounds__(256) block_copy_kernel(const CopyArgs a) {
+  const int32_t p = blockIdx.y;
+  const int32_t src = __ldg(a.pairs + 2 * p);
+  const int32_t dst = __ldg(a.pairs + 2 * p + 1);
+  if (src < 0 || src >= a.num_blocks || dst < 0 || dst >= a.num_blocks) {
+    if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+      record_status(a.status, PKV_EDEVICE, (src < 0 || src >= a.num_blocks) ? src : dst,
+                    kKernelBlockCopy);
+    return;
+  }
+  uint4* pool = blockIdx.z == 0 ? a.k_cache : a.v_cache;
+  const uint4* s = pool + (int64_t)src * a.vec_per_block;
+  uint4* d = pool + (int64_t)dst * a.vec_per_block;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < a.vec_per_block;
+       i += (int64_t)gridDim.x * blockDim.x)
+    d[i] = s[i];
+}
+
+int check_shape(int32_t Hkv, int32_t D, int32_t block_size, const char* who) {
+  PKV_REQUIRE(Hkv > 0, "%s: Hkv must be > 0 (got %d)", who, Hkv);
+  PKV_REQUIRE(D == 64 || D == 128, "%s: D must be 64 or 128 (got %d)", who, D);
+  PKV_REQUIRE(block_size == 8 || block_size == 16 || block_size == 32,
+              "%s: block_size must be 8, 16 or 32 (got %d)", who, block_size);
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" int pkv_kv_append(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                             int32_t T, void* k_cache, void* v_cache, int32_t num_blocks,
+                             int32_t Hkv, int32_t D, int32_t block_size, int32_t* dev_status,
+                             void* stream) {
+  if (int rc = check_shape(Hkv, D, block_size, "pkv_kv_append")) return rc;
+  PKV_REQUIRE(T >= 0, "pkv_kv_append: T must be >= 0 (got %d)", T);
+  PKV_REQUIRE(num_blocks > 0 && (int64_t)num_blocks * block_size < (int64_t(1) << 31),
+              "pkv_kv_append: num_blocks * block_size must be in [1, 2^31)");
+  if (T == 0) return ok();
+  PKV_REQUIRE(k_new && v_new && slot_mapping && k_cache && v_cache, "pkv_kv_append: NULL pointer");
+  PKV_REQUIRE(aligned16(k_new) && aligned16(v_new) && aligned16(k_cache) && aligned16(v_cache),
+              "pkv_kv_append: bf16 arrays must be 16-byte aligned");
+  const DeviceInfo* dev = nullptr;
+  if (int rc = current_device_info(&dev)) return rc;
+  AppendArgs a;
+  a.k_new = static_cast<const uint4*>(k_new);
+  a.v_new = static_cast<const uint4*>(v_new);
+  a.slot_mapping = slot_mapping;
+  a.k_cache = static_cast<uint4*>(k_cache);
+  a.v_cache = static_cast<uint4*>(v_cache);
+  a.num_slots = (int64_t)num_blocks * block_size;
+  a.T = T;
+  a.Hkv = Hkv;
+  a.vec_per_row = D / 8;
+  a.block_size = block_size;
+  a.status = dev_status;
+  const int64_t total = (int64_t)T * Hkv * (D / 8);
+  const int64_t want = (total + 255) / 256;
+  const int64_t cap = (int64_t)dev->sm_count * 8;  // 8 resident CTAs of 256 per SM
+  const int grid = (int)(want < cap ? want : cap);
+  kv_append_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  if (int rc = check_launch("pkv_kv_append")) return rc;
+  return ok();
+}
+
+extern "C" int pkv_block_copy(void* k_cache, void* v_cache, const int32_t* pairs, int32_t n,
+                              int32_t num_blocks, int32_t Hkv, int32_t D, int32_t block_size,
+                              int32_t* dev_status, void* stream) {
+  if (int rc = check_shape(Hkv, D, block_size, "pkv_block_copy")) return rc;
+  PKV_REQUIRE(n >= 0 && n <= 65535, "pkv_block_copy: n must be in [0, 65535] (got %d)", n);
+  PKV_REQUIRE(num_blocks > 0, "pkv_block_copy: num_blocks must be > 0");
+  if (n == 0) return ok();
+  PKV_REQUIRE(k_cache && v_cache && pairs, "pkv_block_copy: NULL pointer");
+  PKV_REQUIRE(aligned16(k_cache) && aligned16(v_cache),
+              "pkv_block_copy: pools must be 16-byte aligned");
+  const DeviceInfo* dev = nullptr;
+  if (int rc = current_device_info(&dev)) return rc;
+  CopyArgs a;
+  a.k_cache = static_cast<uint4*>(k_cache);
+  a.v_cache = static_cast<uint4*>(v_cache);
+  a.pairs = pairs;
+  a.n = n;
+  a.num_blocks = num_blocks;
+  a.vec_per_block = (int64_t)Hkv * block_size * D / 8;
+  a.status = dev_status;
+  int64_t per_block = (a.vec_per_block + 255) / 256;
+  if (per_block > 16) per_block = 16;
+  dim3 grid((unsigned)per_block, (unsigned)n, 2);
+  block_copy_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  if (int rc = check_launch("pkv_block_copy")) return rc;
+  return ok();
+}

@@ -1,0 +1,605 @@
+// paged_attention_decode: one query token per sequence over its paged K/V.
+//
+// What it computes ("Deep Dive: continuous batching", section Selective
+// batching; "Batching, Scheduling, and Paging", section PagedAttention): for
+// sequence s and query head h, softmax(scale * q . K_s^T) V_s over the s-th
+// request's own L_s tokens, where K_s and V_s are gathered page by page
+// through its block table.
+//
+// How (GB300 design):
+//  * Split-K. A sequence's tokens are cut into partitions of a fixed number of
+//    16-token tiles. A work item is (sequence, kv head, partition); a plan
+//    kernel lists the items (full partitions first, partial ones last) and a
+//    persistent grid of 2 CTAs per SM pulls them from an atomic ticket. Items
+//    of multi-partition sequences write an unnormalised partial state
+//    (m, l, o) that a combine kernel merges with the online-softmax rule; a
+//    sequence with one partition is normalised in place.
+//  * Data movement. Each of the CTA's 4 warps owns every 4th tile of the item
+//    and a private 3-stage ring in shared memory. One lane per warp issues TMA
+//    tile loads (two 64-column halves per tensor, 128-byte swizzle) for whole
+//    pages located through the block table, signalling an mbarrier with the
+//    byte count; the warp waits on it with a time limit.
+//  * Arithmetic. The G query heads that share a kv head form the rows of a
+//    16-row MMA operand (rows >= G are zero). Scores S = Q K^T and the update
+//    O += P V run as m16n8k16 bf16 MMAs with fp32 accumulators held in
+//    registers; the online softmax (running max m, running sum l) works on
+//    the accumulator fragment directly, in base 2 (scale pre-multiplied by
+//    log2 e). P enters the second MMA as a bf16 pair P_hi + P_lo (rows 0..7
+//    and 8..15 of the operand), so the P.V product keeps ~fp32 precision.
+//  * Robustness. Block-table entries outside the pool are skipped and
+//    recorded; V rows past the sequence end are zeroed in shared memory so
+//    that whatever the pool holds there (even NaN) cannot leak into O.
+#include <cmath>
+#include <mutex>
+
+#include "device.cuh"
+#include "host_util.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTileTokens = 16;
+constexpr int kDefaultPartition = 512;
+
+template <int D>
+struct Cfg {
+  static constexpr int kHalves = D / 64;            // 128-byte swizzled column halves
+  static constexpr int kHalfBytes = kTileTokens * 128;
+  static constexpr int kTensorBytes = kHalves * kHalfBytes;
+  static constexpr int kStageBytes = 2 * kTensorBytes;  // keys, then values
+  static constexpr int kStages = D == 128 ? 3 : 6;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kSmemBytes = kWarps * kRingBytes + 1024;  // + alignment slack
+};
+
+struct DecodeArgs {
+  __nv_bfloat16* out;
+  const __nv_bfloat16* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int32_t max_blocks_per_seq;
+  int32_t S, Hq, Hkv;
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t max_context_len;
+  int32_t partition_tiles;
+  int32_t max_partitions;
+  float scale_log2;
+  int2* items;
+  int32_t* n_items;
+  int32_t* ticket;
+  float2* ws_ml;
+  float* ws_o;
+  int32_t* status;
+  uint64_t timeout_ns;
+  int32_t force_timeout;
+};
+
+// Lists the work items: pass 0 emits every full partition (s, p), pass 1 the
+// trailing partial partition of each sequence. Single CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
+  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t s_base, s_chunk;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = a.partition_tiles * kTileTokens;
+  if (tid == 0) s_base = 0;
+  __syncthreads();
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int c0 = 0; c0 < a.S; c0 += 1024) {
+      const int s = c0 + tid;
+      int L = 0;
+      if (s < a.S) {
+        L = a.context_lens[s];
+        if (L < 1 || L > a.max_context_len) {
+          if (pass == 0) record_status(a.status, PKV_EDEVICE, L, kKernelDecodePlan);
+          L = 0;
+        }
+      }
+      const int cnt = pass == 0 ? L / P : (L % P != 0 ? 1 : 0);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (lane == 31) warp_tot[warp] = incl;
+      __syncthreads();
+      if (warp == 0) {
+        const int w = warp_tot[lane];
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, wi, o);
+          if (lane >= o) wi += v;
+        }
+        warp_tot[lane] = wi - w;  // exclusive prefix of the warp totals
+        if (lane == 31) s_chunk = wi;
+      }
+      __syncthreads();
+      const int excl = s_base + warp_tot[warp] + incl - cnt;
+      for (int i = 0; i < cnt; ++i) a.items[excl + i] = make_int2(s, pass == 0 ? i : L / P);
+      __syncthreads();
+      if (tid == 0) s_base += s_chunk;
+      __syncthreads();
+    }
+  }
+  if (tid == 0) {
+    *a.n_items = s_base;
+    *a.ticket = 0;
+  }
+}
+
+// Issues the TMA loads of one 16-token tile (keys and values of kv head `kvh`)
+// into `stage` and arms `bar` with the number of bytes that will land.
+template <int D>
+__device__ __forceinline__ void issue_tile(const CUtensorMap* tk, const CUtensorMap* tv,
+                                           const DecodeArgs& a, const int32_t* bt, int kvh,
+                                           int tile, int L, uint32_t stage, uint32_t bar) {
+  using C = Cfg<D>;
+  const int B = a.block_size;
+  const int R = B < kTileTokens ? B : kTileTokens;  // rows per TMA box
+  const int nsub = kTileTokens / R;
+  int32_t rows[2] = {-1, -1};
+  uint32_t bytes = 0;
+  for (int sub = 0; sub < nsub; ++sub) {
+    const int tok = tile * kTileTokens + sub * R;
+    if (tok >= L) break;
+    const int32_t blk = __ldg(bt + tok / B);
+    if (blk < 0 || blk >= a.num_blocks) {
+      record_status(a.status, PKV_EDEVICE, blk, kKernelDecode);
+      continue;
+    }
+    rows[sub] = (blk * a.Hkv + kvh) * B + tok % B;
+    bytes += 2u * C::kHalves * R * 128u;
+  }
+  mbar_arrive_expect_tx(bar, bytes);
+  for (int sub = 0; sub < nsub; ++sub) {
+    if (rows[sub] < 0) continue;
+#pragma unroll
+    for (int half = 0; half < C::kHalves; ++half) {
+      const uint32_t off = half * C::kHalfBytes + sub * R * 128;
+      tma_load_2d(stage + off, tk, half * 64, rows[sub], bar);
+      tma_load_2d(stage + C::kTensorBytes + off, tv, half * 64, rows[sub], bar);
+    }
+  }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 2)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                        const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
+  using C = Cfg<D>;
+  constexpr int KS = D / 16;  // k-steps of the score MMA
+  constexpr int NT = D / 8;   // n-tiles of the output MMA
+  extern __shared__ uint8_t dsm[];
+  __shared__ __align__(8) uint64_t bars[kWarps][C::kStages];
+  __shared__ int32_t s_next;
+  __shared__ int32_t s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;  // MMA fragment row / column group
+  const uint32_t dsm_u32 = smem_u32(dsm);
+  const uint32_t base = (dsm_u32 + 1023u) & ~1023u;
+  uint8_t* base_ptr = dsm + (base - dsm_u32);
+  const uint32_t ring = base + warp * C::kRingBytes;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < C::kStages; ++st) mbar_init(smem_u32(&bars[warp][st]), 1);
+    fence_barrier_init();
+  }
+  if (tid == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+    s_abort = 0;
+    s_next = atomicAdd(a.ticket, 1);
+  }
+  __syncthreads();
+  const int total = __ldg(a.n_items) * a.Hkv;
+  const int P = a.partition_tiles * kTileTokens;
+  uint32_t phase = 0;  // bit st: parity of the next completion of stage st
+  int cur = s_next;
+
+  while (cur < total) {
+    __syncthreads();  // everyone has read s_next
+    if (tid == 0) s_next = atomicAdd(a.ticket, 1);
+    const int2 item = __ldg(a.items + cur / a.Hkv);
+    const int kvh = cur % a.Hkv;
+    const int s = item.x, p = item.y;
+    const int L = __ldg(a.context_lens + s);
+    const int t_begin = p * a.partition_tiles;
+    const int t_end = min((L + kTileTokens - 1) / kTileTokens, t_begin + a.partition_tiles);
+    const int n_item = t_end - t_begin;
+    const int n_mine = n_item > warp ? (n_item - warp + kWarps - 1) / kWarps : 0;
+    const int32_t* bt = a.block_tables + (int64_t)s * a.max_blocks_per_seq;
+
+    if (lane == 0) {
+      const int npro = n_mine < C::kStages ? n_mine : C::kStages;
+      for (int k = 0; k < npro; ++k)
+        issue_tile<D>(&tmap_k, &tmap_v, a, bt, kvh, t_begin + warp + k * kWarps, L,
+                      ring + k * C::kStageBytes, smem_u32(&bars[warp][k]));
+    }
+
+    // Q fragments (A operand rows g < G; rows g+8 are always zero).
+    uint32_t qa[KS][2];
+    {
+      const bool live = g < G;
+      const __nv_bfloat16* qrow = a.q + ((int64_t)s * a.Hq + kvh * G + (live ? g : 0)) * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qa[ks][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * t)) : 0u;
+        qa[ks][1] =
+            live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * t)) : 0u;
+      }
+    }
+
+    float m = -INFINITY, l = 0.f;
+    float o[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+
+    for (int k = 0; k < n_mine; ++k) {
+      const int st = k % C::kStages;
+      const int tile = t_begin + warp + k * kWarps;
+      const uint32_t bar = smem_u32(&bars[warp][st]);
+      const uint32_t par = (phase >> st) & 1u;
+      const bool landed = mbar_wait_bounded(bar, par, a.timeout_ns, a.force_timeout);
+      if (!__all_sync(0xffffffffu, landed)) {
+        if (lane == 0) {
+          record_status(a.status, PKV_ETIMEOUT, k, kKernelDecode);
+          s_abort = 1;
+        }
+        // Let this warp's loads in flight land before leaving: tiles k .. k+stages-1.
+        uint32_t ph = phase;
+        const int last = min(k + C::kStages, n_mine);
+        for (int j = k; j < last; ++j) {
+          const int sj = j % C::kStages;
+          mbar_wait_bounded(smem_u32(&bars[warp][sj]), (ph >> sj) & 1u, 4 * a.timeout_ns, 0);
+          ph ^= 1u << sj;
+        }
+        phase = ph;
+        break;
+      }
+      phase ^= 1u << st;
+      const uint32_t stage = ring + st * C::kStageBytes;
+      const int valid = min(kTileTokens, L - tile * kTileTokens);
+      if (valid < kTileTokens) {
+        // Rows past the sequence end hold whatever the pool holds: clear V there.
+        const int n16 = (kTileTokens - valid) * C::kHalves * 8;
+        for (int i = lane; i < n16; i += 32) {
+          const int row = valid + i / (C::kHalves * 8);
+          const int rem = i % (C::kHalves * 8);
+          const uint32_t addr = stage + C::kTensorBytes + (rem >> 3) * C::kHalfBytes + row * 128 +
+                                (rem & 7) * 16;
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u)
+                       : "memory");
+        }
+        __syncwarp();
+      }
+
+      // S = Q K^T over this tile: two n-tiles of 8 tokens.
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int tok = (lane & 7) + ((lane >> 4) << 3);
+        const int csel = (lane >> 3) & 1;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const int chunk = 2 * ks + csel;
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(stage + (chunk >> 3) * C::kHalfBytes + swz128(tok, chunk & 7), b0, b1, b2,
+                      b3);
+          mma_bf16_16816(sc[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+          mma_bf16_16816(sc[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+        }
+      }
+
+      // Online softmax on row g (tokens 2t, 2t+1, 8+2t, 8+2t+1 of the tile).
+      float x[4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          x[2 * j + e] = (8 * j + 2 * t + e < valid) ? sc[j][e] * a.scale_log2 : -INFINITY;
+      float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m, mx);
+      const float alpha = fast_exp2(m - m_new);
+      float pr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pr[i] = fast_exp2(x[i] - m_new);
+      l = l * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+      m = m_new;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        o[nt][0] *= alpha;
+        o[nt][1] *= alpha;
+        o[nt][2] *= alpha;
+        o[nt][3] *= alpha;
+      }
+      // P = P_hi + P_lo with both parts in bf16: P_hi drives A rows 0..7 and
+      // the residual P_lo the otherwise empty rows 8..15, so one MMA gives
+      // the P.V product to about 2^-17 relative precision.
+      const uint32_t pa0 = pack_bf16x2(pr[0], pr[1]);
+      const uint32_t pa2 = pack_bf16x2(pr[2], pr[3]);
+      const uint32_t pl0 = pack_bf16x2(pr[0] - bf16_lo_to_f32(pa0), pr[1] - bf16_hi_to_f32(pa0));
+      const uint32_t pl2 = pack_bf16x2(pr[2] - bf16_lo_to_f32(pa2), pr[3] - bf16_hi_to_f32(pa2));
+
+      // O += P V: n-tiles of 8 columns, two per ldmatrix.
+      {
+        const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int csel = lane >> 4;
+#pragma unroll
+        for (int n2 = 0; n2 < NT / 2; ++n2) {
+          const int chunk = 2 * n2 + csel;
+          uint32_t r0, r1, r2, r3;
+          ldmatrix_x4_trans(
+              stage + C::kTensorBytes + (chunk >> 3) * C::kHalfBytes + swz128(tok, chunk & 7), r0,
+              r1, r2, r3);
+          mma_bf16_16816(o[2 * n2], pa0, pl0, pa2, pl2, r0, r1);
+          mma_bf16_16816(o[2 * n2 + 1], pa0, pl0, pa2, pl2, r2, r3);
+        }
+      }
+      if (valid < kTileTokens) fence_proxy_async_smem();  // zeroing stores before TMA reuse
+      __syncwarp();
+      if (lane == 0 && k + C::kStages < n_mine) {
+        issue_tile<D>(&tmap_k, &tmap_v, a, bt, kvh, t_begin + warp + (k + C::kStages) * kWarps, L,
+                      stage, bar);
+      }
+    }
+
+    // Merge the 4 warps' states through shared memory (the rings are drained).
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    __syncthreads();
+    if (s_abort) return;
+    float2* cml = reinterpret_cast<float2*>(base_ptr);                  // [kWarps][G]
+    float* co = reinterpret_cast<float*>(base_ptr + 256);               // [kWarps][G][D]
+    if (g < G) {
+      if (t == 0) cml[warp * G + g] = make_float2(m, l);
+      float* row = co + (warp * G + g) * D;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        *reinterpret_cast<float2*>(row + nt * 8 + 2 * t) =
+            make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3]);
+    }
+    __syncthreads();
+    const int nparts = (L + P - 1) / P;
+    for (int e = tid; e < G * D; e += kThreads) {
+      const int h = e / D, d = e % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cml[w * G + h].x);
+      float lsum = 0.f, acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float sw = fast_exp2(cml[w * G + h].x - M);
+        lsum += sw * cml[w * G + h].y;
+        acc += sw * co[(w * G + h) * D + d];
+      }
+      const int64_t qh = (int64_t)s * a.Hq + kvh * G + h;
+      if (nparts == 1) {
+        a.out[qh * D + d] = __float2bfloat16_rn(acc / lsum);
+      } else {
+        const int64_t idx = qh * a.max_partitions + p;
+        a.ws_o[idx * D + d] = acc;
+        if (d == 0) a.ws_ml[idx] = make_float2(M, lsum);
+      }
+    }
+    fence_proxy_async_smem();  // merge-buffer stores before the ring's next TMA writes
+    __syncthreads();           // the ring is free again for the next item's loads
+    cur = s_next;
+  }
+}
+
+// Merges the partial states of multi-partition sequences: one warp per
+// (sequence, query head).
+template <int D>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t sh = (int64_t)blockIdx.x * 4 + warp;
+  if (sh >= (int64_t)a.S * a.Hq) return;
+  const int s = (int)(sh / a.Hq);
+  const int L = __ldg(a.context_lens + s);
+  if (L < 1 || L > a.max_context_len) return;
+  const int P = a.partition_tiles * kTileTokens;
+  const int np = (L + P - 1) / P;
+  if (np <= 1) return;
+  const float2* ml = a.ws_ml + sh * a.max_partitions;
+  float M = -INFINITY;
+  for (int p = lane; p < np; p += 32) M = fmaxf(M, ml[p].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float lsum = 0.f;
+  for (int p = lane; p < np; p += 32) lsum += fast_exp2(ml[p].x - M) * ml[p].y;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  const float* ob = a.ws_o + sh * a.max_partitions * D + lane * E;
+  for (int p = 0; p < np; ++p) {
+    const float w = fast_exp2(ml[p].x - M);
+    if constexpr (E == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(ob + (int64_t)p * D);
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
+      acc[2] += w * v.z;
+      acc[3] += w * v.w;
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(ob + (int64_t)p * D);
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
+    }
+  }
+  const float inv = 1.f / lsum;
+  __nv_bfloat16* out = a.out + sh * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e += 2)
+    *reinterpret_cast<__nv_bfloat162*>(out + e) =
+        __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+}
+
+struct WsLayout {
+  size_t items_off, ml_off, o_off, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+WsLayout ws_layout(int64_t S, int64_t Hq, int64_t D, int64_t max_parts) {
+  WsLayout w;
+  w.items_off = 256;
+  w.ml_off = align256(w.items_off + S * max_parts * sizeof(int2));
+  w.o_off = align256(w.ml_off + S * Hq * max_parts * sizeof(float2));
+  w.total = align256(w.o_off + S * Hq * max_parts * D * sizeof(float));
+  return w;
+}
+
+int resolve_partition(int32_t partition_size, int32_t* tiles) {
+  const int32_t P = partition_size == 0 ? kDefaultPartition : partition_size;
+  PKV_REQUIRE(P >= kTileTokens && P % kTileTokens == 0 && P <= (1 << 20),
+              "partition_size must be a positive multiple of 16 (got %d)", partition_size);
+  *tiles = P / kTileTokens;
+  return PKV_OK;
+}
+
+template <int D, int G>
+int launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                  const DeviceInfo& dev, cudaStream_t stream) {
+  using C = Cfg<D>;
+  static std::once_flag once;
+  static int blocks_per_sm = 0;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, []() {
+    attr_err = cudaFuncSetAttribute(paged_decode_kernel<D, G>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &blocks_per_sm, paged_decode_kernel<D, G>, kThreads, C::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "decode kernel attributes");
+  if (blocks_per_sm < 1) return fail(PKV_ECUDA, "decode kernel does not fit on an SM");
+  decode_plan_kernel<<<1, 1024, 0, stream>>>(a);
+  if (int rc = check_launch("decode plan")) return rc;
+  const int grid = dev.sm_count * blocks_per_sm;
+  paged_decode_kernel<D, G><<<grid, kThreads, C::kSmemBytes, stream>>>(tk, tv, a);
+  if (int rc = check_launch("decode")) return rc;
+  if (a.max_partitions > 1) {
+    const int64_t pairs = (int64_t)a.S * a.Hq;
+    decode_combine_kernel<D><<<(unsigned)((pairs + 3) / 4), 128, 0, stream>>>(a);
+    if (int rc = check_launch("decode combine")) return rc;
+  }
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" int pkv_decode_workspace_bytes(int32_t S, int32_t Hq, int32_t D,
+                                          int32_t max_context_len, int32_t partition_size,
+                                          size_t* out) {
+  PKV_REQUIRE(out, "pkv_decode_workspace_bytes: out is NULL");
+  PKV_REQUIRE(S >= 0 && Hq > 0 && (D == 64 || D == 128) && max_context_len >= 0,
+              "pkv_decode_workspace_bytes: bad sizes");
+  int32_t tiles = 0;
+  if (int rc = resolve_partition(partition_size, &tiles)) return rc;
+  const int64_t P = (int64_t)tiles * kTileTokens;
+  const int64_t max_parts = max_context_len > 0 ? (max_context_len + P - 1) / P : 1;
+  *out = ws_layout(S, Hq, D, max_parts).total;
+  return ok();
+}
+
+extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
+                                          const void* v_cache, const int32_t* block_tables,
+                                          int32_t max_blocks_per_seq,
+                                          const int32_t* context_lens, int32_t max_context_len,
+                                          int32_t S, int32_t Hq, int32_t Hkv, int32_t D,
+                                          int32_t block_size, int32_t num_blocks, float scale,
+                                          int32_t partition_size, void* workspace,
+                                          size_t workspace_bytes, int32_t* dev_status,
+                                          void* stream) {
+  PKV_REQUIRE(S >= 0, "decode: S must be >= 0");
+  PKV_REQUIRE(Hkv > 0 && Hq > 0 && Hq % Hkv == 0, "decode: Hq (%d) must be a multiple of Hkv (%d)",
+              Hq, Hkv);
+  const int G = Hq / Hkv;
+  PKV_REQUIRE(G == 1 || G == 2 || G == 4 || G == 8, "decode: Hq/Hkv must be 1, 2, 4 or 8 (got %d)",
+              G);
+  PKV_REQUIRE(D == 64 || D == 128, "decode: D must be 64 or 128 (got %d)", D);
+  PKV_REQUIRE(block_size == 8 || block_size == 16 || block_size == 32,
+              "decode: block_size must be 8, 16 or 32 (got %d)", block_size);
+  PKV_REQUIRE(num_blocks > 0 && (int64_t)num_blocks * Hkv * block_size < (int64_t(1) << 31),
+              "decode: num_blocks * Hkv * block_size must be in [1, 2^31)");
+  PKV_REQUIRE(max_context_len >= 1, "decode: max_context_len must be >= 1");
+  PKV_REQUIRE((int64_t)max_blocks_per_seq * block_size >= max_context_len,
+              "decode: max_context_len %d exceeds max_blocks_per_seq * block_size", max_context_len);
+  PKV_REQUIRE(std::isfinite(scale), "decode: scale must be finite");
+  if (S == 0) return ok();
+  PKV_REQUIRE(out && q && k_cache && v_cache && block_tables && context_lens && workspace,
+              "decode: NULL pointer");
+  PKV_REQUIRE(aligned16(out) && aligned16(q) && aligned16(k_cache) && aligned16(v_cache),
+              "decode: bf16 arrays must be 16-byte aligned");
+  PKV_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0,
+              "decode: workspace must be 256-byte aligned");
+  int32_t tiles = 0;
+  if (int rc = resolve_partition(partition_size, &tiles)) return rc;
+  const int64_t P = (int64_t)tiles * kTileTokens;
+  const int64_t max_parts = (max_context_len + P - 1) / P;
+  const WsLayout ws = ws_layout(S, Hq, D, max_parts);
+  PKV_REQUIRE(workspace_bytes >= ws.total, "decode: workspace has %zu bytes, needs %zu",
+              workspace_bytes, ws.total);
+  const DeviceInfo* dev = nullptr;
+  if (int rc = current_device_info(&dev)) return rc;
+
+  CUtensorMap tk, tv;
+  const uint64_t rows = (uint64_t)num_blocks * Hkv * block_size;
+  const uint32_t box_rows = block_size < kTileTokens ? block_size : kTileTokens;
+  if (int rc = encode_tile_map_2d(&tk, k_cache, D, rows, (uint64_t)D * 2, 64, box_rows)) return rc;
+  if (int rc = encode_tile_map_2d(&tv, v_cache, D, rows, (uint64_t)D * 2, 64, box_rows)) return rc;
+
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  DecodeArgs a;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.S = S;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.max_context_len = max_context_len;
+  a.partition_tiles = tiles;
+  a.max_partitions = (int32_t)max_parts;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.ticket = reinterpret_cast<int32_t*>(wsb);
+  a.n_items = reinterpret_cast<int32_t*>(wsb) + 1;
+  a.items = reinterpret_cast<int2*>(wsb + ws.items_off);
+  a.ws_ml = reinterpret_cast<float2*>(wsb + ws.ml_off);
+  a.ws_o = reinterpret_cast<float*>(wsb + ws.o_off);
+  a.status = dev_status;
+  const WaitConfig wc = wait_config();
+  a.timeout_ns = wc.timeout_ns;
+  a.force_timeout = wc.force_timeout;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = PKV_OK;
+#define PKV_DECODE_CASE(DD, GG) \
+  if (D == DD && G == GG) rc = launch_decode<DD, GG>(tk, tv, a, *dev, st);
+  PKV_DECODE_CASE(64, 1)
+  PKV_DECODE_CASE(64, 2)
+  PKV_DECODE_CASE(64, 4)
+  PKV_DECODE_CASE(64, 8)
+  PKV_DECODE_CASE(128, 1)
+  PKV_DECODE_CASE(128, 2)
+  PKV_DECODE_CASE(128, 4)
+  PKV_DECODE_CASE(128, 8)
+#undef PKV_DECODE_CASE
+  if (rc) return rc;
+  return ok();
+}

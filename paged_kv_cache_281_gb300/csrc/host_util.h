@@ -1,0 +1,38 @@
+// Host-side CUDA helpers used by the launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace pkv {
+
+struct DeviceInfo {
+  bool ok = false;
+  int sm_count = 0;
+  int cc_major = 0;
+  int cc_minor = 0;
+  int max_smem_optin = 0;
+};
+
+// Properties of the current device, queried once per device. Fails unless the
+// device is sm_103 (the only architecture the kernels are compiled for).
+int current_device_info(const DeviceInfo** out);
+
+int cuda_fail(cudaError_t err, const char* what);
+int check_launch(const char* what);
+
+// Row-major bf16 matrix of `outer_rows` rows, `inner_elems` elements each, rows
+// `row_stride_bytes` apart; tiles of box_outer rows x box_inner elements,
+// 128-byte swizzled in shared memory.
+int encode_tile_map_2d(CUtensorMap* map, const void* base, uint64_t inner_elems,
+                       uint64_t outer_rows, uint64_t row_stride_bytes, uint32_t box_inner,
+                       uint32_t box_outer);
+
+int encode_tile_map_3d(CUtensorMap* map, const void* base, const uint64_t dims[3],
+                       const uint64_t strides_bytes[2], const uint32_t box[3]);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace pkv
