@@ -183,6 +183,33 @@ int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
                                int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * paged_attention_decode_noalloc — the same decode as above, for callers that
+ * cannot provide device scratch memory (a plugin handed only its inputs and
+ * outputs, an engine whose KV pool already holds all free HBM, a decode loop
+ * that must not call cudaMalloc because it can synchronise the device). The
+ * pages have no counterpart: this is an interface convenience of the library.
+ *   - Scratch: a fixed array of PKV_DECODE_NOALLOC_SCRATCH_BYTES inside the
+ *     library, held on every GPU that loads the library until the process
+ *     exits. A batch whose pkv_decode_workspace_bytes() exceeds it is rejected
+ *     with PKV_EINVAL (a larger partition_size needs less).
+ *   - Allocates nothing. The first call on a device looks up the array's
+ *     device address for that device (once, with it current); make that first
+ *     call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents;
+ *     every call rewrites what it reads first. Calls that overlap on the GPU
+ *     (other streams, other host threads) race on it: serialise them.
+ *   Arguments, layouts and results are those of pkv_paged_attention_decode.
+ * ---------------------------------------------------------------------- */
+#define PKV_DECODE_NOALLOC_SCRATCH_BYTES (64u << 20)
+int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                       const void* v_cache, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                       int32_t max_context_len, int32_t S, int32_t Hq,
+                                       int32_t Hkv, int32_t D, int32_t block_size,
+                                       int32_t num_blocks, float scale, int32_t partition_size,
+                                       int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * paged_attention_prefill — a chunk of a prompt attending causally over its
  * own cached blocks ("Deep Dive: continuous batching", section The
  * prefill/decode mix; the chunk's keys and values are appended first).

@@ -44,6 +44,9 @@ SIGNATURES = {
     "pkv_decode_workspace_bytes": (ctypes.c_int, [i32, i32, i32, i32, i32, P(sz)]),
     "pkv_paged_attention_decode": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
                                                   i32, i32, i32, f32, i32, vp, sz, vp, vp]),
+    "pkv_paged_attention_decode_noalloc": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, vp, i32, i32,
+                                                          i32, i32, i32, i32, i32, f32, i32, vp,
+                                                          vp]),
     "pkv_prefill_workspace_bytes": (ctypes.c_int, [i32, i32, i32, i32, P(sz)]),
     "pkv_paged_attention_prefill": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                    i32, i32, i32, i32, i32, i32, f32, vp, sz, vp,

@@ -24,7 +24,8 @@ from ._lib import PagedKVError, check, lib
 __all__ = [
     "PagedKVError", "pkv_version", "pkv_last_error", "BlockAllocator",
     "pkv_kv_append", "pkv_block_copy", "pkv_decode_workspace_bytes",
-    "pkv_paged_attention_decode", "pkv_prefill_workspace_bytes",
+    "pkv_paged_attention_decode", "pkv_paged_attention_decode_noalloc",
+    "NOALLOC_SCRATCH_BYTES", "pkv_prefill_workspace_bytes",
     "pkv_paged_attention_prefill", "pkv_status_reset", "pkv_check_status",
     "pkv_debug_set_wait", "new_status",
 ]
@@ -227,6 +228,32 @@ def pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_l
         block_tables.data_ptr(), int(block_tables.shape[1]), context_lens.data_ptr(),
         int(max_context_len), S, Hq, Hkv, D, B, N, float(scale), int(partition_size),
         workspace.data_ptr(), int(workspace.numel()), _ptr(status), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20  # PKV_DECODE_NOALLOC_SCRATCH_BYTES
+
+
+def pkv_paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
+                                       max_context_len: int, scale: float, partition_size: int = 0,
+                                       status=None, stream=None) -> None:
+    """Decode for callers that cannot supply device scratch: the library uses a
+    fixed internal array of NOALLOC_SCRATCH_BYTES instead, shared by all calls
+    (serialise overlapping calls). Allocates no memory."""
+    N, Hkv, B, D = _pool_shape(k_cache, v_cache)
+    _dev(q, "q", torch.bfloat16, 3)
+    _dev(out, "out", torch.bfloat16, 3)
+    _dev(block_tables, "block_tables", torch.int32, 2)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    S, Hq = int(q.shape[0]), int(q.shape[1])
+    if q.shape[2] != D or out.shape != q.shape:
+        raise ValueError("q/out must be [S, Hq, D] with the pools' D")
+    if block_tables.shape[0] != S or context_lens.shape[0] != S:
+        raise ValueError("block_tables/context_lens must have S rows")
+    check(lib().pkv_paged_attention_decode_noalloc(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_tables.data_ptr(), int(block_tables.shape[1]), context_lens.data_ptr(),
+        int(max_context_len), S, Hq, Hkv, D, B, N, float(scale), int(partition_size),
+        _ptr(status), _stream(stream)))
 
 
 def pkv_prefill_workspace_bytes(S: int, total_q: int, Hq: int, D: int) -> int:

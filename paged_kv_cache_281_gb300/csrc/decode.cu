@@ -603,3 +603,70 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
   if (rc) return rc;
   return ok();
 }
+
+// ---------------------------------------------------------------------------
+// Decode without a caller-supplied workspace.
+//
+// Some callers cannot hand the library device scratch memory: a plugin that
+// is given only its input and output buffers by the host framework, an engine
+// whose KV pool already reserved every free byte of HBM, or a latency-critical
+// loop that must not call cudaMalloc (which can synchronise the device). For
+// them the split-K scratch lives in this fixed array, which every GPU that
+// loads the library holds until the process exits.
+static __device__ __align__(256) uint8_t g_decode_noalloc_scratch[PKV_DECODE_NOALLOC_SCRATCH_BYTES];
+
+namespace pkv {
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+cudaError_t g_noalloc_err[kNoAllocMaxDevices] = {};
+std::once_flag g_noalloc_once[kNoAllocMaxDevices];
+
+// Device address of the scratch array on the current device. In host code the
+// array's name is only a stand-in, so the address is looked up once per
+// device, with that device current.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return fail(PKV_EINVAL, "decode_noalloc: device ordinal %d unsupported", dev);
+  std::call_once(g_noalloc_once[dev], [dev]() {
+    void* p = nullptr;
+    g_noalloc_err[dev] = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
+    if (g_noalloc_err[dev] == cudaSuccess) g_noalloc_ptr[dev] = p;
+  });
+  if (g_noalloc_err[dev] != cudaSuccess)
+    return cuda_fail(g_noalloc_err[dev], "decode_noalloc: cudaGetSymbolAddress");
+  *out = g_noalloc_ptr[dev];
+  return PKV_OK;
+}
+}  // namespace
+}  // namespace pkv
+
+extern "C" int pkv_paged_attention_decode_noalloc(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t max_context_len, int32_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t block_size,
+    int32_t num_blocks, float scale, int32_t partition_size, int32_t* dev_status, void* stream) {
+  size_t need = 0;
+  if (int rc = pkv_decode_workspace_bytes(S, Hq, D, max_context_len, partition_size, &need))
+    return rc;
+  if (need > (size_t)PKV_DECODE_NOALLOC_SCRATCH_BYTES)
+    return fail(PKV_EINVAL,
+                "decode_noalloc: this batch needs %zu bytes of scratch, more than the built-in "
+                "%zu (use pkv_paged_attention_decode with a workspace, or a larger "
+                "partition_size)",
+                need, (size_t)PKV_DECODE_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  if (S > 0) {
+    if (int rc = noalloc_scratch(&scratch)) return rc;
+  }
+  // The plan kernel rewrites the item list and resets the work ticket at the
+  // start of every call, so nothing left in the array by an earlier call is
+  // read before it is written.
+  return pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                    context_lens, max_context_len, S, Hq, Hkv, D, block_size,
+                                    num_blocks, scale, partition_size, scratch,
+                                    (size_t)PKV_DECODE_NOALLOC_SCRATCH_BYTES, dev_status, stream);
+}
