@@ -68,6 +68,18 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def max_over_ranks(x: float) -> float:
+    """The maximum of ``x`` over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def workload_for_rank(rank: int):
     from workloads import config3, make_decode_workload, SEED_BASE
     w = config3()
@@ -267,10 +279,7 @@ def main():
     pkv.pkv_check_status(d.status)
     total_ms = start.elapsed_time(end)
     decode_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms)
     ms_per_step = total_ms / args.steps
     kv_bytes = w.kv_bytes()
     value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
