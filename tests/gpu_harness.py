@@ -114,3 +114,154 @@ def decode_step(w, d: DeviceDecode, stream=None) -> torch.Tensor:
     pkv.pkv_kv_append(d.k_last, d.v_last, d.last_slot_mapping, d.k_cache, d.v_cache,
                       status=d.status, stream=stream)
     return run_decode(w, d, stream=stream)
+
+
+# ---------------------------------------------------------------- shared prefix
+
+@dataclass
+class DeviceSharedPrefix:
+    alloc: pkv.BlockAllocator
+    sample_ids: list
+    prefix_slots: list
+    tail_slots: list
+    cow_pairs: list
+    tables: np.ndarray
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    q: torch.Tensor
+    block_tables: torch.Tensor
+    context_lens: torch.Tensor
+    status: torch.Tensor
+    max_context_len: int
+
+
+def setup_shared_prefix(w, device="cuda") -> DeviceSharedPrefix:
+    """The shared-prefix build order through the library: prefixes appended,
+    samples forked, tails reserved (copy-on-write pairs collected), copies
+    made, then tails written."""
+    alloc = pkv.BlockAllocator(w.num_blocks, w.block_size, w.free_order)
+    sample_ids, prefix_slots = [], []
+    for _ in range(w.n_prompts):
+        sid = alloc.seq_create()
+        sl, pair = alloc.seq_append_slots(sid, w.prefix_len)
+        assert pair is None
+        prefix_slots.append(sl)
+        sample_ids.append(sid)
+        for _ in range(w.n_samples - 1):
+            sample_ids.append(alloc.seq_fork(sid))
+    tail_slots, pairs = [], []
+    for i, sid in enumerate(sample_ids):
+        sl, pair = alloc.seq_append_slots(sid, int(w.tails.reshape(-1)[i]))
+        tail_slots.append(sl)
+        if pair is not None:
+            pairs.append(pair)
+    k_cache, v_cache = poisoned_pools(w.num_blocks, w.Hkv, w.block_size, w.D, device)
+    status = pkv.new_status(device)
+    pkv.pkv_kv_append(to_dev_bf16(w.prefix_k.reshape(-1, w.Hkv, w.D), device),
+                      to_dev_bf16(w.prefix_v.reshape(-1, w.Hkv, w.D), device),
+                      torch.from_numpy(np.concatenate(prefix_slots).astype(np.int32)).to(device),
+                      k_cache, v_cache, status=status)
+    if pairs:
+        pkv.pkv_block_copy(k_cache, v_cache,
+                           torch.tensor(pairs, dtype=torch.int32, device=device), status=status)
+    tails = np.concatenate(tail_slots).astype(np.int32)
+    if tails.size:
+        pkv.pkv_kv_append(to_dev_bf16(w.tail_k, device), to_dev_bf16(w.tail_v, device),
+                          torch.from_numpy(tails).to(device), k_cache, v_cache, status=status)
+    lens = w.context_lens
+    maxB = -(-int(lens.max()) // w.block_size)
+    tables, got_lens = alloc.build_block_tables(sample_ids, maxB)
+    assert np.array_equal(got_lens, lens)
+    return DeviceSharedPrefix(alloc, sample_ids, prefix_slots, tail_slots, pairs, tables,
+                              k_cache, v_cache, to_dev_bf16(w.q, device),
+                              torch.from_numpy(tables).to(device),
+                              torch.from_numpy(got_lens).to(device), status, int(lens.max()))
+
+
+def decode_shared_prefix(w, d: DeviceSharedPrefix, partition_size=0) -> torch.Tensor:
+    out = torch.empty(w.S, w.Hq, w.D, dtype=torch.bfloat16, device=d.q.device)
+    ws = torch.empty(pkv.pkv_decode_workspace_bytes(w.S, w.Hq, w.D, d.max_context_len,
+                                                    partition_size),
+                     dtype=torch.uint8, device=d.q.device)
+    pkv.pkv_paged_attention_decode(out, d.q, d.k_cache, d.v_cache, d.block_tables,
+                                   d.context_lens, d.max_context_len, w.scale, ws,
+                                   partition_size=partition_size, status=d.status)
+    return out
+
+
+# ---------------------------------------------------------------- trace
+
+class DeviceTrace:
+    """Runs the continuous-batching trace through the library: per iteration,
+    the allocator reserves slots (new blocks only when the last one fills),
+    ``kv_append`` writes every new token, prefill attends for the prompt
+    chunks and decode for the running sequences, and finished requests free
+    their blocks."""
+
+    def __init__(self, cfg, device="cuda"):
+        self.cfg = cfg
+        self.device = device
+        self.alloc = pkv.BlockAllocator(cfg.num_blocks, cfg.block_size)
+        self.k_cache, self.v_cache = poisoned_pools(cfg.num_blocks, cfg.Hkv, cfg.block_size,
+                                                    cfg.D, device)
+        self.status = pkv.new_status(device)
+        self.sid = {}
+        self.max_blocks = -(-(cfg.prompt_max + cfg.out_cap) // cfg.block_size)
+        self.scale = 1.0 / np.sqrt(cfg.D)
+        self.ws = torch.empty(pkv.pkv_decode_workspace_bytes(
+            cfg.max_running, cfg.Hq, cfg.D, cfg.prompt_max + cfg.out_cap),
+            dtype=torch.uint8, device=device)
+        self.pws = torch.empty(256, dtype=torch.uint8, device=device)
+
+    def host_metadata(self, itr):
+        """Allocator work and metadata for one iteration (host side)."""
+        for rid in itr.admitted:
+            self.sid[rid] = self.alloc.seq_create()
+        slots = []
+        for wk in itr.work:
+            sl, pair = self.alloc.seq_append_slots(self.sid[wk.rid], wk.n)
+            assert pair is None
+            slots.append(sl)
+        pre, dec = itr.prefill, itr.decode
+        meta = {"slots": np.concatenate(slots).astype(np.int32) if slots else
+                np.zeros(0, np.int32)}
+        for name, works in (("prefill", pre), ("decode", dec)):
+            ids = [self.sid[wk.rid] for wk in works]
+            tables, lens = self.alloc.build_block_tables(ids, self.max_blocks)
+            meta[name] = (tables, lens)
+        meta["cu"] = np.concatenate([[0], np.cumsum([wk.n for wk in pre])]).astype(np.int32)
+        return meta
+
+    def run_iteration(self, itr, meta, stream=None):
+        """The GPU part of one iteration; returns (prefill_out, decode_out)."""
+        cfg, dev = self.cfg, self.device
+        T = itr.num_tokens
+        n_pre = int(meta["cu"][-1])
+        q = to_dev_bf16(np.ascontiguousarray(itr.q), dev)
+        if T:
+            pkv.pkv_kv_append(to_dev_bf16(np.ascontiguousarray(itr.k), dev),
+                              to_dev_bf16(np.ascontiguousarray(itr.v), dev),
+                              torch.from_numpy(meta["slots"]).to(dev), self.k_cache,
+                              self.v_cache, status=self.status, stream=stream)
+        pre_out = dec_out = None
+        tables, lens = meta["prefill"]
+        if len(lens):
+            pre_out = torch.empty(n_pre, cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
+            chunks = np.diff(meta["cu"])
+            pkv.pkv_paged_attention_prefill(
+                pre_out, q[:n_pre], torch.from_numpy(meta["cu"]).to(dev),
+                torch.from_numpy(lens).to(dev), self.k_cache, self.v_cache,
+                torch.from_numpy(tables).to(dev), int(chunks.max()), int(lens.max()),
+                self.scale, self.pws, status=self.status, stream=stream)
+        tables, lens = meta["decode"]
+        if len(lens):
+            dec_out = torch.empty(len(lens), cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
+            pkv.pkv_paged_attention_decode(
+                dec_out, q[n_pre:], self.k_cache, self.v_cache,
+                torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev),
+                int(lens.max()), self.scale, self.ws, status=self.status, stream=stream)
+        return pre_out, dec_out
+
+    def finish(self, itr):
+        for rid in itr.finished:
+            self.alloc.seq_free(self.sid.pop(rid))

@@ -109,3 +109,60 @@ def build_shared_prefix_state(w, poison=True) -> OracleSharedPrefixState:
 def bf16_tolerance_ok(gpu: np.ndarray, ref: np.ndarray, atol=2e-3, rtol=1e-2) -> np.ndarray:
     """Elementwise ``|gpu - ref| <= atol + rtol * |ref|``."""
     return np.abs(gpu - ref) <= atol + rtol * np.abs(ref)
+
+
+class OracleTrace:
+    """The continuous-batching trace on the oracle side: the oracle's
+    allocator model, its own pools and fp64 attention for chosen sequences."""
+
+    def __init__(self, cfg, poison=True):
+        self.cfg = cfg
+        self.alloc = paging.BlockAllocator(cfg.num_blocks, cfg.block_size)
+        self.k_cache, self.v_cache = empty_pools(cfg.num_blocks, cfg.Hkv, cfg.block_size,
+                                                 cfg.D, poison)
+        self.sid = {}
+        self.scale = 1.0 / np.sqrt(cfg.D)
+
+    def step(self, itr):
+        """Reserve slots and write this iteration's tokens; returns the slots."""
+        for rid in itr.admitted:
+            self.sid[rid] = self.alloc.create()
+        slots = []
+        for wk in itr.work:
+            sl, pairs = self.alloc.append_slots(self.sid[wk.rid], wk.n)
+            assert not pairs
+            slots.extend(sl)
+        cache.append(self.k_cache, self.v_cache, itr.k, itr.v, slots, self.cfg.block_size)
+        return np.asarray(slots, dtype=np.int32)
+
+    def prefill(self, itr, which):
+        """fp64 outputs of the prefill works with indices ``which``: {index: [n, Hq, D]}."""
+        out = {}
+        pre = itr.prefill
+        row0 = np.concatenate([[0], np.cumsum([wk.n for wk in pre])])
+        for i in which:
+            wk = pre[i]
+            sid = self.sid[wk.rid]
+            L = self.alloc.seq_len(sid)
+            cu = np.array([0, wk.n])
+            out[i] = attention.prefill(itr.q[row0[i]:row0[i] + wk.n], cu, [L], self.k_cache,
+                                       self.v_cache, [self.alloc.block_table(sid)],
+                                       self.cfg.block_size, self.scale)
+        return out
+
+    def decode(self, itr, which):
+        """fp64 outputs of the decode works with indices ``which``: {index: [Hq, D]}."""
+        out = {}
+        n_pre = sum(wk.n for wk in itr.prefill)
+        dec = itr.decode
+        for i in which:
+            sid = self.sid[dec[i].rid]
+            L = self.alloc.seq_len(sid)
+            out[i] = attention.decode(itr.q[n_pre + i:n_pre + i + 1], self.k_cache, self.v_cache,
+                                      [self.alloc.block_table(sid)], [L], self.cfg.block_size,
+                                      self.scale)[0]
+        return out
+
+    def finish(self, itr):
+        for rid in itr.finished:
+            self.alloc.free_seq(self.sid.pop(rid))
