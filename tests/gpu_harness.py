@@ -232,35 +232,55 @@ class DeviceTrace:
         meta["cu"] = np.concatenate([[0], np.cumsum([wk.n for wk in pre])]).astype(np.int32)
         return meta
 
-    def run_iteration(self, itr, meta, stream=None):
-        """The GPU part of one iteration; returns (prefill_out, decode_out)."""
-        cfg, dev = self.cfg, self.device
-        T = itr.num_tokens
-        n_pre = int(meta["cu"][-1])
-        q = to_dev_bf16(np.ascontiguousarray(itr.q), dev)
-        if T:
-            pkv.pkv_kv_append(to_dev_bf16(np.ascontiguousarray(itr.k), dev),
-                              to_dev_bf16(np.ascontiguousarray(itr.v), dev),
-                              torch.from_numpy(meta["slots"]).to(dev), self.k_cache,
-                              self.v_cache, status=self.status, stream=stream)
-        pre_out = dec_out = None
+    def upload(self, itr, meta):
+        """Host -> device copies of one iteration's inputs and metadata."""
+        dev = self.device
+        t = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        up = {"q": to_dev_bf16(np.ascontiguousarray(itr.q), dev), "n_pre": int(meta["cu"][-1])}
+        if itr.num_tokens:
+            up["k"] = to_dev_bf16(np.ascontiguousarray(itr.k), dev)
+            up["v"] = to_dev_bf16(np.ascontiguousarray(itr.v), dev)
+            up["slots"] = t(meta["slots"])
         tables, lens = meta["prefill"]
         if len(lens):
-            pre_out = torch.empty(n_pre, cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
-            chunks = np.diff(meta["cu"])
-            pkv.pkv_paged_attention_prefill(
-                pre_out, q[:n_pre], torch.from_numpy(meta["cu"]).to(dev),
-                torch.from_numpy(lens).to(dev), self.k_cache, self.v_cache,
-                torch.from_numpy(tables).to(dev), int(chunks.max()), int(lens.max()),
-                self.scale, self.pws, status=self.status, stream=stream)
+            up["pre"] = (t(meta["cu"]), t(lens), t(tables), int(np.diff(meta["cu"]).max()),
+                         int(lens.max()))
         tables, lens = meta["decode"]
         if len(lens):
-            dec_out = torch.empty(len(lens), cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
-            pkv.pkv_paged_attention_decode(
-                dec_out, q[n_pre:], self.k_cache, self.v_cache,
-                torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev),
-                int(lens.max()), self.scale, self.ws, status=self.status, stream=stream)
+            up["dec"] = (t(lens), t(tables), int(lens.max()), len(lens))
+        return up
+
+    def launch(self, up, stream=None, events=None):
+        """The GPU part of one iteration: kv_append, prefill, decode. With
+        ``events`` (four CUDA events) the boundaries are recorded on ``stream``."""
+        cfg, dev = self.cfg, self.device
+        rec = (lambda i: events[i].record(stream)) if events else (lambda i: None)
+        rec(0)
+        if "k" in up:
+            pkv.pkv_kv_append(up["k"], up["v"], up["slots"], self.k_cache, self.v_cache,
+                              status=self.status, stream=stream)
+        rec(1)
+        pre_out = dec_out = None
+        n_pre = up["n_pre"]
+        if "pre" in up:
+            cu, lens, tables, max_q, max_ctx = up["pre"]
+            pre_out = torch.empty(n_pre, cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
+            pkv.pkv_paged_attention_prefill(pre_out, up["q"][:n_pre], cu, lens, self.k_cache,
+                                            self.v_cache, tables, max_q, max_ctx, self.scale,
+                                            self.pws, status=self.status, stream=stream)
+        rec(2)
+        if "dec" in up:
+            lens, tables, max_ctx, n = up["dec"]
+            dec_out = torch.empty(n, cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
+            pkv.pkv_paged_attention_decode(dec_out, up["q"][n_pre:], self.k_cache, self.v_cache,
+                                           tables, lens, max_ctx, self.scale, self.ws,
+                                           status=self.status, stream=stream)
+        rec(3)
         return pre_out, dec_out
+
+    def run_iteration(self, itr, meta, stream=None):
+        """Upload and run one iteration; returns (prefill_out, decode_out)."""
+        return self.launch(self.upload(itr, meta), stream=stream)
 
     def finish(self, itr):
         for rid in itr.finished:
