@@ -102,7 +102,7 @@ def workload_description(w, partition_size):
         "context_len": {"median": 1024, "sigma": 0.8, "clip": [16, 8192],
                         "max": w.max_context_len},
         "kv_bytes_per_step": w.kv_bytes(),
-        "partition_size": partition_size or 512,
+        "partition_size": partition_size or 1024,
         "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB of L2"
               % (w.kv_bytes() / 1e9),
     }
@@ -349,7 +349,7 @@ def main():
     stream = torch.cuda.current_stream()
     parts = pkv.pkv_decode_workspace_bytes(1, 1, w.D, w.max_context_len, args.partition_size)
     del parts
-    P = args.partition_size or 512
+    P = args.partition_size or 1024
     launches_per_step = 1 + 2 + (1 if math.ceil(w.max_context_len / P) > 1 else 0)
 
     def barrier():

@@ -164,7 +164,7 @@ int pkv_block_copy(void* k_cache, void* v_cache, const int32_t* pairs, int32_t n
  *   max_context_len : an upper bound of context_lens (host value); it sizes
  *                  the split into partitions and the workspace.
  *   partition_size : tokens per split-K partition (multiple of 16, >= 16), or
- *                  0 for the library default (512). Long contexts are split
+ *                  0 for the library default (1024). Long contexts are split
  *                  into partitions whose partial softmax states are merged by
  *                  a second kernel; the split depends only on positions, so
  *                  results do not depend on physical placement.

@@ -41,7 +41,7 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileTokens = 16;
-constexpr int kDefaultPartition = 512;
+constexpr int kDefaultPartition = 1024;
 
 template <int D>
 struct Cfg {
