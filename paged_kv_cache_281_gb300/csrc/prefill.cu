@@ -13,10 +13,10 @@
 // share one kv head, so every key/value tile loaded serves all of them.
 //  * Q is loaded once by a 3-D TMA box (64 columns x G heads x 128/G queries)
 //    per 64-column half, 128-byte swizzled.
-//  * For each 128-key tile (whole pages located through the block table, one
+//  * For each 64-key tile (whole pages located through the block table, one
 //    TMA box per page and half) S = Q K^T is computed by tcgen05.mma
-//    (M=128, N=128, K=16 steps) into tensor memory.
-//  * Thread r owns TMEM lane r = row r: it loads its 128 scores, applies the
+//    (M=128, N=64, K=16 steps) into tensor memory.
+//  * Thread r owns TMEM lane r = row r: it loads its 64 scores, applies the
 //    causal limit, updates its running max and sum (base 2) and writes its
 //    probabilities to shared memory as two bf16 parts P_hi + P_lo in the
 //    swizzled K-major layout the next MMA reads. When the max moved, it
@@ -27,8 +27,10 @@
 //    soon as the P V MMA retires, so loads overlap the softmax.
 //  * Every mbarrier wait has a time limit; on expiry the CTA records
 //    PKV_ETIMEOUT, waits (with a limit) for its own copies and MMAs, frees its
-//    tensor memory and returns. The shared-memory request keeps one CTA per
-//    SM, so the tensor-memory allocation never waits on another CTA.
+//    tensor memory and returns. About 97 KB of shared memory per CTA lets two
+//    CTAs share an SM (one's softmax overlaps the other's MMAs and loads); the
+//    request never allows a third, so the two 256-column tensor-memory
+//    allocations always fit and allocation never waits.
 #include <cmath>
 #include <mutex>
 
@@ -39,22 +41,25 @@ namespace pkv {
 namespace {
 
 constexpr int kRows = 128;       // (query, head) rows per tile = TMEM lanes
-constexpr int kKeys = 128;       // keys per KV tile
+constexpr int kKeys = 64;        // keys per KV tile
 constexpr int kThreadsP = 128;
-constexpr uint32_t kHalfTile = 128 * 128;  // bytes of one 128-row x 128-byte region
+constexpr uint32_t kQHalf = kRows * 128;   // one 64-column half of Q: 128 rows x 128 B
+constexpr uint32_t kKVHalf = kKeys * 128;  // one 64-column half of a K or V tile
+constexpr uint32_t kPTile = kRows * kKeys * 2;  // P (one part): 128 rows x 64 keys
 
 template <int D>
 struct PCfg {
   static constexpr int kHalves = D / 64;
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kHalves * kHalfTile;
-  static constexpr uint32_t kV = kK + kHalves * kHalfTile;
-  static constexpr uint32_t kPhi = kV + kHalves * kHalfTile;
-  static constexpr uint32_t kPlo = kPhi + 2 * kHalfTile;
-  static constexpr uint32_t kBytes = kPlo + 2 * kHalfTile;
-  // more than half of an SM's shared memory: one CTA per SM
-  static constexpr uint32_t kSmem = kBytes + 1024 > 120u * 1024 ? kBytes + 1024 : 120u * 1024;
-  static constexpr uint32_t kTmemCols = 256;  // S: 128 columns, O: D columns
+  static constexpr uint32_t kK = kQ + kHalves * kQHalf;
+  static constexpr uint32_t kV = kK + kHalves * kKVHalf;
+  static constexpr uint32_t kPhi = kV + kHalves * kKVHalf;
+  static constexpr uint32_t kPlo = kPhi + kPTile;
+  static constexpr uint32_t kBytes = kPlo + kPTile;
+  // more than a third of an SM's shared memory: at most two CTAs per SM, whose
+  // two tensor-memory allocations always fit, so allocation never waits
+  static constexpr uint32_t kSmem = kBytes + 1024 > 80u * 1024 ? kBytes + 1024 : 80u * 1024;
+  static constexpr uint32_t kTmemCols = 256;  // S: 64 columns, O: D columns at 128
   static constexpr uint32_t kOcol = 128;
 };
 
@@ -71,7 +76,7 @@ struct PrefillArgs {
   int32_t force_timeout;
 };
 
-// Loads the pages holding keys [key0, min(key0 + 128, kv_end)) of kv head
+// Loads the pages holding keys [key0, min(key0 + 64, kv_end)) of kv head
 // `kvh` from the pool behind `map` (keys or values) into `dst`; arms `bar`.
 template <int D>
 __device__ void load_kv_tile(const CUtensorMap* map, const PrefillArgs& a, const int32_t* bt,
@@ -98,12 +103,12 @@ __device__ void load_kv_tile(const CUtensorMap* map, const PrefillArgs& a, const
     const int row = (blk * a.Hkv + kvh) * B;
 #pragma unroll
     for (int h = 0; h < C::kHalves; ++h)
-      tma_load_2d(dst + h * kHalfTile + pg * B * 128, map, h * 64, row, bar);
+      tma_load_2d(dst + h * kKVHalf + pg * B * 128, map, h * 64, row, bar);
   }
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreadsP, 1)
+__global__ void __launch_bounds__(kThreadsP, 2)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                          const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
@@ -162,10 +167,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   // timed-out CTA waits for before it leaves.
   int armed[5] = {0, 0, 0, 0, 0}, seen[5] = {0, 0, 0, 0, 0};
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar_of[kBarQ], C::kHalves * kHalfTile);
+    mbar_arrive_expect_tx(bar_of[kBarQ], C::kHalves * kQHalf);
 #pragma unroll
     for (int h = 0; h < C::kHalves; ++h)
-      tma_load_3d(base + C::kQ + h * kHalfTile, &tmap_q, h * 64, kvh * G, c0 + q0,
+      tma_load_3d(base + C::kQ + h * kQHalf, &tmap_q, h * 64, kvh * G, c0 + q0,
                   bar_of[kBarQ]);
     load_kv_tile<D>(&tmap_k, a, bt, kvh, 0, kv_end, base + C::kK, bar_of[kBarK]);
     load_kv_tile<D>(&tmap_v, a, bt, kvh, 0, kv_end, base + C::kV, bar_of[kBarV]);
@@ -199,9 +204,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       tcgen05_after_sync();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kHalfTile + (kk & 3) * 32;
-        umma_bf16(t_s, umma_desc_sw128(base + C::kQ + off, 16, 1024),
-                  umma_desc_sw128(base + C::kK + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+        const uint32_t koff = (kk & 3) * 32;
+        umma_bf16(t_s, umma_desc_sw128(base + C::kQ + (kk >> 2) * kQHalf + koff, 16, 1024),
+                  umma_desc_sw128(base + C::kK + (kk >> 2) * kKVHalf + koff, 16, 1024), kIdescS,
+                  kk > 0 ? 1u : 0u);
       }
       umma_commit(bar_of[kBarS]);
       ++armed[kBarS];
@@ -246,7 +252,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         hi[e] = pack_bf16x2(p0, p1);
         lo[e] = pack_bf16x2(p0 - bf16_lo_to_f32(hi[e]), p1 - bf16_hi_to_f32(hi[e]));
       }
-      const uint32_t off = (ch >> 3) * kHalfTile + swz128(r, ch & 7);
+      const uint32_t off = swz128(r, ch);  // 64 keys: one 128-byte row per row
       *reinterpret_cast<uint4*>(phi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(plo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
@@ -267,14 +273,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 
     ok = wait(kBarV);
     if (!ok) break;
-    if (key0 + kKeys > kv_end && r >= kv_end - key0) {
+    if (key0 + kKeys > kv_end && r < kKeys && r >= kv_end - key0) {
       // keys past the last visible one: their value rows (unloaded pages, or
       // slots past the sequence end) must not reach O, not even as NaN * 0
 #pragma unroll
       for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(base_ptr + C::kV + h * kHalfTile + r * 128 + ch * 16) =
+          *reinterpret_cast<uint4*>(base_ptr + C::kV + h * kKVHalf + r * 128 + ch * 16) =
               make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();  // P and zeroed V rows before the tensor core reads them
@@ -284,8 +290,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       tcgen05_after_sync();
 #pragma unroll
       for (int kk = 0; kk < kKeys / 16; ++kk) {
-        const uint32_t poff = (kk >> 2) * kHalfTile + (kk & 3) * 32;
-        const uint64_t vdesc = umma_desc_sw128(base + C::kV + kk * 16 * 128, kHalfTile, 1024);
+        const uint32_t poff = kk * 32;
+        const uint64_t vdesc = umma_desc_sw128(base + C::kV + kk * 16 * 128, kKVHalf, 1024);
         umma_bf16(t_o, umma_desc_sw128(base + C::kPhi + poff, 16, 1024), vdesc, kIdescO,
                   (kt > 0 || kk > 0) ? 1u : 0u);
         umma_bf16(t_o, umma_desc_sw128(base + C::kPlo + poff, 16, 1024), vdesc, kIdescO, 1u);
