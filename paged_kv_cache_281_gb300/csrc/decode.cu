@@ -15,10 +15,11 @@
 //    (m, l, o) that a combine kernel merges with the online-softmax rule; a
 //    sequence with one partition is normalised in place.
 //  * Data movement. Each of the CTA's 4 warps owns every 4th tile of the item
-//    and a private 3-stage ring in shared memory. One lane per warp issues TMA
-//    tile loads (two 64-column halves per tensor, 128-byte swizzle) for whole
-//    pages located through the block table, signalling an mbarrier with the
-//    byte count; the warp waits on it with a time limit.
+//    and a private 3-stage ring in shared memory. The warp's lanes look up the
+//    block-table entries of its tiles in parallel; one lane issues TMA tile
+//    loads (two 64-column halves per tensor, 128-byte swizzle) for whole
+//    pages, signalling an mbarrier with the byte count; the warp waits on it
+//    with a time limit.
 //  * Arithmetic. The G query heads that share a kv head form the rows of a
 //    16-row MMA operand (rows >= G are zero). Scores S = Q K^T and the update
 //    O += P V run as m16n8k16 bf16 MMAs with fp32 accumulators held in
@@ -131,18 +132,25 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
   }
 }
 
-// Issues the TMA loads of one 16-token tile (keys and values of kv head `kvh`)
-// into `stage` and arms `bar` with the number of bytes that will land.
+// TMA box rows (at most two boxes of min(B,16) rows) holding the keys and
+// values of one 16-token tile of kv head `kvh`, and the bytes they bring.
+// A box past the sequence end is not loaded; a block-table entry outside the
+// pool is skipped and recorded.
+struct TileRows {
+  int32_t row[2];
+  uint32_t bytes;
+};
+
 template <int D>
-__device__ __forceinline__ void issue_tile(const CUtensorMap* tk, const CUtensorMap* tv,
-                                           const DecodeArgs& a, const int32_t* bt, int kvh,
-                                           int tile, int L, uint32_t stage, uint32_t bar) {
+__device__ __forceinline__ TileRows tile_rows(const DecodeArgs& a, const int32_t* bt, int kvh,
+                                              int tile, int L) {
   using C = Cfg<D>;
   const int B = a.block_size;
   const int R = B < kTileTokens ? B : kTileTokens;  // rows per TMA box
   const int nsub = kTileTokens / R;
-  int32_t rows[2] = {-1, -1};
-  uint32_t bytes = 0;
+  TileRows tr;
+  tr.row[0] = tr.row[1] = -1;
+  tr.bytes = 0;
   for (int sub = 0; sub < nsub; ++sub) {
     const int tok = tile * kTileTokens + sub * R;
     if (tok >= L) break;
@@ -151,17 +159,29 @@ __device__ __forceinline__ void issue_tile(const CUtensorMap* tk, const CUtensor
       record_status(a.status, PKV_EDEVICE, blk, kKernelDecode);
       continue;
     }
-    rows[sub] = (blk * a.Hkv + kvh) * B + tok % B;
-    bytes += 2u * C::kHalves * R * 128u;
+    tr.row[sub] = (blk * a.Hkv + kvh) * B + tok % B;
+    tr.bytes += 2u * C::kHalves * R * 128u;
   }
+  return tr;
+}
+
+// Arms `bar` with the tile's bytes and issues its TMA loads into `stage`.
+template <int D>
+__device__ __forceinline__ void issue_tile_rows(const CUtensorMap* tk, const CUtensorMap* tv,
+                                                int block_size, int32_t row0, int32_t row1,
+                                                uint32_t bytes, uint32_t stage, uint32_t bar) {
+  using C = Cfg<D>;
+  const int R = block_size < kTileTokens ? block_size : kTileTokens;
   mbar_arrive_expect_tx(bar, bytes);
-  for (int sub = 0; sub < nsub; ++sub) {
-    if (rows[sub] < 0) continue;
+#pragma unroll
+  for (int sub = 0; sub < 2; ++sub) {
+    const int32_t row = sub == 0 ? row0 : row1;
+    if (row < 0) continue;
 #pragma unroll
     for (int half = 0; half < C::kHalves; ++half) {
       const uint32_t off = half * C::kHalfBytes + sub * R * 128;
-      tma_load_2d(stage + off, tk, half * 64, rows[sub], bar);
-      tma_load_2d(stage + C::kTensorBytes + off, tv, half * 64, rows[sub], bar);
+      tma_load_2d(stage + off, tk, half * 64, row, bar);
+      tma_load_2d(stage + C::kTensorBytes + off, tv, half * 64, row, bar);
     }
   }
 }
@@ -215,11 +235,29 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int n_mine = n_item > warp ? (n_item - warp + kWarps - 1) / kWarps : 0;
     const int32_t* bt = a.block_tables + (int64_t)s * a.max_blocks_per_seq;
 
-    if (lane == 0) {
+    // The warp's lanes look up the block-table entries of its tiles of this
+    // item together (32 tiles at a time); lane 0 issues the copies.
+    TileRows mine = {{-1, -1}, 0u};
+    int chunk0 = 0;
+    if (lane < n_mine) mine = tile_rows<D>(a, bt, kvh, t_begin + warp + lane * kWarps, L);
+    auto issue = [&](int k, uint32_t st) {
+      if (k - chunk0 >= 32) {  // next 32 tiles of this warp (warp-uniform)
+        chunk0 += 32;
+        mine = {{-1, -1}, 0u};
+        if (chunk0 + lane < n_mine)
+          mine = tile_rows<D>(a, bt, kvh, t_begin + warp + (chunk0 + lane) * kWarps, L);
+      }
+      const int src = k - chunk0;
+      const int32_t r0 = __shfl_sync(0xffffffffu, mine.row[0], src);
+      const int32_t r1 = __shfl_sync(0xffffffffu, mine.row[1], src);
+      const uint32_t by = __shfl_sync(0xffffffffu, mine.bytes, src);
+      if (lane == 0)
+        issue_tile_rows<D>(&tmap_k, &tmap_v, a.block_size, r0, r1, by,
+                           ring + st * C::kStageBytes, smem_u32(&bars[warp][st]));
+    };
+    {
       const int npro = n_mine < C::kStages ? n_mine : C::kStages;
-      for (int k = 0; k < npro; ++k)
-        issue_tile<D>(&tmap_k, &tmap_v, a, bt, kvh, t_begin + warp + k * kWarps, L,
-                      ring + k * C::kStageBytes, smem_u32(&bars[warp][k]));
+      for (int k = 0; k < npro; ++k) issue(k, k);
     }
 
     // Q fragments (A operand rows g < G; rows g+8 are always zero).
@@ -344,10 +382,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       if (valid < kTileTokens) fence_proxy_async_smem();  // zeroing stores before TMA reuse
       __syncwarp();
-      if (lane == 0 && k + C::kStages < n_mine) {
-        issue_tile<D>(&tmap_k, &tmap_v, a, bt, kvh, t_begin + warp + (k + C::kStages) * kWarps, L,
-                      stage, bar);
-      }
+      if (k + C::kStages < n_mine) issue(k + C::kStages, st);
     }
 
     // Merge the 4 warps' states through shared memory (the rings are drained).
