@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
   __shared__ int32_t s_base, s_chunk;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = a.partition_tiles * kTileTokens;
+  grid_dep_launch();  // the decode kernel may start its set-up now
   if (tid == 0) s_base = 0;
   __syncthreads();
   for (int pass = 0; pass < 2; ++pass) {
@@ -210,6 +211,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int st = 0; st < C::kStages; ++st) mbar_init(smem_u32(&bars[warp][st]), 1);
     fence_barrier_init();
   }
+  grid_dep_launch();  // the combine kernel may start its set-up
+  grid_dep_wait();    // the plan (and, before it, the appended tokens) are complete
   if (tid == 0) {
     prefetch_tensormap(&tmap_k);
     prefetch_tensormap(&tmap_v);
@@ -436,6 +439,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a)
   constexpr int E = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t sh = (int64_t)blockIdx.x * 4 + warp;
+  grid_dep_wait();  // every partial state has been written
   if (sh >= (int64_t)a.S * a.Hq) return;
   const int s = (int)(sh / a.Hq);
   const int L = __ldg(a.context_lens + s);
@@ -517,15 +521,29 @@ int launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "decode kernel attributes");
   if (blocks_per_sm < 1) return fail(PKV_ECUDA, "decode kernel does not fit on an SM");
+  // plan -> decode -> combine, each dependent launch overlapping its set-up
+  // with the end of its predecessor (programmatic stream serialisation)
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
   decode_plan_kernel<<<1, 1024, 0, stream>>>(a);
   if (int rc = check_launch("decode plan")) return rc;
-  const int grid = dev.sm_count * blocks_per_sm;
-  paged_decode_kernel<D, G><<<grid, kThreads, C::kSmemBytes, stream>>>(tk, tv, a);
-  if (int rc = check_launch("decode")) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(dev.sm_count * blocks_per_sm));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G>, tk, tv, a);
+  if (err != cudaSuccess) return cuda_fail(err, "decode launch");
   if (a.max_partitions > 1) {
     const int64_t pairs = (int64_t)a.S * a.Hq;
-    decode_combine_kernel<D><<<(unsigned)((pairs + 3) / 4), 128, 0, stream>>>(a);
-    if (int rc = check_launch("decode combine")) return rc;
+    cfg.gridDim = dim3((unsigned)((pairs + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    err = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, a);
+    if (err != cudaSuccess) return cuda_fail(err, "decode combine launch");
   }
   return PKV_OK;
 }

@@ -94,6 +94,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   return true;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before its predecessor ends; `grid_dep_wait`
+// blocks until the predecessor has completed and its writes are visible, and
+// `grid_dep_launch` lets the successor start launching. Both are no-ops for
+// a normally launched kernel.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
