@@ -201,3 +201,11 @@ def test_empty_batches_are_no_ops():
     assert _call("pkv_block_copy", None, None, None, 0, 4, 8, 128, 16, None, None) == 0
     assert _call("pkv_paged_attention_decode", None, None, None, None, None, 4, None, 64, 0, 8, 2,
                  128, 16, 8, 0.1, 0, None, 0, None, None) == 0
+
+
+def test_pool_beyond_int32_rows_is_rejected():
+    # num_blocks * Hkv * block_size rows must fit the int32 TMA coordinates
+    big = (1 << 31) // (8 * 16)
+    assert _call("pkv_paged_attention_decode", None, None, None, None, None, 8, None, 64, 2, 32,
+                 8, 128, 16, big, 0.1, 0, None, 0, None, None) == PKV_EINVAL
+    assert "2^31" in pkv.pkv_last_error()

@@ -166,3 +166,13 @@ def test_rejects_small_workspace():
         pkv.pkv_paged_attention_decode(d.out, d.q, d.k_cache, d.v_cache, d.block_tables,
                                        d.context_lens, d.max_context_len, w.scale,
                                        d.workspace[:256], partition_size=16)
+
+
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_maximum_context_length(B):
+    # the longest context the workloads produce (the 8192-token clip), next to
+    # a one-token sequence and one just past a partition boundary, with the
+    # largest GQA group
+    w = make_decode_workload(f"max_len_B{B}", (8192, 1, 4097), Hq=16, Hkv=2, D=128,
+                             block_size=B, seed=1300 + B)
+    check_against_oracle(w)

@@ -130,3 +130,10 @@ def test_forced_timeout_reports_and_recovers():
         pkv.pkv_debug_set_wait(False)
     pkv.pkv_status_reset(d.status)
     check_prefill(w, [300, 140], seed=9)
+
+
+def test_long_prefix_chunks():
+    # chunks after a long cached prefix: up to 128 key tiles per query tile
+    w = make_decode_workload("prefill_long", (8192, 4096, 2000), Hq=16, Hkv=2, D=128,
+                             block_size=16, seed=3200)
+    check_prefill(w, [512, 1, 700], seed=11)
