@@ -54,9 +54,12 @@ def parse_args():
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--workload", choices=["llama3_8b_gqa", "trace"], default="llama3_8b_gqa",
-                    help="trace: the 200-iteration continuous-batching workload (a separate "
-                         "line; the default is the headline decode step)")
+    ap.add_argument("--workload", choices=["llama3_8b_gqa", "trace", "swap"],
+                    default="llama3_8b_gqa",
+                    help="trace: the 200-iteration continuous-batching workload; swap: "
+                         "preemption by swapping, every block of the decode batch out to "
+                         "pinned host memory and back (separate lines; the default is the "
+                         "headline decode step)")
     ap.add_argument("--iterations", type=int, default=200)
     return ap.parse_args()
 
@@ -354,12 +357,113 @@ def run_trace(args):
     return 0
 
 
+def run_swap(args):
+    """Preemption by swapping: ``pkv_swap_blocks`` moves every block of the
+    Llama-3-8B GQA batch (block-table order) out to pinned host memory and back
+    into the same blocks. Reported against a copy-engine ``cudaMemcpyAsync`` of
+    the same bytes as one contiguous buffer, each direction."""
+    import torch
+    import paged_kv_cache_281_gb300 as pkv
+    from tests.gpu_harness import setup_decode
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    w = workload_for_rank(rank)
+    d = setup_decode(w, append_last=False)
+    tables = d.block_tables.cpu().numpy()
+    blocks = np.concatenate([t[:math.ceil(L / w.block_size)]
+                             for t, L in zip(tables, w.context_lens)]).astype(np.int32)
+    n = len(blocks)
+    shape = (n, w.Hkv, w.block_size, w.D)
+    kb = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    vb = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    bl = torch.from_numpy(blocks).cuda()
+    nbytes = 2 * kb.numel() * 2
+    stream = torch.cuda.current_stream()
+    before = d.k_cache[bl[:64].long()].clone()
+
+    def swap(out_events):
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(stream)
+        pkv.pkv_swap_blocks(d.k_cache, d.v_cache, bl, kb, vb, True, status=d.status,
+                            stream=stream)
+        b.record(stream)
+        pkv.pkv_swap_blocks(d.k_cache, d.v_cache, bl, kb, vb, False, status=d.status,
+                            stream=stream)
+        c.record(stream)
+        out_events.append((a, b, c))
+
+    warm = []
+    for _ in range(max(3, args.warmup)):
+        swap(warm)
+    torch.cuda.synchronize()
+    pkv.pkv_check_status(d.status)
+    steps = max(5, min(args.steps, 50))
+    evs = []
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        for _ in range(steps):
+            swap(evs)
+        torch.cuda.synchronize()
+    pkv.pkv_check_status(d.status)
+    assert torch.equal(d.k_cache[bl[:64].long()], before), "swap round trip changed the cache"
+    out_ms = sum(a.elapsed_time(b) for a, b, _ in evs) / steps
+    in_ms = sum(b.elapsed_time(c) for _, b, c in evs) / steps
+
+    # copy engine, one contiguous buffer of the same size each way
+    dev_buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    host_buf = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    ce = []
+    for i in range(3 + steps):
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(stream)
+        host_buf.copy_(dev_buf, non_blocking=True)
+        b.record(stream)
+        dev_buf.copy_(host_buf, non_blocking=True)
+        c.record(stream)
+        if i >= 3:
+            ce.append((a, b, c))
+    torch.cuda.synchronize()
+    ce_out = sum(a.elapsed_time(b) for a, b, _ in ce) / steps
+    ce_in = sum(b.elapsed_time(c) for _, b, c in ce) / steps
+    gbs = lambda ms: nbytes / (ms * 1e-3) / 1e9
+    ms_per_step = out_ms + in_ms
+    line = {
+        "metric": "preemption swap: KV bytes moved per second (swap-out + swap-in)",
+        "value": world * 2 * nbytes / (ms_per_step * 1e-3) / 1e9, "unit": "GB/s",
+        "n_gpus": world, "steps": steps, "warmup": max(3, args.warmup),
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "swap every block of the Llama-3-8B GQA decode batch (256 seqs, "
+                               "8 KV heads, D=128, B=16) to pinned host memory and back",
+                   "blocks": n, "bytes_each_way": nbytes,
+                   "l2": "%.2f GB each way (> 129 MB L2)" % (nbytes / 1e9)},
+        "swap_out_gbs": gbs(out_ms), "swap_in_gbs": gbs(in_ms),
+        "roofline": {"bound": "host link", "kernel": "swap_blocks_kernel",
+                     "achieved": 2 * gbs(out_ms + in_ms), "unit": "GB/s",
+                     "peak": 2 * gbs(ce_out + ce_in),
+                     "peak_kind": "measured here: copy-engine cudaMemcpyAsync of one contiguous "
+                                  "buffer of the same size, out and back",
+                     "frac": (ce_out + ce_in) / (out_ms + in_ms), "traffic": None},
+        "copy_engine_gbs": {"d2h": gbs(ce_out), "h2d": gbs(ce_in)},
+        "gpu_launches": 2 * steps,
+        "clocks": clocks.summary(),
+        "cpu_baseline": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == "trace":
         return run_trace(args)
+    if args.workload == "swap":
+        return run_swap(args)
     import torch
     import paged_kv_cache_281_gb300 as pkv
     from tests.gpu_harness import decode_step, setup_decode, to_dev_bf16

@@ -107,6 +107,21 @@ int pkv_num_free_blocks(pkv_alloc* a, int32_t* out);
 int pkv_build_block_tables(pkv_alloc* a, const int64_t* seqs, int32_t n, int32_t* tables_out,
                            int32_t max_blocks_per_seq, int32_t* lens_out);
 
+/* Preemption ("Batching, Scheduling, and Paging", section PagedAttention: if
+ * HBM runs out a request is evicted, swapped to CPU memory or discarded and
+ * recomputed later).
+ *   swap_out: the sequence gives its blocks back (table order, written to
+ *     blocks_out, *n of them) and keeps its length; each block loses one
+ *     reference and may be handed out again at once, so copy the blocks out
+ *     (pkv_swap_blocks, on the stream that will later write into them) before
+ *     the next kv_append. A swapped-out sequence cannot be appended to,
+ *     forked or put in a block table until it is swapped in.
+ *   swap_in: fresh blocks for all of its tokens (first in, first out), all or
+ *     nothing (PKV_ENOMEM); copy the saved contents into them before use.
+ *   Recompute: pkv_seq_free, then create the request again and re-append. */
+int pkv_seq_swap_out(pkv_alloc* a, int64_t seq, int32_t* blocks_out, int32_t cap, int32_t* n);
+int pkv_seq_swap_in(pkv_alloc* a, int64_t seq, int32_t* blocks_out, int32_t cap, int32_t* n);
+
 /* ------------------------------------------------------------------------
  * Device status block (4 int32 in device memory, owned by the caller):
  *   [0] first error code (0, PKV_ETIMEOUT or PKV_EDEVICE), [1] detail (the
@@ -148,6 +163,22 @@ int pkv_kv_append(const void* k_new, const void* v_new, const int32_t* slot_mapp
 int pkv_block_copy(void* k_cache, void* v_cache, const int32_t* pairs, int32_t n,
                    int32_t num_blocks, int32_t Hkv, int32_t D, int32_t block_size,
                    int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * swap_blocks — copies whole blocks (keys and values) between the pools and
+ * a contiguous buffer, for swapping a preempted request out and back in
+ * ("Batching, Scheduling, and Paging", section PagedAttention).
+ *   blocks       : int32 [n] (device), block ids in the pool; an id outside
+ *                  [0, num_blocks) skips that slot (PKV_EDEVICE).
+ *   k_buf, v_buf : bf16 [n][Hkv][block_size][D] each: device memory or
+ *                  pinned host memory (the GPU reads or writes it over the
+ *                  CPU-GPU link); pageable host memory is refused (PKV_EINVAL).
+ *   to_buffer    : 1 copies pool -> buffer (swap-out), 0 buffer -> pool.
+ * Bit-exact. The listed blocks must be distinct.
+ * ---------------------------------------------------------------------- */
+int pkv_swap_blocks(void* k_cache, void* v_cache, const int32_t* blocks, int32_t n,
+                    int32_t num_blocks, int32_t Hkv, int32_t D, int32_t block_size, void* k_buf,
+                    void* v_buf, int32_t to_buffer, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
  * paged_attention_decode — one query token per sequence ("Deep Dive:

@@ -39,3 +39,20 @@ def gather(cache: np.ndarray, block_table, length: int, block_size: int) -> np.n
     for j in range(length):
         out[j] = cache[int(block_table[j // block_size]), :, j % block_size, :]
     return out
+
+
+def swap_blocks(k_cache: np.ndarray, v_cache: np.ndarray, blocks, k_buf: np.ndarray,
+                v_buf: np.ndarray, direction: int) -> None:
+    """Whole-block copies between the pools and a contiguous buffer.
+
+    ``direction`` 0: buffer slot ``i`` receives block ``blocks[i]`` (swap-out);
+    1: block ``blocks[i]`` receives buffer slot ``i`` (swap-in).
+    """
+    for i, b in enumerate(blocks):
+        b = int(b)
+        if direction == 0:
+            k_buf[i] = k_cache[b]
+            v_buf[i] = v_cache[b]
+        else:
+            k_cache[b] = k_buf[i]
+            v_cache[b] = v_buf[i]

@@ -21,7 +21,12 @@ Readings where the page is silent:
   blocks are never written and never copied;
 * a slot is ``physical_block * block_size + offset``;
 * an append that cannot get all the blocks it needs fails as a whole and
-  changes nothing.
+  changes nothing;
+* eviction when memory runs out (same page, section PagedAttention: swap the
+  request to CPU memory or discard and recompute it): swapping out hands the
+  sequence's blocks back in table order (each loses one reference) and keeps
+  its length; swapping in takes fresh blocks for all its tokens, first in
+  first out, all or nothing. Recomputing is freeing and starting again.
 
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 """
@@ -52,7 +57,7 @@ class BlockAllocator:
     def create(self) -> int:
         sid = self._next_id
         self._next_id += 1
-        self.seqs[sid] = {"blocks": [], "len": 0}
+        self.seqs[sid] = {"blocks": [], "len": 0, "swapped": False}
         return sid
 
     def fork(self, parent: int) -> int:
@@ -60,7 +65,8 @@ class BlockAllocator:
         src = self.seqs[parent]
         sid = self._next_id
         self._next_id += 1
-        self.seqs[sid] = {"blocks": list(src["blocks"]), "len": src["len"]}
+        assert not src["swapped"], "cannot fork a swapped-out sequence"
+        self.seqs[sid] = {"blocks": list(src["blocks"]), "len": src["len"], "swapped": False}
         for b in src["blocks"]:
             self.refcount[b] += 1
         return sid
@@ -87,8 +93,33 @@ class BlockAllocator:
             need += 1
         return need
 
+    def swap_out(self, sid: int) -> list[int]:
+        """Give the sequence's blocks back (table order); it keeps its length."""
+        seq = self.seqs[sid]
+        assert not seq["swapped"]
+        blocks = list(seq["blocks"])
+        for b in blocks:
+            self.refcount[b] -= 1
+            if self.refcount[b] == 0:
+                self.free.append(b)
+        seq["blocks"] = []
+        seq["swapped"] = True
+        return blocks
+
+    def swap_in(self, sid: int) -> list[int]:
+        """Fresh blocks for all of a swapped-out sequence's tokens."""
+        seq = self.seqs[sid]
+        assert seq["swapped"]
+        need = -(-seq["len"] // self.block_size)
+        if need > len(self.free):
+            raise OutOfBlocks(f"sequence {sid} needs {need} blocks, {len(self.free)} free")
+        seq["blocks"] = [self._take() for _ in range(need)]
+        seq["swapped"] = False
+        return list(seq["blocks"])
+
     def append_slots(self, sid: int, n: int):
         """Reserve slots for ``n`` new tokens; return ``(slots, cow_pairs)``."""
+        assert not self.seqs[sid]["swapped"], "append to a swapped-out sequence"
         if self.blocks_needed(sid, n) > len(self.free):
             raise OutOfBlocks(f"sequence {sid} needs {self.blocks_needed(sid, n)} blocks, "
                               f"{len(self.free)} free")
@@ -125,6 +156,9 @@ class BlockAllocator:
         """Counts equal table references; free + referenced = all blocks."""
         refs = [0] * self.num_blocks
         for seq in self.seqs.values():
+            if seq["swapped"]:
+                assert not seq["blocks"]
+                continue
             assert len(seq["blocks"]) == -(-seq["len"] // self.block_size)
             for b in seq["blocks"]:
                 refs[b] += 1

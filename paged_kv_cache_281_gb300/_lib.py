@@ -36,6 +36,9 @@ SIGNATURES = {
     "pkv_block_refcount": (ctypes.c_int, [vp, i32, P(i32)]),
     "pkv_num_free_blocks": (ctypes.c_int, [vp, P(i32)]),
     "pkv_build_block_tables": (ctypes.c_int, [vp, P(i64), i32, P(i32), i32, P(i32)]),
+    "pkv_seq_swap_out": (ctypes.c_int, [vp, i64, P(i32), i32, P(i32)]),
+    "pkv_seq_swap_in": (ctypes.c_int, [vp, i64, P(i32), i32, P(i32)]),
+    "pkv_swap_blocks": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, vp]),
     "pkv_status_reset": (ctypes.c_int, [vp, vp]),
     "pkv_check_status": (ctypes.c_int, [vp, vp]),
     "pkv_debug_set_wait": (ctypes.c_int, [i32, u64]),

@@ -23,7 +23,7 @@ from ._lib import PagedKVError, check, lib
 
 __all__ = [
     "PagedKVError", "pkv_version", "pkv_last_error", "BlockAllocator",
-    "pkv_kv_append", "pkv_block_copy", "pkv_decode_workspace_bytes",
+    "pkv_kv_append", "pkv_block_copy", "pkv_swap_blocks", "pkv_decode_workspace_bytes",
     "pkv_paged_attention_decode", "pkv_paged_attention_decode_noalloc",
     "NOALLOC_SCRATCH_BYTES", "pkv_prefill_workspace_bytes",
     "pkv_paged_attention_prefill", "pkv_status_reset", "pkv_check_status",
@@ -131,6 +131,22 @@ class BlockAllocator:
                                         n.value, ctypes.byref(n)))
         return buf[:n.value].tolist()
 
+    def _blocks_call(self, fn, seq: int) -> list[int]:
+        cap = max(1, self.num_blocks)
+        buf = np.empty(cap, dtype=np.int32)
+        n = ctypes.c_int32()
+        check(fn(self._h, int(seq), buf.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), cap,
+                 ctypes.byref(n)))
+        return buf[:n.value].tolist()
+
+    def seq_swap_out(self, seq: int) -> list[int]:
+        """Give the sequence's blocks back (table order); it keeps its length."""
+        return self._blocks_call(lib().pkv_seq_swap_out, seq)
+
+    def seq_swap_in(self, seq: int) -> list[int]:
+        """Fresh blocks for a swapped-out sequence (PagedKVError PKV_ENOMEM if short)."""
+        return self._blocks_call(lib().pkv_seq_swap_in, seq)
+
     def block_refcount(self, block: int) -> int:
         out = ctypes.c_int32()
         check(lib().pkv_block_refcount(self._h, int(block), ctypes.byref(out)))
@@ -199,6 +215,21 @@ def pkv_block_copy(k_cache, v_cache, pairs, status=None, stream=None) -> None:
         raise ValueError("pairs must be [n, 2]")
     check(lib().pkv_block_copy(k_cache.data_ptr(), v_cache.data_ptr(), pairs.data_ptr(),
                                int(pairs.shape[0]), N, Hkv, D, B, _ptr(status), _stream(stream)))
+
+
+def pkv_swap_blocks(k_cache, v_cache, blocks, k_buf, v_buf, to_buffer: bool, status=None,
+                    stream=None) -> None:
+    """Copy whole blocks between the pools and ``k_buf``/``v_buf`` (device or
+    pinned host tensors shaped ``[n, Hkv, B, D]``)."""
+    N, Hkv, B, D = _pool_shape(k_cache, v_cache)
+    _dev(blocks, "blocks", torch.int32, 1)
+    n = int(blocks.shape[0])
+    for name, t in (("k_buf", k_buf), ("v_buf", v_buf)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != (n, Hkv, B, D):
+            raise ValueError(f"{name} must be a contiguous bf16 [{n}, {Hkv}, {B}, {D}] tensor")
+    check(lib().pkv_swap_blocks(k_cache.data_ptr(), v_cache.data_ptr(), blocks.data_ptr(), n, N,
+                                Hkv, D, B, k_buf.data_ptr(), v_buf.data_ptr(),
+                                1 if to_buffer else 0, _ptr(status), _stream(stream)))
 
 
 def pkv_decode_workspace_bytes(S: int, Hq: int, D: int, max_context_len: int,

@@ -30,6 +30,7 @@ struct pkv_alloc {
   struct Seq {
     std::vector<int32_t> blocks;
     int32_t len = 0;
+    bool swapped = false;  // blocks handed back; contents kept by the caller
   };
   std::unordered_map<int64_t, Seq> seqs;
   int64_t next_id = 0;
@@ -105,6 +106,7 @@ extern "C" int pkv_seq_fork(pkv_alloc* a, int64_t parent, int64_t* child) {
   PKV_REQUIRE(a && child, "pkv_seq_fork: NULL argument");
   pkv_alloc::Seq* p = a->find(parent);
   PKV_REQUIRE(p, "pkv_seq_fork: unknown sequence %lld", (long long)parent);
+  PKV_REQUIRE(!p->swapped, "pkv_seq_fork: sequence %lld is swapped out", (long long)parent);
   pkv_alloc::Seq copy = *p;
   for (int32_t b : copy.blocks) ++a->refcount[b];
   int64_t id = a->next_id++;
@@ -120,6 +122,7 @@ extern "C" int pkv_seq_append_slots(pkv_alloc* a, int64_t seq, int32_t n, int32_
   PKV_REQUIRE(n == 0 || slots_out, "pkv_seq_append_slots: slots_out is NULL");
   pkv_alloc::Seq* s = a->find(seq);
   PKV_REQUIRE(s, "pkv_seq_append_slots: unknown sequence %lld", (long long)seq);
+  PKV_REQUIRE(!s->swapped, "pkv_seq_append_slots: sequence %lld is swapped out", (long long)seq);
   *n_cow = 0;
   if (n == 0) return ok();
   const int32_t B = a->block_size;
@@ -206,6 +209,8 @@ extern "C" int pkv_build_block_tables(pkv_alloc* a, const int64_t* seqs, int32_t
   for (int32_t i = 0; i < n; ++i) {
     pkv_alloc::Seq* s = a->find(seqs[i]);
     PKV_REQUIRE(s, "pkv_build_block_tables: unknown sequence %lld", (long long)seqs[i]);
+    PKV_REQUIRE(!s->swapped, "pkv_build_block_tables: sequence %lld is swapped out",
+                (long long)seqs[i]);
     PKV_REQUIRE((int32_t)s->blocks.size() <= max_blocks_per_seq,
                 "pkv_build_block_tables: sequence %lld has %zu blocks > %d", (long long)seqs[i],
                 s->blocks.size(), max_blocks_per_seq);
@@ -218,5 +223,50 @@ extern "C" int pkv_build_block_tables(pkv_alloc* a, const int64_t* seqs, int32_t
     for (int32_t j = m; j < max_blocks_per_seq; ++j) row[j] = 0;
     lens_out[i] = s->len;
   }
+  return ok();
+}
+
+// Preemption ("Batching, Scheduling, and Paging", section PagedAttention: when
+// HBM runs out a request is evicted, swapped to CPU memory or recomputed).
+extern "C" int pkv_seq_swap_out(pkv_alloc* a, int64_t seq, int32_t* blocks_out, int32_t cap,
+                                int32_t* n) {
+  PKV_REQUIRE(a && n, "pkv_seq_swap_out: NULL argument");
+  pkv_alloc::Seq* s = a->find(seq);
+  PKV_REQUIRE(s, "pkv_seq_swap_out: unknown sequence %lld", (long long)seq);
+  PKV_REQUIRE(!s->swapped, "pkv_seq_swap_out: sequence %lld is already swapped out",
+              (long long)seq);
+  const int32_t m = (int32_t)s->blocks.size();
+  PKV_REQUIRE(cap >= m && (m == 0 || blocks_out),
+              "pkv_seq_swap_out: blocks_out holds %d entries, %d needed", cap, m);
+  for (int32_t i = 0; i < m; ++i) {
+    const int32_t b = s->blocks[i];
+    blocks_out[i] = b;
+    if (--a->refcount[b] == 0) a->push_free(b);
+  }
+  s->blocks.clear();
+  s->swapped = true;
+  *n = m;
+  return ok();
+}
+
+extern "C" int pkv_seq_swap_in(pkv_alloc* a, int64_t seq, int32_t* blocks_out, int32_t cap,
+                               int32_t* n) {
+  PKV_REQUIRE(a && n, "pkv_seq_swap_in: NULL argument");
+  pkv_alloc::Seq* s = a->find(seq);
+  PKV_REQUIRE(s, "pkv_seq_swap_in: unknown sequence %lld", (long long)seq);
+  PKV_REQUIRE(s->swapped, "pkv_seq_swap_in: sequence %lld is not swapped out", (long long)seq);
+  const int32_t m = (s->len + a->block_size - 1) / a->block_size;
+  PKV_REQUIRE(cap >= m && (m == 0 || blocks_out),
+              "pkv_seq_swap_in: blocks_out holds %d entries, %d needed", cap, m);
+  if (m > a->count)
+    return fail(PKV_ENOMEM, "pkv_seq_swap_in: sequence %lld needs %d blocks, %d free",
+                (long long)seq, m, a->count);
+  for (int32_t i = 0; i < m; ++i) {
+    const int32_t b = a->pop_free();
+    s->blocks.push_back(b);
+    blocks_out[i] = b;
+  }
+  s->swapped = false;
+  *n = m;
   return ok();
 }

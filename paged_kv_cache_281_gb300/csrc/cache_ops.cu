@@ -84,6 +84,52 @@ __global__ void __launch_bounds__(256) block_copy_kernel(const CopyArgs a) {
     d[i] = s[i];
 }
 
+struct SwapArgs {
+  uint4* k_cache;
+  uint4* v_cache;
+  const int32_t* blocks;
+  uint4* k_buf;
+  uint4* v_buf;
+  int32_t n;
+  int32_t num_blocks;
+  int64_t vec_per_block;
+  int32_t to_buffer;  // 1: pool -> buffer (swap-out), 0: buffer -> pool (swap-in)
+  int32_t* status;
+};
+
+// blockIdx.y picks the listed block, blockIdx.z the pool (0 keys, 1 values);
+// blockIdx.x strides over the block's vectors. The buffer may be pinned host
+// memory reached over the CPU-GPU link.
+__global__ void __launch_bounds__(256) swap_blocks_kernel(const SwapArgs a) {
+  const int32_t i = blockIdx.y;
+  const int32_t blk = __ldg(a.blocks + i);
+  if (blk < 0 || blk >= a.num_blocks) {
+    if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+      record_status(a.status, PKV_EDEVICE, blk, kKernelBlockCopy);
+    return;
+  }
+  uint4* pool = (blockIdx.z == 0 ? a.k_cache : a.v_cache) + (int64_t)blk * a.vec_per_block;
+  uint4* buf = (blockIdx.z == 0 ? a.k_buf : a.v_buf) + (int64_t)i * a.vec_per_block;
+  const uint4* src = a.to_buffer ? pool : buf;
+  uint4* dst = a.to_buffer ? buf : pool;
+  for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < a.vec_per_block;
+       j += (int64_t)gridDim.x * blockDim.x)
+    dst[j] = src[j];
+}
+
+// Device-usable address of a buffer, or an error for memory the GPU cannot
+// reach (pageable host memory).
+int device_address(void* p, void** out, const char* who) {
+  cudaPointerAttributes attr;
+  cudaError_t err = cudaPointerGetAttributes(&attr, p);
+  if (err != cudaSuccess) return cuda_fail(err, who);
+  if (attr.type == cudaMemoryTypeUnregistered || attr.devicePointer == nullptr)
+    return fail(PKV_EINVAL,
+                "%s: buffer %p is pageable host memory; use device or pinned host memory", who, p);
+  *out = attr.devicePointer;
+  return PKV_OK;
+}
+
 int check_shape(int32_t Hkv, int32_t D, int32_t block_size, const char* who) {
   PKV_REQUIRE(Hkv > 0, "%s: Hkv must be > 0 (got %d)", who, Hkv);
   PKV_REQUIRE(D == 64 || D == 128, "%s: D must be 64 or 128 (got %d)", who, D);
@@ -157,5 +203,42 @@ extern "C" int pkv_block_copy(void* k_cache, void* v_cache, const int32_t* pairs
   dim3 grid((unsigned)per_block, (unsigned)n, 2);
   block_copy_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
   if (int rc = check_launch("pkv_block_copy")) return rc;
+  return ok();
+}
+
+extern "C" int pkv_swap_blocks(void* k_cache, void* v_cache, const int32_t* blocks, int32_t n,
+                               int32_t num_blocks, int32_t Hkv, int32_t D, int32_t block_size,
+                               void* k_buf, void* v_buf, int32_t to_buffer, int32_t* dev_status,
+                               void* stream) {
+  if (int rc = check_shape(Hkv, D, block_size, "pkv_swap_blocks")) return rc;
+  PKV_REQUIRE(n >= 0 && n <= 65535, "pkv_swap_blocks: n must be in [0, 65535] (got %d)", n);
+  PKV_REQUIRE(num_blocks > 0, "pkv_swap_blocks: num_blocks must be > 0");
+  PKV_REQUIRE(to_buffer == 0 || to_buffer == 1, "pkv_swap_blocks: to_buffer must be 0 or 1");
+  if (n == 0) return ok();
+  PKV_REQUIRE(k_cache && v_cache && blocks && k_buf && v_buf, "pkv_swap_blocks: NULL pointer");
+  PKV_REQUIRE(aligned16(k_cache) && aligned16(v_cache) && aligned16(k_buf) && aligned16(v_buf),
+              "pkv_swap_blocks: arrays must be 16-byte aligned");
+  const DeviceInfo* dev = nullptr;
+  if (int rc = current_device_info(&dev)) return rc;
+  void* kd = nullptr;
+  void* vd = nullptr;
+  if (int rc = device_address(k_buf, &kd, "pkv_swap_blocks")) return rc;
+  if (int rc = device_address(v_buf, &vd, "pkv_swap_blocks")) return rc;
+  SwapArgs a;
+  a.k_cache = static_cast<uint4*>(k_cache);
+  a.v_cache = static_cast<uint4*>(v_cache);
+  a.blocks = blocks;
+  a.k_buf = static_cast<uint4*>(kd);
+  a.v_buf = static_cast<uint4*>(vd);
+  a.n = n;
+  a.num_blocks = num_blocks;
+  a.vec_per_block = (int64_t)Hkv * block_size * D / 8;
+  a.to_buffer = to_buffer;
+  a.status = dev_status;
+  int64_t per_block = (a.vec_per_block + 255) / 256;
+  if (per_block > 16) per_block = 16;
+  dim3 grid((unsigned)per_block, (unsigned)n, 2);
+  swap_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  if (int rc = check_launch("pkv_swap_blocks")) return rc;
   return ok();
 }

@@ -1,0 +1,390 @@
+"""Iteration-level scheduling with a pool too small for the worst case.
+
+"Batching, Scheduling, and Paging" (section PagedAttention): when HBM runs
+out, a request is evicted — swapped to CPU memory, or discarded and
+recomputed later. This scheduler runs a continuous-batching trace against an
+undersized pool and evicts the most recently admitted running request when an
+append cannot get its blocks, in one of two modes:
+
+* ``swap``: the victim's blocks are copied out and handed back; it resumes
+  (first in, first out, before new admissions) when its blocks fit again;
+* ``recompute``: the victim's blocks are freed and it re-enters the queue; on
+  resumption it re-prefills every token it had cached, with the same values.
+
+The scheduler only decides; an allocator adapter (the library's allocator or
+the oracle's model) answers the block requests, and the two executors (GPU,
+oracle) replay the resulting events. Test infrastructure.
+"""
+
+from __future__ import annotations
+
+from collections import deque
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from workloads import TraceConfig, generator, normal_bf16_from
+
+
+class OutOfBlocks(Exception):
+    pass
+
+
+class LibraryAllocator:
+    """Adapter over paged_kv_cache_281_gb300.BlockAllocator."""
+
+    def __init__(self, num_blocks, block_size):
+        import paged_kv_cache_281_gb300 as pkv
+        from paged_kv_cache_281_gb300._lib import PKV_ENOMEM
+        self.pkv, self.enomem = pkv, PKV_ENOMEM
+        self.a = pkv.BlockAllocator(num_blocks, block_size)
+
+    def _guard(self, fn, *args):
+        try:
+            return fn(*args)
+        except self.pkv.PagedKVError as e:
+            if e.code == self.enomem:
+                raise OutOfBlocks(str(e)) from None
+            raise
+
+    def create(self):
+        return self.a.seq_create()
+
+    def append(self, sid, n):
+        slots, pair = self._guard(self.a.seq_append_slots, sid, n)
+        assert pair is None
+        return [int(x) for x in slots]
+
+    def free(self, sid):
+        self.a.seq_free(sid)
+
+    def swap_out(self, sid):
+        return self.a.seq_swap_out(sid)
+
+    def swap_in(self, sid):
+        return self._guard(self.a.seq_swap_in, sid)
+
+    def table(self, sid):
+        return self.a.seq_block_table(sid)
+
+    def num_free(self):
+        return self.a.num_free_blocks()
+
+
+class OracleAllocator:
+    """Adapter over oracle.paging.BlockAllocator."""
+
+    def __init__(self, num_blocks, block_size):
+        from oracle import paging
+        self.paging = paging
+        self.a = paging.BlockAllocator(num_blocks, block_size)
+
+    def create(self):
+        return self.a.create()
+
+    def append(self, sid, n):
+        try:
+            slots, pairs = self.a.append_slots(sid, n)
+        except self.paging.OutOfBlocks as e:
+            raise OutOfBlocks(str(e)) from None
+        assert not pairs
+        return slots
+
+    def free(self, sid):
+        self.a.free_seq(sid)
+
+    def swap_out(self, sid):
+        return self.a.swap_out(sid)
+
+    def swap_in(self, sid):
+        try:
+            return self.a.swap_in(sid)
+        except self.paging.OutOfBlocks as e:
+            raise OutOfBlocks(str(e)) from None
+
+    def table(self, sid):
+        return self.a.block_table(sid)
+
+    def num_free(self):
+        return self.a.num_free()
+
+
+class TokenValues:
+    """Per-request q/k/v values drawn in position order and kept, so that a
+    recomputed request re-appends exactly the values it had."""
+
+    def __init__(self, cfg: TraceConfig):
+        self.cfg = cfg
+        self.W = (cfg.Hq + 2 * cfg.Hkv) * cfg.D
+        self.rows: dict[int, np.ndarray] = {}
+        self.gens: dict[int, np.random.Generator] = {}
+
+    def get(self, rid, start, n):
+        have = self.rows.get(rid, np.zeros((0, self.W), np.uint16))
+        if start + n > have.shape[0]:
+            g = self.gens.setdefault(rid, generator(self.cfg.seed, 1, rid))
+            more = normal_bf16_from(g, (start + n - have.shape[0], self.W))
+            have = np.concatenate([have, more])
+            self.rows[rid] = have
+        return have[start:start + n]
+
+
+@dataclass
+class Req:
+    rid: int
+    prompt: int
+    out: int
+    sid: int = -1
+    pos: int = 0              # tokens in the cache
+    prefill_to: int = 0       # tokens to (re-)prefill before decoding
+    generated: int = 0
+    state: str = "waiting"    # waiting | running | swapped
+
+
+@dataclass
+class Event:
+    """What one iteration did, in the order the host decided it."""
+
+    index: int
+    ops: list = field(default_factory=list)      # ("swap_in"|"swap_out", rid, blocks)
+    work: list = field(default_factory=list)     # (rid, sid, start, n, kind, slots)
+    tables: dict = field(default_factory=dict)   # rid -> block table after this step's appends
+    finished: list = field(default_factory=list)
+    preempted: int = 0
+
+
+class PreemptingScheduler:
+    def __init__(self, cfg: TraceConfig, num_blocks: int, mode: str, alloc):
+        assert mode in ("swap", "recompute")
+        self.cfg, self.mode, self.alloc = cfg, mode, alloc
+        self.num_blocks = num_blocks
+        self.g = generator(cfg.seed, 0)
+        self.waiting: deque = deque()
+        self.swapped: deque = deque()
+        self.running: list[Req] = []
+        self.next_rid = 0
+
+    def _evict(self, victim: Req, ev: Event):
+        self.running.remove(victim)
+        ev.preempted += 1
+        if self.mode == "swap":
+            blocks = self.alloc.swap_out(victim.sid)
+            ev.ops.append(("swap_out", victim.rid, blocks))
+            victim.state = "swapped"
+            self.swapped.append(victim)
+        else:
+            self.alloc.free(victim.sid)
+            victim.prefill_to = max(victim.prompt, victim.pos)
+            victim.pos = 0
+            victim.sid = -1
+            victim.state = "waiting"
+            self.waiting.appendleft(victim)
+
+    def step(self, it: int) -> Event:
+        cfg, B = self.cfg, self.cfg.block_size
+        ev = Event(index=it)
+        for _ in range(int(self.g.poisson(cfg.arrival_rate))):
+            prompt = int(self.g.integers(cfg.prompt_min, cfg.prompt_max, endpoint=True))
+            out = int(min(cfg.out_cap, self.g.geometric(1.0 / cfg.out_mean)))
+            self.waiting.append(Req(self.next_rid, prompt, out, prefill_to=prompt))
+            self.next_rid += 1
+        # resume swapped requests first, then admit queued ones
+        while self.swapped and len(self.running) < cfg.max_running:
+            r = self.swapped[0]
+            try:
+                blocks = self.alloc.swap_in(r.sid)
+            except OutOfBlocks:
+                break
+            self.swapped.popleft()
+            ev.ops.append(("swap_in", r.rid, blocks))
+            r.state = "running"
+            self.running.append(r)
+        while (self.waiting and not self.swapped and len(self.running) < cfg.max_running
+               and self.alloc.num_free() >= -(-min(cfg.chunk, self.waiting[0].prefill_to) // B)):
+            r = self.waiting.popleft()
+            r.sid = self.alloc.create()
+            r.state = "running"
+            self.running.append(r)
+        # one step of work per running request, evicting the newest on shortage
+        i = 0
+        while i < len(self.running):
+            r = self.running[i]
+            if r.pos < r.prefill_to:
+                n, kind = min(cfg.chunk, r.prefill_to - r.pos), "prefill"
+            else:
+                n, kind = 1, "decode"
+            while True:
+                try:
+                    slots = self.alloc.append(r.sid, n)
+                    break
+                except OutOfBlocks:
+                    victim = self.running[-1]
+                    self._evict(victim, ev)
+                    if victim is r:
+                        slots = None
+                        break
+            if slots is None:
+                continue  # r itself was evicted; the list shrank
+            ev.work.append((r.rid, r.sid, r.pos, n, kind, slots))
+            r.pos += n
+            if kind == "prefill":
+                if r.pos == r.prefill_to and r.generated == 0:
+                    r.generated = 1
+            else:
+                r.generated += 1
+            i += 1
+        ev.tables = {w[0]: self.alloc.table(w[1]) for w in ev.work}
+        for r in list(self.running):
+            if r.generated >= r.out:
+                self.alloc.free(r.sid)
+                self.running.remove(r)
+                ev.finished.append(r.rid)
+        return ev
+
+
+def small_trace_config(iterations=60) -> TraceConfig:
+    """A trace small enough to keep every request's values and check often."""
+    return TraceConfig(iterations=iterations, arrival_rate=4.0, prompt_min=16, prompt_max=200,
+                       chunk=128, out_mean=40.0, out_cap=160, max_running=48, Hq=16, Hkv=4, D=128,
+                       block_size=16, seed=0x281 + 50)
+
+
+def run_schedule(cfg, num_blocks, mode, alloc_factory):
+    """All events of the trace for one allocator."""
+    sched = PreemptingScheduler(cfg, num_blocks, mode, alloc_factory(num_blocks, cfg.block_size))
+    return [sched.step(it) for it in range(cfg.iterations)], sched
+
+
+def iteration_inputs(cfg, ev: Event, values: TokenValues):
+    """Per-token q/k/v of an iteration (prefill rows first, then decode rows),
+    the slots, and the prefill/decode metadata."""
+    pre = [w for w in ev.work if w[4] == "prefill"]
+    dec = [w for w in ev.work if w[4] == "decode"]
+    order = pre + dec
+    rows = [values.get(w[0], w[2], w[3]) for w in order]
+    W = values.W
+    vals = np.concatenate(rows) if rows else np.zeros((0, W), np.uint16)
+    T = vals.shape[0]
+    qd, kd = cfg.Hq * cfg.D, cfg.Hkv * cfg.D
+    q = np.ascontiguousarray(vals[:, :qd]).reshape(T, cfg.Hq, cfg.D)
+    k = np.ascontiguousarray(vals[:, qd:qd + kd]).reshape(T, cfg.Hkv, cfg.D)
+    v = np.ascontiguousarray(vals[:, qd + kd:]).reshape(T, cfg.Hkv, cfg.D)
+    slots = np.asarray([s for w in order for s in w[5]], dtype=np.int32)
+    width = max([len(ev.tables[w[0]]) for w in order] + [1])
+    meta = {}
+    for name, ws in (("prefill", pre), ("decode", dec)):
+        tables = np.zeros((len(ws), width), dtype=np.int32)
+        for i, w in enumerate(ws):
+            t = ev.tables[w[0]]
+            tables[i, :len(t)] = t
+        lens = np.asarray([w[2] + w[3] for w in ws], dtype=np.int32)
+        meta[name] = (tables, lens)
+    meta["cu"] = np.concatenate([[0], np.cumsum([w[3] for w in pre])]).astype(np.int32)
+    return pre, dec, q, k, v, slots, meta
+
+
+class GpuRunner:
+    """Replays scheduler events with the library on the GPU."""
+
+    def __init__(self, cfg, num_blocks, device="cuda"):
+        import torch
+        import paged_kv_cache_281_gb300 as pkv
+        from tests.gpu_harness import poisoned_pools
+        self.torch, self.pkv, self.cfg, self.dev = torch, pkv, cfg, device
+        self.k_cache, self.v_cache = poisoned_pools(num_blocks, cfg.Hkv, cfg.block_size, cfg.D,
+                                                    device)
+        self.status = pkv.new_status(device)
+        self.saved = {}
+        self.swap_bytes = 0
+        self.scale = 1.0 / np.sqrt(cfg.D)
+        self.ws = torch.empty(pkv.pkv_decode_workspace_bytes(
+            cfg.max_running, cfg.Hq, cfg.D, cfg.prompt_max + cfg.out_cap + cfg.chunk),
+            dtype=torch.uint8, device=device)
+        self.pws = torch.empty(pkv.pkv_prefill_workspace_bytes(cfg.max_running, cfg.max_running
+                                                               * cfg.chunk, cfg.Hq, cfg.D),
+                               dtype=torch.uint8, device=device)
+
+    def run(self, ev: Event, values: TokenValues):
+        torch, pkv, cfg, dev = self.torch, self.pkv, self.cfg, self.dev
+        from tests.gpu_harness import to_dev_bf16
+        shape = (cfg.Hkv, cfg.block_size, cfg.D)
+        for kind, rid, blocks in ev.ops:
+            bl = torch.tensor(blocks, dtype=torch.int32, device=dev)
+            if kind == "swap_out":
+                kb = torch.empty((len(blocks),) + shape, dtype=torch.bfloat16).pin_memory()
+                vb = torch.empty_like(kb).pin_memory()
+                pkv.pkv_swap_blocks(self.k_cache, self.v_cache, bl, kb, vb, True,
+                                    status=self.status)
+                self.saved[rid] = (kb, vb)
+            else:
+                kb, vb = self.saved.pop(rid)
+                pkv.pkv_swap_blocks(self.k_cache, self.v_cache, bl, kb, vb, False,
+                                    status=self.status)
+            self.swap_bytes += 2 * kb.numel() * 2
+        pre, dec, q, k, v, slots, meta = iteration_inputs(cfg, ev, values)
+        pre_out = dec_out = None
+        if len(slots):
+            pkv.pkv_kv_append(to_dev_bf16(k, dev), to_dev_bf16(v, dev),
+                              torch.from_numpy(slots).to(dev), self.k_cache, self.v_cache,
+                              status=self.status)
+        qd = to_dev_bf16(q, dev)
+        n_pre = int(meta["cu"][-1])
+        if pre:
+            tables, lens = meta["prefill"]
+            pre_out = torch.empty(n_pre, cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
+            pkv.pkv_paged_attention_prefill(
+                pre_out, qd[:n_pre], torch.from_numpy(meta["cu"]).to(dev),
+                torch.from_numpy(lens).to(dev), self.k_cache, self.v_cache,
+                torch.from_numpy(tables).to(dev), int(np.diff(meta["cu"]).max()),
+                int(lens.max()), self.scale, self.pws, status=self.status)
+        if dec:
+            tables, lens = meta["decode"]
+            dec_out = torch.empty(len(dec), cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
+            pkv.pkv_paged_attention_decode(
+                dec_out, qd[n_pre:], self.k_cache, self.v_cache, torch.from_numpy(tables).to(dev),
+                torch.from_numpy(lens).to(dev), int(lens.max()), self.scale, self.ws,
+                status=self.status)
+        torch.cuda.synchronize()  # the pinned swap buffers of swap-ins may be released now
+        return pre, dec, pre_out, dec_out
+
+
+class OracleRunner:
+    """Replays the same events with the CPU oracle."""
+
+    def __init__(self, cfg, num_blocks):
+        from tests.oracle_side import empty_pools
+        self.cfg = cfg
+        self.k_cache, self.v_cache = empty_pools(num_blocks, cfg.Hkv, cfg.block_size, cfg.D)
+        self.saved = {}
+        self.scale = 1.0 / np.sqrt(cfg.D)
+
+    def run(self, ev: Event, values: TokenValues):
+        from oracle import cache
+        cfg = self.cfg
+        shape = (cfg.Hkv, cfg.block_size, cfg.D)
+        for kind, rid, blocks in ev.ops:
+            if kind == "swap_out":
+                kb = np.empty((len(blocks),) + shape, np.uint16)
+                vb = np.empty_like(kb)
+                cache.swap_blocks(self.k_cache, self.v_cache, blocks, kb, vb, 0)
+                self.saved[rid] = (kb, vb)
+            else:
+                kb, vb = self.saved.pop(rid)
+                cache.swap_blocks(self.k_cache, self.v_cache, blocks, kb, vb, 1)
+        pre, dec, q, k, v, slots, meta = iteration_inputs(cfg, ev, values)
+        cache.append(self.k_cache, self.v_cache, k, v, slots, cfg.block_size)
+        return pre, dec, q, meta
+
+    def prefill(self, ev, pre, q, meta, i):
+        from oracle import attention
+        tables, lens = meta["prefill"]
+        a, b = int(meta["cu"][i]), int(meta["cu"][i + 1])
+        return attention.prefill(q[a:b], np.array([0, b - a]), [int(lens[i])], self.k_cache,
+                                 self.v_cache, [tables[i]], self.cfg.block_size, self.scale)
+
+    def decode(self, ev, q, meta, i):
+        from oracle import attention
+        tables, lens = meta["decode"]
+        n_pre = int(meta["cu"][-1])
+        return attention.decode(q[n_pre + i:n_pre + i + 1], self.k_cache, self.v_cache,
+                                [tables[i]], [int(lens[i])], self.cfg.block_size, self.scale)[0]
