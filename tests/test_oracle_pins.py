@@ -31,7 +31,7 @@ import pytest
 
 import oracle
 from oracle import attention, cache, paging
-from tests.oracle_side import build_decode_state, build_shared_prefix_state
+from tests.oracle_side import build_decode_state, build_shared_prefix_state, empty_pools
 from workloads import config1, config4, make_decode_workload, normal_bf16
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -379,11 +379,50 @@ def pin_allocator_fuzz():
         assert alloc.num_free() == N
 
 
+def pin_swap_round_trip():
+    """Evicting a request to host memory and bringing it back ("Batching,
+    Scheduling, and Paging", section PagedAttention) restores its tokens in
+    whatever blocks it gets back; blocks a fork still uses stay allocated."""
+    N, B, Hkv, D, L = 12, 4, 2, 8, 10
+    alloc = paging.BlockAllocator(N, B, list(range(N)))
+    kc, vc = empty_pools(N, Hkv, B, D)
+    k, v = normal_bf16((L, Hkv, D), 901), normal_bf16((L, Hkv, D), 902)
+    q = normal_bf16((1, 2 * Hkv, D), 903)
+    s = alloc.create()
+    slots, _ = alloc.append_slots(s, L)
+    cache.append(kc, vc, k, v, slots, B)
+    before = attention.decode(q, kc, vc, [alloc.block_table(s)], [L], B, 0.3)
+    f = alloc.fork(s)
+    out_blocks = alloc.swap_out(s)
+    alloc.check_invariants()
+    assert out_blocks == [0, 1, 2] and alloc.num_free() == N - 3   # the fork holds them
+    kb, vb = np.zeros((3, Hkv, B, D), np.uint16), np.zeros((3, Hkv, B, D), np.uint16)
+    cache.swap_blocks(kc, vc, out_blocks, kb, vb, 0)
+    alloc.free_seq(f)
+    assert alloc.num_free() == N
+    # another request takes (and overwrites) every free block but two
+    t = alloc.create()
+    t_slots, _ = alloc.append_slots(t, 4 * B * 2 + 2 * B)
+    cache.append(kc, vc, normal_bf16((len(t_slots), Hkv, D), 904),
+                 normal_bf16((len(t_slots), Hkv, D), 905), t_slots, B)
+    alloc.free_seq(t)
+    in_blocks = alloc.swap_in(s)
+    alloc.check_invariants()
+    assert len(in_blocks) == -(-L // B) and in_blocks != out_blocks
+    assert alloc.seq_len(s) == L and alloc.block_table(s) == in_blocks
+    cache.swap_blocks(kc, vc, in_blocks, kb, vb, 1)
+    assert np.array_equal(cache.gather(kc, in_blocks, L, B), k)
+    assert np.array_equal(cache.gather(vc, in_blocks, L, B), v)
+    after = attention.decode(q, kc, vc, [in_blocks], [L], B, 0.3)
+    assert np.array_equal(after, before)
+
+
 PINS = [pin_widen_bf16, pin_decode_brute_force, pin_prefill_brute_force,
         pin_decode_torch_sdpa, pin_prefill_torch_sdpa, pin_single_key_returns_v,
         pin_closed_forms, pin_placement_invariance, pin_shared_equals_duplicated,
         pin_cow_isolation, pin_decode_equals_last_prefill_row, pin_append_gather_roundtrip,
-        pin_poisoned_slots_unread, pin_allocator_golden, pin_allocator_fuzz]
+        pin_poisoned_slots_unread, pin_allocator_golden, pin_allocator_fuzz,
+        pin_swap_round_trip]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -462,7 +501,30 @@ def _mut_free_lifo(self, sid):
             self.free.appendleft(b)
 
 
-_ORIG = {"attend": attention.attend, "widen": attention.widen_bf16,
+def _mut_swap_direction(k_cache, v_cache, blocks, k_buf, v_buf, direction):
+    _ORIG["swap_blocks"](k_cache, v_cache, blocks, k_buf, v_buf, 1 - direction)
+
+
+def _mut_swap_out_ignores_sharing(self, sid):
+    seq = self.seqs[sid]
+    blocks = list(seq["blocks"])
+    for b in blocks:
+        self.refcount[b] = 0
+        self.free.append(b)
+    seq["blocks"] = []
+    seq["swapped"] = True
+    return blocks
+
+
+def _mut_swap_in_one_short(self, sid):
+    seq = self.seqs[sid]
+    need = max(-(-seq["len"] // self.block_size) - 1, 0)
+    seq["blocks"] = [self._take() for _ in range(need)]
+    seq["swapped"] = False
+    return list(seq["blocks"])
+
+
+_ORIG = {"attend": attention.attend, "swap_blocks": cache.swap_blocks, "widen": attention.widen_bf16,
          "group": attention._group}
 
 MUTATIONS = {
@@ -478,6 +540,10 @@ MUTATIONS = {
     "gqa_all_heads_on_kv0": (attention, "_group", _mut_group_all_on_first),
     "no_copy_on_write": (paging.BlockAllocator, "append_slots", _mut_append_no_cow),
     "free_list_lifo": (paging.BlockAllocator, "free_seq", _mut_free_lifo),
+    "swap_direction": (cache, "swap_blocks", _mut_swap_direction),
+    "swap_out_ignores_sharing": (paging.BlockAllocator, "swap_out",
+                                 _mut_swap_out_ignores_sharing),
+    "swap_in_one_short": (paging.BlockAllocator, "swap_in", _mut_swap_in_one_short),
 }
 
 
