@@ -54,12 +54,13 @@ def parse_args():
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--workload", choices=["llama3_8b_gqa", "trace", "swap"],
+    ap.add_argument("--workload", choices=["llama3_8b_gqa", "trace", "swap", "prefix_cache"],
                     default="llama3_8b_gqa",
                     help="trace: the 200-iteration continuous-batching workload; swap: "
                          "preemption by swapping, every block of the decode batch out to "
-                         "pinned host memory and back (separate lines; the default is the "
-                         "headline decode step)")
+                         "pinned host memory and back; prefix_cache: 256 requests sharing a "
+                         "1024-token system prompt, prefilled with and without the prefix "
+                         "cache (separate lines; the default is the headline decode step)")
     ap.add_argument("--iterations", type=int, default=200)
     return ap.parse_args()
 
@@ -457,6 +458,132 @@ def run_swap(args):
     return 0
 
 
+def run_prefix_cache(args):
+    """Prefix caching: 256 requests share a 1024-token system prompt and each
+    adds a question of U[16, 256] tokens (Llama-3-8B GQA layer: 32/8 heads,
+    D=128, B=16). One iteration admits them all: the library's allocator maps
+    every request after the first onto the prompt's registered blocks, so
+    kv_append and prefill cover only the questions; without the cache every
+    request appends and prefills its whole prompt. Reports prompt tokens
+    served per second of GPU time (kv_append + prefill) both ways."""
+    import torch
+    import paged_kv_cache_281_gb300 as pkv
+    from tests.gpu_harness import poisoned_pools
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    S, P, Hq, Hkv, D, B = 256, 1024, 32, 8, 128, 16
+    g = np.random.default_rng(0x281 + 70 + rank)
+    qlen = g.integers(16, 256, size=S, endpoint=True)
+    system = g.integers(0, 32000, size=P).tolist()
+    prompts = [system + g.integers(0, 32000, size=int(n)).tolist() for n in qlen]
+    num_blocks = S * math.ceil((P + 256) / B) + 64
+    tg = torch.Generator(device="cuda").manual_seed(0x281 + 70 + rank)
+    randn = lambda *shape: torch.randn(*shape, generator=tg, device="cuda").to(torch.bfloat16)
+    sys_q, sys_k, sys_v = randn(P, Hq, D), randn(P, Hkv, D), randn(P, Hkv, D)
+    own = [(randn(int(n), Hq, D), randn(int(n), Hkv, D), randn(int(n), Hkv, D)) for n in qlen]
+    scale = 1.0 / math.sqrt(D)
+    stream = torch.cuda.current_stream()
+
+    def plan(cached):
+        alloc = pkv.BlockAllocator(num_blocks, B)
+        h0 = time.perf_counter()
+        sids, starts, slots = [], [], []
+        for toks in prompts:
+            if cached:
+                sid, nc = alloc.seq_create_cached(toks)
+            else:
+                sid, nc = alloc.seq_create(), 0
+            sl, _ = alloc.seq_append_tokens(sid, toks[nc:])
+            sids.append(sid), starts.append(nc), slots.append(sl)
+        tables, lens = alloc.build_block_tables(sids, math.ceil((P + 256) / B))
+        host_ms = 1e3 * (time.perf_counter() - h0)
+        used = num_blocks - alloc.num_free_blocks()
+        # device inputs: rows start .. len-1 of every request
+        qs, ks, vs = [], [], []
+        for i, st in enumerate(starts):
+            if st < P:
+                qs.append(sys_q[st:]), ks.append(sys_k[st:]), vs.append(sys_v[st:])
+            qs.append(own[i][0]), ks.append(own[i][1]), vs.append(own[i][2])
+        chunks = [len(t) - st for t, st in zip(prompts, starts)]
+        cu = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+        d = {"q": torch.cat(qs), "k": torch.cat(ks), "v": torch.cat(vs),
+             "slots": torch.from_numpy(np.concatenate(slots).astype(np.int32)).cuda(),
+             "cu": torch.from_numpy(cu).cuda(), "lens": torch.from_numpy(lens).cuda(),
+             "tables": torch.from_numpy(tables).cuda(), "max_q": int(max(chunks)),
+             "max_ctx": int(lens.max())}
+        d["out"] = torch.empty_like(d["q"])
+        flops = sum(4 * D * Hq * (c * (L - c) + c * (c + 1) // 2)
+                    for c, L in zip(chunks, lens.tolist()))
+        return d, {"host_ms": host_ms, "blocks_used": used, "rows": int(cu[-1]),
+                   "flops": flops}
+
+    def run(d, kc, vc, status, steps):
+        evs = []
+        for _ in range(steps):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record(stream)
+            pkv.pkv_kv_append(d["k"], d["v"], d["slots"], kc, vc, status=status, stream=stream)
+            e[1].record(stream)
+            pkv.pkv_paged_attention_prefill(d["out"], d["q"], d["cu"], d["lens"], kc, vc,
+                                            d["tables"], d["max_q"], d["max_ctx"], scale, ws,
+                                            status=status, stream=stream)
+            e[2].record(stream)
+            evs.append(e)
+        torch.cuda.synchronize()
+        pkv.pkv_check_status(status)
+        app = sum(a.elapsed_time(b) for a, b, _ in evs) / steps
+        pre = sum(b.elapsed_time(c) for _, b, c in evs) / steps
+        return app, pre
+
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    steps = max(5, min(args.steps, 50))
+    results = {}
+    with ClockSampler(local) as clocks:
+        for cached in (True, False):
+            d, info = plan(cached)
+            kc, vc = poisoned_pools(num_blocks, Hkv, B, D)
+            status = pkv.new_status()
+            run(d, kc, vc, status, max(3, args.warmup))
+            app, pre = run(d, kc, vc, status, steps)
+            info.update(kv_append_ms=app, prefill_ms=pre)
+            results["cached" if cached else "uncached"] = info
+            del d, kc, vc
+    prompt_tokens = int(sum(len(t) for t in prompts))
+    c, u = results["cached"], results["uncached"]
+    ms = c["kv_append_ms"] + c["prefill_ms"]
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {"bf16_tflops": 1900.0}
+    tf = c["flops"] / (c["prefill_ms"] * 1e-3) / 1e12
+    line = {
+        "metric": "prefix caching: prompt tokens served per second (kv_append + prefill GPU "
+                  "time), 256 requests sharing a 1024-token system prompt",
+        "value": world * prompt_tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "256 requests = 1024-token system prompt + U[16,256]-token "
+                               "question, 32/8 heads, D=128, B=16, one admission iteration",
+                   "prompt_tokens": prompt_tokens,
+                   "l2": "K/V pools of %.2f GB (> 129 MB L2); each request's prefix pages "
+                         "are shared" % (2 * num_blocks * Hkv * B * D * 2 / 1e9)},
+        "cached": c, "uncached": u,
+        "uncached_tokens_per_s": world * prompt_tokens /
+                                 ((u["kv_append_ms"] + u["prefill_ms"]) * 1e-3),
+        "speedup": (u["kv_append_ms"] + u["prefill_ms"]) / ms,
+        "kv_blocks_saved": u["blocks_used"] - c["blocks_used"],
+        "roofline": {"bound": "tensor", "kernel": "paged_prefill_kernel (cached run)",
+                     "achieved": tf, "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
+                     "frac": tf / float(peaks["bf16_tflops"]), "traffic": None},
+        "gpu_launches": 2 * 2 * (steps + max(3, args.warmup)),
+        "clocks": clocks.summary(),
+        "cpu_baseline": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -465,6 +592,8 @@ def main():
         return run_trace(args)
     if args.workload == "swap":
         return run_swap(args)
+    if args.workload == "prefix_cache":
+        return run_prefix_cache(args)
     import torch
     import paged_kv_cache_281_gb300 as pkv
     from tests.gpu_harness import decode_step, setup_decode, to_dev_bf16

@@ -122,6 +122,36 @@ int pkv_build_block_tables(pkv_alloc* a, const int64_t* seqs, int32_t n, int32_t
 int pkv_seq_swap_out(pkv_alloc* a, int64_t seq, int32_t* blocks_out, int32_t cap, int32_t* n);
 int pkv_seq_swap_in(pkv_alloc* a, int64_t seq, int32_t* blocks_out, int32_t cap, int32_t* n);
 
+/* Prefix caching ("Batching, Scheduling, and Paging", section Block sharing:
+ * identical prefixes of different requests can share physical blocks;
+ * "Paging the KV Cache": a system prompt common to many concurrent requests
+ * occupies one set of pages that all of them reference).
+ *   A full block of a sequence whose token ids are known is registered under
+ *   (the block before it, or none for the first block; its block_size token
+ *   ids). Entries are compared in full, never by hash alone. A registered
+ *   block keeps its entry after its last user leaves; it sits in the free
+ *   list as usual, a lookup can take it back from there, and it loses the
+ *   entry (with the entries that chain from it) when the free list hands it
+ *   out again.
+ *   create_cached: a new sequence whose table starts with the registered
+ *     blocks matching token_ids[0..n) block by block from the start, at most
+ *     (n - 1) / block_size of them, so that the last token is always computed;
+ *     each matched block gains one reference (leaving the free list if it was
+ *     there). *n_cached = matched blocks * block_size tokens, already in the
+ *     cache: append token_ids[*n_cached..n) with append_tokens.
+ *   append_tokens: append_slots that also records the n token ids
+ *     (token_ids: n int32, host) and registers blocks as they fill; a block
+ *     whose entry already exists (an identical block elsewhere) is not
+ *     registered, nor is anything after it in that sequence. Sequences that
+ *     were ever appended with append_slots, and swapped-in sequences,
+ *     register nothing.
+ *   num_cached_blocks: registered blocks, in use or free. */
+int pkv_seq_create_cached(pkv_alloc* a, const int32_t* token_ids, int32_t n, int64_t* seq_id,
+                          int32_t* n_cached);
+int pkv_seq_append_tokens(pkv_alloc* a, int64_t seq, const int32_t* token_ids, int32_t n,
+                          int32_t* slots_out, int32_t* cow_pair_out, int32_t* n_cow);
+int pkv_num_cached_blocks(pkv_alloc* a, int32_t* out);
+
 /* ------------------------------------------------------------------------
  * Device status block (4 int32 in device memory, owned by the caller):
  *   [0] first error code (0, PKV_ETIMEOUT or PKV_EDEVICE), [1] detail (the

@@ -38,6 +38,9 @@ SIGNATURES = {
     "pkv_build_block_tables": (ctypes.c_int, [vp, P(i64), i32, P(i32), i32, P(i32)]),
     "pkv_seq_swap_out": (ctypes.c_int, [vp, i64, P(i32), i32, P(i32)]),
     "pkv_seq_swap_in": (ctypes.c_int, [vp, i64, P(i32), i32, P(i32)]),
+    "pkv_seq_create_cached": (ctypes.c_int, [vp, P(i32), i32, P(i64), P(i32)]),
+    "pkv_seq_append_tokens": (ctypes.c_int, [vp, i64, P(i32), i32, P(i32), P(i32), P(i32)]),
+    "pkv_num_cached_blocks": (ctypes.c_int, [vp, P(i32)]),
     "pkv_swap_blocks": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, vp]),
     "pkv_status_reset": (ctypes.c_int, [vp, vp]),
     "pkv_check_status": (ctypes.c_int, [vp, vp]),

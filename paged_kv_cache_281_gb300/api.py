@@ -114,6 +114,34 @@ class BlockAllocator:
             pair.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), ctypes.byref(ncow)))
         return slots[:int(n)], ((int(pair[0]), int(pair[1])) if ncow.value else None)
 
+    def seq_append_tokens(self, seq: int, token_ids):
+        """``seq_append_slots`` that also records the token ids for the prefix cache."""
+        ids = np.ascontiguousarray(token_ids, dtype=np.int32)
+        n = int(ids.shape[0])
+        slots = np.empty(max(n, 1), dtype=np.int32)
+        pair = np.zeros(2, dtype=np.int32)
+        ncow = ctypes.c_int32()
+        check(lib().pkv_seq_append_tokens(
+            self._h, int(seq), ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), n,
+            slots.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            pair.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), ctypes.byref(ncow)))
+        return slots[:n], ((int(pair[0]), int(pair[1])) if ncow.value else None)
+
+    def seq_create_cached(self, token_ids):
+        """A new sequence starting with the cached blocks of ``token_ids``'s
+        prefix; returns ``(seq, n_cached)``."""
+        ids = np.ascontiguousarray(token_ids, dtype=np.int32)
+        sid, nc = ctypes.c_int64(), ctypes.c_int32()
+        check(lib().pkv_seq_create_cached(self._h, ids.ctypes.data_as(
+            ctypes.POINTER(ctypes.c_int32)), int(ids.shape[0]), ctypes.byref(sid),
+            ctypes.byref(nc)))
+        return sid.value, nc.value
+
+    def num_cached_blocks(self) -> int:
+        out = ctypes.c_int32()
+        check(lib().pkv_num_cached_blocks(self._h, ctypes.byref(out)))
+        return out.value
+
     def seq_free(self, seq: int) -> None:
         check(lib().pkv_seq_free(self._h, int(seq)))
 

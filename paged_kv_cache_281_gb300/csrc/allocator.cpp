@@ -8,9 +8,9 @@
 //     the first divergent write copies (copy-on-write) and reference counts
 //     keep a shared block alive until its last user finishes.
 //
-// Data structures: a ring buffer holding the free list (first in, first out),
-// one int32 count per block, and a hash map from sequence id to its block
-// list and token count. Every operation checks its preconditions before it
+// Data structures: a doubly linked free list (first in, first out), one
+// int32 count per block, a hash map from sequence id to its block list and
+// token count, and the prefix-cache index of full blocks. Every operation checks its preconditions before it
 // mutates anything, so a failed call leaves the allocator unchanged.
 #include <cstring>
 #include <new>
@@ -22,29 +22,150 @@
 struct pkv_alloc {
   int32_t num_blocks = 0;
   int32_t block_size = 0;
-  // free list as a ring buffer of capacity num_blocks
-  std::vector<int32_t> ring;
-  int32_t head = 0;
+  // free list, first in first out, as a doubly linked list over block ids so
+  // that a cached block can leave it from the middle when a lookup revives it
+  std::vector<int32_t> next, prev;
+  std::vector<char> on_free;
+  int32_t head = -1, tail = -1;
   int32_t count = 0;
   std::vector<int32_t> refcount;
   struct Seq {
     std::vector<int32_t> blocks;
     int32_t len = 0;
     bool swapped = false;  // blocks handed back; contents kept by the caller
+    bool tracked = true;   // token ids known for every position (prefix cache)
+    std::vector<int32_t> tokens;
+    int32_t reg_upto = 0;  // leading blocks that are registered, chained
   };
   std::unordered_map<int64_t, Seq> seqs;
   int64_t next_id = 0;
 
-  int32_t pop_free() {
-    int32_t b = ring[head];
-    head = (head + 1) % num_blocks;
+  // Prefix cache: a full block is registered under (the registered block
+  // before it, or -1, and its B token ids). Registered blocks keep their
+  // entry after their last user leaves and can be revived by a lookup until
+  // the free list hands them out again.
+  struct Entry {
+    bool registered = false;
+    int32_t parent = -1;
+    std::vector<int32_t> tokens;
+    std::vector<int32_t> children;
+  };
+  std::vector<Entry> entry;
+  std::unordered_map<uint64_t, std::vector<int32_t>> index;
+  int32_t num_registered = 0;
+
+  static uint64_t key_of(int32_t parent, const int32_t* tok, int32_t B) {
+    // FNV-1a over the parent id and the token ids; entries are compared in
+    // full, so collisions only cost a longer bucket
+    uint64_t h = 1469598103934665603ull;
+    auto mix = [&h](uint32_t x) {
+      for (int i = 0; i < 4; ++i) {
+        h ^= (x >> (8 * i)) & 0xffu;
+        h *= 1099511628211ull;
+      }
+    };
+    mix((uint32_t)parent);
+    for (int32_t i = 0; i < B; ++i) mix((uint32_t)tok[i]);
+    return h;
+  }
+  int32_t lookup(int32_t parent, const int32_t* tok) const {
+    auto it = index.find(key_of(parent, tok, block_size));
+    if (it == index.end()) return -1;
+    for (int32_t c : it->second) {
+      const Entry& e = entry[c];
+      if (e.parent == parent && std::memcmp(e.tokens.data(), tok, sizeof(int32_t) * block_size) == 0)
+        return c;
+    }
+    return -1;
+  }
+  void register_block(int32_t b, int32_t parent, const int32_t* tok) {
+    Entry& e = entry[b];
+    e.registered = true;
+    e.parent = parent;
+    e.tokens.assign(tok, tok + block_size);
+    index[key_of(parent, tok, block_size)].push_back(b);
+    if (parent >= 0) entry[parent].children.push_back(b);
+    ++num_registered;
+  }
+  // Drops b's entry and, below it, its descendants' (all of them are free
+  // whenever b is: a user of a block also uses the block before it).
+  void unregister(int32_t b) {
+    std::vector<int32_t> stack{b};
+    const int32_t root_parent = entry[b].parent;
+    if (root_parent >= 0) {
+      auto& ch = entry[root_parent].children;
+      for (size_t i = 0; i < ch.size(); ++i)
+        if (ch[i] == b) {
+          ch[i] = ch.back();
+          ch.pop_back();
+          break;
+        }
+    }
+    while (!stack.empty()) {
+      int32_t x = stack.back();
+      stack.pop_back();
+      Entry& e = entry[x];
+      auto it = index.find(key_of(e.parent, e.tokens.data(), block_size));
+      auto& bucket = it->second;
+      for (size_t i = 0; i < bucket.size(); ++i)
+        if (bucket[i] == x) {
+          bucket[i] = bucket.back();
+          bucket.pop_back();
+          break;
+        }
+      if (bucket.empty()) index.erase(it);
+      for (int32_t c : e.children) stack.push_back(c);
+      e = Entry{};
+      --num_registered;
+    }
+  }
+
+  void unlink(int32_t b) {
+    if (prev[b] >= 0) next[prev[b]] = next[b]; else head = next[b];
+    if (next[b] >= 0) prev[next[b]] = prev[b]; else tail = prev[b];
+    prev[b] = next[b] = -1;
+    on_free[b] = 0;
     --count;
+  }
+  int32_t pop_free() {
+    int32_t b = head;
+    unlink(b);
+    if (entry[b].registered) unregister(b);  // handed out again: its contents will change
     refcount[b] = 1;
     return b;
   }
   void push_free(int32_t b) {
-    ring[(head + count) % num_blocks] = b;
+    prev[b] = tail;
+    next[b] = -1;
+    if (tail >= 0) next[tail] = b; else head = b;
+    tail = b;
+    on_free[b] = 1;
     ++count;
+  }
+  // A reference to a block found by a lookup (revived from the free list if
+  // nobody holds it).
+  void take_cached(int32_t b) {
+    if (refcount[b] == 0) unlink(b);
+    ++refcount[b];
+  }
+  // Registers the blocks of a tracked sequence that have become full, in
+  // order; an identical block registered elsewhere ends the chain (the
+  // sequence's later blocks then stay unregistered).
+  void register_full_blocks(Seq& s) {
+    const int32_t B = block_size;
+    const int32_t full = s.len / B;
+    while (s.tracked && s.reg_upto < full) {
+      const int32_t j = s.reg_upto;
+      const int32_t parent = j == 0 ? -1 : s.blocks[j - 1];
+      const int32_t* tok = s.tokens.data() + (int64_t)j * B;
+      if (lookup(parent, tok) >= 0) {
+        s.tracked = false;
+        s.tokens.clear();
+        break;
+      }
+      register_block(s.blocks[j], parent, tok);
+      ++s.reg_upto;
+    }
   }
   Seq* find(int64_t id) {
     auto it = seqs.find(id);
@@ -67,8 +188,11 @@ extern "C" int pkv_alloc_create(int32_t num_blocks, int32_t block_size, const in
   if (!a) return fail(PKV_ENOMEM, "pkv_alloc_create: out of host memory");
   a->num_blocks = num_blocks;
   a->block_size = block_size;
-  a->ring.resize(num_blocks);
+  a->next.assign(num_blocks, -1);
+  a->prev.assign(num_blocks, -1);
+  a->on_free.assign(num_blocks, 0);
   a->refcount.assign(num_blocks, 0);
+  a->entry.resize(num_blocks);
   if (free_order) {
     std::vector<char> seen(num_blocks, 0);
     for (int32_t i = 0; i < num_blocks; ++i) {
@@ -79,12 +203,11 @@ extern "C" int pkv_alloc_create(int32_t num_blocks, int32_t block_size, const in
                     i, b);
       }
       seen[b] = 1;
-      a->ring[i] = b;
     }
+    for (int32_t i = 0; i < num_blocks; ++i) a->push_free(free_order[i]);
   } else {
-    for (int32_t i = 0; i < num_blocks; ++i) a->ring[i] = i;
+    for (int32_t i = 0; i < num_blocks; ++i) a->push_free(i);
   }
-  a->count = num_blocks;
   *out = a;
   return ok();
 }
@@ -115,28 +238,33 @@ extern "C" int pkv_seq_fork(pkv_alloc* a, int64_t parent, int64_t* child) {
   return ok();
 }
 
-extern "C" int pkv_seq_append_slots(pkv_alloc* a, int64_t seq, int32_t n, int32_t* slots_out,
-                                    int32_t* cow_pair_out, int32_t* n_cow) {
-  PKV_REQUIRE(a && n_cow, "pkv_seq_append_slots: NULL argument");
-  PKV_REQUIRE(n >= 0, "pkv_seq_append_slots: n must be >= 0 (got %d)", n);
-  PKV_REQUIRE(n == 0 || slots_out, "pkv_seq_append_slots: slots_out is NULL");
+namespace {
+
+// Reserves slots for n new tokens of a sequence; token_ids (nullable) are
+// recorded for the prefix cache.
+int append_impl(pkv_alloc* a, int64_t seq, int32_t n, const int32_t* token_ids,
+                int32_t* slots_out, int32_t* cow_pair_out, int32_t* n_cow, const char* who) {
+  PKV_REQUIRE(a && n_cow, "%s: NULL argument", who);
+  PKV_REQUIRE(n >= 0, "%s: n must be >= 0 (got %d)", who, n);
+  PKV_REQUIRE(n == 0 || slots_out, "%s: slots_out is NULL", who);
   pkv_alloc::Seq* s = a->find(seq);
-  PKV_REQUIRE(s, "pkv_seq_append_slots: unknown sequence %lld", (long long)seq);
-  PKV_REQUIRE(!s->swapped, "pkv_seq_append_slots: sequence %lld is swapped out", (long long)seq);
+  PKV_REQUIRE(s, "%s: unknown sequence %lld", who, (long long)seq);
+  PKV_REQUIRE(!s->swapped, "%s: sequence %lld is swapped out", who, (long long)seq);
   *n_cow = 0;
   if (n == 0) return ok();
   const int32_t B = a->block_size;
   const int64_t new_len = (int64_t)s->len + n;
+  PKV_REQUIRE(new_len < (int64_t(1) << 31), "%s: sequence length overflows int32", who);
   // Blocks needed: the ones that open past the current table, plus one copy
   // when the first new token lands in a shared, partially filled last block.
   const bool partial = (s->len % B) != 0;
   const bool cow = partial && a->refcount[s->blocks.back()] > 1;
   const int64_t need = (new_len + B - 1) / B - (int64_t)s->blocks.size() + (cow ? 1 : 0);
   if (need > a->count)
-    return fail(PKV_ENOMEM, "pkv_seq_append_slots: sequence %lld needs %lld blocks, %d free",
+    return fail(PKV_ENOMEM, "%s: sequence %lld needs %lld blocks, %d free", who,
                 (long long)seq, (long long)need, a->count);
+  PKV_REQUIRE(!cow || cow_pair_out, "%s: cow_pair_out is NULL but a copy is needed", who);
   if (cow) {
-    PKV_REQUIRE(cow_pair_out, "pkv_seq_append_slots: cow_pair_out is NULL but a copy is needed");
     int32_t& last = s->blocks.back();
     int32_t fresh = a->pop_free();
     --a->refcount[last];
@@ -152,6 +280,63 @@ extern "C" int pkv_seq_append_slots(pkv_alloc* a, int64_t seq, int32_t n, int32_
     slots_out[i] = s->blocks[j] * B + pos % B;
   }
   s->len = (int32_t)new_len;
+  if (s->tracked && token_ids) {
+    s->tokens.insert(s->tokens.end(), token_ids, token_ids + n);
+    a->register_full_blocks(*s);
+  } else {
+    s->tracked = false;
+    s->tokens.clear();
+  }
+  return ok();
+}
+
+}  // namespace
+
+extern "C" int pkv_seq_append_slots(pkv_alloc* a, int64_t seq, int32_t n, int32_t* slots_out,
+                                    int32_t* cow_pair_out, int32_t* n_cow) {
+  return append_impl(a, seq, n, nullptr, slots_out, cow_pair_out, n_cow, "pkv_seq_append_slots");
+}
+
+// Prefix caching ("Batching, Scheduling, and Paging", section Block sharing:
+// identical prefixes of different requests can share blocks; "Paging the KV
+// Cache": a system prompt common to many requests occupies one set of pages).
+extern "C" int pkv_seq_append_tokens(pkv_alloc* a, int64_t seq, const int32_t* token_ids,
+                                     int32_t n, int32_t* slots_out, int32_t* cow_pair_out,
+                                     int32_t* n_cow) {
+  PKV_REQUIRE(n == 0 || token_ids, "pkv_seq_append_tokens: token_ids is NULL");
+  return append_impl(a, seq, n, token_ids, slots_out, cow_pair_out, n_cow,
+                     "pkv_seq_append_tokens");
+}
+
+extern "C" int pkv_seq_create_cached(pkv_alloc* a, const int32_t* token_ids, int32_t n,
+                                     int64_t* seq_id, int32_t* n_cached) {
+  PKV_REQUIRE(a && seq_id && n_cached, "pkv_seq_create_cached: NULL argument");
+  PKV_REQUIRE(n >= 0 && (n == 0 || token_ids), "pkv_seq_create_cached: bad token array");
+  const int32_t B = a->block_size;
+  pkv_alloc::Seq s;
+  // at most the full blocks before the last token: that token is always computed
+  const int32_t max_full = n > 0 ? (n - 1) / B : 0;
+  int32_t parent = -1;
+  for (int32_t j = 0; j < max_full; ++j) {
+    const int32_t b = a->lookup(parent, token_ids + (int64_t)j * B);
+    if (b < 0) break;
+    a->take_cached(b);
+    s.blocks.push_back(b);
+    parent = b;
+  }
+  s.len = (int32_t)s.blocks.size() * B;
+  s.reg_upto = (int32_t)s.blocks.size();
+  s.tokens.assign(token_ids, token_ids + s.len);
+  int64_t id = a->next_id++;
+  a->seqs.emplace(id, std::move(s));
+  *seq_id = id;
+  *n_cached = (int32_t)(a->seqs[id].len);
+  return ok();
+}
+
+extern "C" int pkv_num_cached_blocks(pkv_alloc* a, int32_t* out) {
+  PKV_REQUIRE(a && out, "pkv_num_cached_blocks: NULL argument");
+  *out = a->num_registered;
   return ok();
 }
 
@@ -267,6 +452,9 @@ extern "C" int pkv_seq_swap_in(pkv_alloc* a, int64_t seq, int32_t* blocks_out, i
     blocks_out[i] = b;
   }
   s->swapped = false;
+  s->tracked = false;  // fresh blocks are not registered
+  s->tokens.clear();
+  s->reg_upto = 0;
   *n = m;
   return ok();
 }

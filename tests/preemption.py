@@ -58,6 +58,17 @@ class LibraryAllocator:
     def free(self, sid):
         self.a.seq_free(sid)
 
+    def create_cached(self, tokens):
+        return self.a.seq_create_cached(tokens)
+
+    def append_tokens(self, sid, tokens):
+        slots, pair = self._guard(self.a.seq_append_tokens, sid, tokens)
+        assert pair is None
+        return [int(x) for x in slots]
+
+    def num_cached(self):
+        return self.a.num_cached_blocks()
+
     def swap_out(self, sid):
         return self.a.seq_swap_out(sid)
 
@@ -92,6 +103,20 @@ class OracleAllocator:
 
     def free(self, sid):
         self.a.free_seq(sid)
+
+    def create_cached(self, tokens):
+        return self.a.create_cached(tokens)
+
+    def append_tokens(self, sid, tokens):
+        try:
+            slots, pairs = self.a.append_tokens(sid, tokens)
+        except self.paging.OutOfBlocks as e:
+            raise OutOfBlocks(str(e)) from None
+        assert not pairs
+        return slots
+
+    def num_cached(self):
+        return self.a.num_cached()
 
     def swap_out(self, sid):
         return self.a.swap_out(sid)

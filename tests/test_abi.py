@@ -18,6 +18,7 @@ from paged_kv_cache_281_gb300 import _lib
 from paged_kv_cache_281_gb300._lib import (PKV_EINVAL, PKV_ENOMEM, PagedKVError,
                                             header_functions, lib)
 from oracle import paging
+from tests.test_oracle_pins import parse_ids
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -53,9 +54,17 @@ def _replay_on_library(path):
             names[args[0]] = alloc.seq_create()
         elif op == "fork":
             names[args[1]] = alloc.seq_fork(names[args[0]])
+        elif op == "create_cached":
+            names[args[0]], n_cached = alloc.seq_create_cached(parse_ids(args[1]))
+            assert n_cached == int(args[2]), line
+        elif op == "append_tokens":
+            slots, pair = alloc.seq_append_tokens(names[args[0]], parse_ids(args[1]))
+            assert slots.tolist() == parse_ids(args[2]) and pair is None, line
+        elif op == "ncached":
+            assert alloc.num_cached_blocks() == int(args[0]), line
         elif op == "append":
             slots, pair = alloc.seq_append_slots(names[args[0]], int(args[1]))
-            want = [int(x) for x in args[2].split(",")] if args[2] != "-" else []
+            want = parse_ids(args[2])
             want_pairs = ([tuple(int(y) for y in x.split(">")) for x in args[3].split(",")]
                           if args[3] != "-" else [])
             assert slots.tolist() == want, line
@@ -87,6 +96,113 @@ def _replay_on_library(path):
 
 def test_allocator_golden_scenario():
     _replay_on_library("allocator_block_sharing.txt")
+
+
+def test_prefix_cache_golden_scenario():
+    _replay_on_library("prefix_cache.txt")
+
+
+def _prefix_cache_fuzz(seed):
+    """Random requests drawn from a few shared prompts, with forks, frees,
+    swaps and untracked appends: every result and the whole state agree.
+    Returns (lookups that hit, operations that dropped entries)."""
+    rng = np.random.default_rng(100 + seed)
+    N, B = int(rng.integers(6, 24)), int(rng.choice([1, 2, 4, 8]))
+    order = rng.permutation(N)
+    lib_a = pkv.BlockAllocator(N, B, order)
+    ref = paging.BlockAllocator(N, B, order)
+    prompts = [rng.integers(0, 3, size=int(rng.integers(1, 6 * B + 3))).tolist()
+               for _ in range(4)]
+    live, swapped, pos = [], [], {}
+    hits = drops = 0
+    for _ in range(500):
+        cached_before = ref.num_cached()
+        op = int(rng.integers(0, 10))
+        if op <= 1 or not live:
+            base = prompts[int(rng.integers(len(prompts)))]
+            toks = base[:int(rng.integers(1, len(base) + 1))] + \
+                rng.integers(0, 3, size=int(rng.integers(0, 2 * B))).tolist()
+            try:
+                want = ref.create_cached(toks)
+            except paging.OutOfBlocks:
+                raise AssertionError("create_cached never allocates")
+            got = lib_a.seq_create_cached(toks)
+            assert got == want
+            sid, nc = got
+            hits += nc > 0
+            live.append(sid)
+            pos[sid] = toks[nc:]
+        elif op == 2:
+            p = live[int(rng.integers(len(live)))]
+            assert lib_a.seq_fork(p) == ref.fork(p)
+            live.append(ref._next_id - 1)
+            pos[live[-1]] = list(pos[p])
+        elif op in (3, 4):
+            sid = live[int(rng.integers(len(live)))]
+            pending = pos[sid]
+            toks = pending if pending else rng.integers(0, 3, size=int(
+                rng.integers(1, 2 * B + 2))).tolist()
+            try:
+                want_slots, want_pairs = ref.append_tokens(sid, toks)
+            except paging.OutOfBlocks:
+                with pytest.raises(PagedKVError) as e:
+                    lib_a.seq_append_tokens(sid, toks)
+                assert e.value.code == PKV_ENOMEM
+            else:
+                slots, pair = lib_a.seq_append_tokens(sid, toks)
+                assert slots.tolist() == want_slots
+                assert ([pair] if pair else []) == want_pairs
+                pos[sid] = []
+        elif op == 5:
+            sid = live[int(rng.integers(len(live)))]
+            n = int(rng.integers(1, B + 2))
+            try:
+                want_slots, _ = ref.append_slots(sid, n)
+            except paging.OutOfBlocks:
+                with pytest.raises(PagedKVError):
+                    lib_a.seq_append_slots(sid, n)
+            else:
+                assert lib_a.seq_append_slots(sid, n)[0].tolist() == want_slots
+                pos[sid] = []
+        elif op in (6, 7, 8):
+            sid = live.pop(int(rng.integers(len(live))))
+            if rng.random() < 0.3:
+                assert lib_a.seq_swap_out(sid) == ref.swap_out(sid)
+                swapped.append(sid)
+            else:
+                lib_a.seq_free(sid)
+                ref.free_seq(sid)
+        elif swapped:
+            sid = swapped[0]
+            try:
+                want = ref.swap_in(sid)
+            except paging.OutOfBlocks:
+                with pytest.raises(PagedKVError):
+                    lib_a.seq_swap_in(sid)
+            else:
+                assert lib_a.seq_swap_in(sid) == want
+                swapped.pop(0)
+                live.append(sid)
+        ref.check_invariants()
+        drops += ref.num_cached() < cached_before
+        assert lib_a.num_free_blocks() == ref.num_free()
+        assert lib_a.num_cached_blocks() == ref.num_cached()
+        for sid in live:
+            assert lib_a.seq_block_table(sid) == ref.block_table(sid)
+            assert lib_a.seq_len(sid) == ref.seq_len(sid)
+        for blk in range(N):
+            assert lib_a.block_refcount(blk) == ref.refcount[blk]
+    return hits, drops
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_prefix_cache_matches_oracle_model(seed):
+    _prefix_cache_fuzz(seed)
+
+
+def test_prefix_cache_fuzz_reaches_hits_and_evictions():
+    hits, drops = np.sum([_prefix_cache_fuzz(s) for s in range(8)], axis=0)
+    assert hits > 100 and drops > 10, (hits, drops)
 
 
 def test_allocator_free_list_order_after_release():

@@ -303,6 +303,20 @@ def pin_poisoned_slots_unread():
     assert np.isfinite(decode_oracle(w, st)).all()
 
 
+def parse_ids(spec):
+    """A golden-file id list: comma items, each an id or an inclusive range a..b."""
+    if spec == "-":
+        return []
+    out = []
+    for item in spec.split(","):
+        if ".." in item:
+            a, b = item.split("..")
+            out.extend(range(int(a), int(b) + 1))
+        else:
+            out.append(int(item))
+    return out
+
+
 def _run_allocator_script(path):
     """Replays ``tests/golden/<path>``; see that file for the format."""
     alloc = None
@@ -320,9 +334,18 @@ def _run_allocator_script(path):
             names[args[0]] = alloc.create()
         elif op == "fork":
             names[args[1]] = alloc.fork(names[args[0]])
+        elif op == "create_cached":
+            names[args[0]], n_cached = alloc.create_cached(parse_ids(args[1]))
+            assert n_cached == int(args[2]), (line, n_cached)
+        elif op == "append_tokens":
+            slots, pairs = alloc.append_tokens(names[args[0]], parse_ids(args[1]))
+            assert slots == parse_ids(args[2]), (line, slots)
+            assert pairs == [] and args[3] == "-", line
+        elif op == "ncached":
+            assert alloc.num_cached() == int(args[0]), (line, alloc.num_cached())
         elif op == "append":
             slots, pairs = alloc.append_slots(names[args[0]], int(args[1]))
-            exp_slots = [int(x) for x in args[2].split(",")] if args[2] != "-" else []
+            exp_slots = parse_ids(args[2])
             exp_pairs = ([tuple(int(y) for y in x.split(">")) for x in args[3].split(",")]
                          if args[3] != "-" else [])
             assert slots == exp_slots, (line, slots)
@@ -351,6 +374,10 @@ def _run_allocator_script(path):
 
 def pin_allocator_golden():
     _run_allocator_script("allocator_block_sharing.txt")
+
+
+def pin_prefix_cache_golden():
+    _run_allocator_script("prefix_cache.txt")
 
 
 def pin_allocator_fuzz():
@@ -422,7 +449,7 @@ PINS = [pin_widen_bf16, pin_decode_brute_force, pin_prefill_brute_force,
         pin_closed_forms, pin_placement_invariance, pin_shared_equals_duplicated,
         pin_cow_isolation, pin_decode_equals_last_prefill_row, pin_append_gather_roundtrip,
         pin_poisoned_slots_unread, pin_allocator_golden, pin_allocator_fuzz,
-        pin_swap_round_trip]
+        pin_swap_round_trip, pin_prefix_cache_golden]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -480,7 +507,7 @@ def _mut_group_all_on_first(Hq, Hkv):
     return Hq
 
 
-def _mut_append_no_cow(self, sid, n):
+def _mut_append_no_cow(self, sid, n, _keep_tokens=False):
     seq = self.seqs[sid]
     B = self.block_size
     slots = []
@@ -490,6 +517,8 @@ def _mut_append_no_cow(self, sid, n):
             seq["blocks"].append(self._take())
         slots.append(seq["blocks"][j] * B + off)
     seq["len"] += n
+    if n > 0 and not _keep_tokens:
+        seq["tokens"] = None
     return slots, []
 
 
@@ -524,6 +553,31 @@ def _mut_swap_in_one_short(self, sid):
     return list(seq["blocks"])
 
 
+def _mut_take_keeps_descendants(self):
+    b = self.free.popleft()
+    self.refcount[b] = 1
+    if b in self.prefix_of:
+        del self.registry[self.prefix_of.pop(b)]      # extensions wrongly kept
+    return b
+
+
+def _mut_cached_whole_prompt(self, tokens):
+    tokens = [int(t) for t in tokens]
+    B = self.block_size
+    sid = self.create()
+    seq = self.seqs[sid]
+    j = 0
+    while j < len(tokens) // B and tuple(tokens[:(j + 1) * B]) in self.registry:
+        b = self.registry[tuple(tokens[:(j + 1) * B])]
+        if self.refcount[b] == 0:
+            self.free.remove(b)
+        self.refcount[b] += 1
+        seq["blocks"].append(b)
+        j += 1
+    seq["len"], seq["tokens"], seq["registered"] = j * B, tokens[:j * B], j
+    return sid, j * B
+
+
 _ORIG = {"attend": attention.attend, "swap_blocks": cache.swap_blocks, "widen": attention.widen_bf16,
          "group": attention._group}
 
@@ -544,6 +598,10 @@ MUTATIONS = {
     "swap_out_ignores_sharing": (paging.BlockAllocator, "swap_out",
                                  _mut_swap_out_ignores_sharing),
     "swap_in_one_short": (paging.BlockAllocator, "swap_in", _mut_swap_in_one_short),
+    "prefix_cache_keeps_extensions": (paging.BlockAllocator, "_take",
+                                      _mut_take_keeps_descendants),
+    "prefix_cache_whole_prompt": (paging.BlockAllocator, "create_cached",
+                                  _mut_cached_whole_prompt),
 }
 
 
