@@ -8,29 +8,30 @@
 // through the block table ("Batching, Scheduling, and Paging", section
 // PagedAttention).
 //
-// How (GB300 design). One CTA of 4 warps owns a tile of 128 rows, each row a
-// (query, head) pair: 128/G consecutive queries times the G query heads that
-// share one kv head, so every key/value tile loaded serves all of them.
-//  * Q is loaded once by a 3-D TMA box (64 columns x G heads x 128/G queries)
-//    per 64-column half, 128-byte swizzled.
-//  * For each 64-key tile (whole pages located through the block table, one
-//    TMA box per page and half) S = Q K^T is computed by tcgen05.mma
-//    (M=128, N=64, K=16 steps) into tensor memory.
-//  * Thread r owns TMEM lane r = row r: it loads its 64 scores, applies the
-//    causal limit, updates its running max and sum (base 2) and writes its
-//    probabilities to shared memory as two bf16 parts P_hi + P_lo in the
-//    swizzled K-major layout the next MMA reads. When the max moved, it
-//    rescales its O row in tensor memory.
-//  * O += P_hi V + P_lo V runs as tcgen05.mma with V as an MN-major operand
-//    (M=128, N=D); the two parts keep the product at ~fp32 precision.
-//  * The K buffer is refilled as soon as the S MMA retires and the V buffer as
-//    soon as the P V MMA retires, so loads overlap the softmax.
-//  * Every mbarrier wait has a time limit; on expiry the CTA records
-//    PKV_ETIMEOUT, waits (with a limit) for its own copies and MMAs, frees its
-//    tensor memory and returns. About 97 KB of shared memory per CTA lets two
-//    CTAs share an SM (one's softmax overlaps the other's MMAs and loads); the
-//    request never allows a third, so the two 256-column tensor-memory
-//    allocations always fit and allocation never waits.
+// How (GB300 design). One CTA owns a tile of 128 rows, each row a (query,
+// head) pair: 128/G consecutive queries times the G query heads that share one
+// kv head, so every key/value tile loaded serves all of them. Its six warps
+// specialise and run as a pipeline over 64-key tiles:
+//  * warp 0 (one lane) loads Q once by a 3-D TMA box per 64-column half and
+//    streams K and V tiles (whole pages located through the block table, one
+//    TMA box per page and half, 128-byte swizzled) into rings of NS stages;
+//  * warp 1 (one lane issues) runs the tensor core: S_j = Q K_j^T into one of
+//    two TMEM score buffers, then O += P_{j-1} V_{j-1}, so the scores of the
+//    next tile are computed while the softmax works on the current one; the
+//    warp also zeroes the value rows past the last visible key before the
+//    final product (they may hold stale or poisoned bytes, and 0 * NaN is NaN);
+//  * warps 2-5 own one TMEM lane (= row) per thread: they read the 64 scores,
+//    apply the causal limit, keep a running sum against a reference maximum
+//    (base 2), and write the probabilities back into the same TMEM columns as
+//    two bf16 parts P_hi + P_lo (~fp32 precision for the product), which the
+//    P V MMA reads as its A operand straight from tensor memory. O is
+//    rescaled (in TMEM) only when a row's maximum grows by more than 2^8, so
+//    the stored probabilities stay below 256 and the rescale is rare; the
+//    final division by the row sum makes the result independent of the
+//    reference chosen.
+// Every mbarrier wait has a time limit and gives up early once another warp
+// has given up; the CTA then records PKV_ETIMEOUT, waits (with a limit) for its
+// own copies and MMAs, frees its tensor memory and returns.
 #include <cmath>
 #include <mutex>
 
@@ -40,27 +41,35 @@
 namespace pkv {
 namespace {
 
-constexpr int kRows = 128;       // (query, head) rows per tile = TMEM lanes
+constexpr int kRows = 128;       // (query, head) rows per Q tile = TMEM lanes
+constexpr int kQTiles = 2;       // Q tiles per CTA, sharing every K/V tile
 constexpr int kKeys = 64;        // keys per KV tile
-constexpr int kThreadsP = 128;
-constexpr uint32_t kQHalf = kRows * 128;   // one 64-column half of Q: 128 rows x 128 B
-constexpr uint32_t kKVHalf = kKeys * 128;  // one 64-column half of a K or V tile
-constexpr uint32_t kPTile = kRows * kKeys * 2;  // P (one part): 128 rows x 64 keys
+constexpr int kThreadsP = 576;   // producer warp, MMA warp, eight softmax warps per Q tile
+constexpr uint32_t kQHalf = kQTiles * kRows * 128;  // one 64-column half of both Q tiles
+constexpr uint32_t kKVHalf = kKeys * 128;           // one 64-column half of a K or V tile
+constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows past 2^8
+constexpr int kWin = 256;            // block-table entries held in shared memory
 
-template <int D>
+template <int D, int NS>
 struct PCfg {
   static constexpr int kHalves = D / 64;
+  static constexpr uint32_t kStage = kHalves * kKVHalf;
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kK = kQ + kHalves * kQHalf;
-  static constexpr uint32_t kV = kK + kHalves * kKVHalf;
-  static constexpr uint32_t kPhi = kV + kHalves * kKVHalf;
-  static constexpr uint32_t kPlo = kPhi + kPTile;
-  static constexpr uint32_t kBytes = kPlo + kPTile;
-  // more than a third of an SM's shared memory: at most two CTAs per SM, whose
-  // two tensor-memory allocations always fit, so allocation never waits
-  static constexpr uint32_t kSmem = kBytes + 1024 > 80u * 1024 ? kBytes + 1024 : 80u * 1024;
-  static constexpr uint32_t kTmemCols = 256;  // S: 64 columns, O: D columns at 128
-  static constexpr uint32_t kOcol = 128;
+  static constexpr uint32_t kV = kK + NS * kStage;
+  static constexpr uint32_t kBytes = kV + NS * kStage;
+  // + alignment slack; more than half of an SM's shared memory, so that one
+  // CTA (which takes all 512 TMEM columns) runs per SM and allocation never waits
+  static constexpr uint32_t kSmem = kBytes + 1024 > 116u * 1024 ? kBytes + 1024 : 116u * 1024;
+  // barriers: Q; K full/empty and V full/empty per stage; per Q tile and
+  // buffer: S full, P full, PV done, row maxima exchanged; per Q tile: row
+  // sums exchanged; final
+  static constexpr int kBarQ = 0, kBarKF = 1, kBarKE = 1 + NS, kBarVF = 1 + 2 * NS,
+                       kBarVE = 1 + 3 * NS, kBarSF = 1 + 4 * NS, kBarPF = 5 + 4 * NS,
+                       kBarPV = 9 + 4 * NS, kBarX = 13 + 4 * NS, kBarL = 17 + 4 * NS,
+                       kBarFin = 19 + 4 * NS, kNumBars = 20 + 4 * NS;
+  // TMEM per Q tile t at column 256 t: S buffers 0..63 and 64..127, O 128..128+D
+  static constexpr uint32_t kTmemCols = 512;
 };
 
 struct PrefillArgs {
@@ -76,76 +85,164 @@ struct PrefillArgs {
   int32_t force_timeout;
 };
 
-// Loads the pages holding keys [key0, min(key0 + 64, kv_end)) of kv head
-// `kvh` from the pool behind `map` (keys or values) into `dst`; arms `bar`.
-template <int D>
-__device__ void load_kv_tile(const CUtensorMap* map, const PrefillArgs& a, const int32_t* bt,
-                             int kvh, int key0, int kv_end, uint32_t dst, uint32_t bar) {
-  using C = PCfg<D>;
-  const int B = a.block_size;
-  const int pages = kKeys / B;
-  uint32_t bytes = 0;
-  for (int pg = 0; pg < pages; ++pg) {
-    const int tok = key0 + pg * B;
-    if (tok >= kv_end) break;
-    const int32_t blk = __ldg(bt + tok / B);
-    if (blk >= 0 && blk < a.num_blocks) bytes += C::kHalves * B * 128u;
+// Bounded wait that also gives up as soon as another warp of the CTA has
+// given up (`abort` set). The first waiter to run out of time sets `abort`
+// to the site where it waited.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const PrefillArgs& a,
+                                              volatile int* abort, int site) {
+  if (a.force_timeout) {
+    *abort = site;
+    return false;
   }
-  mbar_arrive_expect_tx(bar, bytes);
-  for (int pg = 0; pg < pages; ++pg) {
-    const int tok = key0 + pg * B;
-    if (tok >= kv_end) break;
-    const int32_t blk = __ldg(bt + tok / B);
-    if (blk < 0 || blk >= a.num_blocks) {
-      record_status(a.status, PKV_EDEVICE, blk, kKernelPrefill);
-      continue;
+  if (mbar_try_wait(bar, parity)) return true;
+  // the clocks and the abort flag are read every 32nd retry only, so that a
+  // retry follows a failed one closely
+  const uint64_t t0 = globaltimer_ns();
+  const long long c0 = clock64();
+  const long long cycle_limit =
+      (long long)(a.timeout_ns < (1ull << 60) ? a.timeout_ns : (1ull << 60)) * 4;
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 31) == 0) {
+      if (*abort) return false;
+      if (clock64() - c0 > cycle_limit || globaltimer_ns() - t0 > a.timeout_ns) {
+        *abort = site;
+        return false;
+      }
     }
-    const int row = (blk * a.Hkv + kvh) * B;
-#pragma unroll
-    for (int h = 0; h < C::kHalves; ++h)
-      tma_load_2d(dst + h * kKVHalf + pg * B * 128, map, h * 64, row, bar);
   }
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(kThreadsP, 2)
+// tcgen05.mma kind::f16 with A (M x 16, bf16 pairs per 32-bit column, row =
+// lane) in tensor memory and B in shared memory.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Packed pairs of fp32 (two lanes of one 64-bit register) and their
+// arithmetic, one instruction for both lanes.
+__device__ __forceinline__ uint64_t f32x2_pack(float x, float y) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float& x, float& y) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// 16 consecutive 32-bit columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%16], {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
+      "%10, %11, %12, %13, %14, %15};" ::"r"(r[0]),
+      "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(taddr)
+      : "memory");
+}
+
+template <int D, int G, int NS>
+__global__ void __launch_bounds__(kThreadsP, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                          const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
-  using C = PCfg<D>;
-  constexpr int QT = kRows / G;  // queries per tile
+  using C = PCfg<D, NS>;
+  constexpr int QT = kRows / G;  // queries per Q tile
   constexpr uint32_t kIdescS = umma_idesc_bf16(128, kKeys, false);
   constexpr uint32_t kIdescO = umma_idesc_bf16(128, D, true);
 
   extern __shared__ uint8_t dsm[];
-  __shared__ __align__(8) uint64_t bars[5];  // q, k, v, s, o
+  __shared__ __align__(8) uint64_t bars[C::kNumBars];
   __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int32_t s_pages[kWin];  // window of this sequence's block table
+  // row maxima of the two key halves, per Q tile and score buffer; the two
+  // halves' row sums at the end
+  __shared__ float s_xmax[kQTiles][2][2][kRows];
+  __shared__ float s_lsum[kQTiles][2][kRows];
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int qt = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // heaviest tiles (the chunk's last queries see the most keys) start first
+  const int qt = gridDim.x - 1 - blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int c0 = __ldg(a.cu_q_lens + s);
   const int c = __ldg(a.cu_q_lens + s + 1) - c0;
   const int L = __ldg(a.context_lens + s);
-  const int q0 = qt * QT;
+  const int q0 = qt * kQTiles * QT;
   if (q0 >= c) return;
   if (L < c || L > a.max_context_len) {
     if (tid == 0) record_status(a.status, PKV_EDEVICE, L, kKernelPrefill);
     return;
   }
-  const int qn = min(QT, c - q0);
-  const int kv_end = L - c + q0 + qn;  // keys 0 .. kv_end-1 are visible to some row
+  // Q tile t holds queries q0 + t QT .. + QT - 1 of the chunk; its rows see
+  // keys below kv_end_t, i.e. nkt_t key tiles (0 when it has no query)
+  int nkt_t[kQTiles];
+  int kv_end = 0;
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t) {
+    const int qn = max(0, min(QT, c - (q0 + t * QT)));
+    const int e = L - c + q0 + t * QT + qn;
+    nkt_t[t] = qn > 0 ? (e + kKeys - 1) / kKeys : 0;
+    if (qn > 0) kv_end = e;
+  }
   const int nkt = (kv_end + kKeys - 1) / kKeys;
   const int32_t* bt = a.block_tables + (int64_t)s * a.max_blocks_per_seq;
 
   const uint32_t raw = smem_u32(dsm);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = dsm + (base - raw);
-  const uint32_t bar_of[5] = {smem_u32(&bars[0]), smem_u32(&bars[1]), smem_u32(&bars[2]),
-                              smem_u32(&bars[3]), smem_u32(&bars[4])};
-  enum { kBarQ = 0, kBarK = 1, kBarV = 2, kBarS = 3, kBarO = 4 };
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  volatile int* abort = &s_abort;
+  // a wait whose outcome is the same on every lane of the warp
+  auto wait_warp = [&](int b, uint32_t parity, int site) {
+    return __all_sync(0xffffffffu, wait_or_abort(bar(b), parity, a, abort, site)) != 0;
+  };
 
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(bar_of[i], 1);
+    mbar_init(bar(C::kBarQ), 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(bar(C::kBarKF + i), 1);
+      mbar_init(bar(C::kBarKE + i), 1);
+      mbar_init(bar(C::kBarVF + i), 1);
+      mbar_init(bar(C::kBarVE + i), 1);
+    }
+    for (int i = 0; i < 2 * kQTiles; ++i) {
+      mbar_init(bar(C::kBarSF + i), 1);
+      mbar_init(bar(C::kBarPF + i), 256);
+      mbar_init(bar(C::kBarPV + i), 1);
+      mbar_init(bar(C::kBarX + i), 256);
+    }
+    for (int i = 0; i < kQTiles; ++i) mbar_init(bar(C::kBarL + i), 256);
+    mbar_init(bar(C::kBarFin), 1);
+    s_abort = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmap_q);
     prefetch_tensormap(&tmap_k);
@@ -159,188 +256,302 @@ __global__ void __launch_bounds__(kThreadsP, 2)
   __syncthreads();
   tcgen05_after_sync();
   const uint32_t tmem = s_tmem;
-  const uint32_t t_s = tmem, t_o = tmem + C::kOcol;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 
-  // Phases armed (by thread 0) and observed (by everyone) per barrier: at
-  // most one phase of each is outstanding at any time, which is what a
-  // timed-out CTA waits for before it leaves.
-  int armed[5] = {0, 0, 0, 0, 0}, seen[5] = {0, 0, 0, 0, 0};
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar_of[kBarQ], C::kHalves * kQHalf);
+  // phases of the Q, K and V barriers this CTA armed: what a CTA that gives up
+  // waits for before its shared memory goes
+  int armed_q = 0, armed_k[NS], armed_v[NS];
 #pragma unroll
-    for (int h = 0; h < C::kHalves; ++h)
-      tma_load_3d(base + C::kQ + h * kQHalf, &tmap_q, h * 64, kvh * G, c0 + q0,
-                  bar_of[kBarQ]);
-    load_kv_tile<D>(&tmap_k, a, bt, kvh, 0, kv_end, base + C::kK, bar_of[kBarK]);
-    load_kv_tile<D>(&tmap_v, a, bt, kvh, 0, kv_end, base + C::kV, bar_of[kBarV]);
-    armed[kBarQ] = armed[kBarK] = armed[kBarV] = 1;
-  }
+  for (int i = 0; i < NS; ++i) armed_k[i] = armed_v[i] = 0;
 
-  // this thread's row: query qi (within the chunk) and head r % G of the group
-  const int r = tid;
-  const int qi = q0 + r / G;
-  const bool row_valid = (r / G) < qn;
-  const int limit = row_valid ? (L - c + qi + 1) : 1;  // number of visible keys
-  float m = -INFINITY, l = 0.f;
-  int fail_site = 0;
-
-  // Waits for the next phase of barrier `b` on every thread; the result is
-  // the same on every thread of the CTA.
-  auto wait = [&](int b) {
-    const bool landed = mbar_wait_bounded(bar_of[b], seen[b] & 1, a.timeout_ns, a.force_timeout);
-    if (!landed) fail_site = b + 1;
-    const bool all = __syncthreads_and(landed) != 0;
-    if (all) ++seen[b];
-    return all;
-  };
-
-  bool ok = wait(kBarQ);
-  for (int kt = 0; ok && kt < nkt; ++kt) {
-    const int key0 = kt * kKeys;
-    ok = wait(kBarK);
-    if (!ok) break;
-    if (tid == 0) {
-      tcgen05_after_sync();
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t koff = (kk & 3) * 32;
-        umma_bf16(t_s, umma_desc_sw128(base + C::kQ + (kk >> 2) * kQHalf + koff, 16, 1024),
-                  umma_desc_sw128(base + C::kK + (kk >> 2) * kKVHalf + koff, 16, 1024), kIdescS,
-                  kk > 0 ? 1u : 0u);
-      }
-      umma_commit(bar_of[kBarS]);
-      ++armed[kBarS];
-    }
-    ok = wait(kBarS);
-    if (!ok) break;
-    tcgen05_after_sync();
-    if (tid == 0 && kt + 1 < nkt) {
-      load_kv_tile<D>(&tmap_k, a, bt, kvh, key0 + kKeys, kv_end, base + C::kK, bar_of[kBarK]);
-      ++armed[kBarK];
-    }
-
-    // ---- softmax on this thread's row
-    float x[kKeys];
-#pragma unroll
-    for (int c32 = 0; c32 < kKeys / 32; ++c32) {
-      uint32_t rr[32];
-      tmem_ld32(t_s + lane_off + c32 * 32, rr);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) x[c32 * 32 + i] = __uint_as_float(rr[i]) * a.scale_log2;
-    }
-    const int vis = min(kKeys, limit - key0);  // visible columns of this tile (may be <= 0)
-    float mx = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kKeys; ++i)
-      if (i < vis) mx = fmaxf(mx, x[i]);
-    const float m_new = fmaxf(m, mx);          // finite: tile 0 always shows key 0
-    const float alpha = fast_exp2(m - m_new);  // 0 on the first tile
-    float sum = 0.f;
-    uint8_t* phi = base_ptr + C::kPhi;
-    uint8_t* plo = base_ptr + C::kPlo;
-#pragma unroll
-    for (int ch = 0; ch < kKeys / 8; ++ch) {
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i0 = ch * 8 + 2 * e;
-        const float p0 = i0 < vis ? fast_exp2(x[i0] - m_new) : 0.f;
-        const float p1 = i0 + 1 < vis ? fast_exp2(x[i0 + 1] - m_new) : 0.f;
-        sum += p0 + p1;
-        hi[e] = pack_bf16x2(p0, p1);
-        lo[e] = pack_bf16x2(p0 - bf16_lo_to_f32(hi[e]), p1 - bf16_hi_to_f32(hi[e]));
-      }
-      const uint32_t off = swz128(r, ch);  // 64 keys: one 128-byte row per row
-      *reinterpret_cast<uint4*>(phi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(plo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-    l = l * alpha + sum;
-    m = m_new;
-    if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-      for (int c32 = 0; c32 < D / 32; ++c32) {
-        uint32_t rr[32];
-        tmem_ld32(t_o + lane_off + c32 * 32, rr);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-        tmem_st32(t_o + lane_off + c32 * 32, rr);
-      }
-      tmem_wait_st();
-    }
-
-    ok = wait(kBarV);
-    if (!ok) break;
-    if (key0 + kKeys > kv_end && r < kKeys && r >= kv_end - key0) {
-      // keys past the last visible one: their value rows (unloaded pages, or
-      // slots past the sequence end) must not reach O, not even as NaN * 0
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // Page numbers come from a window of the block table held in shared
+    // memory (refilled by the whole warp), so no tile's loads wait for a
+    // global read; K runs one tile ahead of V, the order in which the tensor
+    // core needs them.
+    const int B = a.block_size, ppt = kKeys / B;  // pages per tile
+    const int npages = (kv_end + B - 1) / B;
+    int win0 = 0;
+    for (int i = lane; i < kWin && i < npages; i += 32) s_pages[i] = __ldg(bt + i);
+    __syncwarp();
+    // Loads key or value tile t: lane k issues box k (page k / halves, column
+    // half k % halves), so the boxes of a tile leave the warp together.
+    auto issue = [&](const CUtensorMap* map, int t, uint32_t dst, uint32_t fbar) {
+      const int p0 = t * ppt, np = min(ppt, npages - p0);
+      const bool mine = lane < np * C::kHalves;
+      const int pg = lane / C::kHalves, hh = lane % C::kHalves;
+      const int32_t blk = mine ? s_pages[p0 + pg - win0] : -1;
+      const bool valid = mine && blk >= 0 && blk < a.num_blocks;
+      const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+      if (lane == 0) mbar_arrive_expect_tx(fbar, nvalid * B * 128u);
+      __syncwarp();
+      if (mine && !valid) record_status(a.status, PKV_EDEVICE, blk, kKernelPrefill);
+      if (valid)
+        tma_load_2d(dst + hh * kKVHalf + pg * B * 128, map, hh * 64, (blk * a.Hkv + kvh) * B,
+                    fbar);
+    };
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(C::kBarQ), C::kHalves * kQHalf);
 #pragma unroll
       for (int h = 0; h < C::kHalves; ++h)
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(base_ptr + C::kV + h * kKVHalf + r * 128 + ch * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
+        tma_load_3d(base + C::kQ + h * kQHalf, &tmap_q, h * 64, kvh * G, c0 + q0, bar(C::kBarQ));
+      armed_q = 1;
     }
-    fence_proxy_async_smem();  // P and zeroed V rows before the tensor core reads them
-    tcgen05_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-      tcgen05_after_sync();
-#pragma unroll
-      for (int kk = 0; kk < kKeys / 16; ++kk) {
-        const uint32_t poff = kk * 32;
-        const uint64_t vdesc = umma_desc_sw128(base + C::kV + kk * 16 * 128, kKVHalf, 1024);
-        umma_bf16(t_o, umma_desc_sw128(base + C::kPhi + poff, 16, 1024), vdesc, kIdescO,
-                  (kt > 0 || kk > 0) ? 1u : 0u);
-        umma_bf16(t_o, umma_desc_sw128(base + C::kPlo + poff, 16, 1024), vdesc, kIdescO, 1u);
+    bool ok = true;
+    for (int j = 0; ok && j <= nkt; ++j) {
+      if (j < nkt) {
+        if (min((j + 1) * ppt, npages) > win0 + kWin) {
+          // slide the window: tile j-1 (whose values are still to load) and on
+          win0 = (j - 1) * ppt;
+          __syncwarp();
+          for (int i = lane; i < kWin && win0 + i < npages; i += 32)
+            s_pages[i] = __ldg(bt + win0 + i);
+          __syncwarp();
+        }
+        const int st = j % NS, u = j / NS;
+        if (j >= NS) ok = wait_warp(C::kBarKE + st, (u - 1) & 1, 1);
+        if (!ok) break;
+        issue(&tmap_k, j, base + C::kK + st * C::kStage, bar(C::kBarKF + st));
+        ++armed_k[st];
       }
-      umma_commit(bar_of[kBarO]);
-      ++armed[kBarO];
+      if (j >= 1) {
+        const int i = j - 1, st = i % NS, u = i / NS;
+        if (i >= NS) ok = wait_warp(C::kBarVE + st, (u - 1) & 1, 2);
+        if (!ok) break;
+        issue(&tmap_v, i, base + C::kV + st * C::kStage, bar(C::kBarVF + st));
+        ++armed_v[st];
+      }
+      __syncwarp();
     }
-    ok = wait(kBarO);
-    if (!ok) break;
-    tcgen05_after_sync();
-    if (tid == 0 && kt + 1 < nkt) {
-      load_kv_tile<D>(&tmap_v, a, bt, kvh, key0 + kKeys, kv_end, base + C::kV, bar_of[kBarV]);
-      ++armed[kBarV];
-    }
-  }
-
-  if (ok) {
-    // ---- epilogue: O / l -> bf16, row r -> (query qi, head kvh*G + r%G)
-    const float inv = 1.f / l;
-    __nv_bfloat16* orow = a.out + ((int64_t)(c0 + qi) * a.Hq + kvh * G + (r % G)) * D;
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ tensor core
+    // Order: S_0(j), S_1(j), then P_0(j-1) V, P_1(j-1) V; the scores of both Q
+    // tiles for the next key tile are computed while their softmax runs.
+    bool ok = wait_warp(C::kBarQ, 0, 3);
+    for (int j = 0; ok && j <= nkt; ++j) {
+      if (j < nkt) {
+        const int st = j % NS, u = j / NS, b = j & 1;
+        ok = wait_warp(C::kBarKF + st, u & 1, 4);
+        if (!ok) break;
+        tcgen05_after_sync();
+        if (lane == 0) {
+          const uint32_t kbase = base + C::kK + st * C::kStage;
 #pragma unroll
-    for (int c32 = 0; c32 < D / 32; ++c32) {
-      uint32_t rr[32];
-      tmem_ld32(t_o + lane_off + c32 * 32, rr);
+          for (int t = 0; t < kQTiles; ++t) {
+            if (j >= nkt_t[t]) continue;
+            const uint32_t qbase = base + C::kQ + t * kRows * 128;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff = (kk & 3) * 32;
+              umma_bf16(tmem + t * 256 + b * kKeys,
+                        umma_desc_sw128(qbase + (kk >> 2) * kQHalf + koff, 16, 1024),
+                        umma_desc_sw128(kbase + (kk >> 2) * kKVHalf + koff, 16, 1024), kIdescS,
+                        kk > 0 ? 1u : 0u);
+            }
+            umma_commit(bar(C::kBarSF + 2 * t + b));
+          }
+          umma_commit(bar(C::kBarKE + st));
+        }
+        __syncwarp();
+      }
+      if (j >= 1) {
+        const int i = j - 1, st = i % NS, u = i / NS, b = i & 1;
+        ok = wait_warp(C::kBarVF + st, u & 1, 6);
+        if (!ok) break;
+        const int key0 = i * kKeys;
+        const uint32_t vbase = base + C::kV + st * C::kStage;
+        if (key0 + kKeys > kv_end) {
+          // value rows past the last visible key: stale or poisoned bytes that
+          // must not reach O, not even as NaN * 0
+          uint8_t* vp = base_ptr + C::kV + st * C::kStage;
+          for (int r = kv_end - key0 + lane; r < kKeys; r += 32)
+#pragma unroll
+            for (int h = 0; h < C::kHalves; ++h)
+#pragma unroll
+              for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4*>(vp + h * kKVHalf + r * 128 + ch * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < kQTiles; ++t) {
+          if (i >= nkt_t[t]) continue;
+          ok = wait_warp(C::kBarPF + 2 * t + b, (i >> 1) & 1, 5);
+          if (!ok) break;
+          tcgen05_after_sync();
+          if (lane == 0) {
+            const uint32_t p = tmem + t * 256 + b * kKeys;
+            const uint32_t o = tmem + t * 256 + 128;
+#pragma unroll
+            for (int kk = 0; kk < kKeys / 16; ++kk) {
+              const uint64_t vdesc = umma_desc_sw128(vbase + kk * 16 * 128, kKVHalf, 1024);
+              umma_bf16_ts(o, p + kk * 8, vdesc, kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
+              umma_bf16_ts(o, p + 32 + kk * 8, vdesc, kIdescO, 1u);
+            }
+            umma_commit(bar(C::kBarPV + 2 * t + b));
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) umma_commit(bar(C::kBarVE + st));
+        __syncwarp();
+      }
+    }
+    // every MMA (and the arrivals it triggers) is done before the CTA leaves
+    if (lane == 0) {
+      umma_commit(bar(C::kBarFin));
+      mbar_wait_bounded(bar(C::kBarFin), 0, 4 * a.timeout_ns, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    // Eight warps per Q tile: each TMEM lane (= row) is shared by two threads,
+    // one per half of the 64 key columns (and of the D output columns); the
+    // two exchange their row maxima through shared memory once per tile.
+    const int sw = warp - 2;
+    const int t = sw >> 3;            // Q tile of this warp
+    const int h = (sw >> 2) & 1;      // key half (columns 32h .. 32h+31)
+    const int nk = nkt_t[t];
+    const int quarter = warp & 3;     // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t t_o = tmem + t * 256 + 128 + lane_off + h * (D / 2);
+    const int qi = q0 + t * QT + r / G;
+    const bool row_valid = qi < c;
+    const int limit = row_valid ? (L - c + qi + 1) : 1;  // number of visible keys
+    const uint64_t scale2 = f32x2_pack(a.scale_log2, a.scale_log2);
+    float m_ref = 0.f;
+    uint64_t l2 = f32x2_pack(0.f, 0.f);  // this thread's share of the row sum, two lanes
+    bool ok = true;
+    for (int j = 0; j < nk; ++j) {
+      const int b = j & 1, key0 = j * kKeys + 32 * h;
+      ok = wait_warp(C::kBarSF + 2 * t + b, (j >> 1) & 1, 7);
+      if (!ok) break;
+      tcgen05_after_sync();
+      const uint32_t t_s = tmem + t * 256 + lane_off + b * kKeys;
+      uint32_t x[32];
+      tmem_ld32(t_s + 32 * h, x);
       tmem_wait_ld();
-      if (row_valid) {
+      const int vis = min(32, limit - key0);  // visible columns of this half (may be <= 0)
+      const bool full = __all_sync(0xffffffffu, vis >= 32) != 0;
+      if (!full) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-          uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(rr[i + 0]) * inv, __uint_as_float(rr[i + 1]) * inv);
-          v.y = pack_bf16x2(__uint_as_float(rr[i + 2]) * inv, __uint_as_float(rr[i + 3]) * inv);
-          v.z = pack_bf16x2(__uint_as_float(rr[i + 4]) * inv, __uint_as_float(rr[i + 5]) * inv);
-          v.w = pack_bf16x2(__uint_as_float(rr[i + 6]) * inv, __uint_as_float(rr[i + 7]) * inv);
-          *reinterpret_cast<uint4*>(orow + c32 * 32 + i) = v;
+        for (int i = 0; i < 32; ++i)
+          if (i >= vis) x[i] = __float_as_uint(-INFINITY);
+      }
+      float m4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        m4[e] = fmax3(__uint_as_float(x[8 * e]), __uint_as_float(x[8 * e + 1]),
+                      fmax3(__uint_as_float(x[8 * e + 2]), __uint_as_float(x[8 * e + 3]),
+                            fmax3(__uint_as_float(x[8 * e + 4]), __uint_as_float(x[8 * e + 5]),
+                                  fmax3(__uint_as_float(x[8 * e + 6]),
+                                        __uint_as_float(x[8 * e + 7]), -INFINITY))));
+      const float mine = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+      s_xmax[t][b][h][r] = mine;
+      mbar_arrive(bar(C::kBarX + 2 * t + b));
+      ok = wait_warp(C::kBarX + 2 * t + b, (j >> 1) & 1, 10);
+      if (!ok) break;
+      const float m_tile = fmaxf(mine, s_xmax[t][b][h ^ 1][r]) * a.scale_log2;  // -inf: none visible
+      if (j == 0) m_ref = m_tile;  // key 0 is visible to every row
+      const bool need = m_tile > m_ref + kRescaleLog2;
+      if (__any_sync(0xffffffffu, need)) {
+        // O must be complete up to tile j-1 before it is rescaled
+        ok = wait_warp(C::kBarPV + 2 * t + ((j - 1) & 1), ((j - 1) >> 1) & 1, 8);
+        if (!ok) break;
+        tcgen05_after_sync();
+        const float alpha = need ? fast_exp2(m_ref - m_tile) : 1.f;
+        if (need) m_ref = m_tile;
+        l2 = f32x2_mul(l2, f32x2_pack(alpha, alpha));
+#pragma unroll 1
+        for (int c32 = 0; c32 < D / 64; ++c32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c32 * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(t_o + c32 * 32, o);
+        }
+      }
+      // p = 2^(x scale - m_ref) for two columns at a time, split into bf16
+      // hi + lo parts; masked columns hold -inf and give 0
+      const uint64_t negm = f32x2_pack(-m_ref, -m_ref);
+      uint32_t hi[16], lo[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float y0, y1;
+        f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])),
+                               scale2, negm), y0, y1);
+        const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+        const uint64_t p = f32x2_pack(p0, p1);
+        l2 = f32x2_add(l2, p);
+        hi[e] = pack_bf16x2(p0, p1);
+        float d0, d1;
+        f32x2_unpack(f32x2_sub(p, f32x2_pack(bf16_lo_to_f32(hi[e]), bf16_hi_to_f32(hi[e]))), d0,
+                     d1);
+        lo[e] = pack_bf16x2(d0, d1);
+      }
+      tmem_st16(t_s + 16 * h, hi);
+      tmem_st16(t_s + 32 + 16 * h, lo);
+      tmem_wait_st();
+      tcgen05_before_sync();
+      mbar_arrive(bar(C::kBarPF + 2 * t + b));
+    }
+    if (ok && nk > 0)
+      ok = wait_warp(C::kBarPV + 2 * t + ((nk - 1) & 1), ((nk - 1) >> 1) & 1, 9);
+    if (ok && nk > 0) {
+      // ---- epilogue: O / l -> bf16, row r -> (query qi, head kvh*G + r%G);
+      // this thread writes its half of the D columns
+      float l0, l1;
+      f32x2_unpack(l2, l0, l1);
+      s_lsum[t][h][r] = l0 + l1;
+      mbar_arrive(bar(C::kBarL + t));
+      ok = wait_warp(C::kBarL + t, 0, 11);
+    }
+    if (ok && nk > 0) {
+      const float inv = 1.f / (s_lsum[t][0][r] + s_lsum[t][1][r]);
+      tcgen05_after_sync();
+      __nv_bfloat16* orow =
+          a.out + ((int64_t)(c0 + qi) * a.Hq + kvh * G + (r % G)) * D + h * (D / 2);
+#pragma unroll 1
+      for (int c32 = 0; c32 < D / 64; ++c32) {
+        uint32_t o[32];
+        tmem_ld32(t_o + c32 * 32, o);
+        tmem_wait_ld();
+        if (row_valid) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c32 * 32 + e) = v;
+          }
         }
       }
     }
-  } else {
-    if (fail_site) record_status(a.status, PKV_ETIMEOUT, fail_site, kKernelPrefill);
-    // Let this CTA's own copies and MMAs land before its shared and tensor
-    // memory are released: wait (again with a limit) for each armed phase
-    // that nobody has observed yet.
-    if (tid == 0) {
-      for (int b = 0; b < 5; ++b)
-        if (armed[b] > seen[b]) mbar_wait_bounded(bar_of[b], seen[b] & 1, 4 * a.timeout_ns, 0);
-    }
   }
+
   tcgen05_before_sync();
   __syncthreads();
+  if (*abort) {
+    if (tid == 0) record_status(a.status, PKV_ETIMEOUT, *abort, kKernelPrefill);
+    // Let this CTA's own copies land before its shared memory is released:
+    // wait (again with a limit) for the last phase armed on each barrier.
+    if (tid == 0) {
+      if (armed_q) mbar_wait_bounded(bar(C::kBarQ), 0, 4 * a.timeout_ns, 0);
+      for (int i = 0; i < NS; ++i) {
+        if (armed_k[i]) mbar_wait_bounded(bar(C::kBarKF + i), (armed_k[i] - 1) & 1,
+                                          4 * a.timeout_ns, 0);
+        if (armed_v[i]) mbar_wait_bounded(bar(C::kBarVF + i), (armed_v[i] - 1) & 1,
+                                          4 * a.timeout_ns, 0);
+      }
+    }
+    __syncthreads();
+  }
   if (warp == 0) {
     tcgen05_after_sync();
     tmem_dealloc(tmem, C::kTmemCols);
@@ -350,17 +561,18 @@ __global__ void __launch_bounds__(kThreadsP, 2)
 template <int D, int G>
 int launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    const PrefillArgs& a, int max_q_len, cudaStream_t stream) {
-  using C = PCfg<D>;
+  constexpr int NS = 3;
+  using C = PCfg<D, NS>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, []() {
-    attr_err = cudaFuncSetAttribute(paged_prefill_kernel<D, G>,
+    attr_err = cudaFuncSetAttribute(paged_prefill_kernel<D, G, NS>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "prefill kernel attributes");
-  constexpr int QT = kRows / G;
-  dim3 grid((unsigned)((max_q_len + QT - 1) / QT), (unsigned)a.Hkv, (unsigned)a.S);
-  paged_prefill_kernel<D, G><<<grid, kThreadsP, C::kSmem, stream>>>(tq, tk, tv, a);
+  constexpr int QC = kQTiles * kRows / G;  // queries per CTA
+  dim3 grid((unsigned)((max_q_len + QC - 1) / QC), (unsigned)a.Hkv, (unsigned)a.S);
+  paged_prefill_kernel<D, G, NS><<<grid, kThreadsP, C::kSmem, stream>>>(tq, tk, tv, a);
   return check_launch("prefill");
 }
 
@@ -416,7 +628,7 @@ extern "C" int pkv_paged_attention_prefill(void* out, const void* q, const int32
   {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)total_q};
     const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)Hq * D * 2};
-    const uint32_t box[3] = {64, (uint32_t)G, (uint32_t)(kRows / G)};
+    const uint32_t box[3] = {64, (uint32_t)G, (uint32_t)(kQTiles * kRows / G)};
     if (int rc = encode_tile_map_3d(&tq, q, dims, strides, box)) return rc;
   }
   const uint64_t rows = (uint64_t)num_blocks * Hkv * block_size;
