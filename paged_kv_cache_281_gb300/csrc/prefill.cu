@@ -170,6 +170,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// One lane of the warp, chosen by the hardware; the branch it guards stays
+// warp-uniform for the compiler, so the tcgen05 operands stay in uniform
+// registers (a lane-index test made the MMA issue markedly slower).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 template <int D, int G, int NS>
 __global__ void __launch_bounds__(kThreadsP, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -204,16 +215,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   }
   // Q tile t holds queries q0 + t QT .. + QT - 1 of the chunk; its rows see
   // keys below kv_end_t, i.e. nkt_t key tiles (0 when it has no query)
-  int nkt_t[kQTiles];
-  int kv_end = 0;
-#pragma unroll
-  for (int t = 0; t < kQTiles; ++t) {
-    const int qn = max(0, min(QT, c - (q0 + t * QT)));
-    const int e = L - c + q0 + t * QT + qn;
-    nkt_t[t] = qn > 0 ? (e + kKeys - 1) / kKeys : 0;
-    if (qn > 0) kv_end = e;
-  }
+  static_assert(kQTiles == 2, "two Q tiles per CTA");
+  const int qn1 = max(0, min(QT, c - (q0 + QT)));
+  const int kv_end0 = L - c + q0 + min(QT, c - q0);
+  const int kv_end = qn1 > 0 ? L - c + q0 + QT + qn1 : kv_end0;
+  const int nkt0 = (kv_end0 + kKeys - 1) / kKeys;
+  const int nkt1 = qn1 > 0 ? (kv_end + kKeys - 1) / kKeys : 0;
   const int nkt = (kv_end + kKeys - 1) / kKeys;
+  auto nkt_t = [&](int t) { return t == 0 ? nkt0 : nkt1; };
   const int32_t* bt = a.block_tables + (int64_t)s * a.max_blocks_per_seq;
 
   const uint32_t raw = smem_u32(dsm);
@@ -257,11 +266,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   tcgen05_after_sync();
   const uint32_t tmem = s_tmem;
 
-  // phases of the Q, K and V barriers this CTA armed: what a CTA that gives up
-  // waits for before its shared memory goes
-  int armed_q = 0, armed_k[NS], armed_v[NS];
-#pragma unroll
-  for (int i = 0; i < NS; ++i) armed_k[i] = armed_v[i] = 0;
+  // loads this CTA issued (Q, and K and V tiles, counted by the producer):
+  // what a CTA that gives up waits for before its shared memory goes
+  int armed_q = 0, issued_k = 0, issued_v = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -312,14 +319,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         if (j >= NS) ok = wait_warp(C::kBarKE + st, (u - 1) & 1, 1);
         if (!ok) break;
         issue(&tmap_k, j, base + C::kK + st * C::kStage, bar(C::kBarKF + st));
-        ++armed_k[st];
+        ++issued_k;
       }
       if (j >= 1) {
         const int i = j - 1, st = i % NS, u = i / NS;
         if (i >= NS) ok = wait_warp(C::kBarVE + st, (u - 1) & 1, 2);
         if (!ok) break;
         issue(&tmap_v, i, base + C::kV + st * C::kStage, bar(C::kBarVF + st));
-        ++armed_v[st];
+        ++issued_v;
       }
       __syncwarp();
     }
@@ -328,6 +335,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     // ------------------------------------------------------------ tensor core
     // Order: S_0(j), S_1(j), then P_0(j-1) V, P_1(j-1) V; the scores of both Q
     // tiles for the next key tile are computed while their softmax runs.
+    // shared-memory descriptors of the first Q, K and V tiles; the others
+    // differ only in the start address field (bytes / 16)
+    const uint64_t dq = umma_desc_sw128(base + C::kQ, 16, 1024);
+    const uint64_t dk = umma_desc_sw128(base + C::kK, 16, 1024);
+    const uint64_t dv = umma_desc_sw128(base + C::kV, kKVHalf, 1024);
     bool ok = wait_warp(C::kBarQ, 0, 3);
     for (int j = 0; ok && j <= nkt; ++j) {
       if (j < nkt) {
@@ -335,18 +347,16 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         ok = wait_warp(C::kBarKF + st, u & 1, 4);
         if (!ok) break;
         tcgen05_after_sync();
-        if (lane == 0) {
-          const uint32_t kbase = base + C::kK + st * C::kStage;
+        if (elect_one()) {
+          const uint64_t dks = dk + ((st * C::kStage) >> 4);
 #pragma unroll
           for (int t = 0; t < kQTiles; ++t) {
-            if (j >= nkt_t[t]) continue;
-            const uint32_t qbase = base + C::kQ + t * kRows * 128;
+            if (j >= nkt_t(t)) continue;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t koff = (kk & 3) * 32;
-              umma_bf16(tmem + t * 256 + b * kKeys,
-                        umma_desc_sw128(qbase + (kk >> 2) * kQHalf + koff, 16, 1024),
-                        umma_desc_sw128(kbase + (kk >> 2) * kKVHalf + koff, 16, 1024), kIdescS,
+              const uint32_t koff = (kk >> 2) * kKVHalf + (kk & 3) * 32;
+              const uint32_t qoff = t * kRows * 128 + (kk >> 2) * kQHalf + (kk & 3) * 32;
+              umma_bf16(tmem + t * 256 + b * kKeys, dq + (qoff >> 4), dks + (koff >> 4), kIdescS,
                         kk > 0 ? 1u : 0u);
             }
             umma_commit(bar(C::kBarSF + 2 * t + b));
@@ -360,7 +370,6 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         ok = wait_warp(C::kBarVF + st, u & 1, 6);
         if (!ok) break;
         const int key0 = i * kKeys;
-        const uint32_t vbase = base + C::kV + st * C::kStage;
         if (key0 + kKeys > kv_end) {
           // value rows past the last visible key: stale or poisoned bytes that
           // must not reach O, not even as NaN * 0
@@ -377,16 +386,17 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         __syncwarp();
 #pragma unroll
         for (int t = 0; t < kQTiles; ++t) {
-          if (i >= nkt_t[t]) continue;
+          if (i >= nkt_t(t)) continue;
           ok = wait_warp(C::kBarPF + 2 * t + b, (i >> 1) & 1, 5);
           if (!ok) break;
           tcgen05_after_sync();
-          if (lane == 0) {
+          if (elect_one()) {
             const uint32_t p = tmem + t * 256 + b * kKeys;
             const uint32_t o = tmem + t * 256 + 128;
+            const uint64_t dvs = dv + ((st * C::kStage) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kKeys / 16; ++kk) {
-              const uint64_t vdesc = umma_desc_sw128(vbase + kk * 16 * 128, kKVHalf, 1024);
+              const uint64_t vdesc = dvs + ((kk * 16 * 128) >> 4);
               umma_bf16_ts(o, p + kk * 8, vdesc, kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
               umma_bf16_ts(o, p + 32 + kk * 8, vdesc, kIdescO, 1u);
             }
@@ -395,7 +405,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           __syncwarp();
         }
         if (!ok) break;
-        if (lane == 0) umma_commit(bar(C::kBarVE + st));
+        if (elect_one()) umma_commit(bar(C::kBarVE + st));
         __syncwarp();
       }
     }
@@ -413,7 +423,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     const int sw = warp - 2;
     const int t = sw >> 3;            // Q tile of this warp
     const int h = (sw >> 2) & 1;      // key half (columns 32h .. 32h+31)
-    const int nk = nkt_t[t];
+    const int nk = nkt_t(t);
     const int quarter = warp & 3;     // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -544,10 +554,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     if (tid == 0) {
       if (armed_q) mbar_wait_bounded(bar(C::kBarQ), 0, 4 * a.timeout_ns, 0);
       for (int i = 0; i < NS; ++i) {
-        if (armed_k[i]) mbar_wait_bounded(bar(C::kBarKF + i), (armed_k[i] - 1) & 1,
-                                          4 * a.timeout_ns, 0);
-        if (armed_v[i]) mbar_wait_bounded(bar(C::kBarVF + i), (armed_v[i] - 1) & 1,
-                                          4 * a.timeout_ns, 0);
+        // tiles i, i + NS, ... went to stage i: wait for the last one's phase
+        const int nk = issued_k > i ? (issued_k - 1 - i) / NS + 1 : 0;
+        const int nv = issued_v > i ? (issued_v - 1 - i) / NS + 1 : 0;
+        if (nk) mbar_wait_bounded(bar(C::kBarKF + i), (nk - 1) & 1, 4 * a.timeout_ns, 0);
+        if (nv) mbar_wait_bounded(bar(C::kBarVF + i), (nv - 1) & 1, 4 * a.timeout_ns, 0);
       }
     }
     __syncthreads();
