@@ -12,6 +12,8 @@ from the pages on continuous batching and PagedAttention:
                   request's own tokens ("Deep Dive: continuous batching",
                   section *Selective batching*), for one decode query per
                   sequence and for a causal prompt chunk.
+* ``fp8``       — e4m3 pages with per-row scales: quantisation of new rows
+                  and decode attention over the dequantised pages.
 
 Only the test-suite, the package's smoke check and the benchmark's CPU
 baseline may import this package.  The library never calls it, and it shares
@@ -19,6 +21,6 @@ no code with the library: it reads the same memory layout through its own
 indexing.
 """
 
-from . import attention, cache, paging
+from . import attention, cache, fp8, paging
 
-__all__ = ["attention", "cache", "paging"]
+__all__ = ["attention", "cache", "fp8", "paging"]

@@ -30,7 +30,7 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle import attention, cache, paging
+from oracle import attention, cache, fp8, paging
 from tests.oracle_side import build_decode_state, build_shared_prefix_state, empty_pools
 from workloads import config1, config4, make_decode_workload, normal_bf16
 
@@ -444,12 +444,91 @@ def pin_swap_round_trip():
     assert np.array_equal(after, before)
 
 
+def pin_e4m3_against_torch():
+    """torch's float8_e4m3fn conversion (an independent implementation of the
+    same format, round to nearest even) agrees code for code inside the range
+    where it does not turn to NaN, and value for value on all 256 codes."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(81)
+    x = np.concatenate([
+        (rng.standard_normal(100000) * 40).astype(np.float32),
+        (rng.standard_normal(20000) * 0.01).astype(np.float32),
+        # exact midpoints between neighbouring codes, where ties decide
+        ((fp8.e4m3_decode(np.arange(0, 126)) + fp8.e4m3_decode(np.arange(1, 127))) / 2
+         ).astype(np.float32),
+        np.float32([0.0, -0.0, 448.0, -448.0, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -10]),
+    ])
+    x = x[np.abs(x) < 464]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(fp8.e4m3_encode(x), want)
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = fp8.e4m3_decode(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)])
+
+
+def pin_e4m3_closed_forms():
+    """Round trip of every finite code, saturation, and hand-worked ties."""
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    assert np.array_equal(fp8.e4m3_encode(fp8.e4m3_decode(codes).astype(np.float32)), codes)
+    assert fp8.e4m3_encode(np.float32([1000.0, -1e9, 449.0])).tolist() == [0x7E, 0xFE, 0x7E]
+    assert fp8.e4m3_decode(np.uint8([0x7E, 0x38, 0x01, 0x08, 0x3A])).tolist() == \
+        [448.0, 1.0, 2.0 ** -9, 2.0 ** -6, 1.25]
+    # 1 + 1/16 lies halfway between 1 (mantissa 000) and 1.125 (001): even wins
+    # 1 + 3/16 lies halfway between 1.125 (001) and 1.25 (010): even wins
+    assert fp8.e4m3_encode(np.float32([1.0625, 1.1875, -1.0625])).tolist() == [0x38, 0x3A, 0xB8]
+
+
+def pin_fp8_quantize_rows():
+    """Zero rows, single-value rows and the relative error bound of e4m3."""
+    D = 64
+    rows = np.zeros((3, D), dtype=np.uint16)
+    one = attention.widen_bf16(np.uint16([0x3FC0]))[0]            # 1.5
+    rows[1, 5] = 0x3FC0
+    rows[2] = normal_bf16((D,), 82)
+    codes, scales = fp8.quantize_rows(rows)
+    assert scales[0] == 0 and not codes[0].any()
+    assert codes[1, 5] == 0x7E and np.count_nonzero(codes[1]) == 1
+    assert scales[1] == np.float32(one) / np.float32(448.0)
+    x = attention.widen_bf16(rows[2])
+    deq = fp8.e4m3_decode(codes[2]) * float(scales[2])
+    amax = np.max(np.abs(x))
+    # normal codes: half a mantissa step (2^-4 relative); subnormals: 2^-10 of amax
+    assert np.all(np.abs(deq - x) <= np.maximum(np.abs(x) * 2.0 ** -4, amax * 2.0 ** -10) * 1.001)
+
+
+def pin_fp8_decode_exact_values():
+    """K/V rows that e4m3 represents exactly (codes times a power of two, each
+    row reaching +-448 times it): the fp8 path equals the bf16 oracle."""
+    rng = np.random.default_rng(83)
+    w = tiny_gqa_workload(seed=84, lens=(5, 17, 33))
+    for arr in (w.k, w.v):
+        codes = rng.integers(0, 0x7E, size=arr.shape).astype(np.uint8)
+        codes[..., 0] = 0x7E
+        codes |= (rng.integers(0, 2, size=arr.shape) * 0x80).astype(np.uint8)
+        vals = fp8.e4m3_decode(codes) * 2.0 ** -6
+        arr[...] = (vals.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    st = build_decode_state(w)
+    ref = attention.decode(w.q, st.k_cache, st.v_cache, st.tables, w.context_lens, w.block_size,
+                           w.scale)
+    N, Hkv, B, D = st.k_cache.shape
+    k8, v8 = np.zeros((N, Hkv, B, D), np.uint8), np.zeros((N, Hkv, B, D), np.uint8)
+    ks, vs = np.zeros((N, Hkv, B), np.float32), np.zeros((N, Hkv, B), np.float32)
+    slots = np.concatenate([[st.tables[s][j // B] * B + j % B for j in range(w.context_lens[s])]
+                            for s in range(w.S)])
+    fp8.append(k8, v8, ks, vs, w.k, w.v, slots, B)
+    got = fp8.decode(w.q, k8, v8, ks, vs, st.tables, w.context_lens, B, w.scale)
+    assert np.array_equal(got, ref)
+
+
 PINS = [pin_widen_bf16, pin_decode_brute_force, pin_prefill_brute_force,
         pin_decode_torch_sdpa, pin_prefill_torch_sdpa, pin_single_key_returns_v,
         pin_closed_forms, pin_placement_invariance, pin_shared_equals_duplicated,
         pin_cow_isolation, pin_decode_equals_last_prefill_row, pin_append_gather_roundtrip,
         pin_poisoned_slots_unread, pin_allocator_golden, pin_allocator_fuzz,
-        pin_swap_round_trip, pin_prefix_cache_golden]
+        pin_swap_round_trip, pin_prefix_cache_golden, pin_e4m3_against_torch,
+        pin_e4m3_closed_forms, pin_fp8_quantize_rows, pin_fp8_decode_exact_values]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -578,7 +657,36 @@ def _mut_cached_whole_prompt(self, tokens):
     return sid, j * B
 
 
-_ORIG = {"attend": attention.attend, "swap_blocks": cache.swap_blocks, "widen": attention.widen_bf16,
+def _mut_e4m3_ties_away(x):
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    vals = fp8.e4m3_decode(np.arange(0, 127))
+    a = np.minimum(np.abs(x), 448.0)
+    hi = np.minimum(np.searchsorted(vals, a, side="left"), 126)
+    lo = np.maximum(hi - 1, 0)
+    idx = np.where(vals[hi] - a <= a - vals[lo], hi, lo)     # ties go up
+    out = idx.astype(np.uint8)
+    return np.where(np.signbit(x), out | 0x80, out).astype(np.uint8)
+
+
+def _mut_e4m3_bias8(codes):
+    return _ORIG["e4m3_decode"](codes) / 2.0
+
+
+def _mut_quantize_max_240(bits):
+    x = attention.widen_bf16(bits).astype(np.float32)
+    amax = np.max(np.abs(x), axis=-1).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        inv = np.where(amax > 0, np.float32(240.0) / amax, np.float32(0)).astype(np.float32)
+        scale = (amax / np.float32(240.0)).astype(np.float32)
+    return fp8.e4m3_encode((x * inv[..., None]).astype(np.float32)), scale
+
+
+def _mut_dequant_no_scale(codes, scales, table, length, block_size):
+    return _ORIG["dequantize_seq"](codes, np.ones_like(scales), table, length, block_size)
+
+
+_ORIG = {"attend": attention.attend, "e4m3_decode": fp8.e4m3_decode,
+         "dequantize_seq": fp8.dequantize_seq, "swap_blocks": cache.swap_blocks, "widen": attention.widen_bf16,
          "group": attention._group}
 
 MUTATIONS = {
@@ -602,6 +710,10 @@ MUTATIONS = {
                                       _mut_take_keeps_descendants),
     "prefix_cache_whole_prompt": (paging.BlockAllocator, "create_cached",
                                   _mut_cached_whole_prompt),
+    "e4m3_ties_away_from_zero": (fp8, "e4m3_encode", _mut_e4m3_ties_away),
+    "e4m3_exponent_bias_8": (fp8, "e4m3_decode", _mut_e4m3_bias8),
+    "fp8_quantise_to_240": (fp8, "quantize_rows", _mut_quantize_max_240),
+    "fp8_scales_ignored": (fp8, "dequantize_seq", _mut_dequant_no_scale),
 }
 
 
