@@ -54,9 +54,11 @@ def parse_args():
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--workload", choices=["llama3_8b_gqa", "trace", "swap", "prefix_cache"],
+    ap.add_argument("--workload", choices=["llama3_8b_gqa", "llama3_8b_gqa_fp8", "trace", "swap",
+                                           "prefix_cache"],
                     default="llama3_8b_gqa",
-                    help="trace: the 200-iteration continuous-batching workload; swap: "
+                    help="llama3_8b_gqa_fp8: the headline step over FP8 (e4m3) pages; "
+                         "trace: the 200-iteration continuous-batching workload; swap: "
                          "preemption by swapping, every block of the decode batch out to "
                          "pinned host memory and back; prefix_cache: 256 requests sharing a "
                          "1024-token system prompt, prefilled with and without the prefix "
@@ -584,6 +586,105 @@ def run_prefix_cache(args):
     return 0
 
 
+def run_fp8(args):
+    """The Llama-3-8B GQA decode step over FP8 (e4m3) pages with one fp32 scale
+    per token row: kv_append_fp8 of each sequence's newest token, then
+    decode_fp8 over all 256 sequences. Reports the bytes the decode must read
+    (codes and scales) per second and decode tokens per second."""
+    import torch
+    import paged_kv_cache_281_gb300 as pkv
+    from tests.gpu_harness import to_dev_bf16
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    w = workload_for_rank(rank)
+    N, Hkv, B, D = w.num_blocks, w.Hkv, w.block_size, w.D
+    k8, v8, ks, vs = pkv.new_fp8_pools(N, Hkv, B, D)
+    alloc = pkv.BlockAllocator(N, B, w.free_order)
+    seqs, slots = [], []
+    for L in w.context_lens:
+        sid = alloc.seq_create()
+        slots.append(alloc.seq_append_slots(sid, int(L))[0])
+        seqs.append(sid)
+    maxB = math.ceil(w.max_context_len / B)
+    tables, lens = alloc.build_block_tables(seqs, maxB)
+    status = pkv.new_status()
+    # every token but each sequence's newest is cached before the timed steps
+    cu = w.cu_lens
+    older = np.concatenate([np.arange(cu[i], cu[i + 1] - 1) for i in range(w.S)])
+    newest = cu[1:] - 1
+    slot_all = np.concatenate(slots).astype(np.int32)
+    pkv.pkv_kv_append_fp8(to_dev_bf16(w.k[older]), to_dev_bf16(w.v[older]),
+                          torch.from_numpy(slot_all[older]).cuda(), k8, v8, ks, vs, status=status)
+    k_last, v_last = to_dev_bf16(w.k[newest]), to_dev_bf16(w.v[newest])
+    last_slots = torch.from_numpy(slot_all[newest]).cuda()
+    q = to_dev_bf16(w.q)
+    out = torch.empty_like(q)
+    bt, ln = torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda()
+    ws = torch.empty(pkv.pkv_decode_workspace_bytes(w.S, w.Hq, D, w.max_context_len,
+                                                    args.partition_size),
+                     dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        pkv.pkv_kv_append_fp8(k_last, v_last, last_slots, k8, v8, ks, vs, status=status,
+                              stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        pkv.pkv_paged_attention_decode_fp8(out, q, k8, v8, ks, vs, bt, ln, w.max_context_len,
+                                           w.scale, ws, partition_size=args.partition_size,
+                                           status=status, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    pkv.pkv_check_status(status)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    pkv.pkv_check_status(status)
+    ms_per_step = max_over_ranks(start.elapsed_time(end)) / args.steps
+    decode_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    fp8_bytes = w.total_tokens * Hkv * 2 * (D + 4)
+    peak, peak_kind = measured_peaks()
+    achieved = fp8_bytes / (decode_ms * 1e-3) / 1e9
+    line = {
+        "metric": "paged decode attn over FP8 pages: KV bytes read GB/s (codes + scales); "
+                  "attention tokens/s per layer",
+        "value": world * fp8_bytes / (ms_per_step * 1e-3) / 1e9, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+f32",
+        "data": "synthetic",
+        "config": dict(workload_description(w, args.partition_size),
+                       workload="llama3_8b_gqa decode step over FP8 pages (kv_append_fp8 + "
+                                "paged decode attention fp8)",
+                       kv_bytes_per_step=fp8_bytes),
+        "attention_tokens_per_s_per_layer": world * w.S / (ms_per_step * 1e-3),
+        "bf16_equivalent_kv_gbs": world * w.kv_bytes() / (ms_per_step * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "pkv_paged_attention_decode_fp8 (plan + split-K "
+                     "partitions + combine)", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "algorithmic_bytes_per_launch": fp8_bytes,
+                     "avg_launch_ms": decode_ms},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks.summary(),
+        "cpu_baseline": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -592,6 +693,8 @@ def main():
         return run_trace(args)
     if args.workload == "swap":
         return run_swap(args)
+    if args.workload == "llama3_8b_gqa_fp8":
+        return run_fp8(args)
     if args.workload == "prefix_cache":
         return run_prefix_cache(args)
     import torch

@@ -231,7 +231,8 @@ int pkv_swap_blocks(void* k_cache, void* v_cache, const int32_t* blocks, int32_t
  *                  results do not depend on physical placement.
  *   workspace    : device scratch of pkv_decode_workspace_bytes() bytes.
  * Arithmetic: bf16 inputs, fp32 scores and accumulation, probabilities
- * rounded to bf16 for the P.V product, output rounded to bf16.
+ * entering the P.V product as two bf16 parts (hi + lo, ~2^-17 relative),
+ * output rounded to bf16.
  * ---------------------------------------------------------------------- */
 int pkv_decode_workspace_bytes(int32_t S, int32_t Hq, int32_t D, int32_t max_context_len,
                                int32_t partition_size, size_t* out);
@@ -284,7 +285,8 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_c
  *   context_lens : int32 [S] (device), after the chunk was appended.
  *   workspace    : pkv_prefill_workspace_bytes() bytes of device scratch.
  * QK^T and PV run on the tcgen05 tensor cores (bf16 operands, fp32
- * accumulation in tensor memory); probabilities are rounded to bf16.
+ * accumulation in tensor memory); probabilities enter the PV product as two
+ * bf16 parts (hi + lo, ~2^-17 relative).
  * ---------------------------------------------------------------------- */
 int pkv_prefill_workspace_bytes(int32_t S, int32_t total_q, int32_t Hq, int32_t D,
                                 size_t* out);
@@ -296,6 +298,42 @@ int pkv_paged_attention_prefill(void* out, const void* q, const int32_t* cu_q_le
                                 int32_t Hkv, int32_t D, int32_t block_size, int32_t num_blocks,
                                 float scale, void* workspace, size_t workspace_bytes,
                                 int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * FP8 (e4m3) pages. The continuous-batching page (section "Two orthogonal
+ * fixes, one serving engine") counts FP8 arithmetic among the kernel-level
+ * optimisations that stack with paging; the storage format below is this
+ * library's. A page keeps one byte per element and one fp32 scale per token
+ * row, so appending a token never touches the rest of its page:
+ *   k_codes, v_codes   : uint8 [num_blocks][Hkv][block_size][D] (device),
+ *                        e4m3 codes (1 sign, 4 exponent bits biased by 7,
+ *                        3 mantissa bits; 0x7F / 0xFF are NaN; max 448).
+ *   k_scales, v_scales : fp32 [num_blocks][Hkv][block_size] (device).
+ *   element value = e4m3(code) * scale of its row.
+ * kv_append_fp8 quantises each new (token, head) row of k_new / v_new (bf16
+ * [T][Hkv][D]) with amax = its largest magnitude: scale = amax / 448 and
+ * code = e4m3(x * (448 / amax)), both quotients and the product rounded to
+ * fp32, the code rounded to nearest even and saturated; a zero row gets
+ * scale 0. Slots as in pkv_kv_append (-1 skips; out-of-pool recorded).
+ * paged_attention_decode_fp8 is pkv_paged_attention_decode over such pages
+ * (same arguments otherwise, same workspace size): codes are widened to fp16
+ * on chip, q is rounded to fp16 (exact for 2^-14 <= |q| <= 65504), key
+ * scales multiply the scores, value scales the probabilities, and the
+ * scaled probabilities enter the P.V product as two fp16 parts.
+ * All arrays 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+int pkv_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                      int32_t T, void* k_codes, void* v_codes, float* k_scales,
+                      float* v_scales, int32_t num_blocks, int32_t Hkv, int32_t D,
+                      int32_t block_size, int32_t* dev_status, void* stream);
+int pkv_paged_attention_decode_fp8(void* out, const void* q, const void* k_codes,
+                                   const void* v_codes, const float* k_scales,
+                                   const float* v_scales, const int32_t* block_tables,
+                                   int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                   int32_t max_context_len, int32_t S, int32_t Hq, int32_t Hkv,
+                                   int32_t D, int32_t block_size, int32_t num_blocks,
+                                   float scale, int32_t partition_size, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

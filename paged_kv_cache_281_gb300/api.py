@@ -27,7 +27,8 @@ __all__ = [
     "pkv_paged_attention_decode", "pkv_paged_attention_decode_noalloc",
     "NOALLOC_SCRATCH_BYTES", "pkv_prefill_workspace_bytes",
     "pkv_paged_attention_prefill", "pkv_status_reset", "pkv_check_status",
-    "pkv_debug_set_wait", "new_status",
+    "pkv_debug_set_wait", "new_status", "new_fp8_pools", "pkv_kv_append_fp8",
+    "pkv_paged_attention_decode_fp8",
 ]
 
 
@@ -287,6 +288,66 @@ def pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_l
         block_tables.data_ptr(), int(block_tables.shape[1]), context_lens.data_ptr(),
         int(max_context_len), S, Hq, Hkv, D, B, N, float(scale), int(partition_size),
         workspace.data_ptr(), int(workspace.numel()), _ptr(status), _stream(stream)))
+
+
+# ---------------------------------------------------------------- FP8 pages
+
+def _fp8_pools(k_codes, v_codes, k_scales, v_scales):
+    _dev(k_codes, "k_codes", torch.uint8, 4)
+    _dev(v_codes, "v_codes", torch.uint8, 4)
+    _dev(k_scales, "k_scales", torch.float32, 3)
+    _dev(v_scales, "v_scales", torch.float32, 3)
+    if k_codes.shape != v_codes.shape or k_scales.shape != v_scales.shape or \
+            tuple(k_scales.shape) != tuple(k_codes.shape[:3]):
+        raise ValueError("codes must be [N, Hkv, B, D] and scales [N, Hkv, B], K and V alike")
+    return tuple(int(x) for x in k_codes.shape)  # N, Hkv, B, D
+
+
+def new_fp8_pools(num_blocks: int, Hkv: int, block_size: int, D: int, device=None):
+    """Zeroed FP8 pools: (k_codes, v_codes, k_scales, v_scales)."""
+    dev = device or "cuda"
+    codes = [torch.zeros((num_blocks, Hkv, block_size, D), dtype=torch.uint8, device=dev)
+             for _ in range(2)]
+    scales = [torch.zeros((num_blocks, Hkv, block_size), dtype=torch.float32, device=dev)
+              for _ in range(2)]
+    return codes[0], codes[1], scales[0], scales[1]
+
+
+def pkv_kv_append_fp8(k_new, v_new, slot_mapping, k_codes, v_codes, k_scales, v_scales,
+                      status=None, stream=None) -> None:
+    N, Hkv, B, D = _fp8_pools(k_codes, v_codes, k_scales, v_scales)
+    _dev(k_new, "k_new", torch.bfloat16, 3)
+    _dev(v_new, "v_new", torch.bfloat16, 3)
+    _dev(slot_mapping, "slot_mapping", torch.int32, 1)
+    T = int(slot_mapping.shape[0])
+    if k_new.shape != (T, Hkv, D) or v_new.shape != (T, Hkv, D):
+        raise ValueError(f"k_new/v_new must be [{T}, {Hkv}, {D}]")
+    check(lib().pkv_kv_append_fp8(k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), T,
+                                  k_codes.data_ptr(), v_codes.data_ptr(), k_scales.data_ptr(),
+                                  v_scales.data_ptr(), N, Hkv, D, B, _ptr(status),
+                                  _stream(stream)))
+
+
+def pkv_paged_attention_decode_fp8(out, q, k_codes, v_codes, k_scales, v_scales, block_tables,
+                                   context_lens, max_context_len: int, scale: float, workspace,
+                                   partition_size: int = 0, status=None, stream=None) -> None:
+    N, Hkv, B, D = _fp8_pools(k_codes, v_codes, k_scales, v_scales)
+    _dev(q, "q", torch.bfloat16, 3)
+    _dev(out, "out", torch.bfloat16, 3)
+    _dev(block_tables, "block_tables", torch.int32, 2)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    _dev(workspace, "workspace", torch.uint8, 1)
+    S, Hq = int(q.shape[0]), int(q.shape[1])
+    if q.shape[2] != D or out.shape != q.shape:
+        raise ValueError("q/out must be [S, Hq, D] with the pools' D")
+    if block_tables.shape[0] != S or context_lens.shape[0] != S:
+        raise ValueError("block_tables/context_lens must have S rows")
+    check(lib().pkv_paged_attention_decode_fp8(
+        out.data_ptr(), q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(), k_scales.data_ptr(),
+        v_scales.data_ptr(), block_tables.data_ptr(), int(block_tables.shape[1]),
+        context_lens.data_ptr(), int(max_context_len), S, Hq, Hkv, D, B, N, float(scale),
+        int(partition_size), workspace.data_ptr(), int(workspace.numel()), _ptr(status),
+        _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20  # PKV_DECODE_NOALLOC_SCRATCH_BYTES

@@ -117,6 +117,89 @@ __global__ void __launch_bounds__(256) swap_blocks_kernel(const SwapArgs a) {
     dst[j] = src[j];
 }
 
+// ---------------------------------------------------------------------------
+// kv_append into FP8 (e4m3) pages. One warp per (token, head, tensor) row:
+// the row's largest magnitude amax sets scale = amax / 448 and the codes
+// e4m3(x * (448 / amax)) (fp32 quotients and product, round to nearest even,
+// saturating); a row of zeros gets scale 0 and zero codes. Codes land in
+// [N][Hkv][B][D] bytes, the scale in [N][Hkv][B] floats.
+struct AppendFp8Args {
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  const int32_t* slot_mapping;
+  uint8_t* k8;
+  uint8_t* v8;
+  float* ks;
+  float* vs;
+  int64_t num_slots;
+  int32_t T;
+  int32_t Hkv;
+  int32_t D;
+  int32_t block_size;
+  int32_t* status;
+};
+
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 c;\n\tcvt.rn.satfinite.e4m3x2.f32 c, %1, %2;\n\tcvt.u32.u16 %0, c;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) kv_append_fp8_kernel(const AppendFp8Args a) {
+  constexpr int E = D / 32;  // elements per lane: 4 (D=128) or 2 (D=64)
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)a.T * a.Hkv * 2;
+  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; w < rows;
+       w += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int which = (int)(w & 1);           // 0 keys, 1 values
+    const int64_t th = w >> 1;
+    const int32_t t = (int32_t)(th / a.Hkv);
+    const int32_t h = (int32_t)(th - (int64_t)t * a.Hkv);
+    const int32_t slot = __ldg(a.slot_mapping + t);
+    if (slot < 0) continue;
+    if (slot >= a.num_slots) {
+      if (h == 0 && which == 0 && lane == 0)
+        record_status(a.status, PKV_EDEVICE, slot, kKernelAppend);
+      continue;
+    }
+    const __nv_bfloat16* src = (which ? a.v_new : a.k_new) + ((int64_t)t * a.Hkv + h) * D + lane * E;
+    float x[E];
+    if constexpr (E == 4) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
+      x[0] = bf16_lo_to_f32(u.x);
+      x[1] = bf16_hi_to_f32(u.x);
+      x[2] = bf16_lo_to_f32(u.y);
+      x[3] = bf16_hi_to_f32(u.y);
+    } else {
+      const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(src));
+      x[0] = bf16_lo_to_f32(u);
+      x[1] = bf16_hi_to_f32(u);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
+    const int32_t blk = slot / a.block_size;
+    const int32_t off = slot - blk * a.block_size;
+    const int64_t row = ((int64_t)blk * a.Hkv + h) * a.block_size + off;
+    uint8_t* dst = (which ? a.v8 : a.k8) + row * D + lane * E;
+    if constexpr (E == 4) {
+      const uint32_t c01 = e4m3x2_from_f32(__fmul_rn(x[0], inv), __fmul_rn(x[1], inv));
+      const uint32_t c23 = e4m3x2_from_f32(__fmul_rn(x[2], inv), __fmul_rn(x[3], inv));
+      *reinterpret_cast<uint32_t*>(dst) = c01 | (c23 << 16);
+    } else {
+      const uint32_t c01 = e4m3x2_from_f32(__fmul_rn(x[0], inv), __fmul_rn(x[1], inv));
+      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)c01;
+    }
+    if (lane == 0) (which ? a.vs : a.ks)[row] = __fdiv_rn(amax, 448.f);
+  }
+}
+
 // Device-usable address of a buffer, or an error for memory the GPU cannot
 // reach (pageable host memory).
 int device_address(void* p, void** out, const char* who) {
@@ -175,6 +258,49 @@ extern "C" int pkv_kv_append(const void* k_new, const void* v_new, const int32_t
   const int grid = (int)(want < cap ? want : cap);
   kv_append_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
   if (int rc = check_launch("pkv_kv_append")) return rc;
+  return ok();
+}
+
+extern "C" int pkv_kv_append_fp8(const void* k_new, const void* v_new,
+                                 const int32_t* slot_mapping, int32_t T, void* k_codes,
+                                 void* v_codes, float* k_scales, float* v_scales,
+                                 int32_t num_blocks, int32_t Hkv, int32_t D, int32_t block_size,
+                                 int32_t* dev_status, void* stream) {
+  if (int rc = check_shape(Hkv, D, block_size, "pkv_kv_append_fp8")) return rc;
+  PKV_REQUIRE(T >= 0, "pkv_kv_append_fp8: T must be >= 0 (got %d)", T);
+  PKV_REQUIRE(num_blocks > 0 && (int64_t)num_blocks * block_size < (int64_t(1) << 31),
+              "pkv_kv_append_fp8: num_blocks * block_size must be in [1, 2^31)");
+  if (T == 0) return ok();
+  PKV_REQUIRE(k_new && v_new && slot_mapping && k_codes && v_codes && k_scales && v_scales,
+              "pkv_kv_append_fp8: NULL pointer");
+  PKV_REQUIRE(aligned16(k_new) && aligned16(v_new) && aligned16(k_codes) && aligned16(v_codes) &&
+                  aligned16(k_scales) && aligned16(v_scales),
+              "pkv_kv_append_fp8: arrays must be 16-byte aligned");
+  const DeviceInfo* dev = nullptr;
+  if (int rc = current_device_info(&dev)) return rc;
+  AppendFp8Args a;
+  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  a.slot_mapping = slot_mapping;
+  a.k8 = static_cast<uint8_t*>(k_codes);
+  a.v8 = static_cast<uint8_t*>(v_codes);
+  a.ks = k_scales;
+  a.vs = v_scales;
+  a.num_slots = (int64_t)num_blocks * block_size;
+  a.T = T;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.block_size = block_size;
+  a.status = dev_status;
+  const int64_t rows = (int64_t)T * Hkv * 2;
+  const int64_t want = (rows + 7) / 8;  // 8 warps per CTA
+  const int64_t cap = (int64_t)dev->sm_count * 8;
+  const int grid = (int)(want < cap ? want : cap);
+  if (D == 128)
+    kv_append_fp8_kernel<128><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  else
+    kv_append_fp8_kernel<64><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  if (int rc = check_launch("pkv_kv_append_fp8")) return rc;
   return ok();
 }
 

@@ -76,6 +76,11 @@ struct DecodeArgs {
   int32_t* status;
   uint64_t timeout_ns;
   int32_t force_timeout;
+  // FP8 pages (the e4m3 variant): codes [N][Hkv][B][D], scales [N][Hkv][B]
+  const uint8_t* k8;
+  const uint8_t* v8;
+  const float* ks;
+  const float* vs;
 };
 
 // Lists the work items: pass 0 emits every full partition (s, p), pass 1 the
@@ -497,6 +502,360 @@ WsLayout ws_layout(int64_t S, int64_t Hq, int64_t D, int64_t max_parts) {
   return w;
 }
 
+// ---------------------------------------------------------------------------
+// Decode over FP8 (e4m3) pages with one fp32 scale per token row.
+//
+// Same work items, partitions, ring discipline and merge as the bf16 kernel;
+// what differs is the tile:
+//  * a tile's codes (16 rows x D bytes per tensor) and its 16 key and 16 value
+//    scales arrive by four contiguous bulk copies per page (no tensor map);
+//  * the warp widens the codes to fp16 (exact: every e4m3 value is an fp16
+//    value) into a private staging tile in the 128-byte-swizzled layout the
+//    ldmatrix loads of the bf16 kernel read, writing zeros for value rows past
+//    the sequence end;
+//  * the MMAs run in fp16 (Q rounded to fp16 once per item, exact for
+//    2^-14 <= |q| <= 65504); a key's scale multiplies its score column and a
+//    value's scale its probability before the P V product, so the codes are
+//    never rescaled element by element. P' = p * s_v enters the MMA as
+//    fp16 hi + lo parts.
+template <int D>
+struct Cfg8 {
+  static constexpr int kTile8 = kTileTokens * D;       // codes of one tensor tile
+  static constexpr int kScaleBytes = kTileTokens * 4;  // scales of one tensor tile
+  static constexpr int kStageBytes = 2 * kTile8 + 2 * kScaleBytes;
+  static constexpr int kStages = D == 128 ? 4 : 6;
+  static constexpr int kHalves = D / 64;
+  static constexpr int kHalfBytes = kTileTokens * 128;  // fp16 staging: 16 rows x 64 columns
+  static constexpr int kTensorBytes = kHalves * kHalfBytes;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kWarpBytes = kRingBytes + 2 * kTensorBytes;
+  static constexpr int kSmemBytes = kWarps * kWarpBytes + 1024;
+  static_assert(kStageBytes % 128 == 0 && kWarpBytes % 128 == 0, "stage alignment");
+};
+
+struct TileRows8 {
+  int32_t row[2];
+  uint32_t bytes;
+};
+
+template <int D>
+__device__ __forceinline__ TileRows8 tile_rows8(const DecodeArgs& a, const int32_t* bt, int kvh,
+                                                int tile, int L) {
+  const int B = a.block_size;
+  const int R = B < kTileTokens ? B : kTileTokens;
+  const int nsub = kTileTokens / R;
+  TileRows8 tr;
+  tr.row[0] = tr.row[1] = -1;
+  tr.bytes = 0;
+  for (int sub = 0; sub < nsub; ++sub) {
+    const int tok = tile * kTileTokens + sub * R;
+    if (tok >= L) break;
+    const int32_t blk = __ldg(bt + tok / B);
+    if (blk < 0 || blk >= a.num_blocks) {
+      record_status(a.status, PKV_EDEVICE, blk, kKernelDecode);
+      continue;
+    }
+    tr.row[sub] = (blk * a.Hkv + kvh) * B + tok % B;
+    tr.bytes += 2u * R * (D + 4);
+  }
+  return tr;
+}
+
+template <int D>
+__device__ __forceinline__ void issue_tile_rows8(const DecodeArgs& a, int32_t row0, int32_t row1,
+                                                 uint32_t bytes, uint32_t stage, uint32_t bar) {
+  using C = Cfg8<D>;
+  const int R = a.block_size < kTileTokens ? a.block_size : kTileTokens;
+  mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+  for (int sub = 0; sub < 2; ++sub) {
+    const int32_t row = sub == 0 ? row0 : row1;
+    if (row < 0) continue;
+    bulk_load(stage + sub * R * D, a.k8 + (int64_t)row * D, R * D, bar);
+    bulk_load(stage + C::kTile8 + sub * R * D, a.v8 + (int64_t)row * D, R * D, bar);
+    bulk_load(stage + 2 * C::kTile8 + sub * R * 4, a.ks + row, R * 4, bar);
+    bulk_load(stage + 2 * C::kTile8 + C::kScaleBytes + sub * R * 4, a.vs + row, R * 4, bar);
+  }
+}
+
+// Widens one tensor tile of codes (row-major, D bytes a row) to fp16 in the
+// swizzled staging layout; rows >= zero_from are written as zeros.
+template <int D>
+__device__ __forceinline__ void widen_tile(const uint8_t* src, uint32_t dst, int lane,
+                                           int zero_from) {
+  using C = Cfg8<D>;
+  constexpr int kChunks = kTileTokens * D / 16;  // 16-code chunks
+#pragma unroll
+  for (int i = lane; i < kChunks; i += 32) {
+    const int r = i / (D / 16), c = i % (D / 16);
+    uint32_t h[8];
+    if (r < zero_from) {
+      const uint4 w = *reinterpret_cast<const uint4*>(src + r * D + c * 16);
+      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        h[2 * e] = e4m3x2_to_f16x2(wv[e] & 0xffffu);
+        h[2 * e + 1] = e4m3x2_to_f16x2(wv[e] >> 16);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) h[e] = 0u;
+    }
+    // fp16 columns 16c .. 16c+15: half c/4, 16-byte chunks 2(c%4) and 2(c%4)+1
+    const uint32_t half = dst + (c >> 2) * C::kHalfBytes;
+    const uint32_t ch = (c & 3) * 2;
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(half + swz128(r, ch)),
+                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                 : "memory");
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(half + swz128(r, ch + 1)),
+                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                 : "memory");
+  }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 2) paged_decode_fp8_kernel(const DecodeArgs a) {
+  using C = Cfg8<D>;
+  constexpr int KS = D / 16;
+  constexpr int NT = D / 8;
+  extern __shared__ uint8_t dsm[];
+  __shared__ __align__(8) uint64_t bars[kWarps][C::kStages];
+  __shared__ int32_t s_next;
+  __shared__ int32_t s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t dsm_u32 = smem_u32(dsm);
+  const uint32_t base = (dsm_u32 + 1023u) & ~1023u;
+  uint8_t* base_ptr = dsm + (base - dsm_u32);
+  const uint32_t ring = base + warp * C::kWarpBytes;
+  const uint8_t* ring_ptr = base_ptr + warp * C::kWarpBytes;
+  const uint32_t kstage16 = ring + C::kRingBytes;  // fp16 keys, then fp16 values
+  const uint32_t vstage16 = kstage16 + C::kTensorBytes;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < C::kStages; ++st) mbar_init(smem_u32(&bars[warp][st]), 1);
+    fence_barrier_init();
+  }
+  grid_dep_launch();
+  grid_dep_wait();
+  if (tid == 0) {
+    s_abort = 0;
+    s_next = atomicAdd(a.ticket, 1);
+  }
+  __syncthreads();
+  const int total = __ldg(a.n_items) * a.Hkv;
+  const int P = a.partition_tiles * kTileTokens;
+  uint32_t phase = 0;
+  int cur = s_next;
+
+  while (cur < total) {
+    __syncthreads();
+    if (tid == 0) s_next = atomicAdd(a.ticket, 1);
+    const int2 item = __ldg(a.items + cur / a.Hkv);
+    const int kvh = cur % a.Hkv;
+    const int s = item.x, p = item.y;
+    const int L = __ldg(a.context_lens + s);
+    const int t_begin = p * a.partition_tiles;
+    const int t_end = min((L + kTileTokens - 1) / kTileTokens, t_begin + a.partition_tiles);
+    const int n_item = t_end - t_begin;
+    const int n_mine = n_item > warp ? (n_item - warp + kWarps - 1) / kWarps : 0;
+    const int32_t* bt = a.block_tables + (int64_t)s * a.max_blocks_per_seq;
+
+    TileRows8 mine = {{-1, -1}, 0u};
+    int chunk0 = 0;
+    if (lane < n_mine) mine = tile_rows8<D>(a, bt, kvh, t_begin + warp + lane * kWarps, L);
+    auto issue = [&](int k, uint32_t st) {
+      if (k - chunk0 >= 32) {
+        chunk0 += 32;
+        mine = {{-1, -1}, 0u};
+        if (chunk0 + lane < n_mine)
+          mine = tile_rows8<D>(a, bt, kvh, t_begin + warp + (chunk0 + lane) * kWarps, L);
+      }
+      const int src = k - chunk0;
+      const int32_t r0 = __shfl_sync(0xffffffffu, mine.row[0], src);
+      const int32_t r1 = __shfl_sync(0xffffffffu, mine.row[1], src);
+      const uint32_t by = __shfl_sync(0xffffffffu, mine.bytes, src);
+      if (lane == 0)
+        issue_tile_rows8<D>(a, r0, r1, by, ring + st * C::kStageBytes, smem_u32(&bars[warp][st]));
+    };
+    {
+      const int npro = n_mine < C::kStages ? n_mine : C::kStages;
+      for (int k = 0; k < npro; ++k) issue(k, k);
+    }
+
+    // Q fragments in fp16 (rows g < G; rows g+8 are always zero)
+    uint32_t qa[KS][2];
+    {
+      const bool live = g < G;
+      const __nv_bfloat16* qrow = a.q + ((int64_t)s * a.Hq + kvh * G + (live ? g : 0)) * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t w0 = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * t)) : 0u;
+        uint32_t w1 =
+            live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * t)) : 0u;
+        qa[ks][0] = pack_f16x2(bf16_lo_to_f32(w0), bf16_hi_to_f32(w0));
+        qa[ks][1] = pack_f16x2(bf16_lo_to_f32(w1), bf16_hi_to_f32(w1));
+      }
+    }
+
+    float m = -INFINITY, l = 0.f;
+    float o[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+
+    for (int k = 0; k < n_mine; ++k) {
+      const int st = k % C::kStages;
+      const int tile = t_begin + warp + k * kWarps;
+      const uint32_t bar = smem_u32(&bars[warp][st]);
+      const uint32_t par = (phase >> st) & 1u;
+      const bool landed = mbar_wait_bounded(bar, par, a.timeout_ns, a.force_timeout);
+      if (!__all_sync(0xffffffffu, landed)) {
+        if (lane == 0) {
+          record_status(a.status, PKV_ETIMEOUT, k, kKernelDecode);
+          s_abort = 1;
+        }
+        uint32_t ph = phase;
+        const int last = min(k + C::kStages, n_mine);
+        for (int j = k; j < last; ++j) {
+          const int sj = j % C::kStages;
+          mbar_wait_bounded(smem_u32(&bars[warp][sj]), (ph >> sj) & 1u, 4 * a.timeout_ns, 0);
+          ph ^= 1u << sj;
+        }
+        phase = ph;
+        break;
+      }
+      phase ^= 1u << st;
+      const uint8_t* stage = ring_ptr + st * C::kStageBytes;
+      const int valid = min(kTileTokens, L - tile * kTileTokens);
+      // widen the codes; value rows past the sequence end become zeros
+      widen_tile<D>(stage, kstage16, lane, kTileTokens);
+      widen_tile<D>(stage + C::kTile8, vstage16, lane, valid);
+      const float* ksc = reinterpret_cast<const float*>(stage + 2 * C::kTile8);
+      const float* vsc = reinterpret_cast<const float*>(stage + 2 * C::kTile8 + C::kScaleBytes);
+      float kscale[2][2], vscale[2][2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          kscale[j][e] = ksc[8 * j + 2 * t + e];
+          vscale[j][e] = vsc[8 * j + 2 * t + e];
+        }
+      __syncwarp();
+
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int tok = (lane & 7) + ((lane >> 4) << 3);
+        const int csel = (lane >> 3) & 1;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const int chunk = 2 * ks + csel;
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(kstage16 + (chunk >> 3) * C::kHalfBytes + swz128(tok, chunk & 7), b0, b1,
+                      b2, b3);
+          mma_f16_16816(sc[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+          mma_f16_16816(sc[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+        }
+      }
+
+      float x[4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          x[2 * j + e] = (8 * j + 2 * t + e < valid)
+                             ? sc[j][e] * kscale[j][e] * a.scale_log2
+                             : -INFINITY;
+      float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m, mx);
+      const float alpha = fast_exp2(m - m_new);
+      float pr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pr[i] = fast_exp2(x[i] - m_new);
+      l = l * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+      m = m_new;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        o[nt][0] *= alpha;
+        o[nt][1] *= alpha;
+        o[nt][2] *= alpha;
+        o[nt][3] *= alpha;
+      }
+      // P' = p * s_v in fp16 hi (rows 0..7) + lo (rows 8..15); rows past the
+      // end carry p = 0 and a zero value row
+      float pv[4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          pv[2 * j + e] = (8 * j + 2 * t + e < valid) ? pr[2 * j + e] * vscale[j][e] : 0.f;
+      const uint32_t pa0 = pack_f16x2(pv[0], pv[1]);
+      const uint32_t pa2 = pack_f16x2(pv[2], pv[3]);
+      const uint32_t pl0 = pack_f16x2(pv[0] - f16_lo_to_f32(pa0), pv[1] - f16_hi_to_f32(pa0));
+      const uint32_t pl2 = pack_f16x2(pv[2] - f16_lo_to_f32(pa2), pv[3] - f16_hi_to_f32(pa2));
+      {
+        const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int csel = lane >> 4;
+#pragma unroll
+        for (int n2 = 0; n2 < NT / 2; ++n2) {
+          const int chunk = 2 * n2 + csel;
+          uint32_t r0, r1, r2, r3;
+          ldmatrix_x4_trans(vstage16 + (chunk >> 3) * C::kHalfBytes + swz128(tok, chunk & 7), r0,
+                            r1, r2, r3);
+          mma_f16_16816(o[2 * n2], pa0, pl0, pa2, pl2, r0, r1);
+          mma_f16_16816(o[2 * n2 + 1], pa0, pl0, pa2, pl2, r2, r3);
+        }
+      }
+      __syncwarp();  // staging and stage reads done before they are overwritten
+      if (k + C::kStages < n_mine) issue(k + C::kStages, st);
+    }
+
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    __syncthreads();
+    if (s_abort) return;
+    float2* cml = reinterpret_cast<float2*>(base_ptr);
+    float* co = reinterpret_cast<float*>(base_ptr + 256);
+    if (g < G) {
+      if (t == 0) cml[warp * G + g] = make_float2(m, l);
+      float* row = co + (warp * G + g) * D;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        *reinterpret_cast<float2*>(row + nt * 8 + 2 * t) =
+            make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3]);
+    }
+    __syncthreads();
+    const int nparts = (L + P - 1) / P;
+    for (int e = tid; e < G * D; e += kThreads) {
+      const int h = e / D, d = e % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cml[w * G + h].x);
+      float lsum = 0.f, acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float sw = fast_exp2(cml[w * G + h].x - M);
+        lsum += sw * cml[w * G + h].y;
+        acc += sw * co[(w * G + h) * D + d];
+      }
+      const int64_t qh = (int64_t)s * a.Hq + kvh * G + h;
+      if (nparts == 1) {
+        a.out[qh * D + d] = __float2bfloat16_rn(acc / lsum);
+      } else {
+        const int64_t idx = qh * a.max_partitions + p;
+        a.ws_o[idx * D + d] = acc;
+        if (d == 0) a.ws_ml[idx] = make_float2(M, lsum);
+      }
+    }
+    fence_proxy_async_smem();  // merge-buffer stores before the ring's next bulk writes
+    __syncthreads();
+    cur = s_next;
+  }
+}
+
 int resolve_partition(int32_t partition_size, int32_t* tiles) {
   const int32_t P = partition_size == 0 ? kDefaultPartition : partition_size;
   PKV_REQUIRE(P >= kTileTokens && P % kTileTokens == 0 && P <= (1 << 20),
@@ -537,6 +896,46 @@ int launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs
   cfg.numAttrs = 1;
   cudaError_t err = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, G>, tk, tv, a);
   if (err != cudaSuccess) return cuda_fail(err, "decode launch");
+  if (a.max_partitions > 1) {
+    const int64_t pairs = (int64_t)a.S * a.Hq;
+    cfg.gridDim = dim3((unsigned)((pairs + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    err = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, a);
+    if (err != cudaSuccess) return cuda_fail(err, "decode combine launch");
+  }
+  return PKV_OK;
+}
+
+template <int D, int G>
+int launch_decode_fp8(const DecodeArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+  using C = Cfg8<D>;
+  static std::once_flag once;
+  static int blocks_per_sm = 0;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, []() {
+    attr_err = cudaFuncSetAttribute(paged_decode_fp8_kernel<D, G>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &blocks_per_sm, paged_decode_fp8_kernel<D, G>, kThreads, C::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "fp8 decode kernel attributes");
+  if (blocks_per_sm < 1) return fail(PKV_ECUDA, "fp8 decode kernel does not fit on an SM");
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  decode_plan_kernel<<<1, 1024, 0, stream>>>(a);
+  if (int rc = check_launch("decode plan")) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(dev.sm_count * blocks_per_sm));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, paged_decode_fp8_kernel<D, G>, a);
+  if (err != cudaSuccess) return cuda_fail(err, "fp8 decode launch");
   if (a.max_partitions > 1) {
     const int64_t pairs = (int64_t)a.S * a.Hq;
     cfg.gridDim = dim3((unsigned)((pairs + 3) / 4));
@@ -615,7 +1014,7 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
   if (int rc = encode_tile_map_2d(&tv, v_cache, D, rows, (uint64_t)D * 2, 64, box_rows)) return rc;
 
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
-  DecodeArgs a;
+  DecodeArgs a = {};
   a.out = static_cast<__nv_bfloat16*>(out);
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.block_tables = block_tables;
@@ -653,6 +1052,94 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
   PKV_DECODE_CASE(128, 4)
   PKV_DECODE_CASE(128, 8)
 #undef PKV_DECODE_CASE
+  if (rc) return rc;
+  return ok();
+}
+
+extern "C" int pkv_paged_attention_decode_fp8(
+    void* out, const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
+    const float* v_scales, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* context_lens, int32_t max_context_len, int32_t S, int32_t Hq, int32_t Hkv,
+    int32_t D, int32_t block_size, int32_t num_blocks, float scale, int32_t partition_size,
+    void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  PKV_REQUIRE(S >= 0, "decode_fp8: S must be >= 0");
+  PKV_REQUIRE(Hkv > 0 && Hq > 0 && Hq % Hkv == 0,
+              "decode_fp8: Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  const int G = Hq / Hkv;
+  PKV_REQUIRE(G == 1 || G == 2 || G == 4 || G == 8,
+              "decode_fp8: Hq/Hkv must be 1, 2, 4 or 8 (got %d)", G);
+  PKV_REQUIRE(D == 64 || D == 128, "decode_fp8: D must be 64 or 128 (got %d)", D);
+  PKV_REQUIRE(block_size == 8 || block_size == 16 || block_size == 32,
+              "decode_fp8: block_size must be 8, 16 or 32 (got %d)", block_size);
+  PKV_REQUIRE(num_blocks > 0 && (int64_t)num_blocks * Hkv * block_size < (int64_t(1) << 31),
+              "decode_fp8: num_blocks * Hkv * block_size must be in [1, 2^31)");
+  PKV_REQUIRE(max_context_len >= 1, "decode_fp8: max_context_len must be >= 1");
+  PKV_REQUIRE((int64_t)max_blocks_per_seq * block_size >= max_context_len,
+              "decode_fp8: max_context_len %d exceeds max_blocks_per_seq * block_size",
+              max_context_len);
+  PKV_REQUIRE(std::isfinite(scale), "decode_fp8: scale must be finite");
+  if (S == 0) return ok();
+  PKV_REQUIRE(out && q && k_codes && v_codes && k_scales && v_scales && block_tables &&
+                  context_lens && workspace,
+              "decode_fp8: NULL pointer");
+  PKV_REQUIRE(aligned16(out) && aligned16(q) && aligned16(k_codes) && aligned16(v_codes) &&
+                  aligned16(k_scales) && aligned16(v_scales),
+              "decode_fp8: arrays must be 16-byte aligned");
+  PKV_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0,
+              "decode_fp8: workspace must be 256-byte aligned");
+  int32_t tiles = 0;
+  if (int rc = resolve_partition(partition_size, &tiles)) return rc;
+  const int64_t P = (int64_t)tiles * kTileTokens;
+  const int64_t max_parts = (max_context_len + P - 1) / P;
+  const WsLayout ws = ws_layout(S, Hq, D, max_parts);
+  PKV_REQUIRE(workspace_bytes >= ws.total, "decode_fp8: workspace has %zu bytes, needs %zu",
+              workspace_bytes, ws.total);
+  const DeviceInfo* dev = nullptr;
+  if (int rc = current_device_info(&dev)) return rc;
+
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  DecodeArgs a = {};
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.S = S;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.max_context_len = max_context_len;
+  a.partition_tiles = tiles;
+  a.max_partitions = (int32_t)max_parts;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.ticket = reinterpret_cast<int32_t*>(wsb);
+  a.n_items = reinterpret_cast<int32_t*>(wsb) + 1;
+  a.items = reinterpret_cast<int2*>(wsb + ws.items_off);
+  a.ws_ml = reinterpret_cast<float2*>(wsb + ws.ml_off);
+  a.ws_o = reinterpret_cast<float*>(wsb + ws.o_off);
+  a.status = dev_status;
+  const WaitConfig wc = wait_config();
+  a.timeout_ns = wc.timeout_ns;
+  a.force_timeout = wc.force_timeout;
+  a.k8 = static_cast<const uint8_t*>(k_codes);
+  a.v8 = static_cast<const uint8_t*>(v_codes);
+  a.ks = k_scales;
+  a.vs = v_scales;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = PKV_OK;
+#define PKV_DECODE8_CASE(DD, GG) \
+  if (D == DD && G == GG) rc = launch_decode_fp8<DD, GG>(a, *dev, st);
+  PKV_DECODE8_CASE(64, 1)
+  PKV_DECODE8_CASE(64, 2)
+  PKV_DECODE8_CASE(64, 4)
+  PKV_DECODE8_CASE(64, 8)
+  PKV_DECODE8_CASE(128, 1)
+  PKV_DECODE8_CASE(128, 2)
+  PKV_DECODE8_CASE(128, 4)
+  PKV_DECODE8_CASE(128, 8)
+#undef PKV_DECODE8_CASE
   if (rc) return rc;
   return ok();
 }
