@@ -507,31 +507,43 @@ WsLayout ws_layout(int64_t S, int64_t Hq, int64_t D, int64_t max_parts) {
 //
 // Same work items, partitions, ring discipline and merge as the bf16 kernel;
 // what differs is the tile:
-//  * a tile's codes (16 rows x D bytes per tensor) and its 16 key and 16 value
-//    scales arrive by four contiguous bulk copies per page (no tensor map);
-//  * the warp widens the codes to fp16 (exact: every e4m3 value is an fp16
-//    value) into a private staging tile in the 128-byte-swizzled layout the
-//    ldmatrix loads of the bf16 kernel read, writing zeros for value rows past
-//    the sequence end;
-//  * the MMAs run in fp16 (Q rounded to fp16 once per item, exact for
-//    2^-14 <= |q| <= 65504); a key's scale multiplies its score column and a
-//    value's scale its probability before the P V product, so the codes are
-//    never rescaled element by element. P' = p * s_v enters the MMA as
-//    fp16 hi + lo parts.
+//  * a tile's codes arrive by TMA (16 rows x D bytes per tensor, 128-byte
+//    swizzled when D = 128) and its 16 key and 16 value scales by two small
+//    bulk copies into a separate scale ring;
+//  * scores: the MMA's k index is a sum index, so each thread owns a
+//    contiguous D/4-byte run of every key row (and the matching run of q,
+//    rounded to fp16 once per item: exact for 2^-14 <= |q| <= 65504) instead
+//    of the columns the hardware layout names; two codes widen to one fp16
+//    pair (exact: every e4m3 value is an fp16 value);
+//  * values: one transposing 8-bit ldmatrix per 16 x 16 code block hands
+//    thread (g, t) value rows 4t .. 4t+3 at columns g and 8 + g, which are
+//    the B fragments of two fp16 MMAs once the score columns are assigned to
+//    keys so that the thread's probabilities cover the same four rows;
+//  * a key's scale multiplies its score and a value's scale its probability
+//    (P' = p * s_v, as fp16 hi + lo parts) before the P V product, so no code
+//    is rescaled element by element; value rows past the sequence end are
+//    zeroed in shared memory.
 template <int D>
 struct Cfg8 {
-  static constexpr int kTile8 = kTileTokens * D;       // codes of one tensor tile
-  static constexpr int kScaleBytes = kTileTokens * 4;  // scales of one tensor tile
-  static constexpr int kStageBytes = 2 * kTile8 + 2 * kScaleBytes;
+  static constexpr int kTile8 = kTileTokens * D;         // codes of one tensor tile
+  static constexpr int kCodeStage = 2 * kTile8;          // keys, then values
+  static constexpr int kScaleStage = 2 * kTileTokens * 4;  // key scales, then value scales
   static constexpr int kStages = D == 128 ? 4 : 6;
-  static constexpr int kHalves = D / 64;
-  static constexpr int kHalfBytes = kTileTokens * 128;  // fp16 staging: 16 rows x 64 columns
-  static constexpr int kTensorBytes = kHalves * kHalfBytes;
-  static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kWarpBytes = kRingBytes + 2 * kTensorBytes;
+  static constexpr int kWarpBytes =
+      (kStages * (kCodeStage + kScaleStage) + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes = kWarps * kWarpBytes + 1024;
-  static_assert(kStageBytes % 128 == 0 && kWarpBytes % 128 == 0, "stage alignment");
+  static_assert(kCodeStage % 1024 == 0, "swizzled code tiles need 1024-byte alignment");
 };
+
+// Byte offset of 16-byte chunk c of code row r inside a tile: 128-byte
+// swizzled rows for D = 128 (as TMA writes them), plain rows for D = 64.
+template <int D>
+__device__ __forceinline__ uint32_t code_off(int r, int c) {
+  if constexpr (D == 128)
+    return swz128(r, c);
+  else
+    return r * D + c * 16;
+}
 
 struct TileRows8 {
   int32_t row[2];
@@ -562,8 +574,10 @@ __device__ __forceinline__ TileRows8 tile_rows8(const DecodeArgs& a, const int32
 }
 
 template <int D>
-__device__ __forceinline__ void issue_tile_rows8(const DecodeArgs& a, int32_t row0, int32_t row1,
-                                                 uint32_t bytes, uint32_t stage, uint32_t bar) {
+__device__ __forceinline__ void issue_tile_rows8(const CUtensorMap* tk, const CUtensorMap* tv,
+                                                 const DecodeArgs& a, int32_t row0, int32_t row1,
+                                                 uint32_t bytes, uint32_t codes, uint32_t scales,
+                                                 uint32_t bar) {
   using C = Cfg8<D>;
   const int R = a.block_size < kTileTokens ? a.block_size : kTileTokens;
   mbar_arrive_expect_tx(bar, bytes);
@@ -571,50 +585,26 @@ __device__ __forceinline__ void issue_tile_rows8(const DecodeArgs& a, int32_t ro
   for (int sub = 0; sub < 2; ++sub) {
     const int32_t row = sub == 0 ? row0 : row1;
     if (row < 0) continue;
-    bulk_load(stage + sub * R * D, a.k8 + (int64_t)row * D, R * D, bar);
-    bulk_load(stage + C::kTile8 + sub * R * D, a.v8 + (int64_t)row * D, R * D, bar);
-    bulk_load(stage + 2 * C::kTile8 + sub * R * 4, a.ks + row, R * 4, bar);
-    bulk_load(stage + 2 * C::kTile8 + C::kScaleBytes + sub * R * 4, a.vs + row, R * 4, bar);
+    tma_load_2d(codes + sub * R * D, tk, 0, row, bar);
+    tma_load_2d(codes + C::kTile8 + sub * R * D, tv, 0, row, bar);
+    bulk_load(scales + sub * R * 4, a.ks + row, R * 4, bar);
+    bulk_load(scales + kTileTokens * 4 + sub * R * 4, a.vs + row, R * 4, bar);
   }
 }
 
-// Widens one tensor tile of codes (row-major, D bytes a row) to fp16 in the
-// swizzled staging layout; rows >= zero_from are written as zeros.
-template <int D>
-__device__ __forceinline__ void widen_tile(const uint8_t* src, uint32_t dst, int lane,
-                                           int zero_from) {
-  using C = Cfg8<D>;
-  constexpr int kChunks = kTileTokens * D / 16;  // 16-code chunks
-#pragma unroll
-  for (int i = lane; i < kChunks; i += 32) {
-    const int r = i / (D / 16), c = i % (D / 16);
-    uint32_t h[8];
-    if (r < zero_from) {
-      const uint4 w = *reinterpret_cast<const uint4*>(src + r * D + c * 16);
-      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        h[2 * e] = e4m3x2_to_f16x2(wv[e] & 0xffffu);
-        h[2 * e + 1] = e4m3x2_to_f16x2(wv[e] >> 16);
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) h[e] = 0u;
-    }
-    // fp16 columns 16c .. 16c+15: half c/4, 16-byte chunks 2(c%4) and 2(c%4)+1
-    const uint32_t half = dst + (c >> 2) * C::kHalfBytes;
-    const uint32_t ch = (c & 3) * 2;
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(half + swz128(r, ch)),
-                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
-                 : "memory");
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(half + swz128(r, ch + 1)),
-                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
-                 : "memory");
-  }
+// 16 x 16 bytes at row addresses given by lanes 0..15, transposed: thread
+// (g, t) receives rows 4t .. 4t+3 of column g (r0) and of column 8 + g (r1).
+__device__ __forceinline__ void ldmatrix_b8_16x16_trans(uint32_t addr, uint32_t& r0,
+                                                        uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x1.trans.shared.b8 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 2) paged_decode_fp8_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 3)
+    paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                            const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
   using C = Cfg8<D>;
   constexpr int KS = D / 16;
   constexpr int NT = D / 8;
@@ -628,10 +618,10 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_fp8_kernel(const Dec
   const uint32_t dsm_u32 = smem_u32(dsm);
   const uint32_t base = (dsm_u32 + 1023u) & ~1023u;
   uint8_t* base_ptr = dsm + (base - dsm_u32);
-  const uint32_t ring = base + warp * C::kWarpBytes;
-  const uint8_t* ring_ptr = base_ptr + warp * C::kWarpBytes;
-  const uint32_t kstage16 = ring + C::kRingBytes;  // fp16 keys, then fp16 values
-  const uint32_t vstage16 = kstage16 + C::kTensorBytes;
+  const uint32_t ring = base + warp * C::kWarpBytes;       // code stages
+  const uint32_t sring = ring + C::kStages * C::kCodeStage;  // scale stages
+  uint8_t* ring_ptr = base_ptr + warp * C::kWarpBytes;
+  const uint8_t* sring_ptr = ring_ptr + C::kStages * C::kCodeStage;
 
   if (lane == 0) {
 #pragma unroll
@@ -641,6 +631,8 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_fp8_kernel(const Dec
   grid_dep_launch();
   grid_dep_wait();
   if (tid == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
     s_abort = 0;
     s_next = atomicAdd(a.ticket, 1);
   }
@@ -678,25 +670,27 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_fp8_kernel(const Dec
       const int32_t r1 = __shfl_sync(0xffffffffu, mine.row[1], src);
       const uint32_t by = __shfl_sync(0xffffffffu, mine.bytes, src);
       if (lane == 0)
-        issue_tile_rows8<D>(a, r0, r1, by, ring + st * C::kStageBytes, smem_u32(&bars[warp][st]));
+        issue_tile_rows8<D>(&tmap_k, &tmap_v, a, r0, r1, by, ring + st * C::kCodeStage,
+                            sring + st * C::kScaleStage, smem_u32(&bars[warp][st]));
     };
     {
       const int npro = n_mine < C::kStages ? n_mine : C::kStages;
       for (int k = 0; k < npro; ++k) issue(k, k);
     }
 
-    // Q fragments in fp16 (rows g < G; rows g+8 are always zero)
+    // Q fragments in fp16 (rows g < G; rows g+8 are always zero). Thread t
+    // owns d = (D/4) t + 4 ks + {0,1 | 2,3} in k-step ks (see the key loads).
     uint32_t qa[KS][2];
     {
       const bool live = g < G;
-      const __nv_bfloat16* qrow = a.q + ((int64_t)s * a.Hq + kvh * G + (live ? g : 0)) * D;
+      const __nv_bfloat16* qrow =
+          a.q + ((int64_t)s * a.Hq + kvh * G + (live ? g : 0)) * D + (D / 4) * t;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        uint32_t w0 = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * t)) : 0u;
-        uint32_t w1 =
-            live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * t)) : 0u;
-        qa[ks][0] = pack_f16x2(bf16_lo_to_f32(w0), bf16_hi_to_f32(w0));
-        qa[ks][1] = pack_f16x2(bf16_lo_to_f32(w1), bf16_hi_to_f32(w1));
+        const uint2 w =
+            live ? __ldg(reinterpret_cast<const uint2*>(qrow + 4 * ks)) : make_uint2(0u, 0u);
+        qa[ks][0] = pack_f16x2(bf16_lo_to_f32(w.x), bf16_hi_to_f32(w.x));
+        qa[ks][1] = pack_f16x2(bf16_lo_to_f32(w.y), bf16_hi_to_f32(w.y));
       }
     }
 
@@ -727,46 +721,52 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_fp8_kernel(const Dec
         break;
       }
       phase ^= 1u << st;
-      const uint8_t* stage = ring_ptr + st * C::kStageBytes;
+      const uint32_t kcodes = ring + st * C::kCodeStage;
+      const uint32_t vcodes = kcodes + C::kTile8;
+      const uint8_t* kptr = ring_ptr + st * C::kCodeStage;
       const int valid = min(kTileTokens, L - tile * kTileTokens);
-      // widen the codes; value rows past the sequence end become zeros
-      widen_tile<D>(stage, kstage16, lane, kTileTokens);
-      widen_tile<D>(stage + C::kTile8, vstage16, lane, valid);
-      const float* ksc = reinterpret_cast<const float*>(stage + 2 * C::kTile8);
-      const float* vsc = reinterpret_cast<const float*>(stage + 2 * C::kTile8 + C::kScaleBytes);
-      float kscale[2][2], vscale[2][2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          kscale[j][e] = ksc[8 * j + 2 * t + e];
-          vscale[j][e] = vsc[8 * j + 2 * t + e];
+      if (valid < kTileTokens) {
+        // value rows past the sequence end hold whatever the pool holds
+        for (int i = lane; i < (kTileTokens - valid) * (D / 16); i += 32) {
+          const int r = valid + i / (D / 16), c = i % (D / 16);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vcodes + code_off<D>(r, c)),
+                       "r"(0u)
+                       : "memory");
         }
-      __syncwarp();
+        __syncwarp();
+      }
+      const float* ksc = reinterpret_cast<const float*>(sring_ptr + st * C::kScaleStage);
+      const float* vsc = ksc + kTileTokens;
 
+      // S = Q K^T. Score column n of n-block j belongs to key
+      // 4 (n >> 1) + 2 j + (n & 1), so thread (g, t) loads key row
+      // 4 (g >> 1) + 2 j + (g & 1) and ends up with the scores of keys
+      // 4t + 2j + {0, 1}.
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      {
-        const int tok = (lane & 7) + ((lane >> 4) << 3);
-        const int csel = (lane >> 3) & 1;
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          const int chunk = 2 * ks + csel;
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(kstage16 + (chunk >> 3) * C::kHalfBytes + swz128(tok, chunk & 7), b0, b1,
-                      b2, b3);
-          mma_f16_16816(sc[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
-          mma_f16_16816(sc[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+      for (int j = 0; j < 2; ++j) {
+        const int kr = 4 * (g >> 1) + 2 * j + (g & 1);
+        uint32_t kw[KS];
+#pragma unroll
+        for (int v = 0; v < KS / 4; ++v) {
+          const uint4 u =
+              *reinterpret_cast<const uint4*>(kptr + code_off<D>(kr, (KS / 4) * t + v));
+          kw[4 * v] = u.x, kw[4 * v + 1] = u.y, kw[4 * v + 2] = u.z, kw[4 * v + 3] = u.w;
         }
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+          mma_f16_16816(sc[j], qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(kw[ks] & 0xffffu),
+                        e4m3x2_to_f16x2(kw[ks] >> 16));
       }
 
       float x[4];
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
-          x[2 * j + e] = (8 * j + 2 * t + e < valid)
-                             ? sc[j][e] * kscale[j][e] * a.scale_log2
-                             : -INFINITY;
+        for (int e = 0; e < 2; ++e) {
+          const int key = 4 * t + 2 * j + e;
+          x[2 * j + e] = key < valid ? sc[j][e] * ksc[key] * a.scale_log2 : -INFINITY;
+        }
       float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -777,39 +777,35 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_fp8_kernel(const Dec
       for (int i = 0; i < 4; ++i) pr[i] = fast_exp2(x[i] - m_new);
       l = l * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
       m = m_new;
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {  // the running max moved
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        o[nt][0] *= alpha;
-        o[nt][1] *= alpha;
-        o[nt][2] *= alpha;
-        o[nt][3] *= alpha;
+        for (int nt = 0; nt < NT; ++nt) {
+          o[nt][0] *= alpha;
+          o[nt][1] *= alpha;
+          o[nt][2] *= alpha;
+          o[nt][3] *= alpha;
+        }
       }
-      // P' = p * s_v in fp16 hi (rows 0..7) + lo (rows 8..15); rows past the
-      // end carry p = 0 and a zero value row
+      // P' = p * s_v for keys 4t .. 4t+3 in fp16 hi (rows 0..7) + lo (rows
+      // 8..15); keys past the end carry p = 0 and a zeroed value row
       float pv[4];
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          pv[2 * j + e] = (8 * j + 2 * t + e < valid) ? pr[2 * j + e] * vscale[j][e] : 0.f;
+      for (int i = 0; i < 4; ++i) pv[i] = 4 * t + i < valid ? pr[i] * vsc[4 * t + i] : 0.f;
       const uint32_t pa0 = pack_f16x2(pv[0], pv[1]);
       const uint32_t pa2 = pack_f16x2(pv[2], pv[3]);
       const uint32_t pl0 = pack_f16x2(pv[0] - f16_lo_to_f32(pa0), pv[1] - f16_hi_to_f32(pa0));
       const uint32_t pl2 = pack_f16x2(pv[2] - f16_lo_to_f32(pa2), pv[3] - f16_hi_to_f32(pa2));
-      {
-        const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int csel = lane >> 4;
 #pragma unroll
-        for (int n2 = 0; n2 < NT / 2; ++n2) {
-          const int chunk = 2 * n2 + csel;
-          uint32_t r0, r1, r2, r3;
-          ldmatrix_x4_trans(vstage16 + (chunk >> 3) * C::kHalfBytes + swz128(tok, chunk & 7), r0,
-                            r1, r2, r3);
-          mma_f16_16816(o[2 * n2], pa0, pl0, pa2, pl2, r0, r1);
-          mma_f16_16816(o[2 * n2 + 1], pa0, pl0, pa2, pl2, r2, r3);
-        }
+      for (int c = 0; c < D / 16; ++c) {
+        uint32_t r0, r1;
+        ldmatrix_b8_16x16_trans(vcodes + code_off<D>(lane & 15, c), r0, r1);
+        mma_f16_16816(o[2 * c], pa0, pl0, pa2, pl2, e4m3x2_to_f16x2(r0 & 0xffffu),
+                      e4m3x2_to_f16x2(r0 >> 16));
+        mma_f16_16816(o[2 * c + 1], pa0, pl0, pa2, pl2, e4m3x2_to_f16x2(r1 & 0xffffu),
+                      e4m3x2_to_f16x2(r1 >> 16));
       }
-      __syncwarp();  // staging and stage reads done before they are overwritten
+      if (valid < kTileTokens) fence_proxy_async_smem();  // zeroing stores before TMA reuse
+      __syncwarp();
       if (k + C::kStages < n_mine) issue(k + C::kStages, st);
     }
 
@@ -850,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_fp8_kernel(const Dec
         if (d == 0) a.ws_ml[idx] = make_float2(M, lsum);
       }
     }
-    fence_proxy_async_smem();  // merge-buffer stores before the ring's next bulk writes
+    fence_proxy_async_smem();  // merge-buffer stores before the ring's next TMA writes
     __syncthreads();
     cur = s_next;
   }
@@ -908,7 +904,8 @@ int launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs
 }
 
 template <int D, int G>
-int launch_decode_fp8(const DecodeArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+int launch_decode_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                      const DeviceInfo& dev, cudaStream_t stream) {
   using C = Cfg8<D>;
   static std::once_flag once;
   static int blocks_per_sm = 0;
@@ -934,7 +931,7 @@ int launch_decode_fp8(const DecodeArgs& a, const DeviceInfo& dev, cudaStream_t s
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  cudaError_t err = cudaLaunchKernelEx(&cfg, paged_decode_fp8_kernel<D, G>, a);
+  cudaError_t err = cudaLaunchKernelEx(&cfg, paged_decode_fp8_kernel<D, G>, tk, tv, a);
   if (err != cudaSuccess) return cuda_fail(err, "fp8 decode launch");
   if (a.max_partitions > 1) {
     const int64_t pairs = (int64_t)a.S * a.Hq;
@@ -1126,11 +1123,16 @@ extern "C" int pkv_paged_attention_decode_fp8(
   a.v8 = static_cast<const uint8_t*>(v_codes);
   a.ks = k_scales;
   a.vs = v_scales;
+  CUtensorMap tk, tv;
+  const uint64_t rows = (uint64_t)num_blocks * Hkv * block_size;
+  const uint32_t box_rows = block_size < kTileTokens ? block_size : kTileTokens;
+  if (int rc = encode_byte_rows_map(&tk, k_codes, D, rows, box_rows, D == 128)) return rc;
+  if (int rc = encode_byte_rows_map(&tv, v_codes, D, rows, box_rows, D == 128)) return rc;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc = PKV_OK;
 #define PKV_DECODE8_CASE(DD, GG) \
-  if (D == DD && G == GG) rc = launch_decode_fp8<DD, GG>(a, *dev, st);
+  if (D == DD && G == GG) rc = launch_decode_fp8<DD, GG>(tk, tv, a, *dev, st);
   PKV_DECODE8_CASE(64, 1)
   PKV_DECODE8_CASE(64, 2)
   PKV_DECODE8_CASE(64, 4)

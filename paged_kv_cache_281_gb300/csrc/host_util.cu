@@ -91,6 +91,23 @@ int encode_tile_map_3d(CUtensorMap* map, const void* base, const uint64_t dims[3
   return PKV_OK;
 }
 
+int encode_byte_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes,
+                         uint64_t rows, uint32_t box_rows, bool swizzle128) {
+  if (!encode_fn()) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)row_bytes, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(PKV_ECUDA, "cuTensorMapEncodeTiled (bytes) failed (%d) for %llu rows of %llu",
+                (int)r, (unsigned long long)rows, (unsigned long long)row_bytes);
+  return PKV_OK;
+}
+
 int check_launch(const char* what) {
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return cuda_fail(err, what);

@@ -33,6 +33,11 @@ int encode_tile_map_2d(CUtensorMap* map, const void* base, uint64_t inner_elems,
 int encode_tile_map_3d(CUtensorMap* map, const void* base, const uint64_t dims[3],
                        const uint64_t strides_bytes[2], const uint32_t box[3]);
 
+// `rows` rows of `row_bytes` bytes (a multiple of 16, at most 128 when
+// swizzled), tiles of box_rows whole rows, 128-byte swizzled or plain.
+int encode_byte_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes,
+                         uint64_t rows, uint32_t box_rows, bool swizzle128);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace pkv
