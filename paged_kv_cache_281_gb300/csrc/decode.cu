@@ -754,9 +754,11 @@ __global__ void __launch_bounds__(kThreads, 3)
           kw[4 * v] = u.x, kw[4 * v + 1] = u.y, kw[4 * v + 2] = u.z, kw[4 * v + 3] = u.w;
         }
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks)
-          mma_f16_16816(sc[j], qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(kw[ks] & 0xffffu),
-                        e4m3x2_to_f16x2(kw[ks] >> 16));
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t b0, b1;
+          e4m3x4_to_f16x4(kw[ks], b0, b1);
+          mma_f16_16816(sc[j], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+        }
       }
 
       float x[4];
@@ -799,10 +801,11 @@ __global__ void __launch_bounds__(kThreads, 3)
       for (int c = 0; c < D / 16; ++c) {
         uint32_t r0, r1;
         ldmatrix_b8_16x16_trans(vcodes + code_off<D>(lane & 15, c), r0, r1);
-        mma_f16_16816(o[2 * c], pa0, pl0, pa2, pl2, e4m3x2_to_f16x2(r0 & 0xffffu),
-                      e4m3x2_to_f16x2(r0 >> 16));
-        mma_f16_16816(o[2 * c + 1], pa0, pl0, pa2, pl2, e4m3x2_to_f16x2(r1 & 0xffffu),
-                      e4m3x2_to_f16x2(r1 >> 16));
+        uint32_t b0, b1, b2, b3;
+        e4m3x4_to_f16x4(r0, b0, b1);
+        e4m3x4_to_f16x4(r1, b2, b3);
+        mma_f16_16816(o[2 * c], pa0, pl0, pa2, pl2, b0, b1);
+        mma_f16_16816(o[2 * c + 1], pa0, pl0, pa2, pl2, b2, b3);
       }
       if (valid < kTileTokens) fence_proxy_async_smem();  // zeroing stores before TMA reuse
       __syncwarp();

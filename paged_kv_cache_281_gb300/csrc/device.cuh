@@ -201,6 +201,16 @@ __device__ __forceinline__ float f16_hi_to_f32(uint32_t packed) {
   return __half2float(__ushort_as_half((unsigned short)(packed >> 16)));
 }
 
+// Four e4m3 codes (lowest byte first) -> two registers of two fp16 values
+// each (exact): lo holds codes 0, 1 and hi codes 2, 3, low half first.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t four_codes, uint32_t& lo,
+                                                uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_codes));
+}
+
 // Two e4m3 codes (low byte first) -> two fp16 values (exact), low half first.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   uint32_t r;
