@@ -245,6 +245,43 @@ int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
                                int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * paged_attention_decode_shared — the same decode for a batch in which
+ * groups of sequences share their first tokens' physical blocks (parallel
+ * samples of one prompt: "Batching, Scheduling, and Paging", section Block
+ * sharing). The shared prefix of a group is read once for up to 16 / (Hq /
+ * Hkv) members at a time (their query heads fill one 16-row MMA operand),
+ * instead of once per member; each member's remaining tokens are decoded
+ * as usual and the partial results merged. Results equal those of
+ * pkv_paged_attention_decode up to floating-point rounding.
+ *   group_start   : int32 [n_groups + 1] (device), members of group g are
+ *                   group_members[group_start[g] .. group_start[g+1]).
+ *   group_members : int32 (device), sequence indices; a sequence belongs to
+ *                   at most one group; sequences in no group are decoded
+ *                   alone.
+ *   group_shared  : int32 [n_groups] (device): the number of leading tokens
+ *                   whose block-table entries are identical for every member
+ *                   (the caller's guarantee; the kernel reads the first
+ *                   member's table for them). It is cut to whole 16-token
+ *                   tiles and to the shortest member.
+ *   workspace     : pkv_decode_shared_workspace_bytes() bytes.
+ * Other arguments as in pkv_paged_attention_decode. Bad group entries
+ * (indices outside 0..S-1, decreasing starts) are skipped and recorded
+ * (PKV_EDEVICE).
+ * ---------------------------------------------------------------------- */
+int pkv_decode_shared_workspace_bytes(int32_t S, int32_t Hq, int32_t D,
+                                      int32_t max_context_len, int32_t partition_size,
+                                      size_t* out);
+int pkv_paged_attention_decode_shared(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                      int32_t max_context_len, const int32_t* group_start,
+                                      const int32_t* group_members, const int32_t* group_shared,
+                                      int32_t n_groups, int32_t S, int32_t Hq, int32_t Hkv,
+                                      int32_t D, int32_t block_size, int32_t num_blocks,
+                                      float scale, int32_t partition_size, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * paged_attention_decode_noalloc — the same decode as above, for callers that
  * cannot provide device scratch memory (a plugin handed only its inputs and
  * outputs, an engine whose KV pool already holds all free HBM, a decode loop

@@ -46,6 +46,10 @@ SIGNATURES = {
     "pkv_check_status": (ctypes.c_int, [vp, vp]),
     "pkv_debug_set_wait": (ctypes.c_int, [i32, u64]),
     "pkv_kv_append": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, vp, vp]),
+    "pkv_decode_shared_workspace_bytes": (ctypes.c_int, [i32, i32, i32, i32, i32, P(sz)]),
+    "pkv_paged_attention_decode_shared": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, vp, i32, vp, vp,
+                                                         vp, i32, i32, i32, i32, i32, i32, i32,
+                                                         f32, i32, vp, sz, vp, vp]),
     "pkv_kv_append_fp8": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp,
                                          vp]),
     "pkv_paged_attention_decode_fp8": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32,

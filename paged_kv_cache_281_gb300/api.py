@@ -28,7 +28,8 @@ __all__ = [
     "NOALLOC_SCRATCH_BYTES", "pkv_prefill_workspace_bytes",
     "pkv_paged_attention_prefill", "pkv_status_reset", "pkv_check_status",
     "pkv_debug_set_wait", "new_status", "new_fp8_pools", "pkv_kv_append_fp8",
-    "pkv_paged_attention_decode_fp8",
+    "pkv_paged_attention_decode_fp8", "pkv_decode_shared_workspace_bytes",
+    "pkv_paged_attention_decode_shared",
 ]
 
 
@@ -288,6 +289,48 @@ def pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_l
         block_tables.data_ptr(), int(block_tables.shape[1]), context_lens.data_ptr(),
         int(max_context_len), S, Hq, Hkv, D, B, N, float(scale), int(partition_size),
         workspace.data_ptr(), int(workspace.numel()), _ptr(status), _stream(stream)))
+
+
+# ---------------------------------------------------------------- shared prefixes
+
+def pkv_decode_shared_workspace_bytes(S: int, Hq: int, D: int, max_context_len: int,
+                                      partition_size: int = 0) -> int:
+    out = ctypes.c_size_t()
+    check(lib().pkv_decode_shared_workspace_bytes(int(S), int(Hq), int(D), int(max_context_len),
+                                                  int(partition_size), ctypes.byref(out)))
+    return out.value
+
+
+def pkv_paged_attention_decode_shared(out, q, k_cache, v_cache, block_tables, context_lens,
+                                      max_context_len: int, group_start, group_members,
+                                      group_shared, scale: float, workspace,
+                                      partition_size: int = 0, status=None, stream=None) -> None:
+    """Decode where groups of sequences share their first tokens' blocks: each
+    group's shared prefix is read once for several members."""
+    N, Hkv, B, D = _pool_shape(k_cache, v_cache)
+    _dev(q, "q", torch.bfloat16, 3)
+    _dev(out, "out", torch.bfloat16, 3)
+    _dev(block_tables, "block_tables", torch.int32, 2)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    _dev(workspace, "workspace", torch.uint8, 1)
+    for name, t in (("group_start", group_start), ("group_members", group_members),
+                    ("group_shared", group_shared)):
+        _dev(t, name, torch.int32, 1)
+    n_groups = int(group_shared.shape[0])
+    if group_start.shape[0] != n_groups + 1:
+        raise ValueError("group_start must have n_groups + 1 entries")
+    S, Hq = int(q.shape[0]), int(q.shape[1])
+    if q.shape[2] != D or out.shape != q.shape:
+        raise ValueError("q/out must be [S, Hq, D] with the pools' D")
+    if block_tables.shape[0] != S or context_lens.shape[0] != S:
+        raise ValueError("block_tables/context_lens must have S rows")
+    check(lib().pkv_paged_attention_decode_shared(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_tables.data_ptr(), int(block_tables.shape[1]), context_lens.data_ptr(),
+        int(max_context_len), group_start.data_ptr(), group_members.data_ptr(),
+        group_shared.data_ptr(), n_groups, S, Hq, Hkv, D, B, N, float(scale),
+        int(partition_size), workspace.data_ptr(), int(workspace.numel()), _ptr(status),
+        _stream(stream)))
 
 
 # ---------------------------------------------------------------- FP8 pages

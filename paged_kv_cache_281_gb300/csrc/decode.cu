@@ -81,6 +81,15 @@ struct DecodeArgs {
   const uint8_t* v8;
   const float* ks;
   const float* vs;
+  // shared-prefix decode: groups of sequences whose first tokens share blocks
+  const int32_t* grp_start;    // [n_groups + 1]
+  const int32_t* grp_members;  // sequence indices
+  const int32_t* grp_shared;   // [n_groups] tokens all members share
+  int32_t n_groups;
+  int32_t members_per_item;    // 16 / G
+  int32_t item_cap;
+  int4* gitems;                // (kind, id, partition, chunk)
+  int32_t* seq_shared;         // [S] shared tokens processed by group items (0: none)
 };
 
 // Lists the work items: pass 0 emits every full partition (s, p), pass 1 the
@@ -450,7 +459,11 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a)
   const int L = __ldg(a.context_lens + s);
   if (L < 1 || L > a.max_context_len) return;
   const int P = a.partition_tiles * kTileTokens;
-  const int np = (L + P - 1) / P;
+  int np = (L + P - 1) / P;
+  if (a.seq_shared) {  // shared-prefix decode: shared partitions, then private ones
+    const int shr = __ldg(a.seq_shared + s);
+    np = (shr + P - 1) / P + (L - shr + P - 1) / P;
+  }
   if (np <= 1) return;
   const float2* ml = a.ws_ml + sh * a.max_partitions;
   float M = -INFINITY;
@@ -855,6 +868,416 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Shared-prefix decode ("Batching, Scheduling, and Paging", section Block
+// sharing: parallel samples point at the same physical blocks for their
+// common prefix). A group's members share their first tokens' blocks, so the
+// group's prefix is read once for up to 16 / G members: their (member, query
+// head) pairs form the 16 rows of the MMA operand. The rest of each member's
+// context is decoded as usual. A member's partial states are its shared
+// partitions followed by its private ones; the combine kernel merges them.
+//
+// Item kinds: 1 = (group, shared partition, member chunk), 0 = (sequence,
+// private partition). Built by one CTA with atomics (the item order does not
+// affect any result: each item's arithmetic depends only on its own data and
+// the merge runs in partition order).
+__global__ void __launch_bounds__(1024) decode_group_plan_kernel(DecodeArgs a) {
+  __shared__ int32_t s_n;
+  const int tid = threadIdx.x;
+  const int P = a.partition_tiles * kTileTokens;
+  const int M = a.members_per_item;
+  grid_dep_launch();
+  if (tid == 0) s_n = 0;
+  for (int s = tid; s < a.S; s += 1024) a.seq_shared[s] = 0;
+  __syncthreads();
+  for (int g = tid; g < a.n_groups; g += 1024) {
+    const int b = __ldg(a.grp_start + g), e = __ldg(a.grp_start + g + 1);
+    if (b < 0 || e < b) {
+      record_status(a.status, PKV_EDEVICE, g, kKernelDecodePlan);
+      continue;
+    }
+    int minL = 1 << 30;
+    bool bad = false;
+    for (int i = b; i < e; ++i) {
+      const int s = __ldg(a.grp_members + i);
+      if (s < 0 || s >= a.S) {
+        bad = true;
+        break;
+      }
+      const int L = __ldg(a.context_lens + s);
+      minL = min(minL, (L < 1 || L > a.max_context_len) ? 0 : L);
+    }
+    if (bad || e == b) {
+      if (bad) record_status(a.status, PKV_EDEVICE, g, kKernelDecodePlan);
+      continue;
+    }
+    // whole tiles only, and never past a member's end
+    const int sh = min(max(__ldg(a.grp_shared + g), 0), minL) / kTileTokens * kTileTokens;
+    if (sh == 0) continue;
+    for (int i = b; i < e; ++i) a.seq_shared[__ldg(a.grp_members + i)] = sh;
+    const int nsp = (sh + P - 1) / P, chunks = (e - b + M - 1) / M;
+    const int k = atomicAdd(&s_n, nsp * chunks);
+    if (k + nsp * chunks > a.item_cap) {
+      record_status(a.status, PKV_EDEVICE, g, kKernelDecodePlan);
+      continue;
+    }
+    for (int p = 0; p < nsp; ++p)
+      for (int c = 0; c < chunks; ++c) a.gitems[k + p * chunks + c] = make_int4(1, g, p, c);
+  }
+  __syncthreads();
+  for (int s = tid; s < a.S; s += 1024) {
+    const int L = __ldg(a.context_lens + s);
+    if (L < 1 || L > a.max_context_len) {
+      record_status(a.status, PKV_EDEVICE, L, kKernelDecodePlan);
+      continue;
+    }
+    const int sh = a.seq_shared[s];
+    const int np = (L - sh + P - 1) / P;
+    if (np == 0) continue;
+    const int k = atomicAdd(&s_n, np);
+    if (k + np > a.item_cap) {
+      record_status(a.status, PKV_EDEVICE, s, kKernelDecodePlan);
+      continue;
+    }
+    for (int p = 0; p < np; ++p) a.gitems[k + p] = make_int4(0, s, p, 0);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    *a.n_items = min(s_n, a.item_cap);
+    *a.ticket = 0;
+  }
+}
+
+// Decode of group items: up to 16 rows (member, query head) per kv head; each
+// thread owns rows g and g + 8 of the MMA fragments. P enters the P V product
+// as two MMAs (bf16 hi, then lo), since all 16 operand rows may be in use.
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 2)
+    paged_decode_group_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                              const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
+  using C = Cfg<D>;
+  constexpr int KS = D / 16;
+  constexpr int NT = D / 8;
+  constexpr int M = 16 / G;  // members per item
+  extern __shared__ uint8_t dsm[];
+  __shared__ __align__(8) uint64_t bars[kWarps][C::kStages];
+  __shared__ int32_t s_next;
+  __shared__ int32_t s_abort;
+  __shared__ int32_t s_mem[M];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t dsm_u32 = smem_u32(dsm);
+  const uint32_t base = (dsm_u32 + 1023u) & ~1023u;
+  uint8_t* base_ptr = dsm + (base - dsm_u32);
+  const uint32_t ring = base + warp * C::kRingBytes;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < C::kStages; ++st) mbar_init(smem_u32(&bars[warp][st]), 1);
+    fence_barrier_init();
+  }
+  grid_dep_launch();
+  grid_dep_wait();
+  if (tid == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+    s_abort = 0;
+    s_next = atomicAdd(a.ticket, 1);
+  }
+  __syncthreads();
+  const int total = __ldg(a.n_items) * a.Hkv;
+  const int P = a.partition_tiles * kTileTokens;
+  uint32_t phase = 0;
+  int cur = s_next;
+
+  while (cur < total) {
+    __syncthreads();
+    const int4 item = a.gitems[cur / a.Hkv];
+    const int kvh = cur % a.Hkv;
+    int nm, first, r_begin, r_end;  // members, token range
+    if (item.x == 1) {
+      const int b = __ldg(a.grp_start + item.y) + item.w * M;
+      nm = min(M, __ldg(a.grp_start + item.y + 1) - b);
+      first = __ldg(a.grp_members + b);
+      const int sh = a.seq_shared[first];
+      r_begin = item.z * P;
+      r_end = min(r_begin + P, sh);
+      if (tid < nm) s_mem[tid] = __ldg(a.grp_members + b + tid);
+    } else {
+      nm = 1;
+      first = item.y;
+      const int sh = a.seq_shared[first];
+      r_begin = sh + item.z * P;
+      r_end = min(r_begin + P, __ldg(a.context_lens + first));
+      if (tid == 0) s_mem[0] = first;
+    }
+    if (tid == 0) s_next = atomicAdd(a.ticket, 1);
+    __syncthreads();
+    const int t_begin = r_begin / kTileTokens;
+    const int t_end = (r_end + kTileTokens - 1) / kTileTokens;
+    const int n_item = t_end - t_begin;
+    const int n_mine = n_item > warp ? (n_item - warp + kWarps - 1) / kWarps : 0;
+    const int32_t* bt = a.block_tables + (int64_t)first * a.max_blocks_per_seq;
+
+    TileRows mine = {{-1, -1}, 0u};
+    int chunk0 = 0;
+    if (lane < n_mine) mine = tile_rows<D>(a, bt, kvh, t_begin + warp + lane * kWarps, r_end);
+    auto issue = [&](int k, uint32_t st) {
+      if (k - chunk0 >= 32) {
+        chunk0 += 32;
+        mine = {{-1, -1}, 0u};
+        if (chunk0 + lane < n_mine)
+          mine = tile_rows<D>(a, bt, kvh, t_begin + warp + (chunk0 + lane) * kWarps, r_end);
+      }
+      const int src = k - chunk0;
+      const int32_t q0 = __shfl_sync(0xffffffffu, mine.row[0], src);
+      const int32_t q1 = __shfl_sync(0xffffffffu, mine.row[1], src);
+      const uint32_t by = __shfl_sync(0xffffffffu, mine.bytes, src);
+      if (lane == 0)
+        issue_tile_rows<D>(&tmap_k, &tmap_v, a.block_size, q0, q1, by, ring + st * C::kStageBytes,
+                           smem_u32(&bars[warp][st]));
+    };
+    {
+      const int npro = n_mine < C::kStages ? n_mine : C::kStages;
+      for (int k = 0; k < npro; ++k) issue(k, k);
+    }
+
+    // Q fragments for rows g and g + 8: row r is (member r / G, head r % G)
+    uint32_t qa[KS][4];
+    {
+      const int r0 = g, r1 = g + 8;
+      const bool l0 = r0 / G < nm, l1 = r1 / G < nm;
+      const __nv_bfloat16* q0 =
+          a.q + ((int64_t)s_mem[l0 ? r0 / G : 0] * a.Hq + kvh * G + r0 % G) * D;
+      const __nv_bfloat16* q1 =
+          a.q + ((int64_t)s_mem[l1 ? r1 / G : 0] * a.Hq + kvh * G + r1 % G) * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qa[ks][0] = l0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + ks * 16 + 2 * t)) : 0u;
+        qa[ks][1] = l1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + ks * 16 + 2 * t)) : 0u;
+        qa[ks][2] = l0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + ks * 16 + 8 + 2 * t)) : 0u;
+        qa[ks][3] = l1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + ks * 16 + 8 + 2 * t)) : 0u;
+      }
+    }
+
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    float o[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+
+    for (int k = 0; k < n_mine; ++k) {
+      const int st = k % C::kStages;
+      const int tile = t_begin + warp + k * kWarps;
+      const uint32_t bar = smem_u32(&bars[warp][st]);
+      const uint32_t par = (phase >> st) & 1u;
+      const bool landed = mbar_wait_bounded(bar, par, a.timeout_ns, a.force_timeout);
+      if (!__all_sync(0xffffffffu, landed)) {
+        if (lane == 0) {
+          record_status(a.status, PKV_ETIMEOUT, k, kKernelDecode);
+          s_abort = 1;
+        }
+        uint32_t ph = phase;
+        const int last = min(k + C::kStages, n_mine);
+        for (int j = k; j < last; ++j) {
+          const int sj = j % C::kStages;
+          mbar_wait_bounded(smem_u32(&bars[warp][sj]), (ph >> sj) & 1u, 4 * a.timeout_ns, 0);
+          ph ^= 1u << sj;
+        }
+        phase = ph;
+        break;
+      }
+      phase ^= 1u << st;
+      const uint32_t stage = ring + st * C::kStageBytes;
+      const int valid = min(kTileTokens, r_end - tile * kTileTokens);
+      if (valid < kTileTokens) {
+        const int n16 = (kTileTokens - valid) * C::kHalves * 8;
+        for (int i = lane; i < n16; i += 32) {
+          const int row = valid + i / (C::kHalves * 8);
+          const int rem = i % (C::kHalves * 8);
+          const uint32_t addr = stage + C::kTensorBytes + (rem >> 3) * C::kHalfBytes + row * 128 +
+                                (rem & 7) * 16;
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u)
+                       : "memory");
+        }
+        __syncwarp();
+      }
+
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int tok = (lane & 7) + ((lane >> 4) << 3);
+        const int csel = (lane >> 3) & 1;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const int chunk = 2 * ks + csel;
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(stage + (chunk >> 3) * C::kHalfBytes + swz128(tok, chunk & 7), b0, b1, b2,
+                      b3);
+          mma_bf16_16816(sc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+          mma_bf16_16816(sc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+        }
+      }
+
+      // online softmax on rows g (fragment entries 0, 1) and g + 8 (2, 3)
+      float pr[2][4];
+      float alpha[2];
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        float x[4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            x[2 * j + e] =
+                (8 * j + 2 * t + e < valid) ? sc[j][2 * hr + e] * a.scale_log2 : -INFINITY;
+        float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m[hr], mx);
+        alpha[hr] = fast_exp2(m[hr] - m_new);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pr[hr][i] = fast_exp2(x[i] - m_new);
+        l[hr] = l[hr] * alpha[hr] + ((pr[hr][0] + pr[hr][1]) + (pr[hr][2] + pr[hr][3]));
+        m[hr] = m_new;
+      }
+      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          o[nt][0] *= alpha[0];
+          o[nt][1] *= alpha[0];
+          o[nt][2] *= alpha[1];
+          o[nt][3] *= alpha[1];
+        }
+      }
+      // P = P_hi + P_lo, each a full 16-row bf16 operand
+      uint32_t ph[4], pl[4];
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float p0 = pr[hr][2 * j], p1 = pr[hr][2 * j + 1];
+          const uint32_t hi = pack_bf16x2(p0, p1);
+          ph[2 * j + hr] = hi;  // a0: row g keys 2t; a1: row g+8; a2/a3: keys 8+2t
+          pl[2 * j + hr] = pack_bf16x2(p0 - bf16_lo_to_f32(hi), p1 - bf16_hi_to_f32(hi));
+        }
+      {
+        const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int csel = lane >> 4;
+#pragma unroll
+        for (int n2 = 0; n2 < NT / 2; ++n2) {
+          const int chunk = 2 * n2 + csel;
+          uint32_t r0, r1, r2, r3;
+          ldmatrix_x4_trans(
+              stage + C::kTensorBytes + (chunk >> 3) * C::kHalfBytes + swz128(tok, chunk & 7), r0,
+              r1, r2, r3);
+          mma_bf16_16816(o[2 * n2], ph[0], ph[1], ph[2], ph[3], r0, r1);
+          mma_bf16_16816(o[2 * n2], pl[0], pl[1], pl[2], pl[3], r0, r1);
+          mma_bf16_16816(o[2 * n2 + 1], ph[0], ph[1], ph[2], ph[3], r2, r3);
+          mma_bf16_16816(o[2 * n2 + 1], pl[0], pl[1], pl[2], pl[3], r2, r3);
+        }
+      }
+      if (valid < kTileTokens) fence_proxy_async_smem();
+      __syncwarp();
+      if (k + C::kStages < n_mine) issue(k + C::kStages, st);
+    }
+
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 1);
+      l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 2);
+    }
+    __syncthreads();
+    if (s_abort) return;
+    constexpr int R = 16;
+    float2* cml = reinterpret_cast<float2*>(base_ptr);     // [kWarps][R]
+    float* co = reinterpret_cast<float*>(base_ptr + 512);  // [kWarps][R][D]
+    {
+      if (t == 0) {
+        cml[warp * R + g] = make_float2(m[0], l[0]);
+        cml[warp * R + g + 8] = make_float2(m[1], l[1]);
+      }
+      float* row0 = co + (warp * R + g) * D;
+      float* row1 = co + (warp * R + g + 8) * D;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        *reinterpret_cast<float2*>(row0 + nt * 8 + 2 * t) = make_float2(o[nt][0], o[nt][1]);
+        *reinterpret_cast<float2*>(row1 + nt * 8 + 2 * t) = make_float2(o[nt][2], o[nt][3]);
+      }
+    }
+    __syncthreads();
+    const int rows = nm * G;
+    for (int e = tid; e < rows * D; e += kThreads) {
+      const int r = e / D, d = e % D;
+      float Mx = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) Mx = fmaxf(Mx, cml[w * R + r].x);
+      float lsum = 0.f, acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float sw = fast_exp2(cml[w * R + r].x - Mx);
+        lsum += sw * cml[w * R + r].y;
+        acc += sw * co[(w * R + r) * D + d];
+      }
+      const int sq = s_mem[r / G];
+      const int L = __ldg(a.context_lens + sq);
+      const int shr = a.seq_shared[sq];
+      const int nsp = (shr + P - 1) / P;
+      const int nparts = nsp + (L - shr + P - 1) / P;
+      const int part = item.x == 1 ? item.z : nsp + item.z;
+      const int64_t qh = (int64_t)sq * a.Hq + kvh * G + r % G;
+      if (nparts == 1) {
+        a.out[qh * D + d] = __float2bfloat16_rn(acc / lsum);
+      } else {
+        const int64_t idx = qh * a.max_partitions + part;
+        a.ws_o[idx * D + d] = acc;
+        if (d == 0) a.ws_ml[idx] = make_float2(Mx, lsum);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    cur = s_next;
+  }
+}
+
+template <int D, int G>
+int launch_decode_group(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                        const DeviceInfo& dev, cudaStream_t stream) {
+  using C = Cfg<D>;
+  static std::once_flag once;
+  static int blocks_per_sm = 0;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, []() {
+    attr_err = cudaFuncSetAttribute(paged_decode_group_kernel<D, G>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &blocks_per_sm, paged_decode_group_kernel<D, G>, kThreads, C::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "shared decode kernel attributes");
+  if (blocks_per_sm < 1) return fail(PKV_ECUDA, "shared decode kernel does not fit on an SM");
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  decode_group_plan_kernel<<<1, 1024, 0, stream>>>(a);
+  if (int rc = check_launch("shared decode plan")) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(dev.sm_count * blocks_per_sm));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, paged_decode_group_kernel<D, G>, tk, tv, a);
+  if (err != cudaSuccess) return cuda_fail(err, "shared decode launch");
+  const int64_t pairs = (int64_t)a.S * a.Hq;
+  cfg.gridDim = dim3((unsigned)((pairs + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  err = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, a);
+  if (err != cudaSuccess) return cuda_fail(err, "decode combine launch");
+  return PKV_OK;
+}
+
 int resolve_partition(int32_t partition_size, int32_t* tiles) {
   const int32_t P = partition_size == 0 ? kDefaultPartition : partition_size;
   PKV_REQUIRE(P >= kTileTokens && P % kTileTokens == 0 && P <= (1 << 20),
@@ -1145,6 +1568,137 @@ extern "C" int pkv_paged_attention_decode_fp8(
   PKV_DECODE8_CASE(128, 4)
   PKV_DECODE8_CASE(128, 8)
 #undef PKV_DECODE8_CASE
+  if (rc) return rc;
+  return ok();
+}
+
+// Shared-prefix decode: workspace (header, items, per-sequence shared
+// lengths, partial states with one extra partition per sequence).
+struct WsShared {
+  size_t items_off, shared_off, ml_off, o_off, total;
+  int64_t item_cap, parts;
+};
+
+WsShared ws_shared_layout(int64_t S, int64_t Hq, int64_t D, int64_t max_parts) {
+  WsShared w;
+  w.parts = max_parts + 1;
+  w.item_cap = 2 * S * max_parts + 1;
+  w.items_off = 256;
+  w.shared_off = align256(w.items_off + w.item_cap * sizeof(int4));
+  w.ml_off = align256(w.shared_off + S * sizeof(int32_t));
+  w.o_off = align256(w.ml_off + S * Hq * w.parts * sizeof(float2));
+  w.total = align256(w.o_off + S * Hq * w.parts * D * sizeof(float));
+  return w;
+}
+
+extern "C" int pkv_decode_shared_workspace_bytes(int32_t S, int32_t Hq, int32_t D,
+                                                 int32_t max_context_len, int32_t partition_size,
+                                                 size_t* out) {
+  PKV_REQUIRE(out, "pkv_decode_shared_workspace_bytes: out is NULL");
+  PKV_REQUIRE(S >= 0 && Hq > 0 && (D == 64 || D == 128) && max_context_len >= 0,
+              "pkv_decode_shared_workspace_bytes: bad sizes");
+  int32_t tiles = 0;
+  if (int rc = resolve_partition(partition_size, &tiles)) return rc;
+  const int64_t P = (int64_t)tiles * kTileTokens;
+  const int64_t max_parts = max_context_len > 0 ? (max_context_len + P - 1) / P : 1;
+  *out = ws_shared_layout(S, Hq, D, max_parts).total;
+  return ok();
+}
+
+extern "C" int pkv_paged_attention_decode_shared(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t max_context_len, const int32_t* group_start, const int32_t* group_members,
+    const int32_t* group_shared, int32_t n_groups, int32_t S, int32_t Hq, int32_t Hkv, int32_t D,
+    int32_t block_size, int32_t num_blocks, float scale, int32_t partition_size, void* workspace,
+    size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  PKV_REQUIRE(S >= 0 && n_groups >= 0, "decode_shared: S and n_groups must be >= 0");
+  PKV_REQUIRE(Hkv > 0 && Hq > 0 && Hq % Hkv == 0,
+              "decode_shared: Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  const int G = Hq / Hkv;
+  PKV_REQUIRE(G == 1 || G == 2 || G == 4 || G == 8,
+              "decode_shared: Hq/Hkv must be 1, 2, 4 or 8 (got %d)", G);
+  PKV_REQUIRE(D == 64 || D == 128, "decode_shared: D must be 64 or 128 (got %d)", D);
+  PKV_REQUIRE(block_size == 8 || block_size == 16 || block_size == 32,
+              "decode_shared: block_size must be 8, 16 or 32 (got %d)", block_size);
+  PKV_REQUIRE(num_blocks > 0 && (int64_t)num_blocks * Hkv * block_size < (int64_t(1) << 31),
+              "decode_shared: num_blocks * Hkv * block_size must be in [1, 2^31)");
+  PKV_REQUIRE(max_context_len >= 1, "decode_shared: max_context_len must be >= 1");
+  PKV_REQUIRE((int64_t)max_blocks_per_seq * block_size >= max_context_len,
+              "decode_shared: max_context_len %d exceeds max_blocks_per_seq * block_size",
+              max_context_len);
+  PKV_REQUIRE(std::isfinite(scale), "decode_shared: scale must be finite");
+  if (S == 0) return ok();
+  PKV_REQUIRE(out && q && k_cache && v_cache && block_tables && context_lens && workspace &&
+                  (n_groups == 0 || (group_start && group_members && group_shared)),
+              "decode_shared: NULL pointer");
+  PKV_REQUIRE(aligned16(out) && aligned16(q) && aligned16(k_cache) && aligned16(v_cache),
+              "decode_shared: bf16 arrays must be 16-byte aligned");
+  PKV_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0,
+              "decode_shared: workspace must be 256-byte aligned");
+  int32_t tiles = 0;
+  if (int rc = resolve_partition(partition_size, &tiles)) return rc;
+  const int64_t P = (int64_t)tiles * kTileTokens;
+  const int64_t max_parts = (max_context_len + P - 1) / P;
+  const WsShared ws = ws_shared_layout(S, Hq, D, max_parts);
+  PKV_REQUIRE(workspace_bytes >= ws.total, "decode_shared: workspace has %zu bytes, needs %zu",
+              workspace_bytes, ws.total);
+  PKV_REQUIRE(ws.item_cap < (int64_t(1) << 31) / 16, "decode_shared: batch too large");
+  const DeviceInfo* dev = nullptr;
+  if (int rc = current_device_info(&dev)) return rc;
+
+  CUtensorMap tk, tv;
+  const uint64_t rows = (uint64_t)num_blocks * Hkv * block_size;
+  const uint32_t box_rows = block_size < kTileTokens ? block_size : kTileTokens;
+  if (int rc = encode_tile_map_2d(&tk, k_cache, D, rows, (uint64_t)D * 2, 64, box_rows)) return rc;
+  if (int rc = encode_tile_map_2d(&tv, v_cache, D, rows, (uint64_t)D * 2, 64, box_rows)) return rc;
+
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  DecodeArgs a = {};
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.S = S;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.max_context_len = max_context_len;
+  a.partition_tiles = tiles;
+  a.max_partitions = (int32_t)ws.parts;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.ticket = reinterpret_cast<int32_t*>(wsb);
+  a.n_items = reinterpret_cast<int32_t*>(wsb) + 1;
+  a.gitems = reinterpret_cast<int4*>(wsb + ws.items_off);
+  a.seq_shared = reinterpret_cast<int32_t*>(wsb + ws.shared_off);
+  a.ws_ml = reinterpret_cast<float2*>(wsb + ws.ml_off);
+  a.ws_o = reinterpret_cast<float*>(wsb + ws.o_off);
+  a.status = dev_status;
+  const WaitConfig wc = wait_config();
+  a.timeout_ns = wc.timeout_ns;
+  a.force_timeout = wc.force_timeout;
+  a.grp_start = group_start;
+  a.grp_members = group_members;
+  a.grp_shared = group_shared;
+  a.n_groups = n_groups;
+  a.members_per_item = 16 / G;
+  a.item_cap = (int32_t)ws.item_cap;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = PKV_OK;
+#define PKV_DECODEG_CASE(DD, GG) \
+  if (D == DD && G == GG) rc = launch_decode_group<DD, GG>(tk, tv, a, *dev, st);
+  PKV_DECODEG_CASE(64, 1)
+  PKV_DECODEG_CASE(64, 2)
+  PKV_DECODEG_CASE(64, 4)
+  PKV_DECODEG_CASE(64, 8)
+  PKV_DECODEG_CASE(128, 1)
+  PKV_DECODEG_CASE(128, 2)
+  PKV_DECODEG_CASE(128, 4)
+  PKV_DECODEG_CASE(128, 8)
+#undef PKV_DECODEG_CASE
   if (rc) return rc;
   return ok();
 }

@@ -189,6 +189,41 @@ def decode_shared_prefix(w, d: DeviceSharedPrefix, partition_size=0) -> torch.Te
     return out
 
 
+def shared_groups(w, d: DeviceSharedPrefix, shared=None):
+    """Group arrays for pkv_paged_attention_decode_shared: one group per
+    prompt (its samples), sharing the leading block-table entries that are
+    identical for all of them (``shared`` overrides the token count)."""
+    B, n = w.block_size, w.n_samples
+    start = np.arange(0, w.S + 1, n, dtype=np.int32)
+    members = np.arange(w.S, dtype=np.int32)
+    sh = []
+    for p in range(w.n_prompts):
+        rows = d.tables[p * n:(p + 1) * n]
+        lens = w.context_lens[p * n:(p + 1) * n]
+        nb = min(-(-int(L) // B) for L in lens)
+        same = 0
+        while same < nb and np.all(rows[:, same] == rows[0, same]):
+            same += 1
+        sh.append(same * B if shared is None else shared)
+    return start, members, np.asarray(sh, dtype=np.int32)
+
+
+def decode_shared_grouped(w, d: DeviceSharedPrefix, groups=None, partition_size=0):
+    """Shared-prefix decode of the workload through the group path."""
+    dev = d.q.device
+    start, members, sh = groups if groups is not None else shared_groups(w, d)
+    out = torch.full((w.S, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(pkv.pkv_decode_shared_workspace_bytes(w.S, w.Hq, w.D, d.max_context_len,
+                                                           partition_size),
+                     dtype=torch.uint8, device=dev)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    pkv.pkv_paged_attention_decode_shared(out, d.q, d.k_cache, d.v_cache, d.block_tables,
+                                          d.context_lens, d.max_context_len, t(start),
+                                          t(members), t(sh), w.scale, ws,
+                                          partition_size=partition_size, status=d.status)
+    return out
+
+
 # ---------------------------------------------------------------- trace
 
 class DeviceTrace:

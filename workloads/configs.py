@@ -197,12 +197,11 @@ class SharedPrefixWorkload:
         return toks * 2 * self.Hkv * self.D * 2
 
 
-def config4(variant: str = "a", n_prompts: int = 64, n_samples: int = 4,
-            tail_max: int = 512) -> SharedPrefixWorkload:
-    seed = SEED_BASE + 4
-    prefix = {"a": 1024, "b": 1032}[variant]
-    B, Hq, Hkv, D = 16, 32, 8, 128
-    tails = generator(seed, 0).integers(0, tail_max, size=(n_prompts, n_samples),
+def make_shared_prefix_workload(name: str, n_prompts: int, n_samples: int, prefix: int,
+                                tail_max: int, Hq: int, Hkv: int, D: int, block_size: int,
+                                seed: int, tail_min: int = 0) -> SharedPrefixWorkload:
+    B = block_size
+    tails = generator(seed, 0).integers(tail_min, tail_max, size=(n_prompts, n_samples),
                                         endpoint=True).astype(np.int32)
     # Every sample may own a copy of the last shared block plus its tail blocks.
     per_prompt = -(-prefix // B)
@@ -212,7 +211,7 @@ def config4(variant: str = "a", n_prompts: int = 64, n_samples: int = 4,
     free_order = generator(seed, 1).permutation(num_blocks).astype(np.int32)
     total_tail = int(tails.sum())
     return SharedPrefixWorkload(
-        name=f"shared_prefix_{variant}", n_prompts=n_prompts, n_samples=n_samples,
+        name=name, n_prompts=n_prompts, n_samples=n_samples,
         prefix_len=prefix, tails=tails, Hq=Hq, Hkv=Hkv, D=D, block_size=B,
         num_blocks=num_blocks, free_order=free_order,
         prefix_k=normal_bf16_from(generator(seed, 2), (n_prompts, prefix, Hkv, D)),
@@ -221,6 +220,15 @@ def config4(variant: str = "a", n_prompts: int = 64, n_samples: int = 4,
         tail_v=normal_bf16_from(generator(seed, 5), (total_tail, Hkv, D)),
         q=normal_bf16_from(generator(seed, 6), (n_prompts * n_samples, Hq, D)),
         scale=1.0 / math.sqrt(D))
+
+
+def config4(variant: str = "a", n_prompts: int = 64, n_samples: int = 4,
+            tail_max: int = 512) -> SharedPrefixWorkload:
+    prefix = {"a": 1024, "b": 1032}[variant]
+    w = make_shared_prefix_workload(f"shared_prefix_{variant}", n_prompts, n_samples, prefix,
+                                    tail_max, Hq=32, Hkv=8, D=128, block_size=16,
+                                    seed=SEED_BASE + 4)
+    return w
 
 
 # --------------------------------------------------------------------------
