@@ -55,9 +55,11 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", choices=["llama3_8b_gqa", "llama3_8b_gqa_fp8", "trace", "swap",
-                                           "prefix_cache"],
+                                           "prefix_cache", "shared_prefix"],
                     default="llama3_8b_gqa",
                     help="llama3_8b_gqa_fp8: the headline step over FP8 (e4m3) pages; "
+                         "shared_prefix: 64 prompts x 4 samples sharing a 1024-token prefix, "
+                         "ordinary and sharing-aware decode; "
                          "trace: the 200-iteration continuous-batching workload; swap: "
                          "preemption by swapping, every block of the decode batch out to "
                          "pinned host memory and back; prefix_cache: 256 requests sharing a "
@@ -685,6 +687,90 @@ def run_fp8(args):
     return 0
 
 
+def run_shared_prefix(args):
+    """64 prompts x 4 samples sharing a 1024-token prefix (tails U[0,512];
+    32/8 heads, D=128, B=16): the ordinary decode reads every prefix page once
+    per sample, the sharing-aware decode once per group of samples. Reports
+    decode tokens per second and bytes per second both ways, on the logical
+    (per-sample) and on the unique (each page once) byte counts."""
+    import torch
+    import paged_kv_cache_281_gb300 as pkv
+    from tests.gpu_harness import setup_shared_prefix, shared_groups
+    from workloads import config4
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    w = config4("a")
+    d = setup_shared_prefix(w)
+    start, members, sh = shared_groups(w, d)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    gs, gm, gsh = t(start), t(members), t(sh)
+    out = torch.empty(w.S, w.Hq, w.D, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(pkv.pkv_decode_workspace_bytes(w.S, w.Hq, w.D, d.max_context_len),
+                         pkv.pkv_decode_shared_workspace_bytes(w.S, w.Hq, w.D,
+                                                               d.max_context_len)),
+                     dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def plain():
+        pkv.pkv_paged_attention_decode(out, d.q, d.k_cache, d.v_cache, d.block_tables,
+                                       d.context_lens, d.max_context_len, w.scale, ws,
+                                       status=d.status, stream=stream)
+
+    def grouped():
+        pkv.pkv_paged_attention_decode_shared(out, d.q, d.k_cache, d.v_cache, d.block_tables,
+                                              d.context_lens, d.max_context_len, gs, gm, gsh,
+                                              w.scale, ws, status=d.status, stream=stream)
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps
+
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        plain_ms = timed(plain)
+        grouped_ms = timed(grouped)
+    pkv.pkv_check_status(d.status)
+    logical, unique = w.logical_kv_bytes(), w.unique_kv_bytes()
+    peak, peak_kind = measured_peaks()
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "shared-prefix decode: decode tokens/s per layer (sharing-aware)",
+        "value": world * w.S / (grouped_ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": grouped_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "64 prompts x 4 samples, shared 1024-token prefix (forked "
+                               "blocks), tails U[0,512], 32/8 heads, D=128, B=16",
+                   "logical_kv_bytes": logical, "unique_kv_bytes": unique,
+                   "l2": "%.2f GB of unique K/V (> 129 MB L2)" % (unique / 1e9)},
+        "ordinary_ms": plain_ms, "sharing_aware_ms": grouped_ms,
+        "speedup": plain_ms / grouped_ms,
+        "ordinary_tokens_per_s": world * w.S / (plain_ms * 1e-3),
+        "logical_gbs": {"ordinary": gbs(logical, plain_ms), "sharing_aware": gbs(logical, grouped_ms)},
+        "unique_gbs": {"ordinary": gbs(unique, plain_ms), "sharing_aware": gbs(unique, grouped_ms)},
+        "roofline": {"bound": "hbm", "kernel": "pkv_paged_attention_decode_shared (plan + group "
+                     "and private partitions + combine)", "achieved": gbs(unique, grouped_ms),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": gbs(unique, grouped_ms) / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": unique},
+        "gpu_launches": 2 * 3 * args.steps,
+        "clocks": clocks.summary(),
+        "cpu_baseline": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -695,6 +781,8 @@ def main():
         return run_swap(args)
     if args.workload == "llama3_8b_gqa_fp8":
         return run_fp8(args)
+    if args.workload == "shared_prefix":
+        return run_shared_prefix(args)
     if args.workload == "prefix_cache":
         return run_prefix_cache(args)
     import torch
