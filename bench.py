@@ -42,6 +42,10 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode attn KV GB/s and % of HBM peak; attention tokens/s per layer"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+# DRAM read + write bytes of one paged_decode_kernel<128,4> launch on this
+# workload, from ncu (profiles/decode_llama3_8b_gqa.md); None once the kernel
+# changes.
+DECODE_TRAFFIC_BYTES = 1_403_409_920
 CPU_SAMPLE_SEQS = 48
 
 
@@ -852,7 +856,9 @@ def main():
                      "partitions + combine)", "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": DECODE_TRAFFIC_BYTES if args.partition_size in (0, 1024) else None,
+                     "traffic_kernel": "paged_decode_kernel<128,4> (ncu, one launch)",
                      "algorithmic_bytes_per_launch": kv_bytes,
                      "avg_launch_ms": decode_ms},
         "gpu_launches": launches_per_step * args.steps,
