@@ -43,8 +43,8 @@ METRIC = "paged decode attn KV GB/s and % of HBM peak; attention tokens/s per la
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 # DRAM read + write bytes of one paged_decode_kernel<128,4> launch on this
-# workload, from ncu (profiles/decode_llama3_8b_gqa.md); None once the kernel
-# changes.
+# workload, taken with ncu (dram__bytes_read.sum + dram__bytes_write.sum);
+# to be set to None whenever the kernel changes.
 DECODE_TRAFFIC_BYTES = 1_403_409_920
 CPU_SAMPLE_SEQS = 48
 
