@@ -58,10 +58,12 @@ def parse_args():
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--workload", choices=["llama3_8b_gqa", "llama3_8b_gqa_fp8", "trace", "swap",
-                                           "prefix_cache", "shared_prefix"],
+    ap.add_argument("--workload", choices=["llama3_8b_gqa", "llama3_8b_gqa_fp8", "trace",
+                                           "trace_preempt", "swap", "prefix_cache",
+                                           "shared_prefix"],
                     default="llama3_8b_gqa",
                     help="llama3_8b_gqa_fp8: the headline step over FP8 (e4m3) pages; "
+                         "trace_preempt: the trace on an undersized pool with preemption; "
                          "shared_prefix: 64 prompts x 4 samples sharing a 1024-token prefix, "
                          "ordinary and sharing-aware decode; "
                          "trace: the 200-iteration continuous-batching workload; swap: "
@@ -70,6 +72,9 @@ def parse_args():
                          "1024-token system prompt, prefilled with and without the prefix "
                          "cache (separate lines; the default is the headline decode step)")
     ap.add_argument("--iterations", type=int, default=200)
+    ap.add_argument("--pool-blocks", type=int, default=9000,
+                    help="trace_preempt: KV blocks in the pool (the trace peaks near 10,400)")
+    ap.add_argument("--preempt", choices=["swap", "recompute"], default="swap")
     return ap.parse_args()
 
 
@@ -359,6 +364,156 @@ def run_trace(args):
                         sum(1 for x in stats if x[1]),
         "clocks": clocks.summary(),
         "input_generation_s": gen_s,
+        "cpu_baseline": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_trace_preempt(args):
+    """The continuous-batching trace on a pool smaller than its peak use: when
+    an append cannot get its blocks the newest running request is evicted,
+    swapped to pinned host memory (pkv_swap_blocks) or freed and recomputed
+    later. The host schedule (library allocator) is computed first; then every
+    iteration's swaps, kv_append, prefill and decode run back to back on the
+    GPU. Token values are drawn on the device (this line measures speed; the
+    parity of the same path is checked at a smaller size by the tests)."""
+    import torch
+    import paged_kv_cache_281_gb300 as pkv
+    from tests.gpu_harness import poisoned_pools
+    from tests.preemption import LibraryAllocator, PreemptingScheduler
+    from workloads import TraceConfig
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    cfg = TraceConfig(iterations=args.iterations)
+    nb, B = args.pool_blocks, cfg.block_size
+    t0 = time.perf_counter()
+    sched = PreemptingScheduler(cfg, nb, args.preempt, LibraryAllocator(nb, B),
+                                watermark=max(1, nb // 100))
+    events = [sched.step(it) for it in range(cfg.iterations)]
+    host_ms = 1e3 * (time.perf_counter() - t0)
+    dev = "cuda"
+    tg = torch.Generator(device=dev).manual_seed(0x281 + 80 + rank)
+    randn = lambda *shape: torch.randn(*shape, generator=tg, device=dev).to(torch.bfloat16)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    max_ctx = cfg.prompt_max + cfg.out_cap + cfg.chunk
+    width = -(-max_ctx // B)
+    shape = (cfg.Hkv, B, cfg.D)
+    ups, saved = [], {}
+    n_pre = n_dec = swap_bytes = flops = 0
+    for ev in events:
+        ops = []
+        for kind, rid, blocks in ev.ops:
+            bl = t(blocks)
+            if kind == "swap_out":
+                kb = torch.empty((len(blocks),) + shape, dtype=torch.bfloat16, pin_memory=True)
+                vb = torch.empty_like(kb, pin_memory=True)
+                saved[rid] = (kb, vb)
+            else:
+                kb, vb = saved.pop(rid)
+            ops.append((bl, kb, vb, kind == "swap_out"))
+            swap_bytes += 2 * kb.numel() * 2
+        pre = [w for w in ev.work if w[4] == "prefill"]
+        dec = [w for w in ev.work if w[4] == "decode"]
+        T = sum(w[3] for w in pre + dec)
+        up = {"ops": ops}
+        if T:
+            up["k"], up["v"] = randn(T, cfg.Hkv, cfg.D), randn(T, cfg.Hkv, cfg.D)
+            up["q"] = randn(T, cfg.Hq, cfg.D)
+            up["slots"] = t([s for w in pre + dec for s in w[5]])
+        if pre:
+            tables = np.zeros((len(pre), width), np.int32)
+            for i, w in enumerate(pre):
+                tables[i, :len(ev.tables[w[0]])] = ev.tables[w[0]]
+            lens = np.array([w[2] + w[3] for w in pre], np.int32)
+            cu = np.concatenate([[0], np.cumsum([w[3] for w in pre])])
+            up["pre"] = (t(cu), t(lens), t(tables), int(max(w[3] for w in pre)), int(lens.max()),
+                         int(cu[-1]))
+            for w in pre:
+                c, L = w[3], w[2] + w[3]
+                flops += 4 * cfg.D * cfg.Hq * (c * (L - c) + c * (c + 1) // 2)
+            n_pre += int(cu[-1])
+        if dec:
+            tables = np.zeros((len(dec), width), np.int32)
+            for i, w in enumerate(dec):
+                tables[i, :len(ev.tables[w[0]])] = ev.tables[w[0]]
+            lens = np.array([w[2] + w[3] for w in dec], np.int32)
+            up["dec"] = (t(lens), t(tables), int(lens.max()), len(dec))
+            n_dec += len(dec)
+        ups.append(up)
+    scale = 1.0 / math.sqrt(cfg.D)
+    ws = torch.empty(pkv.pkv_decode_workspace_bytes(cfg.max_running, cfg.Hq, cfg.D, max_ctx),
+                     dtype=torch.uint8, device=dev)
+    pws = torch.empty(256, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def one_pass(timed):
+        kc, vc = poisoned_pools(nb, cfg.Hkv, B, cfg.D)
+        status = pkv.new_status()
+        evs = []
+        for up in ups:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(5)] if timed else None
+            rec = (lambda i: e[i].record(stream)) if timed else (lambda i: None)
+            rec(0)
+            for bl, kb, vb, out in up["ops"]:
+                pkv.pkv_swap_blocks(kc, vc, bl, kb, vb, out, status=status, stream=stream)
+            rec(1)
+            if "k" in up:
+                pkv.pkv_kv_append(up["k"], up["v"], up["slots"], kc, vc, status=status,
+                                  stream=stream)
+            rec(2)
+            npre = 0
+            if "pre" in up:
+                cu, lens, tables, mq, mc, npre = up["pre"]
+                o = torch.empty(npre, cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
+                pkv.pkv_paged_attention_prefill(o, up["q"][:npre], cu, lens, kc, vc, tables, mq,
+                                                mc, scale, pws, status=status, stream=stream)
+            rec(3)
+            if "dec" in up:
+                lens, tables, mc, n = up["dec"]
+                o = torch.empty(n, cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
+                pkv.pkv_paged_attention_decode(o, up["q"][npre:], kc, vc, tables, lens, mc, scale,
+                                               ws, status=status, stream=stream)
+            rec(4)
+            if timed:
+                evs.append(e)
+        torch.cuda.synchronize()
+        pkv.pkv_check_status(status)
+        return evs
+
+    one_pass(False)
+    with ClockSampler(local) as clocks:
+        evs = one_pass(True)
+    part = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) for i in range(4)]
+    gpu_ms = sum(part)
+    tokens = n_pre + n_dec
+    preempted = sum(ev.preempted for ev in events)
+    line = {
+        "metric": "continuous-batching trace on an undersized pool (preemption by %s): attention "
+                  "query tokens/s per layer (GPU time)" % args.preempt,
+        "value": world * tokens / (gpu_ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": len(events), "warmup": 1, "ms_per_step": gpu_ms / len(events),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "trace: %d iterations, Poisson(8) arrivals, prompts U[32,1024] in "
+                               "chunks <= 512, outputs Geometric(1/256) <= 1536, <= 256 running, "
+                               "64/8 heads, D=128, B=16, pool of %d blocks (the trace peaks "
+                               "near 10,400), admission watermark %d blocks"
+                               % (cfg.iterations, nb, max(1, nb // 100)),
+                   "prefill_tokens": n_pre, "decode_tokens": n_dec,
+                   "l2": "decode reads ~0.4 GB of K/V per iteration (> 129 MB L2)"},
+        "preemptions": preempted, "swap_bytes": swap_bytes,
+        "kernel_ms": {"swap": part[0], "kv_append": part[1], "prefill": part[2],
+                      "decode": part[3]},
+        "swap_gbs": swap_bytes / (part[0] * 1e-3) / 1e9 if part[0] > 0 else None,
+        "prefill_tflops": flops / (part[2] * 1e-3) / 1e12 if part[2] > 0 else None,
+        "host_scheduler_ms": host_ms,
+        "roofline": None,
+        "gpu_launches": sum(len(u["ops"]) + ("k" in u) + ("pre" in u) + 3 * ("dec" in u)
+                            for u in ups),
+        "clocks": clocks.summary(),
         "cpu_baseline": None,
     }
     if rank == 0:
@@ -781,6 +936,8 @@ def main():
         return run_reference(args)
     if args.workload == "trace":
         return run_trace(args)
+    if args.workload == "trace_preempt":
+        return run_trace_preempt(args)
     if args.workload == "swap":
         return run_swap(args)
     if args.workload == "llama3_8b_gqa_fp8":

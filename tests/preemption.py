@@ -179,10 +179,14 @@ class Event:
 
 
 class PreemptingScheduler:
-    def __init__(self, cfg: TraceConfig, num_blocks: int, mode: str, alloc):
+    """``watermark`` blocks are kept free at admission (new requests wait
+    rather than take the last blocks the running ones will grow into)."""
+
+    def __init__(self, cfg: TraceConfig, num_blocks: int, mode: str, alloc, watermark: int = 0):
         assert mode in ("swap", "recompute")
         self.cfg, self.mode, self.alloc = cfg, mode, alloc
         self.num_blocks = num_blocks
+        self.watermark = watermark
         self.g = generator(cfg.seed, 0)
         self.waiting: deque = deque()
         self.swapped: deque = deque()
@@ -225,7 +229,8 @@ class PreemptingScheduler:
             r.state = "running"
             self.running.append(r)
         while (self.waiting and not self.swapped and len(self.running) < cfg.max_running
-               and self.alloc.num_free() >= -(-min(cfg.chunk, self.waiting[0].prefill_to) // B)):
+               and self.alloc.num_free() - self.watermark
+               >= -(-min(cfg.chunk, self.waiting[0].prefill_to) // B)):
             r = self.waiting.popleft()
             r.sid = self.alloc.create()
             r.state = "running"
@@ -274,9 +279,10 @@ def small_trace_config(iterations=60) -> TraceConfig:
                        block_size=16, seed=0x281 + 50)
 
 
-def run_schedule(cfg, num_blocks, mode, alloc_factory):
+def run_schedule(cfg, num_blocks, mode, alloc_factory, watermark=0):
     """All events of the trace for one allocator."""
-    sched = PreemptingScheduler(cfg, num_blocks, mode, alloc_factory(num_blocks, cfg.block_size))
+    sched = PreemptingScheduler(cfg, num_blocks, mode, alloc_factory(num_blocks, cfg.block_size),
+                                watermark)
     return [sched.step(it) for it in range(cfg.iterations)], sched
 
 
