@@ -42,34 +42,37 @@ namespace pkv {
 namespace {
 
 constexpr int kRows = 128;       // (query, head) rows per Q tile = TMEM lanes
-constexpr int kQTiles = 2;       // Q tiles per CTA, sharing every K/V tile
 constexpr int kKeys = 64;        // keys per KV tile
-constexpr int kThreadsP = 576;   // producer warp, MMA warp, eight softmax warps per Q tile
-constexpr uint32_t kQHalf = kQTiles * kRows * 128;  // one 64-column half of both Q tiles
-constexpr uint32_t kKVHalf = kKeys * 128;           // one 64-column half of a K or V tile
+constexpr uint32_t kKVHalf = kKeys * 128;  // one 64-column half of a K or V tile
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows past 2^8
 constexpr int kWin = 256;            // block-table entries held in shared memory
 
-template <int D, int NS>
+// NQ Q tiles per CTA share every K/V tile: two (one CTA per SM, all 512 TMEM
+// columns) halve the K/V traffic per row; one (two CTAs per SM) lets a CTA's
+// start and end overlap the other's work, which pays for short chunks.
+template <int D, int NS, int NQ>
 struct PCfg {
+  static constexpr int kThreads = 64 + 256 * NQ;  // producer, MMA, eight softmax warps per tile
+  static constexpr uint32_t kQHalf = NQ * kRows * 128;  // one 64-column half of the Q tiles
   static constexpr int kHalves = D / 64;
   static constexpr uint32_t kStage = kHalves * kKVHalf;
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kK = kQ + kHalves * kQHalf;
   static constexpr uint32_t kV = kK + NS * kStage;
   static constexpr uint32_t kBytes = kV + NS * kStage;
-  // + alignment slack; more than half of an SM's shared memory, so that one
-  // CTA (which takes all 512 TMEM columns) runs per SM and allocation never waits
-  static constexpr uint32_t kSmem = kBytes + 1024 > 116u * 1024 ? kBytes + 1024 : 116u * 1024;
+  // + alignment slack; padded so that at most 2 / NQ CTAs share an SM: their
+  // TMEM allocations (256 NQ columns each) always fit and never wait
+  static constexpr uint32_t kMinSmem = NQ == 2 ? 116u * 1024 : 80u * 1024;
+  static constexpr uint32_t kSmem = kBytes + 1024 > kMinSmem ? kBytes + 1024 : kMinSmem;
   // barriers: Q; K full/empty and V full/empty per stage; per Q tile and
   // buffer: S full, P full, PV done, row maxima exchanged; per Q tile: row
   // sums exchanged; final
   static constexpr int kBarQ = 0, kBarKF = 1, kBarKE = 1 + NS, kBarVF = 1 + 2 * NS,
-                       kBarVE = 1 + 3 * NS, kBarSF = 1 + 4 * NS, kBarPF = 5 + 4 * NS,
-                       kBarPV = 9 + 4 * NS, kBarX = 13 + 4 * NS, kBarL = 17 + 4 * NS,
-                       kBarFin = 19 + 4 * NS, kNumBars = 20 + 4 * NS;
+                       kBarVE = 1 + 3 * NS, kBarSF = 1 + 4 * NS, kBarPF = kBarSF + 2 * NQ,
+                       kBarPV = kBarPF + 2 * NQ, kBarX = kBarPV + 2 * NQ, kBarL = kBarX + 2 * NQ,
+                       kBarFin = kBarL + NQ, kNumBars = kBarFin + 1;
   // TMEM per Q tile t at column 256 t: S buffers 0..63 and 64..127, O 128..128+D
-  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmemCols = 256 * NQ;
 };
 
 struct PrefillArgs {
@@ -181,12 +184,13 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
-template <int D, int G, int NS>
-__global__ void __launch_bounds__(kThreadsP, 1)
+template <int D, int G, int NS, int NQ>
+__global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                          const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
-  using C = PCfg<D, NS>;
+  using C = PCfg<D, NS, NQ>;
+  constexpr int kQHalf = C::kQHalf;
   constexpr int QT = kRows / G;  // queries per Q tile
   constexpr uint32_t kIdescS = umma_idesc_bf16(128, kKeys, false);
   constexpr uint32_t kIdescO = umma_idesc_bf16(128, D, true);
@@ -198,8 +202,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   __shared__ int32_t s_pages[kWin];  // window of this sequence's block table
   // row maxima of the two key halves, per Q tile and score buffer; the two
   // halves' row sums at the end
-  __shared__ float s_xmax[kQTiles][2][2][kRows];
-  __shared__ float s_lsum[kQTiles][2][kRows];
+  __shared__ float s_xmax[NQ][2][2][kRows];
+  __shared__ float s_lsum[NQ][2][kRows];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // heaviest tiles (the chunk's last queries see the most keys) start first
@@ -207,7 +211,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   const int c0 = __ldg(a.cu_q_lens + s);
   const int c = __ldg(a.cu_q_lens + s + 1) - c0;
   const int L = __ldg(a.context_lens + s);
-  const int q0 = qt * kQTiles * QT;
+  const int q0 = qt * NQ * QT;
   if (q0 >= c) return;
   if (L < c || L > a.max_context_len) {
     if (tid == 0) record_status(a.status, PKV_EDEVICE, L, kKernelPrefill);
@@ -215,8 +219,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   }
   // Q tile t holds queries q0 + t QT .. + QT - 1 of the chunk; its rows see
   // keys below kv_end_t, i.e. nkt_t key tiles (0 when it has no query)
-  static_assert(kQTiles == 2, "two Q tiles per CTA");
-  const int qn1 = max(0, min(QT, c - (q0 + QT)));
+  const int qn1 = NQ == 2 ? max(0, min(QT, c - (q0 + QT))) : 0;
   const int kv_end0 = L - c + q0 + min(QT, c - q0);
   const int kv_end = qn1 > 0 ? L - c + q0 + QT + qn1 : kv_end0;
   const int nkt0 = (kv_end0 + kKeys - 1) / kKeys;
@@ -243,13 +246,13 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       mbar_init(bar(C::kBarVF + i), 1);
       mbar_init(bar(C::kBarVE + i), 1);
     }
-    for (int i = 0; i < 2 * kQTiles; ++i) {
+    for (int i = 0; i < 2 * NQ; ++i) {
       mbar_init(bar(C::kBarSF + i), 1);
       mbar_init(bar(C::kBarPF + i), 256);
       mbar_init(bar(C::kBarPV + i), 1);
       mbar_init(bar(C::kBarX + i), 256);
     }
-    for (int i = 0; i < kQTiles; ++i) mbar_init(bar(C::kBarL + i), 256);
+    for (int i = 0; i < NQ; ++i) mbar_init(bar(C::kBarL + i), 256);
     mbar_init(bar(C::kBarFin), 1);
     s_abort = 0;
     fence_barrier_init();
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         if (elect_one()) {
           const uint64_t dks = dk + ((st * C::kStage) >> 4);
 #pragma unroll
-          for (int t = 0; t < kQTiles; ++t) {
+          for (int t = 0; t < NQ; ++t) {
             if (j >= nkt_t(t)) continue;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -385,7 +388,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         }
         __syncwarp();
 #pragma unroll
-        for (int t = 0; t < kQTiles; ++t) {
+        for (int t = 0; t < NQ; ++t) {
           if (i >= nkt_t(t)) continue;
           ok = wait_warp(C::kBarPF + 2 * t + b, (i >> 1) & 1, 5);
           if (!ok) break;
@@ -569,21 +572,21 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   }
 }
 
-template <int D, int G>
+template <int D, int G, int NQ>
 int launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    const PrefillArgs& a, int max_q_len, cudaStream_t stream) {
-  constexpr int NS = 3;
-  using C = PCfg<D, NS>;
+  constexpr int NS = NQ == 2 ? 3 : 2;
+  using C = PCfg<D, NS, NQ>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, []() {
-    attr_err = cudaFuncSetAttribute(paged_prefill_kernel<D, G, NS>,
+    attr_err = cudaFuncSetAttribute(paged_prefill_kernel<D, G, NS, NQ>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "prefill kernel attributes");
-  constexpr int QC = kQTiles * kRows / G;  // queries per CTA
+  constexpr int QC = NQ * kRows / G;  // queries per CTA
   dim3 grid((unsigned)((max_q_len + QC - 1) / QC), (unsigned)a.Hkv, (unsigned)a.S);
-  paged_prefill_kernel<D, G, NS><<<grid, kThreadsP, C::kSmem, stream>>>(tq, tk, tv, a);
+  paged_prefill_kernel<D, G, NS, NQ><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, a);
   return check_launch("prefill");
 }
 
@@ -634,12 +637,18 @@ extern "C" int pkv_paged_attention_prefill(void* out, const void* q, const int32
               "prefill: bf16 arrays must be 16-byte aligned");
   const DeviceInfo* dev = nullptr;
   if (int rc = current_device_info(&dev)) return rc;
+  // Two Q tiles per CTA halve the key/value reads per query row, which pays
+  // when chunks are short next to the contexts they attend (chunks after a
+  // long cached prefix); otherwise one tile per CTA and two CTAs per SM, whose
+  // starts and ends overlap, are faster (measured on GB300).
+  const int64_t mean_chunk = ((int64_t)total_q + S - 1) / S;
+  const int NQ = (max_q_len * G > kRows && max_context_len >= 4 * mean_chunk) ? 2 : 1;
 
   CUtensorMap tq, tk, tv;
   {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)total_q};
     const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)Hq * D * 2};
-    const uint32_t box[3] = {64, (uint32_t)G, (uint32_t)(kQTiles * kRows / G)};
+    const uint32_t box[3] = {64, (uint32_t)G, (uint32_t)(NQ * kRows / G)};
     if (int rc = encode_tile_map_3d(&tq, q, dims, strides, box)) return rc;
   }
   const uint64_t rows = (uint64_t)num_blocks * Hkv * block_size;
@@ -668,8 +677,10 @@ extern "C" int pkv_paged_attention_prefill(void* out, const void* q, const int32
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc = PKV_OK;
-#define PKV_PREFILL_CASE(DD, GG) \
-  if (D == DD && G == GG) rc = launch_prefill<DD, GG>(tq, tk, tv, a, max_q_len, st);
+#define PKV_PREFILL_CASE(DD, GG)                                                   \
+  if (D == DD && G == GG)                                                          \
+    rc = NQ == 2 ? launch_prefill<DD, GG, 2>(tq, tk, tv, a, max_q_len, st)         \
+                 : launch_prefill<DD, GG, 1>(tq, tk, tv, a, max_q_len, st);
   PKV_PREFILL_CASE(64, 1)
   PKV_PREFILL_CASE(64, 2)
   PKV_PREFILL_CASE(64, 4)
