@@ -282,8 +282,6 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
     const int B = a.block_size, ppt = kKeys / B;  // pages per tile
     const int npages = (kv_end + B - 1) / B;
     int win0 = 0;
-    for (int i = lane; i < kWin && i < npages; i += 32) s_pages[i] = __ldg(bt + i);
-    __syncwarp();
     // Loads key or value tile t: lane k issues box k (page k / halves, column
     // half k % halves), so the boxes of a tile leave the warp together.
     auto issue = [&](const CUtensorMap* map, int t, uint32_t dst, uint32_t fbar) {
@@ -307,6 +305,9 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
         tma_load_3d(base + C::kQ + h * kQHalf, &tmap_q, h * 64, kvh * G, c0 + q0, bar(C::kBarQ));
       armed_q = 1;
     }
+    // the block-table window loads while Q is in flight
+    for (int i = lane; i < kWin && i < npages; i += 32) s_pages[i] = __ldg(bt + i);
+    __syncwarp();
     bool ok = true;
     for (int j = 0; ok && j <= nkt; ++j) {
       if (j < nkt) {
