@@ -180,3 +180,11 @@ def test_fp8_close_to_bf16_decode():
     d = setup_decode(w)
     out16 = bf16_to_f64(run_decode(w, d))
     assert np.max(np.abs(out8 - out16)) < 0.05
+
+
+@pytest.mark.parametrize("B", [16, 32])
+def test_maximum_context_length(B):
+    # the longest context the configurations use (8192 tokens), next to tiny ones
+    w = make_decode_workload(f"fp8_max_B{B}", (8192, 1, 4097, 8191), Hq=64, Hkv=8, D=128,
+                             block_size=B, seed=6500 + B)
+    check(w)

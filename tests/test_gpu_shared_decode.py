@@ -122,3 +122,15 @@ def test_bad_group_entry_is_reported_then_recovers():
     out = bf16_to_f64(decode_shared_grouped(w, d))
     pkv.pkv_check_status(d.status)
     assert_close(out, reference(w), "after recovery")
+
+
+def test_long_shared_prefix_many_partitions():
+    # 4 x 2000-token prefixes shared by 6 samples each, tails up to 3000 tokens
+    # (contexts up to 5000): several shared and private partitions per member
+    w = make_shared_prefix_workload("grouped_long", n_prompts=4, n_samples=6, prefix=2000,
+                                    tail_max=3000, Hq=32, Hkv=8, D=128, block_size=16,
+                                    seed=7500)
+    d = setup_shared_prefix(w)
+    out = bf16_to_f64(decode_shared_grouped(w, d, partition_size=512))
+    pkv.pkv_check_status(d.status)
+    assert_close(out, reference(w), "long shared prefixes")
