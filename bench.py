@@ -446,7 +446,9 @@ def run_trace_preempt(args):
     scale = 1.0 / math.sqrt(cfg.D)
     ws = torch.empty(pkv.pkv_decode_workspace_bytes(cfg.max_running, cfg.Hq, cfg.D, max_ctx),
                      dtype=torch.uint8, device=dev)
-    pws = torch.empty(256, dtype=torch.uint8, device=dev)
+    pws = torch.empty(max(pkv.pkv_prefill_workspace_bytes(len(u["pre"][1]), u["pre"][5], cfg.Hq,
+                                                          cfg.D) for u in ups if "pre" in u),
+                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def one_pass(timed):
@@ -699,7 +701,8 @@ def run_prefix_cache(args):
         pre = sum(b.elapsed_time(c) for _, b, c in evs) / steps
         return app, pre
 
-    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(pkv.pkv_prefill_workspace_bytes(S, S * (P + 256), Hq, D), dtype=torch.uint8,
+                     device="cuda")
     steps = max(5, min(args.steps, 50))
     results = {}
     with ClockSampler(local) as clocks:

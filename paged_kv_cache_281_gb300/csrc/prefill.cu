@@ -46,6 +46,7 @@ constexpr int kKeys = 64;        // keys per KV tile
 constexpr uint32_t kKVHalf = kKeys * 128;  // one 64-column half of a K or V tile
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows past 2^8
 constexpr int kWin = 256;            // block-table entries held in shared memory
+constexpr int kItemRing = 4;         // work-item indices handed from the producer to the others
 
 // NQ Q tiles per CTA share every K/V tile: two (one CTA per SM, all 512 TMEM
 // columns) halve the K/V traffic per row; one (two CTAs per SM) lets a CTA's
@@ -66,11 +67,14 @@ struct PCfg {
   static constexpr uint32_t kSmem = kBytes + 1024 > kMinSmem ? kBytes + 1024 : kMinSmem;
   // barriers: Q; K full/empty and V full/empty per stage; per Q tile and
   // buffer: S full, P full, PV done, row maxima exchanged; per Q tile: row
-  // sums exchanged; final
+  // sums exchanged, output read out (O free); Q free; work item posted /
+  // taken per item-ring slot; final
   static constexpr int kBarQ = 0, kBarKF = 1, kBarKE = 1 + NS, kBarVF = 1 + 2 * NS,
                        kBarVE = 1 + 3 * NS, kBarSF = 1 + 4 * NS, kBarPF = kBarSF + 2 * NQ,
                        kBarPV = kBarPF + 2 * NQ, kBarX = kBarPV + 2 * NQ, kBarL = kBarX + 2 * NQ,
-                       kBarFin = kBarL + NQ, kNumBars = kBarFin + 1;
+                       kBarOE = kBarL + NQ, kBarQE = kBarOE + NQ, kBarIF = kBarQE + 1,
+                       kBarIE = kBarIF + kItemRing, kBarFin = kBarIE + kItemRing,
+                       kNumBars = kBarFin + 1;
   // TMEM per Q tile t at column 256 t: S buffers 0..63 and 64..127, O 128..128+D
   static constexpr uint32_t kTmemCols = 256 * NQ;
 };
@@ -86,7 +90,70 @@ struct PrefillArgs {
   int32_t* status;
   uint64_t timeout_ns;
   int32_t force_timeout;
+  int32_t qc;         // queries per work item (NQ tiles of 128 / G)
+  int32_t item_cap;
+  int4* items;        // (sequence, query group, kv head, -)
+  int32_t* n_items;
+  int32_t* ticket;    // next item to hand out
+  int32_t direct;     // 1: one CTA per (query group, kv head, sequence), no plan
 };
+
+// Lists the work items (sequence, query group, kv head): for each sequence
+// its query groups from the last (which sees the most keys) to the first.
+// One CTA of 1024 threads; sequences with an inconsistent length are
+// recorded and skipped.
+__global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillArgs a) {
+  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t s_base, s_chunk;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  grid_dep_launch();  // the prefill kernel may start its set-up now
+  if (tid == 0) s_base = 0;
+  __syncthreads();
+  for (int c0 = 0; c0 < a.S; c0 += 1024) {
+    const int s = c0 + tid;
+    int ng = 0;
+    if (s < a.S) {
+      const int c = __ldg(a.cu_q_lens + s + 1) - __ldg(a.cu_q_lens + s);
+      const int L = __ldg(a.context_lens + s);
+      if (c < 0 || L < c || L > a.max_context_len) {
+        if (c != 0) record_status(a.status, PKV_EDEVICE, L, kKernelPrefill);
+      } else {
+        ng = (c + a.qc - 1) / a.qc;
+      }
+    }
+    const int cnt = ng * a.Hkv;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int w = warp_tot[lane];
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += v;
+      }
+      warp_tot[lane] = wi - w;
+      if (lane == 31) s_chunk = wi;
+    }
+    __syncthreads();
+    const int excl = s_base + warp_tot[warp] + incl - cnt;
+    for (int i = 0; i < cnt && excl + i < a.item_cap; ++i)
+      a.items[excl + i] = make_int4(s, ng - 1 - i / a.Hkv, i % a.Hkv, 0);
+    __syncthreads();
+    if (tid == 0) s_base += s_chunk;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    *a.n_items = min(s_base, a.item_cap);
+    *a.ticket = 0;
+  }
+}
 
 // Bounded wait that also gives up as soon as another warp of the CTA has
 // given up (`abort` set). The first waiter to run out of time sets `abort`
@@ -184,6 +251,40 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// One work item: queries q0 .. q0 + qc - 1 of sequence s's chunk, kv head kvh.
+struct PItem {
+  int s, kvh, c0, c, L, q0;
+  int kv_end0, kv_end, nkt0, nkt1, nkt;
+};
+
+template <int NQ>
+__device__ __forceinline__ PItem load_item(const PrefillArgs& a, int idx, int QT) {
+  // direct launches: the item is the CTA's own grid position
+  const int4 it = idx < 0 ? make_int4(blockIdx.z, gridDim.x - 1 - blockIdx.x, blockIdx.y, 0)
+                          : a.items[idx];
+  PItem p;
+  p.s = it.x;
+  p.kvh = it.z;
+  p.c0 = __ldg(a.cu_q_lens + p.s);
+  p.c = __ldg(a.cu_q_lens + p.s + 1) - p.c0;
+  p.L = __ldg(a.context_lens + p.s);
+  p.q0 = it.y * NQ * QT;
+  // Q tile t holds queries q0 + t QT .. + QT - 1 of the chunk; its rows see
+  // keys below kv_end_t, i.e. nkt_t key tiles (0 when it has no query)
+  const int qn1 = NQ == 2 ? max(0, min(QT, p.c - (p.q0 + QT))) : 0;
+  p.kv_end0 = p.L - p.c + p.q0 + min(QT, p.c - p.q0);
+  p.kv_end = qn1 > 0 ? p.L - p.c + p.q0 + QT + qn1 : p.kv_end0;
+  p.nkt0 = (p.kv_end0 + kKeys - 1) / kKeys;
+  p.nkt1 = qn1 > 0 ? (p.kv_end + kKeys - 1) / kKeys : 0;
+  p.nkt = (p.kv_end + kKeys - 1) / kKeys;
+  return p;
+}
+
+// Persistent: the producer warp takes the next work item from a global
+// ticket and posts its index in a small shared ring that the MMA and softmax
+// warps read in the same order; every barrier's phase follows a running
+// count, so the next item's Q and first K/V tiles load while this item
+// finishes and its scores are computed while this item's output is written.
 template <int D, int G, int NS, int NQ>
 __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -199,34 +300,25 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
   __shared__ __align__(8) uint64_t bars[C::kNumBars];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int32_t s_pages[kWin];  // window of this sequence's block table
+  __shared__ int32_t s_pages[kWin];  // window of the current sequence's block table
   // row maxima of the two key halves, per Q tile and score buffer; the two
   // halves' row sums at the end
   __shared__ float s_xmax[NQ][2][2][kRows];
   __shared__ float s_lsum[NQ][2][kRows];
+  __shared__ int32_t s_item[kItemRing];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // heaviest tiles (the chunk's last queries see the most keys) start first
-  const int qt = gridDim.x - 1 - blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
-  const int c0 = __ldg(a.cu_q_lens + s);
-  const int c = __ldg(a.cu_q_lens + s + 1) - c0;
-  const int L = __ldg(a.context_lens + s);
-  const int q0 = qt * NQ * QT;
-  if (q0 >= c) return;
-  if (L < c || L > a.max_context_len) {
-    if (tid == 0) record_status(a.status, PKV_EDEVICE, L, kKernelPrefill);
-    return;
+  if (a.direct) {
+    // one item per CTA: leave at once when its query group is empty
+    const int s = blockIdx.z;
+    const int c = __ldg(a.cu_q_lens + s + 1) - __ldg(a.cu_q_lens + s);
+    const int L = __ldg(a.context_lens + s);
+    if ((int)(gridDim.x - 1 - blockIdx.x) * NQ * QT >= c) return;
+    if (L < c || L > a.max_context_len) {
+      if (tid == 0) record_status(a.status, PKV_EDEVICE, L, kKernelPrefill);
+      return;
+    }
   }
-  // Q tile t holds queries q0 + t QT .. + QT - 1 of the chunk; its rows see
-  // keys below kv_end_t, i.e. nkt_t key tiles (0 when it has no query)
-  const int qn1 = NQ == 2 ? max(0, min(QT, c - (q0 + QT))) : 0;
-  const int kv_end0 = L - c + q0 + min(QT, c - q0);
-  const int kv_end = qn1 > 0 ? L - c + q0 + QT + qn1 : kv_end0;
-  const int nkt0 = (kv_end0 + kKeys - 1) / kKeys;
-  const int nkt1 = qn1 > 0 ? (kv_end + kKeys - 1) / kKeys : 0;
-  const int nkt = (kv_end + kKeys - 1) / kKeys;
-  auto nkt_t = [&](int t) { return t == 0 ? nkt0 : nkt1; };
-  const int32_t* bt = a.block_tables + (int64_t)s * a.max_blocks_per_seq;
 
   const uint32_t raw = smem_u32(dsm);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -240,6 +332,7 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
 
   if (tid == 0) {
     mbar_init(bar(C::kBarQ), 1);
+    mbar_init(bar(C::kBarQE), 1);
     for (int i = 0; i < NS; ++i) {
       mbar_init(bar(C::kBarKF + i), 1);
       mbar_init(bar(C::kBarKE + i), 1);
@@ -252,7 +345,14 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
       mbar_init(bar(C::kBarPV + i), 1);
       mbar_init(bar(C::kBarX + i), 256);
     }
-    for (int i = 0; i < NQ; ++i) mbar_init(bar(C::kBarL + i), 256);
+    for (int i = 0; i < NQ; ++i) {
+      mbar_init(bar(C::kBarL + i), 256);
+      mbar_init(bar(C::kBarOE + i), 256);
+    }
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(bar(C::kBarIF + i), 1);
+      mbar_init(bar(C::kBarIE + i), 1 + 8 * NQ);  // the MMA warp and each softmax warp
+    }
     mbar_init(bar(C::kBarFin), 1);
     s_abort = 0;
     fence_barrier_init();
@@ -268,10 +368,25 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
   __syncthreads();
   tcgen05_after_sync();
   const uint32_t tmem = s_tmem;
+  grid_dep_wait();  // the plan (and everything before it) is complete
+  const int n_items = a.direct ? 1 : *reinterpret_cast<volatile int32_t*>(a.n_items);
+
+  // The n-th item of this CTA (-1: no more; -2: the CTA's own grid position),
+  // as posted by the producer; every
+  // consuming warp calls it once per n, in order.
+  auto take_item = [&](int n, bool& ok) -> int {
+    const int slot = n % kItemRing;
+    ok = wait_warp(C::kBarIF + slot, (n / kItemRing) & 1, 14);
+    if (!ok) return -1;
+    const int idx = *reinterpret_cast<volatile int32_t*>(&s_item[slot]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(C::kBarIE + slot));
+    return idx;
+  };
 
   // loads this CTA issued (Q, and K and V tiles, counted by the producer):
   // what a CTA that gives up waits for before its shared memory goes
-  int armed_q = 0, issued_k = 0, issued_v = 0;
+  int issued_q = 0, issued_k = 0, issued_v = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -280,137 +395,184 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
     // global read; K runs one tile ahead of V, the order in which the tensor
     // core needs them.
     const int B = a.block_size, ppt = kKeys / B;  // pages per tile
-    const int npages = (kv_end + B - 1) / B;
-    int win0 = 0;
-    // Loads key or value tile t: lane k issues box k (page k / halves, column
-    // half k % halves), so the boxes of a tile leave the warp together.
-    auto issue = [&](const CUtensorMap* map, int t, uint32_t dst, uint32_t fbar) {
-      const int p0 = t * ppt, np = min(ppt, npages - p0);
-      const bool mine = lane < np * C::kHalves;
-      const int pg = lane / C::kHalves, hh = lane % C::kHalves;
-      const int32_t blk = mine ? s_pages[p0 + pg - win0] : -1;
-      const bool valid = mine && blk >= 0 && blk < a.num_blocks;
-      const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
-      if (lane == 0) mbar_arrive_expect_tx(fbar, nvalid * B * 128u);
-      __syncwarp();
-      if (mine && !valid) record_status(a.status, PKV_EDEVICE, blk, kKernelPrefill);
-      if (valid)
-        tma_load_2d(dst + hh * kKVHalf + pg * B * 128, map, hh * 64, (blk * a.Hkv + kvh) * B,
-                    fbar);
-    };
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(C::kBarQ), C::kHalves * kQHalf);
-#pragma unroll
-      for (int h = 0; h < C::kHalves; ++h)
-        tma_load_3d(base + C::kQ + h * kQHalf, &tmap_q, h * 64, kvh * G, c0 + q0, bar(C::kBarQ));
-      armed_q = 1;
-    }
-    // the block-table window loads while Q is in flight
-    for (int i = lane; i < kWin && i < npages; i += 32) s_pages[i] = __ldg(bt + i);
-    __syncwarp();
     bool ok = true;
-    for (int j = 0; ok && j <= nkt; ++j) {
-      if (j < nkt) {
-        if (min((j + 1) * ppt, npages) > win0 + kWin) {
-          // slide the window: tile j-1 (whose values are still to load) and on
-          win0 = (j - 1) * ppt;
-          __syncwarp();
-          for (int i = lane; i < kWin && win0 + i < npages; i += 32)
-            s_pages[i] = __ldg(bt + win0 + i);
-          __syncwarp();
+    int jg = 0;  // K/V tiles issued so far (ring position)
+    for (int n = 0; ok; ++n) {
+      // post the next item (or the end) in the ring
+      const int slot = n % kItemRing;
+      if (n >= kItemRing) ok = wait_warp(C::kBarIE + slot, (n / kItemRing - 1) & 1, 15);
+      if (!ok) break;
+      // direct launches post their own item (index -2) once, then the end
+      int idx = 0;
+      if (lane == 0) {
+        idx = a.direct ? (n == 0 ? -2 : n_items) : atomicAdd(a.ticket, 1);
+        s_item[slot] = idx < n_items ? idx : -1;
+        mbar_arrive(bar(C::kBarIF + slot));  // release: the index is visible to the waiters
+      }
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      if (idx >= n_items) break;
+      const PItem it = load_item<NQ>(a, idx, QT);
+      const int32_t* bt = a.block_tables + (int64_t)it.s * a.max_blocks_per_seq;
+      const int npages = (it.kv_end + B - 1) / B;
+      int win0 = 0;
+      // Loads key or value tile t of this item into ring slot g: lane k issues
+      // box k (page k / halves, column half k % halves).
+      auto issue = [&](const CUtensorMap* map, int t, uint32_t dst, uint32_t fbar) {
+        const int p0 = t * ppt, np = min(ppt, npages - p0);
+        const bool mine = lane < np * C::kHalves;
+        const int pg = lane / C::kHalves, hh = lane % C::kHalves;
+        const int32_t blk = mine ? s_pages[p0 + pg - win0] : -1;
+        const bool valid = mine && blk >= 0 && blk < a.num_blocks;
+        const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+        if (lane == 0) mbar_arrive_expect_tx(fbar, nvalid * B * 128u);
+        __syncwarp();
+        if (mine && !valid) record_status(a.status, PKV_EDEVICE, blk, kKernelPrefill);
+        if (valid)
+          tma_load_2d(dst + hh * kKVHalf + pg * B * 128, map, hh * 64,
+                      (blk * a.Hkv + it.kvh) * B, fbar);
+      };
+      // Q of this item once the previous item's score MMAs have read theirs
+      if (n > 0) ok = wait_warp(C::kBarQE, (n - 1) & 1, 12);
+      if (!ok) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(C::kBarQ), C::kHalves * kQHalf);
+#pragma unroll
+        for (int h = 0; h < C::kHalves; ++h)
+          tma_load_3d(base + C::kQ + h * kQHalf, &tmap_q, h * 64, it.kvh * G, it.c0 + it.q0,
+                      bar(C::kBarQ));
+      }
+      ++issued_q;
+      // the block-table window loads while Q is in flight
+      __syncwarp();
+      for (int i = lane; i < kWin && i < npages; i += 32) s_pages[i] = __ldg(bt + i);
+      __syncwarp();
+      for (int j = 0; ok && j <= it.nkt; ++j) {
+        if (j < it.nkt) {
+          if (min((j + 1) * ppt, npages) > win0 + kWin) {
+            // slide the window: tile j-1 (whose values are still to load) and on
+            win0 = (j - 1) * ppt;
+            __syncwarp();
+            for (int i = lane; i < kWin && win0 + i < npages; i += 32)
+              s_pages[i] = __ldg(bt + win0 + i);
+            __syncwarp();
+          }
+          const int g = jg + j, st = g % NS, u = g / NS;
+          if (g >= NS) ok = wait_warp(C::kBarKE + st, (u - 1) & 1, 1);
+          if (!ok) break;
+          issue(&tmap_k, j, base + C::kK + st * C::kStage, bar(C::kBarKF + st));
+          ++issued_k;
         }
-        const int st = j % NS, u = j / NS;
-        if (j >= NS) ok = wait_warp(C::kBarKE + st, (u - 1) & 1, 1);
-        if (!ok) break;
-        issue(&tmap_k, j, base + C::kK + st * C::kStage, bar(C::kBarKF + st));
-        ++issued_k;
+        if (j >= 1) {
+          const int g = jg + j - 1, st = g % NS, u = g / NS;
+          if (g >= NS) ok = wait_warp(C::kBarVE + st, (u - 1) & 1, 2);
+          if (!ok) break;
+          issue(&tmap_v, j - 1, base + C::kV + st * C::kStage, bar(C::kBarVF + st));
+          ++issued_v;
+        }
+        __syncwarp();
       }
-      if (j >= 1) {
-        const int i = j - 1, st = i % NS, u = i / NS;
-        if (i >= NS) ok = wait_warp(C::kBarVE + st, (u - 1) & 1, 2);
-        if (!ok) break;
-        issue(&tmap_v, i, base + C::kV + st * C::kStage, bar(C::kBarVF + st));
-        ++issued_v;
-      }
+      jg += it.nkt;
       __syncwarp();
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ tensor core
-    // Order: S_0(j), S_1(j), then P_0(j-1) V, P_1(j-1) V; the scores of both Q
-    // tiles for the next key tile are computed while their softmax runs.
+    // Order within an item: S_t(j) for each Q tile, then P_t(j-1) V; the
+    // scores of the next key tile are computed while their softmax runs.
     // shared-memory descriptors of the first Q, K and V tiles; the others
     // differ only in the start address field (bytes / 16)
     const uint64_t dq = umma_desc_sw128(base + C::kQ, 16, 1024);
     const uint64_t dk = umma_desc_sw128(base + C::kK, 16, 1024);
     const uint64_t dv = umma_desc_sw128(base + C::kV, kKVHalf, 1024);
-    bool ok = wait_warp(C::kBarQ, 0, 3);
-    for (int j = 0; ok && j <= nkt; ++j) {
-      if (j < nkt) {
-        const int st = j % NS, u = j / NS, b = j & 1;
-        ok = wait_warp(C::kBarKF + st, u & 1, 4);
-        if (!ok) break;
-        tcgen05_after_sync();
-        if (elect_one()) {
-          const uint64_t dks = dk + ((st * C::kStage) >> 4);
+    bool ok = true;
+    int jg = 0;                   // K/V ring position
+    int sg[NQ], oe[NQ];           // score-buffer uses and finished outputs per Q tile
 #pragma unroll
-          for (int t = 0; t < NQ; ++t) {
-            if (j >= nkt_t(t)) continue;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t koff = (kk >> 2) * kKVHalf + (kk & 3) * 32;
-              const uint32_t qoff = t * kRows * 128 + (kk >> 2) * kQHalf + (kk & 3) * 32;
-              umma_bf16(tmem + t * 256 + b * kKeys, dq + (qoff >> 4), dks + (koff >> 4), kIdescS,
-                        kk > 0 ? 1u : 0u);
-            }
-            umma_commit(bar(C::kBarSF + 2 * t + b));
-          }
-          umma_commit(bar(C::kBarKE + st));
-        }
-        __syncwarp();
-      }
-      if (j >= 1) {
-        const int i = j - 1, st = i % NS, u = i / NS, b = i & 1;
-        ok = wait_warp(C::kBarVF + st, u & 1, 6);
-        if (!ok) break;
-        const int key0 = i * kKeys;
-        if (key0 + kKeys > kv_end) {
-          // value rows past the last visible key: stale or poisoned bytes that
-          // must not reach O, not even as NaN * 0
-          uint8_t* vp = base_ptr + C::kV + st * C::kStage;
-          for (int r = kv_end - key0 + lane; r < kKeys; r += 32)
-#pragma unroll
-            for (int h = 0; h < C::kHalves; ++h)
-#pragma unroll
-              for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4*>(vp + h * kKVHalf + r * 128 + ch * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-#pragma unroll
-        for (int t = 0; t < NQ; ++t) {
-          if (i >= nkt_t(t)) continue;
-          ok = wait_warp(C::kBarPF + 2 * t + b, (i >> 1) & 1, 5);
+    for (int t = 0; t < NQ; ++t) sg[t] = oe[t] = 0;
+    for (int n = 0; ok; ++n) {
+      const int idx = take_item(n, ok);
+      if (!ok || idx == -1) break;
+      const PItem it = load_item<NQ>(a, idx, QT);
+      auto nkt_t = [&](int t) { return t == 0 ? it.nkt0 : it.nkt1; };
+      ok = wait_warp(C::kBarQ, n & 1, 3);
+      for (int j = 0; ok && j <= it.nkt; ++j) {
+        if (j < it.nkt) {
+          const int g = jg + j, st = g % NS, u = g / NS;
+          ok = wait_warp(C::kBarKF + st, u & 1, 4);
           if (!ok) break;
           tcgen05_after_sync();
           if (elect_one()) {
-            const uint32_t p = tmem + t * 256 + b * kKeys;
-            const uint32_t o = tmem + t * 256 + 128;
-            const uint64_t dvs = dv + ((st * C::kStage) >> 4);
+            const uint64_t dks = dk + ((st * C::kStage) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kKeys / 16; ++kk) {
-              const uint64_t vdesc = dvs + ((kk * 16 * 128) >> 4);
-              umma_bf16_ts(o, p + kk * 8, vdesc, kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
-              umma_bf16_ts(o, p + 32 + kk * 8, vdesc, kIdescO, 1u);
+            for (int t = 0; t < NQ; ++t) {
+              if (j >= nkt_t(t)) continue;
+              const int b = (sg[t] + j) & 1;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t koff = (kk >> 2) * kKVHalf + (kk & 3) * 32;
+                const uint32_t qoff = t * kRows * 128 + (kk >> 2) * kQHalf + (kk & 3) * 32;
+                umma_bf16(tmem + t * 256 + b * kKeys, dq + (qoff >> 4), dks + (koff >> 4),
+                          kIdescS, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(bar(C::kBarSF + 2 * t + b));
             }
-            umma_commit(bar(C::kBarPV + 2 * t + b));
+            umma_commit(bar(C::kBarKE + st));
+            if (j == it.nkt - 1) umma_commit(bar(C::kBarQE));  // Q may be replaced
           }
           __syncwarp();
         }
-        if (!ok) break;
-        if (elect_one()) umma_commit(bar(C::kBarVE + st));
-        __syncwarp();
+        if (j >= 1) {
+          const int i = j - 1, g = jg + i, st = g % NS, u = g / NS;
+          ok = wait_warp(C::kBarVF + st, u & 1, 6);
+          if (!ok) break;
+          const int key0 = i * kKeys;
+          if (key0 + kKeys > it.kv_end) {
+            // value rows past the last visible key: stale or poisoned bytes that
+            // must not reach O, not even as NaN * 0
+            uint8_t* vp = base_ptr + C::kV + st * C::kStage;
+            for (int r = it.kv_end - key0 + lane; r < kKeys; r += 32)
+#pragma unroll
+              for (int h = 0; h < C::kHalves; ++h)
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                  *reinterpret_cast<uint4*>(vp + h * kKVHalf + r * 128 + ch * 16) =
+                      make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+#pragma unroll
+          for (int t = 0; t < NQ; ++t) {
+            if (i >= nkt_t(t)) continue;
+            const int sgi = sg[t] + i, b = sgi & 1;
+            ok = wait_warp(C::kBarPF + 2 * t + b, (sgi >> 1) & 1, 5);
+            // the previous item's output must have been read out of O
+            if (ok && i == 0 && oe[t] > 0) ok = wait_warp(C::kBarOE + t, (oe[t] - 1) & 1, 13);
+            if (!ok) break;
+            tcgen05_after_sync();
+            if (elect_one()) {
+              const uint32_t p = tmem + t * 256 + b * kKeys;
+              const uint32_t o = tmem + t * 256 + 128;
+              const uint64_t dvs = dv + ((st * C::kStage) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < kKeys / 16; ++kk) {
+                const uint64_t vdesc = dvs + ((kk * 16 * 128) >> 4);
+                umma_bf16_ts(o, p + kk * 8, vdesc, kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
+                umma_bf16_ts(o, p + 32 + kk * 8, vdesc, kIdescO, 1u);
+              }
+              umma_commit(bar(C::kBarPV + 2 * t + b));
+            }
+            __syncwarp();
+          }
+          if (!ok) break;
+          if (elect_one()) umma_commit(bar(C::kBarVE + st));
+          __syncwarp();
+        }
+      }
+      jg += it.nkt;
+#pragma unroll
+      for (int t = 0; t < NQ; ++t) {
+        sg[t] += nkt_t(t);
+        oe[t] += nkt_t(t) > 0 ? 1 : 0;
       }
     }
     // every MMA (and the arrivals it triggers) is done before the CTA leaves
@@ -427,125 +589,142 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
     const int sw = warp - 2;
     const int t = sw >> 3;            // Q tile of this warp
     const int h = (sw >> 2) & 1;      // key half (columns 32h .. 32h+31)
-    const int nk = nkt_t(t);
     const int quarter = warp & 3;     // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t t_o = tmem + t * 256 + 128 + lane_off + h * (D / 2);
-    const int qi = q0 + t * QT + r / G;
-    const bool row_valid = qi < c;
-    const int limit = row_valid ? (L - c + qi + 1) : 1;  // number of visible keys
     const uint64_t scale2 = f32x2_pack(a.scale_log2, a.scale_log2);
-    float m_ref = 0.f;
-    uint64_t l2 = f32x2_pack(0.f, 0.f);  // this thread's share of the row sum, two lanes
     bool ok = true;
-    for (int j = 0; j < nk; ++j) {
-      const int b = j & 1, key0 = j * kKeys + 32 * h;
-      ok = wait_warp(C::kBarSF + 2 * t + b, (j >> 1) & 1, 7);
-      if (!ok) break;
-      tcgen05_after_sync();
-      const uint32_t t_s = tmem + t * 256 + lane_off + b * kKeys;
-      uint32_t x[32];
-      tmem_ld32(t_s + 32 * h, x);
-      tmem_wait_ld();
-      const int vis = min(32, limit - key0);  // visible columns of this half (may be <= 0)
-      const bool full = __all_sync(0xffffffffu, vis >= 32) != 0;
-      if (!full) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i >= vis) x[i] = __float_as_uint(-INFINITY);
-      }
-      float m4[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        m4[e] = fmax3(__uint_as_float(x[8 * e]), __uint_as_float(x[8 * e + 1]),
-                      fmax3(__uint_as_float(x[8 * e + 2]), __uint_as_float(x[8 * e + 3]),
-                            fmax3(__uint_as_float(x[8 * e + 4]), __uint_as_float(x[8 * e + 5]),
-                                  fmax3(__uint_as_float(x[8 * e + 6]),
-                                        __uint_as_float(x[8 * e + 7]), -INFINITY))));
-      const float mine = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
-      s_xmax[t][b][h][r] = mine;
-      mbar_arrive(bar(C::kBarX + 2 * t + b));
-      ok = wait_warp(C::kBarX + 2 * t + b, (j >> 1) & 1, 10);
-      if (!ok) break;
-      const float m_tile = fmaxf(mine, s_xmax[t][b][h ^ 1][r]) * a.scale_log2;  // -inf: none visible
-      if (j == 0) m_ref = m_tile;  // key 0 is visible to every row
-      const bool need = m_tile > m_ref + kRescaleLog2;
-      if (__any_sync(0xffffffffu, need)) {
-        // O must be complete up to tile j-1 before it is rescaled
-        ok = wait_warp(C::kBarPV + 2 * t + ((j - 1) & 1), ((j - 1) >> 1) & 1, 8);
+    int sg = 0, ne = 0;  // score-buffer uses and finished outputs of this Q tile
+    for (int n = 0; ok; ++n) {
+      const int idx = take_item(n, ok);
+      if (!ok || idx == -1) break;
+      const PItem it = load_item<NQ>(a, idx, QT);
+      const int nk = t == 0 ? it.nkt0 : it.nkt1;
+      const int qi = it.q0 + t * QT + r / G;
+      const bool row_valid = qi < it.c;
+      const int limit = row_valid ? (it.L - it.c + qi + 1) : 1;  // number of visible keys
+      float m_ref = 0.f;
+      uint64_t l2 = f32x2_pack(0.f, 0.f);  // this thread's share of the row sum, two lanes
+      for (int j = 0; j < nk; ++j) {
+        const int sj = sg + j, b = sj & 1, key0 = j * kKeys + 32 * h;
+        ok = wait_warp(C::kBarSF + 2 * t + b, (sj >> 1) & 1, 7);
         if (!ok) break;
         tcgen05_after_sync();
-        const float alpha = need ? fast_exp2(m_ref - m_tile) : 1.f;
-        if (need) m_ref = m_tile;
-        l2 = f32x2_mul(l2, f32x2_pack(alpha, alpha));
+        const uint32_t t_s = tmem + t * 256 + lane_off + b * kKeys;
+        uint32_t x[32];
+        tmem_ld32(t_s + 32 * h, x);
+        tmem_wait_ld();
+        const int vis = min(32, limit - key0);  // visible columns of this half (may be <= 0)
+        const bool full = __all_sync(0xffffffffu, vis >= 32) != 0;
+        if (!full) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i >= vis) x[i] = __float_as_uint(-INFINITY);
+        }
+        float m4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          m4[e] = fmax3(__uint_as_float(x[8 * e]), __uint_as_float(x[8 * e + 1]),
+                        fmax3(__uint_as_float(x[8 * e + 2]), __uint_as_float(x[8 * e + 3]),
+                              fmax3(__uint_as_float(x[8 * e + 4]), __uint_as_float(x[8 * e + 5]),
+                                    fmax3(__uint_as_float(x[8 * e + 6]),
+                                          __uint_as_float(x[8 * e + 7]), -INFINITY))));
+        const float mine = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+        s_xmax[t][b][h][r] = mine;
+        mbar_arrive(bar(C::kBarX + 2 * t + b));
+        ok = wait_warp(C::kBarX + 2 * t + b, (sj >> 1) & 1, 10);
+        if (!ok) break;
+        const float m_tile = fmaxf(mine, s_xmax[t][b][h ^ 1][r]) * a.scale_log2;  // -inf: none
+        if (j == 0) m_ref = m_tile;  // key 0 is visible to every row
+        const bool need = m_tile > m_ref + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          // O must be complete up to tile j-1 before it is rescaled
+          ok = wait_warp(C::kBarPV + 2 * t + ((sj - 1) & 1), ((sj - 1) >> 1) & 1, 8);
+          if (!ok) break;
+          tcgen05_after_sync();
+          const float alpha = need ? fast_exp2(m_ref - m_tile) : 1.f;
+          if (need) m_ref = m_tile;
+          l2 = f32x2_mul(l2, f32x2_pack(alpha, alpha));
+#pragma unroll 1
+          for (int c32 = 0; c32 < D / 64; ++c32) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c32 * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(t_o + c32 * 32, o);
+          }
+        }
+        // p = 2^(x scale - m_ref) for two columns at a time, split into bf16
+        // hi + lo parts; masked columns hold -inf and give 0
+        const uint64_t negm = f32x2_pack(-m_ref, -m_ref);
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float y0, y1;
+          f32x2_unpack(
+              f32x2_fma(f32x2_pack(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])),
+                        scale2, negm),
+              y0, y1);
+          const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+          const uint64_t p = f32x2_pack(p0, p1);
+          l2 = f32x2_add(l2, p);
+          hi[e] = pack_bf16x2(p0, p1);
+          float d0, d1;
+          f32x2_unpack(f32x2_sub(p, f32x2_pack(bf16_lo_to_f32(hi[e]), bf16_hi_to_f32(hi[e]))),
+                       d0, d1);
+          lo[e] = pack_bf16x2(d0, d1);
+        }
+        tmem_st16(t_s + 16 * h, hi);
+        tmem_st16(t_s + 32 + 16 * h, lo);
+        tmem_wait_st();
+        tcgen05_before_sync();
+        mbar_arrive(bar(C::kBarPF + 2 * t + b));
+      }
+      if (!ok || nk == 0) {
+        sg += nk;
+        continue;
+      }
+      const int sl = sg + nk - 1;
+      ok = wait_warp(C::kBarPV + 2 * t + (sl & 1), (sl >> 1) & 1, 9);
+      if (ok) {
+        // ---- epilogue: O / l -> bf16, row r -> (query qi, head kvh*G + r%G);
+        // this thread writes its half of the D columns
+        float l0, l1;
+        f32x2_unpack(l2, l0, l1);
+        s_lsum[t][h][r] = l0 + l1;
+        mbar_arrive(bar(C::kBarL + t));
+        ok = wait_warp(C::kBarL + t, ne & 1, 11);
+      }
+      if (ok) {
+        const float inv = 1.f / (s_lsum[t][0][r] + s_lsum[t][1][r]);
+        tcgen05_after_sync();
+        __nv_bfloat16* orow =
+            a.out + ((int64_t)(it.c0 + qi) * a.Hq + it.kvh * G + (r % G)) * D + h * (D / 2);
 #pragma unroll 1
         for (int c32 = 0; c32 < D / 64; ++c32) {
           uint32_t o[32];
           tmem_ld32(t_o + c32 * 32, o);
           tmem_wait_ld();
+          if (row_valid) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(t_o + c32 * 32, o);
-        }
-      }
-      // p = 2^(x scale - m_ref) for two columns at a time, split into bf16
-      // hi + lo parts; masked columns hold -inf and give 0
-      const uint64_t negm = f32x2_pack(-m_ref, -m_ref);
-      uint32_t hi[16], lo[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        float y0, y1;
-        f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])),
-                               scale2, negm), y0, y1);
-        const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
-        const uint64_t p = f32x2_pack(p0, p1);
-        l2 = f32x2_add(l2, p);
-        hi[e] = pack_bf16x2(p0, p1);
-        float d0, d1;
-        f32x2_unpack(f32x2_sub(p, f32x2_pack(bf16_lo_to_f32(hi[e]), bf16_hi_to_f32(hi[e]))), d0,
-                     d1);
-        lo[e] = pack_bf16x2(d0, d1);
-      }
-      tmem_st16(t_s + 16 * h, hi);
-      tmem_st16(t_s + 32 + 16 * h, lo);
-      tmem_wait_st();
-      tcgen05_before_sync();
-      mbar_arrive(bar(C::kBarPF + 2 * t + b));
-    }
-    if (ok && nk > 0)
-      ok = wait_warp(C::kBarPV + 2 * t + ((nk - 1) & 1), ((nk - 1) >> 1) & 1, 9);
-    if (ok && nk > 0) {
-      // ---- epilogue: O / l -> bf16, row r -> (query qi, head kvh*G + r%G);
-      // this thread writes its half of the D columns
-      float l0, l1;
-      f32x2_unpack(l2, l0, l1);
-      s_lsum[t][h][r] = l0 + l1;
-      mbar_arrive(bar(C::kBarL + t));
-      ok = wait_warp(C::kBarL + t, 0, 11);
-    }
-    if (ok && nk > 0) {
-      const float inv = 1.f / (s_lsum[t][0][r] + s_lsum[t][1][r]);
-      tcgen05_after_sync();
-      __nv_bfloat16* orow =
-          a.out + ((int64_t)(c0 + qi) * a.Hq + kvh * G + (r % G)) * D + h * (D / 2);
-#pragma unroll 1
-      for (int c32 = 0; c32 < D / 64; ++c32) {
-        uint32_t o[32];
-        tmem_ld32(t_o + c32 * 32, o);
-        tmem_wait_ld();
-        if (row_valid) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + c32 * 32 + e) = v;
+            for (int e = 0; e < 32; e += 8) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+              *reinterpret_cast<uint4*>(orow + c32 * 32 + e) = v;
+            }
           }
         }
+        // O and this tile's row-sum slots may be reused by the next item
+        tcgen05_before_sync();
+        mbar_arrive(bar(C::kBarOE + t));
       }
+      sg += nk;
+      ++ne;
     }
   }
 
@@ -556,7 +735,7 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
     // Let this CTA's own copies land before its shared memory is released:
     // wait (again with a limit) for the last phase armed on each barrier.
     if (tid == 0) {
-      if (armed_q) mbar_wait_bounded(bar(C::kBarQ), 0, 4 * a.timeout_ns, 0);
+      if (issued_q) mbar_wait_bounded(bar(C::kBarQ), (issued_q - 1) & 1, 4 * a.timeout_ns, 0);
       for (int i = 0; i < NS; ++i) {
         // tiles i, i + NS, ... went to stage i: wait for the last one's phase
         const int nk = issued_k > i ? (issued_k - 1 - i) / NS + 1 : 0;
@@ -575,7 +754,8 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
 
 template <int D, int G, int NQ>
 int launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                   const PrefillArgs& a, int max_q_len, cudaStream_t stream) {
+                   PrefillArgs a, const DeviceInfo& dev, int total_q, int max_q_len,
+                   cudaStream_t stream) {
   constexpr int NS = NQ == 2 ? 3 : 2;
   using C = PCfg<D, NS, NQ>;
   static std::once_flag once;
@@ -585,10 +765,34 @@ int launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "prefill kernel attributes");
-  constexpr int QC = NQ * kRows / G;  // queries per CTA
-  dim3 grid((unsigned)((max_q_len + QC - 1) / QC), (unsigned)a.Hkv, (unsigned)a.S);
-  paged_prefill_kernel<D, G, NS, NQ><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, a);
-  return check_launch("prefill");
+  a.qc = NQ * kRows / G;  // queries per work item
+  const int slots = dev.sm_count * (NQ == 1 ? 2 : 1);
+  // Few items: one CTA each, straight from the grid (no plan launch); many:
+  // a plan and a persistent grid that hands them out.
+  const int64_t items = ((int64_t)total_q / a.qc + a.S) * a.Hkv;
+  if (items < 4 * (int64_t)slots) {
+    a.direct = 1;
+    dim3 grid((unsigned)((max_q_len + a.qc - 1) / a.qc), (unsigned)a.Hkv, (unsigned)a.S);
+    paged_prefill_kernel<D, G, NS, NQ><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, a);
+    return check_launch("prefill");
+  }
+  a.direct = 0;
+  prefill_plan_kernel<<<1, 1024, 0, stream>>>(a);
+  if (int rc = check_launch("prefill plan")) return rc;
+  // persistent: every resident slot; its set-up overlaps the plan
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)slots);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D, G, NS, NQ>, tq, tk, tv, a);
+  if (err != cudaSuccess) return cuda_fail(err, "prefill launch");
+  return PKV_OK;
 }
 
 }  // namespace
@@ -596,12 +800,21 @@ int launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
 
 using namespace pkv;
 
+// Workspace: 256-byte header (item count, ticket), then the work items, at most one
+// per 16 queries plus one per sequence, per kv head (<= Hq).
+static int64_t prefill_item_cap(int64_t S, int64_t total_q, int64_t Hq) {
+  return (total_q / 16 + S + 1) * Hq;
+}
+static size_t prefill_ws_bytes(int64_t S, int64_t total_q, int64_t Hq) {
+  return 256 + (size_t)prefill_item_cap(S, total_q, Hq) * sizeof(int4);
+}
+
 extern "C" int pkv_prefill_workspace_bytes(int32_t S, int32_t total_q, int32_t Hq, int32_t D,
                                            size_t* out) {
   PKV_REQUIRE(out, "pkv_prefill_workspace_bytes: out is NULL");
   PKV_REQUIRE(S >= 0 && total_q >= 0 && Hq > 0 && (D == 64 || D == 128),
               "pkv_prefill_workspace_bytes: bad sizes");
-  *out = 256;  // reserved: the kernel keeps all of its state on chip
+  *out = prefill_ws_bytes(S, total_q, Hq);
   return ok();
 }
 
@@ -633,7 +846,12 @@ extern "C" int pkv_paged_attention_prefill(void* out, const void* q, const int32
   PKV_REQUIRE(out && q && cu_q_lens && context_lens && k_cache && v_cache && block_tables &&
                   workspace,
               "prefill: NULL pointer");
-  PKV_REQUIRE(workspace_bytes >= 256, "prefill: workspace too small");
+  PKV_REQUIRE(workspace_bytes >= prefill_ws_bytes(S, total_q, Hq),
+              "prefill: workspace has %zu bytes, needs %zu", workspace_bytes,
+              prefill_ws_bytes(S, total_q, Hq));
+  PKV_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 15u) == 0,
+              "prefill: workspace must be 16-byte aligned");
+  PKV_REQUIRE(prefill_item_cap(S, total_q, Hq) < (int64_t(1) << 31), "prefill: batch too large");
   PKV_REQUIRE(aligned16(out) && aligned16(q) && aligned16(k_cache) && aligned16(v_cache),
               "prefill: bf16 arrays must be 16-byte aligned");
   const DeviceInfo* dev = nullptr;
@@ -658,7 +876,7 @@ extern "C" int pkv_paged_attention_prefill(void* out, const void* q, const int32
   if (int rc = encode_tile_map_2d(&tv, v_cache, D, rows, (uint64_t)D * 2, 64, block_size))
     return rc;
 
-  PrefillArgs a;
+  PrefillArgs a = {};
   a.out = static_cast<__nv_bfloat16*>(out);
   a.cu_q_lens = cu_q_lens;
   a.context_lens = context_lens;
@@ -675,13 +893,17 @@ extern "C" int pkv_paged_attention_prefill(void* out, const void* q, const int32
   const WaitConfig wc = wait_config();
   a.timeout_ns = wc.timeout_ns;
   a.force_timeout = wc.force_timeout;
+  a.item_cap = (int32_t)prefill_item_cap(S, total_q, Hq);
+  a.n_items = static_cast<int32_t*>(workspace);
+  a.ticket = static_cast<int32_t*>(workspace) + 1;
+  a.items = reinterpret_cast<int4*>(static_cast<uint8_t*>(workspace) + 256);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc = PKV_OK;
 #define PKV_PREFILL_CASE(DD, GG)                                                   \
   if (D == DD && G == GG)                                                          \
-    rc = NQ == 2 ? launch_prefill<DD, GG, 2>(tq, tk, tv, a, max_q_len, st)         \
-                 : launch_prefill<DD, GG, 1>(tq, tk, tv, a, max_q_len, st);
+    rc = NQ == 2 ? launch_prefill<DD, GG, 2>(tq, tk, tv, a, *dev, total_q, max_q_len, st) \
+                 : launch_prefill<DD, GG, 1>(tq, tk, tv, a, *dev, total_q, max_q_len, st);
   PKV_PREFILL_CASE(64, 1)
   PKV_PREFILL_CASE(64, 2)
   PKV_PREFILL_CASE(64, 4)

@@ -246,7 +246,10 @@ class DeviceTrace:
         self.ws = torch.empty(pkv.pkv_decode_workspace_bytes(
             cfg.max_running, cfg.Hq, cfg.D, cfg.prompt_max + cfg.out_cap),
             dtype=torch.uint8, device=device)
-        self.pws = torch.empty(256, dtype=torch.uint8, device=device)
+        # prefill work items: at most every running request's whole chunk
+        self.pws = torch.empty(pkv.pkv_prefill_workspace_bytes(
+            cfg.max_running, cfg.max_running * cfg.chunk, cfg.Hq, cfg.D),
+            dtype=torch.uint8, device=device)
 
     def host_metadata(self, itr):
         """Allocator work and metadata for one iteration (host side)."""

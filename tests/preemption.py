@@ -331,9 +331,7 @@ class GpuRunner:
         self.ws = torch.empty(pkv.pkv_decode_workspace_bytes(
             cfg.max_running, cfg.Hq, cfg.D, cfg.prompt_max + cfg.out_cap + cfg.chunk),
             dtype=torch.uint8, device=device)
-        self.pws = torch.empty(pkv.pkv_prefill_workspace_bytes(cfg.max_running, cfg.max_running
-                                                               * cfg.chunk, cfg.Hq, cfg.D),
-                               dtype=torch.uint8, device=device)
+        self.pws = None  # prefill work items, sized per call
 
     def run(self, ev: Event, values: TokenValues):
         torch, pkv, cfg, dev = self.torch, self.pkv, self.cfg, self.dev
@@ -362,6 +360,9 @@ class GpuRunner:
         n_pre = int(meta["cu"][-1])
         if pre:
             tables, lens = meta["prefill"]
+            need = pkv.pkv_prefill_workspace_bytes(len(pre), n_pre, cfg.Hq, cfg.D)
+            if self.pws is None or self.pws.numel() < need:
+                self.pws = torch.empty(need, dtype=torch.uint8, device=dev)
             pre_out = torch.empty(n_pre, cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
             pkv.pkv_paged_attention_prefill(
                 pre_out, qd[:n_pre], torch.from_numpy(meta["cu"]).to(dev),
