@@ -137,3 +137,57 @@ def test_long_prefix_chunks():
     w = make_decode_workload("prefill_long", (8192, 4096, 2000), Hq=16, Hkv=2, D=128,
                              block_size=16, seed=3200)
     check_prefill(w, [512, 1, 700], seed=11)
+
+
+# Launches with at least four work items per resident CTA run on the
+# persistent grid (plan + ticket); these two cover its one- and two-tile forms.
+def check_prefill_sampled(w, chunks, seqs, seed):
+    d = setup_decode(w)
+    q_bits = normal_bf16((int(sum(chunks)), w.Hq, w.D), 5000 + seed)
+    out, cu = run_prefill(w, d, chunks, q_bits)
+    pkv.pkv_check_status(d.status)
+    st = build_decode_state(w)
+    ref = attention.prefill(q_bits, cu, w.context_lens, st.k_cache, st.v_cache, st.tables,
+                            w.block_size, w.scale, seqs=seqs)
+    got = bf16_to_f64(out)
+    rows = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in seqs]).astype(np.int64)
+    assert_close(got[rows], ref[rows], w.name)
+    return d, q_bits, cu
+
+
+def test_persistent_grid_long_chunks():
+    # 16 fresh 600-token prompts, 32/8 heads: ~2,500 items of one Q tile
+    lens = [600] * 16
+    w = make_decode_workload("prefill_persistent_1", lens, Hq=32, Hkv=8, D=128, block_size=16,
+                             seed=3300)
+    check_prefill_sampled(w, lens, [0, 5, 15], seed=21)
+
+
+def test_persistent_grid_short_chunks_after_long_prefixes():
+    # 64 chunks of 40 tokens after ~2,000 cached tokens, 64/8 heads: two Q tiles
+    lens = [2000 + 7 * i for i in range(64)]
+    w = make_decode_workload("prefill_persistent_2", lens, Hq=64, Hkv=8, D=128, block_size=16,
+                             seed=3301)
+    check_prefill_sampled(w, [40] * 64, [0, 31, 63], seed=22)
+
+
+def test_persistent_grid_timeout_and_bad_entry():
+    lens = [600] * 16
+    w = make_decode_workload("prefill_persistent_err", lens, Hq=32, Hkv=8, D=128,
+                             block_size=16, seed=3302)
+    d = setup_decode(w)
+    q_bits = normal_bf16((sum(lens), w.Hq, w.D), 5400)
+    try:
+        pkv.pkv_debug_set_wait(True)
+        run_prefill(w, d, lens, q_bits)
+        with pytest.raises(pkv.PagedKVError) as e:
+            pkv.pkv_check_status(d.status)
+        assert e.value.code == -4
+    finally:
+        pkv.pkv_debug_set_wait(False)
+    pkv.pkv_status_reset(d.status)
+    d.block_tables[3, 5] = w.num_blocks + 1
+    run_prefill(w, d, lens, q_bits)
+    with pytest.raises(pkv.PagedKVError) as e:
+        pkv.pkv_check_status(d.status)
+    assert e.value.code == -5
