@@ -46,7 +46,6 @@ FALLBACK_HBM_GBS = 6800.0
 # workload, taken with ncu (dram__bytes_read.sum + dram__bytes_write.sum);
 # to be set to None whenever the kernel changes.
 DECODE_TRAFFIC_BYTES = 1_403_409_920
-CPU_SAMPLE_SEQS = 48
 
 
 def parse_args():
@@ -58,11 +57,15 @@ def parse_args():
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--workload", choices=["llama3_8b_gqa", "llama3_8b_gqa_fp8", "trace",
+    ap.add_argument("--workload", choices=["llama3_8b_gqa", "llama2_7b_mha", "tiny",
+                                           "llama3_8b_gqa_fp8", "trace",
                                            "trace_preempt", "swap", "prefix_cache",
                                            "shared_prefix"],
                     default="llama3_8b_gqa",
-                    help="llama3_8b_gqa_fp8: the headline step over FP8 (e4m3) pages; "
+                    help="llama2_7b_mha: the same decode step on 64 sequences of a "
+                         "Llama-2-7B-shaped MHA layer (32/32 heads, L ~ U[128, 2048]); "
+                         "tiny: 4 sequences, 8/8 heads, D=64 (launch-bound, parity-sized); "
+                         "llama3_8b_gqa_fp8: the headline step over FP8 (e4m3) pages; "
                          "trace_preempt: the trace on an undersized pool with preemption; "
                          "shared_prefix: 64 prompts x 4 samples sharing a 1024-token prefix, "
                          "ordinary and sharing-aware decode; "
@@ -75,6 +78,10 @@ def parse_args():
     ap.add_argument("--pool-blocks", type=int, default=9000,
                     help="trace_preempt: KV blocks in the pool (the trace peaks near 10,400)")
     ap.add_argument("--preempt", choices=["swap", "recompute"], default="swap")
+    ap.add_argument("--variant", choices=["a", "b"], default="a",
+                    help="shared_prefix: a = 1024-token prefix (whole blocks, no copies), "
+                         "b = 1032-token prefix (the last shared block is half full, so "
+                         "three of each prompt's four samples copy it on their first append)")
     return ap.parse_args()
 
 
@@ -106,27 +113,38 @@ def max_over_ranks(x: float) -> float:
     return float(t.item())
 
 
-def workload_for_rank(rank: int):
-    from workloads import config3, make_decode_workload, SEED_BASE
-    w = config3()
+DECODE_WORKLOADS = {
+    # name: (config index, length distribution as reported)
+    "llama3_8b_gqa": (3, {"median": 1024, "sigma": 0.8, "clip": [16, 8192]}),
+    "llama2_7b_mha": (2, {"uniform": [128, 2048]}),
+    "tiny": (1, {"cached": [5, 17, 33, 64], "appended": 1}),
+}
+
+
+def workload_for_rank(rank: int, name: str = "llama3_8b_gqa"):
+    from workloads import config1, config2, config3, make_decode_workload, SEED_BASE
+    idx = DECODE_WORKLOADS[name][0]
+    w = {1: config1, 2: config2, 3: config3}[idx]()
     if rank == 0:
         return w
     # weak scaling: every rank decodes its own batch of the same shape
     return make_decode_workload(w.name, w.context_lens, w.Hq, w.Hkv, w.D, w.block_size,
-                                seed=SEED_BASE + 3 + 1000 * rank)
+                                seed=SEED_BASE + idx + 1000 * rank, num_blocks=w.num_blocks)
 
 
-def workload_description(w, partition_size):
+def workload_description(w, partition_size, name: str = "llama3_8b_gqa"):
+    l2 = w.kv_bytes() > 129e6
     return {
-        "workload": "llama3_8b_gqa decode step (kv_append + paged decode attention)",
+        "workload": f"{name} decode step (kv_append + paged decode attention)",
         "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "block_size": w.block_size,
         "num_blocks": w.num_blocks, "context_tokens": w.total_tokens,
-        "context_len": {"median": 1024, "sigma": 0.8, "clip": [16, 8192],
-                        "max": w.max_context_len},
+        "context_len": dict(DECODE_WORKLOADS[name][1], max=w.max_context_len),
         "kv_bytes_per_step": w.kv_bytes(),
         "partition_size": partition_size or 1024,
-        "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB of L2"
-              % (w.kv_bytes() / 1e9),
+        "l2": ("inputs larger than L2: %.2f GB of K/V read per step vs 129 MB of L2"
+               % (w.kv_bytes() / 1e9)) if l2 else
+              ("L2-resident: %.2f MB of K/V per step (launch-bound; reported in us)"
+               % (w.kv_bytes() / 1e6)),
     }
 
 
@@ -183,11 +201,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(w, seqs: int = CPU_SAMPLE_SEQS):
-    """Times the fp64 oracle's decode on a bounded sample of the workload, in a
-    single-threaded child process."""
+def cpu_baseline(name: str = "llama3_8b_gqa"):
+    """Times the fp64 oracle's decode over the whole batch of the workload in a
+    child process: once on one thread, then with the sequences dealt out to
+    one process per host core."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    cmd = [sys.executable, os.path.abspath(__file__), "--_oracle-sample", str(seqs)]
+    cmd = [sys.executable, os.path.abspath(__file__), "--_oracle-sample", name]
     r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
         return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -195,24 +214,64 @@ def cpu_baseline(w, seqs: int = CPU_SAMPLE_SEQS):
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def oracle_sample_main(n_seqs: int):
-    """Child process: the oracle on ``n_seqs`` sequences drawn from the workload."""
-    from oracle import attention
+def _oracle_state(name: str, pick=None, seed_offset: int = 0):
     from tests.oracle_side import build_decode_state
-    from workloads import config3_lengths, generator, make_decode_workload, SEED_BASE
-    lens = config3_lengths()
-    pick = np.sort(generator(SEED_BASE + 3, 9).choice(len(lens), n_seqs, replace=False))
-    w = make_decode_workload("llama3_8b_gqa_sample", lens[pick], Hq=32, Hkv=8, D=128,
-                             block_size=16, seed=SEED_BASE + 3)
-    st = build_decode_state(w)
+    from workloads import make_decode_workload, SEED_BASE
+    w = workload_for_rank(0, name)
+    if pick is not None:
+        w = make_decode_workload(w.name, w.context_lens[pick], w.Hq, w.Hkv, w.D,
+                                 w.block_size, seed=SEED_BASE + 7000 + seed_offset)
+    return w, build_decode_state(w)
+
+
+def _oracle_worker(name, pick, idx, barrier, queue):
+    """One host process of the all-cores oracle run: its own slice of the
+    batch (same lengths and shapes, its own seeded values)."""
+    from oracle import attention
+    w, st = _oracle_state(name, pick, idx)
+    barrier.wait()
+    t0 = time.monotonic()
+    attention.decode(w.q, st.k_cache, st.v_cache, st.tables, w.context_lens, w.block_size,
+                     w.scale)
+    queue.put((t0, time.monotonic(), w.kv_bytes()))
+
+
+def oracle_sample_main(name: str):
+    """Child process: the oracle over the whole batch on one thread, then on
+    every host core (one spawned process per core, sequences dealt out by
+    length so the slices are balanced)."""
+    import multiprocessing as mp
+    from oracle import attention
+    w, st = _oracle_state(name)
     t0 = time.perf_counter()
     attention.decode(w.q, st.k_cache, st.v_cache, st.tables, w.context_lens, w.block_size,
                      w.scale)
     dt = time.perf_counter() - t0
-    print(json.dumps({"value": w.kv_bytes() / dt / 1e9, "unit": UNIT, "cores": 1,
-                      "kind": "oracle", "seconds": dt,
-                      "sample": f"{n_seqs} of 256 sequences ({w.total_tokens} context tokens, "
-                                f"seeded pick), fp64 gather + softmax attention, 1 thread"}))
+    del st
+    line = {"value": w.kv_bytes() / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"the whole batch ({w.S} sequences, {w.total_tokens} context tokens), "
+                      "fp64 gather + softmax attention, 1 thread"}
+    cores = min(os.cpu_count() or 1, w.S)
+    if cores > 1:
+        order = np.argsort(-w.context_lens, kind="stable")
+        picks = [np.sort(order[i::cores]) for i in range(cores)]
+        ctx = mp.get_context("spawn")
+        barrier, queue = ctx.Barrier(cores), ctx.Queue()
+        procs = [ctx.Process(target=_oracle_worker, args=(name, picks[i], i, barrier, queue))
+                 for i in range(cores)]
+        for p in procs:
+            p.start()
+        res = [queue.get(timeout=600) for _ in procs]
+        for p in procs:
+            p.join(timeout=60)
+        wall = max(r[1] for r in res) - min(r[0] for r in res)
+        line["all_cores"] = {"value": sum(r[2] for r in res) / wall / 1e9, "unit": UNIT,
+                             "cores": cores, "seconds": wall,
+                             "sample": "the same lengths dealt out over one process per core "
+                                       "(each with its own seeded values), wall time from a "
+                                       "common barrier to the last finish"}
+    print(json.dumps(line))
 
 
 def run_reference(args):
@@ -862,7 +921,7 @@ def run_shared_prefix(args):
 
     rank, world, local = dist_info()
     torch.cuda.set_device(local)
-    w = config4("a")
+    w = config4(args.variant)
     d = setup_shared_prefix(w)
     start, members, sh = shared_groups(w, d)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
@@ -896,10 +955,25 @@ def run_shared_prefix(args):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / args.steps
 
+    pairs = None
+    if d.cow_pairs:
+        # the copy-on-write copies of variant b (half-full shared blocks),
+        # timed again into blocks of a scratch sequence so the samples' own
+        # copies keep their tails
+        scratch = d.alloc.seq_create()
+        d.alloc.seq_append_slots(scratch, len(d.cow_pairs) * w.block_size)
+        dst = d.alloc.seq_block_table(scratch)
+        pairs = torch.tensor([[src, dst[i]] for i, (src, _) in enumerate(d.cow_pairs)],
+                             dtype=torch.int32, device="cuda")
+
+    def copies():
+        pkv.pkv_block_copy(d.k_cache, d.v_cache, pairs, status=d.status, stream=stream)
+
     with ClockSampler(local) as clocks:
         time.sleep(0.3)
         plain_ms = timed(plain)
         grouped_ms = timed(grouped)
+        copy_ms = timed(copies) if pairs is not None else None
     pkv.pkv_check_status(d.status)
     logical, unique = w.logical_kv_bytes(), w.unique_kv_bytes()
     peak, peak_kind = measured_peaks()
@@ -910,8 +984,9 @@ def run_shared_prefix(args):
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": grouped_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "64 prompts x 4 samples, shared 1024-token prefix (forked "
-                               "blocks), tails U[0,512], 32/8 heads, D=128, B=16",
+        "config": {"workload": "64 prompts x 4 samples, shared %d-token prefix (forked "
+                               "blocks), tails U[0,512], 32/8 heads, D=128, B=16" % w.prefix_len,
+                   "variant": args.variant,
                    "logical_kv_bytes": logical, "unique_kv_bytes": unique,
                    "l2": "%.2f GB of unique K/V (> 129 MB L2)" % (unique / 1e9)},
         "ordinary_ms": plain_ms, "sharing_aware_ms": grouped_ms,
@@ -924,10 +999,15 @@ def run_shared_prefix(args):
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": gbs(unique, grouped_ms) / peak, "traffic": None,
                      "algorithmic_bytes_per_launch": unique},
-        "gpu_launches": 2 * 3 * args.steps,
+        "gpu_launches": 2 * 3 * args.steps + (args.steps if pairs is not None else 0),
         "clocks": clocks.summary(),
         "cpu_baseline": None,
     }
+    if pairs is not None:
+        blk = 2 * w.Hkv * w.block_size * w.D * 2
+        line["block_copy"] = {"pairs": len(d.cow_pairs), "ms": copy_ms,
+                              "gbs": 2 * blk * len(d.cow_pairs) / (copy_ms * 1e-3) / 1e9,
+                              "note": "read + write of each copied block (K and V)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -958,7 +1038,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    w = workload_for_rank(rank)
+    w = workload_for_rank(rank, args.workload)
     d = setup_decode(w, partition_size=args.partition_size, append_last=False)
     stream = torch.cuda.current_stream()
     parts = pkv.pkv_decode_workspace_bytes(1, 1, w.D, w.max_context_len, args.partition_size)
@@ -996,7 +1076,8 @@ def main():
         barrier()
     pkv.pkv_check_status(d.status)
     total_ms = start.elapsed_time(end)
-    decode_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    per_call = np.array([a.elapsed_time(b) for a, b in ev])
+    decode_ms = float(per_call.mean())
     total_ms = max_over_ranks(total_ms)
     ms_per_step = total_ms / args.steps
     kv_bytes = w.kv_bytes()
@@ -1009,7 +1090,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_description(w, args.partition_size),
+        "config": workload_description(w, args.partition_size, args.workload),
         "attention_tokens_per_s_per_layer": world * w.S / (ms_per_step * 1e-3),
         "pct_hbm_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "hbm", "kernel": "pkv_paged_attention_decode (plan + split-K "
@@ -1017,17 +1098,22 @@ def main():
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": DECODE_TRAFFIC_BYTES if args.partition_size in (0, 1024) else None,
-                     "traffic_kernel": "paged_decode_kernel<128,4> (ncu, one launch)",
+                     "traffic": DECODE_TRAFFIC_BYTES if (args.partition_size in (0, 1024) and
+                                                         args.workload == "llama3_8b_gqa")
+                     else None,
+                     "traffic_kernel": "paged_decode_kernel<%d,%d> (ncu, one launch)"
+                                       % (w.D, w.Hq // w.Hkv),
                      "algorithmic_bytes_per_launch": kv_bytes,
-                     "avg_launch_ms": decode_ms},
+                     "avg_launch_ms": decode_ms,
+                     "launch_ms_percentiles": {q: float(np.percentile(per_call, int(q[1:])))
+                                               for q in ("p10", "p50", "p90")}},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
     if e2e is not None:
         line["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(args.workload)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -1079,6 +1165,6 @@ def e2e_measure(w, d, args, pkv, torch, steps=None):
 
 if __name__ == "__main__":
     if len(sys.argv) >= 3 and sys.argv[1] == "--_oracle-sample":
-        oracle_sample_main(int(sys.argv[2]))
+        oracle_sample_main(sys.argv[2])
         sys.exit(0)
     sys.exit(main())
