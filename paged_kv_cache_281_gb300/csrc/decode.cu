@@ -528,20 +528,25 @@ WsLayout ws_layout(int64_t S, int64_t Hq, int64_t D, int64_t max_parts) {
 //    rounded to fp16 once per item: exact for 2^-14 <= |q| <= 65504) instead
 //    of the columns the hardware layout names; two codes widen to one fp16
 //    pair (exact: every e4m3 value is an fp16 value);
-//  * values: one transposing 8-bit ldmatrix per 16 x 16 code block hands
-//    thread (g, t) value rows 4t .. 4t+3 at columns g and 8 + g, which are
-//    the B fragments of two fp16 MMAs once the score columns are assigned to
-//    keys so that the thread's probabilities cover the same four rows;
+//  * values: the product runs transposed, O^T += V^T P'^T, with 16 value
+//    columns as the MMA's rows and the probabilities as its 8 columns. One
+//    transposing 8-bit ldmatrix per 16 x 16 code block hands thread (g, t)
+//    value rows 4t .. 4t+3 at columns g and 8 + g: exactly its A fragment
+//    once the score columns are assigned to keys so that the thread's
+//    probabilities cover the same four rows, which are then its B fragment;
 //  * a key's scale multiplies its score and a value's scale its probability
-//    (P' = p * s_v, as fp16 hi + lo parts) before the P V product, so no code
-//    is rescaled element by element; value rows past the sequence end are
-//    zeroed in shared memory.
+//    (P' = p * s_v) before the P V product, so no code is rescaled element by
+//    element; P' enters as fp16 hi + lo parts: for G <= 4 the score rows
+//    4..7 repeat rows 0..3 and carry the lo parts, so one MMA per 16 value
+//    columns takes both (G = 8 issues a second MMA for lo); value rows past
+//    the sequence end are zeroed in shared memory.
 template <int D>
 struct Cfg8 {
   static constexpr int kTile8 = kTileTokens * D;         // codes of one tensor tile
   static constexpr int kCodeStage = 2 * kTile8;          // keys, then values
   static constexpr int kScaleStage = 2 * kTileTokens * 4;  // key scales, then value scales
-  static constexpr int kStages = D == 128 ? 4 : 6;
+  // four CTAs per SM: 4 warps x 3 stages x 4.2 KB at D = 128
+  static constexpr int kStages = D == 128 ? 3 : 6;
   static constexpr int kWarpBytes =
       (kStages * (kCodeStage + kScaleStage) + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes = kWarps * kWarpBytes + 1024;
@@ -615,12 +620,15 @@ __device__ __forceinline__ void ldmatrix_b8_16x16_trans(uint32_t addr, uint32_t&
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, 4)
     paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
   using C = Cfg8<D>;
   constexpr int KS = D / 16;
-  constexpr int NT = D / 8;
+  constexpr int NC = D / 16;  // 16-column blocks of O^T
+  // G <= 4: score row r < 4 is query head r (hi part of P'), row 4 + r the
+  // same head again (lo part); G = 8: rows are heads, lo takes its own MMA
+  constexpr bool kLoRows = G <= 4;
   extern __shared__ uint8_t dsm[];
   __shared__ __align__(8) uint64_t bars[kWarps][C::kStages];
   __shared__ int32_t s_next;
@@ -691,13 +699,15 @@ __global__ void __launch_bounds__(kThreads, 3)
       for (int k = 0; k < npro; ++k) issue(k, k);
     }
 
-    // Q fragments in fp16 (rows g < G; rows g+8 are always zero). Thread t
-    // owns d = (D/4) t + 4 ks + {0,1 | 2,3} in k-step ks (see the key loads).
+    // Q fragments in fp16 (row g holds head g, or head g & 3 when G <= 4;
+    // rows g+8 are always zero). Thread t owns d = (D/4) t + 4 ks + {0,1 |
+    // 2,3} in k-step ks (see the key loads).
     uint32_t qa[KS][2];
     {
-      const bool live = g < G;
+      const int qh = kLoRows ? (g & 3) : g;
+      const bool live = qh < G;
       const __nv_bfloat16* qrow =
-          a.q + ((int64_t)s * a.Hq + kvh * G + (live ? g : 0)) * D + (D / 4) * t;
+          a.q + ((int64_t)s * a.Hq + kvh * G + (live ? qh : 0)) * D + (D / 4) * t;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const uint2 w =
@@ -708,9 +718,11 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
 
     float m = -INFINITY, l = 0.f;
-    float o[NT][4];
+    // O^T block c: thread (g, t) holds value columns 16c + g (o[c][0..1]) and
+    // 16c + 8 + g (o[c][2..3]) of score rows 2t and 2t + 1
+    float o[NC][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    for (int c = 0; c < NC; ++c) o[c][0] = o[c][1] = o[c][2] = o[c][3] = 0.f;
 
     for (int k = 0; k < n_mine; ++k) {
       const int st = k % C::kStages;
@@ -793,32 +805,38 @@ __global__ void __launch_bounds__(kThreads, 3)
       l = l * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
       m = m_new;
       if (__any_sync(0xffffffffu, alpha != 1.f)) {  // the running max moved
+        const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
+        const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          o[nt][0] *= alpha;
-          o[nt][1] *= alpha;
-          o[nt][2] *= alpha;
-          o[nt][3] *= alpha;
+        for (int c = 0; c < NC; ++c) {
+          o[c][0] *= a0;
+          o[c][1] *= a1;
+          o[c][2] *= a0;
+          o[c][3] *= a1;
         }
       }
-      // P' = p * s_v for keys 4t .. 4t+3 in fp16 hi (rows 0..7) + lo (rows
-      // 8..15); keys past the end carry p = 0 and a zeroed value row
+      // P' = p * s_v for keys 4t .. 4t+3 of score row g, in fp16 hi + lo;
+      // keys past the end carry p = 0 and a zeroed value row
       float pv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) pv[i] = 4 * t + i < valid ? pr[i] * vsc[4 * t + i] : 0.f;
-      const uint32_t pa0 = pack_f16x2(pv[0], pv[1]);
-      const uint32_t pa2 = pack_f16x2(pv[2], pv[3]);
-      const uint32_t pl0 = pack_f16x2(pv[0] - f16_lo_to_f32(pa0), pv[1] - f16_hi_to_f32(pa0));
-      const uint32_t pl2 = pack_f16x2(pv[2] - f16_lo_to_f32(pa2), pv[3] - f16_hi_to_f32(pa2));
+      const uint32_t ph0 = pack_f16x2(pv[0], pv[1]);
+      const uint32_t ph2 = pack_f16x2(pv[2], pv[3]);
+      const uint32_t pl0 = pack_f16x2(pv[0] - f16_lo_to_f32(ph0), pv[1] - f16_hi_to_f32(ph0));
+      const uint32_t pl2 = pack_f16x2(pv[2] - f16_lo_to_f32(ph2), pv[3] - f16_hi_to_f32(ph2));
+      const bool lo_row = kLoRows && g >= 4;
+      const uint32_t pb0 = lo_row ? pl0 : ph0, pb2 = lo_row ? pl2 : ph2;
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
+      for (int c = 0; c < NC; ++c) {
         uint32_t r0, r1;
         ldmatrix_b8_16x16_trans(vcodes + code_off<D>(lane & 15, c), r0, r1);
-        uint32_t b0, b1, b2, b3;
-        e4m3x4_to_f16x4(r0, b0, b1);
-        e4m3x4_to_f16x4(r1, b2, b3);
-        mma_f16_16816(o[2 * c], pa0, pl0, pa2, pl2, b0, b1);
-        mma_f16_16816(o[2 * c + 1], pa0, pl0, pa2, pl2, b2, b3);
+        // v0, v1: keys (4t, 4t+1), (4t+2, 4t+3) of value column 16c + g;
+        // v2, v3: the same keys of column 16c + 8 + g
+        uint32_t v0, v1, v2, v3;
+        e4m3x4_to_f16x4(r0, v0, v1);
+        e4m3x4_to_f16x4(r1, v2, v3);
+        mma_f16_16816(o[c], v0, v2, v1, v3, pb0, pb2);
+        if constexpr (!kLoRows) mma_f16_16816(o[c], v0, v2, v1, v3, pl0, pl2);
       }
       if (valid < kTileTokens) fence_proxy_async_smem();  // zeroing stores before TMA reuse
       __syncwarp();
@@ -831,13 +849,27 @@ __global__ void __launch_bounds__(kThreads, 3)
     if (s_abort) return;
     float2* cml = reinterpret_cast<float2*>(base_ptr);
     float* co = reinterpret_cast<float*>(base_ptr + 256);
-    if (g < G) {
-      if (t == 0) cml[warp * G + g] = make_float2(m, l);
-      float* row = co + (warp * G + g) * D;
+    if (g < G && t == 0) cml[warp * G + g] = make_float2(m, l);
+    if constexpr (kLoRows) {
+      // columns 4 + r (lo) sit two lanes up from columns r (hi)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        *reinterpret_cast<float2*>(row + nt * 8 + 2 * t) =
-            make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3]);
+      for (int c = 0; c < NC; ++c)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[c][e] += __shfl_down_sync(0xffffffffu, o[c][e], 2);
+    }
+    if (!kLoRows || t < 2) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int h = 2 * t + j;
+        if (h < G) {
+          float* row = co + (warp * G + h) * D;
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            row[16 * c + g] = o[c][j];
+            row[16 * c + 8 + g] = o[c][2 + j];
+          }
+        }
+      }
     }
     __syncthreads();
     const int nparts = (L + P - 1) / P;
