@@ -523,23 +523,26 @@ WsLayout ws_layout(int64_t S, int64_t Hq, int64_t D, int64_t max_parts) {
 //  * a tile's codes arrive by TMA (16 rows x D bytes per tensor, 128-byte
 //    swizzled when D = 128) and its 16 key and 16 value scales by two small
 //    bulk copies into a separate scale ring;
-//  * scores: the MMA's k index is a sum index, so each thread owns a
-//    contiguous D/4-byte run of every key row (and the matching run of q,
-//    rounded to fp16 once per item: exact for 2^-14 <= |q| <= 65504) instead
-//    of the columns the hardware layout names; two codes widen to one fp16
-//    pair (exact: every e4m3 value is an fp16 value);
-//  * values: the product runs transposed, O^T += V^T P'^T, with 16 value
-//    columns as the MMA's rows and the probabilities as its 8 columns. One
-//    transposing 8-bit ldmatrix per 16 x 16 code block hands thread (g, t)
-//    value rows 4t .. 4t+3 at columns g and 8 + g: exactly its A fragment
-//    once the score columns are assigned to keys so that the thread's
-//    probabilities cover the same four rows, which are then its B fragment;
+//  * scores run transposed, S^T = K Q^T, with the tile's 16 keys as the
+//    MMA's rows and 8 score columns (query heads) as its columns. The MMA's
+//    k index is a sum index, so each thread owns a contiguous D/4-byte run
+//    of its two key rows (and the matching run of q, rounded to fp16 once
+//    per item: exact for 2^-14 <= |q| <= 65504) instead of the columns the
+//    hardware layout names; two codes widen to one fp16 pair (exact: every
+//    e4m3 value is an fp16 value);
+//  * values: the product runs transposed too, O^T += V^T P'^T, with 16
+//    value columns as the MMA's rows. One transposing 8-bit ldmatrix per
+//    16 x 16 code block hands thread (g, t) value rows 4t .. 4t+3 at
+//    columns g and 8 + g, its A fragment; the keys of the score rows are
+//    ordered so that a movmatrix transpose of the packed P' blocks hands the
+//    same thread column g of those four keys, its B fragment;
 //  * a key's scale multiplies its score and a value's scale its probability
 //    (P' = p * s_v) before the P V product, so no code is rescaled element by
-//    element; P' enters as fp16 hi + lo parts: for G <= 4 the score rows
-//    4..7 repeat rows 0..3 and carry the lo parts, so one MMA per 16 value
-//    columns takes both (G = 8 issues a second MMA for lo); value rows past
-//    the sequence end are zeroed in shared memory.
+//    element; P' enters as fp16 hi + lo parts: for G <= 4 the score
+//    columns 4..7 repeat columns 0..3 and carry the lo parts, so one MMA per
+//    16 value columns takes both (G = 8 issues a second MMA for lo); O^T and
+//    S^T share their columns, so every lane rescales with its own factors;
+//    value rows past the sequence end are zeroed in shared memory.
 template <int D>
 struct Cfg8 {
   static constexpr int kTile8 = kTileTokens * D;         // codes of one tensor tile
@@ -610,6 +613,14 @@ __device__ __forceinline__ void issue_tile_rows8(const CUtensorMap* tk, const CU
   }
 }
 
+// An 8 x 8 matrix of 16-bit values, one pair per thread (thread (g, t) holds
+// row g, columns 2t and 2t + 1), transposed across the warp.
+__device__ __forceinline__ uint32_t movmatrix_trans_b16(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
 // 16 x 16 bytes at row addresses given by lanes 0..15, transposed: thread
 // (g, t) receives rows 4t .. 4t+3 of column g (r0) and of column 8 + g (r1).
 __device__ __forceinline__ void ldmatrix_b8_16x16_trans(uint32_t addr, uint32_t& r0,
@@ -626,8 +637,9 @@ __global__ void __launch_bounds__(kThreads, 4)
   using C = Cfg8<D>;
   constexpr int KS = D / 16;
   constexpr int NC = D / 16;  // 16-column blocks of O^T
-  // G <= 4: score row r < 4 is query head r (hi part of P'), row 4 + r the
-  // same head again (lo part); G = 8: rows are heads, lo takes its own MMA
+  // G <= 4: score column r < 4 is query head r (hi part of P'), column
+  // 4 + r the same head again (lo part); G = 8: columns are heads, lo takes
+  // its own MMA
   constexpr bool kLoRows = G <= 4;
   extern __shared__ uint8_t dsm[];
   __shared__ __align__(8) uint64_t bars[kWarps][C::kStages];
@@ -699,9 +711,9 @@ __global__ void __launch_bounds__(kThreads, 4)
       for (int k = 0; k < npro; ++k) issue(k, k);
     }
 
-    // Q fragments in fp16 (row g holds head g, or head g & 3 when G <= 4;
-    // rows g+8 are always zero). Thread t owns d = (D/4) t + 4 ks + {0,1 |
-    // 2,3} in k-step ks (see the key loads).
+    // Q^T fragments in fp16 (column g holds head g, or head g & 3 when
+    // G <= 4). Thread t owns d = (D/4) t + 4 ks + {0,1 | 2,3} in k-step ks
+    // (see the key loads).
     uint32_t qa[KS][2];
     {
       const int qh = kLoRows ? (g & 3) : g;
@@ -717,9 +729,11 @@ __global__ void __launch_bounds__(kThreads, 4)
       }
     }
 
-    float m = -INFINITY, l = 0.f;
+    // running max and sum of score columns 2t (m0, l0) and 2t + 1 (m1, l1);
+    // l holds this thread's keys only until the end of the item
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     // O^T block c: thread (g, t) holds value columns 16c + g (o[c][0..1]) and
-    // 16c + 8 + g (o[c][2..3]) of score rows 2t and 2t + 1
+    // 16c + 8 + g (o[c][2..3]) of score columns 2t and 2t + 1
     float o[NC][4];
 #pragma unroll
     for (int c = 0; c < NC; ++c) o[c][0] = o[c][1] = o[c][2] = o[c][3] = 0.f;
@@ -763,69 +777,86 @@ __global__ void __launch_bounds__(kThreads, 4)
       const float* ksc = reinterpret_cast<const float*>(sring_ptr + st * C::kScaleStage);
       const float* vsc = ksc + kTileTokens;
 
-      // S = Q K^T. Score column n of n-block j belongs to key
-      // 4 (n >> 1) + 2 j + (n & 1), so thread (g, t) loads key row
-      // 4 (g >> 1) + 2 j + (g & 1) and ends up with the scores of keys
-      // 4t + 2j + {0, 1}.
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // S^T = K Q^T: the tile's 16 keys are the MMA rows, the 8 score
+      // columns its columns. Row r holds key 4 (r >> 1) + (r & 1) for r < 8
+      // and that key + 2 for row r + 8, so thread (g, t) loads keys kr0 (row
+      // g) and kr1 (row g + 8) and holds their scores for columns 2t, 2t + 1;
+      // after a transpose it holds columns g of keys 4t .. 4t+3, the rows its
+      // value fragments cover.
+      const int kr0 = 4 * (g >> 1) + (g & 1), kr1 = kr0 + 2;
+      uint32_t kw0[KS], kw1[KS];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int kr = 4 * (g >> 1) + 2 * j + (g & 1);
-        uint32_t kw[KS];
+      for (int v = 0; v < KS / 4; ++v) {
+        const uint4 u0 =
+            *reinterpret_cast<const uint4*>(kptr + code_off<D>(kr0, (KS / 4) * t + v));
+        const uint4 u1 =
+            *reinterpret_cast<const uint4*>(kptr + code_off<D>(kr1, (KS / 4) * t + v));
+        kw0[4 * v] = u0.x, kw0[4 * v + 1] = u0.y, kw0[4 * v + 2] = u0.z, kw0[4 * v + 3] = u0.w;
+        kw1[4 * v] = u1.x, kw1[4 * v + 1] = u1.y, kw1[4 * v + 2] = u1.z, kw1[4 * v + 3] = u1.w;
+      }
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};  // even, odd k-steps
 #pragma unroll
-        for (int v = 0; v < KS / 4; ++v) {
-          const uint4 u =
-              *reinterpret_cast<const uint4*>(kptr + code_off<D>(kr, (KS / 4) * t + v));
-          kw[4 * v] = u.x, kw[4 * v + 1] = u.y, kw[4 * v + 2] = u.z, kw[4 * v + 3] = u.w;
-        }
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          uint32_t b0, b1;
-          e4m3x4_to_f16x4(kw[ks], b0, b1);
-          mma_f16_16816(sc[j], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
-        }
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t x0, x1, y0, y1;
+        e4m3x4_to_f16x4(kw0[ks], x0, x1);
+        e4m3x4_to_f16x4(kw1[ks], y0, y1);
+        if (ks & 1)
+          mma_f16_16816(sb, x0, y0, x1, y1, qa[ks][0], qa[ks][1]);
+        else
+          mma_f16_16816(sa, x0, y0, x1, y1, qa[ks][0], qa[ks][1]);
       }
 
+      const bool ok0 = kr0 < valid, ok1 = kr1 < valid;
+      const float sk0 = ksc[kr0] * a.scale_log2, sk1 = ksc[kr1] * a.scale_log2;
+      // x: (key kr0, column 2t), (kr0, 2t + 1), (kr1, 2t), (kr1, 2t + 1)
       float x[4];
+      x[0] = ok0 ? (sa[0] + sb[0]) * sk0 : -INFINITY;
+      x[1] = ok0 ? (sa[1] + sb[1]) * sk0 : -INFINITY;
+      x[2] = ok1 ? (sa[2] + sb[2]) * sk1 : -INFINITY;
+      x[3] = ok1 ? (sa[3] + sb[3]) * sk1 : -INFINITY;
+      float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int key = 4 * t + 2 * j + e;
-          x[2 * j + e] = key < valid ? sc[j][e] * ksc[key] * a.scale_log2 : -INFINITY;
-        }
-      float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m, mx);
-      const float alpha = fast_exp2(m - m_new);
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
       float pr[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) pr[i] = fast_exp2(x[i] - m_new);
-      l = l * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
-      m = m_new;
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {  // the running max moved
-        const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
-        const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+      pr[0] = fast_exp2(x[0] - mn0);
+      pr[1] = fast_exp2(x[1] - mn1);
+      pr[2] = fast_exp2(x[2] - mn0);
+      pr[3] = fast_exp2(x[3] - mn1);
+      l0 = l0 * al0 + (pr[0] + pr[2]);
+      l1 = l1 * al1 + (pr[1] + pr[3]);
+      m0 = mn0;
+      m1 = mn1;
+      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {  // a running max moved
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-          o[c][0] *= a0;
-          o[c][1] *= a1;
-          o[c][2] *= a0;
-          o[c][3] *= a1;
+          o[c][0] *= al0;
+          o[c][1] *= al1;
+          o[c][2] *= al0;
+          o[c][3] *= al1;
         }
       }
-      // P' = p * s_v for keys 4t .. 4t+3 of score row g, in fp16 hi + lo;
-      // keys past the end carry p = 0 and a zeroed value row
-      float pv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) pv[i] = 4 * t + i < valid ? pr[i] * vsc[4 * t + i] : 0.f;
-      const uint32_t ph0 = pack_f16x2(pv[0], pv[1]);
-      const uint32_t ph2 = pack_f16x2(pv[2], pv[3]);
-      const uint32_t pl0 = pack_f16x2(pv[0] - f16_lo_to_f32(ph0), pv[1] - f16_hi_to_f32(ph0));
-      const uint32_t pl2 = pack_f16x2(pv[2] - f16_lo_to_f32(ph2), pv[3] - f16_hi_to_f32(ph2));
-      const bool lo_row = kLoRows && g >= 4;
-      const uint32_t pb0 = lo_row ? pl0 : ph0, pb2 = lo_row ? pl2 : ph2;
+      // P' = p * s_v in fp16 hi + lo; keys past the end carry p = 0 (and a
+      // zero scale: their scale slots are stale) and a zeroed value row
+      const float sv0 = ok0 ? vsc[kr0] : 0.f, sv1 = ok1 ? vsc[kr1] : 0.f;
+      const float pv0 = pr[0] * sv0, pv1 = pr[1] * sv0, pv2 = pr[2] * sv1, pv3 = pr[3] * sv1;
+      const uint32_t hA = pack_f16x2(pv0, pv1), hB = pack_f16x2(pv2, pv3);
+      const uint32_t lA = pack_f16x2(pv0 - f16_lo_to_f32(hA), pv1 - f16_hi_to_f32(hA));
+      const uint32_t lB = pack_f16x2(pv2 - f16_lo_to_f32(hB), pv3 - f16_hi_to_f32(hB));
+      // the 8 x 8 blocks (rows 0..7 and 8..15) transposed: column g of keys
+      // (4t, 4t+1) and (4t+2, 4t+3); columns 4..7 carry the lo parts (G <= 4)
+      const bool lo_col = kLoRows && t >= 2;
+      const uint32_t pb0 = movmatrix_trans_b16(lo_col ? lA : hA);
+      const uint32_t pb2 = movmatrix_trans_b16(lo_col ? lB : hB);
+      uint32_t pl0 = 0u, pl2 = 0u;
+      if constexpr (!kLoRows) {
+        pl0 = movmatrix_trans_b16(lA);
+        pl2 = movmatrix_trans_b16(lB);
+      }
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         uint32_t r0, r1;
@@ -843,13 +874,19 @@ __global__ void __launch_bounds__(kThreads, 4)
       if (k + C::kStages < n_mine) issue(k + C::kStages, st);
     }
 
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
     __syncthreads();
     if (s_abort) return;
     float2* cml = reinterpret_cast<float2*>(base_ptr);
     float* co = reinterpret_cast<float*>(base_ptr + 256);
-    if (g < G && t == 0) cml[warp * G + g] = make_float2(m, l);
+    if (g == 0 && (!kLoRows || t < 2)) {
+      if (2 * t < G) cml[warp * G + 2 * t] = make_float2(m0, l0);
+      if (2 * t + 1 < G) cml[warp * G + 2 * t + 1] = make_float2(m1, l1);
+    }
     if constexpr (kLoRows) {
       // columns 4 + r (lo) sit two lanes up from columns r (hi)
 #pragma unroll
