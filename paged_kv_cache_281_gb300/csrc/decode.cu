@@ -44,13 +44,13 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kTileTokens = 16;
 constexpr int kDefaultPartition = 1024;
 
-template <int D>
+template <int D, int Stages = (D == 128 ? 3 : 6)>
 struct Cfg {
   static constexpr int kHalves = D / 64;            // 128-byte swizzled column halves
   static constexpr int kHalfBytes = kTileTokens * 128;
   static constexpr int kTensorBytes = kHalves * kHalfBytes;
   static constexpr int kStageBytes = 2 * kTensorBytes;  // keys, then values
-  static constexpr int kStages = D == 128 ? 3 : 6;
+  static constexpr int kStages = Stages;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kSmemBytes = kWarps * kRingBytes + 1024;  // + alignment slack
 };
@@ -1021,13 +1021,16 @@ __global__ void __launch_bounds__(1024) decode_group_plan_kernel(DecodeArgs a) {
 // thread owns rows g and g + 8 of the MMA fragments. P enters the P V product
 // as two MMAs (bf16 hi, then lo), since all 16 operand rows may be in use.
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     paged_decode_group_kernel(const __grid_constant__ CUtensorMap tmap_k,
                               const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
-  using C = Cfg<D>;
+  // three CTAs per SM: 2 stages of 8 KB per warp at D = 128 (168 registers)
+  using C = Cfg<D, D == 128 ? 2 : 4>;
   constexpr int KS = D / 16;
   constexpr int NT = D / 8;
   constexpr int M = 16 / G;  // members per item
+  static_assert(512 + kWarps * 16 * D * 4 <= kWarps * C::kRingBytes,
+                "the merge buffer reuses the rings");
   extern __shared__ uint8_t dsm[];
   __shared__ __align__(8) uint64_t bars[kWarps][C::kStages];
   __shared__ int32_t s_next;
@@ -1311,7 +1314,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 template <int D, int G>
 int launch_decode_group(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                         const DeviceInfo& dev, cudaStream_t stream) {
-  using C = Cfg<D>;
+  using C = Cfg<D, D == 128 ? 2 : 4>;
   static std::once_flag once;
   static int blocks_per_sm = 0;
   static cudaError_t attr_err = cudaSuccess;
