@@ -60,7 +60,7 @@ def parse_args():
     ap.add_argument("--workload", choices=["llama3_8b_gqa", "llama2_7b_mha", "tiny",
                                            "llama3_8b_gqa_fp8", "trace",
                                            "trace_preempt", "swap", "prefix_cache",
-                                           "shared_prefix"],
+                                           "shared_prefix", "prefill"],
                     default="llama3_8b_gqa",
                     help="llama2_7b_mha: the same decode step on 64 sequences of a "
                          "Llama-2-7B-shaped MHA layer (32/32 heads, L ~ U[128, 2048]); "
@@ -68,7 +68,8 @@ def parse_args():
                          "llama3_8b_gqa_fp8: the headline step over FP8 (e4m3) pages; "
                          "trace_preempt: the trace on an undersized pool with preemption; "
                          "shared_prefix: 64 prompts x 4 samples sharing a 1024-token prefix, "
-                         "ordinary and sharing-aware decode; "
+                         "ordinary and sharing-aware decode; prefill: chunked prefill over "
+                         "fresh prompts (--prefill-shapes); "
                          "trace: the 200-iteration continuous-batching workload; swap: "
                          "preemption by swapping, every block of the decode batch out to "
                          "pinned host memory and back; prefix_cache: 256 requests sharing a "
@@ -78,6 +79,9 @@ def parse_args():
     ap.add_argument("--pool-blocks", type=int, default=9000,
                     help="trace_preempt: KV blocks in the pool (the trace peaks near 10,400)")
     ap.add_argument("--preempt", choices=["swap", "recompute"], default="swap")
+    ap.add_argument("--prefill-shapes", default="32x1024,152x512,8x4096",
+                    help="prefill: comma-separated SxC launches (S fresh prompts of C tokens); "
+                         "the first is the headline")
     ap.add_argument("--variant", choices=["a", "b"], default="a",
                     help="shared_prefix: a = 1024-token prefix (whole blocks, no copies), "
                          "b = 1032-token prefix (the last shared block is half full, so "
@@ -809,6 +813,94 @@ def run_prefix_cache(args):
     return 0
 
 
+def run_prefill(args):
+    """Chunked prefill over fresh prompts (no cached prefix): S sequences of C
+    prompt tokens each, 32 query / 8 KV heads, D=128, B=16, blocks placed by
+    a seeded permutation, values N(0,1) from a seeded device generator. One
+    line; the first shape of ``--prefill-shapes`` is the headline, the
+    others are reported beside it."""
+    import torch
+    import paged_kv_cache_281_gb300 as pkv
+    from tests.gpu_harness import poisoned_pools
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    Hq, Hkv, D, B = 32, 8, 128, 16
+    scale = 1.0 / math.sqrt(D)
+    stream = torch.cuda.current_stream()
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {"bf16_tflops": 1900.0}
+    peak = float(peaks["bf16_tflops"])
+    shapes = [tuple(int(v) for v in x.split("x")) for x in args.prefill_shapes.split(",")]
+    steps = max(5, min(args.steps, 100))
+    res = []
+    with ClockSampler(local) as clocks:
+        for S, C in shapes:
+            nb = S * math.ceil(C / B)
+            kc, vc = poisoned_pools(nb, Hkv, B, D, poison=False)
+            gen = torch.Generator(device="cuda").manual_seed(0x281 + S * 100003 + C)
+            kc.copy_(torch.randn(kc.shape, generator=gen, device="cuda").to(torch.bfloat16))
+            vc.copy_(torch.randn(vc.shape, generator=gen, device="cuda").to(torch.bfloat16))
+            perm = torch.randperm(nb, generator=torch.Generator().manual_seed(0x281 + C))
+            tables = perm.to(torch.int32).view(S, -1).cuda()
+            lens = torch.full((S,), C, dtype=torch.int32, device="cuda")
+            cu = torch.arange(0, S + 1, dtype=torch.int32, device="cuda") * C
+            q = torch.randn(S * C, Hq, D, generator=gen, device="cuda").to(torch.bfloat16)
+            out = torch.empty_like(q)
+            ws = torch.empty(pkv.pkv_prefill_workspace_bytes(S, S * C, Hq, D), dtype=torch.uint8,
+                             device="cuda")
+            status = pkv.new_status()
+
+            def one():
+                pkv.pkv_paged_attention_prefill(out, q, cu, lens, kc, vc, tables, C, C, scale, ws,
+                                                status=status, stream=stream)
+
+            for _ in range(max(3, args.warmup)):
+                one()
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(steps)]
+            for a, b in ev:
+                a.record(stream)
+                one()
+                b.record(stream)
+            torch.cuda.synchronize()
+            pkv.pkv_check_status(status)
+            t = np.array([a.elapsed_time(b) for a, b in ev])
+            flops = S * 4 * D * Hq * (C * (C + 1) // 2)
+            ms = float(t.mean())
+            res.append({"S": S, "chunk": C, "ms": ms, "p10_ms": float(np.percentile(t, 10)),
+                        "p90_ms": float(np.percentile(t, 90)), "tflops": flops / ms / 1e9,
+                        "frac": flops / ms / 1e9 / peak, "flops": flops,
+                        "kv_bytes": 2 * nb * Hkv * B * D * 2})
+            del kc, vc, q, out, ws
+            torch.cuda.empty_cache()
+    h = res[0]
+    line = {
+        "metric": "chunked prefill: attention TFLOP/s (algorithmic 4*D*Hq*visible keys per "
+                  "query row)",
+        "value": world * h["tflops"], "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
+        "warmup": max(3, args.warmup), "ms_per_step": h["ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "fresh prompts, %d sequences x %d tokens, 32/8 heads, D=128, "
+                               "B=16, causal" % (h["S"], h["chunk"]),
+                   "l2": "K/V pools of %.2f GB, Q/O %.2f GB (> 129 MB L2)"
+                         % (h["kv_bytes"] / 1e9, 2 * h["S"] * h["chunk"] * Hq * D * 2 / 1e9)},
+        "shapes": res,
+        "roofline": {"bound": "tensor", "kernel": "paged_prefill_kernel (plan + persistent "
+                     "grid, or one CTA per item)", "achieved": h["tflops"], "peak": peak,
+                     "peak_kind": "measured bf16_tflops (burst)", "unit": "TFLOP/s",
+                     "frac": h["frac"], "traffic": None,
+                     "algorithmic_flops_per_launch": h["flops"]},
+        "gpu_launches": 2 * steps * len(shapes),
+        "clocks": clocks.summary(),
+        "cpu_baseline": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_fp8(args):
     """The Llama-3-8B GQA decode step over FP8 (e4m3) pages with one fp32 scale
     per token row: kv_append_fp8 of each sequence's newest token, then
@@ -1029,6 +1121,8 @@ def main():
         return run_shared_prefix(args)
     if args.workload == "prefix_cache":
         return run_prefix_cache(args)
+    if args.workload == "prefill":
+        return run_prefill(args)
     import torch
     import paged_kv_cache_281_gb300 as pkv
     from tests.gpu_harness import decode_step, setup_decode, to_dev_bf16

@@ -91,6 +91,23 @@ int encode_tile_map_3d(CUtensorMap* map, const void* base, const uint64_t dims[3
   return PKV_OK;
 }
 
+int encode_row_group_map(CUtensorMap* map, const void* base, uint64_t D, uint64_t rows,
+                         uint32_t box_rows) {
+  if (!encode_fn()) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled is not available");
+  // dimensions, innermost first: 64 elements of a half row, 8 rows of a
+  // group, the D / 64 halves of a row, the groups
+  cuuint64_t d[4] = {64, 8, D / 64, rows / 8};
+  cuuint64_t s[3] = {D * 2, 128, 8 * D * 2};
+  cuuint32_t b[4] = {64, 8, (cuuint32_t)(D / 64), box_rows / 8};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), d, s,
+                        b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(PKV_ECUDA, "cuTensorMapEncodeTiled (row groups) failed (%d)", (int)r);
+  return PKV_OK;
+}
+
 int encode_byte_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes,
                          uint64_t rows, uint32_t box_rows, bool swizzle128) {
   if (!encode_fn()) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled is not available");

@@ -33,6 +33,13 @@ int encode_tile_map_2d(CUtensorMap* map, const void* base, uint64_t inner_elems,
 int encode_tile_map_3d(CUtensorMap* map, const void* base, const uint64_t dims[3],
                        const uint64_t strides_bytes[2], const uint32_t box[3]);
 
+// A bf16 pool of `rows` rows of D elements (D = 64 or 128, rows a multiple
+// of 8) seen as 8-row groups: one box of `box_rows` rows (a multiple of 8)
+// lands in shared memory as [8-row group][64-column half][8 rows x 128 B],
+// 128-byte swizzled. The box is addressed by (0, 0, 0, first row / 8).
+int encode_row_group_map(CUtensorMap* map, const void* base, uint64_t D, uint64_t rows,
+                         uint32_t box_rows);
+
 // `rows` rows of `row_bytes` bytes (a multiple of 16, at most 128 when
 // swizzled), tiles of box_rows whole rows, 128-byte swizzled or plain.
 int encode_byte_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes,

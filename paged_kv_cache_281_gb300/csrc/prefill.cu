@@ -43,7 +43,9 @@ namespace {
 
 constexpr int kRows = 128;       // (query, head) rows per Q tile = TMEM lanes
 constexpr int kKeys = 64;        // keys per KV tile
-constexpr uint32_t kKVHalf = kKeys * 128;  // one 64-column half of a K or V tile
+// K and V tiles sit in shared memory as [8-row group][64-column half][8 rows
+// x 128 B] (128-byte swizzled), so that one TMA box brings a whole page (both
+// halves) and the tensor core still sees equal strides between 8-row groups
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows past 2^8
 constexpr int kWin = 256;            // block-table entries held in shared memory
 constexpr int kItemRing = 4;         // work-item indices handed from the producer to the others
@@ -56,7 +58,8 @@ struct PCfg {
   static constexpr int kThreads = 64 + 256 * NQ;  // producer, MMA, eight softmax warps per tile
   static constexpr uint32_t kQHalf = NQ * kRows * 128;  // one 64-column half of the Q tiles
   static constexpr int kHalves = D / 64;
-  static constexpr uint32_t kStage = kHalves * kKVHalf;
+  static constexpr uint32_t kGroup = kHalves * 1024;  // one 8-row group of a K or V tile
+  static constexpr uint32_t kStage = (kKeys / 8) * kGroup;
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kK = kQ + kHalves * kQHalf;
   static constexpr uint32_t kV = kK + NS * kStage;
@@ -416,20 +419,19 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
       const int npages = (it.kv_end + B - 1) / B;
       int win0 = 0;
       // Loads key or value tile t of this item into ring slot g: lane k issues
-      // box k (page k / halves, column half k % halves).
+      // the box of page k (all its rows and both column halves).
       auto issue = [&](const CUtensorMap* map, int t, uint32_t dst, uint32_t fbar) {
         const int p0 = t * ppt, np = min(ppt, npages - p0);
-        const bool mine = lane < np * C::kHalves;
-        const int pg = lane / C::kHalves, hh = lane % C::kHalves;
-        const int32_t blk = mine ? s_pages[p0 + pg - win0] : -1;
+        const bool mine = lane < np;
+        const int32_t blk = mine ? s_pages[p0 + lane - win0] : -1;
         const bool valid = mine && blk >= 0 && blk < a.num_blocks;
         const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
-        if (lane == 0) mbar_arrive_expect_tx(fbar, nvalid * B * 128u);
+        if (lane == 0) mbar_arrive_expect_tx(fbar, nvalid * B * C::kHalves * 128u);
         __syncwarp();
         if (mine && !valid) record_status(a.status, PKV_EDEVICE, blk, kKernelPrefill);
         if (valid)
-          tma_load_2d(dst + hh * kKVHalf + pg * B * 128, map, hh * 64,
-                      (blk * a.Hkv + it.kvh) * B, fbar);
+          tma_load_4d(dst + lane * (B / 8) * C::kGroup, map, 0, 0, 0,
+                      (blk * a.Hkv + it.kvh) * (B / 8), fbar);
       };
       // Q of this item once the previous item's score MMAs have read theirs
       if (n > 0) ok = wait_warp(C::kBarQE, (n - 1) & 1, 12);
@@ -482,8 +484,8 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
     // shared-memory descriptors of the first Q, K and V tiles; the others
     // differ only in the start address field (bytes / 16)
     const uint64_t dq = umma_desc_sw128(base + C::kQ, 16, 1024);
-    const uint64_t dk = umma_desc_sw128(base + C::kK, 16, 1024);
-    const uint64_t dv = umma_desc_sw128(base + C::kV, kKVHalf, 1024);
+    const uint64_t dk = umma_desc_sw128(base + C::kK, 16, C::kGroup);
+    const uint64_t dv = umma_desc_sw128(base + C::kV, 1024, C::kGroup);
     bool ok = true;
     int jg = 0;                   // K/V ring position
     int sg[NQ], oe[NQ];           // score-buffer uses and finished outputs per Q tile
@@ -509,7 +511,7 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
               const int b = (sg[t] + j) & 1;
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t koff = (kk >> 2) * kKVHalf + (kk & 3) * 32;
+                const uint32_t koff = (kk >> 2) * 1024 + (kk & 3) * 32;
                 const uint32_t qoff = t * kRows * 128 + (kk >> 2) * kQHalf + (kk & 3) * 32;
                 umma_bf16(tmem + t * 256 + b * kKeys, dq + (qoff >> 4), dks + (koff >> 4),
                           kIdescS, kk > 0 ? 1u : 0u);
@@ -535,8 +537,8 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
               for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch)
-                  *reinterpret_cast<uint4*>(vp + h * kKVHalf + r * 128 + ch * 16) =
-                      make_uint4(0u, 0u, 0u, 0u);
+                  *reinterpret_cast<uint4*>(vp + (r >> 3) * C::kGroup + h * 1024 +
+                                            (r & 7) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
             fence_proxy_async_smem();
           }
           __syncwarp();
@@ -555,7 +557,7 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
               const uint64_t dvs = dv + ((st * C::kStage) >> 4);
 #pragma unroll
               for (int kk = 0; kk < kKeys / 16; ++kk) {
-                const uint64_t vdesc = dvs + ((kk * 16 * 128) >> 4);
+                const uint64_t vdesc = dvs + ((kk * 2 * C::kGroup) >> 4);
                 umma_bf16_ts(o, p + kk * 8, vdesc, kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
                 umma_bf16_ts(o, p + 32 + kk * 8, vdesc, kIdescO, 1u);
               }
@@ -871,10 +873,8 @@ extern "C" int pkv_paged_attention_prefill(void* out, const void* q, const int32
     if (int rc = encode_tile_map_3d(&tq, q, dims, strides, box)) return rc;
   }
   const uint64_t rows = (uint64_t)num_blocks * Hkv * block_size;
-  if (int rc = encode_tile_map_2d(&tk, k_cache, D, rows, (uint64_t)D * 2, 64, block_size))
-    return rc;
-  if (int rc = encode_tile_map_2d(&tv, v_cache, D, rows, (uint64_t)D * 2, 64, block_size))
-    return rc;
+  if (int rc = encode_row_group_map(&tk, k_cache, D, rows, block_size)) return rc;
+  if (int rc = encode_row_group_map(&tv, v_cache, D, rows, block_size)) return rc;
 
   PrefillArgs a = {};
   a.out = static_cast<__nv_bfloat16*>(out);
