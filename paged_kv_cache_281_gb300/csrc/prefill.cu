@@ -418,21 +418,6 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
       const int32_t* bt = a.block_tables + (int64_t)it.s * a.max_blocks_per_seq;
       const int npages = (it.kv_end + B - 1) / B;
       int win0 = 0;
-      // Loads key or value tile t of this item into ring slot g: lane k issues
-      // the box of page k (all its rows and both column halves).
-      auto issue = [&](const CUtensorMap* map, int t, uint32_t dst, uint32_t fbar) {
-        const int p0 = t * ppt, np = min(ppt, npages - p0);
-        const bool mine = lane < np;
-        const int32_t blk = mine ? s_pages[p0 + lane - win0] : -1;
-        const bool valid = mine && blk >= 0 && blk < a.num_blocks;
-        const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
-        if (lane == 0) mbar_arrive_expect_tx(fbar, nvalid * B * C::kHalves * 128u);
-        __syncwarp();
-        if (mine && !valid) record_status(a.status, PKV_EDEVICE, blk, kKernelPrefill);
-        if (valid)
-          tma_load_4d(dst + lane * (B / 8) * C::kGroup, map, 0, 0, 0,
-                      (blk * a.Hkv + it.kvh) * (B / 8), fbar);
-      };
       // Q of this item once the previous item's score MMAs have read theirs
       if (n > 0) ok = wait_warp(C::kBarQE, (n - 1) & 1, 12);
       if (!ok) break;
@@ -448,29 +433,45 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
       __syncwarp();
       for (int i = lane; i < kWin && i < npages; i += 32) s_pages[i] = __ldg(bt + i);
       __syncwarp();
+      // Step j loads key tile j and value tile j - 1 (the order in which the
+      // tensor core needs them) in one pass of the warp: lane k < 8 issues
+      // the box of page k of the key tile, lane 8 + k that of the value tile
+      // (all rows of the page and both column halves in one box).
       for (int j = 0; ok && j <= it.nkt; ++j) {
-        if (j < it.nkt) {
-          if (min((j + 1) * ppt, npages) > win0 + kWin) {
-            // slide the window: tile j-1 (whose values are still to load) and on
-            win0 = (j - 1) * ppt;
-            __syncwarp();
-            for (int i = lane; i < kWin && win0 + i < npages; i += 32)
-              s_pages[i] = __ldg(bt + win0 + i);
-            __syncwarp();
-          }
-          const int g = jg + j, st = g % NS, u = g / NS;
-          if (g >= NS) ok = wait_warp(C::kBarKE + st, (u - 1) & 1, 1);
-          if (!ok) break;
-          issue(&tmap_k, j, base + C::kK + st * C::kStage, bar(C::kBarKF + st));
-          ++issued_k;
+        const bool do_k = j < it.nkt, do_v = j >= 1;
+        if (do_k && min((j + 1) * ppt, npages) > win0 + kWin) {
+          // slide the window: tile j-1 (whose values are still to load) and on
+          win0 = (j - 1) * ppt;
+          __syncwarp();
+          for (int i = lane; i < kWin && win0 + i < npages; i += 32)
+            s_pages[i] = __ldg(bt + win0 + i);
+          __syncwarp();
         }
-        if (j >= 1) {
-          const int g = jg + j - 1, st = g % NS, u = g / NS;
-          if (g >= NS) ok = wait_warp(C::kBarVE + st, (u - 1) & 1, 2);
-          if (!ok) break;
-          issue(&tmap_v, j - 1, base + C::kV + st * C::kStage, bar(C::kBarVF + st));
-          ++issued_v;
-        }
+        const int gk = jg + j, gv = jg + j - 1;
+        const int stk = gk % NS, stv = do_v ? gv % NS : 0;
+        if (do_k && gk >= NS) ok = wait_warp(C::kBarKE + stk, (gk / NS - 1) & 1, 1);
+        if (!ok) break;
+        if (do_v && gv >= NS) ok = wait_warp(C::kBarVE + stv, (gv / NS - 1) & 1, 2);
+        if (!ok) break;
+        const bool is_v = lane >= 8;
+        const int pl = lane & 7, p0 = (is_v ? j - 1 : j) * ppt;
+        const bool mine = lane < 16 && (is_v ? do_v : do_k) && pl < min(ppt, npages - p0);
+        const int32_t blk = mine ? s_pages[p0 + pl - win0] : -1;
+        const bool valid = mine && blk >= 0 && blk < a.num_blocks;
+        const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+        const uint32_t kf = bar(C::kBarKF + stk), vf = bar(C::kBarVF + stv);
+        const uint32_t page_bytes = B * C::kHalves * 128u;
+        if (lane == 0 && do_k) mbar_arrive_expect_tx(kf, __popc(vmask & 0xffu) * page_bytes);
+        if (lane == 8 && do_v) mbar_arrive_expect_tx(vf, __popc(vmask & 0xff00u) * page_bytes);
+        __syncwarp();
+        if (mine && !valid) record_status(a.status, PKV_EDEVICE, blk, kKernelPrefill);
+        if (valid)
+          tma_load_4d((is_v ? base + C::kV + stv * C::kStage : base + C::kK + stk * C::kStage) +
+                          pl * (B / 8) * C::kGroup,
+                      is_v ? &tmap_v : &tmap_k, 0, 0, 0, (blk * a.Hkv + it.kvh) * (B / 8),
+                      is_v ? vf : kf);
+        issued_k += do_k ? 1 : 0;
+        issued_v += do_v ? 1 : 0;
         __syncwarp();
       }
       jg += it.nkt;

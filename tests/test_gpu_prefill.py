@@ -155,11 +155,13 @@ def check_prefill_sampled(w, chunks, seqs, seed):
     return d, q_bits, cu
 
 
-def test_persistent_grid_long_chunks():
-    # 16 fresh 600-token prompts, 32/8 heads: ~2,500 items of one Q tile
+@pytest.mark.parametrize("D,B", [(128, 16), (128, 8), (64, 32)])
+def test_persistent_grid_long_chunks(D, B):
+    # 16 fresh 600-token prompts, 32/8 heads: ~2,500 items of one Q tile; a
+    # key tile holds 64 / B pages, one load each
     lens = [600] * 16
-    w = make_decode_workload("prefill_persistent_1", lens, Hq=32, Hkv=8, D=128, block_size=16,
-                             seed=3300)
+    w = make_decode_workload(f"prefill_persistent_1_D{D}_B{B}", lens, Hq=32, Hkv=8, D=D,
+                             block_size=B, seed=3300 + D + B)
     check_prefill_sampled(w, lens, [0, 5, 15], seed=21)
 
 
