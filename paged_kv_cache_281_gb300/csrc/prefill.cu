@@ -487,6 +487,16 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
     const uint64_t dq = umma_desc_sw128(base + C::kQ, 16, 1024);
     const uint64_t dk = umma_desc_sw128(base + C::kK, 16, C::kGroup);
     const uint64_t dv = umma_desc_sw128(base + C::kV, 1024, C::kGroup);
+    // A descriptor's start address (bytes / 16) sits in its low word and never
+    // carries into the high word (shared memory is below 2^18 bytes), so an
+    // offset is added to the low word alone
+    auto at = [](uint64_t d, uint32_t bytes) -> uint64_t {
+      uint64_t r;
+      asm("mov.b64 %0, {%1, %2};"
+          : "=l"(r)
+          : "r"((uint32_t)d + (bytes >> 4)), "r"((uint32_t)(d >> 32)));
+      return r;
+    };
     bool ok = true;
     int jg = 0;                   // K/V ring position
     int sg[NQ], oe[NQ];           // score-buffer uses and finished outputs per Q tile
@@ -505,7 +515,7 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
           if (!ok) break;
           tcgen05_after_sync();
           if (elect_one()) {
-            const uint64_t dks = dk + ((st * C::kStage) >> 4);
+            const uint32_t kst = st * C::kStage;
 #pragma unroll
             for (int t = 0; t < NQ; ++t) {
               if (j >= nkt_t(t)) continue;
@@ -514,8 +524,8 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t koff = (kk >> 2) * 1024 + (kk & 3) * 32;
                 const uint32_t qoff = t * kRows * 128 + (kk >> 2) * kQHalf + (kk & 3) * 32;
-                umma_bf16(tmem + t * 256 + b * kKeys, dq + (qoff >> 4), dks + (koff >> 4),
-                          kIdescS, kk > 0 ? 1u : 0u);
+                umma_bf16(tmem + t * 256 + b * kKeys, at(dq, qoff), at(dk, kst + koff), kIdescS,
+                          kk > 0 ? 1u : 0u);
               }
               umma_commit(bar(C::kBarSF + 2 * t + b));
             }
@@ -555,10 +565,10 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
             if (elect_one()) {
               const uint32_t p = tmem + t * 256 + b * kKeys;
               const uint32_t o = tmem + t * 256 + 128;
-              const uint64_t dvs = dv + ((st * C::kStage) >> 4);
+              const uint32_t vst = st * C::kStage;
 #pragma unroll
               for (int kk = 0; kk < kKeys / 16; ++kk) {
-                const uint64_t vdesc = dvs + ((kk * 2 * C::kGroup) >> 4);
+                const uint64_t vdesc = at(dv, vst + kk * 2 * C::kGroup);
                 umma_bf16_ts(o, p + kk * 8, vdesc, kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
                 umma_bf16_ts(o, p + 32 + kk * 8, vdesc, kIdescO, 1u);
               }
