@@ -32,6 +32,9 @@ struct AppendArgs {
 
 // One thread per 16-byte vector of the new rows; grid-stride over T*Hkv*D/8.
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendArgs a) {
+  // a plan launched after this kernel may start launching; it waits for this
+  // kernel's writes before it reads anything
+  grid_dep_launch();
   const int64_t vec_per_tok = (int64_t)a.Hkv * a.vec_per_row;
   const int64_t total = (int64_t)a.T * vec_per_tok;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -149,6 +152,7 @@ __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
 
 template <int D>
 __global__ void __launch_bounds__(256) kv_append_fp8_kernel(const AppendFp8Args a) {
+  grid_dep_launch();  // as in kv_append_kernel
   constexpr int E = D / 32;  // elements per lane: 4 (D=128) or 2 (D=64)
   const int lane = threadIdx.x & 31;
   const int64_t rows = (int64_t)a.T * a.Hkv * 2;

@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = a.partition_tiles * kTileTokens;
   grid_dep_launch();  // the decode kernel may start its set-up now
+  grid_dep_wait();    // launched early: whatever ran before (the append) is complete
   if (tid == 0) s_base = 0;
   __syncthreads();
   for (int pass = 0; pass < 2; ++pass) {
@@ -956,6 +957,7 @@ __global__ void __launch_bounds__(1024) decode_group_plan_kernel(DecodeArgs a) {
   const int P = a.partition_tiles * kTileTokens;
   const int M = a.members_per_item;
   grid_dep_launch();
+  grid_dep_wait();  // launched early: whatever ran before is complete
   if (tid == 0) s_n = 0;
   for (int s = tid; s < a.S; s += 1024) a.seq_shared[s] = 0;
   __syncthreads();
@@ -1311,6 +1313,24 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 }
 
+// Launches a one-CTA plan kernel that may start while the previous kernel in
+// the stream ends (it waits for it before touching memory).
+template <typename Args>
+int launch_plan(void (*kernel)(Args), const Args& a, cudaStream_t stream, const char* what) {
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1024);
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, a);
+  if (err != cudaSuccess) return cuda_fail(err, what);
+  return PKV_OK;
+}
+
 template <int D, int G>
 int launch_decode_group(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                         const DeviceInfo& dev, cudaStream_t stream) {
@@ -1330,7 +1350,7 @@ int launch_decode_group(const CUtensorMap& tk, const CUtensorMap& tv, const Deco
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  decode_group_plan_kernel<<<1, 1024, 0, stream>>>(a);
+  if (int rc = launch_plan(decode_group_plan_kernel, a, stream, "decode plan launch")) return rc;
   if (int rc = check_launch("shared decode plan")) return rc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(dev.sm_count * blocks_per_sm));
@@ -1379,7 +1399,7 @@ int launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  decode_plan_kernel<<<1, 1024, 0, stream>>>(a);
+  if (int rc = launch_plan(decode_plan_kernel, a, stream, "decode plan launch")) return rc;
   if (int rc = check_launch("decode plan")) return rc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(dev.sm_count * blocks_per_sm));
@@ -1420,7 +1440,7 @@ int launch_decode_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const Decode
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  decode_plan_kernel<<<1, 1024, 0, stream>>>(a);
+  if (int rc = launch_plan(decode_plan_kernel, a, stream, "decode plan launch")) return rc;
   if (int rc = check_launch("decode plan")) return rc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(dev.sm_count * blocks_per_sm));

@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillArgs a)
   __shared__ int32_t s_base, s_chunk;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   grid_dep_launch();  // the prefill kernel may start its set-up now
+  grid_dep_wait();    // launched early: whatever ran before (the append) is complete
   if (tid == 0) s_base = 0;
   __syncthreads();
   for (int c0 = 0; c0 < a.S; c0 += 1024) {
@@ -790,12 +791,21 @@ int launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
     return check_launch("prefill");
   }
   a.direct = 0;
-  prefill_plan_kernel<<<1, 1024, 0, stream>>>(a);
-  if (int rc = check_launch("prefill plan")) return rc;
-  // persistent: every resident slot; its set-up overlaps the plan
+  // the plan may start launching while the previous kernel ends (it waits
+  // for it first); the persistent grid's set-up overlaps the plan
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  {
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3(1);
+    pc.blockDim = dim3(1024);
+    pc.stream = stream;
+    pc.attrs = pdl;
+    pc.numAttrs = 1;
+    cudaError_t perr = cudaLaunchKernelEx(&pc, prefill_plan_kernel, a);
+    if (perr != cudaSuccess) return cuda_fail(perr, "prefill plan launch");
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)slots);
   cfg.blockDim = dim3(C::kThreads);
