@@ -349,7 +349,7 @@ def run_trace(args):
     # for the whole trace (timed as the scheduler cost), uploaded to the
     # device; then the GPU side runs back to back, so the events time kernels
     # rather than the host's launch latency.
-    dt = DeviceTrace(cfg)
+    dt = DeviceTrace(cfg, partition_size=args.partition_size)
     host_s, ups, stats = 0.0, [], []
     for itr in its:
         h0 = time.perf_counter()
@@ -369,7 +369,8 @@ def run_trace(args):
     torch.cuda.synchronize()
 
     def one_pass(timed):
-        run = DeviceTrace(cfg)                # fresh pools; the metadata above drives it
+        # fresh pools; the metadata above drives it
+        run = DeviceTrace(cfg, partition_size=args.partition_size)
         evs = []
         t_all = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
         t_all[0].record(stream)
@@ -409,6 +410,7 @@ def run_trace(args):
         "config": {"workload": "trace: 200 iterations, Poisson(8) arrivals, prompts U[32,1024] "
                                "in chunks <= 512, outputs Geometric(1/256) <= 1536, <= 256 "
                                "running, 64/8 heads, D=128, B=16, 40,960-block pool",
+                   "decode_partition_size": args.partition_size or 1024,
                    "prefill_tokens": int(sum(x[1] for x in stats)),
                    "decode_tokens": int(sum(x[2] for x in stats)),
                    "l2": "decode reads ~0.4 GB of K/V per iteration (> 129 MB L2)"},
@@ -1019,21 +1021,23 @@ def run_shared_prefix(args):
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
     gs, gm, gsh = t(start), t(members), t(sh)
     out = torch.empty(w.S, w.Hq, w.D, dtype=torch.bfloat16, device="cuda")
-    ws = torch.empty(max(pkv.pkv_decode_workspace_bytes(w.S, w.Hq, w.D, d.max_context_len),
+    P = args.partition_size
+    ws = torch.empty(max(pkv.pkv_decode_workspace_bytes(w.S, w.Hq, w.D, d.max_context_len, P),
                          pkv.pkv_decode_shared_workspace_bytes(w.S, w.Hq, w.D,
-                                                               d.max_context_len)),
+                                                               d.max_context_len, P)),
                      dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
     def plain():
         pkv.pkv_paged_attention_decode(out, d.q, d.k_cache, d.v_cache, d.block_tables,
                                        d.context_lens, d.max_context_len, w.scale, ws,
-                                       status=d.status, stream=stream)
+                                       partition_size=P, status=d.status, stream=stream)
 
     def grouped():
         pkv.pkv_paged_attention_decode_shared(out, d.q, d.k_cache, d.v_cache, d.block_tables,
                                               d.context_lens, d.max_context_len, gs, gm, gsh,
-                                              w.scale, ws, status=d.status, stream=stream)
+                                              w.scale, ws, partition_size=P, status=d.status,
+                                              stream=stream)
 
     def timed(fn):
         for _ in range(max(3, args.warmup)):
@@ -1078,7 +1082,7 @@ def run_shared_prefix(args):
         "data": "synthetic",
         "config": {"workload": "64 prompts x 4 samples, shared %d-token prefix (forked "
                                "blocks), tails U[0,512], 32/8 heads, D=128, B=16" % w.prefix_len,
-                   "variant": args.variant,
+                   "variant": args.variant, "partition_size": P or 1024,
                    "logical_kv_bytes": logical, "unique_kv_bytes": unique,
                    "l2": "%.2f GB of unique K/V (> 129 MB L2)" % (unique / 1e9)},
         "ordinary_ms": plain_ms, "sharing_aware_ms": grouped_ms,

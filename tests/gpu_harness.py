@@ -233,9 +233,10 @@ class DeviceTrace:
     chunks and decode for the running sequences, and finished requests free
     their blocks."""
 
-    def __init__(self, cfg, device="cuda"):
+    def __init__(self, cfg, device="cuda", partition_size=0):
         self.cfg = cfg
         self.device = device
+        self.partition_size = partition_size  # decode split-K partition (0: the default)
         self.alloc = pkv.BlockAllocator(cfg.num_blocks, cfg.block_size)
         self.k_cache, self.v_cache = poisoned_pools(cfg.num_blocks, cfg.Hkv, cfg.block_size,
                                                     cfg.D, device)
@@ -244,7 +245,7 @@ class DeviceTrace:
         self.max_blocks = -(-(cfg.prompt_max + cfg.out_cap) // cfg.block_size)
         self.scale = 1.0 / np.sqrt(cfg.D)
         self.ws = torch.empty(pkv.pkv_decode_workspace_bytes(
-            cfg.max_running, cfg.Hq, cfg.D, cfg.prompt_max + cfg.out_cap),
+            cfg.max_running, cfg.Hq, cfg.D, cfg.prompt_max + cfg.out_cap, partition_size),
             dtype=torch.uint8, device=device)
         # prefill work items: at most every running request's whole chunk
         self.pws = torch.empty(pkv.pkv_prefill_workspace_bytes(
@@ -312,6 +313,7 @@ class DeviceTrace:
             dec_out = torch.empty(n, cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
             pkv.pkv_paged_attention_decode(dec_out, up["q"][n_pre:], self.k_cache, self.v_cache,
                                            tables, lens, max_ctx, self.scale, self.ws,
+                                           partition_size=self.partition_size,
                                            status=self.status, stream=stream)
         rec(3)
         return pre_out, dec_out
