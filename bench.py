@@ -45,7 +45,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM read + write bytes of one paged_decode_kernel<128,4> launch on this
 # workload, taken with ncu (dram__bytes_read.sum + dram__bytes_write.sum);
 # to be set to None whenever the kernel changes.
-DECODE_TRAFFIC_BYTES = 1_403_409_920
+DECODE_TRAFFIC_BYTES = 1_403_613_440
 
 
 def parse_args():

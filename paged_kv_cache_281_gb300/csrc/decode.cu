@@ -44,7 +44,8 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kTileTokens = 16;
 constexpr int kDefaultPartition = 1024;
 
-template <int D, int Stages = (D == 128 ? 3 : 6)>
+// two stages of 8 KB per warp at D = 128: three CTAs (12 warps) per SM
+template <int D, int Stages = (D == 128 ? 2 : 4)>
 struct Cfg {
   static constexpr int kHalves = D / 64;            // 128-byte swizzled column halves
   static constexpr int kHalfBytes = kTileTokens * 128;
@@ -203,12 +204,14 @@ __device__ __forceinline__ void issue_tile_rows(const CUtensorMap* tk, const CUt
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
-  using C = Cfg<D>;
+  using C = Cfg<D>;  // three CTAs per SM (168 registers)
   constexpr int KS = D / 16;  // k-steps of the score MMA
   constexpr int NT = D / 8;   // n-tiles of the output MMA
+  static_assert(256 + kWarps * G * D * 4 <= kWarps * C::kRingBytes,
+                "the merge buffer reuses the rings");
   extern __shared__ uint8_t dsm[];
   __shared__ __align__(8) uint64_t bars[kWarps][C::kStages];
   __shared__ int32_t s_next;
@@ -1026,8 +1029,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 3)
     paged_decode_group_kernel(const __grid_constant__ CUtensorMap tmap_k,
                               const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
-  // three CTAs per SM: 2 stages of 8 KB per warp at D = 128 (168 registers)
-  using C = Cfg<D, D == 128 ? 2 : 4>;
+  using C = Cfg<D>;  // three CTAs per SM (168 registers)
   constexpr int KS = D / 16;
   constexpr int NT = D / 8;
   constexpr int M = 16 / G;  // members per item
@@ -1334,7 +1336,7 @@ int launch_plan(void (*kernel)(Args), const Args& a, cudaStream_t stream, const 
 template <int D, int G>
 int launch_decode_group(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                         const DeviceInfo& dev, cudaStream_t stream) {
-  using C = Cfg<D, D == 128 ? 2 : 4>;
+  using C = Cfg<D>;
   static std::once_flag once;
   static int blocks_per_sm = 0;
   static cudaError_t attr_err = cudaSuccess;
