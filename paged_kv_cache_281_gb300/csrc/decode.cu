@@ -10,16 +10,18 @@
 //  * Split-K. A sequence's tokens are cut into partitions of a fixed number of
 //    16-token tiles. A work item is (sequence, kv head, partition); a plan
 //    kernel lists the items (full partitions first, partial ones last) and a
-//    persistent grid of 2 CTAs per SM pulls them from an atomic ticket. Items
+//    persistent grid of 3 CTAs per SM pulls them from an atomic ticket. Items
 //    of multi-partition sequences write an unnormalised partial state
 //    (m, l, o) that a combine kernel merges with the online-softmax rule; a
 //    sequence with one partition is normalised in place.
 //  * Data movement. Each of the CTA's 4 warps owns every 4th tile of the item
-//    and a private 3-stage ring in shared memory. The warp's lanes look up the
+//    and a private 2-stage ring in shared memory. The warp's lanes look up the
 //    block-table entries of its tiles in parallel; one lane issues TMA tile
 //    loads (two 64-column halves per tensor, 128-byte swizzle) for whole
 //    pages, signalling an mbarrier with the byte count; the warp waits on it
-//    with a time limit.
+//    with a time limit. The plan is launched early after the previous kernel
+//    (programmatic dependent launch) and waits for it before reading; the
+//    decode and combine kernels follow the same way.
 //  * Arithmetic. The G query heads that share a kv head form the rows of a
 //    16-row MMA operand (rows >= G are zero). Scores S = Q K^T and the update
 //    O += P V run as m16n8k16 bf16 MMAs with fp32 accumulators held in
