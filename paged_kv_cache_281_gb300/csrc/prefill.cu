@@ -8,27 +8,37 @@
 // through the block table ("Batching, Scheduling, and Paging", section
 // PagedAttention).
 //
-// How (GB300 design). One CTA owns a tile of 128 rows, each row a (query,
-// head) pair: 128/G consecutive queries times the G query heads that share one
-// kv head, so every key/value tile loaded serves all of them. Its six warps
-// specialise and run as a pipeline over 64-key tiles:
-//  * warp 0 (one lane) loads Q once by a 3-D TMA box per 64-column half and
-//    streams K and V tiles (whole pages located through the block table, one
-//    TMA box per page and half, 128-byte swizzled) into rings of NS stages;
-//  * warp 1 (one lane issues) runs the tensor core: S_j = Q K_j^T into one of
-//    two TMEM score buffers, then O += P_{j-1} V_{j-1}, so the scores of the
-//    next tile are computed while the softmax works on the current one; the
-//    warp also zeroes the value rows past the last visible key before the
-//    final product (they may hold stale or poisoned bytes, and 0 * NaN is NaN);
-//  * warps 2-5 own one TMEM lane (= row) per thread: they read the 64 scores,
-//    apply the causal limit, keep a running sum against a reference maximum
-//    (base 2), and write the probabilities back into the same TMEM columns as
-//    two bf16 parts P_hi + P_lo (~fp32 precision for the product), which the
-//    P V MMA reads as its A operand straight from tensor memory. O is
-//    rescaled (in TMEM) only when a row's maximum grows by more than 2^8, so
-//    the stored probabilities stay below 256 and the rescale is rare; the
-//    final division by the row sum makes the result independent of the
-//    reference chosen.
+// How (GB300 design). A Q tile is 128 rows, each row a (query, head) pair:
+// 128/G consecutive queries times the G query heads that share one kv head,
+// so every key/value tile loaded serves all of them. A work item is (sequence,
+// query group, kv head) with NQ = 1 or 2 Q tiles; large launches run a plan
+// kernel and a persistent grid that takes items from an atomic ticket (the
+// producer posts them to the other warps through a small ring), small ones
+// one CTA per item. The warps specialise and run as a pipeline over 64-key
+// tiles:
+//  * warp 0 (producer) loads Q by 3-D TMA boxes and streams K and V tiles
+//    into rings of NS stages: page numbers come from a block-table window in
+//    shared memory, and in one pass lanes 0-7 issue the boxes of key tile j
+//    and lanes 8-15 those of value tile j - 1, one 4-D box per page holding
+//    all its rows and both 64-column halves (tiles sit in shared memory as
+//    [8-row group][half][8 rows x 128 B], 128-byte swizzled);
+//  * warp 1 runs the tensor core (issue under elect.sync): S_j = Q K_j^T into
+//    one of two TMEM score buffers per Q tile, then O += P_{j-1} V_{j-1}, so
+//    the scores of the next tile are computed while the softmax works on the
+//    current one; it also zeroes the value rows past the last visible key
+//    before the product (they may hold stale or poisoned bytes, and 0 * NaN
+//    is NaN);
+//  * eight softmax warps per Q tile share each TMEM lane (= row) between two
+//    threads, one per key half: they read the scores, apply the causal
+//    limit, exchange the row maxima, keep a running sum against a reference
+//    maximum (base 2, packed f32x2 arithmetic), and write the probabilities
+//    back into the same TMEM columns as two bf16 parts P_hi + P_lo (~fp32
+//    precision for the product), which the P V MMA reads as its A operand
+//    straight from tensor memory. O is rescaled (in TMEM) only when a row's
+//    maximum grows by more than 2^8, so the stored probabilities stay below
+//    256 and the rescale is rare; the final division by the row sum makes
+//    the result independent of the reference chosen. The same warps write
+//    the item's output rows.
 // Every mbarrier wait has a time limit and gives up early once another warp
 // has given up; the CTA then records PKV_ETIMEOUT, waits (with a limit) for its
 // own copies and MMAs, frees its tensor memory and returns.
