@@ -11,7 +11,7 @@
 // How (GB300 design). A Q tile is 128 rows, each row a (query, head) pair:
 // 128/G consecutive queries times the G query heads that share one kv head,
 // so every key/value tile loaded serves all of them. A work item is (sequence,
-// query group, kv head) with NQ = 1 or 2 Q tiles; large launches run a plan
+// query group, kv head) with NQ Q tiles (one in the launcher); large launches run a plan
 // kernel and a persistent grid that takes items from an atomic ticket (the
 // producer posts them to the other warps through a small ring), small ones
 // one CTA per item. The warps specialise and run as a pipeline over 64-key
@@ -62,7 +62,8 @@ constexpr int kItemRing = 4;         // work-item indices handed from the produc
 
 // NQ Q tiles per CTA share every K/V tile: two (one CTA per SM, all 512 TMEM
 // columns) halve the K/V traffic per row; one (two CTAs per SM) lets a CTA's
-// start and end overlap the other's work, which pays for short chunks.
+// start and end overlap the other's work. The launcher uses one (measured
+// faster); two remain a compile-time variant.
 template <int D, int NS, int NQ>
 struct PCfg {
   static constexpr int kThreads = 64 + 256 * NQ;  // producer, MMA, eight softmax warps per tile
@@ -889,13 +890,12 @@ extern "C" int pkv_paged_attention_prefill(void* out, const void* q, const int32
               "prefill: bf16 arrays must be 16-byte aligned");
   const DeviceInfo* dev = nullptr;
   if (int rc = current_device_info(&dev)) return rc;
-  // Two Q tiles per CTA halve the key/value reads per query row, which pays
-  // when chunks are short next to the contexts they attend (chunks after a
-  // long cached prefix); otherwise one tile per CTA and two CTAs per SM, whose
-  // starts and ends overlap, are faster (measured on GB300).
-  const int64_t mean_chunk = ((int64_t)total_q + S - 1) / S;
-  const int NQ = (max_q_len * G > kRows && max_context_len >= 4 * mean_chunk) ? 2 : 1;
-
+  // One Q tile per CTA and two CTAs per SM, whose starts and ends overlap:
+  // measured faster on GB300 than two Q tiles per CTA (which halve the
+  // key/value reads per row) for fresh prompts and for short chunks after long
+  // cached prefixes alike, since the producer loads a step's keys and values
+  // in one pass. The kernel keeps NQ = 2 as a compile-time variant.
+  constexpr int NQ = 1;
   CUtensorMap tq, tk, tv;
   {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)total_q};
@@ -931,10 +931,8 @@ extern "C" int pkv_paged_attention_prefill(void* out, const void* q, const int32
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc = PKV_OK;
-#define PKV_PREFILL_CASE(DD, GG)                                                   \
-  if (D == DD && G == GG)                                                          \
-    rc = NQ == 2 ? launch_prefill<DD, GG, 2>(tq, tk, tv, a, *dev, total_q, max_q_len, st) \
-                 : launch_prefill<DD, GG, 1>(tq, tk, tv, a, *dev, total_q, max_q_len, st);
+#define PKV_PREFILL_CASE(DD, GG) \
+  if (D == DD && G == GG) rc = launch_prefill<DD, GG, NQ>(tq, tk, tv, a, *dev, total_q, max_q_len, st);
   PKV_PREFILL_CASE(64, 1)
   PKV_PREFILL_CASE(64, 2)
   PKV_PREFILL_CASE(64, 4)

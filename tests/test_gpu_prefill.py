@@ -166,7 +166,7 @@ def test_persistent_grid_long_chunks(D, B):
 
 
 def test_persistent_grid_short_chunks_after_long_prefixes():
-    # 64 chunks of 40 tokens after ~2,000 cached tokens, 64/8 heads: two Q tiles
+    # 64 chunks of 40 tokens after ~2,000 cached tokens, 64/8 heads
     lens = [2000 + 7 * i for i in range(64)]
     w = make_decode_workload("prefill_persistent_2", lens, Hq=64, Hkv=8, D=128, block_size=16,
                              seed=3301)
