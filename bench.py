@@ -11,12 +11,18 @@ clipped to [16, 8192], blocks placed by a seeded permutation of a pool with
 ``value`` is the KV bytes the decode must read per step (each sequence's keys
 and values once) divided by the device time of a step; the line also reports
 attention tokens/s per layer (decode queries per second), the decode call's
-share of the HBM roofline, an end-to-end figure through the C ABI with host
-buffers, and the fp64 CPU oracle's throughput on a bounded sample.
+share of the HBM roofline, an end-to-end figure through the C ABI from pinned
+host memory, and the fp64 CPU oracle's throughput on the whole batch (one
+thread, and one process per host core).
 
 ``--impl reference`` times the CPU oracle instead (the only reference
-implementation this method has): each step is the oracle's decode over a
-bounded sample of the same workload.
+implementation this method has): each step is the oracle's decode of a
+seeded sample of the same workload's sequences.
+
+``--workload`` selects the other lines (MHA and tiny decode batches, FP8
+pages, the shared-prefix batch, fresh-prompt prefill, prefix caching, swap,
+and the continuous-batching trace with or without preemption); each prints
+its own JSON line.
 """
 
 from __future__ import annotations
