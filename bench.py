@@ -1220,7 +1220,8 @@ def main():
     }
     if e2e is not None:
         line["e2e"] = e2e
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the oracle is timed once, on the single-GPU run only
         line["cpu_baseline"] = cpu_baseline(args.workload)
     if rank == 0:
         print(json.dumps(line), flush=True)
