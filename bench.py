@@ -1193,7 +1193,15 @@ def main():
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
 
-    e2e = None if args.no_e2e else e2e_measure(w, d, args, pkv, torch)
+    e2e = None
+    if not args.no_e2e:
+        barrier()
+        e2e = e2e_measure(w, d, args, pkv, torch)
+        if world > 1:
+            # whole job: every rank's bytes over the slowest rank's step time
+            ms_e2e = max_over_ranks(e2e["ms_per_step"])
+            e2e.update(ms_per_step=ms_e2e,
+                       value=world * w.kv_bytes() / (ms_e2e * 1e-3) / 1e9)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
