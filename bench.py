@@ -1139,7 +1139,7 @@ def main():
         return run_prefill(args)
     import torch
     import paged_kv_cache_281_gb300 as pkv
-    from tests.gpu_harness import decode_step, setup_decode, to_dev_bf16
+    from tests.gpu_harness import decode_step, setup_decode
 
     rank, world, local = dist_info()
     torch.cuda.set_device(local)
@@ -1149,8 +1149,6 @@ def main():
     w = workload_for_rank(rank, args.workload)
     d = setup_decode(w, partition_size=args.partition_size, append_last=False)
     stream = torch.cuda.current_stream()
-    parts = pkv.pkv_decode_workspace_bytes(1, 1, w.D, w.max_context_len, args.partition_size)
-    del parts
     P = args.partition_size or 1024
     launches_per_step = 1 + 2 + (1 if math.ceil(w.max_context_len / P) > 1 else 0)
 
