@@ -29,7 +29,6 @@ import struct
 import numpy as np
 import pytest
 
-import oracle
 from oracle import attention, cache, fp8, paging
 from tests.oracle_side import build_decode_state, build_shared_prefix_state, empty_pools
 from workloads import config1, config4, make_decode_workload, normal_bf16

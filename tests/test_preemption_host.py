@@ -8,7 +8,6 @@ decision (swap lists, slots, completions) must be identical.
 
 from __future__ import annotations
 
-import numpy as np
 import pytest
 
 import paged_kv_cache_281_gb300 as pkv
