@@ -225,7 +225,7 @@ def cpu_baseline(name: str = "llama3_8b_gqa"):
 
 
 def _oracle_state(name: str, pick=None, seed_offset: int = 0):
-    from tests.oracle_side import build_decode_state
+    from oracle.harness import build_decode_state
     from workloads import make_decode_workload, SEED_BASE
     w = workload_for_rank(0, name)
     if pick is not None:
@@ -289,7 +289,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     from oracle import attention
-    from tests.oracle_side import build_decode_state
+    from oracle.harness import build_decode_state
     from workloads import config3_lengths, generator, make_decode_workload, pool_blocks, SEED_BASE
     lens = config3_lengths()
     # a seeded pool of 32 of the 256 sequences, built once; each step decodes a
@@ -344,7 +344,7 @@ def run_trace(args):
     GPU time, per-kernel times and rooflines, and the host scheduling time."""
     import torch
     import paged_kv_cache_281_gb300 as pkv
-    from tests.gpu_harness import DeviceTrace
+    from workloads.device import DeviceTrace
     from workloads import TraceConfig, trace_iterations
 
     rank, world, local = dist_info()
@@ -456,8 +456,8 @@ def run_trace_preempt(args):
     parity of the same path is checked at a smaller size by the tests)."""
     import torch
     import paged_kv_cache_281_gb300 as pkv
-    from tests.gpu_harness import poisoned_pools
-    from tests.preemption import LibraryAllocator, PreemptingScheduler
+    from workloads.device import poisoned_pools
+    from workloads.schedule import LibraryAllocator, PreemptingScheduler
     from workloads import TraceConfig
 
     rank, world, local = dist_info()
@@ -605,7 +605,7 @@ def run_swap(args):
     the same bytes as one contiguous buffer, each direction."""
     import torch
     import paged_kv_cache_281_gb300 as pkv
-    from tests.gpu_harness import setup_decode
+    from workloads.device import setup_decode
 
     rank, world, local = dist_info()
     torch.cuda.set_device(local)
@@ -708,7 +708,7 @@ def run_prefix_cache(args):
     served per second of GPU time (kv_append + prefill) both ways."""
     import torch
     import paged_kv_cache_281_gb300 as pkv
-    from tests.gpu_harness import poisoned_pools
+    from workloads.device import poisoned_pools
 
     rank, world, local = dist_info()
     torch.cuda.set_device(local)
@@ -833,7 +833,7 @@ def run_prefill(args):
     others are reported beside it."""
     import torch
     import paged_kv_cache_281_gb300 as pkv
-    from tests.gpu_harness import poisoned_pools
+    from workloads.device import poisoned_pools
 
     rank, world, local = dist_info()
     torch.cuda.set_device(local)
@@ -920,7 +920,7 @@ def run_fp8(args):
     (codes and scales) per second and decode tokens per second."""
     import torch
     import paged_kv_cache_281_gb300 as pkv
-    from tests.gpu_harness import to_dev_bf16
+    from workloads.device import to_dev_bf16
 
     rank, world, local = dist_info()
     torch.cuda.set_device(local)
@@ -1020,7 +1020,7 @@ def run_shared_prefix(args):
     (per-sample) and on the unique (each page once) byte counts."""
     import torch
     import paged_kv_cache_281_gb300 as pkv
-    from tests.gpu_harness import setup_shared_prefix, shared_groups
+    from workloads.device import setup_shared_prefix, shared_groups
     from workloads import config4
 
     rank, world, local = dist_info()
@@ -1139,7 +1139,7 @@ def main():
         return run_prefill(args)
     import torch
     import paged_kv_cache_281_gb300 as pkv
-    from tests.gpu_harness import decode_step, setup_decode
+    from workloads.device import decode_step, setup_decode
 
     rank, world, local = dist_info()
     torch.cuda.set_device(local)

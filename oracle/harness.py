@@ -1,7 +1,9 @@
 """Builds the oracle's view of a workload: its own allocator, pools and outputs.
 
-Test infrastructure: everything here runs the CPU oracle on the seeded
-workload inputs; nothing reads a value produced by the library.
+TEST INFRASTRUCTURE ONLY, like the rest of this package: everything here
+runs the CPU oracle on the seeded workload inputs (``workloads``), and
+nothing reads a value produced by the library. The tests, the smoke check
+and the benchmark's CPU-baseline leg use it.
 """
 
 from __future__ import annotations
@@ -12,6 +14,7 @@ import numpy as np
 
 from oracle import attention, cache, paging
 from workloads import BF16_NAN
+from workloads.schedule import OutOfBlocks, iteration_inputs
 
 
 @dataclass
@@ -166,3 +169,95 @@ class OracleTrace:
     def finish(self, itr):
         for rid in itr.finished:
             self.alloc.free_seq(self.sid.pop(rid))
+
+
+# ---------------------------------------------------------------- preemption
+
+
+class OracleAllocator:
+    """Adapter over oracle.paging.BlockAllocator."""
+
+    def __init__(self, num_blocks, block_size):
+        self.paging = paging
+        self.a = paging.BlockAllocator(num_blocks, block_size)
+
+    def create(self):
+        return self.a.create()
+
+    def append(self, sid, n):
+        try:
+            slots, pairs = self.a.append_slots(sid, n)
+        except self.paging.OutOfBlocks as e:
+            raise OutOfBlocks(str(e)) from None
+        assert not pairs
+        return slots
+
+    def free(self, sid):
+        self.a.free_seq(sid)
+
+    def create_cached(self, tokens):
+        return self.a.create_cached(tokens)
+
+    def append_tokens(self, sid, tokens):
+        try:
+            slots, pairs = self.a.append_tokens(sid, tokens)
+        except self.paging.OutOfBlocks as e:
+            raise OutOfBlocks(str(e)) from None
+        assert not pairs
+        return slots
+
+    def num_cached(self):
+        return self.a.num_cached()
+
+    def swap_out(self, sid):
+        return self.a.swap_out(sid)
+
+    def swap_in(self, sid):
+        try:
+            return self.a.swap_in(sid)
+        except self.paging.OutOfBlocks as e:
+            raise OutOfBlocks(str(e)) from None
+
+    def table(self, sid):
+        return self.a.block_table(sid)
+
+    def num_free(self):
+        return self.a.num_free()
+
+
+class OracleRunner:
+    """Replays the same events with the CPU oracle."""
+
+    def __init__(self, cfg, num_blocks):
+        self.cfg = cfg
+        self.k_cache, self.v_cache = empty_pools(num_blocks, cfg.Hkv, cfg.block_size, cfg.D)
+        self.saved = {}
+        self.scale = 1.0 / np.sqrt(cfg.D)
+
+    def run(self, ev, values):
+        cfg = self.cfg
+        shape = (cfg.Hkv, cfg.block_size, cfg.D)
+        for kind, rid, blocks in ev.ops:
+            if kind == "swap_out":
+                kb = np.empty((len(blocks),) + shape, np.uint16)
+                vb = np.empty_like(kb)
+                cache.swap_blocks(self.k_cache, self.v_cache, blocks, kb, vb, 0)
+                self.saved[rid] = (kb, vb)
+            else:
+                kb, vb = self.saved.pop(rid)
+                cache.swap_blocks(self.k_cache, self.v_cache, blocks, kb, vb, 1)
+        pre, dec, q, k, v, slots, meta = iteration_inputs(cfg, ev, values)
+        cache.append(self.k_cache, self.v_cache, k, v, slots, cfg.block_size)
+        return pre, dec, q, meta
+
+    def prefill(self, ev, pre, q, meta, i):
+        tables, lens = meta["prefill"]
+        a, b = int(meta["cu"][i]), int(meta["cu"][i + 1])
+        return attention.prefill(q[a:b], np.array([0, b - a]), [int(lens[i])], self.k_cache,
+                                 self.v_cache, [tables[i]], self.cfg.block_size, self.scale)
+
+    def decode(self, ev, q, meta, i):
+        tables, lens = meta["decode"]
+        n_pre = int(meta["cu"][-1])
+        return attention.decode(q[n_pre + i:n_pre + i + 1], self.k_cache, self.v_cache,
+                                [tables[i]], [int(lens[i])], self.cfg.block_size, self.scale)[0]

@@ -9,7 +9,8 @@ With caching, a request starts from the registered blocks of the prompt's
 full blocks and prefills only the rest; without, it prefills everything.
 The K/V (and query) values of a position inside the system prompt depend only
 on the position, so a cached block holds exactly what the request would have
-computed. Test infrastructure; the executors are those of ``tests.preemption``.
+computed. Test infrastructure; the executors are
+``workloads.device.GpuRunner`` and ``oracle.harness.OracleRunner``.
 """
 
 from __future__ import annotations
@@ -18,7 +19,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-from tests.preemption import Event
+from workloads.schedule import Event
 from workloads import generator, normal_bf16_from
 
 

@@ -14,8 +14,8 @@ import torch
 
 import paged_kv_cache_281_gb300 as pkv
 from oracle import cache
-from tests.gpu_harness import bf16_bits, poisoned_pools, to_dev_bf16
-from tests.oracle_side import empty_pools
+from workloads.device import bf16_bits, poisoned_pools, to_dev_bf16
+from oracle.harness import empty_pools
 from workloads import generator, normal_bf16
 
 pytestmark = pytest.mark.gpu

@@ -16,8 +16,8 @@ import pytest
 import torch
 
 import paged_kv_cache_281_gb300 as pkv
-from tests.gpu_harness import bf16_bits, bf16_to_f64, decode_step, run_decode, setup_decode
-from tests.oracle_side import bf16_tolerance_ok, build_decode_state, decode_reference
+from workloads.device import bf16_bits, bf16_to_f64, decode_step, run_decode, setup_decode
+from oracle.harness import bf16_tolerance_ok, build_decode_state, decode_reference
 from workloads import config1, config2, config3, generator, make_decode_workload
 
 pytestmark = pytest.mark.gpu

@@ -17,7 +17,7 @@ import torch
 
 import paged_kv_cache_281_gb300 as pkv
 from oracle import fp8 as ofp8
-from tests.gpu_harness import bf16_to_f64, to_dev_bf16
+from workloads.device import bf16_to_f64, to_dev_bf16
 from tests.test_gpu_decode import assert_close
 from workloads import generator, make_decode_workload, normal_bf16
 
@@ -172,7 +172,7 @@ def test_bad_table_entry_and_timeout_are_reported():
 
 def test_fp8_close_to_bf16_decode():
     # the quantisation error itself: fp8 decode stays near the bf16 result
-    from tests.gpu_harness import run_decode, setup_decode
+    from workloads.device import run_decode, setup_decode
     w = make_decode_workload("fp8_vs_bf16", (700, 1300, 90), Hq=32, Hkv=8, D=128, block_size=16,
                              seed=6400)
     dev, ora, tables, lens, st = build_fp8(w)

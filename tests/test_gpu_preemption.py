@@ -16,9 +16,10 @@ import pytest
 import torch
 
 import paged_kv_cache_281_gb300 as pkv
-from tests.gpu_harness import bf16_bits, bf16_to_f64
-from tests.preemption import (GpuRunner, LibraryAllocator, OracleAllocator, OracleRunner,
-                              TokenValues, run_schedule, small_trace_config)
+from workloads.device import bf16_bits, bf16_to_f64
+from oracle.harness import OracleAllocator, OracleRunner
+from workloads.device import GpuRunner
+from workloads.schedule import LibraryAllocator, TokenValues, run_schedule, small_trace_config
 from tests.test_gpu_decode import assert_close
 from workloads import generator
 
@@ -66,7 +67,7 @@ def test_undersized_pool_trace(mode):
 
 
 def test_swap_round_trip_bit_exact_through_pinned_host():
-    from tests.gpu_harness import poisoned_pools
+    from workloads.device import poisoned_pools
     from workloads import normal_bf16
     N, Hkv, B, D = 64, 8, 16, 128
     kc, vc = poisoned_pools(N, Hkv, B, D)
@@ -93,7 +94,7 @@ def test_swap_round_trip_bit_exact_through_pinned_host():
 
 
 def test_swap_refuses_pageable_host_memory():
-    from tests.gpu_harness import poisoned_pools
+    from workloads.device import poisoned_pools
     kc, vc = poisoned_pools(8, 2, 16, 64)
     kb = torch.empty((1, 2, 16, 64), dtype=torch.bfloat16)      # pageable
     with pytest.raises(pkv.PagedKVError) as e:

@@ -14,8 +14,8 @@ import torch
 
 import paged_kv_cache_281_gb300 as pkv
 from oracle import attention
-from tests.gpu_harness import bf16_to_f64, run_decode, setup_decode, to_dev_bf16
-from tests.oracle_side import build_decode_state
+from workloads.device import bf16_to_f64, run_decode, setup_decode, to_dev_bf16
+from oracle.harness import build_decode_state
 from tests.test_gpu_decode import assert_close
 from workloads import make_decode_workload, normal_bf16
 

@@ -17,9 +17,11 @@ import numpy as np
 import pytest
 
 import paged_kv_cache_281_gb300 as pkv
-from tests.gpu_harness import bf16_to_f64
+from workloads.device import bf16_to_f64
 from tests.prefix_cache import PrefixConfig, PrefixValues, prefix_schedule
-from tests.preemption import GpuRunner, LibraryAllocator, OracleAllocator, OracleRunner
+from oracle.harness import OracleAllocator, OracleRunner
+from workloads.device import GpuRunner
+from workloads.schedule import LibraryAllocator
 from tests.test_gpu_decode import assert_close
 
 pytestmark = pytest.mark.gpu

@@ -15,9 +15,9 @@ import pytest
 
 import paged_kv_cache_281_gb300 as pkv
 from oracle import attention
-from tests.gpu_harness import (bf16_to_f64, decode_shared_grouped, decode_shared_prefix,
+from workloads.device import (bf16_to_f64, decode_shared_grouped, decode_shared_prefix,
                                setup_shared_prefix, shared_groups)
-from tests.oracle_side import build_shared_prefix_state
+from oracle.harness import build_shared_prefix_state
 from tests.test_gpu_decode import assert_close
 from workloads import config4, make_shared_prefix_workload
 

@@ -20,9 +20,9 @@ import numpy as np
 import pytest
 import torch
 
-from tests.gpu_harness import (DeviceTrace, bf16_bits, bf16_to_f64, decode_shared_prefix,
+from workloads.device import (DeviceTrace, bf16_bits, bf16_to_f64, decode_shared_prefix,
                                run_decode, setup_decode, setup_shared_prefix)
-from tests.oracle_side import OracleTrace, build_shared_prefix_state
+from oracle.harness import OracleTrace, build_shared_prefix_state
 from tests.test_gpu_decode import assert_close
 from oracle import attention
 from workloads import TraceConfig, config4, generator, make_decode_workload, trace_iterations

@@ -30,7 +30,7 @@ import numpy as np
 import pytest
 
 from oracle import attention, cache, fp8, paging
-from tests.oracle_side import build_decode_state, build_shared_prefix_state, empty_pools
+from oracle.harness import build_decode_state, build_shared_prefix_state, empty_pools
 from workloads import config1, config4, make_decode_workload, normal_bf16
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")

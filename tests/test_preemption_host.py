@@ -12,8 +12,8 @@ import pytest
 
 import paged_kv_cache_281_gb300 as pkv
 from oracle import paging
-from tests.preemption import (LibraryAllocator, OracleAllocator, run_schedule,
-                              small_trace_config)
+from oracle.harness import OracleAllocator
+from workloads.schedule import LibraryAllocator, run_schedule, small_trace_config
 
 
 @pytest.mark.parametrize("mode", ["swap", "recompute"])

@@ -18,8 +18,8 @@ import torch
 
 import paged_kv_cache_281_gb300 as pkv
 from paged_kv_cache_281_gb300._lib import PKV_EINVAL, lib
-from tests.gpu_harness import bf16_to_f64, run_decode, setup_decode
-from tests.oracle_side import bf16_tolerance_ok
+from workloads.device import bf16_to_f64, run_decode, setup_decode
+from oracle.harness import bf16_tolerance_ok
 from workloads import config3, make_decode_workload
 
 pytestmark = pytest.mark.gpu

@@ -2,7 +2,8 @@
 
 The library's allocator hands out the blocks, ``pkv_kv_append`` writes the
 tokens into NaN-poisoned pools, and the decode/prefill calls run on them.
-Nothing here computes attention.
+Used by the benchmark, the tests and the smoke check; nothing here computes
+attention, and nothing here touches the oracle.
 """
 
 from __future__ import annotations
@@ -14,6 +15,7 @@ import torch
 
 import paged_kv_cache_281_gb300 as pkv
 from workloads import BF16_NAN
+from workloads.schedule import iteration_inputs
 
 
 def to_dev_bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
@@ -325,3 +327,69 @@ class DeviceTrace:
     def finish(self, itr):
         for rid in itr.finished:
             self.alloc.seq_free(self.sid.pop(rid))
+
+
+# ---------------------------------------------------------------- preemption
+
+class GpuRunner:
+    """Replays scheduler events with the library on the GPU."""
+
+    def __init__(self, cfg, num_blocks, device="cuda"):
+        import torch
+        import paged_kv_cache_281_gb300 as pkv
+        self.torch, self.pkv, self.cfg, self.dev = torch, pkv, cfg, device
+        self.k_cache, self.v_cache = poisoned_pools(num_blocks, cfg.Hkv, cfg.block_size, cfg.D,
+                                                    device)
+        self.status = pkv.new_status(device)
+        self.saved = {}
+        self.swap_bytes = 0
+        self.scale = 1.0 / np.sqrt(cfg.D)
+        self.ws = torch.empty(pkv.pkv_decode_workspace_bytes(
+            cfg.max_running, cfg.Hq, cfg.D, cfg.prompt_max + cfg.out_cap + cfg.chunk),
+            dtype=torch.uint8, device=device)
+        self.pws = None  # prefill work items, sized per call
+
+    def run(self, ev, values):
+        torch, pkv, cfg, dev = self.torch, self.pkv, self.cfg, self.dev
+        shape = (cfg.Hkv, cfg.block_size, cfg.D)
+        for kind, rid, blocks in ev.ops:
+            bl = torch.tensor(blocks, dtype=torch.int32, device=dev)
+            if kind == "swap_out":
+                kb = torch.empty((len(blocks),) + shape, dtype=torch.bfloat16).pin_memory()
+                vb = torch.empty_like(kb).pin_memory()
+                pkv.pkv_swap_blocks(self.k_cache, self.v_cache, bl, kb, vb, True,
+                                    status=self.status)
+                self.saved[rid] = (kb, vb)
+            else:
+                kb, vb = self.saved.pop(rid)
+                pkv.pkv_swap_blocks(self.k_cache, self.v_cache, bl, kb, vb, False,
+                                    status=self.status)
+            self.swap_bytes += 2 * kb.numel() * 2
+        pre, dec, q, k, v, slots, meta = iteration_inputs(cfg, ev, values)
+        pre_out = dec_out = None
+        if len(slots):
+            pkv.pkv_kv_append(to_dev_bf16(k, dev), to_dev_bf16(v, dev),
+                              torch.from_numpy(slots).to(dev), self.k_cache, self.v_cache,
+                              status=self.status)
+        qd = to_dev_bf16(q, dev)
+        n_pre = int(meta["cu"][-1])
+        if pre:
+            tables, lens = meta["prefill"]
+            need = pkv.pkv_prefill_workspace_bytes(len(pre), n_pre, cfg.Hq, cfg.D)
+            if self.pws is None or self.pws.numel() < need:
+                self.pws = torch.empty(need, dtype=torch.uint8, device=dev)
+            pre_out = torch.empty(n_pre, cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
+            pkv.pkv_paged_attention_prefill(
+                pre_out, qd[:n_pre], torch.from_numpy(meta["cu"]).to(dev),
+                torch.from_numpy(lens).to(dev), self.k_cache, self.v_cache,
+                torch.from_numpy(tables).to(dev), int(np.diff(meta["cu"]).max()),
+                int(lens.max()), self.scale, self.pws, status=self.status)
+        if dec:
+            tables, lens = meta["decode"]
+            dec_out = torch.empty(len(dec), cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
+            pkv.pkv_paged_attention_decode(
+                dec_out, qd[n_pre:], self.k_cache, self.v_cache, torch.from_numpy(tables).to(dev),
+                torch.from_numpy(lens).to(dev), int(lens.max()), self.scale, self.ws,
+                status=self.status)
+        torch.cuda.synchronize()  # the pinned swap buffers of swap-ins may be released now
+        return pre, dec, pre_out, dec_out

@@ -11,9 +11,11 @@ append cannot get its blocks, in one of two modes:
 * ``recompute``: the victim's blocks are freed and it re-enters the queue; on
   resumption it re-prefills every token it had cached, with the same values.
 
-The scheduler only decides; an allocator adapter (the library's allocator or
-the oracle's model) answers the block requests, and the two executors (GPU,
-oracle) replay the resulting events. Test infrastructure.
+The scheduler only decides; an allocator adapter (``LibraryAllocator`` here
+over the library's allocator, or the oracle's model of it) answers the block
+requests, and two executors (``workloads.device.GpuRunner`` on the GPU, the
+oracle's runner on the CPU) replay the resulting events. It draws the
+arrivals from the trace's seeded streams and computes no attention.
 """
 
 from __future__ import annotations
@@ -80,58 +82,6 @@ class LibraryAllocator:
 
     def num_free(self):
         return self.a.num_free_blocks()
-
-
-class OracleAllocator:
-    """Adapter over oracle.paging.BlockAllocator."""
-
-    def __init__(self, num_blocks, block_size):
-        from oracle import paging
-        self.paging = paging
-        self.a = paging.BlockAllocator(num_blocks, block_size)
-
-    def create(self):
-        return self.a.create()
-
-    def append(self, sid, n):
-        try:
-            slots, pairs = self.a.append_slots(sid, n)
-        except self.paging.OutOfBlocks as e:
-            raise OutOfBlocks(str(e)) from None
-        assert not pairs
-        return slots
-
-    def free(self, sid):
-        self.a.free_seq(sid)
-
-    def create_cached(self, tokens):
-        return self.a.create_cached(tokens)
-
-    def append_tokens(self, sid, tokens):
-        try:
-            slots, pairs = self.a.append_tokens(sid, tokens)
-        except self.paging.OutOfBlocks as e:
-            raise OutOfBlocks(str(e)) from None
-        assert not pairs
-        return slots
-
-    def num_cached(self):
-        return self.a.num_cached()
-
-    def swap_out(self, sid):
-        return self.a.swap_out(sid)
-
-    def swap_in(self, sid):
-        try:
-            return self.a.swap_in(sid)
-        except self.paging.OutOfBlocks as e:
-            raise OutOfBlocks(str(e)) from None
-
-    def table(self, sid):
-        return self.a.block_table(sid)
-
-    def num_free(self):
-        return self.a.num_free()
 
 
 class TokenValues:
@@ -312,111 +262,3 @@ def iteration_inputs(cfg, ev: Event, values: TokenValues):
         meta[name] = (tables, lens)
     meta["cu"] = np.concatenate([[0], np.cumsum([w[3] for w in pre])]).astype(np.int32)
     return pre, dec, q, k, v, slots, meta
-
-
-class GpuRunner:
-    """Replays scheduler events with the library on the GPU."""
-
-    def __init__(self, cfg, num_blocks, device="cuda"):
-        import torch
-        import paged_kv_cache_281_gb300 as pkv
-        from tests.gpu_harness import poisoned_pools
-        self.torch, self.pkv, self.cfg, self.dev = torch, pkv, cfg, device
-        self.k_cache, self.v_cache = poisoned_pools(num_blocks, cfg.Hkv, cfg.block_size, cfg.D,
-                                                    device)
-        self.status = pkv.new_status(device)
-        self.saved = {}
-        self.swap_bytes = 0
-        self.scale = 1.0 / np.sqrt(cfg.D)
-        self.ws = torch.empty(pkv.pkv_decode_workspace_bytes(
-            cfg.max_running, cfg.Hq, cfg.D, cfg.prompt_max + cfg.out_cap + cfg.chunk),
-            dtype=torch.uint8, device=device)
-        self.pws = None  # prefill work items, sized per call
-
-    def run(self, ev: Event, values: TokenValues):
-        torch, pkv, cfg, dev = self.torch, self.pkv, self.cfg, self.dev
-        from tests.gpu_harness import to_dev_bf16
-        shape = (cfg.Hkv, cfg.block_size, cfg.D)
-        for kind, rid, blocks in ev.ops:
-            bl = torch.tensor(blocks, dtype=torch.int32, device=dev)
-            if kind == "swap_out":
-                kb = torch.empty((len(blocks),) + shape, dtype=torch.bfloat16).pin_memory()
-                vb = torch.empty_like(kb).pin_memory()
-                pkv.pkv_swap_blocks(self.k_cache, self.v_cache, bl, kb, vb, True,
-                                    status=self.status)
-                self.saved[rid] = (kb, vb)
-            else:
-                kb, vb = self.saved.pop(rid)
-                pkv.pkv_swap_blocks(self.k_cache, self.v_cache, bl, kb, vb, False,
-                                    status=self.status)
-            self.swap_bytes += 2 * kb.numel() * 2
-        pre, dec, q, k, v, slots, meta = iteration_inputs(cfg, ev, values)
-        pre_out = dec_out = None
-        if len(slots):
-            pkv.pkv_kv_append(to_dev_bf16(k, dev), to_dev_bf16(v, dev),
-                              torch.from_numpy(slots).to(dev), self.k_cache, self.v_cache,
-                              status=self.status)
-        qd = to_dev_bf16(q, dev)
-        n_pre = int(meta["cu"][-1])
-        if pre:
-            tables, lens = meta["prefill"]
-            need = pkv.pkv_prefill_workspace_bytes(len(pre), n_pre, cfg.Hq, cfg.D)
-            if self.pws is None or self.pws.numel() < need:
-                self.pws = torch.empty(need, dtype=torch.uint8, device=dev)
-            pre_out = torch.empty(n_pre, cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
-            pkv.pkv_paged_attention_prefill(
-                pre_out, qd[:n_pre], torch.from_numpy(meta["cu"]).to(dev),
-                torch.from_numpy(lens).to(dev), self.k_cache, self.v_cache,
-                torch.from_numpy(tables).to(dev), int(np.diff(meta["cu"]).max()),
-                int(lens.max()), self.scale, self.pws, status=self.status)
-        if dec:
-            tables, lens = meta["decode"]
-            dec_out = torch.empty(len(dec), cfg.Hq, cfg.D, dtype=torch.bfloat16, device=dev)
-            pkv.pkv_paged_attention_decode(
-                dec_out, qd[n_pre:], self.k_cache, self.v_cache, torch.from_numpy(tables).to(dev),
-                torch.from_numpy(lens).to(dev), int(lens.max()), self.scale, self.ws,
-                status=self.status)
-        torch.cuda.synchronize()  # the pinned swap buffers of swap-ins may be released now
-        return pre, dec, pre_out, dec_out
-
-
-class OracleRunner:
-    """Replays the same events with the CPU oracle."""
-
-    def __init__(self, cfg, num_blocks):
-        from tests.oracle_side import empty_pools
-        self.cfg = cfg
-        self.k_cache, self.v_cache = empty_pools(num_blocks, cfg.Hkv, cfg.block_size, cfg.D)
-        self.saved = {}
-        self.scale = 1.0 / np.sqrt(cfg.D)
-
-    def run(self, ev: Event, values: TokenValues):
-        from oracle import cache
-        cfg = self.cfg
-        shape = (cfg.Hkv, cfg.block_size, cfg.D)
-        for kind, rid, blocks in ev.ops:
-            if kind == "swap_out":
-                kb = np.empty((len(blocks),) + shape, np.uint16)
-                vb = np.empty_like(kb)
-                cache.swap_blocks(self.k_cache, self.v_cache, blocks, kb, vb, 0)
-                self.saved[rid] = (kb, vb)
-            else:
-                kb, vb = self.saved.pop(rid)
-                cache.swap_blocks(self.k_cache, self.v_cache, blocks, kb, vb, 1)
-        pre, dec, q, k, v, slots, meta = iteration_inputs(cfg, ev, values)
-        cache.append(self.k_cache, self.v_cache, k, v, slots, cfg.block_size)
-        return pre, dec, q, meta
-
-    def prefill(self, ev, pre, q, meta, i):
-        from oracle import attention
-        tables, lens = meta["prefill"]
-        a, b = int(meta["cu"][i]), int(meta["cu"][i + 1])
-        return attention.prefill(q[a:b], np.array([0, b - a]), [int(lens[i])], self.k_cache,
-                                 self.v_cache, [tables[i]], self.cfg.block_size, self.scale)
-
-    def decode(self, ev, q, meta, i):
-        from oracle import attention
-        tables, lens = meta["decode"]
-        n_pre = int(meta["cu"][-1])
-        return attention.decode(q[n_pre + i:n_pre + i + 1], self.k_cache, self.v_cache,
-                                [tables[i]], [int(lens[i])], self.cfg.block_size, self.scale)[0]
