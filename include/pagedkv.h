@@ -293,7 +293,10 @@ int pkv_paged_attention_decode_shared(void* out, const void* q, const void* k_ca
  *     with PKV_EINVAL (a larger partition_size needs less).
  *   - Allocates nothing. The first call on a device looks up the array's
  *     device address for that device (once, with it current); make that first
- *     call before any stream capture.
+ *     call before any stream capture. The address is kept for the life of the
+ *     process: it does not survive cudaDeviceReset (the module is loaded
+ *     again and the array may move), so do not call this entry point on a
+ *     device after resetting it.
  *   - All calls share the one array, which keeps the last call's contents;
  *     every call rewrites what it reads first. Calls that overlap on the GPU
  *     (other streams, other host threads) race on it: serialise them.

@@ -51,11 +51,21 @@ def _stream(stream) -> int | None:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _check_device(name: str, index: int, current: int) -> None:
+    # The library launches on the current device and builds its tile maps
+    # over the pointers it is given; a tensor on another GPU would be read
+    # through the wrong device's address space, so refuse it here.
+    if index != current:
+        raise ValueError(f"{name} lives on cuda:{index} but the current device is "
+                         f"cuda:{current}; call under torch.cuda.device({index})")
+
+
 def _dev(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int | None = None):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must live on a CUDA device")
+    _check_device(name, t.device.index, torch.cuda.current_device())
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():

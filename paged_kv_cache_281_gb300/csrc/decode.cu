@@ -1819,7 +1819,9 @@ std::once_flag g_noalloc_once[kNoAllocMaxDevices];
 
 // Device address of the scratch array on the current device. In host code the
 // array's name is only a stand-in, so the address is looked up once per
-// device, with that device current.
+// device, with that device current, and kept for the life of the process (a
+// cudaDeviceReset reloads the module, after which the kept address is stale;
+// the header tells callers not to use this entry point after a reset).
 int noalloc_scratch(void** out) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);

@@ -12,6 +12,7 @@ import os
 
 import numpy as np
 import pytest
+import torch
 
 import paged_kv_cache_281_gb300 as pkv
 from paged_kv_cache_281_gb300 import _lib
@@ -325,3 +326,14 @@ def test_pool_beyond_int32_rows_is_rejected():
     assert _call("pkv_paged_attention_decode", None, None, None, None, None, 8, None, 64, 2, 32,
                  8, 128, 16, big, 0.1, 0, None, 0, None, None) == PKV_EINVAL
     assert "2^31" in pkv.pkv_last_error()
+
+
+def test_wrappers_refuse_tensors_on_another_device():
+    # The binding checks that each tensor lives on the current device before
+    # it passes the pointer on (the kernels launch on the current device).
+    from paged_kv_cache_281_gb300.api import _check_device, _dev
+    _check_device("q", 0, 0)
+    with pytest.raises(ValueError, match="cuda:1 but the current device is cuda:0"):
+        _check_device("q", 1, 0)
+    with pytest.raises(ValueError, match="CUDA device"):
+        _dev(torch.zeros(4, dtype=torch.int32), "status", torch.int32, 1)
