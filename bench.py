@@ -48,10 +48,39 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode attn KV GB/s and % of HBM peak; attention tokens/s per layer"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-# DRAM read + write bytes of one paged_decode_kernel<128,4> launch on this
-# workload, taken with ncu (dram__bytes_read.sum + dram__bytes_write.sum);
-# to be set to None whenever the kernel changes.
-DECODE_TRAFFIC_BYTES = 1_403_613_440
+# ncu DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+# lives in profiles/traffic_records.md, one row per kernel and workload, with
+# a hash of the kernel's sources at capture time; a record is used only while
+# those sources are unchanged (else the line reports traffic null).
+TRAFFIC_SOURCES = {
+    "decode_llama3_8b_gqa": ("decode.cu", "device.cuh"),
+    "kv_append_20k": ("cache_ops.cu", "device.cuh"),
+}
+
+
+def sources_sha(key: str) -> str:
+    """First 16 hex digits of the sha256 of the kernel sources of ``key``."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES[key]:
+        with open(os.path.join(ROOT, "paged_kv_cache_281_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(key: str):
+    """DRAM bytes per launch from the committed ncu record of ``key``, or None
+    when there is none or the kernel's sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic_records.md")
+    if not os.path.exists(path):
+        return None
+    want = sources_sha(key)
+    with open(path) as f:
+        for line in f:
+            cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
+            if len(cells) >= 4 and cells[0] == key and cells[2] == want:
+                return int(cells[3].replace(",", ""))
+    return None
 
 
 def parse_args():
@@ -66,7 +95,7 @@ def parse_args():
     ap.add_argument("--workload", choices=["llama3_8b_gqa", "llama2_7b_mha", "tiny",
                                            "llama3_8b_gqa_fp8", "trace",
                                            "trace_preempt", "swap", "prefix_cache",
-                                           "shared_prefix", "prefill"],
+                                           "shared_prefix", "prefill", "cache_ops"],
                     default="llama3_8b_gqa",
                     help="llama2_7b_mha: the same decode step on 64 sequences of a "
                          "Llama-2-7B-shaped MHA layer (32/32 heads, L ~ U[128, 2048]); "
@@ -81,6 +110,8 @@ def parse_args():
                          "pinned host memory and back; prefix_cache: 256 requests sharing a "
                          "1024-token system prompt, prefilled with and without the prefix "
                          "cache (separate lines; the default is the headline decode step)")
+    ap.add_argument("--append-tokens", type=int, default=20000,
+                    help="cache_ops: new tokens in the timed kv_append / kv_append_fp8 launch")
     ap.add_argument("--iterations", type=int, default=200)
     ap.add_argument("--pool-blocks", type=int, default=9000,
                     help="trace_preempt: KV blocks in the pool (the trace peaks near 10,400)")
@@ -211,17 +242,266 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(name: str = "llama3_8b_gqa"):
-    """Times the fp64 oracle's decode over the whole batch of the workload in a
-    child process: once on one thread, then with the sequences dealt out to
-    one process per host core."""
+def cpu_baseline(kind: str = "llama3_8b_gqa", *extra: str):
+    """Times the fp64 oracle on a bounded sample of one workload in a child
+    process (one BLAS / OpenMP thread; the child never touches the GPU).
+    ``kind`` names the workload; decode batches are timed whole, once on one
+    thread and once dealt out to one process per host core."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    cmd = [sys.executable, os.path.abspath(__file__), "--_oracle-sample", name]
+    cmd = [sys.executable, os.path.abspath(__file__), "--_oracle-sample", kind, *extra]
     r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
-        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+        return {"value": None, "unit": None, "cores": 1, "kind": "oracle",
                 "sample": "failed: " + r.stderr.strip()[-200:]}
     return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def attach_cpu_baseline(line: dict, args, kind: str, *extra: str) -> None:
+    """The oracle's time on a bounded sample of the line's workload, on rank 0
+    of a single-GPU run only (``--no-cpu-baseline`` skips it)."""
+    rank, world, _ = dist_info()
+    line["cpu_baseline"] = (cpu_baseline(kind, *extra)
+                            if rank == 0 and world == 1 and not args.no_cpu_baseline else None)
+
+
+def _seeded_pick(rng, n: int, frac: int) -> list:
+    """A seeded ceil(n / frac) of range(n), sorted."""
+    if n == 0:
+        return []
+    return sorted(rng.choice(n, -(-n // frac), replace=False).tolist())
+
+
+def _oracle_trace(extra):
+    """Config 5: the oracle replays every iteration's kv_append (untimed) and
+    times its attention on a seeded 1/8 of the prefill requests and decode
+    sequences of every 10th iteration."""
+    from oracle.harness import OracleTrace
+    from workloads import TraceConfig, generator, trace_iterations
+    cfg = TraceConfig(iterations=int(extra[0]) if extra else 200)
+    ora = OracleTrace(cfg)
+    rng = generator(cfg.seed, 91)
+    secs, tokens, items, its = 0.0, 0, 0, []
+    for itr in trace_iterations(cfg):
+        ora.step(itr)
+        if itr.index % 10 == 5:
+            pre = _seeded_pick(rng, len(itr.prefill), 8)
+            dec = _seeded_pick(rng, len(itr.decode), 8)
+            t0 = time.perf_counter()
+            ora.prefill(itr, pre)
+            ora.decode(itr, dec)
+            secs += time.perf_counter() - t0
+            tokens += sum(itr.prefill[i].n for i in pre) + len(dec)
+            items += len(pre) + len(dec)
+            its.append(itr.index)
+        ora.finish(itr)
+    return {"value": tokens / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "seconds": secs,
+            "sample": f"iterations {its[0]}, {its[1]}, ..., {its[-1]} of the trace: a seeded 1/8 "
+                      f"of each one's prefill requests and decode sequences ({items} items, "
+                      f"{tokens} query tokens), fp64 gather + causal softmax attention, 1 "
+                      "thread; the kv_append of every iteration replayed untimed"}
+
+
+def _oracle_paged_request(pools, table, L, vals, block_size):
+    """Writes a request's first L tokens (values ``vals``) into its blocks of
+    the oracle's pools (untimed set-up for a timed attention call)."""
+    from oracle import cache
+    j = np.arange(L)
+    slots = np.asarray(table, dtype=np.int64)[j // block_size] * block_size + j % block_size
+    cache.append(pools[0], pools[1], vals[0][:L], vals[1][:L], slots, block_size)
+
+
+def _oracle_trace_preempt(extra):
+    """The preemption trace: the same schedule (the oracle's allocator model
+    makes the library's decisions); for a seeded 1/8 of the work items of
+    every 10th iteration the request's tokens are written into its current
+    blocks (untimed) and the oracle's attention for that item is timed, with
+    the iteration's swap copies (cache.swap_blocks on the listed blocks)."""
+    from oracle import attention, cache
+    from oracle.harness import OracleAllocator
+    from workloads import TraceConfig, generator, normal_bf16
+    from workloads.schedule import PreemptingScheduler
+    iters, nb, mode = int(extra[0]), int(extra[1]), extra[2]
+    cfg = TraceConfig(iterations=iters)
+    B = cfg.block_size
+    sched = PreemptingScheduler(cfg, nb, mode, OracleAllocator(nb, B), watermark=max(1, nb // 100))
+    max_ctx = cfg.prompt_max + cfg.out_cap + cfg.chunk
+    vals = (normal_bf16((max_ctx, cfg.Hkv, cfg.D), 92), normal_bf16((max_ctx, cfg.Hkv, cfg.D), 93))
+    qv = normal_bf16((cfg.chunk, cfg.Hq, cfg.D), 94)
+    shape = (nb, cfg.Hkv, B, cfg.D)
+    pools = (np.zeros(shape, np.uint16), np.zeros(shape, np.uint16))
+    rng = generator(cfg.seed, 95)
+    scale = 1.0 / math.sqrt(cfg.D)
+    secs, tokens, items, swapped = 0.0, 0, 0, 0
+    for it in range(cfg.iterations):
+        ev = sched.step(it)
+        if it % 10 != 5:
+            continue
+        for kind, _, blocks in ev.ops:
+            buf = np.empty((len(blocks), cfg.Hkv, B, cfg.D), np.uint16)
+            t0 = time.perf_counter()
+            cache.swap_blocks(pools[0], pools[1], blocks, buf, buf.copy(),
+                              0 if kind == "swap_out" else 1)
+            secs += time.perf_counter() - t0
+            swapped += len(blocks)
+        for i in _seeded_pick(rng, len(ev.work), 8):
+            rid, _, start, n, kind, _ = ev.work[i]
+            table, L = ev.tables[rid], start + n
+            _oracle_paged_request(pools, table, L, vals, B)
+            t0 = time.perf_counter()
+            if kind == "prefill":
+                attention.prefill(qv[:n], [0, n], [L], pools[0], pools[1], [table], B, scale)
+            else:
+                attention.decode(qv[:1], pools[0], pools[1], [table], [L], B, scale)
+            secs += time.perf_counter() - t0
+            tokens += n
+            items += 1
+    return {"value": tokens / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "seconds": secs,
+            "sample": f"every 10th iteration of the {mode} schedule ({nb}-block pool): a seeded "
+                      f"1/8 of its work items ({items} items, {tokens} query tokens; fp64 gather + "
+                      f"softmax attention) and all its swap copies ({swapped} blocks), 1 thread; "
+                      "token values drawn on the host"}
+
+
+def _oracle_swap(extra):
+    """Swap: the oracle's whole-block copies of a seeded 4,096 of the decode
+    batch's blocks out to a buffer and back."""
+    from oracle import cache
+    from workloads import config3_lengths, generator, pool_blocks
+    N = pool_blocks(config3_lengths(), 16)
+    shape = (N, 8, 16, 128)
+    pools = (np.zeros(shape, np.uint16), np.zeros(shape, np.uint16))
+    n, reps = 8192, 5
+    blocks = generator(0x281 + 3, 96).choice(N, n, replace=False)
+    kb = np.empty((n,) + shape[1:], np.uint16)
+    vb = np.empty_like(kb)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        cache.swap_blocks(pools[0], pools[1], blocks, kb, vb, 0)
+        cache.swap_blocks(pools[0], pools[1], blocks, kb, vb, 1)
+    secs = time.perf_counter() - t0
+    nbytes = reps * 2 * 2 * kb.nbytes
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": secs,
+            "sample": f"{n} seeded blocks of the {N}-block pool (K and V, 8 heads, B=16, D=128) "
+                      f"copied out to a host buffer and back by the oracle's block loop, {reps} "
+                      "times, 1 thread"}
+
+
+def _oracle_prefix_cache(extra):
+    """Prefix caching: for 96 seeded requests of the 256, the work the cached
+    run does for them (append the rows after the cached prefix, then their
+    causal prefill over the whole context)."""
+    from oracle import attention, cache
+    from workloads import normal_bf16
+    S, P, Hq, Hkv, D, B = 256, 1024, 32, 8, 128, 16
+    g = np.random.default_rng(0x281 + 70)
+    qlen = g.integers(16, 256, size=S, endpoint=True)
+    pick = sorted(np.random.default_rng(0x281 + 97).choice(S, 96, replace=False).tolist())
+    Lmax = P + 256
+    nbk = -(-Lmax // B)
+    table = list(range(nbk))
+    shape = (nbk, Hkv, B, D)
+    pools = (np.zeros(shape, np.uint16), np.zeros(shape, np.uint16))
+    k, v = normal_bf16((Lmax, Hkv, D), 98), normal_bf16((Lmax, Hkv, D), 99)
+    q = normal_bf16((Lmax, Hq, D), 100)
+    scale = 1.0 / math.sqrt(D)
+    secs, served = 0.0, 0
+    for i in pick:
+        L = P + int(qlen[i])
+        start = 0 if i == 0 else (P // B) * B        # request 0 computes its whole prompt
+        _oracle_paged_request(pools, table, start, (k, v), B)
+        j = np.arange(start, L)
+        slots = np.asarray(table)[j // B] * B + j % B
+        t0 = time.perf_counter()
+        cache.append(pools[0], pools[1], k[start:L], v[start:L], slots, B)
+        attention.prefill(q[start:L], [0, L - start], [L], pools[0], pools[1], [table], B, scale)
+        secs += time.perf_counter() - t0
+        served += L
+    return {"value": served / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "seconds": secs,
+            "sample": f"96 seeded requests of the 256: the cached run's work for each "
+                      "(kv_append of the rows after its cached prefix, fp64 causal prefill of "
+                      "those rows over the whole context), prompt tokens served per second, "
+                      "1 thread"}
+
+
+def _oracle_prefill(extra):
+    """Fresh prompts S x C: the oracle's causal prefill of a few of the S
+    sequences (about ten seconds of one core)."""
+    from oracle import attention
+    from workloads import normal_bf16
+    S, C = int(extra[0]), int(extra[1])
+    Hq, Hkv, D, B = 32, 8, 128, 16
+    n = max(1, min(S, (12 * 1024 * 1024) // (C * C)))   # about 10 s of one core
+    nbk = -(-C // B)
+    shape = (nbk, Hkv, B, D)
+    pools = (normal_bf16(shape, 101), normal_bf16(shape, 102))
+    table = list(range(nbk))
+    secs = 0.0
+    for s in range(n):
+        q = normal_bf16((C, Hq, D), 103 + s)
+        t0 = time.perf_counter()
+        attention.prefill(q, [0, C], [C], pools[0], pools[1], [table], B, 1.0 / math.sqrt(D))
+        secs += time.perf_counter() - t0
+    flops = n * 4 * D * Hq * (C * (C + 1) // 2)
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "seconds": secs,
+            "sample": f"{n} of the {S} fresh {C}-token prompts (32/8 heads, D=128): fp64 gather "
+                      "+ causal softmax attention, algorithmic flops 4*D*Hq*C(C+1)/2 each, "
+                      "1 thread"}
+
+
+def _oracle_fp8(extra):
+    """FP8 pages: 32 seeded sequences of the Llama-3-8B GQA batch quantised by
+    the oracle (untimed), then its decode over the dequantised pages."""
+    from oracle import fp8, paging
+    from workloads import config3_lengths, generator, make_decode_workload, SEED_BASE
+    lens = config3_lengths()
+    pick = np.sort(generator(SEED_BASE + 3, 12).choice(len(lens), 32, replace=False))
+    w = make_decode_workload("fp8_sample", lens[pick], Hq=32, Hkv=8, D=128, block_size=16,
+                             seed=SEED_BASE + 7100)
+    alloc = paging.BlockAllocator(w.num_blocks, w.block_size, w.free_order)
+    shape = (w.num_blocks, w.Hkv, w.block_size, w.D)
+    k8, v8 = np.zeros(shape, np.uint8), np.zeros(shape, np.uint8)
+    ks, vs = np.zeros(shape[:3], np.float32), np.zeros(shape[:3], np.float32)
+    cu, tables = w.cu_lens, []
+    for s in range(w.S):
+        sid = alloc.create()
+        sl, _ = alloc.append_slots(sid, int(w.context_lens[s]))
+        fp8.append(k8, v8, ks, vs, w.k[cu[s]:cu[s + 1]], w.v[cu[s]:cu[s + 1]], sl, w.block_size)
+        tables.append(alloc.block_table(sid))
+    t0 = time.perf_counter()
+    fp8.decode(w.q, k8, v8, ks, vs, tables, w.context_lens, w.block_size, w.scale)
+    secs = time.perf_counter() - t0
+    nbytes = w.total_tokens * w.Hkv * 2 * (w.D + 4)
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": secs,
+            "sample": f"32 seeded sequences of the 256 ({w.total_tokens} context tokens): fp64 "
+                      "dequantise + gather + softmax attention over e4m3 codes and row scales, "
+                      "bytes of codes and scales per second, 1 thread"}
+
+
+def _oracle_shared_prefix(extra):
+    """Shared prefix: the oracle's decode of the whole batch (the oracle
+    gathers every sample's pages through its own table)."""
+    from oracle import attention
+    from oracle.harness import build_shared_prefix_state
+    from workloads import config4, generator
+    w = config4(extra[0])
+    st = build_shared_prefix_state(w)
+    t0 = time.perf_counter()
+    attention.decode(w.q, st.k_cache, st.v_cache, st.tables, w.context_lens, w.block_size,
+                     w.scale)
+    secs = time.perf_counter() - t0
+    return {"value": w.S / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "seconds": secs,
+            "sample": f"the whole batch ({w.S} samples, contexts {w.prefix_len} + tail): fp64 "
+                      "gather + softmax attention through each sample's own table, decode "
+                      "tokens per second, 1 thread"}
+
+
 
 
 def _oracle_state(name: str, pick=None, seed_offset: int = 0):
@@ -426,6 +706,11 @@ def run_trace(args):
                    "l2": "decode reads ~0.4 GB of K/V per iteration (> 129 MB L2)"},
         "kernel_ms": {"kv_append": t_app, "prefill": t_pre, "decode": t_dec},
         "pass_ms": pass_ms,
+        "oracle_check": "tests/test_gpu_workloads.py::test_continuous_batching_trace runs this "
+                        "trace against the oracle: every 10th iteration in full and a seeded "
+                        "1/8 of the prefill requests and decode sequences of every other "
+                        "iteration (the oracle needs about 2.3 s of one host core per full "
+                        "iteration, about 8 minutes for all 200)",
         "host_scheduler_ms": 1e3 * host_s,
         "roofline": {"bound": "hbm", "kernel": "pkv_paged_attention_decode", "achieved": dec_gbs,
                      "peak": peak_hbm, "unit": "GB/s", "frac": dec_gbs / peak_hbm,
@@ -439,8 +724,8 @@ def run_trace(args):
                         sum(1 for x in stats if x[1]),
         "clocks": clocks.summary(),
         "input_generation_s": gen_s,
-        "cpu_baseline": None,
     }
+    attach_cpu_baseline(line, args, "trace", str(args.iterations))
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -591,8 +876,9 @@ def run_trace_preempt(args):
         "gpu_launches": sum(len(u["ops"]) + ("k" in u) + ("pre" in u) + 3 * ("dec" in u)
                             for u in ups),
         "clocks": clocks.summary(),
-        "cpu_baseline": None,
     }
+    attach_cpu_baseline(line, args, "trace_preempt", str(args.iterations),
+                        str(args.pool_blocks), args.preempt)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -691,8 +977,8 @@ def run_swap(args):
         "copy_engine_gbs": {"d2h": gbs(ce_out), "h2d": gbs(ce_in)},
         "gpu_launches": 2 * steps,
         "clocks": clocks.summary(),
-        "cpu_baseline": None,
     }
+    attach_cpu_baseline(line, args, "swap")
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -818,8 +1104,8 @@ def run_prefix_cache(args):
                      "frac": tf / float(peaks["bf16_tflops"]), "traffic": None},
         "gpu_launches": 2 * 2 * (steps + max(3, args.warmup)),
         "clocks": clocks.summary(),
-        "cpu_baseline": None,
     }
+    attach_cpu_baseline(line, args, "prefix_cache")
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -906,11 +1192,134 @@ def run_prefill(args):
                      "algorithmic_flops_per_launch": h["flops"]},
         "gpu_launches": 2 * steps * len(shapes),
         "clocks": clocks.summary(),
-        "cpu_baseline": None,
     }
+    attach_cpu_baseline(line, args, "prefill", str(h["S"]), str(h["chunk"]))
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def run_cache_ops(args):
+    """The cache writers at the sizes where they are bandwidth-bound:
+    kv_append and kv_append_fp8 of one prefill-sized batch of new tokens
+    (``--append-tokens``, 8 KV heads, D=128, B=16, the tokens of whole
+    prompts packed into blocks handed out by a seeded permutation of a
+    Llama-3-8B-sized pool), and block_copy of the 192 copy-on-write pairs of
+    the shared-prefix batch with a half-full last shared block. Each launch
+    is timed alone with CUDA events, after a write of 512 MB that evicts the
+    L2, so inputs come from HBM."""
+    import torch
+    import paged_kv_cache_281_gb300 as pkv
+    from workloads import config3_lengths, config4, generator, pool_blocks
+    from workloads.device import poisoned_pools, setup_shared_prefix
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    T, Hkv, D, B = args.append_tokens, 8, 128, 16
+    N = pool_blocks(config3_lengths(), B)
+    stream = torch.cuda.current_stream()
+    g = generator(0x281 + 90, rank)
+    blocks = g.permutation(N)[:-(-T // B)]
+    slots = (blocks[:, None] * B + np.arange(B)[None, :]).reshape(-1)[:T].astype(np.int32)
+    slot_t = torch.from_numpy(slots).cuda()
+    tg = torch.Generator(device="cuda").manual_seed(0x281 + 90 + rank)
+    k_new = torch.randn(T, Hkv, D, generator=tg, device="cuda").to(torch.bfloat16)
+    v_new = torch.randn(T, Hkv, D, generator=tg, device="cuda").to(torch.bfloat16)
+    kc, vc = poisoned_pools(N, Hkv, B, D, poison=False)
+    k8, v8, ks, vs = pkv.new_fp8_pools(N, Hkv, B, D)
+    status = pkv.new_status()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    steps = max(5, min(args.steps, 200))
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        ts = []
+        for _ in range(steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        t = np.array([a.elapsed_time(b) for a, b in ts])
+        return {"ms": float(t.mean()), "p10_ms": float(np.percentile(t, 10)),
+                "p50_ms": float(np.percentile(t, 50)), "p90_ms": float(np.percentile(t, 90))}
+
+    w4 = config4("b")
+    d4 = setup_shared_prefix(w4)
+    scratch = d4.alloc.seq_create()
+    d4.alloc.seq_append_slots(scratch, len(d4.cow_pairs) * w4.block_size)
+    dst = d4.alloc.seq_block_table(scratch)
+    pairs = torch.tensor([[src, dst[i]] for i, (src, _) in enumerate(d4.cow_pairs)],
+                         dtype=torch.int32, device="cuda")
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        app = timed(lambda: pkv.pkv_kv_append(k_new, v_new, slot_t, kc, vc, status=status,
+                                              stream=stream))
+        app8 = timed(lambda: pkv.pkv_kv_append_fp8(k_new, v_new, slot_t, k8, v8, ks, vs,
+                                                   status=status, stream=stream))
+        cow = timed(lambda: pkv.pkv_block_copy(d4.k_cache, d4.v_cache, pairs, status=d4.status,
+                                               stream=stream))
+    pkv.pkv_check_status(status)
+    pkv.pkv_check_status(d4.status)
+    peak, peak_kind = measured_peaks()
+    row = Hkv * D * 2
+    app_bytes = 2 * 2 * T * row                       # read + write, keys and values
+    app8_bytes = 2 * T * row + 2 * T * Hkv * (D + 4)  # bf16 in, codes + scales out
+    blk = Hkv * w4.block_size * D * 2
+    cow_bytes = 2 * 2 * len(d4.cow_pairs) * blk       # read + write, keys and values
+    gbs = lambda b, r: b / (r["ms"] * 1e-3) / 1e9
+    for r, b in ((app, app_bytes), (app8, app8_bytes), (cow, cow_bytes)):
+        r.update(algorithmic_bytes=b, gbs=gbs(b, r), frac=gbs(b, r) / peak)
+    line = {
+        "metric": "kv_append at prefill size: bytes read + written per second (HBM)",
+        "value": world * gbs(app_bytes, app), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": max(3, args.warmup), "ms_per_step": app["ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "kv_append of %d new tokens (8 KV heads, D=128, B=16) into a "
+                               "%d-block pool; kv_append_fp8 of the same tokens; block_copy "
+                               "of the %d copy-on-write pairs of the shared-prefix batch "
+                               "with a 1032-token prefix" % (T, N, len(d4.cow_pairs)),
+                   "tokens": T,
+                   "l2": "512 MB written before every timed launch (L2 is 129 MB)"},
+        "kv_append": app, "kv_append_fp8": app8, "block_copy": cow,
+        "roofline": {"bound": "hbm", "kernel": "kv_append_kernel", "achieved": app["gbs"],
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": app["frac"],
+                     "traffic": traffic_record("kv_append_20k"),
+                     "algorithmic_bytes_per_launch": app_bytes, "avg_launch_ms": app["ms"]},
+        "gpu_launches": 3 * (steps + max(3, args.warmup)),
+        "clocks": clocks.summary(),
+    }
+    attach_cpu_baseline(line, args, "cache_ops", str(T))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def _oracle_cache_ops(extra):
+    """kv_append: the oracle's slot loop over a seeded 4,096 of the batch's
+    new tokens (8 KV heads, D=128) into a pool of the same size."""
+    from oracle import cache
+    from workloads import config3_lengths, generator, normal_bf16, pool_blocks
+    T, Hkv, D, B = 4096, 8, 128, 16
+    N = pool_blocks(config3_lengths(), B)
+    shape = (N, Hkv, B, D)
+    pools = (np.zeros(shape, np.uint16), np.zeros(shape, np.uint16))
+    blocks = generator(0x281 + 90, 0).permutation(N)[:-(-T // B)]
+    slots = (blocks[:, None] * B + np.arange(B)[None, :]).reshape(-1)[:T]
+    k, v = normal_bf16((T, Hkv, D), 105), normal_bf16((T, Hkv, D), 106)
+    reps = 100
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        cache.append(pools[0], pools[1], k, v, slots, B)
+    secs = time.perf_counter() - t0
+    nbytes = reps * 2 * 2 * T * Hkv * D * 2
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": secs,
+            "sample": f"{T} new tokens of the batch written into their slots by the oracle's "
+                      f"per-token loop, {reps} times, bytes read + written per second, 1 thread"}
 
 
 def run_fp8(args):
@@ -1005,8 +1414,8 @@ def run_fp8(args):
                      "avg_launch_ms": decode_ms},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks.summary(),
-        "cpu_baseline": None,
     }
+    attach_cpu_baseline(line, args, "fp8")
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -1107,16 +1516,23 @@ def run_shared_prefix(args):
                      "algorithmic_bytes_per_launch": unique},
         "gpu_launches": 2 * 3 * args.steps + (args.steps if pairs is not None else 0),
         "clocks": clocks.summary(),
-        "cpu_baseline": None,
     }
     if pairs is not None:
         blk = 2 * w.Hkv * w.block_size * w.D * 2
         line["block_copy"] = {"pairs": len(d.cow_pairs), "ms": copy_ms,
                               "gbs": 2 * blk * len(d.cow_pairs) / (copy_ms * 1e-3) / 1e9,
                               "note": "read + write of each copied block (K and V)"}
+    attach_cpu_baseline(line, args, "shared_prefix", args.variant)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+ORACLE_SAMPLES = {
+    "trace": _oracle_trace, "trace_preempt": _oracle_trace_preempt, "swap": _oracle_swap,
+    "prefix_cache": _oracle_prefix_cache, "prefill": _oracle_prefill, "fp8": _oracle_fp8,
+    "shared_prefix": _oracle_shared_prefix, "cache_ops": _oracle_cache_ops,
+}
 
 
 def main():
@@ -1137,6 +1553,8 @@ def main():
         return run_prefix_cache(args)
     if args.workload == "prefill":
         return run_prefill(args)
+    if args.workload == "cache_ops":
+        return run_cache_ops(args)
     import torch
     import paged_kv_cache_281_gb300 as pkv
     from workloads.device import decode_step, setup_decode
@@ -1191,10 +1609,10 @@ def main():
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
 
-    e2e = None
+    e2e = e2e_sync = None
     if not args.no_e2e:
         barrier()
-        e2e = e2e_measure(w, d, args, pkv, torch)
+        e2e, e2e_sync = e2e_measure(w, d, args, pkv, torch)
         if world > 1:
             # whole job: every rank's bytes over the slowest rank's step time
             ms_e2e = max_over_ranks(e2e["ms_per_step"])
@@ -1212,8 +1630,8 @@ def main():
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": DECODE_TRAFFIC_BYTES if (args.partition_size in (0, 1024) and
-                                                         args.workload == "llama3_8b_gqa")
+                     "traffic": traffic_record("decode_llama3_8b_gqa")
+                     if (args.partition_size in (0, 1024) and args.workload == "llama3_8b_gqa")
                      else None,
                      "traffic_kernel": "paged_decode_kernel<%d,%d> (ncu, one launch)"
                                        % (w.D, w.Hq // w.Hkv),
@@ -1226,6 +1644,7 @@ def main():
     }
     if e2e is not None:
         line["e2e"] = e2e
+        line["e2e_sync"] = e2e_sync
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # the oracle is timed once, on the single-GPU run only
         line["cpu_baseline"] = cpu_baseline(args.workload)
@@ -1281,15 +1700,37 @@ def e2e_measure(w, d, args, pkv, torch, steps=None):
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
-    return {"value": w.kv_bytes() / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
-            "steps": steps, "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(d2h),
-            "note": "KV pools stay resident (they are the cache); per-step inputs cross "
-                    "the CPU-GPU link from one pinned staging buffer, the output back "
-                    "into pinned memory"}
+    e2e = {"value": w.kv_bytes() / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
+           "steps": steps, "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(d2h),
+           "note": "KV pools stay resident (they are the cache); per-step inputs cross "
+                   "the CPU-GPU link from one pinned staging buffer, the output back "
+                   "into pinned memory; steps issued back to back (throughput)"}
+    # the same step, with the host waiting for each step's output before it
+    # issues the next one: latency per step on the host's wall clock
+    lat = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        one()
+        stream.synchronize()
+        lat.append(1e3 * (time.perf_counter() - t0))
+    lat = np.array(lat)
+    sync = {"value": w.kv_bytes() / (lat.mean() * 1e-3) / 1e9, "unit": UNIT,
+            "ms_per_step": float(lat.mean()), "p50_ms": float(np.percentile(lat, 50)),
+            "p90_ms": float(np.percentile(lat, 90)), "steps": steps,
+            "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(d2h),
+            "note": "host wall clock from issuing the input copy to the output in pinned "
+                    "memory, the host blocking on every step"}
+    return e2e, sync
 
 
 if __name__ == "__main__":
+    if len(sys.argv) >= 3 and sys.argv[1] == "--sources-sha":
+        print(sources_sha(sys.argv[2]))
+        sys.exit(0)
     if len(sys.argv) >= 3 and sys.argv[1] == "--_oracle-sample":
-        oracle_sample_main(sys.argv[2])
+        if sys.argv[2] in ORACLE_SAMPLES:
+            print(json.dumps(ORACLE_SAMPLES[sys.argv[2]](sys.argv[3:])))
+        else:
+            oracle_sample_main(sys.argv[2])
         sys.exit(0)
     sys.exit(main())

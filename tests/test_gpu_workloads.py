@@ -10,8 +10,10 @@ oracle, and a shared prefix must decode bit-identically to duplicated copies.
 Trace ("Deep Dive: continuous batching", sections Iteration-level scheduling
 and The prefill/decode mix): 200 iterations that admit, chunk-prefill, decode
 and retire requests, each iteration running kv_append, chunked paged prefill
-and paged decode over all active sequences. Every 20th iteration is checked
-against the oracle in full; the others on a seeded sample.
+and paged decode over all active sequences. Checking every iteration in full
+would take the oracle about eight minutes of one host core (about 2.3 s per
+iteration), so every 10th iteration is checked in full and a seeded 1/8 of
+the prefill requests and of the decode sequences of every other iteration.
 """
 
 from __future__ import annotations
@@ -72,6 +74,11 @@ def test_shared_prefix_equals_duplicated_copies_bit_exact():
     assert np.array_equal(shared, bf16_bits(run_decode(dup, dd)))
 
 
+def seeded_eighth(rng, n):
+    """A seeded ceil(n / 8) of range(n), sorted."""
+    return sorted(rng.choice(n, -(-n // 8), replace=False).tolist()) if n else []
+
+
 def test_continuous_batching_trace():
     cfg = TraceConfig()
     gpu, ora = DeviceTrace(cfg), OracleTrace(cfg)
@@ -82,12 +89,10 @@ def test_continuous_batching_trace():
         slots = ora.step(itr)
         assert np.array_equal(meta["slots"], slots), f"iteration {itr.index}: slots differ"
         pre_out, dec_out = gpu.run_iteration(itr, meta)
-        full = itr.index % 20 == 0
+        full = itr.index % 10 == 0
         n_pre, n_dec = len(itr.prefill), len(itr.decode)
-        pick_pre = range(n_pre) if full else (
-            [int(rng.integers(n_pre))] if n_pre else [])
-        pick_dec = range(n_dec) if full else (
-            sorted(set(rng.integers(n_dec, size=2).tolist())) if n_dec else [])
+        pick_pre = range(n_pre) if full else seeded_eighth(rng, n_pre)
+        pick_dec = range(n_dec) if full else seeded_eighth(rng, n_dec)
         if pick_pre:
             got = bf16_to_f64(pre_out)
             row0 = np.concatenate([[0], np.cumsum([wk.n for wk in itr.prefill])])
@@ -107,4 +112,4 @@ def test_continuous_batching_trace():
         ora.finish(itr)
     pkv.pkv_check_status(gpu.status)
     assert gpu.alloc.num_free_blocks() == ora.alloc.num_free()
-    assert checked_pre > 50 and checked_dec > 500
+    assert checked_pre > 100 and checked_dec > 9000
