@@ -647,8 +647,9 @@ def run_trace(args):
         dt.finish(itr)
         host_s += time.perf_counter() - h0
         ups.append(dt.upload(itr, meta))
-        pre_l, dec_l = meta["prefill"][1], meta["decode"][1]
-        chunks = np.diff(meta["cu"])
+        pre_l = dt.host_section(meta, "prefill_lens", meta["n_prefill"])
+        dec_l = dt.host_section(meta, "decode_lens", meta["n_decode"])
+        chunks = np.diff(dt.host_section(meta, "cu_q_lens", meta["n_prefill"] + 1))
         flops = 0
         for L, c in zip(pre_l.tolist(), chunks.tolist()):
             vis = c * (L - c) + c * (c + 1) // 2      # keys seen by the chunk's rows
@@ -674,9 +675,37 @@ def run_trace(args):
         pkv.pkv_check_status(run.status)
         return evs, t_all[0].elapsed_time(t_all[1])
 
+    def live_pass():
+        # The iteration loop a serving engine runs, host and GPU on one clock:
+        # per iteration the host does its allocator call and metadata build
+        # (pkv_iteration_prepare into a pinned staging buffer), one upload of
+        # the metadata and the launches, without waiting for the GPU; token
+        # values (in a model, outputs of the projections) are already on the
+        # device. Wall clock from the first host call to the last kernel's end.
+        run = DeviceTrace(cfg, partition_size=args.partition_size)
+        torch.cuda.synchronize()
+        host = 0.0
+        t0 = time.perf_counter()
+        for itr, up in zip(its, ups):
+            h0 = time.perf_counter()
+            meta = run.host_metadata(itr)
+            run.finish(itr)
+            live = run.upload_meta(meta, stream)
+            host += time.perf_counter() - h0
+            live.update(q=up["q"], n_pre=up["n_pre"])
+            if "k" in up:
+                live.update(k=up["k"], v=up["v"])
+            run.launch(live, stream=stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        pkv.pkv_check_status(run.status)
+        return 1e3 * wall, 1e3 * (host - run.wait_s)
+
     one_pass(False)                       # warm-up pass over the whole trace
+    live_pass()
     with ClockSampler(local) as clocks:
         evs, pass_ms = one_pass(True)
+        live_ms, live_host_ms = live_pass()
     t_app = sum(e[0].elapsed_time(e[1]) for e in evs)
     t_pre = sum(e[1].elapsed_time(e[2]) for e in evs)
     t_dec = sum(e[2].elapsed_time(e[3]) for e in evs)
@@ -712,6 +741,15 @@ def run_trace(args):
                         "iteration (the oracle needs about 2.3 s of one host core per full "
                         "iteration, about 8 minutes for all 200)",
         "host_scheduler_ms": 1e3 * host_s,
+        "iteration_loop": {
+            "tokens_per_s": tokens / (live_ms * 1e-3), "wall_ms": live_ms,
+            "ms_per_iteration": live_ms / len(its), "host_ms": live_host_ms,
+            "gpu_ms": gpu_ms,
+            "note": "host and GPU on one clock: per iteration one pkv_iteration_prepare call "
+                    "(slots, cu_q_lens, lengths, block tables into pinned memory), one "
+                    "metadata upload and the launches, the host waiting only for a free "
+                    "staging buffer (4 in a ring); host_ms is the host's own work in the loop "
+                    "(allocator, metadata, launches); token values resident on the device"},
         "roofline": {"bound": "hbm", "kernel": "pkv_paged_attention_decode", "achieved": dec_gbs,
                      "peak": peak_hbm, "unit": "GB/s", "frac": dec_gbs / peak_hbm,
                      "traffic": None},

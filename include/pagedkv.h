@@ -107,6 +107,50 @@ int pkv_num_free_blocks(pkv_alloc* a, int32_t* out);
 int pkv_build_block_tables(pkv_alloc* a, const int64_t* seqs, int32_t n, int32_t* tables_out,
                            int32_t max_blocks_per_seq, int32_t* lens_out);
 
+/* One iteration's host work in one call ("Batching, Scheduling, and Paging",
+ * section Continuous batching: the batch is rebuilt every iteration and the
+ * CPU work per iteration is overhead to keep small; "Deep Dive: continuous
+ * batching", section Iteration-level scheduling).
+ *   seqs[n], counts[n] (host), n = n_prefill + n_decode: works 0 ..
+ *     n_prefill-1 are prompt chunks (counts >= 1), the rest decodes (count
+ *     1). Each sequence at most once, none swapped out.
+ *   Every work gets its counts[i] slots as pkv_seq_append_slots would give
+ *   them, in order (the same blocks, the same copy-on-write pairs). The batch
+ *   is all or nothing: if the free blocks do not cover every work, nothing
+ *   changes, the call returns PKV_ENOMEM and *n_fit is the number of leading
+ *   works that would fit (evict, then call again). On success *n_fit = n.
+ *   buf (host memory the caller owns, e.g. pinned, of at least
+ *   layout->total_bytes as pkv_iteration_layout_bytes reports for the same
+ *   sizes) receives, at the layout's byte offsets, each section starting on a
+ *   64-byte boundary:
+ *     slot_mapping   int32 [n_tokens]   (prefill works first, then decodes)
+ *     cu_q_lens      int32 [n_prefill + 1]
+ *     prefill_lens   int32 [n_prefill]  (context lengths after the appends)
+ *     prefill_tables int32 [n_prefill][max_blocks_per_seq], padded with 0
+ *     decode_lens    int32 [n_decode]
+ *     decode_tables  int32 [n_decode][max_blocks_per_seq], padded with 0
+ *     cow_pairs      int32 [n_cow][2]  (run pkv_block_copy on them first)
+ *   so one host-to-device copy of the whole buffer feeds pkv_block_copy,
+ *   pkv_kv_append, pkv_paged_attention_prefill and pkv_paged_attention_decode.
+ *   PKV_EINVAL (nothing changed) for unknown, repeated or swapped-out
+ *   sequences, bad counts, a table longer than max_blocks_per_seq or a short
+ *   buf. */
+typedef struct pkv_iteration_layout {
+  int64_t slot_mapping, cu_q_lens, prefill_lens, prefill_tables, decode_lens, decode_tables,
+      cow_pairs;        /* byte offsets into buf */
+  int64_t total_bytes;  /* bytes of buf the layout covers */
+  int32_t n_tokens;     /* sum of counts */
+  int32_t n_cow;        /* copy-on-write pairs written */
+  int32_t max_q_len;    /* longest prompt chunk */
+  int32_t max_prefill_len, max_decode_len; /* longest context of each kind */
+} pkv_iteration_layout;
+int pkv_iteration_layout_bytes(int32_t n_prefill, int32_t n_decode, int32_t n_tokens,
+                               int32_t max_blocks_per_seq, pkv_iteration_layout* layout);
+int pkv_iteration_prepare(pkv_alloc* a, const int64_t* seqs, const int32_t* counts,
+                          int32_t n_prefill, int32_t n_decode, int32_t max_blocks_per_seq,
+                          void* buf, size_t buf_bytes, pkv_iteration_layout* layout,
+                          int32_t* n_fit);
+
 /* Preemption ("Batching, Scheduling, and Paging", section PagedAttention: if
  * HBM runs out a request is evicted, swapped to CPU memory or discarded and
  * recomputed later).

@@ -22,6 +22,14 @@ i32, i64, u64, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_f
 vp, sz = ctypes.c_void_p, ctypes.c_size_t
 P = ctypes.POINTER
 
+class IterationLayout(ctypes.Structure):
+    """``pkv_iteration_layout``: byte offsets of one iteration's metadata."""
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "slot_mapping", "cu_q_lens", "prefill_lens", "prefill_tables", "decode_lens",
+        "decode_tables", "cow_pairs", "total_bytes")] + [(n, ctypes.c_int32) for n in (
+        "n_tokens", "n_cow", "max_q_len", "max_prefill_len", "max_decode_len")]
+
+
 SIGNATURES = {
     "pkv_last_error": (ctypes.c_char_p, []),
     "pkv_version": (ctypes.c_int, []),
@@ -36,6 +44,9 @@ SIGNATURES = {
     "pkv_block_refcount": (ctypes.c_int, [vp, i32, P(i32)]),
     "pkv_num_free_blocks": (ctypes.c_int, [vp, P(i32)]),
     "pkv_build_block_tables": (ctypes.c_int, [vp, P(i64), i32, P(i32), i32, P(i32)]),
+    "pkv_iteration_layout_bytes": (ctypes.c_int, [i32, i32, i32, i32, P(IterationLayout)]),
+    "pkv_iteration_prepare": (ctypes.c_int, [vp, P(i64), P(i32), i32, i32, i32, vp, sz,
+                                             P(IterationLayout), P(i32)]),
     "pkv_seq_swap_out": (ctypes.c_int, [vp, i64, P(i32), i32, P(i32)]),
     "pkv_seq_swap_in": (ctypes.c_int, [vp, i64, P(i32), i32, P(i32)]),
     "pkv_seq_create_cached": (ctypes.c_int, [vp, P(i32), i32, P(i64), P(i32)]),

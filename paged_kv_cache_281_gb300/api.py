@@ -19,7 +19,7 @@ import ctypes
 import numpy as np
 import torch
 
-from ._lib import PagedKVError, check, lib
+from ._lib import IterationLayout, PagedKVError, check, lib
 
 __all__ = [
     "PagedKVError", "pkv_version", "pkv_last_error", "BlockAllocator",
@@ -29,7 +29,7 @@ __all__ = [
     "pkv_paged_attention_prefill", "pkv_status_reset", "pkv_check_status",
     "pkv_debug_set_wait", "new_status", "new_fp8_pools", "pkv_kv_append_fp8",
     "pkv_paged_attention_decode_fp8", "pkv_decode_shared_workspace_bytes",
-    "pkv_paged_attention_decode_shared",
+    "pkv_paged_attention_decode_shared", "IterationLayout", "iteration_layout_bytes",
 ]
 
 
@@ -208,6 +208,49 @@ class BlockAllocator:
             tables.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(max_blocks_per_seq),
             lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
         return tables[:n], lens[:n]
+
+    def iteration_prepare(self, seqs, counts, n_prefill: int, max_blocks_per_seq: int, buf):
+        """``pkv_iteration_prepare``: every work's appends and the iteration's
+        metadata in one call. ``seqs``/``counts`` list the prompt chunks first
+        (``n_prefill`` of them), then the decodes (count 1). ``buf`` is a
+        host buffer (a numpy array or a CPU, e.g. pinned, torch tensor) of at
+        least ``iteration_layout_bytes(...).total_bytes`` bytes. Returns the
+        layout; raises PagedKVError (PKV_ENOMEM, nothing changed) with
+        ``n_fit`` set to the number of leading works that would fit."""
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        cnt = np.ascontiguousarray(counts, dtype=np.int32)
+        n = int(ids.shape[0])
+        if cnt.shape[0] != n or not 0 <= n_prefill <= n:
+            raise ValueError("seqs and counts must have the same length >= n_prefill")
+        if isinstance(buf, torch.Tensor):
+            if buf.is_cuda or not buf.is_contiguous():
+                raise ValueError("buf must be contiguous host memory")
+            addr, nbytes = buf.data_ptr(), buf.numel() * buf.element_size()
+        else:
+            if not buf.flags["C_CONTIGUOUS"] or not buf.flags["WRITEABLE"]:
+                raise ValueError("buf must be a writable contiguous array")
+            addr, nbytes = buf.ctypes.data, buf.nbytes
+        layout, fit = IterationLayout(), ctypes.c_int32()
+        rc = lib().pkv_iteration_prepare(
+            self._h, ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+            cnt.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(n_prefill),
+            n - int(n_prefill), int(max_blocks_per_seq), addr, nbytes, ctypes.byref(layout),
+            ctypes.byref(fit))
+        if rc != 0:
+            err = PagedKVError(rc, pkv_last_error())
+            err.n_fit = fit.value
+            raise err
+        return layout
+
+
+def iteration_layout_bytes(n_prefill: int, n_decode: int, n_tokens: int,
+                           max_blocks_per_seq: int) -> IterationLayout:
+    """``pkv_iteration_layout_bytes``: offsets and size of one iteration's
+    metadata buffer."""
+    layout = IterationLayout()
+    check(lib().pkv_iteration_layout_bytes(int(n_prefill), int(n_decode), int(n_tokens),
+                                           int(max_blocks_per_seq), ctypes.byref(layout)))
+    return layout
 
 
 # ---------------------------------------------------------------- GPU calls

@@ -458,3 +458,149 @@ extern "C" int pkv_seq_swap_in(pkv_alloc* a, int64_t seq, int32_t* blocks_out, i
   *n = m;
   return ok();
 }
+
+// ---------------------------------------------------------------------------
+// One iteration's host work in one call ("Batching, Scheduling, and Paging",
+// section Continuous batching: the batch is rebuilt every iteration, and the
+// CPU-side work per iteration is the overhead to keep small; "Deep Dive:
+// continuous batching", section Iteration-level scheduling). The appends keep
+// the per-sequence rules of append_impl; the batch is all or nothing: a
+// dry run over the whole list (including the refcounts that earlier copies
+// in the same batch release) decides before anything changes.
+
+namespace {
+
+constexpr int64_t kMetaAlign = 64;  // bytes; every section starts on a line
+
+int64_t align_up(int64_t x) { return (x + kMetaAlign - 1) / kMetaAlign * kMetaAlign; }
+
+int layout_impl(int32_t n_prefill, int32_t n_decode, int64_t n_tokens,
+                int32_t max_blocks_per_seq, pkv_iteration_layout* L, const char* who) {
+  PKV_REQUIRE(L, "%s: layout is NULL", who);
+  PKV_REQUIRE(n_prefill >= 0 && n_decode >= 0 && n_tokens >= 0 && max_blocks_per_seq > 0,
+              "%s: bad sizes", who);
+  const int64_t n = (int64_t)n_prefill + n_decode;
+  const int64_t W = max_blocks_per_seq;
+  int64_t off = 0;
+  std::memset(L, 0, sizeof(*L));
+  L->slot_mapping = off;   off = align_up(off + 4 * n_tokens);
+  L->cu_q_lens = off;      off = align_up(off + 4 * ((int64_t)n_prefill + 1));
+  L->prefill_lens = off;   off = align_up(off + 4 * (int64_t)n_prefill);
+  L->prefill_tables = off; off = align_up(off + 4 * (int64_t)n_prefill * W);
+  L->decode_lens = off;    off = align_up(off + 4 * (int64_t)n_decode);
+  L->decode_tables = off;  off = align_up(off + 4 * (int64_t)n_decode * W);
+  L->cow_pairs = off;      off = align_up(off + 8 * n);
+  L->total_bytes = off;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_iteration_layout_bytes(int32_t n_prefill, int32_t n_decode,
+                                          int32_t n_tokens, int32_t max_blocks_per_seq,
+                                          pkv_iteration_layout* layout) {
+  if (int rc = layout_impl(n_prefill, n_decode, n_tokens, max_blocks_per_seq, layout,
+                           "pkv_iteration_layout_bytes"))
+    return rc;
+  return ok();
+}
+
+extern "C" int pkv_iteration_prepare(pkv_alloc* a, const int64_t* seqs, const int32_t* counts,
+                                     int32_t n_prefill, int32_t n_decode,
+                                     int32_t max_blocks_per_seq, void* buf, size_t buf_bytes,
+                                     pkv_iteration_layout* layout, int32_t* n_fit) {
+  const char* who = "pkv_iteration_prepare";
+  PKV_REQUIRE(a && layout && n_fit, "%s: NULL argument", who);
+  PKV_REQUIRE(n_prefill >= 0 && n_decode >= 0, "%s: bad sizes", who);
+  const int32_t n = n_prefill + n_decode;
+  PKV_REQUIRE(n == 0 || (seqs && counts), "%s: NULL array", who);
+  PKV_REQUIRE(buf, "%s: buf is NULL", who);
+  const int32_t B = a->block_size;
+  // validate every work and dry-run the block needs, in order
+  int64_t n_tokens = 0, need = 0;
+  int32_t fit = n;
+  std::unordered_map<int64_t, int32_t> seen;
+  std::unordered_map<int32_t, int32_t> released;  // refs dropped by earlier copies
+  seen.reserve(2 * (size_t)n);
+  for (int32_t i = 0; i < n; ++i) {
+    pkv_alloc::Seq* s = a->find(seqs[i]);
+    PKV_REQUIRE(s, "%s: unknown sequence %lld (work %d)", who, (long long)seqs[i], i);
+    PKV_REQUIRE(!s->swapped, "%s: sequence %lld is swapped out", who, (long long)seqs[i]);
+    PKV_REQUIRE(seen.emplace(seqs[i], i).second, "%s: sequence %lld appears twice", who,
+                (long long)seqs[i]);
+    const int32_t c = counts[i];
+    PKV_REQUIRE(i < n_prefill ? c >= 1 : c == 1,
+                "%s: work %d: a prefill chunk needs >= 1 token and a decode exactly 1 (got %d)",
+                who, i, c);
+    const int64_t new_len = (int64_t)s->len + c;
+    PKV_REQUIRE(new_len < (int64_t(1) << 31), "%s: sequence length overflows int32", who);
+    PKV_REQUIRE((new_len + B - 1) / B <= max_blocks_per_seq,
+                "%s: sequence %lld would need %lld blocks > max_blocks_per_seq %d", who,
+                (long long)seqs[i], (long long)((new_len + B - 1) / B), max_blocks_per_seq);
+    bool cow = false;
+    if (s->len % B != 0) {
+      const int32_t last = s->blocks.back();
+      auto it = released.find(last);
+      const int32_t refs = a->refcount[last] - (it == released.end() ? 0 : it->second);
+      if (refs > 1) {
+        cow = true;
+        ++released[last];
+      }
+    }
+    need += (new_len + B - 1) / B - (int64_t)s->blocks.size() + (cow ? 1 : 0);
+    if (need > a->count && fit == n) fit = i;
+    n_tokens += c;
+  }
+  PKV_REQUIRE(n_tokens < (int64_t(1) << 31), "%s: too many tokens", who);
+  if (int rc = layout_impl(n_prefill, n_decode, n_tokens, max_blocks_per_seq, layout, who))
+    return rc;
+  PKV_REQUIRE(buf_bytes >= (size_t)layout->total_bytes, "%s: buf has %zu bytes, needs %lld", who,
+              buf_bytes, (long long)layout->total_bytes);
+  *n_fit = fit;
+  if (fit < n)
+    return fail(PKV_ENOMEM,
+                "%s: the batch needs %lld free blocks, %d free; the first %d works fit", who,
+                (long long)need, a->count, fit);
+  // apply: cannot fail any more
+  uint8_t* base = static_cast<uint8_t*>(buf);
+  int32_t* slots = reinterpret_cast<int32_t*>(base + layout->slot_mapping);
+  int32_t* cu = reinterpret_cast<int32_t*>(base + layout->cu_q_lens);
+  int32_t* pairs = reinterpret_cast<int32_t*>(base + layout->cow_pairs);
+  int32_t n_cow = 0, max_q = 0;
+  cu[0] = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    int32_t got_cow = 0;
+    append_impl(a, seqs[i], counts[i], nullptr, slots, pairs + 2 * n_cow, &got_cow, who);
+    slots += counts[i];
+    n_cow += got_cow;
+    if (i < n_prefill) {
+      cu[i + 1] = cu[i] + counts[i];
+      if (counts[i] > max_q) max_q = counts[i];
+    }
+  }
+  const int64_t W = max_blocks_per_seq;
+  int32_t max_len[2] = {0, 0};
+  for (int32_t part = 0; part < 2; ++part) {
+    const int32_t first = part == 0 ? 0 : n_prefill;
+    const int32_t count = part == 0 ? n_prefill : n_decode;
+    int32_t* lens = reinterpret_cast<int32_t*>(
+        base + (part == 0 ? layout->prefill_lens : layout->decode_lens));
+    int32_t* tables = reinterpret_cast<int32_t*>(
+        base + (part == 0 ? layout->prefill_tables : layout->decode_tables));
+    for (int32_t k = 0; k < count; ++k) {
+      const pkv_alloc::Seq* s = a->find(seqs[first + k]);
+      int32_t* row = tables + k * W;
+      const int32_t m = (int32_t)s->blocks.size();
+      if (m) std::memcpy(row, s->blocks.data(), sizeof(int32_t) * m);
+      for (int64_t j = m; j < W; ++j) row[j] = 0;
+      lens[k] = s->len;
+      if (s->len > max_len[part]) max_len[part] = s->len;
+    }
+  }
+  layout->n_tokens = (int32_t)n_tokens;
+  layout->n_cow = n_cow;
+  layout->max_q_len = max_q;
+  layout->max_prefill_len = max_len[0];
+  layout->max_decode_len = max_len[1];
+  return ok();
+}

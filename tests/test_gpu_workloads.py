@@ -87,7 +87,8 @@ def test_continuous_batching_trace():
     for itr in trace_iterations(cfg):
         meta = gpu.host_metadata(itr)
         slots = ora.step(itr)
-        assert np.array_equal(meta["slots"], slots), f"iteration {itr.index}: slots differ"
+        got_slots = gpu.host_section(meta, "slot_mapping", itr.num_tokens)
+        assert np.array_equal(got_slots, slots), f"iteration {itr.index}: slots differ"
         pre_out, dec_out = gpu.run_iteration(itr, meta)
         full = itr.index % 10 == 0
         n_pre, n_dec = len(itr.prefill), len(itr.decode)

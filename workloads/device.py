@@ -8,6 +8,7 @@ attention, and nothing here touches the oracle.
 
 from __future__ import annotations
 
+import time
 from dataclasses import dataclass
 
 import numpy as np
@@ -229,11 +230,15 @@ def decode_shared_grouped(w, d: DeviceSharedPrefix, groups=None, partition_size=
 # ---------------------------------------------------------------- trace
 
 class DeviceTrace:
-    """Runs the continuous-batching trace through the library: per iteration,
-    the allocator reserves slots (new blocks only when the last one fills),
-    ``kv_append`` writes every new token, prefill attends for the prompt
-    chunks and decode for the running sequences, and finished requests free
-    their blocks."""
+    """Runs the continuous-batching trace through the library. Per iteration
+    one call (``pkv_iteration_prepare``) reserves every work's slots (new
+    blocks only when the last one fills) and writes the slot mapping, prompt
+    offsets, context lengths and block tables into a pinned staging buffer;
+    one host-to-device copy uploads it; ``kv_append`` writes every new
+    token, prefill attends for the prompt chunks and decode for the running
+    sequences; finished requests free their blocks."""
+
+    RING = 4  # pinned staging buffers the host may fill ahead of the GPU
 
     def __init__(self, cfg, device="cuda", partition_size=0):
         self.cfg = cfg
@@ -253,42 +258,75 @@ class DeviceTrace:
         self.pws = torch.empty(pkv.pkv_prefill_workspace_bytes(
             cfg.max_running, cfg.max_running * cfg.chunk, cfg.Hq, cfg.D),
             dtype=torch.uint8, device=device)
+        cap = pkv.iteration_layout_bytes(cfg.max_running, cfg.max_running,
+                                         cfg.max_running * cfg.chunk, self.max_blocks).total_bytes
+        self.staging = [torch.empty(cap, dtype=torch.uint8).pin_memory()
+                        for _ in range(self.RING)]
+        self.staged = [None] * self.RING   # event after the last upload from each buffer
+        self.next = 0
+        self.wait_s = 0.0                   # host time spent waiting for a free buffer
 
     def host_metadata(self, itr):
-        """Allocator work and metadata for one iteration (host side)."""
+        """The iteration's host side: new sequences for admitted requests,
+        then one library call for every work's slots and the metadata."""
         for rid in itr.admitted:
             self.sid[rid] = self.alloc.seq_create()
-        slots = []
-        for wk in itr.work:
-            sl, pair = self.alloc.seq_append_slots(self.sid[wk.rid], wk.n)
-            assert pair is None
-            slots.append(sl)
-        pre, dec = itr.prefill, itr.decode
-        meta = {"slots": np.concatenate(slots).astype(np.int32) if slots else
-                np.zeros(0, np.int32)}
-        for name, works in (("prefill", pre), ("decode", dec)):
-            ids = [self.sid[wk.rid] for wk in works]
-            tables, lens = self.alloc.build_block_tables(ids, self.max_blocks)
-            meta[name] = (tables, lens)
-        meta["cu"] = np.concatenate([[0], np.cumsum([wk.n for wk in pre])]).astype(np.int32)
-        return meta
+        k = self.next
+        self.next = (k + 1) % self.RING
+        if self.staged[k] is not None:
+            w0 = time.perf_counter()
+            self.staged[k].synchronize()    # its previous upload has left the buffer
+            self.wait_s += time.perf_counter() - w0
+            self.staged[k] = None
+        work = itr.work
+        layout = self.alloc.iteration_prepare([self.sid[w.rid] for w in work],
+                                              [w.n for w in work], len(itr.prefill),
+                                              self.max_blocks, self.staging[k])
+        return {"staging": k, "layout": layout, "n_prefill": len(itr.prefill),
+                "n_decode": len(work) - len(itr.prefill)}
 
-    def upload(self, itr, meta):
-        """Host -> device copies of one iteration's inputs and metadata."""
+    def host_section(self, meta, name, count):
+        """A host view of one section of the staged metadata (int32)."""
+        off = getattr(meta["layout"], name)
+        return self.staging[meta["staging"]][off:off + 4 * count].numpy().view(np.int32)
+
+    def upload_meta(self, meta, stream=None):
+        """One host-to-device copy of the staged metadata; returns the device
+        buffer and the launch arguments read from the layout."""
+        L, k = meta["layout"], meta["staging"]
+        stream = stream or torch.cuda.current_stream()
+        n = int(L.total_bytes)
+        buf = torch.empty(n, dtype=torch.uint8, device=self.device)
+        with torch.cuda.stream(stream):
+            buf.copy_(self.staging[k][:n], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+        self.staged[k] = ev
+        W = self.max_blocks
+        sec = lambda name, count: buf[getattr(L, name):getattr(L, name) + 4 * count].view(
+            torch.int32)
+        npre, ndec = meta["n_prefill"], meta["n_decode"]
+        up = {"meta": buf, "n_pre": 0}
+        if L.n_tokens:
+            up["slots"] = sec("slot_mapping", L.n_tokens)
+        if npre:
+            up["pre"] = (sec("cu_q_lens", npre + 1), sec("prefill_lens", npre),
+                         sec("prefill_tables", npre * W).view(npre, W), int(L.max_q_len),
+                         int(L.max_prefill_len))
+        if ndec:
+            up["dec"] = (sec("decode_lens", ndec), sec("decode_tables", ndec * W).view(ndec, W),
+                         int(L.max_decode_len), ndec)
+        return up
+
+    def upload(self, itr, meta, stream=None):
+        """Host -> device copies of one iteration's metadata and token values."""
         dev = self.device
-        t = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-        up = {"q": to_dev_bf16(np.ascontiguousarray(itr.q), dev), "n_pre": int(meta["cu"][-1])}
+        up = self.upload_meta(meta, stream)
+        up["q"] = to_dev_bf16(np.ascontiguousarray(itr.q), dev)
+        up["n_pre"] = sum(w.n for w in itr.prefill)
         if itr.num_tokens:
             up["k"] = to_dev_bf16(np.ascontiguousarray(itr.k), dev)
             up["v"] = to_dev_bf16(np.ascontiguousarray(itr.v), dev)
-            up["slots"] = t(meta["slots"])
-        tables, lens = meta["prefill"]
-        if len(lens):
-            up["pre"] = (t(meta["cu"]), t(lens), t(tables), int(np.diff(meta["cu"]).max()),
-                         int(lens.max()))
-        tables, lens = meta["decode"]
-        if len(lens):
-            up["dec"] = (t(lens), t(tables), int(lens.max()), len(lens))
         return up
 
     def launch(self, up, stream=None, events=None):
@@ -297,7 +335,7 @@ class DeviceTrace:
         cfg, dev = self.cfg, self.device
         rec = (lambda i: events[i].record(stream)) if events else (lambda i: None)
         rec(0)
-        if "k" in up:
+        if "slots" in up:
             pkv.pkv_kv_append(up["k"], up["v"], up["slots"], self.k_cache, self.v_cache,
                               status=self.status, stream=stream)
         rec(1)
@@ -322,7 +360,7 @@ class DeviceTrace:
 
     def run_iteration(self, itr, meta, stream=None):
         """Upload and run one iteration; returns (prefill_out, decode_out)."""
-        return self.launch(self.upload(itr, meta), stream=stream)
+        return self.launch(self.upload(itr, meta, stream), stream=stream)
 
     def finish(self, itr):
         for rid in itr.finished:
