@@ -67,24 +67,37 @@ struct CopyArgs {
   int32_t* status;
 };
 
-// blockIdx.y picks the pair, blockIdx.z the pool (0 keys, 1 values);
-// blockIdx.x strides over the block's vectors.
+// One CTA per (pair, pool): blockIdx.x picks the pair, blockIdx.y the pool
+// (0 keys, 1 values). Each thread moves up to eight 16-byte vectors per pass,
+// all loads issued before the stores, so a CTA keeps a whole 32 KB block
+// (8 heads, B = 16, D = 128) in flight.
 __global__ void __launch_bounds__(256) block_copy_kernel(const CopyArgs a) {
-  const int32_t p = blockIdx.y;
+  const int32_t p = blockIdx.x;
   const int32_t src = __ldg(a.pairs + 2 * p);
   const int32_t dst = __ldg(a.pairs + 2 * p + 1);
   if (src < 0 || src >= a.num_blocks || dst < 0 || dst >= a.num_blocks) {
-    if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+    if (blockIdx.y == 0 && threadIdx.x == 0)
       record_status(a.status, PKV_EDEVICE, (src < 0 || src >= a.num_blocks) ? src : dst,
                     kKernelBlockCopy);
     return;
   }
-  uint4* pool = blockIdx.z == 0 ? a.k_cache : a.v_cache;
+  uint4* pool = blockIdx.y == 0 ? a.k_cache : a.v_cache;
   const uint4* s = pool + (int64_t)src * a.vec_per_block;
   uint4* d = pool + (int64_t)dst * a.vec_per_block;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < a.vec_per_block;
-       i += (int64_t)gridDim.x * blockDim.x)
-    d[i] = s[i];
+  constexpr int kUnroll = 8;
+  for (int64_t i0 = 0; i0 < a.vec_per_block; i0 += kUnroll * 256) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = i0 + u * 256 + threadIdx.x;
+      if (i < a.vec_per_block) v[u] = __ldg(s + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = i0 + u * 256 + threadIdx.x;
+      if (i < a.vec_per_block) d[i] = v[u];
+    }
+  }
 }
 
 struct SwapArgs {
@@ -121,7 +134,7 @@ __global__ void __launch_bounds__(256) swap_blocks_kernel(const SwapArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// kv_append into FP8 (e4m3) pages. One warp per (token, head, tensor) row:
+// kv_append into FP8 (e4m3) pages. Per (token, head, tensor) row:
 // the row's largest magnitude amax sets scale = amax / 448 and the codes
 // e4m3(x * (448 / amax)) (fp32 quotients and product, round to nearest even,
 // saturating); a row of zeros gets scale 0 and zero codes. Codes land in
@@ -150,57 +163,69 @@ __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
   return r;
 }
 
+// Eight lanes per row: each lane holds D / 8 consecutive elements (16-byte
+// loads), the row's amax is a reduction over its eight lanes, and each lane
+// stores its D / 8 codes at once. A warp covers four rows per pass.
 template <int D>
 __global__ void __launch_bounds__(256) kv_append_fp8_kernel(const AppendFp8Args a) {
   grid_dep_launch();  // as in kv_append_kernel
-  constexpr int E = D / 32;  // elements per lane: 4 (D=128) or 2 (D=64)
-  const int lane = threadIdx.x & 31;
+  constexpr int E = D / 8;    // elements per lane: 16 (D=128) or 8 (D=64)
+  constexpr int V = E / 8;    // 16-byte input vectors per lane
+  const int sub = threadIdx.x & 7;
   const int64_t rows = (int64_t)a.T * a.Hkv * 2;
-  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; w < rows;
-       w += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 3; w < rows;
+       w += ((int64_t)gridDim.x * blockDim.x) >> 3) {
     const int which = (int)(w & 1);           // 0 keys, 1 values
     const int64_t th = w >> 1;
     const int32_t t = (int32_t)(th / a.Hkv);
     const int32_t h = (int32_t)(th - (int64_t)t * a.Hkv);
     const int32_t slot = __ldg(a.slot_mapping + t);
-    if (slot < 0) continue;
-    if (slot >= a.num_slots) {
-      if (h == 0 && which == 0 && lane == 0)
-        record_status(a.status, PKV_EDEVICE, slot, kKernelAppend);
-      continue;
-    }
-    const __nv_bfloat16* src = (which ? a.v_new : a.k_new) + ((int64_t)t * a.Hkv + h) * D + lane * E;
+    // the eight lanes of a row share t, h and slot: every branch below is
+    // uniform across the row's lanes, so the row's shuffles stay converged
+    const bool skip = slot < 0 || slot >= a.num_slots;
+    if (slot >= a.num_slots && h == 0 && which == 0 && sub == 0)
+      record_status(a.status, PKV_EDEVICE, slot, kKernelAppend);
+    const unsigned group = 0xffu << (threadIdx.x & 24);
+    if (skip) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        (which ? a.v_new : a.k_new) + ((int64_t)t * a.Hkv + h) * D + sub * E);
+    uint4 u[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) u[k] = __ldg(src + k);
     float x[E];
-    if constexpr (E == 4) {
-      const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
-      x[0] = bf16_lo_to_f32(u.x);
-      x[1] = bf16_hi_to_f32(u.x);
-      x[2] = bf16_lo_to_f32(u.y);
-      x[3] = bf16_hi_to_f32(u.y);
-    } else {
-      const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(src));
-      x[0] = bf16_lo_to_f32(u);
-      x[1] = bf16_hi_to_f32(u);
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const uint32_t wv[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[8 * k + 2 * e] = bf16_lo_to_f32(wv[e]);
+        x[8 * k + 2 * e + 1] = bf16_hi_to_f32(wv[e]);
+      }
     }
     float amax = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(group, amax, off));
     const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
     const int32_t blk = slot / a.block_size;
     const int32_t off = slot - blk * a.block_size;
     const int64_t row = ((int64_t)blk * a.Hkv + h) * a.block_size + off;
-    uint8_t* dst = (which ? a.v8 : a.k8) + row * D + lane * E;
-    if constexpr (E == 4) {
-      const uint32_t c01 = e4m3x2_from_f32(__fmul_rn(x[0], inv), __fmul_rn(x[1], inv));
-      const uint32_t c23 = e4m3x2_from_f32(__fmul_rn(x[2], inv), __fmul_rn(x[3], inv));
-      *reinterpret_cast<uint32_t*>(dst) = c01 | (c23 << 16);
-    } else {
-      const uint32_t c01 = e4m3x2_from_f32(__fmul_rn(x[0], inv), __fmul_rn(x[1], inv));
-      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)c01;
+    uint32_t c[E / 4];
+#pragma unroll
+    for (int k = 0; k < E / 4; ++k) {
+      const uint32_t c01 =
+          e4m3x2_from_f32(__fmul_rn(x[4 * k], inv), __fmul_rn(x[4 * k + 1], inv));
+      const uint32_t c23 =
+          e4m3x2_from_f32(__fmul_rn(x[4 * k + 2], inv), __fmul_rn(x[4 * k + 3], inv));
+      c[k] = c01 | (c23 << 16);
     }
-    if (lane == 0) (which ? a.vs : a.ks)[row] = __fdiv_rn(amax, 448.f);
+    uint8_t* dst = (which ? a.v8 : a.k8) + row * D + sub * E;
+    if constexpr (E == 16)
+      *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[2], c[3]);
+    else
+      *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[1]);
+    if (sub == 0) (which ? a.vs : a.ks)[row] = __fdiv_rn(amax, 448.f);
   }
 }
 
@@ -297,7 +322,7 @@ extern "C" int pkv_kv_append_fp8(const void* k_new, const void* v_new,
   a.block_size = block_size;
   a.status = dev_status;
   const int64_t rows = (int64_t)T * Hkv * 2;
-  const int64_t want = (rows + 7) / 8;  // 8 warps per CTA
+  const int64_t want = (rows + 31) / 32;  // 32 rows per CTA of 256 threads
   const int64_t cap = (int64_t)dev->sm_count * 8;
   const int grid = (int)(want < cap ? want : cap);
   if (D == 128)
@@ -312,7 +337,7 @@ extern "C" int pkv_block_copy(void* k_cache, void* v_cache, const int32_t* pairs
                               int32_t num_blocks, int32_t Hkv, int32_t D, int32_t block_size,
                               int32_t* dev_status, void* stream) {
   if (int rc = check_shape(Hkv, D, block_size, "pkv_block_copy")) return rc;
-  PKV_REQUIRE(n >= 0 && n <= 65535, "pkv_block_copy: n must be in [0, 65535] (got %d)", n);
+  PKV_REQUIRE(n >= 0, "pkv_block_copy: n must be >= 0 (got %d)", n);
   PKV_REQUIRE(num_blocks > 0, "pkv_block_copy: num_blocks must be > 0");
   if (n == 0) return ok();
   PKV_REQUIRE(k_cache && v_cache && pairs, "pkv_block_copy: NULL pointer");
@@ -328,9 +353,7 @@ extern "C" int pkv_block_copy(void* k_cache, void* v_cache, const int32_t* pairs
   a.num_blocks = num_blocks;
   a.vec_per_block = (int64_t)Hkv * block_size * D / 8;
   a.status = dev_status;
-  int64_t per_block = (a.vec_per_block + 255) / 256;
-  if (per_block > 16) per_block = 16;
-  dim3 grid((unsigned)per_block, (unsigned)n, 2);
+  dim3 grid((unsigned)n, 2);
   block_copy_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
   if (int rc = check_launch("pkv_block_copy")) return rc;
   return ok();

@@ -11,28 +11,29 @@
 // How (GB300 design). A Q tile is 128 rows, each row a (query, head) pair:
 // 128/G consecutive queries times the G query heads that share one kv head,
 // so every key/value tile loaded serves all of them. A work item is (sequence,
-// query group, kv head) with NQ Q tiles (one in the launcher); large launches run a plan
-// kernel and a persistent grid that takes items from an atomic ticket (the
-// producer posts them to the other warps through a small ring), small ones
-// one CTA per item. The warps specialise and run as a pipeline over 64-key
-// tiles:
-//  * warp 0 (producer) loads Q by 3-D TMA boxes and streams K and V tiles
-//    into rings of NS stages: page numbers come from a block-table window in
-//    shared memory, and in one pass lanes 0-7 issue the boxes of key tile j
-//    and lanes 8-15 those of value tile j - 1, one 4-D box per page holding
-//    all its rows and both 64-column halves (tiles sit in shared memory as
-//    [8-row group][half][8 rows x 128 B], 128-byte swizzled);
-//  * warp 1 runs the tensor core (issue under elect.sync): S_j = Q K_j^T into
-//    one of two TMEM score buffers per Q tile, then O += P_{j-1} V_{j-1}, so
-//    the scores of the next tile are computed while the softmax works on the
-//    current one; it also zeroes the value rows past the last visible key
-//    before the product (they may hold stale or poisoned bytes, and 0 * NaN
-//    is NaN);
+// query group, kv head) with two Q tiles; large launches run a plan kernel
+// and a persistent grid (one CTA per SM) that takes items from an atomic
+// ticket (the producer posts them to the other warps through a small ring),
+// small ones one CTA per item. The warps specialise and run as a pipeline
+// over 128-key tiles:
+//  * warp 0 (producer) loads each Q tile by 3-D TMA boxes and streams K and V
+//    tiles into two-stage rings: page numbers come from a block-table window
+//    in shared memory, and in one pass lanes 0-15 issue the boxes of key tile
+//    j and lanes 16-31 those of value tile j - 1, one 4-D box per page
+//    holding all its rows and both 64-column halves (tiles sit in shared
+//    memory as [8-row group][half][8 rows x 128 B], 128-byte swizzled);
+//  * warp 1 runs the tensor core (issue under elect.sync). The two Q tiles
+//    take turns: S_t = Q_t K_j^T (128 x 128 per tile, one score buffer per
+//    tile in tensor memory), then O_t += P_t V_j as soon as tile t's
+//    probabilities are ready, then S_t of the next key tile, so one tile's
+//    products run while the other tile's softmax works. It also zeroes the
+//    value rows past the last visible key before the product (they may hold
+//    stale or poisoned bytes, and 0 * NaN is NaN);
 //  * eight softmax warps per Q tile share each TMEM lane (= row) between two
-//    threads, one per key half: they read the scores, apply the causal
+//    threads, one per 64-key half: they read the scores, apply the causal
 //    limit, exchange the row maxima, keep a running sum against a reference
 //    maximum (base 2, packed f32x2 arithmetic), and write the probabilities
-//    back into the same TMEM columns as two bf16 parts P_hi + P_lo (~fp32
+//    back over their own score columns as two bf16 parts P_hi + P_lo (~fp32
 //    precision for the product), which the P V MMA reads as its A operand
 //    straight from tensor memory. O is rescaled (in TMEM) only when a row's
 //    maximum grows by more than 2^8, so the stored probabilities stay below
@@ -52,7 +53,8 @@ namespace pkv {
 namespace {
 
 constexpr int kRows = 128;       // (query, head) rows per Q tile = TMEM lanes
-constexpr int kKeys = 64;        // keys per KV tile
+constexpr int kKeys = 128;       // keys per K/V tile = columns of a score tile
+constexpr int kNS = 2;           // K and V ring stages
 // K and V tiles sit in shared memory as [8-row group][64-column half][8 rows
 // x 128 B] (128-byte swizzled), so that one TMA box brings a whole page (both
 // halves) and the tensor core still sees equal strides between 8-row groups
@@ -60,37 +62,39 @@ constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows past 2^8
 constexpr int kWin = 256;            // block-table entries held in shared memory
 constexpr int kItemRing = 4;         // work-item indices handed from the producer to the others
 
-// NQ Q tiles per CTA share every K/V tile: two (one CTA per SM, all 512 TMEM
-// columns) halve the K/V traffic per row; one (two CTAs per SM) lets a CTA's
-// start and end overlap the other's work. The launcher uses one (measured
-// faster); two remain a compile-time variant.
-template <int D, int NS, int NQ>
+// Two Q tiles per CTA share every K/V tile and take turns on the tensor
+// core: while the softmax warps of one tile turn its scores into
+// probabilities, the tensor core computes the other tile's products. Tensor
+// memory (512 columns, the whole SM's) holds per tile t, at column 256 t, the
+// score tile S_t (128 columns, overwritten in place by the probabilities as
+// bf16 hi and lo parts) and the output accumulator O_t (D columns).
+template <int D>
 struct PCfg {
-  static constexpr int kThreads = 64 + 256 * NQ;  // producer, MMA, eight softmax warps per tile
-  static constexpr uint32_t kQHalf = NQ * kRows * 128;  // one 64-column half of the Q tiles
+  static constexpr int kThreads = 64 + 512;  // producer, MMA, eight softmax warps per Q tile
   static constexpr int kHalves = D / 64;
-  static constexpr uint32_t kGroup = kHalves * 1024;  // one 8-row group of a K or V tile
+  static constexpr uint32_t kQHalf = kRows * 128;          // one 64-column half of a Q tile
+  static constexpr uint32_t kQTile = kHalves * kQHalf;
+  static constexpr uint32_t kGroup = kHalves * 1024;       // one 8-row group of a K or V tile
   static constexpr uint32_t kStage = (kKeys / 8) * kGroup;
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kHalves * kQHalf;
-  static constexpr uint32_t kV = kK + NS * kStage;
-  static constexpr uint32_t kBytes = kV + NS * kStage;
-  // + alignment slack; padded so that at most 2 / NQ CTAs share an SM: their
-  // TMEM allocations (256 NQ columns each) always fit and never wait
-  static constexpr uint32_t kMinSmem = NQ == 2 ? 116u * 1024 : 80u * 1024;
+  static constexpr uint32_t kK = kQ + 2 * kQTile;
+  static constexpr uint32_t kV = kK + kNS * kStage;
+  static constexpr uint32_t kBytes = kV + kNS * kStage;
+  // + alignment slack; padded so that one CTA holds an SM: its tensor memory
+  // allocation (all 512 columns) then never waits for another CTA's
+  static constexpr uint32_t kMinSmem = 120u * 1024;
   static constexpr uint32_t kSmem = kBytes + 1024 > kMinSmem ? kBytes + 1024 : kMinSmem;
-  // barriers: Q; K full/empty and V full/empty per stage; per Q tile and
-  // buffer: S full, P full, PV done, row maxima exchanged; per Q tile: row
-  // sums exchanged, output read out (O free); Q free; work item posted /
-  // taken per item-ring slot; final
-  static constexpr int kBarQ = 0, kBarKF = 1, kBarKE = 1 + NS, kBarVF = 1 + 2 * NS,
-                       kBarVE = 1 + 3 * NS, kBarSF = 1 + 4 * NS, kBarPF = kBarSF + 2 * NQ,
-                       kBarPV = kBarPF + 2 * NQ, kBarX = kBarPV + 2 * NQ, kBarL = kBarX + 2 * NQ,
-                       kBarOE = kBarL + NQ, kBarQE = kBarOE + NQ, kBarIF = kBarQE + 1,
+  // barriers: per Q tile full / free; K full/empty and V full/empty per
+  // stage; per Q tile: S full, P full (256 arrivals), P V done, row maxima
+  // exchanged (256), row sums exchanged (256), output read out (256); work
+  // item posted / taken per item-ring slot; final
+  static constexpr int kBarQF = 0, kBarQE = 2, kBarKF = 4, kBarKE = kBarKF + kNS,
+                       kBarVF = kBarKE + kNS, kBarVE = kBarVF + kNS, kBarSF = kBarVE + kNS,
+                       kBarPF = kBarSF + 2, kBarPV = kBarPF + 2, kBarX = kBarPV + 2,
+                       kBarL = kBarX + 2, kBarOE = kBarL + 2, kBarIF = kBarOE + 2,
                        kBarIE = kBarIF + kItemRing, kBarFin = kBarIE + kItemRing,
                        kNumBars = kBarFin + 1;
-  // TMEM per Q tile t at column 256 t: S buffers 0..63 and 64..127, O 128..128+D
-  static constexpr uint32_t kTmemCols = 256 * NQ;
+  static constexpr uint32_t kTmemCols = 512;
 };
 
 struct PrefillArgs {
@@ -104,7 +108,7 @@ struct PrefillArgs {
   int32_t* status;
   uint64_t timeout_ns;
   int32_t force_timeout;
-  int32_t qc;         // queries per work item (NQ tiles of 128 / G)
+  int32_t qc;         // queries per work item (two Q tiles of 128 / G)
   int32_t item_cap;
   int4* items;        // (sequence, query group, kv head, -)
   int32_t* n_items;
@@ -243,15 +247,11 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
-}
-// 16 consecutive 32-bit columns of this thread's TMEM lane (warp-collective).
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+}// 8 consecutive 32-bit columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%16], {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
-      "%10, %11, %12, %13, %14, %15};" ::"r"(r[0]),
-      "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-      "r"(taddr)
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%8], {%0, %1, %2, %3, %4, %5, %6, %7};" ::"r"(r[0]),
+      "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(taddr)
       : "memory");
 }
 
@@ -266,13 +266,15 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
-// One work item: queries q0 .. q0 + qc - 1 of sequence s's chunk, kv head kvh.
+// One work item: queries q0 .. q0 + 2 QT - 1 of sequence s's chunk, kv head
+// kvh; Q tile t holds queries q0 + t QT .. q0 + (t + 1) QT - 1.
 struct PItem {
   int s, kvh, c0, c, L, q0;
-  int kv_end0, kv_end, nkt0, nkt1, nkt;
+  int kv_end;     // keys visible to the item's last query
+  int nkt[2];     // key tiles each Q tile needs (0: the tile has no query)
+  int nk;         // key tiles of the item (the larger)
 };
 
-template <int NQ>
 __device__ __forceinline__ PItem load_item(const PrefillArgs& a, int idx, int QT) {
   // direct launches: the item is the CTA's own grid position
   const int4 it = idx < 0 ? make_int4(blockIdx.z, gridDim.x - 1 - blockIdx.x, blockIdx.y, 0)
@@ -283,15 +285,15 @@ __device__ __forceinline__ PItem load_item(const PrefillArgs& a, int idx, int QT
   p.c0 = __ldg(a.cu_q_lens + p.s);
   p.c = __ldg(a.cu_q_lens + p.s + 1) - p.c0;
   p.L = __ldg(a.context_lens + p.s);
-  p.q0 = it.y * NQ * QT;
-  // Q tile t holds queries q0 + t QT .. + QT - 1 of the chunk; its rows see
-  // keys below kv_end_t, i.e. nkt_t key tiles (0 when it has no query)
-  const int qn1 = NQ == 2 ? max(0, min(QT, p.c - (p.q0 + QT))) : 0;
-  p.kv_end0 = p.L - p.c + p.q0 + min(QT, p.c - p.q0);
-  p.kv_end = qn1 > 0 ? p.L - p.c + p.q0 + QT + qn1 : p.kv_end0;
-  p.nkt0 = (p.kv_end0 + kKeys - 1) / kKeys;
-  p.nkt1 = qn1 > 0 ? (p.kv_end + kKeys - 1) / kKeys : 0;
-  p.nkt = (p.kv_end + kKeys - 1) / kKeys;
+  p.q0 = it.y * 2 * QT;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int last = min(p.q0 + (t + 1) * QT, p.c);  // one past the tile's last query
+    const int kv_end = p.L - p.c + last;
+    p.nkt[t] = last > p.q0 + t * QT ? (kv_end + kKeys - 1) / kKeys : 0;
+    if (t == 0 || p.nkt[1] > 0) p.kv_end = kv_end;
+  }
+  p.nk = max(p.nkt[0], p.nkt[1]);
   return p;
 }
 
@@ -300,13 +302,18 @@ __device__ __forceinline__ PItem load_item(const PrefillArgs& a, int idx, int QT
 // warps read in the same order; every barrier's phase follows a running
 // count, so the next item's Q and first K/V tiles load while this item
 // finishes and its scores are computed while this item's output is written.
-template <int D, int G, int NS, int NQ>
-__global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
+//
+// Tensor-core order within an item (j = key tile): S_0(0), S_1(0), then for
+// each j: P_0(j) V_j, S_0(j+1), P_1(j) V_j, S_1(j+1). A score tile is
+// rewritten only after the P V product that read it was issued (the tensor
+// core runs one thread's MMAs in order), and each tile's softmax has the
+// other tile's two products' time to finish.
+template <int D, int G>
+__global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                          const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
-  using C = PCfg<D, NS, NQ>;
-  constexpr int kQHalf = C::kQHalf;
+  using C = PCfg<D>;
   constexpr int QT = kRows / G;  // queries per Q tile
   constexpr uint32_t kIdescS = umma_idesc_bf16(128, kKeys, false);
   constexpr uint32_t kIdescO = umma_idesc_bf16(128, D, true);
@@ -316,10 +323,10 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int32_t s_pages[kWin];  // window of the current sequence's block table
-  // row maxima of the two key halves, per Q tile and score buffer; the two
-  // halves' row sums at the end
-  __shared__ float s_xmax[NQ][2][2][kRows];
-  __shared__ float s_lsum[NQ][2][kRows];
+  // row maxima of the two column halves and, at the end, the two halves' row
+  // sums, per Q tile
+  __shared__ float s_xmax[2][2][kRows];
+  __shared__ float s_lsum[2][2][kRows];
   __shared__ int32_t s_item[kItemRing];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -328,7 +335,7 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
     const int s = blockIdx.z;
     const int c = __ldg(a.cu_q_lens + s + 1) - __ldg(a.cu_q_lens + s);
     const int L = __ldg(a.context_lens + s);
-    if ((int)(gridDim.x - 1 - blockIdx.x) * NQ * QT >= c) return;
+    if ((int)(gridDim.x - 1 - blockIdx.x) * 2 * QT >= c) return;
     if (L < c || L > a.max_context_len) {
       if (tid == 0) record_status(a.status, PKV_EDEVICE, L, kKernelPrefill);
       return;
@@ -346,27 +353,25 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
   };
 
   if (tid == 0) {
-    mbar_init(bar(C::kBarQ), 1);
-    mbar_init(bar(C::kBarQE), 1);
-    for (int i = 0; i < NS; ++i) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kBarQF + t), 1);
+      mbar_init(bar(C::kBarQE + t), 1);
+      mbar_init(bar(C::kBarSF + t), 1);
+      mbar_init(bar(C::kBarPF + t), 256);
+      mbar_init(bar(C::kBarPV + t), 1);
+      mbar_init(bar(C::kBarX + t), 256);
+      mbar_init(bar(C::kBarL + t), 256);
+      mbar_init(bar(C::kBarOE + t), 256);
+    }
+    for (int i = 0; i < kNS; ++i) {
       mbar_init(bar(C::kBarKF + i), 1);
       mbar_init(bar(C::kBarKE + i), 1);
       mbar_init(bar(C::kBarVF + i), 1);
       mbar_init(bar(C::kBarVE + i), 1);
     }
-    for (int i = 0; i < 2 * NQ; ++i) {
-      mbar_init(bar(C::kBarSF + i), 1);
-      mbar_init(bar(C::kBarPF + i), 256);
-      mbar_init(bar(C::kBarPV + i), 1);
-      mbar_init(bar(C::kBarX + i), 256);
-    }
-    for (int i = 0; i < NQ; ++i) {
-      mbar_init(bar(C::kBarL + i), 256);
-      mbar_init(bar(C::kBarOE + i), 256);
-    }
     for (int i = 0; i < kItemRing; ++i) {
       mbar_init(bar(C::kBarIF + i), 1);
-      mbar_init(bar(C::kBarIE + i), 1 + 8 * NQ);  // the MMA warp and each softmax warp
+      mbar_init(bar(C::kBarIE + i), 1 + 16);  // the MMA warp and each softmax warp
     }
     mbar_init(bar(C::kBarFin), 1);
     s_abort = 0;
@@ -387,8 +392,8 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
   const int n_items = a.direct ? 1 : *reinterpret_cast<volatile int32_t*>(a.n_items);
 
   // The n-th item of this CTA (-1: no more; -2: the CTA's own grid position),
-  // as posted by the producer; every
-  // consuming warp calls it once per n, in order.
+  // as posted by the producer; every consuming warp calls it once per n, in
+  // order.
   auto take_item = [&](int n, bool& ok) -> int {
     const int slot = n % kItemRing;
     ok = wait_warp(C::kBarIF + slot, (n / kItemRing) & 1, 14);
@@ -399,9 +404,9 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
     return idx;
   };
 
-  // loads this CTA issued (Q, and K and V tiles, counted by the producer):
-  // what a CTA that gives up waits for before its shared memory goes
-  int issued_q = 0, issued_k = 0, issued_v = 0;
+  // loads this CTA issued (per Q tile, and K and V tiles, counted by the
+  // producer): what a CTA that gives up waits for before its shared memory goes
+  int issued_q[2] = {0, 0}, issued_k = 0, issued_v = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -409,7 +414,7 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
     // memory (refilled by the whole warp), so no tile's loads wait for a
     // global read; K runs one tile ahead of V, the order in which the tensor
     // core needs them.
-    const int B = a.block_size, ppt = kKeys / B;  // pages per tile
+    const int B = a.block_size, ppt = kKeys / B;  // pages per tile (4, 8 or 16)
     bool ok = true;
     int jg = 0;  // K/V tiles issued so far (ring position)
     for (int n = 0; ok; ++n) {
@@ -426,31 +431,35 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
       }
       idx = __shfl_sync(0xffffffffu, idx, 0);
       if (idx >= n_items) break;
-      const PItem it = load_item<NQ>(a, idx, QT);
+      const PItem it = load_item(a, idx, QT);
       const int32_t* bt = a.block_tables + (int64_t)it.s * a.max_blocks_per_seq;
       const int npages = (it.kv_end + B - 1) / B;
       int win0 = 0;
-      // Q of this item once the previous item's score MMAs have read theirs
-      if (n > 0) ok = wait_warp(C::kBarQE, (n - 1) & 1, 12);
-      if (!ok) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(C::kBarQ), C::kHalves * kQHalf);
+      // each Q tile once the previous item's score MMAs on it have been read
+      for (int t = 0; ok && t < 2; ++t) {
+        if (it.nkt[t] == 0) continue;
+        if (issued_q[t] > 0) ok = wait_warp(C::kBarQE + t, (issued_q[t] - 1) & 1, 12);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(C::kBarQF + t), C::kQTile);
 #pragma unroll
-        for (int h = 0; h < C::kHalves; ++h)
-          tma_load_3d(base + C::kQ + h * kQHalf, &tmap_q, h * 64, it.kvh * G, it.c0 + it.q0,
-                      bar(C::kBarQ));
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_3d(base + C::kQ + t * C::kQTile + h * C::kQHalf, &tmap_q, h * 64,
+                        it.kvh * G, it.c0 + it.q0 + t * QT, bar(C::kBarQF + t));
+        }
+        ++issued_q[t];
       }
-      ++issued_q;
+      if (!ok) break;
       // the block-table window loads while Q is in flight
       __syncwarp();
       for (int i = lane; i < kWin && i < npages; i += 32) s_pages[i] = __ldg(bt + i);
       __syncwarp();
-      // Step j loads key tile j and value tile j - 1 (the order in which the
-      // tensor core needs them) in one pass of the warp: lane k < 8 issues
-      // the box of page k of the key tile, lane 8 + k that of the value tile
-      // (all rows of the page and both column halves in one box).
-      for (int j = 0; ok && j <= it.nkt; ++j) {
-        const bool do_k = j < it.nkt, do_v = j >= 1;
+      // Step j loads key tile j and value tile j - 1 in one pass of the warp:
+      // lane k < 16 issues the box of page k of the key tile, lane 16 + k
+      // that of the value tile (all rows of the page and both column halves
+      // in one box).
+      for (int j = 0; ok && j <= it.nk; ++j) {
+        const bool do_k = j < it.nk, do_v = j >= 1;
         if (do_k && min((j + 1) * ppt, npages) > win0 + kWin) {
           // slide the window: tile j-1 (whose values are still to load) and on
           win0 = (j - 1) * ppt;
@@ -460,21 +469,21 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
           __syncwarp();
         }
         const int gk = jg + j, gv = jg + j - 1;
-        const int stk = gk % NS, stv = do_v ? gv % NS : 0;
-        if (do_k && gk >= NS) ok = wait_warp(C::kBarKE + stk, (gk / NS - 1) & 1, 1);
+        const int stk = gk % kNS, stv = do_v ? gv % kNS : 0;
+        if (do_k && gk >= kNS) ok = wait_warp(C::kBarKE + stk, (gk / kNS - 1) & 1, 1);
         if (!ok) break;
-        if (do_v && gv >= NS) ok = wait_warp(C::kBarVE + stv, (gv / NS - 1) & 1, 2);
+        if (do_v && gv >= kNS) ok = wait_warp(C::kBarVE + stv, (gv / kNS - 1) & 1, 2);
         if (!ok) break;
-        const bool is_v = lane >= 8;
-        const int pl = lane & 7, p0 = (is_v ? j - 1 : j) * ppt;
-        const bool mine = lane < 16 && (is_v ? do_v : do_k) && pl < min(ppt, npages - p0);
+        const bool is_v = lane >= 16;
+        const int pl = lane & 15, p0 = (is_v ? j - 1 : j) * ppt;
+        const bool mine = (is_v ? do_v : do_k) && pl < min(ppt, npages - p0);
         const int32_t blk = mine ? s_pages[p0 + pl - win0] : -1;
         const bool valid = mine && blk >= 0 && blk < a.num_blocks;
         const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
         const uint32_t kf = bar(C::kBarKF + stk), vf = bar(C::kBarVF + stv);
         const uint32_t page_bytes = B * C::kHalves * 128u;
-        if (lane == 0 && do_k) mbar_arrive_expect_tx(kf, __popc(vmask & 0xffu) * page_bytes);
-        if (lane == 8 && do_v) mbar_arrive_expect_tx(vf, __popc(vmask & 0xff00u) * page_bytes);
+        if (lane == 0 && do_k) mbar_arrive_expect_tx(kf, __popc(vmask & 0xffffu) * page_bytes);
+        if (lane == 16 && do_v) mbar_arrive_expect_tx(vf, __popc(vmask >> 16) * page_bytes);
         __syncwarp();
         if (mine && !valid) record_status(a.status, PKV_EDEVICE, blk, kKernelPrefill);
         if (valid)
@@ -486,14 +495,12 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
         issued_v += do_v ? 1 : 0;
         __syncwarp();
       }
-      jg += it.nkt;
+      jg += it.nk;
       __syncwarp();
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ tensor core
-    // Order within an item: S_t(j) for each Q tile, then P_t(j-1) V; the
-    // scores of the next key tile are computed while their softmax runs.
     // shared-memory descriptors of the first Q, K and V tiles; the others
     // differ only in the start address field (bytes / 16)
     const uint64_t dq = umma_desc_sw128(base + C::kQ, 16, 1024);
@@ -510,95 +517,103 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
       return r;
     };
     bool ok = true;
-    int jg = 0;                   // K/V ring position
-    int sg[NQ], oe[NQ];           // score-buffer uses and finished outputs per Q tile
+    int jg = 0;                        // K/V ring position
+    int qn[2] = {0, 0}, pn[2] = {0, 0}, on[2] = {0, 0};  // Q loads, P tiles, outputs consumed
+    // S_t(j) = Q_t K_j^T into tile t's score columns; the commit after the
+    // tile's last one frees its Q buffer
+    auto scores = [&](int t, int st, bool last) {
+      if (elect_one()) {
+        const uint32_t kst = st * C::kStage;
 #pragma unroll
-    for (int t = 0; t < NQ; ++t) sg[t] = oe[t] = 0;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * 1024 + (kk & 3) * 32;
+          const uint32_t qoff = t * C::kQTile + (kk >> 2) * C::kQHalf + (kk & 3) * 32;
+          umma_bf16(tmem + t * 256, at(dq, qoff), at(dk, kst + koff), kIdescS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(C::kBarSF + t));
+        if (last) umma_commit(bar(C::kBarQE + t));
+      }
+      __syncwarp();
+    };
+    // O_t (+)= P_t(j) V_j: 16-key steps, each the bf16 hi part then the lo
+    // part; keys 32 c .. 32 c + 31 hold hi in columns 32 c .. + 15 and lo in
+    // 32 c + 16 .. + 31 of the score tile
+    auto values = [&](int t, int st, bool first) {
+      if (elect_one()) {
+        const uint32_t p = tmem + t * 256, o = tmem + t * 256 + 128, vst = st * C::kStage;
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint64_t vdesc = at(dv, vst + kk * 2 * C::kGroup);
+          const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
+          umma_bf16_ts(o, p + col, vdesc, kIdescO, (!first || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(o, p + col + 16, vdesc, kIdescO, 1u);
+        }
+        umma_commit(bar(C::kBarPV + t));
+      }
+      __syncwarp();
+    };
     for (int n = 0; ok; ++n) {
       const int idx = take_item(n, ok);
       if (!ok || idx == -1) break;
-      const PItem it = load_item<NQ>(a, idx, QT);
-      auto nkt_t = [&](int t) { return t == 0 ? it.nkt0 : it.nkt1; };
-      ok = wait_warp(C::kBarQ, n & 1, 3);
-      for (int j = 0; ok && j <= it.nkt; ++j) {
-        if (j < it.nkt) {
-          const int g = jg + j, st = g % NS, u = g / NS;
-          ok = wait_warp(C::kBarKF + st, u & 1, 4);
+      const PItem it = load_item(a, idx, QT);
+      // prologue: both tiles' first scores
+      {
+        const int st = jg % kNS;
+        ok = wait_warp(C::kBarKF + st, (jg / kNS) & 1, 4);
+        for (int t = 0; ok && t < 2; ++t) {
+          if (it.nkt[t] == 0) continue;
+          ok = wait_warp(C::kBarQF + t, qn[t]++ & 1, 3);
           if (!ok) break;
           tcgen05_after_sync();
-          if (elect_one()) {
-            const uint32_t kst = st * C::kStage;
-#pragma unroll
-            for (int t = 0; t < NQ; ++t) {
-              if (j >= nkt_t(t)) continue;
-              const int b = (sg[t] + j) & 1;
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t koff = (kk >> 2) * 1024 + (kk & 3) * 32;
-                const uint32_t qoff = t * kRows * 128 + (kk >> 2) * kQHalf + (kk & 3) * 32;
-                umma_bf16(tmem + t * 256 + b * kKeys, at(dq, qoff), at(dk, kst + koff), kIdescS,
-                          kk > 0 ? 1u : 0u);
-              }
-              umma_commit(bar(C::kBarSF + 2 * t + b));
-            }
-            umma_commit(bar(C::kBarKE + st));
-            if (j == it.nkt - 1) umma_commit(bar(C::kBarQE));  // Q may be replaced
-          }
-          __syncwarp();
+          scores(t, st, it.nkt[t] == 1);
         }
-        if (j >= 1) {
-          const int i = j - 1, g = jg + i, st = g % NS, u = g / NS;
-          ok = wait_warp(C::kBarVF + st, u & 1, 6);
-          if (!ok) break;
-          const int key0 = i * kKeys;
-          if (key0 + kKeys > it.kv_end) {
-            // value rows past the last visible key: stale or poisoned bytes that
-            // must not reach O, not even as NaN * 0
-            uint8_t* vp = base_ptr + C::kV + st * C::kStage;
-            for (int r = it.kv_end - key0 + lane; r < kKeys; r += 32)
+        if (!ok) break;
+        if (elect_one()) umma_commit(bar(C::kBarKE + st));  // K_0 is no longer needed
+        __syncwarp();
+      }
+      for (int j = 0; ok && j < it.nk; ++j) {
+        const int g = jg + j, st = g % kNS;
+        ok = wait_warp(C::kBarVF + st, (g / kNS) & 1, 6);
+        if (!ok) break;
+        const int key0 = j * kKeys;
+        if (key0 + kKeys > it.kv_end) {
+          // value rows past the last visible key: stale or poisoned bytes that
+          // must not reach O, not even as NaN * 0
+          uint8_t* vp = base_ptr + C::kV + st * C::kStage;
+          for (int r = it.kv_end - key0 + lane; r < kKeys; r += 32)
 #pragma unroll
-              for (int h = 0; h < C::kHalves; ++h)
+            for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                  *reinterpret_cast<uint4*>(vp + (r >> 3) * C::kGroup + h * 1024 +
-                                            (r & 7) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
-            fence_proxy_async_smem();
-          }
-          __syncwarp();
-#pragma unroll
-          for (int t = 0; t < NQ; ++t) {
-            if (i >= nkt_t(t)) continue;
-            const int sgi = sg[t] + i, b = sgi & 1;
-            ok = wait_warp(C::kBarPF + 2 * t + b, (sgi >> 1) & 1, 5);
-            // the previous item's output must have been read out of O
-            if (ok && i == 0 && oe[t] > 0) ok = wait_warp(C::kBarOE + t, (oe[t] - 1) & 1, 13);
+              for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4*>(vp + (r >> 3) * C::kGroup + h * 1024 + (r & 7) * 128 +
+                                          ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        const bool more = j + 1 < it.nk;
+        const int g1 = g + 1, st1 = g1 % kNS;
+        if (more) ok = wait_warp(C::kBarKF + st1, (g1 / kNS) & 1, 4);
+        for (int t = 0; ok && t < 2; ++t) {
+          if (j < it.nkt[t]) {
+            ok = wait_warp(C::kBarPF + t, pn[t]++ & 1, 5);
+            // the previous item's output must have been read out of O_t
+            if (ok && j == 0 && on[t] > 0) ok = wait_warp(C::kBarOE + t, (on[t] - 1) & 1, 13);
             if (!ok) break;
             tcgen05_after_sync();
-            if (elect_one()) {
-              const uint32_t p = tmem + t * 256 + b * kKeys;
-              const uint32_t o = tmem + t * 256 + 128;
-              const uint32_t vst = st * C::kStage;
-#pragma unroll
-              for (int kk = 0; kk < kKeys / 16; ++kk) {
-                const uint64_t vdesc = at(dv, vst + kk * 2 * C::kGroup);
-                umma_bf16_ts(o, p + kk * 8, vdesc, kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
-                umma_bf16_ts(o, p + 32 + kk * 8, vdesc, kIdescO, 1u);
-              }
-              umma_commit(bar(C::kBarPV + 2 * t + b));
-            }
-            __syncwarp();
+            values(t, st, j == 0);
           }
-          if (!ok) break;
-          if (elect_one()) umma_commit(bar(C::kBarVE + st));
-          __syncwarp();
+          if (more && j + 1 < it.nkt[t]) scores(t, st1, j + 2 == it.nkt[t]);
         }
+        if (!ok) break;
+        if (elect_one()) {
+          if (more) umma_commit(bar(C::kBarKE + st1));
+          umma_commit(bar(C::kBarVE + st));
+        }
+        __syncwarp();
       }
-      jg += it.nkt;
+      jg += it.nk;
 #pragma unroll
-      for (int t = 0; t < NQ; ++t) {
-        sg[t] += nkt_t(t);
-        oe[t] += nkt_t(t) > 0 ? 1 : 0;
-      }
+      for (int t = 0; t < 2; ++t) on[t] += it.nkt[t] > 0 ? 1 : 0;
     }
     // every MMA (and the arrivals it triggers) is done before the CTA leaves
     if (lane == 0) {
@@ -609,110 +624,124 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
   } else {
     // ------------------------------------------------------------ softmax
     // Eight warps per Q tile: each TMEM lane (= row) is shared by two threads,
-    // one per half of the 64 key columns (and of the D output columns); the
+    // one per half of the 128 key columns (and of the D output columns); the
     // two exchange their row maxima through shared memory once per tile.
     const int sw = warp - 2;
     const int t = sw >> 3;            // Q tile of this warp
-    const int h = (sw >> 2) & 1;      // key half (columns 32h .. 32h+31)
+    const int h = (sw >> 2) & 1;      // column half (keys 64 h .. 64 h + 63)
     const int quarter = warp & 3;     // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t t_s = tmem + t * 256 + lane_off + 64 * h;
     const uint32_t t_o = tmem + t * 256 + 128 + lane_off + h * (D / 2);
     const uint64_t scale2 = f32x2_pack(a.scale_log2, a.scale_log2);
     bool ok = true;
-    int sg = 0, ne = 0;  // score-buffer uses and finished outputs of this Q tile
+    int sn = 0, ne = 0;  // score tiles and finished outputs of this Q tile
     for (int n = 0; ok; ++n) {
       const int idx = take_item(n, ok);
       if (!ok || idx == -1) break;
-      const PItem it = load_item<NQ>(a, idx, QT);
-      const int nk = t == 0 ? it.nkt0 : it.nkt1;
+      const PItem it = load_item(a, idx, QT);
+      const int nk = it.nkt[t];
       const int qi = it.q0 + t * QT + r / G;
       const bool row_valid = qi < it.c;
       const int limit = row_valid ? (it.L - it.c + qi + 1) : 1;  // number of visible keys
       float m_ref = 0.f;
       uint64_t l2 = f32x2_pack(0.f, 0.f);  // this thread's share of the row sum, two lanes
       for (int j = 0; j < nk; ++j) {
-        const int sj = sg + j, b = sj & 1, key0 = j * kKeys + 32 * h;
-        ok = wait_warp(C::kBarSF + 2 * t + b, (sj >> 1) & 1, 7);
+        const int key0 = j * kKeys + 64 * h;
+        ok = wait_warp(C::kBarSF + t, sn & 1, 7);
         if (!ok) break;
         tcgen05_after_sync();
-        const uint32_t t_s = tmem + t * 256 + lane_off + b * kKeys;
+        // two passes over this thread's 64 columns, 32 at a time (registers
+        // are scarce with 18 warps per SM): the row maximum first, then the
+        // probabilities
+        const int vis = min(64, limit - key0);  // visible columns of this half (may be <= 0)
+        const bool full = __all_sync(0xffffffffu, vis >= 64) != 0;
         uint32_t x[32];
-        tmem_ld32(t_s + 32 * h, x);
-        tmem_wait_ld();
-        const int vis = min(32, limit - key0);  // visible columns of this half (may be <= 0)
-        const bool full = __all_sync(0xffffffffu, vis >= 32) != 0;
-        if (!full) {
+        auto load = [&](int c) {
+          tmem_ld32(t_s + 32 * c, x);
+          tmem_wait_ld();
+          if (!full) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i >= vis) x[i] = __float_as_uint(-INFINITY);
+            for (int i = 0; i < 32; ++i)
+              if (32 * c + i >= vis) x[i] = __float_as_uint(-INFINITY);
+          }
+        };
+        float mine = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          load(c);
+          float m4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            m4[e] = fmax3(__uint_as_float(x[8 * e]), __uint_as_float(x[8 * e + 1]),
+                          fmax3(__uint_as_float(x[8 * e + 2]), __uint_as_float(x[8 * e + 3]),
+                                fmax3(__uint_as_float(x[8 * e + 4]), __uint_as_float(x[8 * e + 5]),
+                                      fmax3(__uint_as_float(x[8 * e + 6]),
+                                            __uint_as_float(x[8 * e + 7]), mine))));
+          mine = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
         }
-        float m4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          m4[e] = fmax3(__uint_as_float(x[8 * e]), __uint_as_float(x[8 * e + 1]),
-                        fmax3(__uint_as_float(x[8 * e + 2]), __uint_as_float(x[8 * e + 3]),
-                              fmax3(__uint_as_float(x[8 * e + 4]), __uint_as_float(x[8 * e + 5]),
-                                    fmax3(__uint_as_float(x[8 * e + 6]),
-                                          __uint_as_float(x[8 * e + 7]), -INFINITY))));
-        const float mine = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
-        s_xmax[t][b][h][r] = mine;
-        mbar_arrive(bar(C::kBarX + 2 * t + b));
-        ok = wait_warp(C::kBarX + 2 * t + b, (sj >> 1) & 1, 10);
+        s_xmax[t][h][r] = mine;
+        mbar_arrive(bar(C::kBarX + t));
+        ok = wait_warp(C::kBarX + t, sn & 1, 10);
         if (!ok) break;
-        const float m_tile = fmaxf(mine, s_xmax[t][b][h ^ 1][r]) * a.scale_log2;  // -inf: none
+        const float m_tile = fmaxf(mine, s_xmax[t][h ^ 1][r]) * a.scale_log2;  // -inf: none
         if (j == 0) m_ref = m_tile;  // key 0 is visible to every row
         const bool need = m_tile > m_ref + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
-          // O must be complete up to tile j-1 before it is rescaled
-          ok = wait_warp(C::kBarPV + 2 * t + ((sj - 1) & 1), ((sj - 1) >> 1) & 1, 8);
-          if (!ok) break;
-          tcgen05_after_sync();
+          // O holds the products up to tile j-1 (they were issued before
+          // this tile's scores, whose completion was just observed)
           const float alpha = need ? fast_exp2(m_ref - m_tile) : 1.f;
           if (need) m_ref = m_tile;
           l2 = f32x2_mul(l2, f32x2_pack(alpha, alpha));
 #pragma unroll 1
           for (int c32 = 0; c32 < D / 64; ++c32) {
-            uint32_t o[32];
-            tmem_ld32(t_o + c32 * 32, o);
+            tmem_ld32(t_o + c32 * 32, x);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(t_o + c32 * 32, o);
+            for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) * alpha);
+            tmem_st32(t_o + c32 * 32, x);
           }
         }
         // p = 2^(x scale - m_ref) for two columns at a time, split into bf16
-        // hi + lo parts; masked columns hold -inf and give 0
+        // hi + lo parts; masked columns hold -inf and give 0. Keys 32 c ..
+        // 32 c + 31 of this half go back to the same 32 columns: hi parts
+        // first, then lo parts, 16 keys per store.
         const uint64_t negm = f32x2_pack(-m_ref, -m_ref);
-        uint32_t hi[16], lo[16];
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          load(c);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float y0, y1;
-          f32x2_unpack(
-              f32x2_fma(f32x2_pack(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])),
-                        scale2, negm),
-              y0, y1);
-          const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
-          const uint64_t p = f32x2_pack(p0, p1);
-          l2 = f32x2_add(l2, p);
-          hi[e] = pack_bf16x2(p0, p1);
-          float d0, d1;
-          f32x2_unpack(f32x2_sub(p, f32x2_pack(bf16_lo_to_f32(hi[e]), bf16_hi_to_f32(hi[e]))),
-                       d0, d1);
-          lo[e] = pack_bf16x2(d0, d1);
+          for (int q = 0; q < 2; ++q) {
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int i = 16 * q + 2 * e;
+              float y0, y1;
+              f32x2_unpack(
+                  f32x2_fma(f32x2_pack(__uint_as_float(x[i]), __uint_as_float(x[i + 1])), scale2,
+                            negm),
+                  y0, y1);
+              const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+              const uint64_t p = f32x2_pack(p0, p1);
+              l2 = f32x2_add(l2, p);
+              hi[e] = pack_bf16x2(p0, p1);
+              float d0, d1;
+              f32x2_unpack(
+                  f32x2_sub(p, f32x2_pack(bf16_lo_to_f32(hi[e]), bf16_hi_to_f32(hi[e]))), d0, d1);
+              lo[e] = pack_bf16x2(d0, d1);
+            }
+            tmem_st8(t_s + 32 * c + 8 * q, hi);
+            tmem_st8(t_s + 32 * c + 8 * q + 16, lo);
+          }
         }
-        tmem_st16(t_s + 16 * h, hi);
-        tmem_st16(t_s + 32 + 16 * h, lo);
         tmem_wait_st();
         tcgen05_before_sync();
-        mbar_arrive(bar(C::kBarPF + 2 * t + b));
+        mbar_arrive(bar(C::kBarPF + t));
+        ++sn;
       }
-      if (!ok || nk == 0) {
-        sg += nk;
-        continue;
-      }
-      const int sl = sg + nk - 1;
-      ok = wait_warp(C::kBarPV + 2 * t + (sl & 1), (sl >> 1) & 1, 9);
+      if (!ok || nk == 0) continue;
+      ok = wait_warp(C::kBarPV + t, (sn - 1) & 1, 9);
       if (ok) {
         // ---- epilogue: O / l -> bf16, row r -> (query qi, head kvh*G + r%G);
         // this thread writes its half of the D columns
@@ -748,7 +777,6 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
         tcgen05_before_sync();
         mbar_arrive(bar(C::kBarOE + t));
       }
-      sg += nk;
       ++ne;
     }
   }
@@ -760,11 +788,13 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
     // Let this CTA's own copies land before its shared memory is released:
     // wait (again with a limit) for the last phase armed on each barrier.
     if (tid == 0) {
-      if (issued_q) mbar_wait_bounded(bar(C::kBarQ), (issued_q - 1) & 1, 4 * a.timeout_ns, 0);
-      for (int i = 0; i < NS; ++i) {
-        // tiles i, i + NS, ... went to stage i: wait for the last one's phase
-        const int nk = issued_k > i ? (issued_k - 1 - i) / NS + 1 : 0;
-        const int nv = issued_v > i ? (issued_v - 1 - i) / NS + 1 : 0;
+      for (int t = 0; t < 2; ++t)
+        if (issued_q[t])
+          mbar_wait_bounded(bar(C::kBarQF + t), (issued_q[t] - 1) & 1, 4 * a.timeout_ns, 0);
+      for (int i = 0; i < kNS; ++i) {
+        // tiles i, i + kNS, ... went to stage i: wait for the last one's phase
+        const int nk = issued_k > i ? (issued_k - 1 - i) / kNS + 1 : 0;
+        const int nv = issued_v > i ? (issued_v - 1 - i) / kNS + 1 : 0;
         if (nk) mbar_wait_bounded(bar(C::kBarKF + i), (nk - 1) & 1, 4 * a.timeout_ns, 0);
         if (nv) mbar_wait_bounded(bar(C::kBarVF + i), (nv - 1) & 1, 4 * a.timeout_ns, 0);
       }
@@ -777,28 +807,27 @@ __global__ void __launch_bounds__(PCfg<D, NS, NQ>::kThreads, NQ == 1 ? 2 : 1)
   }
 }
 
-template <int D, int G, int NQ>
+template <int D, int G>
 int launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    PrefillArgs a, const DeviceInfo& dev, int total_q, int max_q_len,
                    cudaStream_t stream) {
-  constexpr int NS = NQ == 2 ? 3 : 2;
-  using C = PCfg<D, NS, NQ>;
+  using C = PCfg<D>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, []() {
-    attr_err = cudaFuncSetAttribute(paged_prefill_kernel<D, G, NS, NQ>,
+    attr_err = cudaFuncSetAttribute(paged_prefill_kernel<D, G>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "prefill kernel attributes");
-  a.qc = NQ * kRows / G;  // queries per work item
-  const int slots = dev.sm_count * (NQ == 1 ? 2 : 1);
+  a.qc = 2 * kRows / G;  // queries per work item
+  const int slots = dev.sm_count;
   // Few items: one CTA each, straight from the grid (no plan launch); many:
   // a plan and a persistent grid that hands them out.
   const int64_t items = ((int64_t)total_q / a.qc + a.S) * a.Hkv;
   if (items < 4 * (int64_t)slots) {
     a.direct = 1;
     dim3 grid((unsigned)((max_q_len + a.qc - 1) / a.qc), (unsigned)a.Hkv, (unsigned)a.S);
-    paged_prefill_kernel<D, G, NS, NQ><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, a);
+    paged_prefill_kernel<D, G><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, a);
     return check_launch("prefill");
   }
   a.direct = 0;
@@ -824,7 +853,7 @@ int launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  cudaError_t err = cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D, G, NS, NQ>, tq, tk, tv, a);
+  cudaError_t err = cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D, G>, tq, tk, tv, a);
   if (err != cudaSuccess) return cuda_fail(err, "prefill launch");
   return PKV_OK;
 }
@@ -890,17 +919,11 @@ extern "C" int pkv_paged_attention_prefill(void* out, const void* q, const int32
               "prefill: bf16 arrays must be 16-byte aligned");
   const DeviceInfo* dev = nullptr;
   if (int rc = current_device_info(&dev)) return rc;
-  // One Q tile per CTA and two CTAs per SM, whose starts and ends overlap:
-  // measured faster on GB300 than two Q tiles per CTA (which halve the
-  // key/value reads per row) for fresh prompts and for short chunks after long
-  // cached prefixes alike, since the producer loads a step's keys and values
-  // in one pass. The kernel keeps NQ = 2 as a compile-time variant.
-  constexpr int NQ = 1;
   CUtensorMap tq, tk, tv;
   {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)total_q};
     const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)Hq * D * 2};
-    const uint32_t box[3] = {64, (uint32_t)G, (uint32_t)(NQ * kRows / G)};
+    const uint32_t box[3] = {64, (uint32_t)G, (uint32_t)(kRows / G)};  // one Q tile
     if (int rc = encode_tile_map_3d(&tq, q, dims, strides, box)) return rc;
   }
   const uint64_t rows = (uint64_t)num_blocks * Hkv * block_size;
@@ -932,7 +955,7 @@ extern "C" int pkv_paged_attention_prefill(void* out, const void* q, const int32
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc = PKV_OK;
 #define PKV_PREFILL_CASE(DD, GG) \
-  if (D == DD && G == GG) rc = launch_prefill<DD, GG, NQ>(tq, tk, tv, a, *dev, total_q, max_q_len, st);
+  if (D == DD && G == GG) rc = launch_prefill<DD, GG>(tq, tk, tv, a, *dev, total_q, max_q_len, st);
   PKV_PREFILL_CASE(64, 1)
   PKV_PREFILL_CASE(64, 2)
   PKV_PREFILL_CASE(64, 4)
