@@ -70,7 +70,7 @@ constexpr int kItemRing = 4;         // work-item indices handed from the produc
 // bf16 hi and lo parts) and the output accumulator O_t (D columns).
 template <int D>
 struct PCfg {
-  static constexpr int kThreads = 64 + 512;  // producer, MMA, eight softmax warps per Q tile
+  static constexpr int kThreads = 64 + 256;  // producer, MMA, four softmax warps per Q tile
   static constexpr int kHalves = D / 64;
   static constexpr uint32_t kQHalf = kRows * 128;          // one 64-column half of a Q tile
   static constexpr uint32_t kQTile = kHalves * kQHalf;
@@ -85,15 +85,13 @@ struct PCfg {
   static constexpr uint32_t kMinSmem = 120u * 1024;
   static constexpr uint32_t kSmem = kBytes + 1024 > kMinSmem ? kBytes + 1024 : kMinSmem;
   // barriers: per Q tile full / free; K full/empty and V full/empty per
-  // stage; per Q tile: S full, P full (256 arrivals), P V done, row maxima
-  // exchanged (256), row sums exchanged (256), output read out (256); work
-  // item posted / taken per item-ring slot; final
+  // stage; per Q tile: S full, P full (128 arrivals), P V done, output read
+  // out (128); work item posted / taken per item-ring slot; final
   static constexpr int kBarQF = 0, kBarQE = 2, kBarKF = 4, kBarKE = kBarKF + kNS,
                        kBarVF = kBarKE + kNS, kBarVE = kBarVF + kNS, kBarSF = kBarVE + kNS,
-                       kBarPF = kBarSF + 2, kBarPV = kBarPF + 2, kBarX = kBarPV + 2,
-                       kBarL = kBarX + 2, kBarOE = kBarL + 2, kBarIF = kBarOE + 2,
-                       kBarIE = kBarIF + kItemRing, kBarFin = kBarIE + kItemRing,
-                       kNumBars = kBarFin + 1;
+                       kBarPF = kBarSF + 2, kBarPV = kBarPF + 2, kBarOE = kBarPV + 2,
+                       kBarIF = kBarOE + 2, kBarIE = kBarIF + kItemRing,
+                       kBarFin = kBarIE + kItemRing, kNumBars = kBarFin + 1;
   static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -248,6 +246,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }// 8 consecutive 32-bit columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%8], {%0, %1, %2, %3, %4, %5, %6, %7};" ::"r"(r[0]),
@@ -323,10 +328,6 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int32_t s_pages[kWin];  // window of the current sequence's block table
-  // row maxima of the two column halves and, at the end, the two halves' row
-  // sums, per Q tile
-  __shared__ float s_xmax[2][2][kRows];
-  __shared__ float s_lsum[2][2][kRows];
   __shared__ int32_t s_item[kItemRing];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -357,11 +358,9 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
       mbar_init(bar(C::kBarQF + t), 1);
       mbar_init(bar(C::kBarQE + t), 1);
       mbar_init(bar(C::kBarSF + t), 1);
-      mbar_init(bar(C::kBarPF + t), 256);
+      mbar_init(bar(C::kBarPF + t), 128);
       mbar_init(bar(C::kBarPV + t), 1);
-      mbar_init(bar(C::kBarX + t), 256);
-      mbar_init(bar(C::kBarL + t), 256);
-      mbar_init(bar(C::kBarOE + t), 256);
+      mbar_init(bar(C::kBarOE + t), 128);
     }
     for (int i = 0; i < kNS; ++i) {
       mbar_init(bar(C::kBarKF + i), 1);
@@ -371,7 +370,7 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
     }
     for (int i = 0; i < kItemRing; ++i) {
       mbar_init(bar(C::kBarIF + i), 1);
-      mbar_init(bar(C::kBarIE + i), 1 + 16);  // the MMA warp and each softmax warp
+      mbar_init(bar(C::kBarIE + i), 1 + 8);  // the MMA warp and each softmax warp
     }
     mbar_init(bar(C::kBarFin), 1);
     s_abort = 0;
@@ -380,6 +379,13 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
     prefetch_tensormap(&tmap_k);
     prefetch_tensormap(&tmap_v);
   }
+  // Value stages start zeroed: the product reads every row of a value tile,
+  // and rows no load has reached yet (pages past an item's last visible
+  // key) must hold finite values, since 0 * NaN is NaN. Later tiles leave
+  // finite values behind: rows past a sequence's end are zeroed below.
+  for (uint32_t i = tid * 16; i < kNS * C::kStage; i += C::kThreads * 16)
+    *reinterpret_cast<uint4*>(base_ptr + C::kV + i) = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   if (warp == 0) {
     tmem_alloc(smem_u32(&s_tmem), C::kTmemCols);
     tmem_relinquish();
@@ -575,18 +581,20 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
         const int g = jg + j, st = g % kNS;
         ok = wait_warp(C::kBarVF + st, (g / kNS) & 1, 6);
         if (!ok) break;
-        const int key0 = j * kKeys;
-        if (key0 + kKeys > it.kv_end) {
-          // value rows past the last visible key: stale or poisoned bytes that
-          // must not reach O, not even as NaN * 0
+        // Value rows of the sequence's last page past its end hold whatever
+        // the pool holds there (stale or poisoned bytes) and must not reach
+        // O, not even as NaN * 0: zero them when this tile loaded that page.
+        // Eight lanes write one 128-byte row segment, four rows per pass.
+        const int B = a.block_size, key0 = j * kKeys;
+        const int last_page = (it.L + B - 1) / B;  // pages of the whole sequence
+        if (j == it.nk - 1 && it.L % B != 0 && (it.kv_end + B - 1) / B == last_page) {
           uint8_t* vp = base_ptr + C::kV + st * C::kStage;
-          for (int r = it.kv_end - key0 + lane; r < kKeys; r += 32)
+          const int r_end = min(last_page * B - key0, kKeys);
+          for (int r = it.L - key0 + (lane >> 3); r < r_end; r += 4)
 #pragma unroll
             for (int h = 0; h < C::kHalves; ++h)
-#pragma unroll
-              for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4*>(vp + (r >> 3) * C::kGroup + h * 1024 + (r & 7) * 128 +
-                                          ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+              *reinterpret_cast<uint4*>(vp + (r >> 3) * C::kGroup + h * 1024 + (r & 7) * 128 +
+                                        (lane & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
           fence_proxy_async_smem();
         }
         __syncwarp();
@@ -623,20 +631,19 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    // Eight warps per Q tile: each TMEM lane (= row) is shared by two threads,
-    // one per half of the 128 key columns (and of the D output columns); the
-    // two exchange their row maxima through shared memory once per tile.
+    // Four warps per Q tile, one thread per TMEM lane (= row): the whole row
+    // of 128 scores sits in this thread's registers, so its maximum and sum
+    // need no exchange with another thread.
     const int sw = warp - 2;
-    const int t = sw >> 3;            // Q tile of this warp
-    const int h = (sw >> 2) & 1;      // column half (keys 64 h .. 64 h + 63)
+    const int t = sw >> 2;            // Q tile of this warp
     const int quarter = warp & 3;     // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t t_s = tmem + t * 256 + lane_off + 64 * h;
-    const uint32_t t_o = tmem + t * 256 + 128 + lane_off + h * (D / 2);
+    const uint32_t t_s = tmem + t * 256 + lane_off;
+    const uint32_t t_o = tmem + t * 256 + 128 + lane_off;
     const uint64_t scale2 = f32x2_pack(a.scale_log2, a.scale_log2);
     bool ok = true;
-    int sn = 0, ne = 0;  // score tiles and finished outputs of this Q tile
+    int sn = 0;  // score tiles of this Q tile
     for (int n = 0; ok; ++n) {
       const int idx = take_item(n, ok);
       if (!ok || idx == -1) break;
@@ -646,46 +653,37 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
       const bool row_valid = qi < it.c;
       const int limit = row_valid ? (it.L - it.c + qi + 1) : 1;  // number of visible keys
       float m_ref = 0.f;
-      uint64_t l2 = f32x2_pack(0.f, 0.f);  // this thread's share of the row sum, two lanes
+      uint64_t l2 = f32x2_pack(0.f, 0.f);  // the row sum, two lanes
       for (int j = 0; j < nk; ++j) {
-        const int key0 = j * kKeys + 64 * h;
         ok = wait_warp(C::kBarSF + t, sn & 1, 7);
         if (!ok) break;
         tcgen05_after_sync();
-        // two passes over this thread's 64 columns, 32 at a time (registers
-        // are scarce with 18 warps per SM): the row maximum first, then the
-        // probabilities
-        const int vis = min(64, limit - key0);  // visible columns of this half (may be <= 0)
-        const bool full = __all_sync(0xffffffffu, vis >= 64) != 0;
-        uint32_t x[32];
-        auto load = [&](int c) {
-          tmem_ld32(t_s + 32 * c, x);
-          tmem_wait_ld();
-          if (!full) {
+        uint32_t x[kKeys];
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (32 * c + i >= vis) x[i] = __float_as_uint(-INFINITY);
-          }
-        };
-        float mine = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          load(c);
-          float m4[4];
+        for (int c = 0; c < kKeys / 32; ++c)
+          tmem_ld32(t_s + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
+        tmem_wait_ld();
+        const int vis = min(kKeys, limit - j * kKeys);  // visible columns (may be <= 0)
+        if (!(__all_sync(0xffffffffu, vis >= kKeys) != 0)) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            m4[e] = fmax3(__uint_as_float(x[8 * e]), __uint_as_float(x[8 * e + 1]),
-                          fmax3(__uint_as_float(x[8 * e + 2]), __uint_as_float(x[8 * e + 3]),
-                                fmax3(__uint_as_float(x[8 * e + 4]), __uint_as_float(x[8 * e + 5]),
-                                      fmax3(__uint_as_float(x[8 * e + 6]),
-                                            __uint_as_float(x[8 * e + 7]), mine))));
-          mine = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+          for (int i = 0; i < kKeys; ++i)
+            if (i >= vis) x[i] = __float_as_uint(-INFINITY);
         }
-        s_xmax[t][h][r] = mine;
-        mbar_arrive(bar(C::kBarX + t));
-        ok = wait_warp(C::kBarX + t, sn & 1, 10);
-        if (!ok) break;
-        const float m_tile = fmaxf(mine, s_xmax[t][h ^ 1][r]) * a.scale_log2;  // -inf: none
+        float m8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t* y = x + 16 * e;
+          m8[e] = fmax3(fmax3(__uint_as_float(y[0]), __uint_as_float(y[1]), __uint_as_float(y[2])),
+                        fmax3(__uint_as_float(y[3]), __uint_as_float(y[4]), __uint_as_float(y[5])),
+                        fmax3(__uint_as_float(y[6]), __uint_as_float(y[7]), __uint_as_float(y[8])));
+          m8[e] = fmax3(m8[e],
+                        fmax3(__uint_as_float(y[9]), __uint_as_float(y[10]), __uint_as_float(y[11])),
+                        fmax3(__uint_as_float(y[12]), __uint_as_float(y[13]),
+                              fmaxf(__uint_as_float(y[14]), __uint_as_float(y[15]))));
+        }
+        const float m_tile =
+            fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) *
+            a.scale_log2;  // -inf: no visible key
         if (j == 0) m_ref = m_tile;  // key 0 is visible to every row
         const bool need = m_tile > m_ref + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
@@ -695,45 +693,43 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
           if (need) m_ref = m_tile;
           l2 = f32x2_mul(l2, f32x2_pack(alpha, alpha));
 #pragma unroll 1
-          for (int c32 = 0; c32 < D / 64; ++c32) {
-            tmem_ld32(t_o + c32 * 32, x);
+          for (int c8 = 0; c8 < D / 8; ++c8) {
+            uint32_t o[8];
+            tmem_ld8(t_o + c8 * 8, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) * alpha);
-            tmem_st32(t_o + c32 * 32, x);
+            for (int e = 0; e < 8; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st8(t_o + c8 * 8, o);
           }
         }
         // p = 2^(x scale - m_ref) for two columns at a time, split into bf16
         // hi + lo parts; masked columns hold -inf and give 0. Keys 32 c ..
-        // 32 c + 31 of this half go back to the same 32 columns: hi parts
-        // first, then lo parts, 16 keys per store.
+        // 32 c + 31 go back to the same 32 columns: hi parts first, then lo
+        // parts, 16 keys per store.
         const uint64_t negm = f32x2_pack(-m_ref, -m_ref);
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          load(c);
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            uint32_t hi[8], lo[8];
+        for (int q = 0; q < kKeys / 16; ++q) {
+          uint32_t hi[8], lo[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int i = 16 * q + 2 * e;
-              float y0, y1;
-              f32x2_unpack(
-                  f32x2_fma(f32x2_pack(__uint_as_float(x[i]), __uint_as_float(x[i + 1])), scale2,
-                            negm),
-                  y0, y1);
-              const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
-              const uint64_t p = f32x2_pack(p0, p1);
-              l2 = f32x2_add(l2, p);
-              hi[e] = pack_bf16x2(p0, p1);
-              float d0, d1;
-              f32x2_unpack(
-                  f32x2_sub(p, f32x2_pack(bf16_lo_to_f32(hi[e]), bf16_hi_to_f32(hi[e]))), d0, d1);
-              lo[e] = pack_bf16x2(d0, d1);
-            }
-            tmem_st8(t_s + 32 * c + 8 * q, hi);
-            tmem_st8(t_s + 32 * c + 8 * q + 16, lo);
+          for (int e = 0; e < 8; ++e) {
+            const int i = 16 * q + 2 * e;
+            float y0, y1;
+            f32x2_unpack(
+                f32x2_fma(f32x2_pack(__uint_as_float(x[i]), __uint_as_float(x[i + 1])), scale2,
+                          negm),
+                y0, y1);
+            const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+            const uint64_t p = f32x2_pack(p0, p1);
+            l2 = f32x2_add(l2, p);
+            hi[e] = pack_bf16x2(p0, p1);
+            float d0, d1;
+            f32x2_unpack(f32x2_sub(p, f32x2_pack(bf16_lo_to_f32(hi[e]), bf16_hi_to_f32(hi[e]))),
+                         d0, d1);
+            lo[e] = pack_bf16x2(d0, d1);
           }
+          const uint32_t col = 32 * (q >> 1) + 8 * (q & 1);
+          tmem_st8(t_s + col, hi);
+          tmem_st8(t_s + col + 16, lo);
         }
         tmem_wait_st();
         tcgen05_before_sync();
@@ -742,42 +738,33 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
       }
       if (!ok || nk == 0) continue;
       ok = wait_warp(C::kBarPV + t, (sn - 1) & 1, 9);
-      if (ok) {
-        // ---- epilogue: O / l -> bf16, row r -> (query qi, head kvh*G + r%G);
-        // this thread writes its half of the D columns
-        float l0, l1;
-        f32x2_unpack(l2, l0, l1);
-        s_lsum[t][h][r] = l0 + l1;
-        mbar_arrive(bar(C::kBarL + t));
-        ok = wait_warp(C::kBarL + t, ne & 1, 11);
-      }
-      if (ok) {
-        const float inv = 1.f / (s_lsum[t][0][r] + s_lsum[t][1][r]);
-        tcgen05_after_sync();
-        __nv_bfloat16* orow =
-            a.out + ((int64_t)(it.c0 + qi) * a.Hq + it.kvh * G + (r % G)) * D + h * (D / 2);
+      if (!ok) break;
+      // ---- epilogue: O / l -> bf16, row r -> (query qi, head kvh*G + r%G)
+      float l0, l1;
+      f32x2_unpack(l2, l0, l1);
+      const float inv = 1.f / (l0 + l1);
+      tcgen05_after_sync();
+      __nv_bfloat16* orow = a.out + ((int64_t)(it.c0 + qi) * a.Hq + it.kvh * G + (r % G)) * D;
 #pragma unroll 1
-        for (int c32 = 0; c32 < D / 64; ++c32) {
-          uint32_t o[32];
-          tmem_ld32(t_o + c32 * 32, o);
-          tmem_wait_ld();
-          if (row_valid) {
+      for (int c32 = 0; c32 < D / 32; ++c32) {
+        uint32_t o[32];
+        tmem_ld32(t_o + c32 * 32, o);
+        tmem_wait_ld();
+        if (row_valid) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-              *reinterpret_cast<uint4*>(orow + c32 * 32 + e) = v;
-            }
+          for (int e = 0; e < 32; e += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c32 * 32 + e) = v;
           }
         }
-        // O and this tile's row-sum slots may be reused by the next item
-        tcgen05_before_sync();
-        mbar_arrive(bar(C::kBarOE + t));
       }
-      ++ne;
+      // O may be overwritten by the next item's products
+      tcgen05_before_sync();
+      mbar_arrive(bar(C::kBarOE + t));
     }
   }
 
