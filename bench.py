@@ -691,11 +691,11 @@ def run_trace(args):
             meta = run.host_metadata(itr)
             run.finish(itr)
             live = run.upload_meta(meta, stream)
-            host += time.perf_counter() - h0
             live.update(q=up["q"], n_pre=up["n_pre"])
             if "k" in up:
                 live.update(k=up["k"], v=up["v"])
-            run.launch(live, stream=stream)
+            run.launch_fused(live, stream=stream)
+            host += time.perf_counter() - h0
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         pkv.pkv_check_status(run.status)
@@ -747,7 +747,8 @@ def run_trace(args):
             "gpu_ms": gpu_ms,
             "note": "host and GPU on one clock: per iteration one pkv_iteration_prepare call "
                     "(slots, cu_q_lens, lengths, block tables into pinned memory), one "
-                    "metadata upload and the launches, the host waiting only for a free "
+                    "metadata upload and one pkv_iteration_run call (append, prefill, "
+                    "decode), the host waiting only for a free "
                     "staging buffer (4 in a ring); host_ms is the host's own work in the loop "
                     "(allocator, metadata, launches); token values resident on the device"},
         "roofline": {"bound": "hbm", "kernel": "pkv_paged_attention_decode", "achieved": dec_gbs,

@@ -151,6 +151,34 @@ int pkv_iteration_prepare(pkv_alloc* a, const int64_t* seqs, const int32_t* coun
                           void* buf, size_t buf_bytes, pkv_iteration_layout* layout,
                           int32_t* n_fit);
 
+/* The GPU side of that iteration in one call ("Deep Dive: continuous
+ * batching", sections Iteration-level scheduling and The prefill/decode mix):
+ * after the caller has copied the buffer pkv_iteration_prepare filled to
+ * device memory `meta` (same offsets, 64-byte aligned or better), this
+ * launches on `stream`, in order, pkv_block_copy of the copy pairs,
+ * pkv_kv_append of every new token, pkv_paged_attention_prefill of the
+ * prompt chunks and pkv_paged_attention_decode of the decodes, with the
+ * arrays read from `meta` and the sizes from `layout` (the host struct the
+ * prepare call returned).
+ *   q, out          : bf16 [n_tokens][Hq][D] (device), prefill rows first
+ *                     (one per prompt token, in work order), then one row
+ *                     per decode.
+ *   k_new, v_new    : bf16 [n_tokens][Hkv][D] (device), the same order.
+ *   decode_ws       : pkv_decode_workspace_bytes(n_decode, Hq, D,
+ *                     max_decode_len, partition_size) bytes or more.
+ *   prefill_ws      : pkv_prefill_workspace_bytes(n_prefill, prefill rows,
+ *                     Hq, D) bytes or more.
+ * Errors are those of the four calls (the first failing one returns; the
+ * launches before it stay queued). An iteration with no token and no copy
+ * does nothing. */
+int pkv_iteration_run(const void* meta, const pkv_iteration_layout* layout, int32_t n_prefill,
+                      int32_t n_decode, int32_t max_blocks_per_seq, const void* q,
+                      const void* k_new, const void* v_new, void* out, void* k_cache,
+                      void* v_cache, int32_t num_blocks, int32_t Hq, int32_t Hkv, int32_t D,
+                      int32_t block_size, float scale, int32_t partition_size, void* decode_ws,
+                      size_t decode_ws_bytes, void* prefill_ws, size_t prefill_ws_bytes,
+                      int32_t* dev_status, void* stream);
+
 /* Preemption ("Batching, Scheduling, and Paging", section PagedAttention: if
  * HBM runs out a request is evicted, swapped to CPU memory or discarded and
  * recomputed later).

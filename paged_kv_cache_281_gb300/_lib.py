@@ -47,6 +47,9 @@ SIGNATURES = {
     "pkv_iteration_layout_bytes": (ctypes.c_int, [i32, i32, i32, i32, P(IterationLayout)]),
     "pkv_iteration_prepare": (ctypes.c_int, [vp, P(i64), P(i32), i32, i32, i32, vp, sz,
                                              P(IterationLayout), P(i32)]),
+    "pkv_iteration_run": (ctypes.c_int, [vp, P(IterationLayout), i32, i32, i32, vp, vp, vp, vp,
+                                         vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp,
+                                         sz, vp, vp]),
     "pkv_seq_swap_out": (ctypes.c_int, [vp, i64, P(i32), i32, P(i32)]),
     "pkv_seq_swap_in": (ctypes.c_int, [vp, i64, P(i32), i32, P(i32)]),
     "pkv_seq_create_cached": (ctypes.c_int, [vp, P(i32), i32, P(i64), P(i32)]),

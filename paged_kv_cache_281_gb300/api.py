@@ -30,6 +30,7 @@ __all__ = [
     "pkv_debug_set_wait", "new_status", "new_fp8_pools", "pkv_kv_append_fp8",
     "pkv_paged_attention_decode_fp8", "pkv_decode_shared_workspace_bytes",
     "pkv_paged_attention_decode_shared", "IterationLayout", "iteration_layout_bytes",
+    "pkv_iteration_run",
 ]
 
 
@@ -241,6 +242,32 @@ class BlockAllocator:
             err.n_fit = fit.value
             raise err
         return layout
+
+
+def pkv_iteration_run(meta, layout, n_prefill: int, n_decode: int, max_blocks_per_seq: int, q,
+                      k_new, v_new, out, k_cache, v_cache, scale: float, decode_ws, prefill_ws,
+                      partition_size: int = 0, status=None, stream=None) -> None:
+    """``pkv_iteration_run``: the iteration's copies, appends, prefill and
+    decode from one device copy (``meta``, uint8) of the buffer
+    ``iteration_prepare`` filled; ``layout`` is what it returned."""
+    N, Hkv, B, D = _pool_shape(k_cache, v_cache)
+    _dev(meta, "meta", torch.uint8, 1)
+    for name, t in (("q", q), ("out", out), ("k_new", k_new), ("v_new", v_new)):
+        _dev(t, name, torch.bfloat16, 3)
+    _dev(decode_ws, "decode_ws", torch.uint8, 1)
+    _dev(prefill_ws, "prefill_ws", torch.uint8, 1)
+    T, Hq = int(layout.n_tokens), int(q.shape[1])
+    if meta.numel() < layout.total_bytes:
+        raise ValueError("meta is shorter than the layout")
+    if q.shape != (T, Hq, D) or out.shape != q.shape or k_new.shape != (T, Hkv, D) or \
+            v_new.shape != k_new.shape:
+        raise ValueError(f"q/out must be [{T}, Hq, {D}] and k_new/v_new [{T}, {Hkv}, {D}]")
+    check(lib().pkv_iteration_run(
+        meta.data_ptr(), ctypes.byref(layout), int(n_prefill), int(n_decode),
+        int(max_blocks_per_seq), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+        out.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), N, Hq, Hkv, D, B, float(scale),
+        int(partition_size), decode_ws.data_ptr(), int(decode_ws.numel()), prefill_ws.data_ptr(),
+        int(prefill_ws.numel()), _ptr(status), _stream(stream)))
 
 
 def iteration_layout_bytes(n_prefill: int, n_decode: int, n_tokens: int,

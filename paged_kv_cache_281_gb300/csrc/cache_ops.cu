@@ -163,29 +163,30 @@ __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
   return r;
 }
 
-// Eight lanes per row: each lane holds D / 8 consecutive elements (16-byte
-// loads), the row's amax is a reduction over its eight lanes, and each lane
-// stores its D / 8 codes at once. A warp covers four rows per pass.
+// Four lanes per row: each lane holds D / 4 consecutive elements (two or
+// four 16-byte loads in flight), the row's amax is a reduction over its four
+// lanes, and each lane stores its D / 4 codes in 16-byte pieces. A warp
+// covers eight rows per pass.
 template <int D>
 __global__ void __launch_bounds__(256) kv_append_fp8_kernel(const AppendFp8Args a) {
   grid_dep_launch();  // as in kv_append_kernel
-  constexpr int E = D / 8;    // elements per lane: 16 (D=128) or 8 (D=64)
+  constexpr int E = D / 4;    // elements per lane: 32 (D=128) or 16 (D=64)
   constexpr int V = E / 8;    // 16-byte input vectors per lane
-  const int sub = threadIdx.x & 7;
+  const int sub = threadIdx.x & 3;
   const int64_t rows = (int64_t)a.T * a.Hkv * 2;
-  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 3; w < rows;
-       w += ((int64_t)gridDim.x * blockDim.x) >> 3) {
+  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 2; w < rows;
+       w += ((int64_t)gridDim.x * blockDim.x) >> 2) {
     const int which = (int)(w & 1);           // 0 keys, 1 values
     const int64_t th = w >> 1;
     const int32_t t = (int32_t)(th / a.Hkv);
     const int32_t h = (int32_t)(th - (int64_t)t * a.Hkv);
     const int32_t slot = __ldg(a.slot_mapping + t);
-    // the eight lanes of a row share t, h and slot: every branch below is
+    // the four lanes of a row share t, h and slot: every branch below is
     // uniform across the row's lanes, so the row's shuffles stay converged
     const bool skip = slot < 0 || slot >= a.num_slots;
     if (slot >= a.num_slots && h == 0 && which == 0 && sub == 0)
       record_status(a.status, PKV_EDEVICE, slot, kKernelAppend);
-    const unsigned group = 0xffu << (threadIdx.x & 24);
+    const unsigned group = 0xfu << (threadIdx.x & 28);
     if (skip) continue;
     const uint4* src = reinterpret_cast<const uint4*>(
         (which ? a.v_new : a.k_new) + ((int64_t)t * a.Hkv + h) * D + sub * E);
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(256) kv_append_fp8_kernel(const AppendFp8Args 
 #pragma unroll
     for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
-    for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(group, amax, off));
+    for (int off = 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(group, amax, off));
     const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
     const int32_t blk = slot / a.block_size;
     const int32_t off = slot - blk * a.block_size;
@@ -220,11 +221,9 @@ __global__ void __launch_bounds__(256) kv_append_fp8_kernel(const AppendFp8Args 
           e4m3x2_from_f32(__fmul_rn(x[4 * k + 2], inv), __fmul_rn(x[4 * k + 3], inv));
       c[k] = c01 | (c23 << 16);
     }
-    uint8_t* dst = (which ? a.v8 : a.k8) + row * D + sub * E;
-    if constexpr (E == 16)
-      *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[2], c[3]);
-    else
-      *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[1]);
+    uint4* dst = reinterpret_cast<uint4*>((which ? a.v8 : a.k8) + row * D + sub * E);
+#pragma unroll
+    for (int k = 0; k < E / 16; ++k) dst[k] = make_uint4(c[4 * k], c[4 * k + 1], c[4 * k + 2], c[4 * k + 3]);
     if (sub == 0) (which ? a.vs : a.ks)[row] = __fdiv_rn(amax, 448.f);
   }
 }
@@ -322,7 +321,7 @@ extern "C" int pkv_kv_append_fp8(const void* k_new, const void* v_new,
   a.block_size = block_size;
   a.status = dev_status;
   const int64_t rows = (int64_t)T * Hkv * 2;
-  const int64_t want = (rows + 31) / 32;  // 32 rows per CTA of 256 threads
+  const int64_t want = (rows + 63) / 64;  // 64 rows per CTA of 256 threads
   const int64_t cap = (int64_t)dev->sm_count * 8;
   const int grid = (int)(want < cap ? want : cap);
   if (D == 128)

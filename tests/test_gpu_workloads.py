@@ -10,7 +10,8 @@ oracle, and a shared prefix must decode bit-identically to duplicated copies.
 Trace ("Deep Dive: continuous batching", sections Iteration-level scheduling
 and The prefill/decode mix): 200 iterations that admit, chunk-prefill, decode
 and retire requests, each iteration running kv_append, chunked paged prefill
-and paged decode over all active sequences. Checking every iteration in full
+and paged decode over all active sequences (the odd iterations through the
+single call pkv_iteration_run). Checking every iteration in full
 would take the oracle about eight minutes of one host core (about 2.3 s per
 iteration), so every 10th iteration is checked in full and a seeded 1/8 of
 the prefill requests and of the decode sequences of every other iteration.
@@ -89,7 +90,8 @@ def test_continuous_batching_trace():
         slots = ora.step(itr)
         got_slots = gpu.host_section(meta, "slot_mapping", itr.num_tokens)
         assert np.array_equal(got_slots, slots), f"iteration {itr.index}: slots differ"
-        pre_out, dec_out = gpu.run_iteration(itr, meta)
+        # odd iterations run through the one-call path (pkv_iteration_run)
+        pre_out, dec_out = gpu.run_iteration(itr, meta, fused=itr.index % 2 == 1)
         full = itr.index % 10 == 0
         n_pre, n_dec = len(itr.prefill), len(itr.decode)
         pick_pre = range(n_pre) if full else seeded_eighth(rng, n_pre)

@@ -192,3 +192,20 @@ def test_layout_sections_are_aligned_and_sized():
     assert L.cu_q_lens >= 4 * 77 and L.prefill_tables >= L.prefill_lens + 4 * 3
     assert L.decode_lens >= L.prefill_tables + 4 * 3 * 10
     assert L.total_bytes >= L.cow_pairs + 8 * 8
+
+
+def test_iteration_run_checks_before_any_launch():
+    # an iteration without tokens or copies launches nothing; bad sizes and a
+    # missing layout are refused before any CUDA call
+    import ctypes
+    from paged_kv_cache_281_gb300._lib import IterationLayout, lib
+    empty = IterationLayout()
+    args = lambda lay, npre, ndec, w: (None, lay, npre, ndec, w, None, None, None, None, None,
+                                       None, 64, 8, 2, 128, 16, ctypes.c_float(0.1), 0, None, 0,
+                                       None, 0, None, None)
+    assert lib().pkv_iteration_run(*args(ctypes.byref(empty), 0, 0, 4)) == 0
+    assert lib().pkv_iteration_run(*args(None, 0, 0, 4)) == PKV_EINVAL
+    assert lib().pkv_iteration_run(*args(ctypes.byref(empty), -1, 0, 4)) == PKV_EINVAL
+    one = IterationLayout()
+    one.n_tokens = 1
+    assert lib().pkv_iteration_run(*args(ctypes.byref(one), 0, 1, 4)) == PKV_EINVAL  # meta NULL

@@ -306,7 +306,7 @@ class DeviceTrace:
         sec = lambda name, count: buf[getattr(L, name):getattr(L, name) + 4 * count].view(
             torch.int32)
         npre, ndec = meta["n_prefill"], meta["n_decode"]
-        up = {"meta": buf, "n_pre": 0}
+        up = {"meta": buf, "n_pre": 0, "layout_meta": meta}
         if L.n_tokens:
             up["slots"] = sec("slot_mapping", L.n_tokens)
         if npre:
@@ -358,9 +358,30 @@ class DeviceTrace:
         rec(3)
         return pre_out, dec_out
 
-    def run_iteration(self, itr, meta, stream=None):
-        """Upload and run one iteration; returns (prefill_out, decode_out)."""
-        return self.launch(self.upload(itr, meta, stream), stream=stream)
+    def launch_fused(self, up, stream=None):
+        """The same GPU work through one library call (pkv_iteration_run):
+        copies, appends, prefill and decode from the uploaded metadata."""
+        cfg = self.cfg
+        meta = up["layout_meta"]
+        out = torch.empty(up["q"].shape[0], cfg.Hq, cfg.D, dtype=torch.bfloat16,
+                          device=self.device)
+        k = up.get("k", up["q"][:0, :cfg.Hkv])
+        v = up.get("v", up["q"][:0, :cfg.Hkv])
+        pkv.pkv_iteration_run(up["meta"], meta["layout"], meta["n_prefill"], meta["n_decode"],
+                              self.max_blocks, up["q"], k, v, out, self.k_cache, self.v_cache,
+                              self.scale, self.ws, self.pws, partition_size=self.partition_size,
+                              status=self.status, stream=stream)
+        n_pre = up["n_pre"]
+        return out[:n_pre], out[n_pre:]
+
+    def run_iteration(self, itr, meta, stream=None, fused=False):
+        """Upload and run one iteration, through the separate calls or through
+        pkv_iteration_run; returns (prefill_out, decode_out)."""
+        up = self.upload(itr, meta, stream)
+        if fused:
+            pre, dec = self.launch_fused(up, stream=stream)
+            return (pre if meta["n_prefill"] else None), (dec if meta["n_decode"] else None)
+        return self.launch(up, stream=stream)
 
     def finish(self, itr):
         for rid in itr.finished:
