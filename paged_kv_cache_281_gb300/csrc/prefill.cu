@@ -60,7 +60,14 @@ constexpr int kNS = 2;           // K and V ring stages
 // halves) and the tensor core still sees equal strides between 8-row groups
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows past 2^8
 constexpr int kWin = 256;            // block-table entries held in shared memory
-constexpr int kItemRing = 4;         // work-item indices handed from the producer to the others
+constexpr int kItemRing = 4;         // work items handed from the producer to the others
+// Barriers of the producer's passes (key tile j and value tile j - 1), used
+// round robin: a pass reuses a barrier only six passes later, by which time
+// the stage releases it waited for prove that the tensor-core warp has
+// finished waiting on the barrier's previous phase (a pass needs stages
+// freed by products of passes at most four back, items of one key tile
+// included), so a waiter never sees a barrier two phases ahead.
+constexpr int kPassBars = 6;
 
 // Two Q tiles per CTA share every K/V tile and take turns on the tensor
 // core: while the softmax warps of one tile turn its scores into
@@ -84,11 +91,12 @@ struct PCfg {
   // allocation (all 512 columns) then never waits for another CTA's
   static constexpr uint32_t kMinSmem = 120u * 1024;
   static constexpr uint32_t kSmem = kBytes + 1024 > kMinSmem ? kBytes + 1024 : kMinSmem;
-  // barriers: per Q tile full / free; K full/empty and V full/empty per
-  // stage; per Q tile: S full, P full (128 arrivals), P V done, output read
-  // out (128); work item posted / taken per item-ring slot; final
-  static constexpr int kBarQF = 0, kBarQE = 2, kBarKF = 4, kBarKE = kBarKF + kNS,
-                       kBarVF = kBarKE + kNS, kBarVE = kBarVF + kNS, kBarSF = kBarVE + kNS,
+  // barriers: per Q tile full / free; per producer pass (key tile j and
+  // value tile j - 1) full, round robin; K empty and V empty per stage;
+  // per Q tile: S full, P full (128 arrivals), P V done, output read out
+  // (128); work item posted / taken per item-ring slot; final
+  static constexpr int kBarQF = 0, kBarQE = 2, kBarKVF = 4, kBarKE = kBarKVF + kPassBars,
+                       kBarVE = kBarKE + kNS, kBarSF = kBarVE + kNS,
                        kBarPF = kBarSF + 2, kBarPV = kBarPF + 2, kBarOE = kBarPV + 2,
                        kBarIF = kBarOE + 2, kBarIE = kBarIF + kItemRing,
                        kBarFin = kBarIE + kItemRing, kNumBars = kBarFin + 1;
@@ -328,7 +336,7 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int32_t s_pages[kWin];  // window of the current sequence's block table
-  __shared__ int32_t s_item[kItemRing];
+  __shared__ PItem s_item[kItemRing];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (a.direct) {
@@ -363,11 +371,10 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
       mbar_init(bar(C::kBarOE + t), 128);
     }
     for (int i = 0; i < kNS; ++i) {
-      mbar_init(bar(C::kBarKF + i), 1);
       mbar_init(bar(C::kBarKE + i), 1);
-      mbar_init(bar(C::kBarVF + i), 1);
       mbar_init(bar(C::kBarVE + i), 1);
     }
+    for (int i = 0; i < kPassBars; ++i) mbar_init(bar(C::kBarKVF + i), 1);
     for (int i = 0; i < kItemRing; ++i) {
       mbar_init(bar(C::kBarIF + i), 1);
       mbar_init(bar(C::kBarIE + i), 1 + 8);  // the MMA warp and each softmax warp
@@ -393,26 +400,42 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
   tcgen05_before_sync();
   __syncthreads();
   tcgen05_after_sync();
-  const uint32_t tmem = s_tmem;
+  // the same value on every lane; the broadcast lets the compiler keep it
+  // (and every tensor-memory address built from it) in uniform registers
+  const uint32_t tmem = __shfl_sync(0xffffffffu, s_tmem, 0);
   grid_dep_wait();  // the plan (and everything before it) is complete
   const int n_items = a.direct ? 1 : *reinterpret_cast<volatile int32_t*>(a.n_items);
 
-  // The n-th item of this CTA (-1: no more; -2: the CTA's own grid position),
-  // as posted by the producer; every consuming warp calls it once per n, in
-  // order.
-  auto take_item = [&](int n, bool& ok) -> int {
+  // The n-th item of this CTA as the producer posted it (s < 0: no more);
+  // every consuming warp calls it once per n, in order. The values are the
+  // same on every lane (read from shared memory after one wait), and the
+  // broadcasts let the compiler keep what is derived from them in uniform
+  // registers.
+  auto take_item = [&](int n, bool& ok) -> PItem {
     const int slot = n % kItemRing;
+    PItem it;
+    it.s = -1;
     ok = wait_warp(C::kBarIF + slot, (n / kItemRing) & 1, 14);
-    if (!ok) return -1;
-    const int idx = *reinterpret_cast<volatile int32_t*>(&s_item[slot]);
+    if (!ok) return it;
+    const volatile PItem& v = s_item[slot];
+    it.s = __shfl_sync(0xffffffffu, v.s, 0);
+    it.kvh = __shfl_sync(0xffffffffu, v.kvh, 0);
+    it.c0 = __shfl_sync(0xffffffffu, v.c0, 0);
+    it.c = __shfl_sync(0xffffffffu, v.c, 0);
+    it.L = __shfl_sync(0xffffffffu, v.L, 0);
+    it.q0 = __shfl_sync(0xffffffffu, v.q0, 0);
+    it.kv_end = __shfl_sync(0xffffffffu, v.kv_end, 0);
+    it.nkt[0] = __shfl_sync(0xffffffffu, v.nkt[0], 0);
+    it.nkt[1] = __shfl_sync(0xffffffffu, v.nkt[1], 0);
+    it.nk = __shfl_sync(0xffffffffu, v.nk, 0);
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(C::kBarIE + slot));
-    return idx;
+    return it;
   };
 
-  // loads this CTA issued (per Q tile, and K and V tiles, counted by the
-  // producer): what a CTA that gives up waits for before its shared memory goes
-  int issued_q[2] = {0, 0}, issued_k = 0, issued_v = 0;
+  // loads this CTA issued (per Q tile, and producer passes of key and value
+  // tiles): what a CTA that gives up waits for before its shared memory goes
+  int issued_q[2] = {0, 0}, issued_p = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -428,16 +451,20 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
       const int slot = n % kItemRing;
       if (n >= kItemRing) ok = wait_warp(C::kBarIE + slot, (n / kItemRing - 1) & 1, 15);
       if (!ok) break;
-      // direct launches post their own item (index -2) once, then the end
+      // direct launches post their own item (index -2) once, then the end;
+      // the producer reads the item's description once and hands it over
+      // whole, so the other warps never wait on a global load for it
       int idx = 0;
-      if (lane == 0) {
-        idx = a.direct ? (n == 0 ? -2 : n_items) : atomicAdd(a.ticket, 1);
-        s_item[slot] = idx < n_items ? idx : -1;
-        mbar_arrive(bar(C::kBarIF + slot));  // release: the index is visible to the waiters
-      }
+      if (lane == 0) idx = a.direct ? (n == 0 ? -2 : n_items) : atomicAdd(a.ticket, 1);
       idx = __shfl_sync(0xffffffffu, idx, 0);
+      PItem it;
+      it.s = -1;
+      if (idx < n_items) it = load_item(a, idx, QT);
+      if (lane == 0) {
+        s_item[slot] = it;
+        mbar_arrive(bar(C::kBarIF + slot));  // release: the item is visible to the waiters
+      }
       if (idx >= n_items) break;
-      const PItem it = load_item(a, idx, QT);
       const int32_t* bt = a.block_tables + (int64_t)it.s * a.max_blocks_per_seq;
       const int npages = (it.kv_end + B - 1) / B;
       int win0 = 0;
@@ -486,19 +513,17 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
         const int32_t blk = mine ? s_pages[p0 + pl - win0] : -1;
         const bool valid = mine && blk >= 0 && blk < a.num_blocks;
         const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
-        const uint32_t kf = bar(C::kBarKF + stk), vf = bar(C::kBarVF + stv);
+        // one barrier per pass for the key and value boxes
+        const uint32_t full = bar(C::kBarKVF + issued_p % kPassBars);
         const uint32_t page_bytes = B * C::kHalves * 128u;
-        if (lane == 0 && do_k) mbar_arrive_expect_tx(kf, __popc(vmask & 0xffffu) * page_bytes);
-        if (lane == 16 && do_v) mbar_arrive_expect_tx(vf, __popc(vmask >> 16) * page_bytes);
+        if (lane == 0) mbar_arrive_expect_tx(full, __popc(vmask) * page_bytes);
         __syncwarp();
         if (mine && !valid) record_status(a.status, PKV_EDEVICE, blk, kKernelPrefill);
         if (valid)
           tma_load_4d((is_v ? base + C::kV + stv * C::kStage : base + C::kK + stk * C::kStage) +
                           pl * (B / 8) * C::kGroup,
-                      is_v ? &tmap_v : &tmap_k, 0, 0, 0, (blk * a.Hkv + it.kvh) * (B / 8),
-                      is_v ? vf : kf);
-        issued_k += do_k ? 1 : 0;
-        issued_v += do_v ? 1 : 0;
+                      is_v ? &tmap_v : &tmap_k, 0, 0, 0, (blk * a.Hkv + it.kvh) * (B / 8), full);
+        ++issued_p;
         __syncwarp();
       }
       jg += it.nk;
@@ -512,16 +537,10 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
     const uint64_t dq = umma_desc_sw128(base + C::kQ, 16, 1024);
     const uint64_t dk = umma_desc_sw128(base + C::kK, 16, C::kGroup);
     const uint64_t dv = umma_desc_sw128(base + C::kV, 1024, C::kGroup);
-    // A descriptor's start address (bytes / 16) sits in its low word and never
-    // carries into the high word (shared memory is below 2^18 bytes), so an
-    // offset is added to the low word alone
-    auto at = [](uint64_t d, uint32_t bytes) -> uint64_t {
-      uint64_t r;
-      asm("mov.b64 %0, {%1, %2};"
-          : "=l"(r)
-          : "r"((uint32_t)d + (bytes >> 4)), "r"((uint32_t)(d >> 32)));
-      return r;
-    };
+    // A descriptor's start address (bytes / 16) is its lowest field and never
+    // carries into the next one (shared memory is below 2^18 bytes), so an
+    // offset is a plain addition
+    auto at = [](uint64_t d, uint32_t bytes) -> uint64_t { return d + (bytes >> 4); };
     bool ok = true;
     int jg = 0;                        // K/V ring position
     int qn[2] = {0, 0}, pn[2] = {0, 0}, on[2] = {0, 0};  // Q loads, P tiles, outputs consumed
@@ -558,14 +577,19 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
       }
       __syncwarp();
     };
+    int pg = 0;  // producer passes consumed (pass p: key tile p and value tile p - 1)
     for (int n = 0; ok; ++n) {
-      const int idx = take_item(n, ok);
-      if (!ok || idx == -1) break;
-      const PItem it = load_item(a, idx, QT);
+      const PItem it = take_item(n, ok);
+      if (!ok || it.s < 0) break;
+      // the sequence's last page, and whether this item's last key tile loads
+      // it with rows past the sequence end (those rows are zeroed below)
+      const int B = a.block_size;
+      const int last_page = (it.L + B - 1) / B;
+      const bool zero_tail = it.L % B != 0 && (it.kv_end + B - 1) / B == last_page;
       // prologue: both tiles' first scores
       {
         const int st = jg % kNS;
-        ok = wait_warp(C::kBarKF + st, (jg / kNS) & 1, 4);
+        ok = wait_warp(C::kBarKVF + pg % kPassBars, (pg / kPassBars) & 1, 4);  // key tile 0
         for (int t = 0; ok && t < 2; ++t) {
           if (it.nkt[t] == 0) continue;
           ok = wait_warp(C::kBarQF + t, qn[t]++ & 1, 3);
@@ -579,15 +603,16 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
       }
       for (int j = 0; ok && j < it.nk; ++j) {
         const int g = jg + j, st = g % kNS;
-        ok = wait_warp(C::kBarVF + st, (g / kNS) & 1, 6);
+        // pass j + 1 brought value tile j and key tile j + 1
+        const int pj = pg + j + 1;
+        ok = wait_warp(C::kBarKVF + pj % kPassBars, (pj / kPassBars) & 1, 6);
         if (!ok) break;
         // Value rows of the sequence's last page past its end hold whatever
         // the pool holds there (stale or poisoned bytes) and must not reach
         // O, not even as NaN * 0: zero them when this tile loaded that page.
         // Eight lanes write one 128-byte row segment, four rows per pass.
-        const int B = a.block_size, key0 = j * kKeys;
-        const int last_page = (it.L + B - 1) / B;  // pages of the whole sequence
-        if (j == it.nk - 1 && it.L % B != 0 && (it.kv_end + B - 1) / B == last_page) {
+        const int key0 = j * kKeys;
+        if (zero_tail && j == it.nk - 1) {
           uint8_t* vp = base_ptr + C::kV + st * C::kStage;
           const int r_end = min(last_page * B - key0, kKeys);
           for (int r = it.L - key0 + (lane >> 3); r < r_end; r += 4)
@@ -600,7 +625,6 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
         __syncwarp();
         const bool more = j + 1 < it.nk;
         const int g1 = g + 1, st1 = g1 % kNS;
-        if (more) ok = wait_warp(C::kBarKF + st1, (g1 / kNS) & 1, 4);
         for (int t = 0; ok && t < 2; ++t) {
           if (j < it.nkt[t]) {
             ok = wait_warp(C::kBarPF + t, pn[t]++ & 1, 5);
@@ -620,6 +644,7 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
         __syncwarp();
       }
       jg += it.nk;
+      pg += it.nk + 1;
 #pragma unroll
       for (int t = 0; t < 2; ++t) on[t] += it.nkt[t] > 0 ? 1 : 0;
     }
@@ -645,9 +670,8 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
     bool ok = true;
     int sn = 0;  // score tiles of this Q tile
     for (int n = 0; ok; ++n) {
-      const int idx = take_item(n, ok);
-      if (!ok || idx == -1) break;
-      const PItem it = load_item(a, idx, QT);
+      const PItem it = take_item(n, ok);
+      if (!ok || it.s < 0) break;
       const int nk = it.nkt[t];
       const int qi = it.q0 + t * QT + r / G;
       const bool row_valid = qi < it.c;
@@ -721,11 +745,13 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
             const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
             const uint64_t p = f32x2_pack(p0, p1);
             l2 = f32x2_add(l2, p);
-            hi[e] = pack_bf16x2(p0, p1);
-            float d0, d1;
-            f32x2_unpack(f32x2_sub(p, f32x2_pack(bf16_lo_to_f32(hi[e]), bf16_hi_to_f32(hi[e]))),
-                         d0, d1);
-            lo[e] = pack_bf16x2(d0, d1);
+            // hi: the upper 16 bits of each probability (bf16 by truncation,
+            // one byte permute for the pair); lo = p - hi exactly in fp32,
+            // then rounded to bf16: hi + lo carries ~16 significant bits
+            const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+            hi[e] = __byte_perm(b0, b1, 0x7632);
+            lo[e] = pack_bf16x2(p0 - __uint_as_float(b0 & 0xffff0000u),
+                                p1 - __uint_as_float(b1 & 0xffff0000u));
           }
           const uint32_t col = 32 * (q >> 1) + 8 * (q & 1);
           tmem_st8(t_s + col, hi);
@@ -778,12 +804,10 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
       for (int t = 0; t < 2; ++t)
         if (issued_q[t])
           mbar_wait_bounded(bar(C::kBarQF + t), (issued_q[t] - 1) & 1, 4 * a.timeout_ns, 0);
-      for (int i = 0; i < kNS; ++i) {
-        // tiles i, i + kNS, ... went to stage i: wait for the last one's phase
-        const int nk = issued_k > i ? (issued_k - 1 - i) / kNS + 1 : 0;
-        const int nv = issued_v > i ? (issued_v - 1 - i) / kNS + 1 : 0;
-        if (nk) mbar_wait_bounded(bar(C::kBarKF + i), (nk - 1) & 1, 4 * a.timeout_ns, 0);
-        if (nv) mbar_wait_bounded(bar(C::kBarVF + i), (nv - 1) & 1, 4 * a.timeout_ns, 0);
+      for (int i = 0; i < kPassBars; ++i) {
+        // passes i, i + kPassBars, ... armed barrier i: wait for the last one's phase
+        const int np = issued_p > i ? (issued_p - 1 - i) / kPassBars + 1 : 0;
+        if (np) mbar_wait_bounded(bar(C::kBarKVF + i), (np - 1) & 1, 4 * a.timeout_ns, 0);
       }
     }
     __syncthreads();
