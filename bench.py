@@ -699,13 +699,13 @@ def run_trace(args):
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         pkv.pkv_check_status(run.status)
-        return 1e3 * wall, 1e3 * (host - run.wait_s)
+        return 1e3 * wall, 1e3 * (host - run.wait_s), 1e3 * run.lib_s
 
     one_pass(False)                       # warm-up pass over the whole trace
     live_pass()
     with ClockSampler(local) as clocks:
         evs, pass_ms = one_pass(True)
-        live_ms, live_host_ms = live_pass()
+        live_ms, live_host_ms, live_lib_ms = live_pass()
     t_app = sum(e[0].elapsed_time(e[1]) for e in evs)
     t_pre = sum(e[1].elapsed_time(e[2]) for e in evs)
     t_dec = sum(e[2].elapsed_time(e[3]) for e in evs)
@@ -744,13 +744,16 @@ def run_trace(args):
         "iteration_loop": {
             "tokens_per_s": tokens / (live_ms * 1e-3), "wall_ms": live_ms,
             "ms_per_iteration": live_ms / len(its), "host_ms": live_host_ms,
+            "library_host_ms": live_lib_ms,
             "gpu_ms": gpu_ms,
             "note": "host and GPU on one clock: per iteration one pkv_iteration_prepare call "
                     "(slots, cu_q_lens, lengths, block tables into pinned memory), one "
                     "metadata upload and one pkv_iteration_run call (append, prefill, "
                     "decode), the host waiting only for a free "
                     "staging buffer (4 in a ring); host_ms is the host's own work in the loop "
-                    "(allocator, metadata, launches); token values resident on the device"},
+                    "(allocator, metadata, launches), library_host_ms the part of it inside the "
+                    "two library calls (argument marshalling included); token values resident "
+                    "on the device"},
         "roofline": {"bound": "hbm", "kernel": "pkv_paged_attention_decode", "achieved": dec_gbs,
                      "peak": peak_hbm, "unit": "GB/s", "frac": dec_gbs / peak_hbm,
                      "traffic": None},

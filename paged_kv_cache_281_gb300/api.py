@@ -61,12 +61,15 @@ def _check_device(name: str, index: int, current: int) -> None:
                          f"cuda:{current}; call under torch.cuda.device({index})")
 
 
-def _dev(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int | None = None):
+def _dev(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int | None = None,
+         cur: int | None = None):
+    """Checks one tensor argument; ``cur`` is the current device (queried when
+    not given, so a call with many tensors can query it once)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must live on a CUDA device")
-    _check_device(name, t.device.index, torch.cuda.current_device())
+    _check_device(name, t.device.index, torch.cuda.current_device() if cur is None else cur)
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -250,12 +253,13 @@ def pkv_iteration_run(meta, layout, n_prefill: int, n_decode: int, max_blocks_pe
     """``pkv_iteration_run``: the iteration's copies, appends, prefill and
     decode from one device copy (``meta``, uint8) of the buffer
     ``iteration_prepare`` filled; ``layout`` is what it returned."""
-    N, Hkv, B, D = _pool_shape(k_cache, v_cache)
-    _dev(meta, "meta", torch.uint8, 1)
+    cur = torch.cuda.current_device()
+    N, Hkv, B, D = _pool_shape(k_cache, v_cache, cur)
+    _dev(meta, "meta", torch.uint8, 1, cur)
     for name, t in (("q", q), ("out", out), ("k_new", k_new), ("v_new", v_new)):
-        _dev(t, name, torch.bfloat16, 3)
-    _dev(decode_ws, "decode_ws", torch.uint8, 1)
-    _dev(prefill_ws, "prefill_ws", torch.uint8, 1)
+        _dev(t, name, torch.bfloat16, 3, cur)
+    _dev(decode_ws, "decode_ws", torch.uint8, 1, cur)
+    _dev(prefill_ws, "prefill_ws", torch.uint8, 1, cur)
     T, Hq = int(layout.n_tokens), int(q.shape[1])
     if meta.numel() < layout.total_bytes:
         raise ValueError("meta is shorter than the layout")
@@ -282,9 +286,9 @@ def iteration_layout_bytes(n_prefill: int, n_decode: int, n_tokens: int,
 
 # ---------------------------------------------------------------- GPU calls
 
-def _pool_shape(k_cache: torch.Tensor, v_cache: torch.Tensor):
-    _dev(k_cache, "k_cache", torch.bfloat16, 4)
-    _dev(v_cache, "v_cache", torch.bfloat16, 4)
+def _pool_shape(k_cache: torch.Tensor, v_cache: torch.Tensor, cur: int | None = None):
+    _dev(k_cache, "k_cache", torch.bfloat16, 4, cur)
+    _dev(v_cache, "v_cache", torch.bfloat16, 4, cur)
     if k_cache.shape != v_cache.shape:
         raise ValueError("k_cache and v_cache must have the same shape")
     return tuple(int(x) for x in k_cache.shape)  # N, Hkv, B, D
@@ -306,10 +310,11 @@ def pkv_debug_set_wait(force_timeout: bool, timeout_ns: int = 0) -> None:
 
 
 def pkv_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, status=None, stream=None) -> None:
-    N, Hkv, B, D = _pool_shape(k_cache, v_cache)
-    _dev(k_new, "k_new", torch.bfloat16, 3)
-    _dev(v_new, "v_new", torch.bfloat16, 3)
-    _dev(slot_mapping, "slot_mapping", torch.int32, 1)
+    cur = torch.cuda.current_device()
+    N, Hkv, B, D = _pool_shape(k_cache, v_cache, cur)
+    _dev(k_new, "k_new", torch.bfloat16, 3, cur)
+    _dev(v_new, "v_new", torch.bfloat16, 3, cur)
+    _dev(slot_mapping, "slot_mapping", torch.int32, 1, cur)
     T = int(slot_mapping.shape[0])
     if k_new.shape != (T, Hkv, D) or v_new.shape != (T, Hkv, D):
         raise ValueError(f"k_new/v_new must be [{T}, {Hkv}, {D}]")
@@ -319,8 +324,9 @@ def pkv_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, status=None, str
 
 
 def pkv_block_copy(k_cache, v_cache, pairs, status=None, stream=None) -> None:
-    N, Hkv, B, D = _pool_shape(k_cache, v_cache)
-    _dev(pairs, "pairs", torch.int32, 2)
+    cur = torch.cuda.current_device()
+    N, Hkv, B, D = _pool_shape(k_cache, v_cache, cur)
+    _dev(pairs, "pairs", torch.int32, 2, cur)
     if pairs.shape[1] != 2:
         raise ValueError("pairs must be [n, 2]")
     check(lib().pkv_block_copy(k_cache.data_ptr(), v_cache.data_ptr(), pairs.data_ptr(),
@@ -353,12 +359,13 @@ def pkv_decode_workspace_bytes(S: int, Hq: int, D: int, max_context_len: int,
 def pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
                                max_context_len: int, scale: float, workspace,
                                partition_size: int = 0, status=None, stream=None) -> None:
-    N, Hkv, B, D = _pool_shape(k_cache, v_cache)
-    _dev(q, "q", torch.bfloat16, 3)
-    _dev(out, "out", torch.bfloat16, 3)
-    _dev(block_tables, "block_tables", torch.int32, 2)
-    _dev(context_lens, "context_lens", torch.int32, 1)
-    _dev(workspace, "workspace", torch.uint8, 1)
+    cur = torch.cuda.current_device()
+    N, Hkv, B, D = _pool_shape(k_cache, v_cache, cur)
+    _dev(q, "q", torch.bfloat16, 3, cur)
+    _dev(out, "out", torch.bfloat16, 3, cur)
+    _dev(block_tables, "block_tables", torch.int32, 2, cur)
+    _dev(context_lens, "context_lens", torch.int32, 1, cur)
+    _dev(workspace, "workspace", torch.uint8, 1, cur)
     S, Hq = int(q.shape[0]), int(q.shape[1])
     if q.shape[2] != D or out.shape != q.shape:
         raise ValueError("q/out must be [S, Hq, D] with the pools' D")
@@ -509,13 +516,14 @@ def pkv_prefill_workspace_bytes(S: int, total_q: int, Hq: int, D: int) -> int:
 def pkv_paged_attention_prefill(out, q, cu_q_lens, context_lens, k_cache, v_cache, block_tables,
                                 max_q_len: int, max_context_len: int, scale: float, workspace,
                                 status=None, stream=None) -> None:
-    N, Hkv, B, D = _pool_shape(k_cache, v_cache)
-    _dev(q, "q", torch.bfloat16, 3)
-    _dev(out, "out", torch.bfloat16, 3)
-    _dev(cu_q_lens, "cu_q_lens", torch.int32, 1)
-    _dev(context_lens, "context_lens", torch.int32, 1)
-    _dev(block_tables, "block_tables", torch.int32, 2)
-    _dev(workspace, "workspace", torch.uint8, 1)
+    cur = torch.cuda.current_device()
+    N, Hkv, B, D = _pool_shape(k_cache, v_cache, cur)
+    _dev(q, "q", torch.bfloat16, 3, cur)
+    _dev(out, "out", torch.bfloat16, 3, cur)
+    _dev(cu_q_lens, "cu_q_lens", torch.int32, 1, cur)
+    _dev(context_lens, "context_lens", torch.int32, 1, cur)
+    _dev(block_tables, "block_tables", torch.int32, 2, cur)
+    _dev(workspace, "workspace", torch.uint8, 1, cur)
     total_q, Hq = int(q.shape[0]), int(q.shape[1])
     S = int(context_lens.shape[0])
     if cu_q_lens.shape[0] != S + 1 or block_tables.shape[0] != S:

@@ -265,6 +265,7 @@ class DeviceTrace:
         self.staged = [None] * self.RING   # event after the last upload from each buffer
         self.next = 0
         self.wait_s = 0.0                   # host time spent waiting for a free buffer
+        self.lib_s = 0.0                    # host time inside the library's two per-iteration calls
 
     def host_metadata(self, itr):
         """The iteration's host side: new sequences for admitted requests,
@@ -279,9 +280,11 @@ class DeviceTrace:
             self.wait_s += time.perf_counter() - w0
             self.staged[k] = None
         work = itr.work
-        layout = self.alloc.iteration_prepare([self.sid[w.rid] for w in work],
-                                              [w.n for w in work], len(itr.prefill),
-                                              self.max_blocks, self.staging[k])
+        ids, counts = [self.sid[w.rid] for w in work], [w.n for w in work]
+        t0 = time.perf_counter()
+        layout = self.alloc.iteration_prepare(ids, counts, len(itr.prefill), self.max_blocks,
+                                              self.staging[k])
+        self.lib_s += time.perf_counter() - t0
         return {"staging": k, "layout": layout, "n_prefill": len(itr.prefill),
                 "n_decode": len(work) - len(itr.prefill)}
 
@@ -367,10 +370,12 @@ class DeviceTrace:
                           device=self.device)
         k = up.get("k", up["q"][:0, :cfg.Hkv])
         v = up.get("v", up["q"][:0, :cfg.Hkv])
+        t0 = time.perf_counter()
         pkv.pkv_iteration_run(up["meta"], meta["layout"], meta["n_prefill"], meta["n_decode"],
                               self.max_blocks, up["q"], k, v, out, self.k_cache, self.v_cache,
                               self.scale, self.ws, self.pws, partition_size=self.partition_size,
                               status=self.status, stream=stream)
+        self.lib_s += time.perf_counter() - t0
         n_pre = up["n_pre"]
         return out[:n_pre], out[n_pre:]
 
