@@ -630,6 +630,10 @@ def run_trace(args):
     rank, world, local = dist_info()
     torch.cuda.set_device(local)
     cfg = TraceConfig(iterations=args.iterations)
+    # decode split-K partition: 2048 tokens unless given (on this trace, whose
+    # contexts stay below 2,560 tokens, 2048 and 4096 decode 4.6% faster than
+    # the library's default 1024: fewer partial states to merge)
+    P = args.partition_size or 2048
     t0 = time.perf_counter()
     its = list(trace_iterations(cfg))
     gen_s = time.perf_counter() - t0
@@ -639,7 +643,7 @@ def run_trace(args):
     # for the whole trace (timed as the scheduler cost), uploaded to the
     # device; then the GPU side runs back to back, so the events time kernels
     # rather than the host's launch latency.
-    dt = DeviceTrace(cfg, partition_size=args.partition_size)
+    dt = DeviceTrace(cfg, partition_size=P)
     host_s, ups, stats = 0.0, [], []
     for itr in its:
         h0 = time.perf_counter()
@@ -661,7 +665,7 @@ def run_trace(args):
 
     def one_pass(timed):
         # fresh pools; the metadata above drives it
-        run = DeviceTrace(cfg, partition_size=args.partition_size)
+        run = DeviceTrace(cfg, partition_size=P)
         evs = []
         t_all = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
         t_all[0].record(stream)
@@ -682,7 +686,7 @@ def run_trace(args):
         # the metadata and the launches, without waiting for the GPU; token
         # values (in a model, outputs of the projections) are already on the
         # device. Wall clock from the first host call to the last kernel's end.
-        run = DeviceTrace(cfg, partition_size=args.partition_size)
+        run = DeviceTrace(cfg, partition_size=P)
         torch.cuda.synchronize()
         host = 0.0
         t0 = time.perf_counter()
@@ -729,7 +733,7 @@ def run_trace(args):
         "config": {"workload": "trace: 200 iterations, Poisson(8) arrivals, prompts U[32,1024] "
                                "in chunks <= 512, outputs Geometric(1/256) <= 1536, <= 256 "
                                "running, 64/8 heads, D=128, B=16, 40,960-block pool",
-                   "decode_partition_size": args.partition_size or 1024,
+                   "decode_partition_size": P,
                    "prefill_tokens": int(sum(x[1] for x in stats)),
                    "decode_tokens": int(sum(x[2] for x in stats)),
                    "l2": "decode reads ~0.4 GB of K/V per iteration (> 129 MB L2)"},

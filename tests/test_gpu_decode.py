@@ -65,7 +65,7 @@ def test_shapes_ragged(D, G, B):
     check_against_oracle(w, partition_size=128)
 
 
-@pytest.mark.parametrize("partition", [16, 48, 256, 0])
+@pytest.mark.parametrize("partition", [16, 48, 256, 2048, 0])
 def test_partition_sizes_agree(partition):
     w = make_decode_workload("parts", (1, 16, 17, 511, 512, 513, 1500, 2049), Hq=32, Hkv=8,
                              D=128, block_size=16, seed=1100)
