@@ -1,0 +1,120 @@
+"""One iteration through the two per-iteration calls, against the oracle.
+
+``pkv_iteration_prepare`` reserves every work's slots and writes the
+iteration's metadata into one host buffer; one copy takes it to the device;
+``pkv_iteration_run`` launches the copy-on-write copies, the appends, the
+prefill of the prompt chunks and the decode of the running sequences from
+it ("Deep Dive: continuous batching", sections Iteration-level scheduling and
+The prefill/decode mix; "Batching, Scheduling, and Paging", sections
+PagedAttention and Block sharing). Prompts are forked into samples so that
+half-full shared blocks are copied on their first divergent write. The
+oracle applies the same appends one by one with its own allocator model,
+copies, writes and attends; pools must match bit for bit, attention within
+|gpu - ref| <= 2e-3 + 1e-2 |ref|.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_281_gb300 as pkv
+from oracle import attention, cache, paging
+from oracle.harness import empty_pools
+from tests.test_gpu_decode import assert_close
+from workloads import normal_bf16
+from workloads.device import bf16_bits, bf16_to_f64, poisoned_pools, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+N, B, Hq, Hkv, D, W = 200, 16, 16, 4, 128, 24
+
+
+class Sides:
+    def __init__(self):
+        self.lib = pkv.BlockAllocator(N, B)
+        self.ora = paging.BlockAllocator(N, B)
+        self.kc, self.vc = poisoned_pools(N, Hkv, B, D)
+        self.ok, self.ov = empty_pools(N, Hkv, B, D)
+        self.status = pkv.new_status()
+        self.ids = []            # (library id, oracle id) per sequence
+        self.buf = torch.empty(1 << 20, dtype=torch.uint8).pin_memory()
+        self.scale = 1.0 / np.sqrt(D)
+
+    def new(self):
+        self.ids.append((self.lib.seq_create(), self.ora.create()))
+        return len(self.ids) - 1
+
+    def fork(self, i):
+        a, b = self.ids[i]
+        self.ids.append((self.lib.seq_fork(a), self.ora.fork(b)))
+        return len(self.ids) - 1
+
+    def iteration(self, works, seed):
+        """``works``: [(sequence index, token count)], prompt chunks first
+        (count > 1 or a first token), then decodes (count 1)."""
+        n_prefill = sum(1 for _, c, kind in works if kind == "prefill")
+        counts = [c for _, c, _ in works]
+        T = sum(counts)
+        q = normal_bf16((T, Hq, D), seed)
+        k = normal_bf16((T, Hkv, D), seed + 1)
+        v = normal_bf16((T, Hkv, D), seed + 2)
+        # library: one prepare, one copy, one run
+        L = self.lib.iteration_prepare([self.ids[i][0] for i, _, _ in works], counts, n_prefill,
+                                       W, self.buf)
+        meta = self.buf[:L.total_bytes].cuda()
+        out = torch.full((T, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        dws = torch.empty(pkv.pkv_decode_workspace_bytes(max(1, len(works)), Hq, D, W * B),
+                          dtype=torch.uint8, device="cuda")
+        pws = torch.empty(pkv.pkv_prefill_workspace_bytes(max(1, n_prefill), T, Hq, D),
+                          dtype=torch.uint8, device="cuda")
+        pkv.pkv_iteration_run(meta, L, n_prefill, len(works) - n_prefill, W, to_dev_bf16(q),
+                              to_dev_bf16(k), to_dev_bf16(v), out, self.kc, self.vc, self.scale,
+                              dws, pws, status=self.status)
+        pkv.pkv_check_status(self.status)
+        # oracle: the same appends one by one, copies first, then the writes
+        slots, pairs = [], []
+        for i, c, _ in works:
+            s, p = self.ora.append_slots(self.ids[i][1], c)
+            slots.extend(s)
+            pairs.extend(p)
+        assert L.n_cow == len(pairs)
+        got_slots = self.buf[L.slot_mapping:L.slot_mapping + 4 * T].numpy().view(np.int32)
+        assert np.array_equal(got_slots, slots)
+        cache.block_copy(self.ok, self.ov, pairs)
+        cache.append(self.ok, self.ov, k, v, slots, B)
+        assert np.array_equal(bf16_bits(self.kc), self.ok)
+        assert np.array_equal(bf16_bits(self.vc), self.ov)
+        got = bf16_to_f64(out)
+        row = 0
+        for i, c, kind in works:
+            sid = self.ids[i][1]
+            table, length = [self.ora.block_table(sid)], [self.ora.seq_len(sid)]
+            if kind == "prefill":
+                ref = attention.prefill(q[row:row + c], [0, c], length, self.ok, self.ov, table,
+                                        B, self.scale)
+            else:
+                ref = attention.decode(q[row:row + 1], self.ok, self.ov, table, length, B,
+                                       self.scale)
+            assert_close(got[row:row + c], ref, f"sequence {i} ({kind})")
+            row += c
+        return L
+
+
+def test_iteration_with_forks_and_copy_on_write():
+    sd = Sides()
+    prompts = [sd.new() for _ in range(4)]
+    # iteration 0: four prompts prefilled (lengths 40, 77, 130, 16)
+    sd.iteration([(p, c, "prefill") for p, c in zip(prompts, (40, 77, 130, 16))], 9100)
+    # two more samples per prompt share its blocks, half-full last ones included
+    samples = [s for p in prompts for s in (p, sd.fork(p), sd.fork(p))]
+    # iteration 1: every sample decodes one token; the first two sharers of a
+    # half-full block copy it, the last writes in place
+    L = sd.iteration([(s, 1, "decode") for s in samples], 9200)
+    assert L.n_cow == 6
+    # iteration 2: prompt chunks for some samples, decodes for the others
+    works = [(samples[0], 21, "prefill"), (samples[4], 5, "prefill"), (samples[10], 33, "prefill")]
+    works += [(s, 1, "decode") for s in samples if s not in (samples[0], samples[4], samples[10])]
+    sd.iteration(works, 9300)
+    assert sd.lib.num_free_blocks() == sd.ora.num_free()
