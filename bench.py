@@ -692,13 +692,10 @@ def run_trace(args):
         t0 = time.perf_counter()
         for itr, up in zip(its, ups):
             h0 = time.perf_counter()
-            meta = run.host_metadata(itr)
+            k = up.get("k", up["q"][:0, :cfg.Hkv])
+            v = up.get("v", up["q"][:0, :cfg.Hkv])
+            run.step(itr, up["q"], k, v, stream=stream)
             run.finish(itr)
-            live = run.upload_meta(meta, stream)
-            live.update(q=up["q"], n_pre=up["n_pre"])
-            if "k" in up:
-                live.update(k=up["k"], v=up["v"])
-            run.launch_fused(live, stream=stream)
             host += time.perf_counter() - h0
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
@@ -750,14 +747,14 @@ def run_trace(args):
             "ms_per_iteration": live_ms / len(its), "host_ms": live_host_ms,
             "library_host_ms": live_lib_ms,
             "gpu_ms": gpu_ms,
-            "note": "host and GPU on one clock: per iteration one pkv_iteration_prepare call "
-                    "(slots, cu_q_lens, lengths, block tables into pinned memory), one "
-                    "metadata upload and one pkv_iteration_run call (append, prefill, "
-                    "decode), the host waiting only for a free "
+            "note": "host and GPU on one clock: per iteration one pkv_iteration_step call "
+                    "(slots, cu_q_lens, lengths, block tables into pinned memory, one copy to "
+                    "the device, then append, prefill and decode), the host waiting only for "
+                    "a free "
                     "staging buffer (4 in a ring); host_ms is the host's own work in the loop "
                     "(allocator, metadata, launches), library_host_ms the part of it inside the "
-                    "two library calls (argument marshalling included); token values resident "
-                    "on the device"},
+                    "library call (argument marshalling included); token values resident on "
+                    "the device"},
         "roofline": {"bound": "hbm", "kernel": "pkv_paged_attention_decode", "achieved": dec_gbs,
                      "peak": peak_hbm, "unit": "GB/s", "frac": dec_gbs / peak_hbm,
                      "traffic": None},

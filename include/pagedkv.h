@@ -179,6 +179,27 @@ int pkv_iteration_run(const void* meta, const pkv_iteration_layout* layout, int3
                       size_t decode_ws_bytes, void* prefill_ws, size_t prefill_ws_bytes,
                       int32_t* dev_status, void* stream);
 
+/* Both halves of an iteration in one call: pkv_iteration_prepare into
+ * host_buf, one cudaMemcpyAsync of the layout's total_bytes to dev_buf on
+ * `stream`, then pkv_iteration_run from dev_buf. Arguments as in those two
+ * calls; *layout and *n_fit are returned as pkv_iteration_prepare returns
+ * them (on PKV_ENOMEM nothing was changed, copied or launched).
+ *   host_buf : host memory the caller owns; pinned memory keeps the copy
+ *              asynchronous. The copy reads it after this call returns:
+ *              do not write into it again until the copy has completed (an
+ *              event recorded after the call, or a ring of buffers).
+ *   dev_buf  : device memory of at least total_bytes, 64-byte aligned;
+ *              stream order protects it from the next iteration's copy. */
+int pkv_iteration_step(pkv_alloc* a, const int64_t* seqs, const int32_t* counts,
+                       int32_t n_prefill, int32_t n_decode, int32_t max_blocks_per_seq,
+                       void* host_buf, size_t host_bytes, void* dev_buf, size_t dev_bytes,
+                       const void* q, const void* k_new, const void* v_new, void* out,
+                       void* k_cache, void* v_cache, int32_t num_blocks, int32_t Hq, int32_t Hkv,
+                       int32_t D, int32_t block_size, float scale, int32_t partition_size,
+                       void* decode_ws, size_t decode_ws_bytes, void* prefill_ws,
+                       size_t prefill_ws_bytes, int32_t* dev_status, void* stream,
+                       pkv_iteration_layout* layout, int32_t* n_fit);
+
 /* Preemption ("Batching, Scheduling, and Paging", section PagedAttention: if
  * HBM runs out a request is evicted, swapped to CPU memory or discarded and
  * recomputed later).

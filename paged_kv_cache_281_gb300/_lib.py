@@ -50,6 +50,9 @@ SIGNATURES = {
     "pkv_iteration_run": (ctypes.c_int, [vp, P(IterationLayout), i32, i32, i32, vp, vp, vp, vp,
                                          vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp,
                                          sz, vp, vp]),
+    "pkv_iteration_step": (ctypes.c_int, [vp, P(i64), P(i32), i32, i32, i32, vp, sz, vp, sz, vp,
+                                          vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
+                                          vp, sz, vp, sz, vp, vp, P(IterationLayout), P(i32)]),
     "pkv_seq_swap_out": (ctypes.c_int, [vp, i64, P(i32), i32, P(i32)]),
     "pkv_seq_swap_in": (ctypes.c_int, [vp, i64, P(i32), i32, P(i32)]),
     "pkv_seq_create_cached": (ctypes.c_int, [vp, P(i32), i32, P(i64), P(i32)]),

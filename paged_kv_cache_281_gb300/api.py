@@ -30,7 +30,7 @@ __all__ = [
     "pkv_debug_set_wait", "new_status", "new_fp8_pools", "pkv_kv_append_fp8",
     "pkv_paged_attention_decode_fp8", "pkv_decode_shared_workspace_bytes",
     "pkv_paged_attention_decode_shared", "IterationLayout", "iteration_layout_bytes",
-    "pkv_iteration_run",
+    "pkv_iteration_run", "pkv_iteration_step",
 ]
 
 
@@ -272,6 +272,50 @@ def pkv_iteration_run(meta, layout, n_prefill: int, n_decode: int, max_blocks_pe
         out.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), N, Hq, Hkv, D, B, float(scale),
         int(partition_size), decode_ws.data_ptr(), int(decode_ws.numel()), prefill_ws.data_ptr(),
         int(prefill_ws.numel()), _ptr(status), _stream(stream)))
+
+
+def pkv_iteration_step(alloc: BlockAllocator, seqs, counts, n_prefill: int,
+                       max_blocks_per_seq: int, host_buf, dev_buf, q, k_new, v_new, out, k_cache,
+                       v_cache, scale: float, decode_ws, prefill_ws, partition_size: int = 0,
+                       status=None, stream=None):
+    """``pkv_iteration_step``: ``iteration_prepare`` into ``host_buf`` (a
+    pinned CPU uint8 tensor), one asynchronous copy to ``dev_buf`` (a device
+    uint8 tensor) and ``pkv_iteration_run``, in one call. Do not reuse
+    ``host_buf`` before the copy has completed. Returns the layout; raises
+    PagedKVError (PKV_ENOMEM, nothing changed) with ``n_fit`` set."""
+    cur = torch.cuda.current_device()
+    N, Hkv, B, D = _pool_shape(k_cache, v_cache, cur)
+    _dev(dev_buf, "dev_buf", torch.uint8, 1, cur)
+    for name, t in (("q", q), ("out", out), ("k_new", k_new), ("v_new", v_new)):
+        _dev(t, name, torch.bfloat16, 3, cur)
+    _dev(decode_ws, "decode_ws", torch.uint8, 1, cur)
+    _dev(prefill_ws, "prefill_ws", torch.uint8, 1, cur)
+    if host_buf.is_cuda or host_buf.dtype != torch.uint8 or not host_buf.is_contiguous():
+        raise ValueError("host_buf must be a contiguous CPU uint8 tensor (pinned)")
+    ids = np.ascontiguousarray(seqs, dtype=np.int64)
+    cnt = np.ascontiguousarray(counts, dtype=np.int32)
+    n = int(ids.shape[0])
+    T, Hq = int(cnt.sum()), int(q.shape[1])
+    if cnt.shape[0] != n or not 0 <= n_prefill <= n:
+        raise ValueError("seqs and counts must have the same length >= n_prefill")
+    if q.shape != (T, Hq, D) or out.shape != q.shape or k_new.shape != (T, Hkv, D) or \
+            v_new.shape != k_new.shape:
+        raise ValueError(f"q/out must be [{T}, Hq, {D}] and k_new/v_new [{T}, {Hkv}, {D}]")
+    layout, fit = IterationLayout(), ctypes.c_int32()
+    rc = lib().pkv_iteration_step(
+        alloc._h, ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+        cnt.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(n_prefill), n - int(n_prefill),
+        int(max_blocks_per_seq), host_buf.data_ptr(), int(host_buf.numel()),
+        dev_buf.data_ptr(), int(dev_buf.numel()), q.data_ptr(), k_new.data_ptr(),
+        v_new.data_ptr(), out.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), N, Hq, Hkv, D,
+        B, float(scale), int(partition_size), decode_ws.data_ptr(), int(decode_ws.numel()),
+        prefill_ws.data_ptr(), int(prefill_ws.numel()), _ptr(status), _stream(stream),
+        ctypes.byref(layout), ctypes.byref(fit))
+    if rc != 0:
+        err = PagedKVError(rc, pkv_last_error())
+        err.n_fit = fit.value
+        raise err
+    return layout
 
 
 def iteration_layout_bytes(n_prefill: int, n_decode: int, n_tokens: int,

@@ -11,7 +11,7 @@
 // it only saves the host the per-kernel argument handling of separate calls.
 #include <cstdint>
 
-#include "internal.h"
+#include "host_util.h"
 
 using pkv::fail;
 using pkv::ok;
@@ -64,4 +64,35 @@ extern "C" int pkv_iteration_run(const void* meta, const pkv_iteration_layout* l
       return rc;
   }
   return ok();
+}
+
+// Both halves of an iteration in one call: the host work of
+// pkv_iteration_prepare into the caller's pinned buffer, one asynchronous
+// copy of it to the caller's device buffer, and pkv_iteration_run from there.
+extern "C" int pkv_iteration_step(pkv_alloc* a, const int64_t* seqs, const int32_t* counts,
+                                  int32_t n_prefill, int32_t n_decode,
+                                  int32_t max_blocks_per_seq, void* host_buf,
+                                  size_t host_bytes, void* dev_buf, size_t dev_bytes,
+                                  const void* q, const void* k_new, const void* v_new, void* out,
+                                  void* k_cache, void* v_cache, int32_t num_blocks, int32_t Hq,
+                                  int32_t Hkv, int32_t D, int32_t block_size, float scale,
+                                  int32_t partition_size, void* decode_ws,
+                                  size_t decode_ws_bytes, void* prefill_ws,
+                                  size_t prefill_ws_bytes, int32_t* dev_status, void* stream,
+                                  pkv_iteration_layout* layout, int32_t* n_fit) {
+  const char* who = "pkv_iteration_step";
+  PKV_REQUIRE(dev_buf, "%s: dev_buf is NULL", who);
+  if (int rc = pkv_iteration_prepare(a, seqs, counts, n_prefill, n_decode, max_blocks_per_seq,
+                                     host_buf, host_bytes, layout, n_fit))
+    return rc;
+  PKV_REQUIRE(dev_bytes >= (size_t)layout->total_bytes,
+              "%s: dev_buf has %zu bytes, needs %lld (the allocator work is done)", who,
+              dev_bytes, (long long)layout->total_bytes);
+  cudaError_t err = cudaMemcpyAsync(dev_buf, host_buf, (size_t)layout->total_bytes,
+                                    cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return pkv::cuda_fail(err, "pkv_iteration_step: metadata copy");
+  return pkv_iteration_run(dev_buf, layout, n_prefill, n_decode, max_blocks_per_seq, q, k_new,
+                           v_new, out, k_cache, v_cache, num_blocks, Hq, Hkv, D, block_size,
+                           scale, partition_size, decode_ws, decode_ws_bytes, prefill_ws,
+                           prefill_ws_bytes, dev_status, stream);
 }

@@ -10,8 +10,9 @@ oracle, and a shared prefix must decode bit-identically to duplicated copies.
 Trace ("Deep Dive: continuous batching", sections Iteration-level scheduling
 and The prefill/decode mix): 200 iterations that admit, chunk-prefill, decode
 and retire requests, each iteration running kv_append, chunked paged prefill
-and paged decode over all active sequences (the odd iterations through the
-single call pkv_iteration_run). Checking every iteration in full
+and paged decode over all active sequences (one iteration in three through
+the separate calls, one through pkv_iteration_run, one through
+pkv_iteration_step). Checking every iteration in full
 would take the oracle about eight minutes of one host core (about 2.3 s per
 iteration), so every 10th iteration is checked in full and a seeded 1/8 of
 the prefill requests and of the decode sequences of every other iteration.
@@ -24,7 +25,7 @@ import pytest
 import torch
 
 from workloads.device import (DeviceTrace, bf16_bits, bf16_to_f64, decode_shared_prefix,
-                               run_decode, setup_decode, setup_shared_prefix)
+                               run_decode, setup_decode, setup_shared_prefix, to_dev_bf16)
 from oracle.harness import OracleTrace, build_shared_prefix_state
 from tests.test_gpu_decode import assert_close
 from oracle import attention
@@ -86,12 +87,18 @@ def test_continuous_batching_trace():
     rng = generator(cfg.seed, 77)
     checked_pre = checked_dec = 0
     for itr in trace_iterations(cfg):
-        meta = gpu.host_metadata(itr)
         slots = ora.step(itr)
+        if itr.index % 3 == 2:
+            # every third iteration through pkv_iteration_step (allocator work,
+            # metadata copy and launches in one call)
+            pre_out, dec_out, meta = gpu.step(itr, to_dev_bf16(itr.q), to_dev_bf16(itr.k),
+                                              to_dev_bf16(itr.v))
+        else:
+            meta = gpu.host_metadata(itr)
+            # the others alternate between the separate calls and pkv_iteration_run
+            pre_out, dec_out = gpu.run_iteration(itr, meta, fused=itr.index % 3 == 1)
         got_slots = gpu.host_section(meta, "slot_mapping", itr.num_tokens)
         assert np.array_equal(got_slots, slots), f"iteration {itr.index}: slots differ"
-        # odd iterations run through the one-call path (pkv_iteration_run)
-        pre_out, dec_out = gpu.run_iteration(itr, meta, fused=itr.index % 2 == 1)
         full = itr.index % 10 == 0
         n_pre, n_dec = len(itr.prefill), len(itr.decode)
         pick_pre = range(n_pre) if full else seeded_eighth(rng, n_pre)

@@ -265,7 +265,8 @@ class DeviceTrace:
         self.staged = [None] * self.RING   # event after the last upload from each buffer
         self.next = 0
         self.wait_s = 0.0                   # host time spent waiting for a free buffer
-        self.lib_s = 0.0                    # host time inside the library's two per-iteration calls
+        self.lib_s = 0.0                    # host time inside the library's per-iteration calls
+        self.dev_meta = None                # device copy of the metadata (pkv_iteration_step)
 
     def host_metadata(self, itr):
         """The iteration's host side: new sequences for admitted requests,
@@ -378,6 +379,42 @@ class DeviceTrace:
         self.lib_s += time.perf_counter() - t0
         n_pre = up["n_pre"]
         return out[:n_pre], out[n_pre:]
+
+    def step(self, itr, q, k, v, stream=None):
+        """One iteration through pkv_iteration_step (the allocator work, the
+        metadata copy and the launches in one library call), with the token
+        values already on the device. Returns (prefill_out, decode_out, meta);
+        ``host_section(meta, ...)`` reads the staged metadata."""
+        cfg = self.cfg
+        for rid in itr.admitted:
+            self.sid[rid] = self.alloc.seq_create()
+        kk = self.next
+        self.next = (kk + 1) % self.RING
+        if self.staged[kk] is not None:
+            w0 = time.perf_counter()
+            self.staged[kk].synchronize()    # its previous copy has left the buffer
+            self.wait_s += time.perf_counter() - w0
+        work = itr.work
+        ids, counts = [self.sid[w.rid] for w in work], [w.n for w in work]
+        n_pre = len(itr.prefill)
+        stream = stream or torch.cuda.current_stream()
+        if self.dev_meta is None:
+            self.dev_meta = torch.empty(self.staging[0].numel(), dtype=torch.uint8,
+                                        device=self.device)
+        out = torch.empty(q.shape[0], cfg.Hq, cfg.D, dtype=torch.bfloat16, device=self.device)
+        t0 = time.perf_counter()
+        layout = pkv.pkv_iteration_step(self.alloc, ids, counts, n_pre, self.max_blocks,
+                               self.staging[kk], self.dev_meta, q, k, v, out, self.k_cache,
+                               self.v_cache, self.scale, self.ws, self.pws,
+                               partition_size=self.partition_size, status=self.status,
+                               stream=stream)
+        self.lib_s += time.perf_counter() - t0
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        self.staged[kk] = ev
+        rows = sum(w.n for w in itr.prefill)
+        meta = {"staging": kk, "layout": layout, "n_prefill": n_pre, "n_decode": len(work) - n_pre}
+        return (out[:rows] if n_pre else None), (out[rows:] if len(work) > n_pre else None), meta
 
     def run_iteration(self, itr, meta, stream=None, fused=False):
         """Upload and run one iteration, through the separate calls or through
