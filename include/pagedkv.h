@@ -120,15 +120,16 @@ int pkv_build_block_tables(pkv_alloc* a, const int64_t* seqs, int32_t n, int32_t
  *   changes, the call returns PKV_ENOMEM and *n_fit is the number of leading
  *   works that would fit (evict, then call again). On success *n_fit = n.
  *   buf (host memory the caller owns, e.g. pinned, of at least
- *   layout->total_bytes as pkv_iteration_layout_bytes reports for the same
- *   sizes) receives, at the layout's byte offsets, each section starting on a
- *   64-byte boundary:
+ *   total_bytes as pkv_iteration_layout_bytes reports for the same sizes)
+ *   receives, at the layout's byte offsets, each section starting on a
+ *   64-byte boundary (W = layout->table_width, the batch's longest table
+ *   after the appends, at most max_blocks_per_seq):
  *     slot_mapping   int32 [n_tokens]   (prefill works first, then decodes)
  *     cu_q_lens      int32 [n_prefill + 1]
  *     prefill_lens   int32 [n_prefill]  (context lengths after the appends)
- *     prefill_tables int32 [n_prefill][max_blocks_per_seq], padded with 0
+ *     prefill_tables int32 [n_prefill][W], padded with 0
  *     decode_lens    int32 [n_decode]
- *     decode_tables  int32 [n_decode][max_blocks_per_seq], padded with 0
+ *     decode_tables  int32 [n_decode][W], padded with 0
  *     cow_pairs      int32 [n_cow][2]  (run pkv_block_copy on them first)
  *   so one host-to-device copy of the whole buffer feeds pkv_block_copy,
  *   pkv_kv_append, pkv_paged_attention_prefill and pkv_paged_attention_decode.
@@ -143,6 +144,7 @@ typedef struct pkv_iteration_layout {
   int32_t n_cow;        /* copy-on-write pairs written */
   int32_t max_q_len;    /* longest prompt chunk */
   int32_t max_prefill_len, max_decode_len; /* longest context of each kind */
+  int32_t table_width;  /* entries per block-table row (the layout_bytes call: its bound) */
 } pkv_iteration_layout;
 int pkv_iteration_layout_bytes(int32_t n_prefill, int32_t n_decode, int32_t n_tokens,
                                int32_t max_blocks_per_seq, pkv_iteration_layout* layout);
@@ -158,8 +160,8 @@ int pkv_iteration_prepare(pkv_alloc* a, const int64_t* seqs, const int32_t* coun
  * launches on `stream`, in order, pkv_block_copy of the copy pairs,
  * pkv_kv_append of every new token, pkv_paged_attention_prefill of the
  * prompt chunks and pkv_paged_attention_decode of the decodes, with the
- * arrays read from `meta` and the sizes from `layout` (the host struct the
- * prepare call returned).
+ * arrays read from `meta` and the sizes (the block-table width included)
+ * from `layout` (the host struct the prepare call returned).
  *   q, out          : bf16 [n_tokens][Hq][D] (device), prefill rows first
  *                     (one per prompt token, in work order), then one row
  *                     per decode.
@@ -172,7 +174,7 @@ int pkv_iteration_prepare(pkv_alloc* a, const int64_t* seqs, const int32_t* coun
  * launches before it stay queued). An iteration with no token and no copy
  * does nothing. */
 int pkv_iteration_run(const void* meta, const pkv_iteration_layout* layout, int32_t n_prefill,
-                      int32_t n_decode, int32_t max_blocks_per_seq, const void* q,
+                      int32_t n_decode, const void* q,
                       const void* k_new, const void* v_new, void* out, void* k_cache,
                       void* v_cache, int32_t num_blocks, int32_t Hq, int32_t Hkv, int32_t D,
                       int32_t block_size, float scale, int32_t partition_size, void* decode_ws,

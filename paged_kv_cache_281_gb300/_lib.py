@@ -27,7 +27,7 @@ class IterationLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "slot_mapping", "cu_q_lens", "prefill_lens", "prefill_tables", "decode_lens",
         "decode_tables", "cow_pairs", "total_bytes")] + [(n, ctypes.c_int32) for n in (
-        "n_tokens", "n_cow", "max_q_len", "max_prefill_len", "max_decode_len")]
+        "n_tokens", "n_cow", "max_q_len", "max_prefill_len", "max_decode_len", "table_width")]
 
 
 SIGNATURES = {
@@ -47,7 +47,7 @@ SIGNATURES = {
     "pkv_iteration_layout_bytes": (ctypes.c_int, [i32, i32, i32, i32, P(IterationLayout)]),
     "pkv_iteration_prepare": (ctypes.c_int, [vp, P(i64), P(i32), i32, i32, i32, vp, sz,
                                              P(IterationLayout), P(i32)]),
-    "pkv_iteration_run": (ctypes.c_int, [vp, P(IterationLayout), i32, i32, i32, vp, vp, vp, vp,
+    "pkv_iteration_run": (ctypes.c_int, [vp, P(IterationLayout), i32, i32, vp, vp, vp, vp,
                                          vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp,
                                          sz, vp, vp]),
     "pkv_iteration_step": (ctypes.c_int, [vp, P(i64), P(i32), i32, i32, i32, vp, sz, vp, sz, vp,

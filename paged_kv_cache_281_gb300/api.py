@@ -247,12 +247,12 @@ class BlockAllocator:
         return layout
 
 
-def pkv_iteration_run(meta, layout, n_prefill: int, n_decode: int, max_blocks_per_seq: int, q,
-                      k_new, v_new, out, k_cache, v_cache, scale: float, decode_ws, prefill_ws,
+def pkv_iteration_run(meta, layout, n_prefill: int, n_decode: int, q, k_new, v_new, out, k_cache, v_cache, scale: float, decode_ws, prefill_ws,
                       partition_size: int = 0, status=None, stream=None) -> None:
     """``pkv_iteration_run``: the iteration's copies, appends, prefill and
     decode from one device copy (``meta``, uint8) of the buffer
-    ``iteration_prepare`` filled; ``layout`` is what it returned."""
+    ``iteration_prepare`` filled; ``layout`` is what it returned (its
+    ``table_width`` is the block tables' row length)."""
     cur = torch.cuda.current_device()
     N, Hkv, B, D = _pool_shape(k_cache, v_cache, cur)
     _dev(meta, "meta", torch.uint8, 1, cur)
@@ -267,8 +267,7 @@ def pkv_iteration_run(meta, layout, n_prefill: int, n_decode: int, max_blocks_pe
             v_new.shape != k_new.shape:
         raise ValueError(f"q/out must be [{T}, Hq, {D}] and k_new/v_new [{T}, {Hkv}, {D}]")
     check(lib().pkv_iteration_run(
-        meta.data_ptr(), ctypes.byref(layout), int(n_prefill), int(n_decode),
-        int(max_blocks_per_seq), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+        meta.data_ptr(), ctypes.byref(layout), int(n_prefill), int(n_decode), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
         out.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), N, Hq, Hkv, D, B, float(scale),
         int(partition_size), decode_ws.data_ptr(), int(decode_ws.numel()), prefill_ws.data_ptr(),
         int(prefill_ws.numel()), _ptr(status), _stream(stream)))

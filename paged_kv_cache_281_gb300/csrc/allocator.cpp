@@ -491,6 +491,7 @@ int layout_impl(int32_t n_prefill, int32_t n_decode, int64_t n_tokens,
   L->decode_tables = off;  off = align_up(off + 4 * (int64_t)n_decode * W);
   L->cow_pairs = off;      off = align_up(off + 8 * n);
   L->total_bytes = off;
+  L->table_width = max_blocks_per_seq;
   return PKV_OK;
 }
 
@@ -518,7 +519,7 @@ extern "C" int pkv_iteration_prepare(pkv_alloc* a, const int64_t* seqs, const in
   const int32_t B = a->block_size;
   // validate every work and dry-run the block needs, in order
   int64_t n_tokens = 0, need = 0;
-  int32_t fit = n;
+  int32_t fit = n, width = 1;  // the longest table after the appends
   std::unordered_map<int64_t, int32_t> seen;
   std::unordered_map<int32_t, int32_t> released;  // refs dropped by earlier copies
   seen.reserve(2 * (size_t)n);
@@ -548,12 +549,14 @@ extern "C" int pkv_iteration_prepare(pkv_alloc* a, const int64_t* seqs, const in
       }
     }
     need += (new_len + B - 1) / B - (int64_t)s->blocks.size() + (cow ? 1 : 0);
+    if ((new_len + B - 1) / B > width) width = (int32_t)((new_len + B - 1) / B);
     if (need > a->count && fit == n) fit = i;
     n_tokens += c;
   }
   PKV_REQUIRE(n_tokens < (int64_t(1) << 31), "%s: too many tokens", who);
-  if (int rc = layout_impl(n_prefill, n_decode, n_tokens, max_blocks_per_seq, layout, who))
-    return rc;
+  // tables are as wide as the batch's longest one (at most max_blocks_per_seq),
+  // so the buffer a caller sized with pkv_iteration_layout_bytes always fits
+  if (int rc = layout_impl(n_prefill, n_decode, n_tokens, width, layout, who)) return rc;
   PKV_REQUIRE(buf_bytes >= (size_t)layout->total_bytes, "%s: buf has %zu bytes, needs %lld", who,
               buf_bytes, (long long)layout->total_bytes);
   *n_fit = fit;
@@ -578,7 +581,7 @@ extern "C" int pkv_iteration_prepare(pkv_alloc* a, const int64_t* seqs, const in
       if (counts[i] > max_q) max_q = counts[i];
     }
   }
-  const int64_t W = max_blocks_per_seq;
+  const int64_t W = width;
   int32_t max_len[2] = {0, 0};
   for (int32_t part = 0; part < 2; ++part) {
     const int32_t first = part == 0 ? 0 : n_prefill;

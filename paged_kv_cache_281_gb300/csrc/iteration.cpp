@@ -17,8 +17,8 @@ using pkv::fail;
 using pkv::ok;
 
 extern "C" int pkv_iteration_run(const void* meta, const pkv_iteration_layout* layout,
-                                 int32_t n_prefill, int32_t n_decode,
-                                 int32_t max_blocks_per_seq, const void* q, const void* k_new,
+                                 int32_t n_prefill, int32_t n_decode, const void* q,
+                                 const void* k_new,
                                  const void* v_new, void* out, void* k_cache, void* v_cache,
                                  int32_t num_blocks, int32_t Hq, int32_t Hkv, int32_t D,
                                  int32_t block_size, float scale, int32_t partition_size,
@@ -26,10 +26,12 @@ extern "C" int pkv_iteration_run(const void* meta, const pkv_iteration_layout* l
                                  size_t prefill_ws_bytes, int32_t* dev_status, void* stream) {
   const char* who = "pkv_iteration_run";
   PKV_REQUIRE(layout, "%s: layout is NULL", who);
-  PKV_REQUIRE(n_prefill >= 0 && n_decode >= 0 && max_blocks_per_seq > 0, "%s: bad sizes", who);
+  PKV_REQUIRE(n_prefill >= 0 && n_decode >= 0, "%s: bad sizes", who);
   const int32_t T = layout->n_tokens;
   if (T == 0 && layout->n_cow == 0) return ok();
   PKV_REQUIRE(meta, "%s: meta is NULL", who);
+  const int32_t max_blocks_per_seq = layout->table_width;
+  PKV_REQUIRE(max_blocks_per_seq > 0, "%s: layout has no table width", who);
   PKV_REQUIRE(Hkv > 0 && Hq > 0 && Hq % Hkv == 0 && D > 0, "%s: bad head shape", who);
   const uint8_t* m = static_cast<const uint8_t*>(meta);
   auto sec = [m](int64_t off) { return reinterpret_cast<const int32_t*>(m + off); };
@@ -91,8 +93,7 @@ extern "C" int pkv_iteration_step(pkv_alloc* a, const int64_t* seqs, const int32
   cudaError_t err = cudaMemcpyAsync(dev_buf, host_buf, (size_t)layout->total_bytes,
                                     cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return pkv::cuda_fail(err, "pkv_iteration_step: metadata copy");
-  return pkv_iteration_run(dev_buf, layout, n_prefill, n_decode, max_blocks_per_seq, q, k_new,
-                           v_new, out, k_cache, v_cache, num_blocks, Hq, Hkv, D, block_size,
+  return pkv_iteration_run(dev_buf, layout, n_prefill, n_decode, q, k_new, v_new, out, k_cache, v_cache, num_blocks, Hq, Hkv, D, block_size,
                            scale, partition_size, decode_ws, decode_ws_bytes, prefill_ws,
                            prefill_ws_bytes, dev_status, stream);
 }

@@ -69,7 +69,7 @@ class Sides:
                           dtype=torch.uint8, device="cuda")
         pws = torch.empty(pkv.pkv_prefill_workspace_bytes(max(1, n_prefill), T, Hq, D),
                           dtype=torch.uint8, device="cuda")
-        pkv.pkv_iteration_run(meta, L, n_prefill, len(works) - n_prefill, W, to_dev_bf16(q),
+        pkv.pkv_iteration_run(meta, L, n_prefill, len(works) - n_prefill, to_dev_bf16(q),
                               to_dev_bf16(k), to_dev_bf16(v), out, self.kc, self.vc, self.scale,
                               dws, pws, status=self.status)
         pkv.pkv_check_status(self.status)

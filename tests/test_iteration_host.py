@@ -30,13 +30,15 @@ def _section(buf, layout, name, count, shape=None):
     return a.reshape(shape) if shape else a
 
 
-def _oracle_batch(ora, ids, counts, n_prefill, W):
-    """The same works through the oracle model, one append at a time."""
+def _oracle_batch(ora, ids, counts, n_prefill):
+    """The same works through the oracle model, one append at a time; the
+    tables are as wide as the batch's longest one."""
     slots, pairs = [], []
     for sid, c in zip(ids, counts):
         s, p = ora.append_slots(sid, int(c))
         slots.extend(s)
         pairs.extend(p)
+    W = max([1] + [len(ora.block_table(sid)) for sid in ids])
     tables = np.zeros((len(ids), W), np.int32)
     for i, sid in enumerate(ids):
         t = ora.block_table(sid)
@@ -83,7 +85,7 @@ def _scenario(seed):
         oids = [ora_ids[i] for i in live]
         snap = copy.deepcopy(ora)
         try:
-            want = _oracle_batch(ora, oids, counts, n_prefill, W)
+            want = _oracle_batch(ora, oids, counts, n_prefill)
             fits = True
         except paging.OutOfBlocks:
             ora = snap
@@ -108,15 +110,17 @@ def _scenario(seed):
             L = lib.iteration_prepare(lids, counts, n_prefill, W, buf)
             slots, pairs, tables, lens, cu = want
             assert L.n_tokens == len(slots) and L.n_cow == len(pairs)
+            Wt = tables.shape[1]
+            assert L.table_width == Wt <= W
             assert np.array_equal(_section(buf, L, "slot_mapping", len(slots)), slots)
             assert np.array_equal(_section(buf, L, "cu_q_lens", n_prefill + 1), cu)
             np_ = n_prefill
             assert np.array_equal(_section(buf, L, "prefill_lens", np_), lens[:np_])
-            assert np.array_equal(_section(buf, L, "prefill_tables", np_ * W, (np_, W)),
+            assert np.array_equal(_section(buf, L, "prefill_tables", np_ * Wt, (np_, Wt)),
                                   tables[:np_])
             nd = len(lids) - np_
             assert np.array_equal(_section(buf, L, "decode_lens", nd), lens[np_:])
-            assert np.array_equal(_section(buf, L, "decode_tables", nd * W, (nd, W)),
+            assert np.array_equal(_section(buf, L, "decode_tables", nd * Wt, (nd, Wt)),
                                   tables[np_:])
             got_pairs = _section(buf, L, "cow_pairs", 2 * len(pairs), (len(pairs), 2))
             assert [tuple(p) for p in got_pairs.tolist()] == [tuple(p) for p in pairs]
@@ -150,12 +154,12 @@ def test_out_of_blocks_counts_the_copies_earlier_works_release():
     assert lib.num_free_blocks() == 8 and lib.block_refcount(lib.seq_block_table(a)[1]) == 3
     # a shorter prompt fits: 6 + 2 copies = 8
     L = lib.iteration_prepare([n3] + la, [96, 1, 1, 1], 1, 8, buf)
-    slots, pairs, tables, lens, cu = _oracle_batch(ora, [o3] + oa, np.array([96, 1, 1, 1]), 1, 8)
-    assert L.n_cow == 2 and len(pairs) == 2
+    slots, pairs, tables, lens, cu = _oracle_batch(ora, [o3] + oa, np.array([96, 1, 1, 1]), 1)
+    assert L.n_cow == 2 and len(pairs) == 2 and L.table_width == 6
     assert np.array_equal(_section(buf, L, "slot_mapping", 99), slots)
     got = _section(buf, L, "cow_pairs", 4, (2, 2)).tolist()
     assert [tuple(p) for p in got] == [tuple(p) for p in pairs]
-    assert np.array_equal(_section(buf, L, "decode_tables", 24, (3, 8)), tables[1:])
+    assert np.array_equal(_section(buf, L, "decode_tables", 18, (3, 6)), tables[1:])
     assert lib.num_free_blocks() == ora.num_free() == 0
 
 
@@ -186,6 +190,7 @@ def test_iteration_prepare_rejects_bad_batches_unchanged():
 
 def test_layout_sections_are_aligned_and_sized():
     L = pkv.iteration_layout_bytes(3, 5, 77, 10)
+    assert L.table_width == 10
     offs = [L.slot_mapping, L.cu_q_lens, L.prefill_lens, L.prefill_tables, L.decode_lens,
             L.decode_tables, L.cow_pairs]
     assert all(o % 64 == 0 for o in offs) and offs == sorted(offs)
@@ -200,12 +205,14 @@ def test_iteration_run_checks_before_any_launch():
     import ctypes
     from paged_kv_cache_281_gb300._lib import IterationLayout, lib
     empty = IterationLayout()
-    args = lambda lay, npre, ndec, w: (None, lay, npre, ndec, w, None, None, None, None, None,
-                                       None, 64, 8, 2, 128, 16, ctypes.c_float(0.1), 0, None, 0,
-                                       None, 0, None, None)
-    assert lib().pkv_iteration_run(*args(ctypes.byref(empty), 0, 0, 4)) == 0
-    assert lib().pkv_iteration_run(*args(None, 0, 0, 4)) == PKV_EINVAL
-    assert lib().pkv_iteration_run(*args(ctypes.byref(empty), -1, 0, 4)) == PKV_EINVAL
+    args = lambda meta, lay, npre, ndec: (meta, lay, npre, ndec, None, None, None, None, None,
+                                          None, 64, 8, 2, 128, 16, ctypes.c_float(0.1), 0, None,
+                                          0, None, 0, None, None)
+    assert lib().pkv_iteration_run(*args(None, ctypes.byref(empty), 0, 0)) == 0
+    assert lib().pkv_iteration_run(*args(None, None, 0, 0)) == PKV_EINVAL
+    assert lib().pkv_iteration_run(*args(None, ctypes.byref(empty), -1, 0)) == PKV_EINVAL
     one = IterationLayout()
     one.n_tokens = 1
-    assert lib().pkv_iteration_run(*args(ctypes.byref(one), 0, 1, 4)) == PKV_EINVAL  # meta NULL
+    assert lib().pkv_iteration_run(*args(None, ctypes.byref(one), 0, 1)) == PKV_EINVAL  # meta NULL
+    junk = ctypes.create_string_buffer(64)
+    assert lib().pkv_iteration_run(*args(junk, ctypes.byref(one), 0, 1)) == PKV_EINVAL  # width 0

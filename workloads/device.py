@@ -306,7 +306,7 @@ class DeviceTrace:
             ev = torch.cuda.Event()
             ev.record(stream)
         self.staged[k] = ev
-        W = self.max_blocks
+        W = int(L.table_width)
         sec = lambda name, count: buf[getattr(L, name):getattr(L, name) + 4 * count].view(
             torch.int32)
         npre, ndec = meta["n_prefill"], meta["n_decode"]
@@ -373,7 +373,7 @@ class DeviceTrace:
         v = up.get("v", up["q"][:0, :cfg.Hkv])
         t0 = time.perf_counter()
         pkv.pkv_iteration_run(up["meta"], meta["layout"], meta["n_prefill"], meta["n_decode"],
-                              self.max_blocks, up["q"], k, v, out, self.k_cache, self.v_cache,
+                              up["q"], k, v, out, self.k_cache, self.v_cache,
                               self.scale, self.ws, self.pws, partition_size=self.partition_size,
                               status=self.status, stream=stream)
         self.lib_s += time.perf_counter() - t0
