@@ -28,9 +28,9 @@
 //    current one; it also zeroes the value rows past the last visible key
 //    before the product (they may hold stale or poisoned bytes, and 0 * NaN
 //    is NaN);
-//  * eight softmax warps per Q tile share each TMEM lane (= row) between two
-//    threads, one per key half: they read the scores, apply the causal
-//    limit, exchange the row maxima, keep a running sum against a reference
+//  * four softmax warps, one thread per TMEM lane (= row) with the row's 64
+//    scores in registers (no exchange with another thread): they read the
+//    scores, apply the causal limit, keep a running sum against a reference
 //    maximum (base 2, packed f32x2 arithmetic), and write the probabilities
 //    back into the same TMEM columns as two bf16 parts P_hi + P_lo (~fp32
 //    precision for the product), which the P V MMA reads as its A operand
@@ -64,7 +64,7 @@ constexpr int kItemRing = 4;         // work-item indices handed from the produc
 // overlap the other's work.
 template <int D, int NS>
 struct PCfg {
-  static constexpr int kThreads = 64 + 256;  // producer, MMA, eight softmax warps
+  static constexpr int kThreads = 64 + 128;  // producer, MMA, four softmax warps
   static constexpr uint32_t kQHalf = kRows * 128;  // one 64-column half of the Q tile
   static constexpr int kHalves = D / 64;
   static constexpr uint32_t kGroup = kHalves * 1024;  // one 8-row group of a K or V tile
@@ -308,10 +308,6 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int32_t s_pages[kWin];  // window of the current sequence's block table
-  // row maxima of the two key halves, per Q tile and score buffer; the two
-  // halves' row sums at the end
-  __shared__ float s_xmax[2][2][kRows];
-  __shared__ float s_lsum[2][kRows];
   __shared__ int32_t s_item[kItemRing];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -348,15 +344,15 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(C::kBarSF + i), 1);
-      mbar_init(bar(C::kBarPF + i), 256);
+      mbar_init(bar(C::kBarPF + i), 128);
       mbar_init(bar(C::kBarPV + i), 1);
-      mbar_init(bar(C::kBarX + i), 256);
+      mbar_init(bar(C::kBarX + i), 128);
     }
-    mbar_init(bar(C::kBarL), 256);
-    mbar_init(bar(C::kBarOE), 256);
+    mbar_init(bar(C::kBarL), 128);
+    mbar_init(bar(C::kBarOE), 128);
     for (int i = 0; i < kItemRing; ++i) {
       mbar_init(bar(C::kBarIF + i), 1);
-      mbar_init(bar(C::kBarIE + i), 1 + 8);  // the MMA warp and each softmax warp
+      mbar_init(bar(C::kBarIE + i), 1 + 4);  // the MMA warp and each softmax warp
     }
     mbar_init(bar(C::kBarFin), 1);
     s_abort = 0;
@@ -583,18 +579,15 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    // Eight warps: each TMEM lane (= row) is shared by two threads, one per
-    // half of the 64 key columns (and of the D output columns); the two
-    // exchange their row maxima through shared memory once per tile.
-    const int sw = warp - 2;
-    const int h = (sw >> 2) & 1;      // key half (columns 32h .. 32h+31)
+    // Four warps, one thread per TMEM lane (= row) holding the row's 64
+    // scores of a tile.
     const int quarter = warp & 3;     // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t t_o = tmem + 128 + lane_off + h * (D / 2);
+    const uint32_t t_o = tmem + 128 + lane_off;
     const uint64_t scale2 = f32x2_pack(a.scale_log2, a.scale_log2);
     bool ok = true;
-    int sg = 0, ne = 0;  // score-buffer uses and finished outputs
+    int sg = 0;  // score-buffer uses
     for (int n = 0; ok; ++n) {
       const int idx = take_item(n, ok);
       if (!ok || idx == -1) break;
@@ -604,37 +597,34 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
       const bool row_valid = qi < it.c;
       const int limit = row_valid ? (it.L - it.c + qi + 1) : 1;  // number of visible keys
       float m_ref = 0.f;
-      uint64_t l2 = f32x2_pack(0.f, 0.f);  // this thread's share of the row sum, two lanes
+      uint64_t l2 = f32x2_pack(0.f, 0.f);  // the row sum, two lanes
       for (int j = 0; j < nk; ++j) {
-        const int sj = sg + j, b = sj & 1, key0 = j * kKeys + 32 * h;
+        const int sj = sg + j, b = sj & 1, key0 = j * kKeys;
         ok = wait_warp(C::kBarSF + b, (sj >> 1) & 1, 7);
         if (!ok) break;
         tcgen05_after_sync();
         const uint32_t t_s = tmem + lane_off + b * kKeys;
-        uint32_t x[32];
-        tmem_ld32(t_s + 32 * h, x);
+        uint32_t x[kKeys];
+        tmem_ld32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+        tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
         tmem_wait_ld();
-        const int vis = min(32, limit - key0);  // visible columns of this half (may be <= 0)
-        const bool full = __all_sync(0xffffffffu, vis >= 32) != 0;
-        if (!full) {
+        const int vis = min(kKeys, limit - key0);  // visible columns (may be <= 0)
+        if (!(__all_sync(0xffffffffu, vis >= kKeys) != 0)) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < kKeys; ++i)
             if (i >= vis) x[i] = __float_as_uint(-INFINITY);
         }
-        float m4[4];
+        float m8[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          m4[e] = fmax3(__uint_as_float(x[8 * e]), __uint_as_float(x[8 * e + 1]),
+        for (int e = 0; e < 8; ++e)
+          m8[e] = fmax3(__uint_as_float(x[8 * e]), __uint_as_float(x[8 * e + 1]),
                         fmax3(__uint_as_float(x[8 * e + 2]), __uint_as_float(x[8 * e + 3]),
                               fmax3(__uint_as_float(x[8 * e + 4]), __uint_as_float(x[8 * e + 5]),
                                     fmax3(__uint_as_float(x[8 * e + 6]),
                                           __uint_as_float(x[8 * e + 7]), -INFINITY))));
-        const float mine = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
-        s_xmax[b][h][r] = mine;
-        mbar_arrive(bar(C::kBarX + b));
-        ok = wait_warp(C::kBarX + b, (sj >> 1) & 1, 10);
-        if (!ok) break;
-        const float m_tile = fmaxf(mine, s_xmax[b][h ^ 1][r]) * a.scale_log2;  // -inf: none
+        const float m_tile =
+            fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) *
+            a.scale_log2;  // -inf: no visible key
         if (j == 0) m_ref = m_tile;  // key 0 is visible to every row
         const bool need = m_tile > m_ref + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
@@ -646,7 +636,7 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
           if (need) m_ref = m_tile;
           l2 = f32x2_mul(l2, f32x2_pack(alpha, alpha));
 #pragma unroll 1
-          for (int c32 = 0; c32 < D / 64; ++c32) {
+          for (int c32 = 0; c32 < D / 32; ++c32) {
             uint32_t o[32];
             tmem_ld32(t_o + c32 * 32, o);
             tmem_wait_ld();
@@ -656,27 +646,33 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
           }
         }
         // p = 2^(x scale - m_ref) for two columns at a time, split into bf16
-        // hi + lo parts; masked columns hold -inf and give 0
+        // hi + lo parts; masked columns hold -inf and give 0. Keys 32 c ..
+        // 32 c + 31: hi parts in columns 16 c .. 16 c + 15, lo parts in
+        // 32 + 16 c .. 32 + 16 c + 15.
         const uint64_t negm = f32x2_pack(-m_ref, -m_ref);
-        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float y0, y1;
-          f32x2_unpack(
-              f32x2_fma(f32x2_pack(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])),
-                        scale2, negm),
-              y0, y1);
-          const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
-          const uint64_t p = f32x2_pack(p0, p1);
-          l2 = f32x2_add(l2, p);
-          hi[e] = pack_bf16x2(p0, p1);
-          float d0, d1;
-          f32x2_unpack(f32x2_sub(p, f32x2_pack(bf16_lo_to_f32(hi[e]), bf16_hi_to_f32(hi[e]))),
-                       d0, d1);
-          lo[e] = pack_bf16x2(d0, d1);
+        for (int c = 0; c < kKeys / 32; ++c) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const uint32_t* y = x + 32 * c;
+            float y0, y1;
+            f32x2_unpack(
+                f32x2_fma(f32x2_pack(__uint_as_float(y[2 * e]), __uint_as_float(y[2 * e + 1])),
+                          scale2, negm),
+                y0, y1);
+            const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+            const uint64_t p = f32x2_pack(p0, p1);
+            l2 = f32x2_add(l2, p);
+            hi[e] = pack_bf16x2(p0, p1);
+            float d0, d1;
+            f32x2_unpack(
+                f32x2_sub(p, f32x2_pack(bf16_lo_to_f32(hi[e]), bf16_hi_to_f32(hi[e]))), d0, d1);
+            lo[e] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(t_s + 16 * c, hi);
+          tmem_st16(t_s + 32 + 16 * c, lo);
         }
-        tmem_st16(t_s + 16 * h, hi);
-        tmem_st16(t_s + 32 + 16 * h, lo);
         tmem_wait_st();
         tcgen05_before_sync();
         mbar_arrive(bar(C::kBarPF + b));
@@ -688,21 +684,14 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
       const int sl = sg + nk - 1;
       ok = wait_warp(C::kBarPV + (sl & 1), (sl >> 1) & 1, 9);
       if (ok) {
-        // ---- epilogue: O / l -> bf16, row r -> (query qi, head kvh*G + r%G);
-        // this thread writes its half of the D columns
+        // ---- epilogue: O / l -> bf16, row r -> (query qi, head kvh*G + r%G)
         float l0, l1;
         f32x2_unpack(l2, l0, l1);
-        s_lsum[h][r] = l0 + l1;
-        mbar_arrive(bar(C::kBarL));
-        ok = wait_warp(C::kBarL, ne & 1, 11);
-      }
-      if (ok) {
-        const float inv = 1.f / (s_lsum[0][r] + s_lsum[1][r]);
+        const float inv = 1.f / (l0 + l1);
         tcgen05_after_sync();
-        __nv_bfloat16* orow =
-            a.out + ((int64_t)(it.c0 + qi) * a.Hq + it.kvh * G + (r % G)) * D + h * (D / 2);
+        __nv_bfloat16* orow = a.out + ((int64_t)(it.c0 + qi) * a.Hq + it.kvh * G + (r % G)) * D;
 #pragma unroll 1
-        for (int c32 = 0; c32 < D / 64; ++c32) {
+        for (int c32 = 0; c32 < D / 32; ++c32) {
           uint32_t o[32];
           tmem_ld32(t_o + c32 * 32, o);
           tmem_wait_ld();
@@ -718,12 +707,11 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
             }
           }
         }
-        // O and this tile's row-sum slots may be reused by the next item
+        // O may be reused by the next item
         tcgen05_before_sync();
         mbar_arrive(bar(C::kBarOE));
       }
       sg += nk;
-      ++ne;
     }
   }
 
