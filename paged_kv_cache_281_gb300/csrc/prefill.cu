@@ -64,7 +64,9 @@ constexpr int kItemRing = 4;         // work-item indices handed from the produc
 // overlap the other's work.
 template <int D, int NS>
 struct PCfg {
-  static constexpr int kThreads = 64 + 128;  // producer, MMA, four softmax warps
+  // key producer, score-MMA warp, P V-MMA warp, four softmax warps, value
+  // producer
+  static constexpr int kThreads = 96 + 128 + 32;
   static constexpr uint32_t kQHalf = kRows * 128;  // one 64-column half of the Q tile
   static constexpr int kHalves = D / 64;
   static constexpr uint32_t kGroup = kHalves * 1024;  // one 8-row group of a K or V tile
@@ -86,7 +88,7 @@ struct PCfg {
                        kBarPV = kBarPF + 2, kBarX = kBarPV + 2, kBarL = kBarX + 2,
                        kBarOE = kBarL + 1, kBarQE = kBarOE + 1, kBarIF = kBarQE + 1,
                        kBarIE = kBarIF + kItemRing, kBarFin = kBarIE + kItemRing,
-                       kNumBars = kBarFin + 1;
+                       kNumBars = kBarFin + 2;
   // TMEM: S buffers at columns 0..63 and 64..127, O at 128..128+D
   static constexpr uint32_t kTmemCols = 256;
 };
@@ -270,21 +272,28 @@ struct PItem {
   int kv_end, nkt;  // keys visible to the item's last query, and their key tiles
 };
 
-__device__ __forceinline__ PItem load_item(const PrefillArgs& a, int idx, int QT) {
-  // direct launches: the item is the CTA's own grid position
-  const int4 it = idx < 0 ? make_int4(blockIdx.z, gridDim.x - 1 - blockIdx.x, blockIdx.y, 0)
-                          : a.items[idx];
+// The item (sequence, query group, kv head) = `it` given its sequence's
+// chunk offsets c0 .. c1 and context length L.
+__device__ __forceinline__ PItem make_item(int4 it, int c0, int c1, int L, int QT) {
   PItem p;
   p.s = it.x;
   p.kvh = it.z;
-  p.c0 = __ldg(a.cu_q_lens + p.s);
-  p.c = __ldg(a.cu_q_lens + p.s + 1) - p.c0;
-  p.L = __ldg(a.context_lens + p.s);
+  p.c0 = c0;
+  p.c = c1 - c0;
+  p.L = L;
   p.q0 = it.y * QT;
   // the tile holds queries q0 .. q0 + QT - 1 of the chunk
   p.kv_end = p.L - p.c + p.q0 + min(QT, p.c - p.q0);
   p.nkt = (p.kv_end + kKeys - 1) / kKeys;
   return p;
+}
+
+__device__ __forceinline__ PItem load_item(const PrefillArgs& a, int idx, int QT) {
+  // direct launches: the item is the CTA's own grid position
+  const int4 it = idx < 0 ? make_int4(blockIdx.z, gridDim.x - 1 - blockIdx.x, blockIdx.y, 0)
+                          : a.items[idx];
+  return make_item(it, __ldg(a.cu_q_lens + it.x), __ldg(a.cu_q_lens + it.x + 1),
+                   __ldg(a.context_lens + it.x), QT);
 }
 
 // Persistent: the producer warp takes the next work item from a global
@@ -307,8 +316,9 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
   __shared__ __align__(8) uint64_t bars[C::kNumBars];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int32_t s_pages[kWin];  // window of the current sequence's block table
-  __shared__ int32_t s_item[kItemRing];
+  // windows of the current sequence's block table, one per producer warp
+  __shared__ int32_t s_pages[2][kWin];
+  __shared__ PItem s_item[kItemRing];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (a.direct) {
@@ -352,9 +362,10 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
     mbar_init(bar(C::kBarOE), 128);
     for (int i = 0; i < kItemRing; ++i) {
       mbar_init(bar(C::kBarIF + i), 1);
-      mbar_init(bar(C::kBarIE + i), 1 + 4);  // the MMA warp and each softmax warp
+      mbar_init(bar(C::kBarIE + i), 2 + 4 + 1);  // MMA, softmax and value-producer warps
     }
     mbar_init(bar(C::kBarFin), 1);
+    mbar_init(bar(C::kBarFin + 1), 1);
     s_abort = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmap_q);
@@ -372,114 +383,137 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
   grid_dep_wait();  // the plan (and everything before it) is complete
   const int n_items = a.direct ? 1 : *reinterpret_cast<volatile int32_t*>(a.n_items);
 
-  // The n-th item of this CTA (-1: no more; -2: the CTA's own grid position),
-  // as posted by the producer; every
+  // The n-th item of this CTA as the producer posted it whole (s < 0: no
+  // more), so that no consuming warp waits on a global load for it; every
   // consuming warp calls it once per n, in order.
-  auto take_item = [&](int n, bool& ok) -> int {
+  auto take_item = [&](int n, bool& ok) -> PItem {
     const int slot = n % kItemRing;
+    PItem it;
+    it.s = -1;
     ok = wait_warp(C::kBarIF + slot, (n / kItemRing) & 1, 14);
-    if (!ok) return -1;
-    const int idx = *reinterpret_cast<volatile int32_t*>(&s_item[slot]);
+    if (!ok) return it;
+    const volatile PItem& v = s_item[slot];
+    it.s = v.s;
+    it.kvh = v.kvh;
+    it.c0 = v.c0;
+    it.c = v.c;
+    it.L = v.L;
+    it.q0 = v.q0;
+    it.kv_end = v.kv_end;
+    it.nkt = v.nkt;
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(C::kBarIE + slot));
-    return idx;
+    return it;
   };
 
   // loads this CTA issued (Q, and K and V tiles, counted by the producer):
   // what a CTA that gives up waits for before its shared memory goes
   int issued_q = 0, issued_k = 0, issued_v = 0;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // Page numbers come from a window of the block table held in shared
-    // memory (refilled by the whole warp), so no tile's loads wait for a
-    // global read; K runs one tile ahead of V, the order in which the tensor
-    // core needs them.
+  if (warp == 0 || warp == 7) {
+    // ------------------------------------------------------------ producers
+    // Warp 0 takes the items, loads each one's Q tile and streams its key
+    // tiles; warp 7 streams the value tiles of the same items (it reads them
+    // from the ring like the other warps). A value stage is freed late (by
+    // the P V product two tiles back) and a key stage early, so one warp
+    // loading both would start an item's Q and first keys only after the
+    // previous item's last value wait. Page numbers come from a window of the
+    // block table held in shared memory (one per producer, refilled by the
+    // whole warp), so no tile's loads wait for a global read; lane k issues
+    // the box of page k of a tile (all rows of the page and both column
+    // halves in one box).
+    const bool keys = warp == 0;
     const int B = a.block_size, ppt = kKeys / B;  // pages per tile
+    int32_t* const sp = s_pages[keys ? 0 : 1];
     bool ok = true;
-    int jg = 0;  // K/V tiles issued so far (ring position)
+    int jg = 0;  // tiles issued so far (ring position)
     for (int n = 0; ok; ++n) {
-      // post the next item (or the end) in the ring
-      const int slot = n % kItemRing;
-      if (n >= kItemRing) ok = wait_warp(C::kBarIE + slot, (n / kItemRing - 1) & 1, 15);
-      if (!ok) break;
-      // direct launches post their own item (index -2) once, then the end
-      int idx = 0;
-      if (lane == 0) {
-        idx = a.direct ? (n == 0 ? -2 : n_items) : atomicAdd(a.ticket, 1);
-        s_item[slot] = idx < n_items ? idx : -1;
-        mbar_arrive(bar(C::kBarIF + slot));  // release: the index is visible to the waiters
+      PItem it;
+      it.s = -1;
+      if (keys) {
+        // post the next item (or the end) in the ring
+        const int slot = n % kItemRing;
+        if (n >= kItemRing) ok = wait_warp(C::kBarIE + slot, (n / kItemRing - 1) & 1, 15);
+        if (!ok) break;
+        // direct launches post their own item (index -2) once, then the end
+        int idx = 0;
+        if (lane == 0) idx = a.direct ? (n == 0 ? -2 : n_items) : atomicAdd(a.ticket, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (idx < n_items) it = load_item(a, idx, QT);
+        if (lane == 0) {
+          s_item[slot] = it;
+          mbar_arrive(bar(C::kBarIF + slot));  // release: the item is visible to the waiters
+        }
+        if (idx >= n_items) break;
+      } else {
+        it = take_item(n, ok);
+        if (!ok || it.s < 0) break;
       }
-      idx = __shfl_sync(0xffffffffu, idx, 0);
-      if (idx >= n_items) break;
-      const PItem it = load_item(a, idx, QT);
       const int32_t* bt = a.block_tables + (int64_t)it.s * a.max_blocks_per_seq;
       const int npages = (it.kv_end + B - 1) / B;
       int win0 = 0;
-      // Q of this item once the previous item's score MMAs have read theirs
-      if (n > 0) ok = wait_warp(C::kBarQE, (n - 1) & 1, 12);
-      if (!ok) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(C::kBarQ), C::kHalves * kQHalf);
+      if (keys) {
+        // Q of this item once the previous item's score MMAs have read theirs
+        if (n > 0) ok = wait_warp(C::kBarQE, (n - 1) & 1, 12);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(C::kBarQ), C::kHalves * kQHalf);
 #pragma unroll
-        for (int h = 0; h < C::kHalves; ++h)
-          tma_load_3d(base + C::kQ + h * kQHalf, &tmap_q, h * 64, it.kvh * G, it.c0 + it.q0,
-                      bar(C::kBarQ));
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_3d(base + C::kQ + h * kQHalf, &tmap_q, h * 64, it.kvh * G, it.c0 + it.q0,
+                        bar(C::kBarQ));
+        }
+        ++issued_q;
       }
-      ++issued_q;
       // the block-table window loads while Q is in flight
       __syncwarp();
-      for (int i = lane; i < kWin && i < npages; i += 32) s_pages[i] = __ldg(bt + i);
+      for (int i = lane; i < kWin && i < npages; i += 32) sp[i] = __ldg(bt + i);
       __syncwarp();
-      // Step j loads key tile j and value tile j - 1 (the order in which the
-      // tensor core needs them) in one pass of the warp: lane k < 8 issues
-      // the box of page k of the key tile, lane 8 + k that of the value tile
-      // (all rows of the page and both column halves in one box).
-      for (int j = 0; ok && j <= it.nkt; ++j) {
-        const bool do_k = j < it.nkt, do_v = j >= 1;
-        if (do_k && min((j + 1) * ppt, npages) > win0 + kWin) {
-          // slide the window: tile j-1 (whose values are still to load) and on
-          win0 = (j - 1) * ppt;
+      for (int j = 0; ok && j < it.nkt; ++j) {
+        if (min((j + 1) * ppt, npages) > win0 + kWin) {
+          // slide the window to tile j
+          win0 = j * ppt;
           __syncwarp();
-          for (int i = lane; i < kWin && win0 + i < npages; i += 32)
-            s_pages[i] = __ldg(bt + win0 + i);
+          for (int i = lane; i < kWin && win0 + i < npages; i += 32) sp[i] = __ldg(bt + win0 + i);
           __syncwarp();
         }
-        const int gk = jg + j, gv = jg + j - 1;
-        const int stk = gk % NS, stv = do_v ? gv % NS : 0;
-        if (do_k && gk >= NS) ok = wait_warp(C::kBarKE + stk, (gk / NS - 1) & 1, 1);
+        const int g = jg + j, st = g % NS;
+        if (g >= NS)
+          ok = wait_warp((keys ? C::kBarKE : C::kBarVE) + st, (g / NS - 1) & 1, keys ? 1 : 2);
         if (!ok) break;
-        if (do_v && gv >= NS) ok = wait_warp(C::kBarVE + stv, (gv / NS - 1) & 1, 2);
-        if (!ok) break;
-        const bool is_v = lane >= 8;
-        const int pl = lane & 7, p0 = (is_v ? j - 1 : j) * ppt;
-        const bool mine = lane < 16 && (is_v ? do_v : do_k) && pl < min(ppt, npages - p0);
-        const int32_t blk = mine ? s_pages[p0 + pl - win0] : -1;
+        const int p0 = j * ppt;
+        const bool mine = lane < ppt && lane < npages - p0;
+        const int32_t blk = mine ? sp[p0 + lane - win0] : -1;
         const bool valid = mine && blk >= 0 && blk < a.num_blocks;
         const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
-        const uint32_t kf = bar(C::kBarKF + stk), vf = bar(C::kBarVF + stv);
+        const uint32_t full = bar((keys ? C::kBarKF : C::kBarVF) + st);
         const uint32_t page_bytes = B * C::kHalves * 128u;
-        if (lane == 0 && do_k) mbar_arrive_expect_tx(kf, __popc(vmask & 0xffu) * page_bytes);
-        if (lane == 8 && do_v) mbar_arrive_expect_tx(vf, __popc(vmask & 0xff00u) * page_bytes);
+        if (lane == 0) mbar_arrive_expect_tx(full, __popc(vmask) * page_bytes);
         __syncwarp();
         if (mine && !valid) record_status(a.status, PKV_EDEVICE, blk, kKernelPrefill);
         if (valid)
-          tma_load_4d((is_v ? base + C::kV + stv * C::kStage : base + C::kK + stk * C::kStage) +
-                          pl * (B / 8) * C::kGroup,
-                      is_v ? &tmap_v : &tmap_k, 0, 0, 0, (blk * a.Hkv + it.kvh) * (B / 8),
-                      is_v ? vf : kf);
-        issued_k += do_k ? 1 : 0;
-        issued_v += do_v ? 1 : 0;
+          tma_load_4d((keys ? base + C::kK : base + C::kV) + st * C::kStage +
+                          lane * (B / 8) * C::kGroup,
+                      keys ? &tmap_k : &tmap_v, 0, 0, 0, (blk * a.Hkv + it.kvh) * (B / 8), full);
+        if (keys)
+          ++issued_k;
+        else
+          ++issued_v;
         __syncwarp();
       }
       jg += it.nkt;
       __syncwarp();
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ tensor core
-    // Order within an item: S_t(j) for each Q tile, then P_t(j-1) V; the
-    // scores of the next key tile are computed while their softmax runs.
+    // Two issuing warps on different SM sub-partitions: warp 1 issues the
+    // score products S_j = Q K_j^T, warp 2 the value products O += P_j V_j.
+    // One warp issuing both spent most of its time issuing (an MMA took ~70
+    // SM clocks to issue beside the softmax warps), and the probabilities it
+    // waited for were picked up late. A score buffer is rewritten only after
+    // the product that read its probabilities has completed (the two warps'
+    // MMAs are not ordered with each other).
     // shared-memory descriptors of the first Q, K and V tiles; the others
     // differ only in the start address field (bytes / 16)
     const uint64_t dq = umma_desc_sw128(base + C::kQ, 16, 1024);
@@ -495,23 +529,25 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
           : "r"((uint32_t)d + (bytes >> 4)), "r"((uint32_t)(d >> 32)));
       return r;
     };
+    const bool scores = warp == 1;
     bool ok = true;
     int jg = 0;                   // K/V ring position
     int sg = 0, oe = 0;           // score-buffer uses and finished outputs
     for (int n = 0; ok; ++n) {
-      const int idx = take_item(n, ok);
-      if (!ok || idx == -1) break;
-      const PItem it = load_item(a, idx, QT);
-      ok = wait_warp(C::kBarQ, n & 1, 3);
-      for (int j = 0; ok && j <= it.nkt; ++j) {
-        if (j < it.nkt) {
+      const PItem it = take_item(n, ok);
+      if (!ok || it.s < 0) break;
+      if (scores) {
+        ok = wait_warp(C::kBarQ, n & 1, 3);
+        for (int j = 0; ok && j < it.nkt; ++j) {
           const int g = jg + j, st = g % NS, u = g / NS;
+          const int sj = sg + j, b = sj & 1;
           ok = wait_warp(C::kBarKF + st, u & 1, 4);
+          // buffer b is free once the product of tile sj - 2 has completed
+          if (ok && sj >= 2) ok = wait_warp(C::kBarPV + b, ((sj - 2) >> 1) & 1, 16);
           if (!ok) break;
           tcgen05_after_sync();
           if (elect_one()) {
             const uint32_t kst = st * C::kStage;
-            const int b = (sg + j) & 1;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t koff = (kk >> 2) * 1024 + (kk & 3) * 32;
@@ -525,8 +561,9 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
           }
           __syncwarp();
         }
-        if (j >= 1) {
-          const int i = j - 1, g = jg + i, st = g % NS, u = g / NS;
+      } else {
+        for (int i = 0; ok && i < it.nkt; ++i) {
+          const int g = jg + i, st = g % NS, u = g / NS;
           ok = wait_warp(C::kBarVF + st, u & 1, 6);
           if (!ok) break;
           const int key0 = i * kKeys;
@@ -561,23 +598,23 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
               umma_bf16_ts(o, p + 32 + kk * 8, vdesc, kIdescO, 1u);
             }
             umma_commit(bar(C::kBarPV + b));
+            umma_commit(bar(C::kBarVE + st));
           }
           __syncwarp();
-          if (elect_one()) umma_commit(bar(C::kBarVE + st));
-          __syncwarp();
         }
+        oe += it.nkt > 0 ? 1 : 0;
       }
       jg += it.nkt;
       sg += it.nkt;
-      oe += it.nkt > 0 ? 1 : 0;
     }
     // every MMA (and the arrivals it triggers) is done before the CTA leaves
+    const int fin = C::kBarFin + (scores ? 0 : 1);
     if (lane == 0) {
-      umma_commit(bar(C::kBarFin));
-      mbar_wait_bounded(bar(C::kBarFin), 0, 4 * a.timeout_ns, 0);
+      umma_commit(bar(fin));
+      mbar_wait_bounded(bar(fin), 0, 4 * a.timeout_ns, 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 3 && warp <= 6) {
     // ------------------------------------------------------------ softmax
     // Four warps, one thread per TMEM lane (= row) holding the row's 64
     // scores of a tile.
@@ -589,9 +626,8 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
     bool ok = true;
     int sg = 0;  // score-buffer uses
     for (int n = 0; ok; ++n) {
-      const int idx = take_item(n, ok);
-      if (!ok || idx == -1) break;
-      const PItem it = load_item(a, idx, QT);
+      const PItem it = take_item(n, ok);
+      if (!ok || it.s < 0) break;
       const int nk = it.nkt;
       const int qi = it.q0 + r / G;
       const bool row_valid = qi < it.c;
@@ -721,7 +757,8 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
     if (tid == 0) record_status(a.status, PKV_ETIMEOUT, *abort, kKernelPrefill);
     // Let this CTA's own copies land before its shared memory is released:
     // wait (again with a limit) for the last phase armed on each barrier.
-    if (tid == 0) {
+    // (each producer for its own loads)
+    if ((warp == 0 || warp == 7) && lane == 0) {
       if (issued_q) mbar_wait_bounded(bar(C::kBarQ), (issued_q - 1) & 1, 4 * a.timeout_ns, 0);
       for (int i = 0; i < NS; ++i) {
         // tiles i, i + NS, ... went to stage i: wait for the last one's phase
