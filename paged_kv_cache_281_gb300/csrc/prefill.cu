@@ -13,21 +13,28 @@
 // so every key/value tile loaded serves all of them. A work item is (sequence,
 // query group, kv head) with one Q tile; large launches run a plan
 // kernel and a persistent grid that takes items from an atomic ticket (the
-// producer posts them to the other warps through a small ring), small ones
-// one CTA per item. The warps specialise and run as a pipeline over 64-key
-// tiles:
-//  * warp 0 (producer) loads Q by 3-D TMA boxes and streams K and V tiles
-//    into rings of NS stages: page numbers come from a block-table window in
-//    shared memory, and in one pass lanes 0-7 issue the boxes of key tile j
-//    and lanes 8-15 those of value tile j - 1, one 4-D box per page holding
-//    all its rows and both 64-column halves (tiles sit in shared memory as
-//    [8-row group][half][8 rows x 128 B], 128-byte swizzled);
-//  * warp 1 runs the tensor core (issue under elect.sync): S_j = Q K_j^T into
-//    one of two TMEM score buffers per Q tile, then O += P_{j-1} V_{j-1}, so
-//    the scores of the next tile are computed while the softmax works on the
-//    current one; it also zeroes the value rows past the last visible key
-//    before the product (they may hold stale or poisoned bytes, and 0 * NaN
-//    is NaN);
+// key producer posts each item whole to the other warps through a small
+// ring), small ones one CTA per item. The warps specialise and run as a
+// pipeline over 64-key tiles:
+//  * warp 0 (key producer) takes the items, loads each one's Q tile by 3-D
+//    TMA boxes and streams its key tiles into a ring of NS stages; warp 7
+//    (value producer) streams the value tiles into their own ring. Page
+//    numbers come from block-table windows in shared memory (one per
+//    producer), and lane k issues the box of page k of a tile, one 4-D box
+//    per page holding all its rows and both 64-column halves (tiles sit in
+//    shared memory as [8-row group][half][8 rows x 128 B], 128-byte
+//    swizzled). A value stage is freed late (by the P V product two tiles
+//    back), a key stage early: apart, the key producer starts the next
+//    item's Q and first keys without waiting for the last value stage;
+//  * warp 1 issues the score products S_j = Q K_j^T into one of two TMEM
+//    score buffers, so the scores of the next tile are computed while the
+//    softmax works on the current one, and warp 2 the value products
+//    O += P_j V_j (both under elect.sync, from different SM
+//    sub-partitions: one warp issuing both took ~70 SM clocks per MMA beside
+//    the softmax warps). A score buffer is rewritten once the value product
+//    that read its probabilities has completed. Warp 2 also zeroes the
+//    value rows past the last visible key before its product (they may hold
+//    stale or poisoned bytes, and 0 * NaN is NaN);
 //  * four softmax warps, one thread per TMEM lane (= row) with the row's 64
 //    scores in registers (no exchange with another thread): they read the
 //    scores, apply the causal limit, keep a running sum against a reference
