@@ -65,7 +65,7 @@ constexpr int kKeys = 64;        // keys per KV tile
 // halves) and the tensor core still sees equal strides between 8-row groups
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows past 2^8
 constexpr int kWin = 256;            // block-table entries held in shared memory
-constexpr int kItemRing = 4;         // work-item indices handed from the producer to the others
+constexpr int kItemRing = 4;         // work items handed from the key producer to the others
 
 // One Q tile per CTA and two CTAs per SM, so that one CTA's start and end
 // overlap the other's work.
@@ -303,11 +303,11 @@ __device__ __forceinline__ PItem load_item(const PrefillArgs& a, int idx, int QT
                    __ldg(a.context_lens + it.x), QT);
 }
 
-// Persistent: the producer warp takes the next work item from a global
-// ticket and posts its index in a small shared ring that the MMA and softmax
-// warps read in the same order; every barrier's phase follows a running
-// count, so the next item's Q and first K/V tiles load while this item
-// finishes and its scores are computed while this item's output is written.
+// Persistent: the key producer takes the next work item from a global
+// ticket and posts it whole in a small shared ring that the other warps read
+// in the same order; every barrier's phase follows a running count, so the
+// next item's Q and first K/V tiles load while this item finishes and its
+// scores are computed while this item's output is written.
 template <int D, int G, int NS>
 __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
   grid_dep_wait();  // the plan (and everything before it) is complete
   const int n_items = a.direct ? 1 : *reinterpret_cast<volatile int32_t*>(a.n_items);
 
-  // The n-th item of this CTA as the producer posted it whole (s < 0: no
+  // The n-th item of this CTA as the key producer posted it whole (s < 0: no
   // more), so that no consuming warp waits on a global load for it; every
   // consuming warp calls it once per n, in order.
   auto take_item = [&](int n, bool& ok) -> PItem {
@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
     return it;
   };
 
-  // loads this CTA issued (Q, and K and V tiles, counted by the producer):
+  // loads this CTA issued (Q, and K and V tiles, each counted by its producer):
   // what a CTA that gives up waits for before its shared memory goes
   int issued_q = 0, issued_k = 0, issued_v = 0;
 
