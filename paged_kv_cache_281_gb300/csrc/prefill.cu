@@ -296,9 +296,18 @@ __device__ __forceinline__ PItem make_item(int4 it, int c0, int c1, int L, int Q
 }
 
 __device__ __forceinline__ PItem load_item(const PrefillArgs& a, int idx, int QT) {
-  // direct launches: the item is the CTA's own grid position
-  const int4 it = idx < 0 ? make_int4(blockIdx.z, gridDim.x - 1 - blockIdx.x, blockIdx.y, 0)
-                          : a.items[idx];
+  if (idx < 0) {
+    // direct launches: the item is the CTA's own grid position, sequence
+    // blockIdx.x and kv head blockIdx.y, its query groups counted from the
+    // last (which sees the most keys) as blockIdx.z grows, so that the grid's
+    // first CTAs hold every sequence's longest items
+    const int s = blockIdx.x;
+    const int c0 = __ldg(a.cu_q_lens + s), c1 = __ldg(a.cu_q_lens + s + 1);
+    const int ng = (c1 - c0 + QT - 1) / QT;
+    return make_item(make_int4(s, ng - 1 - (int)blockIdx.z, blockIdx.y, 0), c0, c1,
+                     __ldg(a.context_lens + s), QT);
+  }
+  const int4 it = a.items[idx];
   return make_item(it, __ldg(a.cu_q_lens + it.x), __ldg(a.cu_q_lens + it.x + 1),
                    __ldg(a.context_lens + it.x), QT);
 }
@@ -330,10 +339,10 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (a.direct) {
     // one item per CTA: leave at once when its query group is empty
-    const int s = blockIdx.z;
+    const int s = blockIdx.x;
     const int c = __ldg(a.cu_q_lens + s + 1) - __ldg(a.cu_q_lens + s);
     const int L = __ldg(a.context_lens + s);
-    if ((int)(gridDim.x - 1 - blockIdx.x) * QT >= c) return;
+    if ((int)blockIdx.z * QT >= c) return;
     if (L < c || L > a.max_context_len) {
       if (tid == 0) record_status(a.status, PKV_EDEVICE, L, kKernelPrefill);
       return;
@@ -801,9 +810,10 @@ int launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   // Few items: one CTA each, straight from the grid (no plan launch); many:
   // a plan and a persistent grid that hands them out.
   const int64_t items = ((int64_t)total_q / a.qc + a.S) * a.Hkv;
-  if (items < 4 * (int64_t)slots) {
+  const int64_t groups = ((int64_t)max_q_len + a.qc - 1) / a.qc;
+  if (items < 4 * (int64_t)slots && groups <= 65535) {
     a.direct = 1;
-    dim3 grid((unsigned)((max_q_len + a.qc - 1) / a.qc), (unsigned)a.Hkv, (unsigned)a.S);
+    dim3 grid((unsigned)a.S, (unsigned)a.Hkv, (unsigned)groups);
     paged_prefill_kernel<D, G, NS><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, a);
     return check_launch("prefill");
   }
