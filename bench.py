@@ -1702,7 +1702,12 @@ def e2e_measure(w, d, args, pkv, torch, steps=None):
     """The same step through the C ABI from pinned host memory: each step
     copies its inputs (queries, new keys and values, slots, block tables,
     lengths), packed in one pinned staging buffer, to the device in one copy,
-    appends, decodes, and reads the output back."""
+    appends, decodes, and reads the output back into pinned memory.
+    Throughput: two sets of device buffers, the input copies on one stream,
+    the kernels on another and the read-backs on a third, so that step k+1's
+    inputs cross while step k decodes; every step's copies are in the timed
+    region. Also the same steps on one stream, one after the other (serial),
+    and with the host blocking on each step's output (latency)."""
     steps = steps or max(20, min(args.steps, 200))
     stream = torch.cuda.current_stream()
     parts = {
@@ -1714,40 +1719,84 @@ def e2e_measure(w, d, args, pkv, torch, steps=None):
         offs[name] = total
         total += -(-t.numel() * t.element_size() // 256) * 256
     host = torch.empty(total, dtype=torch.uint8).pin_memory()
-    dev = torch.empty(total, dtype=torch.uint8, device="cuda")
-    views = {}
+    devs = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    views = [{}, {}]
     for name, t in parts.items():
         nb = t.numel() * t.element_size()
         host[offs[name]:offs[name] + nb].copy_(t.reshape(-1).view(torch.uint8).cpu())
-        views[name] = dev[offs[name]:offs[name] + nb].view(t.dtype).view(t.shape)
-    out_h = torch.empty(d.out.shape, dtype=d.out.dtype).pin_memory()
-    d2h = out_h.numel() * out_h.element_size()
+        for i in range(2):
+            views[i][name] = devs[i][offs[name]:offs[name] + nb].view(t.dtype).view(t.shape)
+    outs = [d.out, torch.empty_like(d.out)]
+    outs_h = [torch.empty(d.out.shape, dtype=d.out.dtype).pin_memory() for _ in range(2)]
+    d2h = outs_h[0].numel() * outs_h[0].element_size()
 
-    def one():
-        dev.copy_(host, non_blocking=True)
-        pkv.pkv_kv_append(views["k"], views["v"], views["slots"], d.k_cache, d.v_cache,
-                          status=d.status, stream=stream)
-        pkv.pkv_paged_attention_decode(d.out, views["q"], d.k_cache, d.v_cache, views["bt"],
-                                       views["lens"], d.max_context_len, w.scale, d.workspace,
+    def kernels(i):
+        pkv.pkv_kv_append(views[i]["k"], views[i]["v"], views[i]["slots"], d.k_cache,
+                          d.v_cache, status=d.status, stream=stream)
+        pkv.pkv_paged_attention_decode(outs[i], views[i]["q"], d.k_cache, d.v_cache,
+                                       views[i]["bt"], views[i]["lens"], d.max_context_len,
+                                       w.scale, d.workspace,
                                        partition_size=args.partition_size, status=d.status,
                                        stream=stream)
-        out_h.copy_(d.out, non_blocking=True)
 
-    for _ in range(5):
-        one()
+    def one():
+        devs[0].copy_(host, non_blocking=True)
+        kernels(0)
+        outs_h[0].copy_(outs[0], non_blocking=True)
+
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    used = [torch.cuda.Event(), torch.cuda.Event()]    # the kernels that read buffer set i
+    copied = [torch.cuda.Event(), torch.cuda.Event()]  # inputs of set i on the device
+    read = [torch.cuda.Event(), torch.cuda.Event()]    # output of set i back in pinned memory
+    for i in range(2):
+        used[i].record(stream)
+        read[i].record(s_out)
+
+    def pipelined(k):
+        i = k & 1
+        s_in.wait_event(used[i])       # the step that last read set i has finished
+        with torch.cuda.stream(s_in):
+            devs[i].copy_(host, non_blocking=True)
+        copied[i].record(s_in)
+        stream.wait_event(copied[i])
+        stream.wait_event(read[i])     # its previous output has been read back
+        kernels(i)
+        used[i].record(stream)
+        s_out.wait_event(used[i])
+        with torch.cuda.stream(s_out):
+            outs_h[i].copy_(outs[i], non_blocking=True)
+        read[i].record(s_out)
+
+    for k in range(6):
+        pipelined(k)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        one()
+    a.record(s_in)
+    for k in range(steps):
+        pipelined(k)
+    stream.wait_stream(s_out)
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
+    # the same steps on one stream
+    for _ in range(5):
+        one()
+    torch.cuda.synchronize()
+    a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a2.record(stream)
+    for _ in range(steps):
+        one()
+    b2.record(stream)
+    torch.cuda.synchronize()
+    ms_serial = a2.elapsed_time(b2) / steps
     e2e = {"value": w.kv_bytes() / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
            "steps": steps, "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(d2h),
+           "serial_ms_per_step": ms_serial,
            "note": "KV pools stay resident (they are the cache); per-step inputs cross "
                    "the CPU-GPU link from one pinned staging buffer, the output back "
-                   "into pinned memory; steps issued back to back (throughput)"}
+                   "into pinned memory; steps issued back to back, the next step's "
+                   "input copy and the previous step's read-back on their own streams "
+                   "while a step decodes (serial_ms_per_step: all on one stream)"}
     # the same step, with the host waiting for each step's output before it
     # issues the next one: latency per step on the host's wall clock
     lat = []
