@@ -16,10 +16,11 @@
 //    sequence with one partition is normalised in place.
 //  * Data movement. Each of the CTA's 4 warps owns every 4th tile of the item
 //    and a private 2-stage ring in shared memory. The warp's lanes look up the
-//    block-table entries of its tiles in parallel; one lane issues TMA tile
-//    loads (two 64-column halves per tensor, 128-byte swizzle) for whole
-//    pages, signalling an mbarrier with the byte count; the warp waits on it
-//    with a time limit. The plan is launched early after the previous kernel
+//    block-table entries of its tiles in parallel; lanes 0..7 issue a tile's
+//    TMA loads, one box each in one instruction (two 64-column halves per
+//    tensor, 128-byte swizzle, whole pages), signalling an mbarrier with the
+//    byte count; the warp waits on it with a time limit. The plan is launched
+//    early after the previous kernel
 //    (programmatic dependent launch) and waits for it before reading; the
 //    decode and combine kernels follow the same way.
 //  * Arithmetic. The G query heads that share a kv head form the rows of a
@@ -188,21 +189,20 @@ __device__ __forceinline__ TileRows tile_rows(const DecodeArgs& a, const int32_t
 template <int D>
 __device__ __forceinline__ void issue_tile_rows(const CUtensorMap* tk, const CUtensorMap* tv,
                                                 int block_size, int32_t row0, int32_t row1,
-                                                uint32_t bytes, uint32_t stage, uint32_t bar) {
+                                                uint32_t bytes, uint32_t stage, uint32_t bar,
+                                                int lane) {
+  // warp-collective: lane 0 arms the barrier, then lane 4 sub + 2 half + v
+  // issues the box of run `sub` (R rows), column half `half` of the keys
+  // (v = 0) or values (v = 1), so that one warp instruction issues them all
   using C = Cfg<D>;
   const int R = block_size < kTileTokens ? block_size : kTileTokens;
-  mbar_arrive_expect_tx(bar, bytes);
-#pragma unroll
-  for (int sub = 0; sub < 2; ++sub) {
-    const int32_t row = sub == 0 ? row0 : row1;
-    if (row < 0) continue;
-#pragma unroll
-    for (int half = 0; half < C::kHalves; ++half) {
-      const uint32_t off = half * C::kHalfBytes + sub * R * 128;
-      tma_load_2d(stage + off, tk, half * 64, row, bar);
-      tma_load_2d(stage + C::kTensorBytes + off, tv, half * 64, row, bar);
-    }
-  }
+  if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+  __syncwarp();
+  const int sub = (lane >> 2) & 1, half = (lane >> 1) & 1, v = lane & 1;
+  const int32_t row = sub == 0 ? row0 : row1;
+  if (lane < 8 && half < C::kHalves && row >= 0)
+    tma_load_2d(stage + (v ? C::kTensorBytes : 0u) + half * C::kHalfBytes + sub * R * 128,
+                v ? tv : tk, half * 64, row, bar);
 }
 
 template <int D, int G>
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int32_t* bt = a.block_tables + (int64_t)s * a.max_blocks_per_seq;
 
     // The warp's lanes look up the block-table entries of its tiles of this
-    // item together (32 tiles at a time); lane 0 issues the copies.
+    // item together (32 tiles at a time); lanes 0..7 issue a tile's copies.
     TileRows mine = {{-1, -1}, 0u};
     int chunk0 = 0;
     if (lane < n_mine) mine = tile_rows<D>(a, bt, kvh, t_begin + warp + lane * kWarps, L);
@@ -274,9 +274,8 @@ __global__ void __launch_bounds__(kThreads, 3)
       const int32_t r0 = __shfl_sync(0xffffffffu, mine.row[0], src);
       const int32_t r1 = __shfl_sync(0xffffffffu, mine.row[1], src);
       const uint32_t by = __shfl_sync(0xffffffffu, mine.bytes, src);
-      if (lane == 0)
-        issue_tile_rows<D>(&tmap_k, &tmap_v, a.block_size, r0, r1, by,
-                           ring + st * C::kStageBytes, smem_u32(&bars[warp][st]));
+      issue_tile_rows<D>(&tmap_k, &tmap_v, a.block_size, r0, r1, by, ring + st * C::kStageBytes,
+                         smem_u32(&bars[warp][st]), lane);
     };
     {
       const int npro = n_mine < C::kStages ? n_mine : C::kStages;
@@ -1112,9 +1111,8 @@ __global__ void __launch_bounds__(kThreads, 3)
       const int32_t q0 = __shfl_sync(0xffffffffu, mine.row[0], src);
       const int32_t q1 = __shfl_sync(0xffffffffu, mine.row[1], src);
       const uint32_t by = __shfl_sync(0xffffffffu, mine.bytes, src);
-      if (lane == 0)
-        issue_tile_rows<D>(&tmap_k, &tmap_v, a.block_size, q0, q1, by, ring + st * C::kStageBytes,
-                           smem_u32(&bars[warp][st]));
+      issue_tile_rows<D>(&tmap_k, &tmap_v, a.block_size, q0, q1, by, ring + st * C::kStageBytes,
+                         smem_u32(&bars[warp][st]), lane);
     };
     {
       const int npro = n_mine < C::kStages ? n_mine : C::kStages;
