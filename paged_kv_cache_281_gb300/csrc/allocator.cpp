@@ -36,9 +36,12 @@ struct pkv_alloc {
     bool tracked = true;   // token ids known for every position (prefix cache)
     std::vector<int32_t> tokens;
     int32_t reg_upto = 0;  // leading blocks that are registered, chained
+    uint64_t mark = 0;     // the last iteration_prepare call that listed it
   };
   std::unordered_map<int64_t, Seq> seqs;
   int64_t next_id = 0;
+  uint64_t epoch = 0;               // iteration_prepare calls so far
+  std::vector<Seq*> batch;          // the current call's sequences, in work order
 
   // Prefix cache: a full block is registered under (the registered block
   // before it, or -1, and its B token ids). Registered blocks keep their
@@ -242,13 +245,24 @@ namespace {
 
 // Reserves slots for n new tokens of a sequence; token_ids (nullable) are
 // recorded for the prefix cache.
+int append_seq(pkv_alloc* a, pkv_alloc::Seq* s, int64_t seq, int32_t n,
+               const int32_t* token_ids, int32_t* slots_out, int32_t* cow_pair_out,
+               int32_t* n_cow, const char* who);
+
 int append_impl(pkv_alloc* a, int64_t seq, int32_t n, const int32_t* token_ids,
                 int32_t* slots_out, int32_t* cow_pair_out, int32_t* n_cow, const char* who) {
   PKV_REQUIRE(a && n_cow, "%s: NULL argument", who);
-  PKV_REQUIRE(n >= 0, "%s: n must be >= 0 (got %d)", who, n);
-  PKV_REQUIRE(n == 0 || slots_out, "%s: slots_out is NULL", who);
   pkv_alloc::Seq* s = a->find(seq);
   PKV_REQUIRE(s, "%s: unknown sequence %lld", who, (long long)seq);
+  return append_seq(a, s, seq, n, token_ids, slots_out, cow_pair_out, n_cow, who);
+}
+
+// append_impl on a sequence already looked up
+int append_seq(pkv_alloc* a, pkv_alloc::Seq* s, int64_t seq, int32_t n,
+               const int32_t* token_ids, int32_t* slots_out, int32_t* cow_pair_out,
+               int32_t* n_cow, const char* who) {
+  PKV_REQUIRE(n >= 0, "%s: n must be >= 0 (got %d)", who, n);
+  PKV_REQUIRE(n == 0 || slots_out, "%s: slots_out is NULL", who);
   PKV_REQUIRE(!s->swapped, "%s: sequence %lld is swapped out", who, (long long)seq);
   *n_cow = 0;
   if (n == 0) return ok();
@@ -520,15 +534,17 @@ extern "C" int pkv_iteration_prepare(pkv_alloc* a, const int64_t* seqs, const in
   // validate every work and dry-run the block needs, in order
   int64_t n_tokens = 0, need = 0;
   int32_t fit = n, width = 1;  // the longest table after the appends
-  std::unordered_map<int64_t, int32_t> seen;
   std::unordered_map<int32_t, int32_t> released;  // refs dropped by earlier copies
-  seen.reserve(2 * (size_t)n);
+  // a sequence listed twice carries this call's mark already
+  const uint64_t ep = ++a->epoch;
+  a->batch.resize((size_t)n);
   for (int32_t i = 0; i < n; ++i) {
     pkv_alloc::Seq* s = a->find(seqs[i]);
     PKV_REQUIRE(s, "%s: unknown sequence %lld (work %d)", who, (long long)seqs[i], i);
     PKV_REQUIRE(!s->swapped, "%s: sequence %lld is swapped out", who, (long long)seqs[i]);
-    PKV_REQUIRE(seen.emplace(seqs[i], i).second, "%s: sequence %lld appears twice", who,
-                (long long)seqs[i]);
+    PKV_REQUIRE(s->mark != ep, "%s: sequence %lld appears twice", who, (long long)seqs[i]);
+    s->mark = ep;
+    a->batch[i] = s;
     const int32_t c = counts[i];
     PKV_REQUIRE(i < n_prefill ? c >= 1 : c == 1,
                 "%s: work %d: a prefill chunk needs >= 1 token and a decode exactly 1 (got %d)",
@@ -573,7 +589,8 @@ extern "C" int pkv_iteration_prepare(pkv_alloc* a, const int64_t* seqs, const in
   cu[0] = 0;
   for (int32_t i = 0; i < n; ++i) {
     int32_t got_cow = 0;
-    append_impl(a, seqs[i], counts[i], nullptr, slots, pairs + 2 * n_cow, &got_cow, who);
+    append_seq(a, a->batch[i], seqs[i], counts[i], nullptr, slots, pairs + 2 * n_cow, &got_cow,
+               who);
     slots += counts[i];
     n_cow += got_cow;
     if (i < n_prefill) {
@@ -591,7 +608,7 @@ extern "C" int pkv_iteration_prepare(pkv_alloc* a, const int64_t* seqs, const in
     int32_t* tables = reinterpret_cast<int32_t*>(
         base + (part == 0 ? layout->prefill_tables : layout->decode_tables));
     for (int32_t k = 0; k < count; ++k) {
-      const pkv_alloc::Seq* s = a->find(seqs[first + k]);
+      const pkv_alloc::Seq* s = a->batch[first + k];
       int32_t* row = tables + k * W;
       const int32_t m = (int32_t)s->blocks.size();
       if (m) std::memcpy(row, s->blocks.data(), sizeof(int32_t) * m);
