@@ -87,13 +87,12 @@ struct PCfg {
   static constexpr uint32_t kMinSmem = 80u * 1024;
   static constexpr uint32_t kSmem = kBytes + 1024 > kMinSmem ? kBytes + 1024 : kMinSmem;
   // barriers: Q; K full/empty and V full/empty per stage; per score
-  // buffer: S full, P full, PV done, row maxima exchanged; row sums
-  // exchanged, output read out (O free); Q free; work item posted / taken
-  // per item-ring slot; final
+  // buffer: S full, P full, PV done; output read out (O free); Q free; work
+  // item posted / taken per item-ring slot; final, per MMA warp
   static constexpr int kBarQ = 0, kBarKF = 1, kBarKE = 1 + NS, kBarVF = 1 + 2 * NS,
                        kBarVE = 1 + 3 * NS, kBarSF = 1 + 4 * NS, kBarPF = kBarSF + 2,
-                       kBarPV = kBarPF + 2, kBarX = kBarPV + 2, kBarL = kBarX + 2,
-                       kBarOE = kBarL + 1, kBarQE = kBarOE + 1, kBarIF = kBarQE + 1,
+                       kBarPV = kBarPF + 2, kBarOE = kBarPV + 2, kBarQE = kBarOE + 1,
+                       kBarIF = kBarQE + 1,
                        kBarIE = kBarIF + kItemRing, kBarFin = kBarIE + kItemRing,
                        kNumBars = kBarFin + 2;
   // TMEM: S buffers at columns 0..63 and 64..127, O at 128..128+D
@@ -372,9 +371,7 @@ __global__ void __launch_bounds__(PCfg<D, NS>::kThreads, 2)
       mbar_init(bar(C::kBarSF + i), 1);
       mbar_init(bar(C::kBarPF + i), 128);
       mbar_init(bar(C::kBarPV + i), 1);
-      mbar_init(bar(C::kBarX + i), 128);
     }
-    mbar_init(bar(C::kBarL), 128);
     mbar_init(bar(C::kBarOE), 128);
     for (int i = 0; i < kItemRing; ++i) {
       mbar_init(bar(C::kBarIF + i), 1);
