@@ -277,6 +277,18 @@ class Iteration:
     q: np.ndarray = field(default=None)   # uint16 [T, Hq, D]
     k: np.ndarray = field(default=None)   # uint16 [T, Hkv, D]
     v: np.ndarray = field(default=None)
+    _arrays: tuple = field(default=None, repr=False)
+
+    def arrays(self):
+        """(request ids int64 [n], token counts int32 [n], prefill works,
+        prefill rows) of ``work`` in order, as the scheduler hands them to
+        the engine (computed once)."""
+        if self._arrays is None:
+            n_pre = sum(1 for w in self.work if w.kind == "prefill")
+            self._arrays = (np.array([w.rid for w in self.work], dtype=np.int64),
+                            np.array([w.n for w in self.work], dtype=np.int32), n_pre,
+                            sum(w.n for w in self.work[:n_pre]))
+        return self._arrays
 
     @property
     def prefill(self) -> list[Work]:

@@ -249,6 +249,7 @@ class DeviceTrace:
                                                     cfg.D, device)
         self.status = pkv.new_status(device)
         self.sid = {}
+        self.sid_arr = np.full(1024, -1, dtype=np.int64)  # the same map, by request id
         self.max_blocks = -(-(cfg.prompt_max + cfg.out_cap) // cfg.block_size)
         self.scale = 1.0 / np.sqrt(cfg.D)
         self.ws = torch.empty(pkv.pkv_decode_workspace_bytes(
@@ -268,11 +269,20 @@ class DeviceTrace:
         self.lib_s = 0.0                    # host time inside the library's per-iteration calls
         self.dev_meta = None                # device copy of the metadata (pkv_iteration_step)
 
+    def admit(self, rid):
+        """A new sequence for request ``rid``."""
+        sid = self.alloc.seq_create()
+        self.sid[rid] = sid
+        if rid >= self.sid_arr.shape[0]:
+            grow = max(rid + 1, 2 * self.sid_arr.shape[0]) - self.sid_arr.shape[0]
+            self.sid_arr = np.concatenate([self.sid_arr, np.full(grow, -1, dtype=np.int64)])
+        self.sid_arr[rid] = sid
+
     def host_metadata(self, itr):
         """The iteration's host side: new sequences for admitted requests,
         then one library call for every work's slots and the metadata."""
         for rid in itr.admitted:
-            self.sid[rid] = self.alloc.seq_create()
+            self.admit(rid)
         k = self.next
         self.next = (k + 1) % self.RING
         if self.staged[k] is not None:
@@ -387,16 +397,15 @@ class DeviceTrace:
         ``host_section(meta, ...)`` reads the staged metadata."""
         cfg = self.cfg
         for rid in itr.admitted:
-            self.sid[rid] = self.alloc.seq_create()
+            self.admit(rid)
         kk = self.next
         self.next = (kk + 1) % self.RING
         if self.staged[kk] is not None:
             w0 = time.perf_counter()
             self.staged[kk].synchronize()    # its previous copy has left the buffer
             self.wait_s += time.perf_counter() - w0
-        work = itr.work
-        ids, counts = [self.sid[w.rid] for w in work], [w.n for w in work]
-        n_pre = len(itr.prefill)
+        rids, counts, n_pre, rows = itr.arrays()
+        ids = self.sid_arr[rids]
         stream = stream or torch.cuda.current_stream()
         if self.dev_meta is None:
             self.dev_meta = torch.empty(self.staging[0].numel(), dtype=torch.uint8,
@@ -412,9 +421,9 @@ class DeviceTrace:
         ev = torch.cuda.Event()
         ev.record(stream)
         self.staged[kk] = ev
-        rows = sum(w.n for w in itr.prefill)
-        meta = {"staging": kk, "layout": layout, "n_prefill": n_pre, "n_decode": len(work) - n_pre}
-        return (out[:rows] if n_pre else None), (out[rows:] if len(work) > n_pre else None), meta
+        n = counts.shape[0]
+        meta = {"staging": kk, "layout": layout, "n_prefill": n_pre, "n_decode": n - n_pre}
+        return (out[:rows] if n_pre else None), (out[rows:] if n > n_pre else None), meta
 
     def run_iteration(self, itr, meta, stream=None, fused=False):
         """Upload and run one iteration, through the separate calls or through
