@@ -1652,6 +1652,7 @@ def main():
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
 
+    graph = graph_measure(w, d, args, torch, decode_step, barrier) if world == 1 else None
     e2e = e2e_sync = None
     if not args.no_e2e:
         barrier()
@@ -1685,6 +1686,8 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
+    if graph is not None:
+        line["graph"] = graph
     if e2e is not None:
         line["e2e"] = e2e
         line["e2e_sync"] = e2e_sync
@@ -1696,6 +1699,37 @@ def main():
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def graph_measure(w, d, args, torch, decode_step, barrier):
+    """The same step (kv_append + decode: the plan, decode and combine
+    launches) captured once in a CUDA graph and replayed back to back: what
+    the step costs without the host's per-launch work."""
+    stream = torch.cuda.current_stream()
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            decode_step(w, d)
+        stream.wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            decode_step(w, d)
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        b.record(stream)
+        barrier()
+    except RuntimeError as e:
+        return {"unavailable": str(e).splitlines()[0][:200]}
+    ms = a.elapsed_time(b) / args.steps
+    return {"ms_per_step": ms, "value": w.kv_bytes() / (ms * 1e-3) / 1e9, "unit": UNIT,
+            "note": "the step captured once in a CUDA graph (torch.cuda.graph) and "
+                    "replayed back to back"}
 
 
 def e2e_measure(w, d, args, pkv, torch, steps=None):
