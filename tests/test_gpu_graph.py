@@ -1,12 +1,13 @@
-"""A decode step captured in a CUDA graph and replayed.
+"""Decode and prefill steps captured in a CUDA graph and replayed.
 
 Every launch of the library is stream-ordered (no host synchronisation, no
 allocation, tensor maps passed by value), so a caller can capture a step of
 the continuous-batching loop ("Deep Dive: continuous batching", section
 Iteration-level scheduling: the same kernels run every iteration) once and
 replay it to save the per-launch host cost. The replayed step must give the
-eager step's output bit for bit, on a batch with one partition per sequence
-(plan, decode) and one with several (plan, decode, combine).
+eager step's output bit for bit: a decode step on a batch with one partition
+per sequence (plan, decode) and one with several (plan, decode, combine), and
+a prefill launch of each kind (one CTA per item; plan and persistent grid).
 """
 
 from __future__ import annotations
@@ -16,8 +17,8 @@ import pytest
 import torch
 
 import paged_kv_cache_281_gb300 as pkv
-from workloads import config1, make_decode_workload
-from workloads.device import bf16_bits, decode_step, setup_decode
+from workloads import config1, make_decode_workload, normal_bf16
+from workloads.device import bf16_bits, decode_step, setup_decode, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -49,3 +50,46 @@ def test_decode_step_replays_from_a_cuda_graph(case):
     torch.cuda.synchronize()
     pkv.pkv_check_status(d.status)
     assert np.array_equal(bf16_bits(d.out), want)
+
+
+@pytest.mark.parametrize("case", ["one CTA per item", "persistent grid"])
+def test_prefill_replays_from_a_cuda_graph(case):
+    # a small launch runs one CTA per work item; a large one a plan kernel and
+    # a persistent grid chained by programmatic dependent launch
+    if case == "one CTA per item":
+        lens, chunks = (300, 129, 40), [300, 33, 40]
+    else:
+        lens, chunks = (1024,) * 16, [1024] * 16
+    w = make_decode_workload("graph_prefill", lens, Hq=32, Hkv=8, D=128, block_size=16,
+                             seed=3302)
+    d = setup_decode(w)
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)).cuda()
+    T = int(sum(chunks))
+    q = to_dev_bf16(normal_bf16((T, w.Hq, w.D), 3303))
+    out = torch.full_like(q, float("nan"))
+    ws = torch.empty(pkv.pkv_prefill_workspace_bytes(w.S, T, w.Hq, w.D), dtype=torch.uint8,
+                     device="cuda")
+
+    def prefill():
+        pkv.pkv_paged_attention_prefill(out, q, cu, d.context_lens, d.k_cache, d.v_cache,
+                                        d.block_tables, max(chunks), w.max_context_len, w.scale,
+                                        ws, status=d.status)
+
+    prefill()
+    torch.cuda.synchronize()
+    pkv.pkv_check_status(d.status)
+    want = bf16_bits(out).copy()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        prefill()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        prefill()
+    out.fill_(float("nan"))
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    pkv.pkv_check_status(d.status)
+    assert np.array_equal(bf16_bits(out), want)
