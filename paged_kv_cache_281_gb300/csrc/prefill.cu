@@ -120,11 +120,14 @@ struct PrefillArgs {
 
 // Lists the work items (sequence, query group, kv head): for each sequence
 // its query groups from the last (which sees the most keys) to the first.
-// One CTA of 1024 threads; sequences with an inconsistent length are
-// recorded and skipped.
+// One CTA of 1024 threads: a scan over the sequences gives each one its first
+// item, then each warp writes the items of every 32nd sequence with its lanes
+// on consecutive items. Sequences with an inconsistent length are recorded
+// and skipped.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillArgs a) {
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t s_base, s_chunk;
+  __shared__ int32_t s_first[1024], s_groups[1024];  // per sequence of the chunk
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   grid_dep_launch();  // the prefill kernel may start its set-up now
   grid_dep_wait();    // launched early: whatever ran before (the append) is complete
@@ -163,9 +166,15 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillArgs a)
       if (lane == 31) s_chunk = wi;
     }
     __syncthreads();
-    const int excl = s_base + warp_tot[warp] + incl - cnt;
-    for (int i = 0; i < cnt && excl + i < a.item_cap; ++i)
-      a.items[excl + i] = make_int4(s, ng - 1 - i / a.Hkv, i % a.Hkv, 0);
+    s_first[tid] = s_base + warp_tot[warp] + incl - cnt;
+    s_groups[tid] = ng;
+    __syncthreads();
+    const int n_seq = min(1024, a.S - c0);
+    for (int j = warp; j < n_seq; j += 32) {
+      const int first = s_first[j], groups = s_groups[j], n = groups * a.Hkv;
+      for (int i = lane; i < n && first + i < a.item_cap; i += 32)
+        a.items[first + i] = make_int4(c0 + j, groups - 1 - i / a.Hkv, i % a.Hkv, 0);
+    }
     __syncthreads();
     if (tid == 0) s_base += s_chunk;
     __syncthreads();
@@ -804,11 +813,12 @@ int launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "prefill kernel attributes");
   a.qc = kRows / G;  // queries per work item
   const int slots = dev.sm_count * 2;
-  // Few items: one CTA each, straight from the grid (no plan launch); many:
-  // a plan and a persistent grid that hands them out.
+  // Few items (under two per resident CTA): one CTA each, straight from the
+  // grid (no plan launch); more: a plan and a persistent grid that hands
+  // them out.
   const int64_t items = ((int64_t)total_q / a.qc + a.S) * a.Hkv;
   const int64_t groups = ((int64_t)max_q_len + a.qc - 1) / a.qc;
-  if (items < 4 * (int64_t)slots && groups <= 65535) {
+  if (items < 2 * (int64_t)slots && groups <= 65535) {
     a.direct = 1;
     dim3 grid((unsigned)a.S, (unsigned)a.Hkv, (unsigned)groups);
     paged_prefill_kernel<D, G, NS><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, a);
