@@ -96,18 +96,21 @@ struct DecodeArgs {
   int32_t* seq_shared;         // [S] shared tokens processed by group items (0: none)
 };
 
-// Lists the work items: pass 0 emits every full partition (s, p), pass 1 the
-// trailing partial partition of each sequence. Single CTA of 1024 threads.
+// Lists the work items: every full partition (s, p) in sequence order, then
+// the trailing partial partition of each sequence. Single CTA of 1024
+// threads; up to 1024 sequences one scan of both counts places both kinds,
+// more take one pass over the sequences per kind.
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
-  __shared__ int32_t warp_tot[32];
-  __shared__ int32_t s_base, s_chunk;
+  __shared__ int32_t warp_tot[2][32];
+  __shared__ int32_t s_base[2], s_chunk[2];  // [0] full partitions, [1] tails
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = a.partition_tiles * kTileTokens;
+  const bool one_pass = a.S <= 1024;
   grid_dep_launch();  // the decode kernel may start its set-up now
   grid_dep_wait();    // launched early: whatever ran before (the append) is complete
-  if (tid == 0) s_base = 0;
+  if (tid == 0) s_base[0] = s_base[1] = 0;
   __syncthreads();
-  for (int pass = 0; pass < 2; ++pass) {
+  for (int pass = 0; pass < (one_pass ? 1 : 2); ++pass) {
     for (int c0 = 0; c0 < a.S; c0 += 1024) {
       const int s = c0 + tid;
       int L = 0;
@@ -118,36 +121,52 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
           L = 0;
         }
       }
-      const int cnt = pass == 0 ? L / P : (L % P != 0 ? 1 : 0);
-      int incl = cnt;
+      const int full = (one_pass || pass == 0) ? L / P : 0;
+      const int tail = (one_pass || pass == 1) && L % P != 0 ? 1 : 0;
+      int incl_f = full, incl_t = tail;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+        const int vf = __shfl_up_sync(0xffffffffu, incl_f, o);
+        const int vt = __shfl_up_sync(0xffffffffu, incl_t, o);
+        if (lane >= o) {
+          incl_f += vf;
+          incl_t += vt;
+        }
       }
-      if (lane == 31) warp_tot[warp] = incl;
+      if (lane == 31) {
+        warp_tot[0][warp] = incl_f;
+        warp_tot[1][warp] = incl_t;
+      }
       __syncthreads();
-      if (warp == 0) {
-        const int w = warp_tot[lane];
+      if (warp < 2) {  // warp k: exclusive prefix of the warp totals of kind k
+        const int w = warp_tot[warp][lane];
         int wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int v = __shfl_up_sync(0xffffffffu, wi, o);
           if (lane >= o) wi += v;
         }
-        warp_tot[lane] = wi - w;  // exclusive prefix of the warp totals
-        if (lane == 31) s_chunk = wi;
+        warp_tot[warp][lane] = wi - w;
+        if (lane == 31) s_chunk[warp] = wi;
       }
       __syncthreads();
-      const int excl = s_base + warp_tot[warp] + incl - cnt;
-      for (int i = 0; i < cnt; ++i) a.items[excl + i] = make_int2(s, pass == 0 ? i : L / P);
+      const int excl_f = s_base[0] + warp_tot[0][warp] + incl_f - full;
+      const int excl_t = s_base[1] + warp_tot[1][warp] + incl_t - tail;
+      // the tails follow every full partition: in one pass this chunk's, else
+      // those of the first pass
+      const int tail_base = one_pass ? s_chunk[0] : s_base[0];
+      for (int i = 0; i < full; ++i) a.items[excl_f + i] = make_int2(s, i);
+      if (tail) a.items[tail_base + excl_t] = make_int2(s, L / P);
       __syncthreads();
-      if (tid == 0) s_base += s_chunk;
+      if (tid == 0) {
+        s_base[0] += s_chunk[0];
+        s_base[1] += s_chunk[1];
+      }
       __syncthreads();
     }
   }
   if (tid == 0) {
-    *a.n_items = s_base;
+    *a.n_items = s_base[0] + s_base[1];
     *a.ticket = 0;
   }
 }

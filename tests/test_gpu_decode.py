@@ -72,6 +72,15 @@ def test_partition_sizes_agree(partition):
     check_against_oracle(w, partition_size=partition)
 
 
+def test_more_sequences_than_plan_threads():
+    # 1,100 sequences: the plan lists full partitions and tails over two
+    # chunks of its 1,024 threads
+    lens = np.random.default_rng(1150).integers(1, 601, size=1100)
+    w = make_decode_workload("many_seqs", tuple(int(x) for x in lens), Hq=4, Hkv=2, D=64,
+                             block_size=16, seed=1151)
+    check_against_oracle(w, partition_size=256)
+
+
 def test_split_independence_within_tolerance():
     w = make_decode_workload("split", (900, 2000, 37), Hq=32, Hkv=8, D=128, block_size=16,
                              seed=1101)

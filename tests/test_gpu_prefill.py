@@ -173,6 +173,17 @@ def test_persistent_grid_short_chunks_after_long_prefixes():
     check_prefill_sampled(w, [40] * 64, [0, 31, 63], seed=22)
 
 
+def test_persistent_grid_many_sequences():
+    # 1,100 sequences (two chunks of the plan's 1,024 threads), ragged chunks
+    # after ragged prefixes, enough items for the persistent grid
+    rng = np.random.default_rng(3170)
+    lens = rng.integers(1, 201, size=1100)
+    chunks = [int(rng.integers(1, L + 1)) for L in lens]
+    w = make_decode_workload("prefill_many", tuple(int(x) for x in lens), Hq=8, Hkv=2, D=64,
+                             block_size=16, seed=3171)
+    check_prefill(w, chunks, seed=71)
+
+
 def test_persistent_grid_timeout_and_bad_entry():
     lens = [600] * 16
     w = make_decode_workload("prefill_persistent_err", lens, Hq=32, Hkv=8, D=128,
