@@ -170,6 +170,13 @@ int pkv_iteration_prepare(pkv_alloc* a, const int64_t* seqs, const int32_t* coun
  *                     max_decode_len, partition_size) bytes or more.
  *   prefill_ws      : pkv_prefill_workspace_bytes(n_prefill, prefill rows,
  *                     Hq, D) bytes or more.
+ * When the iteration has both prompt chunks and decodes, the prefill runs on
+ * a second stream of the library's (one per device, created by the first
+ * such call; the first call should not be made inside a stream capture),
+ * forked from `stream` after the append and joined back into it, beside the
+ * decode on `stream`: work queued on `stream` after this call still waits
+ * for all of it, and a captured call captures both branches. The stream and
+ * its two events do not survive cudaDeviceReset.
  * Errors are those of the four calls (the first failing one returns; the
  * launches before it stay queued). An iteration with no token and no copy
  * does nothing. */

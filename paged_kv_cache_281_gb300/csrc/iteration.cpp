@@ -9,12 +9,54 @@
 // append of every new token, the prefill and the decode, reading each
 // kernel's arrays from that one device buffer. It adds no kernel of its own:
 // it only saves the host the per-kernel argument handling of separate calls.
+//
+// The prefill and the decode of one iteration touch different sequences and
+// only read the cache the append wrote, so they run side by side: the
+// prefill on a second stream of the library's (one per device) forked from
+// the caller's stream after the append and joined back into it after the
+// prefill. The prefill is tensor-bound and the decode HBM-bound, so each
+// fills what the other leaves idle, and the calls' starts and last waves
+// overlap.
 #include <cstdint>
+#include <mutex>
 
 #include "host_util.h"
 
 using pkv::fail;
 using pkv::ok;
+
+namespace {
+
+// The second stream of a device and the events that fork it from and join it
+// into the caller's stream. The mutex keeps one call's record / wait pairs
+// together when several host threads launch on the same device.
+struct SideStream {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
+};
+constexpr int kMaxDevices = 64;
+SideStream g_side[kMaxDevices];
+
+int side_stream(SideStream** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return pkv::cuda_fail(err, "pkv_iteration_run: current device");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ECUDA, "pkv_iteration_run: device %d", dev);
+  SideStream& sd = g_side[dev];
+  std::call_once(sd.once, [&sd]() {
+    sd.err = cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking);
+    if (sd.err == cudaSuccess) sd.err = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming);
+    if (sd.err == cudaSuccess) sd.err = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming);
+  });
+  if (sd.err != cudaSuccess) return pkv::cuda_fail(sd.err, "pkv_iteration_run: side stream");
+  *out = &sd;
+  return PKV_OK;
+}
+
+}  // namespace
 
 extern "C" int pkv_iteration_run(const void* meta, const pkv_iteration_layout* layout,
                                  int32_t n_prefill, int32_t n_decode, const void* q,
@@ -48,24 +90,43 @@ extern "C" int pkv_iteration_run(const void* meta, const pkv_iteration_layout* l
   // prefill rows come first in q and out, one per prompt token
   const int32_t n_pre_rows = T - n_decode;
   const size_t row_bytes = (size_t)Hq * D * 2;
-  if (n_prefill > 0) {
-    if (int rc = pkv_paged_attention_prefill(
-            out, q, sec(layout->cu_q_lens), sec(layout->prefill_lens), k_cache, v_cache,
-            sec(layout->prefill_tables), max_blocks_per_seq, n_prefill, n_pre_rows,
-            layout->max_q_len, layout->max_prefill_len, Hq, Hkv, D, block_size, num_blocks,
-            scale, prefill_ws, prefill_ws_bytes, dev_status, stream))
-      return rc;
+  auto prefill = [&](void* on) {
+    return pkv_paged_attention_prefill(
+        out, q, sec(layout->cu_q_lens), sec(layout->prefill_lens), k_cache, v_cache,
+        sec(layout->prefill_tables), max_blocks_per_seq, n_prefill, n_pre_rows,
+        layout->max_q_len, layout->max_prefill_len, Hq, Hkv, D, block_size, num_blocks, scale,
+        prefill_ws, prefill_ws_bytes, dev_status, on);
+  };
+  auto decode = [&]() {
+    return pkv_paged_attention_decode(
+        static_cast<uint8_t*>(out) + (size_t)n_pre_rows * row_bytes,
+        static_cast<const uint8_t*>(q) + (size_t)n_pre_rows * row_bytes, k_cache, v_cache,
+        sec(layout->decode_tables), max_blocks_per_seq, sec(layout->decode_lens),
+        layout->max_decode_len, n_decode, Hq, Hkv, D, block_size, num_blocks, scale,
+        partition_size, decode_ws, decode_ws_bytes, dev_status, stream);
+  };
+  if (n_prefill == 0 || n_decode == 0) {
+    if (n_prefill > 0)
+      if (int rc = prefill(stream)) return rc;
+    if (n_decode > 0)
+      if (int rc = decode()) return rc;
+    return ok();
   }
-  if (n_decode > 0) {
-    if (int rc = pkv_paged_attention_decode(
-            static_cast<uint8_t*>(out) + (size_t)n_pre_rows * row_bytes,
-            static_cast<const uint8_t*>(q) + (size_t)n_pre_rows * row_bytes, k_cache, v_cache,
-            sec(layout->decode_tables), max_blocks_per_seq, sec(layout->decode_lens),
-            layout->max_decode_len, n_decode, Hq, Hkv, D, block_size, num_blocks, scale,
-            partition_size, decode_ws, decode_ws_bytes, dev_status, stream))
-      return rc;
-  }
-  return ok();
+  SideStream* sd = nullptr;
+  if (int rc = side_stream(&sd)) return rc;
+  cudaStream_t main = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(sd->mu);
+  cudaError_t err = cudaEventRecord(sd->fork, main);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(sd->stream, sd->fork, 0);
+  if (err != cudaSuccess) return pkv::cuda_fail(err, "pkv_iteration_run: fork");
+  const int rc_pre = prefill(sd->stream);
+  // joined back whatever the prefill call returned, so that `stream` waits
+  // for all of it (and a stream capture stays whole)
+  err = cudaEventRecord(sd->join, sd->stream);
+  const int rc_dec = rc_pre ? rc_pre : decode();
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(main, sd->join, 0);
+  if (err != cudaSuccess) return pkv::cuda_fail(err, "pkv_iteration_run: join");
+  return rc_dec ? rc_dec : ok();
 }
 
 // Both halves of an iteration in one call: the host work of

@@ -18,7 +18,8 @@ import torch
 
 import paged_kv_cache_281_gb300 as pkv
 from workloads import config1, make_decode_workload, normal_bf16
-from workloads.device import bf16_bits, decode_step, setup_decode, to_dev_bf16
+from workloads.device import (bf16_bits, bf16_to_f64, decode_step, poisoned_pools,
+                              setup_decode, to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -92,4 +93,61 @@ def test_prefill_replays_from_a_cuda_graph(case):
         graph.replay()
     torch.cuda.synchronize()
     pkv.pkv_check_status(d.status)
+    assert np.array_equal(bf16_bits(out), want)
+
+
+def test_iteration_run_replays_from_a_cuda_graph():
+    # prompt chunks and decodes in one pkv_iteration_run: the prefill runs on
+    # the library's second stream, forked from the captured stream after the
+    # append and joined back into it, so the capture holds both branches
+    N, B, Hq, Hkv, D, W = 200, 16, 16, 4, 128, 24
+    lib = pkv.BlockAllocator(N, B)
+    kc, vc = poisoned_pools(N, Hkv, B, D)
+    seqs = [lib.seq_create() for _ in range(6)]
+    buf = torch.empty(1 << 20, dtype=torch.uint8).pin_memory()
+    status = pkv.new_status()
+    scale = 1.0 / np.sqrt(D)
+
+    def iteration(works, n_prefill, seed):
+        counts = [c for _, c in works]
+        T = sum(counts)
+        q = to_dev_bf16(normal_bf16((T, Hq, D), seed))
+        k = to_dev_bf16(normal_bf16((T, Hkv, D), seed + 1))
+        v = to_dev_bf16(normal_bf16((T, Hkv, D), seed + 2))
+        L = lib.iteration_prepare([seqs[i] for i, _ in works], counts, n_prefill, W, buf)
+        meta = buf[:L.total_bytes].cuda()
+        out = torch.full((T, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        dws = torch.empty(pkv.pkv_decode_workspace_bytes(len(works), Hq, D, W * B),
+                          dtype=torch.uint8, device="cuda")
+        pws = torch.empty(pkv.pkv_prefill_workspace_bytes(max(1, n_prefill), T, Hq, D),
+                          dtype=torch.uint8, device="cuda")
+
+        def run():
+            pkv.pkv_iteration_run(meta, L, n_prefill, len(works) - n_prefill, q, k, v, out, kc,
+                                  vc, scale, dws, pws, status=status)
+        return run, out
+
+    run0, _ = iteration(list(enumerate((40, 77, 130, 16, 300, 9))), 6, 9400)
+    run0()
+    # two prompt chunks beside four decodes (appending the same tokens to the
+    # same slots again leaves the pools as they were)
+    run1, out = iteration([(0, 21), (4, 50), (1, 1), (2, 1), (3, 1), (5, 1)], 2, 9500)
+    run1()
+    torch.cuda.synchronize()
+    pkv.pkv_check_status(status)
+    want = bf16_bits(out).copy()
+    assert np.isfinite(bf16_to_f64(out)).all()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run1()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run1()
+    out.fill_(float("nan"))
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    pkv.pkv_check_status(status)
     assert np.array_equal(bf16_bits(out), want)

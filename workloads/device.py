@@ -264,6 +264,7 @@ class DeviceTrace:
         self.staging = [torch.empty(cap, dtype=torch.uint8).pin_memory()
                         for _ in range(self.RING)]
         self.staged = [None] * self.RING   # event after the last upload from each buffer
+        self.events = [torch.cuda.Event() for _ in range(self.RING)]  # reused by step()
         self.next = 0
         self.wait_s = 0.0                   # host time spent waiting for a free buffer
         self.lib_s = 0.0                    # host time inside the library's per-iteration calls
@@ -290,14 +291,13 @@ class DeviceTrace:
             self.staged[k].synchronize()    # its previous upload has left the buffer
             self.wait_s += time.perf_counter() - w0
             self.staged[k] = None
-        work = itr.work
-        ids, counts = [self.sid[w.rid] for w in work], [w.n for w in work]
+        rids, counts, n_pre, _ = itr.arrays()
         t0 = time.perf_counter()
-        layout = self.alloc.iteration_prepare(ids, counts, len(itr.prefill), self.max_blocks,
+        layout = self.alloc.iteration_prepare(self.sid_arr[rids], counts, n_pre, self.max_blocks,
                                               self.staging[k])
         self.lib_s += time.perf_counter() - t0
-        return {"staging": k, "layout": layout, "n_prefill": len(itr.prefill),
-                "n_decode": len(work) - len(itr.prefill)}
+        return {"staging": k, "layout": layout, "n_prefill": n_pre,
+                "n_decode": counts.shape[0] - n_pre}
 
     def host_section(self, meta, name, count):
         """A host view of one section of the staged metadata (int32)."""
@@ -379,8 +379,7 @@ class DeviceTrace:
         meta = up["layout_meta"]
         out = torch.empty(up["q"].shape[0], cfg.Hq, cfg.D, dtype=torch.bfloat16,
                           device=self.device)
-        k = up.get("k", up["q"][:0, :cfg.Hkv])
-        v = up.get("v", up["q"][:0, :cfg.Hkv])
+        k, v = (up["k"], up["v"]) if "k" in up else (up["q"][:0, :cfg.Hkv],) * 2
         t0 = time.perf_counter()
         pkv.pkv_iteration_run(up["meta"], meta["layout"], meta["n_prefill"], meta["n_decode"],
                               up["q"], k, v, out, self.k_cache, self.v_cache,
@@ -418,7 +417,7 @@ class DeviceTrace:
                                partition_size=self.partition_size, status=self.status,
                                stream=stream)
         self.lib_s += time.perf_counter() - t0
-        ev = torch.cuda.Event()
+        ev = self.events[kk]
         ev.record(stream)
         self.staged[kk] = ev
         n = counts.shape[0]
