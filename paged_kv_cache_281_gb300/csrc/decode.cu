@@ -92,7 +92,7 @@ struct DecodeArgs {
   int32_t n_groups;
   int32_t members_per_item;    // 16 / G
   int32_t item_cap;
-  int4* gitems;                // (kind, id, partition, chunk)
+  int4* gitems;                // two per item (see decode_group_plan_kernel)
   int32_t* seq_shared;         // [S] shared tokens processed by group items (0: none)
 };
 
@@ -266,7 +266,6 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   while (cur < total) {
     __syncthreads();  // everyone has read s_next
-    if (tid == 0) s_next = atomicAdd(a.ticket, 1);
     const int2 item = __ldg(a.items + cur / a.Hkv);
     const int kvh = cur % a.Hkv;
     const int s = item.x, p = item.y;
@@ -300,6 +299,9 @@ __global__ void __launch_bounds__(kThreads, 3)
       const int npro = n_mine < C::kStages ? n_mine : C::kStages;
       for (int k = 0; k < npro; ++k) issue(k, k);
     }
+    // the next ticket, stored at the item's end (nothing waits on it before)
+    int nxt = 0;
+    if (tid == 0) nxt = atomicAdd(a.ticket, 1);
 
     // Q fragments (A operand rows g < G; rows g+8 are always zero).
     uint32_t qa[KS][2];
@@ -429,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     // Merge the 4 warps' states through shared memory (the rings are drained).
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (tid == 0) s_next = nxt;
     __syncthreads();
     if (s_abort) return;
     float2* cml = reinterpret_cast<float2*>(base_ptr);                  // [kWarps][G]
@@ -971,9 +974,13 @@ __global__ void __launch_bounds__(kThreads, 4)
 // partitions followed by its private ones; the combine kernel merges them.
 //
 // Item kinds: 1 = (group, shared partition, member chunk), 0 = (sequence,
-// private partition). Built by one CTA with atomics (the item order does not
-// affect any result: each item's arithmetic depends only on its own data and
-// the merge runs in partition order).
+// private partition), each written resolved as two int4 so that a CTA starts
+// an item from one load: (kind, first member's sequence, first token, end
+// token) and (index of the chunk's first member in grp_members, members,
+// partition index within each member's partial states, 0). Built by one CTA
+// with atomics (the item order does not affect any result: each item's
+// arithmetic depends only on its own data and the merge runs in partition
+// order).
 __global__ void __launch_bounds__(1024) decode_group_plan_kernel(DecodeArgs a) {
   __shared__ int32_t s_n;
   const int tid = threadIdx.x;
@@ -1016,7 +1023,11 @@ __global__ void __launch_bounds__(1024) decode_group_plan_kernel(DecodeArgs a) {
       continue;
     }
     for (int p = 0; p < nsp; ++p)
-      for (int c = 0; c < chunks; ++c) a.gitems[k + p * chunks + c] = make_int4(1, g, p, c);
+      for (int c = 0; c < chunks; ++c) {
+        const int i = 2 * (k + p * chunks + c), mb = b + c * M;
+        a.gitems[i] = make_int4(1, __ldg(a.grp_members + mb), p * P, min(p * P + P, sh));
+        a.gitems[i + 1] = make_int4(mb, min(M, e - mb), p, 0);
+      }
   }
   __syncthreads();
   for (int s = tid; s < a.S; s += 1024) {
@@ -1033,7 +1044,11 @@ __global__ void __launch_bounds__(1024) decode_group_plan_kernel(DecodeArgs a) {
       record_status(a.status, PKV_EDEVICE, s, kKernelDecodePlan);
       continue;
     }
-    for (int p = 0; p < np; ++p) a.gitems[k + p] = make_int4(0, s, p, 0);
+    const int nsp = (sh + P - 1) / P;
+    for (int p = 0; p < np; ++p) {
+      a.gitems[2 * (k + p)] = make_int4(0, s, sh + p * P, min(sh + p * P + P, L));
+      a.gitems[2 * (k + p) + 1] = make_int4(0, 1, nsp + p, 0);
+    }
   }
   __syncthreads();
   if (tid == 0) {
@@ -1059,7 +1074,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   __shared__ __align__(8) uint64_t bars[kWarps][C::kStages];
   __shared__ int32_t s_next;
   __shared__ int32_t s_abort;
-  __shared__ int32_t s_mem[M];
+  __shared__ int32_t s_mem[M];  // the item's members (sequences)
+  __shared__ int32_t s_np[M];   // their partial-state counts
+  __shared__ int32_t s_nm, s_part;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -1088,28 +1105,14 @@ __global__ void __launch_bounds__(kThreads, 3)
   int cur = s_next;
 
   while (cur < total) {
-    __syncthreads();
-    const int4 item = a.gitems[cur / a.Hkv];
+    __syncthreads();  // everyone has read s_next; the rings and s_mem are free
+    // The item from one load; the loads of the first tiles go out before
+    // anything waits on the members or on the next ticket.
+    const int4 h0 = __ldg(a.gitems + 2 * (cur / a.Hkv));
+    const int4 h1 = __ldg(a.gitems + 2 * (cur / a.Hkv) + 1);
     const int kvh = cur % a.Hkv;
-    int nm, first, r_begin, r_end;  // members, token range
-    if (item.x == 1) {
-      const int b = __ldg(a.grp_start + item.y) + item.w * M;
-      nm = min(M, __ldg(a.grp_start + item.y + 1) - b);
-      first = __ldg(a.grp_members + b);
-      const int sh = a.seq_shared[first];
-      r_begin = item.z * P;
-      r_end = min(r_begin + P, sh);
-      if (tid < nm) s_mem[tid] = __ldg(a.grp_members + b + tid);
-    } else {
-      nm = 1;
-      first = item.y;
-      const int sh = a.seq_shared[first];
-      r_begin = sh + item.z * P;
-      r_end = min(r_begin + P, __ldg(a.context_lens + first));
-      if (tid == 0) s_mem[0] = first;
-    }
-    if (tid == 0) s_next = atomicAdd(a.ticket, 1);
-    __syncthreads();
+    const int first = h0.y, r_begin = h0.z, r_end = h0.w;  // token range
+    const int nm = h1.y;                                    // members
     const int t_begin = r_begin / kTileTokens;
     const int t_end = (r_end + kTileTokens - 1) / kTileTokens;
     const int n_item = t_end - t_begin;
@@ -1137,6 +1140,21 @@ __global__ void __launch_bounds__(kThreads, 3)
       const int npro = n_mine < C::kStages ? n_mine : C::kStages;
       for (int k = 0; k < npro; ++k) issue(k, k);
     }
+    // the members, and for the merge their context and shared lengths (not
+    // waited on until then); the next ticket is stored only at the item's end
+    int mem_L = 0, mem_sh = 0, nxt = 0;
+    if (tid < nm) {
+      const int sq = h0.x == 1 ? __ldg(a.grp_members + h1.x + tid) : first;
+      s_mem[tid] = sq;
+      mem_L = __ldg(a.context_lens + sq);
+      mem_sh = a.seq_shared[sq];
+    }
+    if (tid == 0) {
+      s_nm = nm;
+      s_part = h1.z;
+      nxt = atomicAdd(a.ticket, 1);
+    }
+    __syncthreads();
 
     // Q fragments for rows g and g + 8: row r is (member r / G, head r % G)
     uint32_t qa[KS][4];
@@ -1281,6 +1299,8 @@ __global__ void __launch_bounds__(kThreads, 3)
       l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 1);
       l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 2);
     }
+    if (tid < s_nm) s_np[tid] = (mem_sh + P - 1) / P + (mem_L - mem_sh + P - 1) / P;
+    if (tid == 0) s_next = nxt;
     __syncthreads();
     if (s_abort) return;
     constexpr int R = 16;
@@ -1300,7 +1320,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
     }
     __syncthreads();
-    const int rows = nm * G;
+    const int rows = s_nm * G;
     for (int e = tid; e < rows * D; e += kThreads) {
       const int r = e / D, d = e % D;
       float Mx = -INFINITY;
@@ -1314,11 +1334,8 @@ __global__ void __launch_bounds__(kThreads, 3)
         acc += sw * co[(w * R + r) * D + d];
       }
       const int sq = s_mem[r / G];
-      const int L = __ldg(a.context_lens + sq);
-      const int shr = a.seq_shared[sq];
-      const int nsp = (shr + P - 1) / P;
-      const int nparts = nsp + (L - shr + P - 1) / P;
-      const int part = item.x == 1 ? item.z : nsp + item.z;
+      const int nparts = s_np[r / G];
+      const int part = s_part;
       const int64_t qh = (int64_t)sq * a.Hq + kvh * G + r % G;
       if (nparts == 1) {
         a.out[qh * D + d] = __float2bfloat16_rn(acc / lsum);
@@ -1697,7 +1714,7 @@ WsShared ws_shared_layout(int64_t S, int64_t Hq, int64_t D, int64_t max_parts) {
   w.parts = max_parts + 1;
   w.item_cap = 2 * S * max_parts + 1;
   w.items_off = 256;
-  w.shared_off = align256(w.items_off + w.item_cap * sizeof(int4));
+  w.shared_off = align256(w.items_off + w.item_cap * 2 * sizeof(int4));
   w.ml_off = align256(w.shared_off + S * sizeof(int32_t));
   w.o_off = align256(w.ml_off + S * Hq * w.parts * sizeof(float2));
   w.total = align256(w.o_off + S * Hq * w.parts * D * sizeof(float));
