@@ -96,6 +96,12 @@ int pkv_seq_append_slots(pkv_alloc* a, int64_t seq, int32_t n, int32_t* slots_ou
                          int32_t* cow_pair_out, int32_t* n_cow);
 /* The request completed: drop its references, freeing blocks that reach 0. */
 int pkv_seq_free(pkv_alloc* a, int64_t seq);
+/* Batched forms for an iteration's admissions and completions: n new empty
+ * sequences (ids to seq_ids, n int64, host, in creation order); n sequences
+ * freed as by pkv_seq_free. PKV_EINVAL, nothing freed, when an id is unknown
+ * or listed twice. */
+int pkv_seq_create_many(pkv_alloc* a, int32_t n, int64_t* seq_ids);
+int pkv_seq_free_many(pkv_alloc* a, const int64_t* seqs, int32_t n);
 int pkv_seq_len(pkv_alloc* a, int64_t seq, int32_t* len);
 /* Copies min(cap, table length) entries to out (host); *n = table length. */
 int pkv_seq_block_table(pkv_alloc* a, int64_t seq, int32_t* out, int32_t cap, int32_t* n);

@@ -39,6 +39,8 @@ SIGNATURES = {
     "pkv_seq_fork": (ctypes.c_int, [vp, i64, P(i64)]),
     "pkv_seq_append_slots": (ctypes.c_int, [vp, i64, i32, P(i32), P(i32), P(i32)]),
     "pkv_seq_free": (ctypes.c_int, [vp, i64]),
+    "pkv_seq_create_many": (ctypes.c_int, [vp, i32, P(i64)]),
+    "pkv_seq_free_many": (ctypes.c_int, [vp, P(i64), i32]),
     "pkv_seq_len": (ctypes.c_int, [vp, i64, P(i32)]),
     "pkv_seq_block_table": (ctypes.c_int, [vp, i64, P(i32), i32, P(i32)]),
     "pkv_block_refcount": (ctypes.c_int, [vp, i32, P(i32)]),

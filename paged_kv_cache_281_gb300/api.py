@@ -161,6 +161,19 @@ class BlockAllocator:
     def seq_free(self, seq: int) -> None:
         check(lib().pkv_seq_free(self._h, int(seq)))
 
+    def seq_create_many(self, n: int) -> np.ndarray:
+        """``pkv_seq_create_many``: ``n`` new sequences' ids (int64)."""
+        out = np.empty(int(n), dtype=np.int64)
+        check(lib().pkv_seq_create_many(self._h, int(n),
+                                        out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))))
+        return out
+
+    def seq_free_many(self, seqs) -> None:
+        """``pkv_seq_free_many``: frees every listed sequence, or none."""
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        check(lib().pkv_seq_free_many(self._h, ids.ctypes.data_as(
+            ctypes.POINTER(ctypes.c_int64)), int(ids.shape[0])))
+
     def seq_len(self, seq: int) -> int:
         out = ctypes.c_int32()
         check(lib().pkv_seq_len(self._h, int(seq), ctypes.byref(out)))

@@ -228,6 +228,16 @@ extern "C" int pkv_seq_create(pkv_alloc* a, int64_t* seq_id) {
   return ok();
 }
 
+extern "C" int pkv_seq_create_many(pkv_alloc* a, int32_t n, int64_t* seq_ids) {
+  PKV_REQUIRE(a && n >= 0 && (n == 0 || seq_ids), "pkv_seq_create_many: bad arguments");
+  for (int32_t i = 0; i < n; ++i) {
+    const int64_t id = a->next_id++;
+    a->seqs.emplace(id, pkv_alloc::Seq{});
+    seq_ids[i] = id;
+  }
+  return ok();
+}
+
 extern "C" int pkv_seq_fork(pkv_alloc* a, int64_t parent, int64_t* child) {
   PKV_REQUIRE(a && child, "pkv_seq_fork: NULL argument");
   pkv_alloc::Seq* p = a->find(parent);
@@ -361,6 +371,26 @@ extern "C" int pkv_seq_free(pkv_alloc* a, int64_t seq) {
   for (int32_t b : it->second.blocks)
     if (--a->refcount[b] == 0) a->push_free(b);
   a->seqs.erase(it);
+  return ok();
+}
+
+extern "C" int pkv_seq_free_many(pkv_alloc* a, const int64_t* seqs, int32_t n) {
+  const char* who = "pkv_seq_free_many";
+  PKV_REQUIRE(a && n >= 0 && (n == 0 || seqs), "%s: bad arguments", who);
+  // every id known and listed once, else nothing is freed
+  const uint64_t ep = ++a->epoch;
+  for (int32_t i = 0; i < n; ++i) {
+    pkv_alloc::Seq* s = a->find(seqs[i]);
+    PKV_REQUIRE(s, "%s: unknown sequence %lld", who, (long long)seqs[i]);
+    PKV_REQUIRE(s->mark != ep, "%s: sequence %lld appears twice", who, (long long)seqs[i]);
+    s->mark = ep;
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    auto it = a->seqs.find(seqs[i]);
+    for (int32_t b : it->second.blocks)
+      if (--a->refcount[b] == 0) a->push_free(b);
+    a->seqs.erase(it);
+  }
   return ok();
 }
 

@@ -69,14 +69,18 @@ def _scenario(seed):
     for step in range(40):
         # retire sequences about to outgrow the table width, and a random one
         # now and then, so the pool keeps moving
+        # (the library's batched calls, the oracle's one by one)
+        gone = []
         for k in reversed(range(len(lib_ids))):
             if (ora.seq_len(ora_ids[k]) > (W - 8) * B
                     or (rng.random() < 0.05 and len(lib_ids) > 4)):
-                lib.seq_free(lib_ids.pop(k))
+                gone.append(lib_ids.pop(k))
                 ora.free_seq(ora_ids.pop(k))
-        while len(lib_ids) < 6:
-            a, b = lib.seq_create(), ora.create()
-            lib_ids.append(a), ora_ids.append(b)
+        lib.seq_free_many(gone)
+        if len(lib_ids) < 6:
+            k = 6 - len(lib_ids)
+            lib_ids.extend(int(x) for x in lib.seq_create_many(k))
+            ora_ids.extend(ora.create() for _ in range(k))
         live = rng.permutation(len(lib_ids))[:int(rng.integers(1, len(lib_ids) + 1))]
         n_prefill = int(rng.integers(0, len(live) + 1))
         counts = np.array([int(rng.integers(1, 120)) if i < n_prefill else 1
@@ -216,3 +220,23 @@ def test_iteration_run_checks_before_any_launch():
     assert lib().pkv_iteration_run(*args(None, ctypes.byref(one), 0, 1)) == PKV_EINVAL  # meta NULL
     junk = ctypes.create_string_buffer(64)
     assert lib().pkv_iteration_run(*args(junk, ctypes.byref(one), 0, 1)) == PKV_EINVAL  # width 0
+
+
+def test_batched_create_and_free():
+    lib = pkv.BlockAllocator(32, 16)
+    ids = [int(x) for x in lib.seq_create_many(3)]
+    assert ids == [0, 1, 2]
+    for sid in ids:
+        lib.seq_append_slots(sid, 20)          # two blocks each
+    assert lib.num_free_blocks() == 26
+    # a repeated or unknown id: an error, and nothing freed
+    with pytest.raises(pkv.PagedKVError):
+        lib.seq_free_many([ids[0], ids[0]])
+    with pytest.raises(pkv.PagedKVError):
+        lib.seq_free_many([ids[1], 99])
+    assert lib.num_free_blocks() == 26
+    lib.seq_free_many(ids[:2])
+    assert lib.num_free_blocks() == 30
+    lib.seq_free_many([])
+    assert lib.seq_create_many(0).shape == (0,)
+    assert int(lib.seq_create_many(1)[0]) == 3  # ids are never reused

@@ -270,20 +270,22 @@ class DeviceTrace:
         self.lib_s = 0.0                    # host time inside the library's per-iteration calls
         self.dev_meta = None                # device copy of the metadata (pkv_iteration_step)
 
-    def admit(self, rid):
-        """A new sequence for request ``rid``."""
-        sid = self.alloc.seq_create()
-        self.sid[rid] = sid
-        if rid >= self.sid_arr.shape[0]:
-            grow = max(rid + 1, 2 * self.sid_arr.shape[0]) - self.sid_arr.shape[0]
+    def admit(self, rids):
+        """New sequences for the admitted requests ``rids`` (one library call)."""
+        if not len(rids):
+            return
+        sids = self.alloc.seq_create_many(len(rids))
+        top = max(rids)
+        if top >= self.sid_arr.shape[0]:
+            grow = max(top + 1, 2 * self.sid_arr.shape[0]) - self.sid_arr.shape[0]
             self.sid_arr = np.concatenate([self.sid_arr, np.full(grow, -1, dtype=np.int64)])
-        self.sid_arr[rid] = sid
+        self.sid_arr[list(rids)] = sids
+        self.sid.update(zip(rids, sids.tolist()))
 
     def host_metadata(self, itr):
         """The iteration's host side: new sequences for admitted requests,
         then one library call for every work's slots and the metadata."""
-        for rid in itr.admitted:
-            self.admit(rid)
+        self.admit(itr.admitted)
         k = self.next
         self.next = (k + 1) % self.RING
         if self.staged[k] is not None:
@@ -395,8 +397,7 @@ class DeviceTrace:
         values already on the device. Returns (prefill_out, decode_out, meta);
         ``host_section(meta, ...)`` reads the staged metadata."""
         cfg = self.cfg
-        for rid in itr.admitted:
-            self.admit(rid)
+        self.admit(itr.admitted)
         kk = self.next
         self.next = (kk + 1) % self.RING
         if self.staged[kk] is not None:
@@ -434,8 +435,9 @@ class DeviceTrace:
         return self.launch(up, stream=stream)
 
     def finish(self, itr):
-        for rid in itr.finished:
-            self.alloc.seq_free(self.sid.pop(rid))
+        """Frees the sequences of the requests that completed (one library call)."""
+        if len(itr.finished):
+            self.alloc.seq_free_many([self.sid.pop(rid) for rid in itr.finished])
 
 
 # ---------------------------------------------------------------- preemption
