@@ -133,10 +133,12 @@ int pkv_build_block_tables(pkv_alloc* a, const int64_t* seqs, int32_t n, int32_t
  *     slot_mapping   int32 [n_tokens]   (prefill works first, then decodes)
  *     cu_q_lens      int32 [n_prefill + 1]
  *     prefill_lens   int32 [n_prefill]  (context lengths after the appends)
- *     prefill_tables int32 [n_prefill][W], padded with 0
+ *     prefill_tables int32 [n_prefill][W]
  *     decode_lens    int32 [n_decode]
- *     decode_tables  int32 [n_decode][W], padded with 0
+ *     decode_tables  int32 [n_decode][W]
  *     cow_pairs      int32 [n_cow][2]  (run pkv_block_copy on them first)
+ *   (a table row holds the sequence's ceil(len / block_size) blocks; the
+ *   entries after them are left as they were: no kernel reads them),
  *   so one host-to-device copy of the whole buffer feeds pkv_block_copy,
  *   pkv_kv_append, pkv_paged_attention_prefill and pkv_paged_attention_decode.
  *   PKV_EINVAL (nothing changed) for unknown, repeated or swapped-out

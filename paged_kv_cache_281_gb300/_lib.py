@@ -39,20 +39,22 @@ SIGNATURES = {
     "pkv_seq_fork": (ctypes.c_int, [vp, i64, P(i64)]),
     "pkv_seq_append_slots": (ctypes.c_int, [vp, i64, i32, P(i32), P(i32), P(i32)]),
     "pkv_seq_free": (ctypes.c_int, [vp, i64]),
-    "pkv_seq_create_many": (ctypes.c_int, [vp, i32, P(i64)]),
-    "pkv_seq_free_many": (ctypes.c_int, [vp, P(i64), i32]),
+    # (per-iteration calls: host arrays passed as plain addresses, the
+    # cheapest conversion ctypes offers)
+    "pkv_seq_create_many": (ctypes.c_int, [vp, i32, vp]),
+    "pkv_seq_free_many": (ctypes.c_int, [vp, vp, i32]),
     "pkv_seq_len": (ctypes.c_int, [vp, i64, P(i32)]),
     "pkv_seq_block_table": (ctypes.c_int, [vp, i64, P(i32), i32, P(i32)]),
     "pkv_block_refcount": (ctypes.c_int, [vp, i32, P(i32)]),
     "pkv_num_free_blocks": (ctypes.c_int, [vp, P(i32)]),
     "pkv_build_block_tables": (ctypes.c_int, [vp, P(i64), i32, P(i32), i32, P(i32)]),
     "pkv_iteration_layout_bytes": (ctypes.c_int, [i32, i32, i32, i32, P(IterationLayout)]),
-    "pkv_iteration_prepare": (ctypes.c_int, [vp, P(i64), P(i32), i32, i32, i32, vp, sz,
+    "pkv_iteration_prepare": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, vp, sz,
                                              P(IterationLayout), P(i32)]),
     "pkv_iteration_run": (ctypes.c_int, [vp, P(IterationLayout), i32, i32, vp, vp, vp, vp,
                                          vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp,
                                          sz, vp, vp]),
-    "pkv_iteration_step": (ctypes.c_int, [vp, P(i64), P(i32), i32, i32, i32, vp, sz, vp, sz, vp,
+    "pkv_iteration_step": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, vp, sz, vp, sz, vp,
                                           vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
                                           vp, sz, vp, sz, vp, vp, P(IterationLayout), P(i32)]),
     "pkv_seq_swap_out": (ctypes.c_int, [vp, i64, P(i32), i32, P(i32)]),

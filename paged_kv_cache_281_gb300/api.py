@@ -164,15 +164,13 @@ class BlockAllocator:
     def seq_create_many(self, n: int) -> np.ndarray:
         """``pkv_seq_create_many``: ``n`` new sequences' ids (int64)."""
         out = np.empty(int(n), dtype=np.int64)
-        check(lib().pkv_seq_create_many(self._h, int(n),
-                                        out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))))
+        check(lib().pkv_seq_create_many(self._h, int(n), out.ctypes.data))
         return out
 
     def seq_free_many(self, seqs) -> None:
         """``pkv_seq_free_many``: frees every listed sequence, or none."""
         ids = np.ascontiguousarray(seqs, dtype=np.int64)
-        check(lib().pkv_seq_free_many(self._h, ids.ctypes.data_as(
-            ctypes.POINTER(ctypes.c_int64)), int(ids.shape[0])))
+        check(lib().pkv_seq_free_many(self._h, ids.ctypes.data, int(ids.shape[0])))
 
     def seq_len(self, seq: int) -> int:
         out = ctypes.c_int32()
@@ -249,8 +247,7 @@ class BlockAllocator:
             addr, nbytes = buf.ctypes.data, buf.nbytes
         layout, fit = IterationLayout(), ctypes.c_int32()
         rc = lib().pkv_iteration_prepare(
-            self._h, ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
-            cnt.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(n_prefill),
+            self._h, ids.ctypes.data, cnt.ctypes.data, int(n_prefill),
             n - int(n_prefill), int(max_blocks_per_seq), addr, nbytes, ctypes.byref(layout),
             ctypes.byref(fit))
         if rc != 0:
@@ -315,8 +312,7 @@ def pkv_iteration_step(alloc: BlockAllocator, seqs, counts, n_prefill: int,
         raise ValueError(f"q/out must be [{T}, Hq, {D}] and k_new/v_new [{T}, {Hkv}, {D}]")
     layout, fit = IterationLayout(), ctypes.c_int32()
     rc = lib().pkv_iteration_step(
-        alloc._h, ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
-        cnt.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(n_prefill), n - int(n_prefill),
+        alloc._h, ids.ctypes.data, cnt.ctypes.data, int(n_prefill), n - int(n_prefill),
         int(max_blocks_per_seq), host_buf.data_ptr(), int(host_buf.numel()),
         dev_buf.data_ptr(), int(dev_buf.numel()), q.data_ptr(), k_new.data_ptr(),
         v_new.data_ptr(), out.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), N, Hq, Hkv, D,

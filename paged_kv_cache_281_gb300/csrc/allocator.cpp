@@ -641,8 +641,8 @@ extern "C" int pkv_iteration_prepare(pkv_alloc* a, const int64_t* seqs, const in
       const pkv_alloc::Seq* s = a->batch[first + k];
       int32_t* row = tables + k * W;
       const int32_t m = (int32_t)s->blocks.size();
+      // (entries past the last block stay as they were: no kernel reads them)
       if (m) std::memcpy(row, s->blocks.data(), sizeof(int32_t) * m);
-      for (int64_t j = m; j < W; ++j) row[j] = 0;
       lens[k] = s->len;
       if (s->len > max_len[part]) max_len[part] = s->len;
     }

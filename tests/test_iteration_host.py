@@ -1,7 +1,7 @@
 """pkv_iteration_prepare against the oracle's allocator model (CPU only).
 
 One call per iteration reserves every work's slots and writes the slot
-mapping, cu_q_lens, context lengths, padded block tables and copy-on-write
+mapping, cu_q_lens, context lengths, block tables and copy-on-write
 pairs into one host buffer ("Batching, Scheduling, and Paging", section
 Continuous batching: the per-iteration CPU work is the overhead to keep
 small). Each work must get exactly what the per-sequence rules give it
@@ -28,6 +28,14 @@ def _section(buf, layout, name, count, shape=None):
     off = getattr(layout, name)
     a = buf[off:off + 4 * count].view(np.int32)
     return a.reshape(shape) if shape else a
+
+
+def _tables_equal(got, want, lens, B):
+    """Row i holds the first ceil(lens[i] / B) entries of the oracle's table;
+    the entries after them are left unwritten (nothing reads them)."""
+    assert got.shape == want.shape
+    return all(np.array_equal(g[:-(-int(n) // B)], w[:-(-int(n) // B)])
+               for g, w, n in zip(got, want, lens))
 
 
 def _oracle_batch(ora, ids, counts, n_prefill):
@@ -120,12 +128,12 @@ def _scenario(seed):
             assert np.array_equal(_section(buf, L, "cu_q_lens", n_prefill + 1), cu)
             np_ = n_prefill
             assert np.array_equal(_section(buf, L, "prefill_lens", np_), lens[:np_])
-            assert np.array_equal(_section(buf, L, "prefill_tables", np_ * Wt, (np_, Wt)),
-                                  tables[:np_])
+            assert _tables_equal(_section(buf, L, "prefill_tables", np_ * Wt, (np_, Wt)),
+                                 tables[:np_], lens[:np_], B)
             nd = len(lids) - np_
             assert np.array_equal(_section(buf, L, "decode_lens", nd), lens[np_:])
-            assert np.array_equal(_section(buf, L, "decode_tables", nd * Wt, (nd, Wt)),
-                                  tables[np_:])
+            assert _tables_equal(_section(buf, L, "decode_tables", nd * Wt, (nd, Wt)),
+                                 tables[np_:], lens[np_:], B)
             got_pairs = _section(buf, L, "cow_pairs", 2 * len(pairs), (len(pairs), 2))
             assert [tuple(p) for p in got_pairs.tolist()] == [tuple(p) for p in pairs]
             assert L.max_q_len == (int(counts[:np_].max()) if np_ else 0)
@@ -163,7 +171,7 @@ def test_out_of_blocks_counts_the_copies_earlier_works_release():
     assert np.array_equal(_section(buf, L, "slot_mapping", 99), slots)
     got = _section(buf, L, "cow_pairs", 4, (2, 2)).tolist()
     assert [tuple(p) for p in got] == [tuple(p) for p in pairs]
-    assert np.array_equal(_section(buf, L, "decode_tables", 18, (3, 6)), tables[1:])
+    assert _tables_equal(_section(buf, L, "decode_tables", 18, (3, 6)), tables[1:], lens[1:], 16)
     assert lib.num_free_blocks() == ora.num_free() == 0
 
 
