@@ -99,16 +99,24 @@ struct DecodeArgs {
 // Lists the work items: every full partition (s, p) in sequence order, then
 // the trailing partial partition of each sequence. Single CTA of 1024
 // threads; up to 1024 sequences one scan of both counts places both kinds,
-// more take one pass over the sequences per kind.
+// more take one pass over the sequences per kind. In one pass the tails are
+// listed longest first (by 16-token tiles, 64 length classes), so that the
+// items handed out last are the shortest and the CTAs finish together; the
+// order within a class is that of the atomics (no result depends on the
+// item order: each item's arithmetic is its own and the combine merges in
+// partition order).
+constexpr int kTailClasses = 64;
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
   __shared__ int32_t warp_tot[2][32];
   __shared__ int32_t s_base[2], s_chunk[2];  // [0] full partitions, [1] tails
+  __shared__ int32_t s_class_n[kTailClasses], s_class_at[kTailClasses];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = a.partition_tiles * kTileTokens;
   const bool one_pass = a.S <= 1024;
   grid_dep_launch();  // the decode kernel may start its set-up now
   grid_dep_wait();    // launched early: whatever ran before (the append) is complete
   if (tid == 0) s_base[0] = s_base[1] = 0;
+  if (tid < kTailClasses) s_class_n[tid] = 0;
   __syncthreads();
   for (int pass = 0; pass < (one_pass ? 1 : 2); ++pass) {
     for (int c0 = 0; c0 < a.S; c0 += 1024) {
@@ -123,6 +131,11 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
       }
       const int full = (one_pass || pass == 0) ? L / P : 0;
       const int tail = (one_pass || pass == 1) && L % P != 0 ? 1 : 0;
+      int cls = 0;  // length class of the tail, 0 = the longest
+      if (one_pass && tail) {
+        cls = kTailClasses - min((L % P + kTileTokens - 1) / kTileTokens, kTailClasses);
+        atomicAdd(&s_class_n[cls], 1);
+      }
       int incl_f = full, incl_t = tail;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -148,15 +161,33 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
         }
         warp_tot[warp][lane] = wi - w;
         if (lane == 31) s_chunk[warp] = wi;
+      } else if (warp == 2 && one_pass) {  // first position of each length class
+        static_assert(kTailClasses == 64, "two classes per lane");
+        const int n0 = s_class_n[lane], n1 = s_class_n[32 + lane];
+        int i0 = n0, i1 = n1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v0 = __shfl_up_sync(0xffffffffu, i0, o);
+          const int v1 = __shfl_up_sync(0xffffffffu, i1, o);
+          if (lane >= o) {
+            i0 += v0;
+            i1 += v1;
+          }
+        }
+        s_class_at[lane] = i0 - n0;
+        s_class_at[32 + lane] = __shfl_sync(0xffffffffu, i0, 31) + i1 - n1;
       }
       __syncthreads();
       const int excl_f = s_base[0] + warp_tot[0][warp] + incl_f - full;
-      const int excl_t = s_base[1] + warp_tot[1][warp] + incl_t - tail;
-      // the tails follow every full partition: in one pass this chunk's, else
-      // those of the first pass
+      // the tails follow every full partition: in one pass this chunk's (by
+      // length class), else those of the first pass (in sequence order)
       const int tail_base = one_pass ? s_chunk[0] : s_base[0];
       for (int i = 0; i < full; ++i) a.items[excl_f + i] = make_int2(s, i);
-      if (tail) a.items[tail_base + excl_t] = make_int2(s, L / P);
+      if (tail) {
+        const int at = one_pass ? atomicAdd(&s_class_at[cls], 1)
+                                : s_base[1] + warp_tot[1][warp] + incl_t - tail;
+        a.items[tail_base + at] = make_int2(s, L / P);
+      }
       __syncthreads();
       if (tid == 0) {
         s_base[0] += s_chunk[0];
