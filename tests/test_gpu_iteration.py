@@ -118,3 +118,66 @@ def test_iteration_with_forks_and_copy_on_write():
     works += [(s, 1, "decode") for s in samples if s not in (samples[0], samples[4], samples[10])]
     sd.iteration(works, 9300)
     assert sd.lib.num_free_blocks() == sd.ora.num_free()
+
+
+def test_iteration_run_equals_separate_calls_bit_for_bit():
+    # pkv_iteration_run runs the prefill on a second stream beside the decode;
+    # the outputs and the pools must be exactly those of the same calls made
+    # one after another on one stream from the same metadata
+    lib = pkv.BlockAllocator(N, B)
+    kc, vc = poisoned_pools(N, Hkv, B, D)
+    seqs = [lib.seq_create() for _ in range(6)]
+    buf = torch.empty(1 << 20, dtype=torch.uint8).pin_memory()
+    status = pkv.new_status()
+    scale = 1.0 / np.sqrt(D)
+
+    def batch(works, n_prefill, seed):
+        counts = [c for _, c in works]
+        T = sum(counts)
+        q = to_dev_bf16(normal_bf16((T, Hq, D), seed))
+        k = to_dev_bf16(normal_bf16((T, Hkv, D), seed + 1))
+        v = to_dev_bf16(normal_bf16((T, Hkv, D), seed + 2))
+        L = lib.iteration_prepare([seqs[i] for i, _ in works], counts, n_prefill, W, buf)
+        return L, buf[:L.total_bytes].cuda(), q, k, v, T
+
+    def workspaces(n, n_prefill, T):
+        return (torch.empty(pkv.pkv_decode_workspace_bytes(n, Hq, D, W * B), dtype=torch.uint8,
+                            device="cuda"),
+                torch.empty(pkv.pkv_prefill_workspace_bytes(max(1, n_prefill), T, Hq, D),
+                            dtype=torch.uint8, device="cuda"))
+
+    L0, meta0, q0, k0, v0, T0 = batch(list(enumerate((40, 77, 130, 16, 300, 9))), 6, 9600)
+    dws, pws = workspaces(6, 6, T0)
+    out0 = torch.empty(T0, Hq, D, dtype=torch.bfloat16, device="cuda")
+    pkv.pkv_iteration_run(meta0, L0, 6, 0, q0, k0, v0, out0, kc, vc, scale, dws, pws,
+                          status=status)
+    # a mixed iteration: two prompt chunks, four decodes
+    works, n_pre = [(0, 21), (4, 50), (1, 1), (2, 1), (3, 1), (5, 1)], 2
+    L1, meta1, q1, k1, v1, T1 = batch(works, n_pre, 9700)
+    kc2, vc2 = kc.clone(), vc.clone()
+    dws, pws = workspaces(len(works), n_pre, T1)
+    out_run = torch.full((T1, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pkv.pkv_iteration_run(meta1, L1, n_pre, len(works) - n_pre, q1, k1, v1, out_run, kc, vc,
+                          scale, dws, pws, status=status)
+    # the same work through the separate calls, serially, on the copies
+    sec = lambda name, count: meta1[getattr(L1, name):getattr(L1, name) + 4 * count].view(
+        torch.int32)
+    Wt, n_dec, rows = int(L1.table_width), len(works) - n_pre, 21 + 50
+    out_sep = torch.full_like(out_run, float("nan"))
+    pkv.pkv_kv_append(k1, v1, sec("slot_mapping", T1), kc2, vc2, status=status)
+    pkv.pkv_paged_attention_prefill(out_sep[:rows], q1[:rows], sec("cu_q_lens", n_pre + 1),
+                                    sec("prefill_lens", n_pre), kc2, vc2,
+                                    sec("prefill_tables", n_pre * Wt).view(n_pre, Wt),
+                                    int(L1.max_q_len), int(L1.max_prefill_len), scale, pws,
+                                    status=status)
+    pkv.pkv_paged_attention_decode(out_sep[rows:], q1[rows:], kc2, vc2,
+                                   sec("decode_tables", n_dec * Wt).view(n_dec, Wt),
+                                   sec("decode_lens", n_dec), int(L1.max_decode_len), scale, dws,
+                                   status=status)
+    torch.cuda.synchronize()
+    pkv.pkv_check_status(status)
+    assert L1.n_cow == 0
+    assert np.array_equal(bf16_bits(out_run), bf16_bits(out_sep))
+    assert np.isfinite(bf16_to_f64(out_run)).all()
+    assert np.array_equal(bf16_bits(kc), bf16_bits(kc2))
+    assert np.array_equal(bf16_bits(vc), bf16_bits(vc2))
