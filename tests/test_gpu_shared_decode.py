@@ -134,3 +134,24 @@ def test_long_shared_prefix_many_partitions():
     out = bf16_to_f64(decode_shared_grouped(w, d, partition_size=512))
     pkv.pkv_check_status(d.status)
     assert_close(out, reference(w), "long shared prefixes")
+
+
+def test_forced_timeout_reports_and_recovers():
+    # every wait gives up at once: each team of warps leaves its item after
+    # its loads in flight have landed, the status says PKV_ETIMEOUT, and the
+    # next call (waits restored) is correct
+    w = make_shared_prefix_workload("grouped_timeout", n_prompts=3, n_samples=5, prefix=300,
+                                    tail_max=200, Hq=8, Hkv=2, D=128, block_size=16, seed=7190)
+    d = setup_shared_prefix(w)
+    try:
+        pkv.pkv_debug_set_wait(True)
+        decode_shared_grouped(w, d)
+        with pytest.raises(pkv.PagedKVError) as e:
+            pkv.pkv_check_status(d.status)
+        assert e.value.code == -4
+    finally:
+        pkv.pkv_debug_set_wait(False)
+    pkv.pkv_status_reset(d.status)
+    out = bf16_to_f64(decode_shared_grouped(w, d))
+    pkv.pkv_check_status(d.status)
+    assert_close(out, reference(w), "after recovery")
