@@ -114,9 +114,9 @@ extern "C" int pkv_iteration_run(const void* meta, const pkv_iteration_layout* l
   }
   SideStream* sd = nullptr;
   if (int rc = side_stream(&sd)) return rc;
-  cudaStream_t main = static_cast<cudaStream_t>(stream);
+  cudaStream_t caller = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lock(sd->mu);
-  cudaError_t err = cudaEventRecord(sd->fork, main);
+  cudaError_t err = cudaEventRecord(sd->fork, caller);
   if (err == cudaSuccess) err = cudaStreamWaitEvent(sd->stream, sd->fork, 0);
   if (err != cudaSuccess) return pkv::cuda_fail(err, "pkv_iteration_run: fork");
   const int rc_pre = prefill(sd->stream);
@@ -124,7 +124,7 @@ extern "C" int pkv_iteration_run(const void* meta, const pkv_iteration_layout* l
   // for all of it (and a stream capture stays whole)
   err = cudaEventRecord(sd->join, sd->stream);
   const int rc_dec = rc_pre ? rc_pre : decode();
-  if (err == cudaSuccess) err = cudaStreamWaitEvent(main, sd->join, 0);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(caller, sd->join, 0);
   if (err != cudaSuccess) return pkv::cuda_fail(err, "pkv_iteration_run: join");
   return rc_dec ? rc_dec : ok();
 }
