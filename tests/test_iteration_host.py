@@ -248,3 +248,23 @@ def test_batched_create_and_free():
     lib.seq_free_many([])
     assert lib.seq_create_many(0).shape == (0,)
     assert int(lib.seq_create_many(1)[0]) == 3  # ids are never reused
+
+
+def test_table_rows_past_the_last_block_are_left_as_they_were():
+    # each row holds the sequence's blocks; the rest of the row keeps whatever
+    # the buffer held (no kernel reads it), so the prepare writes no more than
+    # the blocks themselves
+    lib = pkv.BlockAllocator(64, 16)
+    ids = [int(x) for x in lib.seq_create_many(3)]
+    buf = np.full(1 << 16, 0x5A, np.uint8)
+    L = lib.iteration_prepare(ids, [40, 100, 1], 2, 16, buf)
+    sentinel = np.frombuffer(bytes([0x5A] * 4), np.int32)[0]
+    W = int(L.table_width)
+    assert W == 7                                   # ceil(100 / 16) is the longest
+    for name, first, count in (("prefill_tables", 0, 2), ("decode_tables", 2, 1)):
+        off = getattr(L, name)
+        rows = buf[off:off + 4 * count * W].view(np.int32).reshape(count, W)
+        for r, sid in enumerate(ids[first:first + count]):
+            table = lib.seq_block_table(sid)
+            assert list(rows[r, :len(table)]) == table
+            assert np.all(rows[r, len(table):] == sentinel)
