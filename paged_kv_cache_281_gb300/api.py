@@ -22,6 +22,7 @@ import torch
 from ._lib import IterationLayout, PagedKVError, check, lib
 
 __all__ = [
+    "IterationStepper",
     "PagedKVError", "pkv_version", "pkv_last_error", "BlockAllocator",
     "pkv_kv_append", "pkv_block_copy", "pkv_swap_blocks", "pkv_decode_workspace_bytes",
     "pkv_paged_attention_decode", "pkv_paged_attention_decode_noalloc",
@@ -324,6 +325,68 @@ def pkv_iteration_step(alloc: BlockAllocator, seqs, counts, n_prefill: int,
         err.n_fit = fit.value
         raise err
     return layout
+
+
+class IterationStepper:
+    """``pkv_iteration_step`` bound to one allocator, its pools, the device
+    copy of the metadata, the workspaces and the status block: their checks
+    are done once, here, and each call checks only that iteration's own
+    arguments (ids, counts, the pinned staging buffer, q, k_new, v_new,
+    out). The bound tensors are kept alive by the stepper; calls must be made
+    with the same current device."""
+
+    def __init__(self, alloc: BlockAllocator, max_blocks_per_seq: int, dev_buf, k_cache, v_cache,
+                 scale: float, decode_ws, prefill_ws, partition_size: int = 0, status=None):
+        cur = torch.cuda.current_device()
+        self._cur = cur
+        N, Hkv, B, D = _pool_shape(k_cache, v_cache, cur)
+        _dev(dev_buf, "dev_buf", torch.uint8, 1, cur)
+        _dev(decode_ws, "decode_ws", torch.uint8, 1, cur)
+        _dev(prefill_ws, "prefill_ws", torch.uint8, 1, cur)
+        if status is not None:
+            _dev(status, "status", torch.int32, 1, cur)
+        self._keep = (alloc, dev_buf, k_cache, v_cache, decode_ws, prefill_ws, status)
+        self._Hkv, self._D = Hkv, D
+        self._head = (alloc._h,)
+        self._fixed = (int(max_blocks_per_seq), dev_buf.data_ptr(), int(dev_buf.numel()))
+        self._pools = (k_cache.data_ptr(), v_cache.data_ptr(), N)
+        self._tail = (B, float(scale), int(partition_size), decode_ws.data_ptr(),
+                      int(decode_ws.numel()), prefill_ws.data_ptr(), int(prefill_ws.numel()),
+                      _ptr(status))
+
+    def __call__(self, seqs, counts, n_prefill: int, host_buf, q, k_new, v_new, out,
+                 stream=None):
+        """One iteration (see ``pkv_iteration_step``); returns the layout."""
+        cur = self._cur
+        if torch.cuda.current_device() != cur:
+            raise ValueError(f"the stepper is bound to cuda:{cur}; call it under "
+                             f"torch.cuda.device({cur})")
+        for name, t in (("q", q), ("out", out), ("k_new", k_new), ("v_new", v_new)):
+            _dev(t, name, torch.bfloat16, 3, cur)
+        if host_buf.is_cuda or host_buf.dtype != torch.uint8 or not host_buf.is_contiguous():
+            raise ValueError("host_buf must be a contiguous CPU uint8 tensor (pinned)")
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        cnt = np.ascontiguousarray(counts, dtype=np.int32)
+        n = int(ids.shape[0])
+        Hkv, D = self._Hkv, self._D
+        T, Hq = int(cnt.sum()), int(q.shape[1])
+        if cnt.shape[0] != n or not 0 <= n_prefill <= n:
+            raise ValueError("seqs and counts must have the same length >= n_prefill")
+        if q.shape != (T, Hq, D) or out.shape != q.shape or k_new.shape != (T, Hkv, D) or \
+                v_new.shape != k_new.shape:
+            raise ValueError(f"q/out must be [{T}, Hq, {D}] and k_new/v_new [{T}, {Hkv}, {D}]")
+        layout, fit = IterationLayout(), ctypes.c_int32()
+        rc = lib().pkv_iteration_step(
+            *self._head, ids.ctypes.data, cnt.ctypes.data, int(n_prefill), n - int(n_prefill),
+            self._fixed[0], host_buf.data_ptr(), int(host_buf.numel()), self._fixed[1],
+            self._fixed[2], q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), out.data_ptr(),
+            *self._pools, Hq, Hkv, D, *self._tail, _stream(stream), ctypes.byref(layout),
+            ctypes.byref(fit))
+        if rc != 0:
+            err = PagedKVError(rc, pkv_last_error())
+            err.n_fit = fit.value
+            raise err
+        return layout
 
 
 def iteration_layout_bytes(n_prefill: int, n_decode: int, n_tokens: int,

@@ -181,3 +181,51 @@ def test_iteration_run_equals_separate_calls_bit_for_bit():
     assert np.isfinite(bf16_to_f64(out_run)).all()
     assert np.array_equal(bf16_bits(kc), bf16_bits(kc2))
     assert np.array_equal(bf16_bits(vc), bf16_bits(vc2))
+
+
+def test_step_function_and_bound_stepper_agree():
+    # pkv_iteration_step through the plain wrapper and through an
+    # IterationStepper (its fixed arguments checked once) on twin allocators
+    # and pools: the same slots, outputs and pools, bit for bit
+    sides = []
+    for _ in range(2):
+        lib = pkv.BlockAllocator(N, B)
+        kc, vc = poisoned_pools(N, Hkv, B, D)
+        sides.append((lib, kc, vc, [int(x) for x in lib.seq_create_many(6)],
+                      torch.empty(1 << 20, dtype=torch.uint8).pin_memory(),
+                      torch.empty(1 << 20, dtype=torch.uint8, device="cuda")))
+    status = pkv.new_status()
+    scale = 1.0 / np.sqrt(D)
+    dws = torch.empty(pkv.pkv_decode_workspace_bytes(6, Hq, D, W * B), dtype=torch.uint8,
+                      device="cuda")
+    pws = torch.empty(pkv.pkv_prefill_workspace_bytes(6, 1024, Hq, D), dtype=torch.uint8,
+                      device="cuda")
+    lib1, kc1, vc1, ids1, hb1, db1 = sides[1]
+    stepper = pkv.IterationStepper(lib1, W, db1, kc1, vc1, scale, dws, pws, status=status)
+    outs = [[], []]
+    batches = [(list(enumerate((40, 77, 130, 16, 300, 9))), 6),
+               ([(0, 21), (4, 50), (1, 1), (2, 1), (3, 1), (5, 1)], 2)]
+    for it, (works, n_pre) in enumerate(batches):
+        counts = np.array([c for _, c in works], np.int32)
+        T = int(counts.sum())
+        q = to_dev_bf16(normal_bf16((T, Hq, D), 9800 + 10 * it))
+        k = to_dev_bf16(normal_bf16((T, Hkv, D), 9801 + 10 * it))
+        v = to_dev_bf16(normal_bf16((T, Hkv, D), 9802 + 10 * it))
+        for side, (lib, kc, vc, ids, hb, db) in enumerate(sides):
+            out = torch.full((T, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+            seqs = [ids[i] for i, _ in works]
+            if side == 0:
+                L = pkv.pkv_iteration_step(lib, seqs, counts, n_pre, W, hb, db, q, k, v, out, kc,
+                                           vc, scale, dws, pws, status=status)
+            else:
+                L = stepper(seqs, counts, n_pre, hb, q, k, v, out)
+            torch.cuda.synchronize()
+            outs[side].append((bf16_bits(out).copy(),
+                               hb[L.slot_mapping:L.slot_mapping + 4 * T].numpy().view(np.int32)
+                               .copy()))
+    pkv.pkv_check_status(status)
+    for (o0, s0), (o1, s1) in zip(*outs):
+        assert np.array_equal(s0, s1)
+        assert np.array_equal(o0, o1)
+    assert np.array_equal(bf16_bits(sides[0][1]), bf16_bits(sides[1][1]))
+    assert np.array_equal(bf16_bits(sides[0][2]), bf16_bits(sides[1][2]))

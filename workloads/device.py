@@ -269,6 +269,7 @@ class DeviceTrace:
         self.wait_s = 0.0                   # host time spent waiting for a free buffer
         self.lib_s = 0.0                    # host time inside the library's per-iteration calls
         self.dev_meta = None                # device copy of the metadata (pkv_iteration_step)
+        self.stepper = None                 # pkv_iteration_step bound to the above
 
     def admit(self, rids):
         """New sequences for the admitted requests ``rids`` (one library call)."""
@@ -407,16 +408,18 @@ class DeviceTrace:
         rids, counts, n_pre, rows = itr.arrays()
         ids = self.sid_arr[rids]
         stream = stream or torch.cuda.current_stream()
-        if self.dev_meta is None:
+        if self.stepper is None:
+            # the call bound once to the allocator, pools, device metadata
+            # buffer and workspaces (their checks done here, not per iteration)
             self.dev_meta = torch.empty(self.staging[0].numel(), dtype=torch.uint8,
                                         device=self.device)
+            self.stepper = pkv.IterationStepper(self.alloc, self.max_blocks, self.dev_meta,
+                                                self.k_cache, self.v_cache, self.scale, self.ws,
+                                                self.pws, partition_size=self.partition_size,
+                                                status=self.status)
         out = torch.empty(q.shape[0], cfg.Hq, cfg.D, dtype=torch.bfloat16, device=self.device)
         t0 = time.perf_counter()
-        layout = pkv.pkv_iteration_step(self.alloc, ids, counts, n_pre, self.max_blocks,
-                               self.staging[kk], self.dev_meta, q, k, v, out, self.k_cache,
-                               self.v_cache, self.scale, self.ws, self.pws,
-                               partition_size=self.partition_size, status=self.status,
-                               stream=stream)
+        layout = self.stepper(ids, counts, n_pre, self.staging[kk], q, k, v, out, stream=stream)
         self.lib_s += time.perf_counter() - t0
         ev = self.events[kk]
         ev.record(stream)
